@@ -1,0 +1,106 @@
+"""The oracle's pins must catch plausible mistakes.
+
+Each case copies the oracle's C source to a temporary directory, plants one
+mistake (a dropped term, a wrong sign or index, a transposed operand), compiles
+it, and runs every pin in test_oracle_pins.py against the mutant.  At least one
+pin must fail for every mutant.  Everything runs on the CPU; the real oracle is
+untouched.
+"""
+import inspect
+import json
+import os
+import subprocess
+import ctypes
+
+import pytest
+
+import oracle
+from tests import test_oracle_pins as pins
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "gattn_oracle.c")
+
+MUTANTS = {
+    "gqa_strided_mapping": ("int g = h / r;", "int g = h % G;"),
+    "scale_by_d_not_sqrt_d": ("double scale = 1.0 / sqrt((double)d);", "double scale = 1.0 / (double)d;"),
+    "no_scale": ("double scale = 1.0 / sqrt((double)d);", "double scale = 1.0;"),
+    "rope_sign_flip": ("y[i] = a * c - b * s;", "y[i] = a * c + b * s;"),
+    "rope_exponent_over_d": ("pow(base, -2.0 * (double)i / (double)rd)", "pow(base, -2.0 * (double)i / (double)d)"),
+    "rope_adjacent_pairs": ("double a = x[i], b = x[i + half];", "double a = x[2 * i], b = x[2 * i + 1];"),
+    "causal_excludes_diagonal": ("attend_row(qt, kb, (int64_t)G * d, vb, (int64_t)G * d, t + 1,",
+                                 "attend_row(qt, kb, (int64_t)G * d, vb, (int64_t)G * d, t > 0 ? t : 1,"),
+    "gate_negated": ("for (int e = 0; e < d; ++e) o[e] *= oracle_sigmoid(z[e]);",
+                     "for (int e = 0; e < d; ++e) o[e] *= oracle_sigmoid(-z[e]);"),
+    "gate_transposed_dim": ("for (int e = 0; e < d; ++e) o[e] *= oracle_sigmoid(z[e]);",
+                            "for (int e = 0; e < d; ++e) o[e] *= oracle_sigmoid(z[d - 1 - e]);"),
+    "rmsnorm_sum_not_mean": ("double inv = 1.0 / sqrt(ss / (double)d + eps);", "double inv = 1.0 / sqrt(ss + eps);"),
+    "rmsnorm_eps_outside": ("double inv = 1.0 / sqrt(ss / (double)d + eps);",
+                            "double inv = 1.0 / (sqrt(ss / (double)d) + eps);"),
+    "rmsnorm_drops_weight": ("y[r * d + e] = xr[e] * inv * w[e];", "y[r * d + e] = xr[e] * inv;"),
+    "softmax_not_normalised": ("double wj = scratch[j] / z;", "double wj = scratch[j];"),
+    "values_from_keys": ("o[e] += wj * v[j * val_stride + e];", "o[e] += wj * kr[j * key_stride + e];"),
+    "decode_position_off_by_one": ("rope_row(tmp, (double)(L - 1), d, rd, base, qr);",
+                                   "rope_row(tmp, (double)L, d, rd, base, qr);"),
+    "prefill_k_uses_q_weight": ("prologue_head(k + (int64_t)b * S * G * d, knorm_w, posb, S, G, g,",
+                                "prologue_head(k + (int64_t)b * S * G * d, qnorm_w, posb, S, G, g,"),
+    "headwise_gate_index": ("apply_gate(o, gate + ((int64_t)b * S + t) * H + h, d, gate_mode);",
+                            "apply_gate(o, gate + ((int64_t)t * B + b) * H + h, d, gate_mode);"),
+}
+
+
+def _pin_functions():
+    out = []
+    for name, fn in inspect.getmembers(pins, inspect.isfunction):
+        if not name.startswith("test_") or name == "test_kv_cache_byte_accounting":
+            continue
+        marks = getattr(fn, "pytestmark", [])
+        params = [m for m in marks if m.name == "parametrize"]
+        if params:
+            argnames, values = params[0].args
+            names = [a.strip() for a in argnames.split(",")]
+            for vals in values:
+                out.append((name, fn, dict(zip(names, vals if isinstance(vals, tuple) else (vals,)))))
+        else:
+            out.append((name, fn, {}))
+    return out
+
+
+def _golden(name):
+    with open(os.path.join(os.path.dirname(pins.__file__), "golden", name)) as f:
+        return json.load(f)
+
+
+def _compile_mutant(tmp_path, old, new):
+    src = open(SRC).read()
+    assert src.count(old) >= 1, "mutation anchor not found: " + old
+    path = tmp_path / "mutant.c"
+    path.write_text(src.replace(old, new))
+    lib = tmp_path / "libmutant.so"
+    subprocess.run(["gcc", "-O1", "-std=c11", "-fPIC", "-shared", "-fopenmp", str(path), "-o", str(lib), "-lm"],
+                   check=True)
+    return str(lib)
+
+
+@pytest.mark.parametrize("mutant", sorted(MUTANTS))
+def test_pins_catch_mutant(mutant, tmp_path):
+    old, new = MUTANTS[mutant]
+    libpath = _compile_mutant(tmp_path, old, new)
+    real = oracle._load()
+    mutant_lib = ctypes.CDLL(libpath)
+    for fname in ("oracle_sigmoid", "oracle_rmsnorm", "oracle_rope", "oracle_gate", "oracle_sdpa_gate",
+                  "oracle_prefill", "oracle_prefill_rows", "oracle_decode"):
+        getattr(mutant_lib, fname).argtypes = getattr(real, fname).argtypes
+        getattr(mutant_lib, fname).restype = getattr(real, fname).restype
+    caught = []
+    oracle._lib = mutant_lib
+    try:
+        for name, fn, kwargs in _pin_functions():
+            args = {}
+            if "golden" in inspect.signature(fn).parameters:
+                args["golden"] = _golden
+            try:
+                fn(**args, **kwargs)
+            except AssertionError:
+                caught.append(name)
+    finally:
+        oracle._lib = real
+    assert caught, "no pin caught mutant " + mutant
