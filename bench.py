@@ -1,0 +1,368 @@
+"""Benchmark of the gated-attention hot path on GB300.
+
+One step = one pass of the whole path on synthetic inputs already resident in
+HBM: a causal prefill of the Qwen3.5-0.8B-shaped full-attention layer (B1 S4096
+H8 G2 d256, rotary 64, elementwise gate) followed by one decode step of 64
+sequences with 16k-32k cached tokens each (H8 G2 d256).  L2 is flushed (a 256 MiB
+write) before every timed call; each call is timed with CUDA events on the stream
+it runs on.
+
+  value        prefill TFLOP/s (algorithmic causal FLOPs / time of the prefill call)
+  decode       decode GB/s (K/V cache + q/gate/out bytes / time of the decode call)
+  roofline     the dominant kernel (tcgen05 prefill) against measured bf16 peak,
+               plus the decode split kernel against measured HBM copy bandwidth
+  e2e          prefill through the public API with pinned host buffers, H2D and
+               D2H copies inside the timed region
+  cpu_baseline the fp64 oracle on a bounded sample of the prefill workload
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+Under torchrun (N > 1) every rank runs the same workload on its own GPU (replicas:
+the path has no exchange step); times are maxed over ranks.
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "gated-attn causal prefill TFLOP/s (% bf16 peak); decode KV GB/s (% HBM)"
+PREFILL = "qwen35_08b_prefill"
+DECODE = "qwen35_08b_decode"
+L2_FLUSH_BYTES = 256 << 20
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--prefill", default=PREFILL, help="prefill workload name (parity/tuning runs)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget-s", type=float, default=12.0)
+    return ap.parse_args()
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return p["hbm_gbs"], p["bf16_tflops"], "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, 1900.0, "fallback"
+
+
+def kernel_source_hash(files):
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, "gated_softmax_attention_gqa_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(summary_name, src_files):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on the
+    kernel source as it is now (else None)."""
+    path = os.path.join(ROOT, "profiles", summary_name)
+    try:
+        kv = {}
+        with open(path) as f:
+            for line in f:
+                if ":" in line and line.strip().startswith("- "):
+                    k, v = line.strip()[2:].split(":", 1)
+                    kv[k.strip()] = v.strip().strip("`")
+        if kv.get("kernel_source_sha256") != kernel_source_hash(src_files):
+            return None
+        return int(float(kv["dram_bytes_per_launch_full_workload"]))
+    except (OSError, KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 20 ms."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "20", "-i",
+                 str(gpu_index)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        self.t0 = self.t1 = None
+
+    def mark_start(self):
+        self.t0 = time.time()
+
+    def mark_end(self):
+        self.t1 = time.time()
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.05)
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        rows = [[c.strip() for c in ln.split(",")] for ln in out.strip().splitlines() if ln.count(",") >= 8]
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        sm = []
+        smax = None
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+                smax = float(r[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, r[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        loaded = [s for s in sm if smax and s > 0.5 * smax] or sm
+        return {"sm_mhz": statistics.median(loaded) if loaded else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(rows)}
+
+
+def cpu_baseline(w, inputs, budget_s):
+    """The fp64 oracle, as it stands, on a bounded sample of the prefill workload:
+    all heads of a seeded set of query rows; TFLOP/s over the causal FLOPs of
+    those rows.  Grows the sample until it takes about budget_s seconds."""
+    import numpy as np
+
+    import oracle
+    from gated_softmax_attention_gqa_gb300.workloads import prefill_flops  # noqa: F401
+
+    rng = np.random.default_rng(1234)
+    n = 16
+    while True:
+        rt = np.sort(rng.integers(0, w.S, size=n)).astype(np.int32)
+        rb = np.zeros(n, dtype=np.int32)
+        t0 = time.perf_counter()
+        oracle.prefill_rows(inputs["q"], inputs["k"], inputs["v"], inputs["gate"], inputs["qnorm_w"],
+                            inputs["knorm_w"], None, w.rotary_dim, w.rope_base, w.eps, w.gate_mode, rb, rt)
+        dt = time.perf_counter() - t0
+        flops = sum(4 * w.H * w.d * (int(t) + 1) for t in rt)
+        if dt >= budget_s * 0.5 or n >= 4096:
+            return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": oracle.threads_used(), "kind": "oracle",
+                    "sample": f"{n} seeded query rows x all {w.H} heads of {w.name} (B{w.B} S{w.S} H{w.H} G{w.G} "
+                              f"d{w.d}); fp64 C loops, OpenMP; {dt:.1f} s",
+                    "seconds": dt}
+        n = min(4096, int(n * max(2.0, budget_s / max(dt, 1e-3))))
+
+
+def run_reference(args):
+    """Reference arm: the fp64 oracle timed on the host cores (rank 0 only)."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    from gated_softmax_attention_gqa_gb300.workloads import WORKLOADS, make_prefill_inputs
+
+    w = WORKLOADS[args.prefill]
+    inputs = make_prefill_inputs(w)
+    per_step = max(2.0, 60.0 / max(1, args.steps + args.warmup))
+    for _ in range(args.warmup):
+        cpu_baseline(w, inputs, min(per_step, 2.0))
+    vals, secs = [], 0.0
+    last = None
+    for _ in range(args.steps):
+        last = cpu_baseline(w, inputs, per_step)
+        vals.append(last["value"])
+        secs += last["seconds"]
+    v = statistics.median(vals)
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "TFLOP/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * secs / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "S": w.S, "H": w.H, "G": w.G, "d": w.d,
+                       "rotary_dim": w.rotary_dim, "gate": w.gate_mode},
+            "cpu_baseline": {"value": v, "unit": "TFLOP/s", "cores": last["cores"], "kind": "oracle",
+                             "sample": last["sample"]},
+            "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+        return
+
+    import torch
+    import torch.distributed as dist
+
+    import gated_softmax_attention_gqa_gb300 as ga
+    from gated_softmax_attention_gqa_gb300.workloads import (WORKLOADS, decode_io_bytes, make_decode_inputs,
+                                                             make_prefill_inputs, prefill_flops)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream(dev)
+    hbm_peak, bf16_peak, peak_kind = peaks()
+
+    wp, wd = WORKLOADS[args.prefill], WORKLOADS[DECODE]
+    pin = make_prefill_inputs(wp)
+    p_dev = {k: v.to(dev) for k, v in pin.items()}
+    din = make_decode_inputs(wd)
+    d_dev = {k: v.to(dev) for k, v in din.items()}
+    seqlens = din["seqlens"].tolist()
+    p_out = torch.empty((wp.B, wp.S, wp.H * wp.d), dtype=torch.bfloat16, device=dev)
+    p_ws = torch.empty(ga.gattn_prefill_workspace_size(wp.B, wp.S, wp.H, wp.G, wp.d), dtype=torch.uint8, device=dev)
+    d_out = torch.empty((wd.B, wd.H * wd.d), dtype=torch.bfloat16, device=dev)
+    d_ws = torch.empty(ga.gattn_decode_workspace_size(wd.B, wd.H, wd.G, wd.d, wd.Lmax), dtype=torch.uint8,
+                       device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def prefill():
+        ga.gattn_prefill(p_dev["q"], p_dev["k"], p_dev["v"], p_dev["gate"], p_dev["qnorm_w"], p_dev["knorm_w"],
+                         rotary_dim=wp.rotary_dim, rope_base=wp.rope_base, eps=wp.eps, gate_mode=wp.gate_mode,
+                         out=p_out, workspace=p_ws)
+
+    def decode():
+        ga.gattn_decode(d_dev["q_new"], d_dev["kv_cache"], d_dev["seqlens"], d_dev["gate"], d_dev["qnorm_w"],
+                        rotary_dim=wd.rotary_dim, rope_base=wd.rope_base, eps=wd.eps, gate_mode=wd.gate_mode,
+                        out=d_out, workspace=d_ws)
+
+    def ev():
+        return torch.cuda.Event(enable_timing=True)
+
+    for _ in range(max(3, args.warmup)):
+        flush.zero_()
+        prefill()
+        flush.zero_()
+        decode()
+    torch.cuda.synchronize()
+    if ga.gattn_get_device_status() != 0:
+        raise RuntimeError("device status set during warm-up")
+
+    K = args.steps
+    evs = {k: [(ev(), ev()) for _ in range(K)] for k in ("p", "pk", "d", "dk")}
+    sampler = ClockSampler(dev.index)
+    time.sleep(0.1)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    sampler.mark_start()
+    for i in range(K):
+        flush.zero_()
+        ga.gattn_set_profile_events(*evs["pk"][i])
+        evs["p"][i][0].record(stream)
+        prefill()
+        evs["p"][i][1].record(stream)
+        flush.zero_()
+        ga.gattn_set_profile_events(*evs["dk"][i])
+        evs["d"][i][0].record(stream)
+        decode()
+        evs["d"][i][1].record(stream)
+    torch.cuda.synchronize()
+    sampler.mark_end()
+    if world > 1:
+        dist.barrier()
+    ga.gattn_set_profile_events(None, None)
+    clocks = sampler.stop()
+
+    def ms(key):
+        return [a.elapsed_time(b) for a, b in evs[key]]
+
+    t = {k: statistics.mean(ms(k)) for k in evs}
+    if world > 1:
+        vec = torch.tensor([t["p"], t["pk"], t["d"], t["dk"]], dtype=torch.float64, device=dev)
+        dist.all_reduce(vec, op=dist.ReduceOp.MAX)
+        t = dict(zip(("p", "pk", "d", "dk"), vec.tolist()))
+    status = ga.gattn_get_device_status()
+
+    flops = prefill_flops(wp.B, wp.S, wp.H, wp.d)
+    dbytes = decode_io_bytes(seqlens, wd.H, wd.G, wd.d, wd.gate_mode)
+    value = world * flops / (t["p"] * 1e-3) / 1e12
+    kern_tflops = flops / (t["pk"] * 1e-3) / 1e12
+    dec_gbs = world * dbytes / (t["d"] * 1e-3) / 1e9
+    dec_kern_gbs = dbytes / (t["dk"] * 1e-3) / 1e9
+
+    # ---- end to end through the public API: pinned host -> device, prefill, device -> host
+    host_in = {k: v.pin_memory() for k, v in pin.items()}
+    host_out = torch.empty(p_out.shape, dtype=p_out.dtype).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in host_in.values())
+    d2h = host_out.numel() * host_out.element_size()
+    e2e_bufs = {k: torch.empty_like(v, device=dev) for k, v in pin.items()}
+
+    def e2e_step():
+        for k, v in host_in.items():
+            e2e_bufs[k].copy_(v, non_blocking=True)
+        ga.gattn_prefill(e2e_bufs["q"], e2e_bufs["k"], e2e_bufs["v"], e2e_bufs["gate"], e2e_bufs["qnorm_w"],
+                         e2e_bufs["knorm_w"], rotary_dim=wp.rotary_dim, rope_base=wp.rope_base, eps=wp.eps,
+                         gate_mode=wp.gate_mode, out=p_out, workspace=p_ws)
+        host_out.copy_(p_out, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = ev(), ev()
+    e0.record(stream)
+    for _ in range(K):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / K
+    if world > 1:
+        vec = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(vec, op=dist.ReduceOp.MAX)
+        e2e_ms = vec.item()
+    e2e_val = world * flops / (e2e_ms * 1e-3) / 1e12
+
+    if rank == 0:
+        tc_src = ["prefill_tc.cu", "common.cuh", "internal.h"]
+        dec_src = ["decode.cu", "common.cuh", "internal.h"]
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": K,
+            "warmup": args.warmup, "ms_per_step": t["p"] + t["d"], "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": f"{wp.name} + {wd.name}",
+                       "prefill": {"B": wp.B, "S": wp.S, "H": wp.H, "G": wp.G, "d": wp.d,
+                                   "rotary_dim": wp.rotary_dim, "rope_base": wp.rope_base, "gate": wp.gate_mode},
+                       "decode": {"B": wd.B, "H": wd.H, "G": wd.G, "d": wd.d, "Lmax": wd.Lmax,
+                                  "seqlens": f"U[{wd.seqlen_range[0]},{wd.seqlen_range[1]}] seed {wd.seed}",
+                                  "sum_seqlens": sum(seqlens)},
+                       "l2": "flushed (256 MiB write) before every timed call", "parallelism": f"replicas x{world}"},
+            "prefill_ms": t["p"], "prefill_kernel_ms": t["pk"],
+            "roofline": {"bound": "tensor", "achieved": kern_tflops, "peak": bf16_peak, "unit": "TFLOP/s",
+                         "frac": kern_tflops / bf16_peak, "peak_kind": f"{peak_kind} bf16 dense (burst)",
+                         "kernel": "prefill_tc_kernel<256>",
+                         "traffic": profiled_traffic("prefill_tc_qwen35_08b.md", tc_src)},
+            "decode": {"value": dec_gbs, "unit": "GB/s", "ms": t["d"], "kernel_ms": t["dk"],
+                       "bytes_per_step": dbytes,
+                       "roofline": {"bound": "hbm", "achieved": dec_kern_gbs, "peak": hbm_peak, "unit": "GB/s",
+                                    "frac": dec_kern_gbs / hbm_peak, "frac_of_8TBs": dec_kern_gbs / 8000.0,
+                                    "peak_kind": f"{peak_kind} HBM copy", "kernel": "decode_split_kernel<256>",
+                                    "traffic": profiled_traffic("decode_split_qwen35_08b.md", dec_src)}},
+            "e2e": {"value": e2e_val, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "ms_per_step": e2e_ms},
+            "gpu_launches": 4 * K,
+            "clocks": clocks,
+            "device_status": status,
+        }
+        if not args.no_cpu_baseline:
+            cb = cpu_baseline(wp, pin, args.cpu_budget_s)
+            cb.pop("seconds", None)
+            line["cpu_baseline"] = cb
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,1 +1,140 @@
-"""GB300-native gated softmax attention with GQA (libgattn)."""
+"""GB300-native gated softmax attention with GQA (libgattn).
+
+The Python names mirror the C ABI in include/gattn.h.  Each call hands raw
+device pointers, sizes and the current CUDA stream to libgattn.so; every step of
+the computation runs in the library's CUDA kernels.  PyTorch only supplies
+device memory and streams.  If the library is not built, calls raise: there is
+no CPU fallback.
+
+    out = gattn_prefill(q, k, v, gate, qnorm_w, knorm_w, rotary_dim=64, rope_base=1e7)
+    out = gattn_decode(q_new, kv_cache, seqlens, gate, qnorm_w, rotary_dim=64, rope_base=1e7)
+"""
+import ctypes
+
+import torch
+
+from . import _lib
+from ._lib import GattnError, check
+
+GATE_MODES = {"none": 0, "elementwise": 1, "headwise": 2}
+DTYPES = {torch.bfloat16: 0, torch.float32: 1}
+
+__all__ = ["gattn_prefill", "gattn_decode", "gattn_prefill_workspace_size", "gattn_decode_workspace_size",
+           "gattn_get_device_status", "gattn_set_profile_events", "gattn_strerror", "GattnError", "GATE_MODES"]
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_handle(stream, device):
+    s = stream if stream is not None else torch.cuda.current_stream(device)
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _mode(gate_mode):
+    return GATE_MODES[gate_mode] if isinstance(gate_mode, str) else int(gate_mode)
+
+
+def gattn_strerror(status: int) -> str:
+    return _lib.strerror(status)
+
+
+def gattn_prefill_workspace_size(B, S, H, G, d, dtype=torch.bfloat16) -> int:
+    return _lib.load().gattn_prefill_workspace_size(B, S, H, G, d, DTYPES[dtype])
+
+
+def gattn_decode_workspace_size(B, H, G, d, Lmax) -> int:
+    return _lib.load().gattn_decode_workspace_size(B, H, G, d, Lmax)
+
+
+def gattn_set_profile_events(start=None, stop=None):
+    """Record `start`/`stop` (torch.cuda.Event) around the main attention kernel of
+    every later call; None, None switches it off."""
+    _lib.load().gattn_set_profile_events(ctypes.c_void_p(start.cuda_event) if start is not None else None,
+                                         ctypes.c_void_p(stop.cuda_event) if stop is not None else None)
+
+
+def gattn_get_device_status(stream=None) -> int:
+    """Read and clear the device status bits (GATTN_DEVICE_* in gattn.h)."""
+    bits = ctypes.c_uint(0)
+    st = _lib.load().gattn_get_device_status(ctypes.byref(bits), _stream_handle(stream, None))
+    if st not in (0, 5):
+        check(st, "gattn_get_device_status")
+    return bits.value
+
+
+def _head_strides(t, name):
+    """(token stride, head stride) in elements of a [B,S,H,*] or [B,S,H] view whose
+    element (b,t,h,...) sits at (b*S + t)*token_stride + h*head_stride + ...."""
+    if t.dim() not in (3, 4):
+        raise ValueError(f"{name}: expected 3 or 4 dimensions")
+    if t.dim() == 4 and t.stride(-1) != 1:
+        raise ValueError(f"{name}: the last dimension must be contiguous")
+    B, S = t.shape[0], t.shape[1]
+    tok = t.stride(1) if S > 1 else t.stride(0)
+    if B > 1 and S > 1 and t.stride(0) != S * t.stride(1):
+        raise ValueError(f"{name}: batches must be evenly spaced tokens (stride(0) == S * stride(1))")
+    return tok, t.stride(2)
+
+
+def gattn_prefill(q, k, v, gate, qnorm_w, knorm_w, pos=None, *, rotary_dim, rope_base, eps=1e-6,
+                  gate_mode="elementwise", out=None, workspace=None, stream=None):
+    """Causal gated GQA attention over whole sequences.
+
+    q [B,S,H,d] (may be a strided view, e.g. the query half of the packed q_proj
+    output [B,S,H,2d]); k, v [B,S,G,d] contiguous; gate [B,S,H,d] (elementwise)
+    or [B,S,H] (headwise) or None; qnorm_w, knorm_w [d]; pos [B,S] int32 or None.
+    All on one CUDA device, bf16 or fp32 (all the same).  Returns out [B,S,H*d]."""
+    mode = _mode(gate_mode)
+    B, S, H, d = q.shape
+    G = k.shape[2]
+    dt = DTYPES[q.dtype]
+    qts, qhs = _head_strides(q, "q")
+    if mode != 0:
+        gts, ghs = _head_strides(gate, "gate")
+    else:
+        gate, gts, ghs = None, 0, 0
+    if not (k.is_contiguous() and v.is_contiguous()):
+        raise ValueError("k and v must be contiguous [B,S,G,d]")
+    if pos is not None and (pos.dtype != torch.int32 or not pos.is_contiguous()):
+        raise ValueError("pos must be a contiguous int32 [B,S] tensor")
+    if out is None:
+        out = torch.empty((B, S, H * d), dtype=q.dtype, device=q.device)
+    need = gattn_prefill_workspace_size(B, S, H, G, d, q.dtype)
+    if workspace is None or workspace.numel() * workspace.element_size() < need:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    st = _lib.load().gattn_prefill(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(gate), _ptr(qnorm_w), _ptr(knorm_w), _ptr(pos), B, S, H, G, d,
+        int(rotary_dim), float(rope_base), float(eps), mode, qts, qhs, gts, ghs, dt, _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _ptr(out), _stream_handle(stream, q.device))
+    check(st, "gattn_prefill")
+    return out
+
+
+def gattn_decode(q_new, kv_cache, seqlens, gate, qnorm_w, *, rotary_dim, rope_base, eps=1e-6,
+                 gate_mode="elementwise", out=None, workspace=None, stream=None):
+    """One decode step.  q_new [B,H,d] raw; kv_cache [2,B,G,Lmax,d] (K normed and
+    rotated, V raw); seqlens [B] int32 including the new token; gate [B,H,d] or
+    [B,H] or None; qnorm_w [d].  bf16.  Returns out [B,H*d]."""
+    mode = _mode(gate_mode)
+    B, H, d = q_new.shape
+    G, Lmax = kv_cache.shape[2], kv_cache.shape[3]
+    for name, t in (("q_new", q_new), ("kv_cache", kv_cache), ("seqlens", seqlens), ("qnorm_w", qnorm_w)):
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    if mode != 0 and not gate.is_contiguous():
+        raise ValueError("gate must be contiguous")
+    if seqlens.dtype != torch.int32:
+        raise ValueError("seqlens must be int32")
+    if out is None:
+        out = torch.empty((B, H * d), dtype=q_new.dtype, device=q_new.device)
+    need = gattn_decode_workspace_size(B, H, G, d, Lmax)
+    if workspace is None or workspace.numel() * workspace.element_size() < need:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q_new.device)
+    st = _lib.load().gattn_decode(
+        _ptr(q_new), _ptr(kv_cache), _ptr(seqlens), _ptr(gate if mode != 0 else None), _ptr(qnorm_w), B, H, G, d,
+        Lmax, int(rotary_dim), float(rope_base), float(eps), mode, _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _ptr(out), _stream_handle(stream, q_new.device))
+    check(st, "gattn_decode")
+    return out

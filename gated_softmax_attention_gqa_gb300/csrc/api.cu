@@ -1,0 +1,319 @@
+// api.cu -- the libgattn C ABI: argument validation, workspace sizing, TMA
+// tensor maps and kernel launches.  See include/gattn.h for the contract.
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace gattn {
+int decode_max_batch();
+}
+
+using namespace gattn;
+
+namespace {
+
+__device__ unsigned int g_device_status;
+
+cudaEvent_t g_prof_start = nullptr, g_prof_stop = nullptr;
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// Device address of the status word on the current device.
+unsigned int* status_ptr() {
+    static unsigned int* ptrs[64] = {};
+    static std::mutex mu;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!ptrs[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) return nullptr;
+        ptrs[dev] = static_cast<unsigned int*>(p);
+    }
+    return ptrs[dev];
+}
+
+int sm_count() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    return n;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+void fill_inv_freq(float* dst, int rd, double base) {
+    for (int i = 0; i < kMaxRotaryHalf; ++i)
+        dst[i] = (i < rd / 2) ? (float)std::pow(base, -2.0 * (double)i / (double)rd) : 0.f;
+}
+
+// bf16 tensor map with a 64-element (128 B) inner box and 128 B swizzle.
+bool encode_bf16_map(CUtensorMap* map, const void* base, int rank, const uint64_t* dims, const uint64_t* strides_bytes,
+                     const uint32_t* box) {
+    auto fn = get_encode_fn();
+    if (!fn) return false;
+    cuuint32_t elem_strides[5] = {1, 1, 1, 1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void*>(base),
+                    reinterpret_cast<const cuuint64_t*>(dims), reinterpret_cast<const cuuint64_t*>(strides_bytes),
+                    reinterpret_cast<const cuuint32_t*>(box), elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+bool valid_gate_mode(int m) { return m == GATTN_GATE_NONE || m == GATTN_GATE_ELEMENTWISE || m == GATTN_GATE_HEADWISE; }
+
+size_t prefill_ws(int B, int S, int H, int G, int d, int dtype) {
+    if (B < 1 || S < 1 || H < 1 || G < 1 || d < 1) return 0;
+    const size_t kr = (size_t)B * G * S * d, qr = (size_t)B * H * S * d;
+    if (dtype == GATTN_BF16) return round_up(kr * 2, 256);
+    if (dtype == GATTN_FP32) return round_up(qr * 4, 256) + round_up(kr * 4, 256);
+    return 0;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* gattn_strerror(gattn_status s) {
+    switch (s) {
+        case GATTN_OK: return "GATTN_OK";
+        case GATTN_ERR_INVALID_ARG: return "GATTN_ERR_INVALID_ARG: invalid argument";
+        case GATTN_ERR_UNSUPPORTED: return "GATTN_ERR_UNSUPPORTED: no kernel for this configuration";
+        case GATTN_ERR_CUDA: return "GATTN_ERR_CUDA: a CUDA call or kernel launch failed";
+        case GATTN_ERR_WORKSPACE: return "GATTN_ERR_WORKSPACE: workspace missing, misaligned or too small";
+        case GATTN_ERR_DEVICE: return "GATTN_ERR_DEVICE: a kernel reported a device-side problem";
+    }
+    return "unknown gattn_status";
+}
+
+void gattn_set_profile_events(void* start, void* stop) {
+    g_prof_start = static_cast<cudaEvent_t>(start);
+    g_prof_stop = static_cast<cudaEvent_t>(stop);
+}
+
+size_t gattn_prefill_workspace_size(int B, int S, int H, int G, int d, int dtype) {
+    return prefill_ws(B, S, H, G, d, dtype);
+}
+
+gattn_status gattn_prefill(const void* q, const void* k, const void* v, const void* gate, const void* qnorm_w,
+                           const void* knorm_w, const int32_t* pos, int B, int S, int H, int G, int d,
+                           int rotary_dim, double rope_base, float eps, int gate_mode, int64_t q_tok_stride,
+                           int64_t q_head_stride, int64_t gate_tok_stride, int64_t gate_head_stride, int dtype,
+                           void* workspace, size_t workspace_bytes, void* out, void* stream_) {
+    // ---- arguments
+    if (!q || !k || !v || !qnorm_w || !knorm_w || !out) return GATTN_ERR_INVALID_ARG;
+    if (!valid_gate_mode(gate_mode) || (gate_mode != GATTN_GATE_NONE && !gate)) return GATTN_ERR_INVALID_ARG;
+    if (dtype != GATTN_BF16 && dtype != GATTN_FP32) return GATTN_ERR_INVALID_ARG;
+    if (B < 1 || S < 1 || H < 1 || G < 1 || d < 1 || H % G != 0) return GATTN_ERR_INVALID_ARG;
+    if (rotary_dim < 0 || rotary_dim > d || (rotary_dim & 1)) return GATTN_ERR_INVALID_ARG;
+    if (rotary_dim > 0 && !(rope_base > 0.0 && std::isfinite(rope_base))) return GATTN_ERR_INVALID_ARG;
+    if (!(eps >= 0.f) || !std::isfinite(eps)) return GATTN_ERR_INVALID_ARG;
+    if ((int64_t)B * S > INT32_MAX || (int64_t)B * G > INT32_MAX || (int64_t)B * H > INT32_MAX)
+        return GATTN_ERR_INVALID_ARG;
+    const bool bf = dtype == GATTN_BF16;
+    const int elt = bf ? 2 : 4;
+    if (bf ? !(d == 64 || d == 128 || d == 256) : !(d == 32 || d == 64 || d == 128 || d == 256))
+        return GATTN_ERR_UNSUPPORTED;
+    if (bf && rotary_dim % 16 != 0) return GATTN_ERR_UNSUPPORTED;
+    if (q_tok_stride == 0) q_tok_stride = (int64_t)H * d;
+    if (q_head_stride == 0) q_head_stride = d;
+    const bool headwise = gate_mode == GATTN_GATE_HEADWISE;
+    if (gate_tok_stride == 0) gate_tok_stride = headwise ? H : (int64_t)H * d;
+    if (gate_head_stride == 0) gate_head_stride = headwise ? 1 : d;
+    if (q_tok_stride < 0 || q_head_stride < 0 || gate_tok_stride < 0 || gate_head_stride < 0)
+        return GATTN_ERR_INVALID_ARG;
+    const int64_t vec = 16 / elt;
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16)) return GATTN_ERR_INVALID_ARG;
+    if (q_tok_stride % vec || q_head_stride % vec) return GATTN_ERR_INVALID_ARG;
+    if (gate_mode == GATTN_GATE_ELEMENTWISE && (!aligned(gate, 16) || gate_tok_stride % vec || gate_head_stride % vec))
+        return GATTN_ERR_INVALID_ARG;
+    if (bf && (!aligned(qnorm_w, 16) || !aligned(knorm_w, 16))) return GATTN_ERR_INVALID_ARG;
+    const size_t need = prefill_ws(B, S, H, G, d, dtype);
+    if (!workspace || !aligned(workspace, 256) || workspace_bytes < need) return GATTN_ERR_WORKSPACE;
+
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+    unsigned int* status = status_ptr();
+    if (!status) return GATTN_ERR_CUDA;
+
+    // ---- K' = rope(rmsnorm(k)) into the workspace, [B,G,S,d]
+    ProloguePlan kp;
+    std::memset(&kp, 0, sizeof(kp));
+    kp.x = k;
+    kp.tok_stride = (int64_t)G * d;
+    kp.head_stride = d;
+    kp.w = knorm_w;
+    kp.pos = pos;
+    kp.B = B;
+    kp.S = S;
+    kp.n_heads = G;
+    kp.d = d;
+    kp.rd = rotary_dim;
+    kp.eps = eps;
+    fill_inv_freq(kp.inv_freq, rotary_dim, rope_base);
+
+    if (bf) {
+        kp.dst = workspace;
+        if (launch_prologue(kp, true, true, stream) != cudaSuccess) return GATTN_ERR_CUDA;
+        CUtensorMap tmK, tmV;
+        const uint64_t kdims[3] = {(uint64_t)d, (uint64_t)S, (uint64_t)B * G};
+        const uint64_t kstr[2] = {(uint64_t)d * 2, (uint64_t)S * d * 2};
+        const uint32_t kbox[3] = {64, (uint32_t)prefill_block_n(d), 1};
+        const uint64_t vdims[4] = {(uint64_t)d, (uint64_t)G, (uint64_t)S, (uint64_t)B};
+        const uint64_t vstr[3] = {(uint64_t)d * 2, (uint64_t)G * d * 2, (uint64_t)S * G * d * 2};
+        const uint32_t vbox[4] = {64, 1, (uint32_t)prefill_block_n(d), 1};
+        if (!encode_bf16_map(&tmK, workspace, 3, kdims, kstr, kbox)) return GATTN_ERR_CUDA;
+        if (!encode_bf16_map(&tmV, v, 4, vdims, vstr, vbox)) return GATTN_ERR_CUDA;
+        PrefillParams pp;
+        std::memset(&pp, 0, sizeof(pp));
+        pp.q = q;
+        pp.gate = gate;
+        pp.qnorm_w = qnorm_w;
+        pp.pos = pos;
+        pp.out = out;
+        pp.q_tok_stride = q_tok_stride;
+        pp.q_head_stride = q_head_stride;
+        pp.gate_tok_stride = gate_tok_stride;
+        pp.gate_head_stride = gate_head_stride;
+        pp.B = B;
+        pp.S = S;
+        pp.H = H;
+        pp.G = G;
+        pp.d = d;
+        pp.rd = rotary_dim;
+        pp.gate_mode = gate_mode;
+        pp.n_qtiles = (S + 127) / 128;
+        pp.eps = eps;
+        pp.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)d));
+        pp.status = status;
+        std::memcpy(pp.inv_freq, kp.inv_freq, sizeof(pp.inv_freq));
+        if (launch_prefill_tc(pp, tmK, tmV, stream, g_prof_start, g_prof_stop) != cudaSuccess) return GATTN_ERR_CUDA;
+        return GATTN_OK;
+    }
+
+    // ---- fp32: q' and k' into the workspace, then the CUDA-core kernel
+    float* qr = static_cast<float*>(workspace);
+    float* kr = reinterpret_cast<float*>(static_cast<char*>(workspace) + round_up((size_t)B * H * S * d * 4, 256));
+    kp.dst = kr;
+    if (launch_prologue(kp, false, false, stream) != cudaSuccess) return GATTN_ERR_CUDA;
+    ProloguePlan qp = kp;
+    qp.x = q;
+    qp.tok_stride = q_tok_stride;
+    qp.head_stride = q_head_stride;
+    qp.w = qnorm_w;
+    qp.n_heads = H;
+    qp.dst = qr;
+    if (launch_prologue(qp, false, false, stream) != cudaSuccess) return GATTN_ERR_CUDA;
+    PrefillF32Params fp;
+    std::memset(&fp, 0, sizeof(fp));
+    fp.qr = qr;
+    fp.kr = kr;
+    fp.v = static_cast<const float*>(v);
+    fp.gate = static_cast<const float*>(gate);
+    fp.out = static_cast<float*>(out);
+    fp.gate_tok_stride = gate_tok_stride;
+    fp.gate_head_stride = gate_head_stride;
+    fp.B = B;
+    fp.S = S;
+    fp.H = H;
+    fp.G = G;
+    fp.d = d;
+    fp.gate_mode = gate_mode;
+    fp.scale = (float)(1.0 / std::sqrt((double)d));
+    if (launch_prefill_f32(fp, stream, g_prof_start, g_prof_stop) != cudaSuccess) return GATTN_ERR_CUDA;
+    return GATTN_OK;
+}
+
+size_t gattn_decode_workspace_size(int B, int H, int G, int d, int Lmax) {
+    if (B < 1 || H < 1 || G < 1 || d < 1 || Lmax < 1 || H % G != 0) return 0;
+    const int n = sm_count();
+    if (n <= 0) return 0;
+    return round_up((size_t)decode_num_slots(n, B, G) * decode_slot_floats(H / G, d) * sizeof(float), 256);
+}
+
+gattn_status gattn_decode(const void* q_new, const void* kv_cache, const int32_t* seqlens, const void* gate,
+                          const void* qnorm_w, int B, int H, int G, int d, int Lmax, int rotary_dim,
+                          double rope_base, float eps, int gate_mode, void* workspace, size_t workspace_bytes,
+                          void* out, void* stream_) {
+    if (!q_new || !kv_cache || !seqlens || !qnorm_w || !out) return GATTN_ERR_INVALID_ARG;
+    if (!valid_gate_mode(gate_mode) || (gate_mode != GATTN_GATE_NONE && !gate)) return GATTN_ERR_INVALID_ARG;
+    if (B < 1 || H < 1 || G < 1 || d < 1 || Lmax < 1 || H % G != 0) return GATTN_ERR_INVALID_ARG;
+    if (rotary_dim < 0 || rotary_dim > d || (rotary_dim & 1)) return GATTN_ERR_INVALID_ARG;
+    if (rotary_dim > 0 && !(rope_base > 0.0 && std::isfinite(rope_base))) return GATTN_ERR_INVALID_ARG;
+    if (!(eps >= 0.f) || !std::isfinite(eps)) return GATTN_ERR_INVALID_ARG;
+    if (!(d == 64 || d == 128 || d == 256) || H / G > 8 || rotary_dim % 16 != 0 || B > decode_max_batch())
+        return GATTN_ERR_UNSUPPORTED;
+    if (2 * (int64_t)B * G * Lmax + kDecodeTileKeys > INT32_MAX) return GATTN_ERR_UNSUPPORTED;
+    if (!aligned(kv_cache, 16) || !aligned(q_new, 4) || !aligned(qnorm_w, 4) || !aligned(out, 2))
+        return GATTN_ERR_INVALID_ARG;
+    const int n_ctas = sm_count();
+    if (n_ctas <= 0) return GATTN_ERR_CUDA;
+    const size_t need = gattn_decode_workspace_size(B, H, G, d, Lmax);
+    if (!workspace || !aligned(workspace, 256) || workspace_bytes < need) return GATTN_ERR_WORKSPACE;
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+    unsigned int* status = status_ptr();
+    if (!status) return GATTN_ERR_CUDA;
+
+    CUtensorMap tm;
+    const uint64_t dims[2] = {(uint64_t)d, 2ull * B * G * Lmax};
+    const uint64_t str[1] = {(uint64_t)d * 2};
+    const uint32_t box[2] = {64, (uint32_t)kDecodeTileKeys};
+    if (!encode_bf16_map(&tm, kv_cache, 2, dims, str, box)) return GATTN_ERR_CUDA;
+
+    DecodeParams dp;
+    std::memset(&dp, 0, sizeof(dp));
+    dp.q = q_new;
+    dp.seqlens = seqlens;
+    dp.gate = gate;
+    dp.qnorm_w = qnorm_w;
+    dp.out = out;
+    dp.part = static_cast<float*>(workspace);
+    dp.B = B;
+    dp.H = H;
+    dp.G = G;
+    dp.d = d;
+    dp.Lmax = Lmax;
+    dp.rd = rotary_dim;
+    dp.gate_mode = gate_mode;
+    dp.n_ctas = n_ctas;
+    dp.eps = eps;
+    dp.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)d));
+    dp.status = status;
+    fill_inv_freq(dp.inv_freq, rotary_dim, rope_base);
+    if (launch_decode(dp, tm, stream, g_prof_start, g_prof_stop) != cudaSuccess) return GATTN_ERR_CUDA;
+    return GATTN_OK;
+}
+
+gattn_status gattn_get_device_status(unsigned int* bits, void* stream_) {
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+    unsigned int* status = status_ptr();
+    if (!status) return GATTN_ERR_CUDA;
+    unsigned int h = 0;
+    if (cudaMemcpyAsync(&h, status, sizeof(h), cudaMemcpyDeviceToHost, stream) != cudaSuccess) return GATTN_ERR_CUDA;
+    if (cudaMemsetAsync(status, 0, sizeof(h), stream) != cudaSuccess) return GATTN_ERR_CUDA;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return GATTN_ERR_CUDA;
+    if (bits) *bits = h;
+    return h ? GATTN_ERR_DEVICE : GATTN_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,84 @@
+// internal.h -- parameter blocks and launchers shared between the host ABI
+// (api.cu) and the kernel translation units.  Not part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace gattn {
+
+constexpr int kMaxRotaryHalf = 128;  // rotary_dim <= 256
+
+// Normalise + rotate rows of a [B,S,n_heads,d] tensor (token/head strides in
+// elements) into a contiguous [B,n_heads,S,d] tensor of the same or wider type.
+struct ProloguePlan {
+    const void* x;
+    int64_t tok_stride, head_stride;
+    const void* w;
+    const int32_t* pos;
+    void* dst;
+    int B, S, n_heads, d, rd;
+    float eps;
+    float inv_freq[kMaxRotaryHalf];
+};
+
+// bf16 tcgen05 prefill.
+struct PrefillParams {
+    const void* q;
+    const void* gate;
+    const void* qnorm_w;
+    const int32_t* pos;
+    void* out;
+    int64_t q_tok_stride, q_head_stride, gate_tok_stride, gate_head_stride;
+    int B, S, H, G, d, rd, gate_mode, n_qtiles;
+    float eps, scale_log2;
+    unsigned int* status;
+    float inv_freq[kMaxRotaryHalf];
+};
+
+// fp32 SIMT prefill over pre-normed/rotated q', k' (workspace) and raw v.
+struct PrefillF32Params {
+    const float* qr;  // [B,H,S,d]
+    const float* kr;  // [B,G,S,d]
+    const float* v;   // [B,S,G,d]
+    const float* gate;
+    float* out;
+    int64_t gate_tok_stride, gate_head_stride;
+    int B, S, H, G, d, gate_mode;
+    float scale;
+};
+
+// bf16 split-KV decode.
+struct DecodeParams {
+    const void* q;  // [B,H,d]
+    const int32_t* seqlens;
+    const void* gate;
+    const void* qnorm_w;
+    void* out;      // [B,H*d]
+    float* part;    // partial softmax states
+    int B, H, G, d, Lmax, rd, gate_mode, n_ctas;
+    float eps, scale_log2;
+    unsigned int* status;
+    float inv_freq[kMaxRotaryHalf];
+};
+
+cudaError_t launch_prologue(const ProloguePlan& p, bool bf16_in, bool bf16_out, cudaStream_t stream);
+cudaError_t launch_prefill_tc(const PrefillParams& p, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
+                              cudaStream_t stream, cudaEvent_t ev_start, cudaEvent_t ev_stop);
+cudaError_t launch_prefill_f32(const PrefillF32Params& p, cudaStream_t stream, cudaEvent_t ev_start,
+                               cudaEvent_t ev_stop);
+cudaError_t launch_decode(const DecodeParams& p, const CUtensorMap& tm_kv, cudaStream_t stream,
+                          cudaEvent_t ev_start, cudaEvent_t ev_stop);
+
+// Prefill tile geometry for the tcgen05 kernel, per head_dim.
+int prefill_block_n(int d);
+
+// Decode work split: the size of one partial-state slot in floats and the
+// number of slots the workspace must hold.
+int decode_slot_floats(int r, int d);
+int64_t decode_num_slots(int n_ctas, int B, int G);
+constexpr int kDecodeConsumerWarps = 4;
+constexpr int kDecodeTileKeys = 64;
+
+}  // namespace gattn

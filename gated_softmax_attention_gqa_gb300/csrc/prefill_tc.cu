@@ -1,0 +1,479 @@
+// prefill_tc.cu -- bf16 causal gated GQA attention on 5th-generation tensor cores.
+//
+// One CTA computes one 128-row query tile of one head:
+//   out[b, t, h*d:(h+1)*d] = sigmoid(z) * sum_{j<=t} softmax_j(q'_t . k'_j / sqrt(d)) v_j
+// where q' = rope(rmsnorm(q)), k' = rope(rmsnorm(k)) and head h reads KV group
+// g = floor(h / (H/G)).  ("Gated attention" handbook chapter, sections "The
+// formula", "Four things Qwen3.5 adds to the textbook" and "The code:
+// qwen/attention.py"; "Attention, worked all the way through", section "Why
+// scaling and stable softmax matter"; "Gated Attention" deep-dive, section
+// "门放在哪里？".)
+//
+// Roles (6 warps):
+//   warp 0      TMA producer: K' tiles (normed+rotated keys from the pre-pass) and
+//               raw V tiles into a 3-stage shared-memory ring, 128 B swizzle.
+//   warp 1      TMEM owner and MMA issuer (one elected lane): S = Q'K'^T and
+//               O += P V with tcgen05.mma, A operand read from TMEM.
+//   warps 2..5  one thread per query row: the fused Q prologue (RMSNorm + RoPE
+//               of the raw query row, written as bf16 straight into TMEM), the
+//               online softmax, and the gate epilogue.
+//
+// TMEM (512 columns x 128 lanes, lane = query row):
+//   [0, d)            O accumulator, fp32
+//   [d, d+BN)         S buffer 0 (fp32 scores; overwritten in place by bf16 P)
+//   [d+BN, d+2BN)     S buffer 1
+//   [d+2BN, d+2BN+d/2) Q' as packed bf16 pairs (A operand of S = Q'K'^T)
+//
+// Pipeline: while the softmax threads turn S_j into P_j, the tensor core already
+// computes S_{j+1} into the other buffer; P_j V_j follows as soon as P_j lands.
+// The running max is only refreshed (and O rescaled in TMEM) when it grows by
+// more than 2^8, so the rescale is rare and exact: O and l always share one
+// reference max.  The causal mask is applied by skipping every KV tile past the
+// query tile and masking only the tiles that straddle the diagonal.
+#include "common.cuh"
+#include "internal.h"
+
+namespace gattn {
+namespace {
+
+template <int D>
+struct PfCfg {
+    static constexpr int BM = 128;
+    static constexpr int BN = (D == 256) ? 64 : 128;
+    static constexpr int NS = 3;
+    static constexpr int KCH = D / 64;               // 128-byte chunks along head_dim
+    static constexpr int CHUNK_BYTES = BN * 128;     // one TMA box: BN rows x 64 bf16
+    static constexpr int TILE_BYTES = BN * D * 2;
+    static constexpr int TM_O = 0;
+    static constexpr int TM_S0 = D;
+    static constexpr int TM_S1 = D + BN;
+    static constexpr int TM_Q = D + 2 * BN;
+    static constexpr int TM_COLS = 512;
+    static_assert(TM_Q + D / 2 <= TM_COLS, "TMEM budget");
+    static constexpr int OFF_K = 0;
+    static constexpr int OFF_V = NS * TILE_BYTES;
+    static constexpr int OFF_BAR = 2 * NS * TILE_BYTES;
+    static constexpr int NBAR = 4 * NS + 8;
+    static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+    static constexpr int SMEM_BYTES = OFF_MISC + 16;
+    // + slack for 1024-byte alignment; never less than 120 KB, so that a second CTA
+    // can never share the SM (each CTA allocates all 512 TMEM columns).
+    static constexpr int SMEM_ALLOC = (SMEM_BYTES + 1024) > 122880 ? (SMEM_BYTES + 1024) : 122880;
+    static constexpr int THREADS = 192;
+    static constexpr uint32_t IDESC_QK = make_idesc_bf16(128, BN, false);
+    static constexpr uint32_t IDESC_PV = make_idesc_bf16(128, D, true);
+    static constexpr float RESCALE_THRESHOLD = 8.0f;  // log2 domain: rescale when the max grows by > 2^8
+};
+
+struct Bars {
+    uint32_t base;
+    int ns;
+    __device__ uint32_t k_full(int s) const { return base + 8u * s; }
+    __device__ uint32_t k_empty(int s) const { return base + 8u * (ns + s); }
+    __device__ uint32_t v_full(int s) const { return base + 8u * (2 * ns + s); }
+    __device__ uint32_t v_empty(int s) const { return base + 8u * (3 * ns + s); }
+    __device__ uint32_t s_full(int i) const { return base + 8u * (4 * ns + i); }
+    __device__ uint32_t p_full(int i) const { return base + 8u * (4 * ns + 2 + i); }
+    __device__ uint32_t o_done() const { return base + 8u * (4 * ns + 4); }
+    __device__ uint32_t o_final() const { return base + 8u * (4 * ns + 5); }
+    __device__ uint32_t q_ready() const { return base + 8u * (4 * ns + 6); }
+    __device__ uint32_t drain() const { return base + 8u * (4 * ns + 7); }
+};
+
+__device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
+    uint4 r;
+    asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
+    return r;
+}
+
+__device__ __forceinline__ void unpack8(const uint4& v, float (&f)[8]) {
+    f[0] = bf16_lo(v.x); f[1] = bf16_hi(v.x);
+    f[2] = bf16_lo(v.y); f[3] = bf16_hi(v.y);
+    f[4] = bf16_lo(v.z); f[5] = bf16_hi(v.z);
+    f[6] = bf16_lo(v.w); f[7] = bf16_hi(v.w);
+}
+
+// ----------------------------------------------------------------- producer
+
+template <int D>
+__device__ void run_producer(const CUtensorMap* tmK, const CUtensorMap* tmV, const Bars& bars, uint32_t sbase,
+                             int n_kv, int b, int g, int G, volatile int* abort_flag, unsigned int* status) {
+    using C = PfCfg<D>;
+    int nk = 0, nv = 0;
+    for (int j = 0; j < n_kv; ++j) {
+        const int st = j % C::NS;
+        const uint32_t ph = (uint32_t)(j / C::NS) & 1u;
+        if (j >= C::NS && !mbar_wait(bars.k_empty(st), ph ^ 1u, abort_flag, status)) break;
+        mbar_arrive_expect_tx(bars.k_full(st), C::TILE_BYTES);
+        const uint32_t kdst = sbase + C::OFF_K + st * C::TILE_BYTES;
+#pragma unroll
+        for (int c = 0; c < C::KCH; ++c)
+            tma_load_3d(kdst + c * C::CHUNK_BYTES, tmK, bars.k_full(st), c * 64, j * C::BN, b * G + g);
+        ++nk;
+        if (j >= C::NS && !mbar_wait(bars.v_empty(st), ph ^ 1u, abort_flag, status)) break;
+        mbar_arrive_expect_tx(bars.v_full(st), C::TILE_BYTES);
+        const uint32_t vdst = sbase + C::OFF_V + st * C::TILE_BYTES;
+#pragma unroll
+        for (int c = 0; c < C::KCH; ++c)
+            tma_load_4d(vdst + c * C::CHUNK_BYTES, tmV, bars.v_full(st), c * 64, g, j * C::BN, b);
+        ++nv;
+    }
+    // Drain: every copy this thread started must land before the CTA can exit.
+    for (int j = nk > C::NS ? nk - C::NS : 0; j < nk; ++j)
+        mbar_wait_drain(bars.k_full(j % C::NS), (uint32_t)(j / C::NS) & 1u, status);
+    for (int j = nv > C::NS ? nv - C::NS : 0; j < nv; ++j)
+        mbar_wait_drain(bars.v_full(j % C::NS), (uint32_t)(j / C::NS) & 1u, status);
+}
+
+// ----------------------------------------------------------------- MMA issuer
+
+template <int D>
+__device__ void run_mma(const Bars& bars, uint32_t sbase, uint32_t tm, int n_kv, volatile int* abort_flag,
+                        unsigned int* status) {
+    using C = PfCfg<D>;
+    bool ok = mbar_wait(bars.q_ready(), 0, abort_flag, status);
+    tc_fence_after();
+
+    auto issue_qk = [&](int j) -> bool {
+        const int st = j % C::NS;
+        if (!mbar_wait(bars.k_full(st), (uint32_t)(j / C::NS) & 1u, abort_flag, status)) return false;
+        tc_fence_after();
+        const uint32_t d_tmem = tm + ((j & 1) ? C::TM_S1 : C::TM_S0);
+        const uint32_t kbase = sbase + C::OFF_K + st * C::TILE_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+            const uint64_t bdesc = make_sdesc_sw128(kbase + (kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32, 16, 1024);
+            mma_ts(d_tmem, tm + C::TM_Q + kk * 8, bdesc, C::IDESC_QK, kk > 0 ? 1u : 0u);
+        }
+        tc_commit(bars.k_empty(st));
+        tc_commit(bars.s_full(j & 1));
+        return true;
+    };
+
+    if (ok) ok = issue_qk(0);
+    for (int j = 0; ok && j < n_kv; ++j) {
+        if (j + 1 < n_kv && !issue_qk(j + 1)) { ok = false; break; }
+        if (!mbar_wait(bars.p_full(j & 1), (uint32_t)(j >> 1) & 1u, abort_flag, status)) { ok = false; break; }
+        tc_fence_after();
+        const int st = j % C::NS;
+        if (!mbar_wait(bars.v_full(st), (uint32_t)(j / C::NS) & 1u, abort_flag, status)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t p_tmem = tm + ((j & 1) ? C::TM_S1 : C::TM_S0);
+        const uint32_t vbase = sbase + C::OFF_V + st * C::TILE_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < C::BN / 16; ++kk) {
+            const uint64_t bdesc = make_sdesc_sw128(vbase + kk * 16 * 128, C::CHUNK_BYTES, 1024);
+            mma_ts(tm + C::TM_O, p_tmem + kk * 8, bdesc, C::IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
+        }
+        tc_commit(bars.v_empty(st));
+        tc_commit(bars.o_done());
+    }
+    if (ok) tc_commit(bars.o_final());
+    // Whatever happened, no MMA may still be in flight when TMEM is released.
+    tc_commit(bars.drain());
+    mbar_wait_drain(bars.drain(), 0, status);
+}
+
+// ----------------------------------------------------------------- softmax / prologue / epilogue
+
+template <int D>
+__device__ void run_softmax(const PrefillParams& p, const Bars& bars, uint32_t tm, int quarter, int lane, int qt,
+                            int b, int h, int n_kv, volatile int* abort_flag) {
+    using C = PfCfg<D>;
+    const int row = quarter * 32 + lane;
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    const uint32_t tl = tm + lane_off;
+    const int t = qt * C::BM + row;
+    const bool valid = t < p.S;
+    const int64_t tok = (int64_t)b * p.S + (valid ? t : 0);
+
+    // ---- fused Q prologue: rmsnorm then partial rotate-half RoPE, bf16 into TMEM
+    {
+        const bf16* qrow = static_cast<const bf16*>(p.q) + tok * p.q_tok_stride + (int64_t)h * p.q_head_stride;
+        const bf16* wq = static_cast<const bf16*>(p.qnorm_w);
+        float ss = 0.f;
+        if (valid) {
+#pragma unroll 4
+            for (int c = 0; c < D / 8; ++c) {
+                float f[8];
+                unpack8(ldg_nc_v4(qrow + 8 * c), f);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) ss = fmaf(f[e], f[e], ss);
+            }
+        }
+        const float rinv = rsqrtf(ss / (float)D + p.eps);
+        const float posf = valid ? (p.pos ? (float)p.pos[tok] : (float)t) : 0.f;
+        const int half = p.rd >> 1;
+        for (int i0 = 0; i0 < half; i0 += 8) {
+            float xa[8], xb[8], wa[8], wb[8];
+            if (valid) {
+                unpack8(ldg_nc_v4(qrow + i0), xa);
+                unpack8(ldg_nc_v4(qrow + i0 + half), xb);
+            } else {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) xa[e] = xb[e] = 0.f;
+            }
+            unpack8(ldg_nc_v4(wq + i0), wa);
+            unpack8(ldg_nc_v4(wq + i0 + half), wb);
+            __syncwarp();
+            uint32_t lo[4], hi[4];
+#pragma unroll
+            for (int e = 0; e < 8; e += 2) {
+                float s0, c0, s1, c1;
+                sincosf(posf * p.inv_freq[i0 + e], &s0, &c0);
+                sincosf(posf * p.inv_freq[i0 + e + 1], &s1, &c1);
+                const float a0 = xa[e] * wa[e], b0 = xb[e] * wb[e];
+                const float a1 = xa[e + 1] * wa[e + 1], b1 = xb[e + 1] * wb[e + 1];
+                lo[e >> 1] = pack_bf16x2((a0 * c0 - b0 * s0) * rinv, (a1 * c1 - b1 * s1) * rinv);
+                hi[e >> 1] = pack_bf16x2((b0 * c0 + a0 * s0) * rinv, (b1 * c1 + a1 * s1) * rinv);
+            }
+            tmem_st4(tl + C::TM_Q + (i0 >> 1), lo[0], lo[1], lo[2], lo[3]);
+            tmem_st4(tl + C::TM_Q + ((i0 + half) >> 1), hi[0], hi[1], hi[2], hi[3]);
+        }
+        for (int e0 = p.rd; e0 < D; e0 += 8) {
+            float x[8], w[8];
+            if (valid) {
+                unpack8(ldg_nc_v4(qrow + e0), x);
+            } else {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) x[e] = 0.f;
+            }
+            unpack8(ldg_nc_v4(wq + e0), w);
+            __syncwarp();
+            tmem_st4(tl + C::TM_Q + (e0 >> 1), pack_bf16x2(x[0] * w[0] * rinv, x[1] * w[1] * rinv),
+                     pack_bf16x2(x[2] * w[2] * rinv, x[3] * w[3] * rinv),
+                     pack_bf16x2(x[4] * w[4] * rinv, x[5] * w[5] * rinv),
+                     pack_bf16x2(x[6] * w[6] * rinv, x[7] * w[7] * rinv));
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bars.q_ready());
+    }
+
+    // ---- main loop: online softmax over the KV tiles this query tile can see
+    const float sl2 = p.scale_log2;
+    const int row_min = qt * C::BM;
+    float m_ref = -INFINITY;  // reference max (log2 domain) shared by O and l
+    float l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < n_kv; ++j) {
+        const int sb = j & 1;
+        const uint32_t s_col = sb ? C::TM_S1 : C::TM_S0;
+        if (!__all_sync(0xffffffffu, mbar_wait(bars.s_full(sb), (uint32_t)(j >> 1) & 1u, abort_flag, p.status))) {
+            ok = false;
+            break;
+        }
+        tc_fence_after();
+        float s[C::BN];
+        {
+            uint32_t r[64];
+#pragma unroll
+            for (int c = 0; c < C::BN; c += 64) {
+                tmem_ld64(tl + s_col + c, r);
+#pragma unroll
+                for (int e = 0; e < 64; ++e) s[c + e] = __uint_as_float(r[e]);
+            }
+        }
+        const int key0 = j * C::BN;
+        if (key0 + C::BN - 1 > row_min) {
+#pragma unroll
+            for (int c = 0; c < C::BN; ++c)
+                if (key0 + c > t) s[c] = -INFINITY;
+        }
+        float mt = s[0];
+#pragma unroll
+        for (int c = 1; c < C::BN; ++c) mt = fmaxf(mt, s[c]);
+        const float m_new = fmaxf(m_ref, mt * sl2);
+        const bool need = (m_new - m_ref) > C::RESCALE_THRESHOLD;
+        if (j == 0) {
+            m_ref = m_new;
+        } else if (__any_sync(0xffffffffu, need)) {
+            const float alpha = need ? ex2_approx(m_ref - m_new) : 1.f;
+            if (need) {
+                l *= alpha;
+                m_ref = m_new;
+            }
+            __syncwarp();
+            // O is only touched once the previous P V has landed.
+            if (!__all_sync(0xffffffffu, mbar_wait(bars.o_done(), (uint32_t)(j - 1) & 1u, abort_flag, p.status))) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+#pragma unroll 1
+            for (int c = 0; c < D; c += 32) {
+                uint32_t r[32];
+                tmem_ld32(tl + C::TM_O + c, r);
+#pragma unroll
+                for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
+                tmem_st32(tl + C::TM_O + c, r);
+            }
+        }
+        // P = exp2(s * scale * log2e - m_ref), packed bf16, written over S in TMEM
+        float rs = 0.f;
+        const float mref = m_ref;
+#pragma unroll
+        for (int c = 0; c < C::BN; c += 64) {
+            uint32_t pk[32];
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+                const float p0 = ex2_approx(fmaf(s[c + 2 * e], sl2, -mref));
+                const float p1 = ex2_approx(fmaf(s[c + 2 * e + 1], sl2, -mref));
+                rs += p0 + p1;
+                pk[e] = pack_bf16x2(p0, p1);
+            }
+            tmem_st32(tl + s_col + (c >> 1), pk);
+        }
+        l += rs;
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bars.p_full(sb));
+    }
+    if (!ok) return;
+
+    // ---- epilogue: O / l * sigmoid(gate) -> bf16 [B,S,H*d]
+    if (!__all_sync(0xffffffffu, mbar_wait(bars.o_final(), 0, abort_flag, p.status))) return;
+    tc_fence_after();
+    const float inv_l = 1.f / l;
+    bf16* orow = static_cast<bf16*>(p.out) + (tok * p.H + h) * D;
+    const bf16* grow = static_cast<const bf16*>(p.gate) + tok * p.gate_tok_stride + (int64_t)h * p.gate_head_stride;
+    float gh = inv_l;
+    if (p.gate_mode == GATTN_GATE_HEADWISE && valid) gh = inv_l * sigmoidf_dev(__bfloat162float(grow[0]));
+#pragma unroll 1
+    for (int c = 0; c < D; c += 32) {
+        uint32_t r[32];
+        __syncwarp();
+        tmem_ld32(tl + C::TM_O + c, r);
+        if (!valid) continue;
+        float gv[32];
+        if (p.gate_mode == GATTN_GATE_ELEMENTWISE) {
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+                float f[8];
+                unpack8(ldg_nc_v4(grow + c + 8 * q4), f);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) gv[8 * q4 + e] = inv_l * sigmoidf_dev(f[e]);
+            }
+        } else {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) gv[e] = gh;
+        }
+        uint4* dst = reinterpret_cast<uint4*>(orow + c);
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+            uint4 v;
+            v.x = pack_bf16x2(__uint_as_float(r[8 * q4 + 0]) * gv[8 * q4 + 0], __uint_as_float(r[8 * q4 + 1]) * gv[8 * q4 + 1]);
+            v.y = pack_bf16x2(__uint_as_float(r[8 * q4 + 2]) * gv[8 * q4 + 2], __uint_as_float(r[8 * q4 + 3]) * gv[8 * q4 + 3]);
+            v.z = pack_bf16x2(__uint_as_float(r[8 * q4 + 4]) * gv[8 * q4 + 4], __uint_as_float(r[8 * q4 + 5]) * gv[8 * q4 + 5]);
+            v.w = pack_bf16x2(__uint_as_float(r[8 * q4 + 6]) * gv[8 * q4 + 6], __uint_as_float(r[8 * q4 + 7]) * gv[8 * q4 + 7]);
+            dst[q4] = v;
+        }
+    }
+}
+
+// ----------------------------------------------------------------- kernel
+
+template <int D>
+__global__ void __launch_bounds__(PfCfg<D>::THREADS, 1)
+    prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                      const __grid_constant__ PrefillParams p) {
+    using C = PfCfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = smem_u32(smem);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const Bars bars{sbase + C::OFF_BAR, C::NS};
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
+
+    // heaviest query tiles first; the heads of one KV group are adjacent
+    const int bh_count = p.B * p.H;
+    const int qt = p.n_qtiles - 1 - (int)(blockIdx.x / bh_count);
+    const int bh = (int)(blockIdx.x % bh_count);
+    const int b = bh / p.H, h = bh % p.H, g = h / (p.H / p.G);
+    const int q_end = min(p.S, (qt + 1) * C::BM);
+    const int n_kv = (q_end + C::BN - 1) / C::BN;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::NS; ++s) {
+            mbar_init(bars.k_full(s), 1);
+            mbar_init(bars.k_empty(s), 1);
+            mbar_init(bars.v_full(s), 1);
+            mbar_init(bars.v_empty(s), 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(bars.s_full(i), 1);
+            mbar_init(bars.p_full(i), 4);
+        }
+        mbar_init(bars.o_done(), 1);
+        mbar_init(bars.o_final(), 1);
+        mbar_init(bars.q_ready(), 4);
+        mbar_init(bars.drain(), 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmK);
+        tma_prefetch_desc(&tmV);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), C::TM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tm = *tmem_slot;
+
+    if (warp == 0) {
+        if (lane == 0) run_producer<D>(&tmK, &tmV, bars, sbase, n_kv, b, g, p.G, abort_flag, p.status);
+        __syncwarp();
+    } else if (warp == 1) {
+        if (lane == 0) run_mma<D>(bars, sbase, tm, n_kv, abort_flag, p.status);
+        __syncwarp();
+    } else {
+        run_softmax<D>(p, bars, tm, warp & 3, lane, qt, b, h, n_kv, abort_flag);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tm, C::TM_COLS);
+    }
+}
+
+template <int D>
+cudaError_t launch_d(const PrefillParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV, cudaStream_t stream,
+                     cudaEvent_t ev_start, cudaEvent_t ev_stop) {
+    using C = PfCfg<D>;
+    cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::SMEM_ALLOC);
+    if (e != cudaSuccess) return e;
+    const long long blocks = (long long)p.n_qtiles * p.B * p.H;
+    if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
+    if (ev_start) cudaEventRecord(ev_start, stream);
+    prefill_tc_kernel<D><<<(unsigned)blocks, C::THREADS, C::SMEM_ALLOC, stream>>>(tmK, tmV, p);
+    cudaError_t err = cudaGetLastError();
+    if (ev_stop) cudaEventRecord(ev_stop, stream);
+    return err;
+}
+
+}  // namespace
+
+int prefill_block_n(int d) { return d == 256 ? PfCfg<256>::BN : d == 128 ? PfCfg<128>::BN : PfCfg<64>::BN; }
+
+cudaError_t launch_prefill_tc(const PrefillParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV,
+                              cudaStream_t stream, cudaEvent_t ev_start, cudaEvent_t ev_stop) {
+    switch (p.d) {
+        case 64: return launch_d<64>(p, tmK, tmV, stream, ev_start, ev_stop);
+        case 128: return launch_d<128>(p, tmK, tmV, stream, ev_start, ev_stop);
+        case 256: return launch_d<256>(p, tmK, tmV, stream, ev_start, ev_stop);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace gattn

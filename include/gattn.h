@@ -1,0 +1,163 @@
+/*
+ * gattn.h -- C ABI of libgattn, the GB300 (sm_103a) gated softmax attention core.
+ *
+ * The library computes, on one GPU, the part of a gated full-attention layer
+ * that sits between the Q/K/V/gate projections and the output projection W_O:
+ *
+ *   1. QK-RMSNorm: per token and head, q and k (not v) are scaled by
+ *      rsqrt(mean(x^2) + eps) and a learned weight of length head_dim.
+ *      ("Gated attention" handbook chapter, section "Four things Qwen3.5 adds to
+ *      the textbook", QK-Norm; "Attention, worked all the way through",
+ *      section "Qwen3's exact order".)
+ *   2. Partial RoPE on the first rotary_dim features of q and k only
+ *      (handbook chapter, same section: "RoPE rotates only the first 64
+ *      dimensions").  Reading used: rotate-half, feature i paired with
+ *      i + rotary_dim/2, angle pos * rope_base^(-2i/rotary_dim).
+ *   3. Causal scaled-dot-product attention with GQA sharing: query head h reads
+ *      KV head floor(h / (H/G)); scores q.k / sqrt(head_dim); key j visible to
+ *      query t iff j <= t; row softmax; weighted sum of v.
+ *      (handbook chapter, section "The formula" and "The code:
+ *      qwen/attention.py"; "Multi-head attention and GQA" chapter, section
+ *      "分组查询注意力".)
+ *   4. Output gate G1: the attention output of each head is multiplied by
+ *      sigmoid(gate logits) -- one logit per dimension (elementwise) or one per
+ *      head (headwise) -- and the heads are concatenated to [tokens, H*d].
+ *      ("Gated Attention" deep-dive, section "门放在哪里？"; paper reading notes,
+ *      section "从标准注意力走到门控，计算流程有什么变化".)
+ *
+ * Conventions for every entry point
+ *   - All tensor pointers are DEVICE pointers owned by the caller.  The library
+ *     never allocates, frees or retains them, and keeps no per-call state.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t passed as void*;
+ *     NULL is the legacy default stream).  Argument errors are detected on the
+ *     host before anything is launched, and return a status without touching
+ *     the GPU.
+ *   - `out` must not alias any input or the workspace.
+ *   - Element types: GATTN_BF16 means q, k, v, gate, norm weights, cache and out
+ *     are all bfloat16 (fp32 accumulation inside); GATTN_FP32 means all fp32.
+ *   - Strides are in ELEMENTS.  A stride of 0 selects the contiguous default.
+ *   - Kernels never trap.  Problems found on the device (a sequence length
+ *     outside [1, Lmax], a bounded wait that ran out) set bits in a device
+ *     status word readable with gattn_get_device_status().
+ */
+#ifndef GATTN_H
+#define GATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    GATTN_OK = 0,
+    GATTN_ERR_INVALID_ARG = 1,  /* null pointer, bad size, misaligned pointer or stride */
+    GATTN_ERR_UNSUPPORTED = 2,  /* valid arguments this build has no kernel for (e.g. head_dim 96) */
+    GATTN_ERR_CUDA = 3,         /* a CUDA runtime/driver call or launch failed */
+    GATTN_ERR_WORKSPACE = 4,    /* workspace pointer missing, misaligned or too small */
+    GATTN_ERR_DEVICE = 5        /* gattn_get_device_status found a device-side problem */
+} gattn_status;
+
+typedef enum { GATTN_GATE_NONE = 0, GATTN_GATE_ELEMENTWISE = 1, GATTN_GATE_HEADWISE = 2 } gattn_gate_mode;
+
+typedef enum { GATTN_BF16 = 0, GATTN_FP32 = 1 } gattn_dtype;
+
+/* Device status bits (gattn_get_device_status). */
+#define GATTN_DEVICE_BAD_SEQLEN 0x1u  /* a decode seqlens[b] was outside [1, Lmax]; that sequence was skipped */
+#define GATTN_DEVICE_TIMEOUT 0x2u     /* a bounded wait inside a kernel ran out; its output is not valid */
+
+/* Human-readable name of a status code.  Never NULL. */
+const char* gattn_strerror(gattn_status status);
+
+/*
+ * Bytes of workspace gattn_prefill needs.  The workspace holds the normed and
+ * rotated keys (and, for GATTN_FP32, the normed and rotated queries), written
+ * and read within one call.  Returns 0 for invalid sizes.
+ */
+size_t gattn_prefill_workspace_size(int B, int S, int H, int G, int d, int dtype);
+
+/*
+ * Causal gated GQA attention over whole sequences (prefill).
+ *
+ * q        [B,S,H,d] raw query projections.  Element (b,t,h,e) is at
+ *          q[(b*S + t)*q_tok_stride + h*q_head_stride + e]; defaults
+ *          q_tok_stride = H*d, q_head_stride = d.  This lets q point into the
+ *          packed q_proj output [B,S,H,2d] whose first d values per head are the
+ *          query (handbook chapter, section "Why the gate is packed into
+ *          q_proj"): pass q_tok_stride = 2*H*d, q_head_stride = 2*d.
+ * k, v     [B,S,G,d] contiguous raw key / value projections.
+ * gate     gate logits; elementwise [B,S,H,d] at gate[(b*S+t)*gate_tok_stride +
+ *          h*gate_head_stride + e] (defaults H*d, d), headwise [B,S,H] at
+ *          gate[(b*S+t)*gate_tok_stride + h*gate_head_stride] (defaults H, 1).
+ *          Ignored (may be NULL) for GATTN_GATE_NONE.
+ * qnorm_w, knorm_w  [d] RMSNorm weights, shared by all heads.
+ * pos      [B,S] int32 RoPE positions, or NULL for positions 0..S-1.  The mask
+ *          always uses the token index, not pos.
+ * B,S,H,G,d  batch, tokens per sequence, query heads, KV heads, head_dim.
+ *          Requires H % G == 0, S >= 1.  d in {64,128,256} for GATTN_BF16 and
+ *          d in {32,64,128,256} for GATTN_FP32 (others: GATTN_ERR_UNSUPPORTED).
+ * rotary_dim  even, 0 <= rotary_dim <= d.  rope_base > 0.  eps >= 0.
+ * workspace  device buffer of at least gattn_prefill_workspace_size() bytes,
+ *          256-byte aligned.
+ * out      [B,S,H*d] contiguous; head h occupies columns h*d .. h*d+d-1.
+ * Alignment: q, k, v, gate, out and the workspace must be 16-byte aligned, and
+ *          the q/gate strides multiples of 8 elements (bf16) / 4 (fp32), except
+ *          headwise gate strides which may be anything.
+ */
+gattn_status gattn_prefill(const void* q, const void* k, const void* v, const void* gate, const void* qnorm_w,
+                           const void* knorm_w, const int32_t* pos, int B, int S, int H, int G, int d,
+                           int rotary_dim, double rope_base, float eps, int gate_mode, int64_t q_tok_stride,
+                           int64_t q_head_stride, int64_t gate_tok_stride, int64_t gate_head_stride, int dtype,
+                           void* workspace, size_t workspace_bytes, void* out, void* stream);
+
+/*
+ * Bytes of workspace gattn_decode needs (per-split partial softmax states).
+ * Depends on the current device's SM count.  Returns 0 for invalid sizes.
+ */
+size_t gattn_decode_workspace_size(int B, int H, int G, int d, int Lmax);
+
+/*
+ * One decode step: each sequence's newest query attends to its cached keys.
+ * (KV cache: "Multi-head attention and GQA" chapter, section "拼接各头 → 用 W_O
+ * 投影": K and V are cached per token, Q is not; the new query dots every cached
+ * key and mixes every cached value.)
+ *
+ * q_new    [B,H,d] raw query projections of the newest token (not yet normed or
+ *          rotated); it sits at position seqlens[b]-1.
+ * kv_cache [2,B,G,Lmax,d] contiguous: plane 0 holds K already normed and rotated
+ *          (as the prefill path computes it), plane 1 holds raw V.  Only tokens
+ *          0..seqlens[b]-1 are read; entries beyond may hold anything.
+ * seqlens  [B] int32 device array, cached tokens per sequence INCLUDING the new
+ *          one, each in [1, Lmax].  A value outside that range sets
+ *          GATTN_DEVICE_BAD_SEQLEN and leaves that sequence's output unwritten.
+ * gate     [B,H,d] (elementwise) or [B,H] (headwise) logits; NULL for none.
+ * qnorm_w  [d].  d in {64,128,256}; H/G <= 8; only GATTN_BF16 (implied).
+ * workspace  >= gattn_decode_workspace_size() bytes, 256-byte aligned.
+ * out      [B,H*d] bf16.
+ */
+gattn_status gattn_decode(const void* q_new, const void* kv_cache, const int32_t* seqlens, const void* gate,
+                          const void* qnorm_w, int B, int H, int G, int d, int Lmax, int rotary_dim,
+                          double rope_base, float eps, int gate_mode, void* workspace, size_t workspace_bytes,
+                          void* out, void* stream);
+
+/*
+ * Read (synchronously on `stream`) and clear the device status word.  Writes the
+ * GATTN_DEVICE_* bits seen since the last call to *bits (may be NULL) and returns
+ * GATTN_ERR_DEVICE if any bit was set, GATTN_OK otherwise.
+ */
+gattn_status gattn_get_device_status(unsigned int* bits, void* stream);
+
+/*
+ * Profiling hook.  When both events are non-NULL (cudaEvent_t passed as void*),
+ * every later gattn_prefill / gattn_decode records `start` on its stream just
+ * before its main attention kernel and `stop` just after it, so a caller can
+ * time that kernel alone.  Pass NULL, NULL to switch it off.  Not thread-safe.
+ */
+void gattn_set_profile_events(void* start, void* stop);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GATTN_H */

@@ -206,25 +206,34 @@ void oracle_prefill(const double* q, const double* k, const double* v, const dou
 }
 
 /* Prefill restricted to selected query rows: row i is (row_b[i], row_t[i]); all
- * heads of that token are computed and written to out[i, H*d].  Keys 0..t of
- * the row's batch are normed and rotated as in oracle_prefill. */
+ * heads of that token are computed and written to out[i, H*d].  The keys of each
+ * (batch, group) are normed and rotated once, exactly as in oracle_prefill. */
 void oracle_prefill_rows(const double* q, const double* k, const double* v, const double* gate,
                          const double* qnorm_w, const double* knorm_w, const double* pos, int B, int S, int H,
                          int G, int d, int rd, double base, double eps, int gate_mode, const int32_t* row_b,
                          const int32_t* row_t, int n_rows, double* out) {
     int r = H / G;
-    (void)B;
+    double* kr_all = (double*)malloc(sizeof(double) * (size_t)B * G * S * d);
+#pragma omp parallel for collapse(2) schedule(dynamic)
+    for (int b = 0; b < B; ++b) {
+        for (int g = 0; g < G; ++g) {
+            double* tmp = (double*)malloc(sizeof(double) * (size_t)d);
+            const double* posb = pos ? pos + (int64_t)b * S : NULL;
+            prologue_head(k + (int64_t)b * S * G * d, knorm_w, posb, S, G, g, d, rd, base, eps,
+                          kr_all + ((int64_t)b * G + g) * S * d, tmp);
+            free(tmp);
+        }
+    }
 #pragma omp parallel for collapse(2) schedule(dynamic)
     for (int i = 0; i < n_rows; ++i) {
         for (int h = 0; h < H; ++h) {
             int b = row_b[i], t = row_t[i], g = h / r;
             const double* posb = pos ? pos + (int64_t)b * S : NULL;
-            double* kr = (double*)malloc(sizeof(double) * (size_t)(t + 1) * d);
+            const double* kr = kr_all + ((int64_t)b * G + g) * S * d;
             double* qr = (double*)malloc(sizeof(double) * (size_t)d);
             double* tmp = (double*)malloc(sizeof(double) * (size_t)d);
             double* o = (double*)malloc(sizeof(double) * (size_t)d);
             double* scratch = (double*)malloc(sizeof(double) * (size_t)(t + 1));
-            prologue_head(k + (int64_t)b * S * G * d, knorm_w, posb, t + 1, G, g, d, rd, base, eps, kr, tmp);
             oracle_rmsnorm(q + (((int64_t)b * S + t) * H + h) * d, qnorm_w, 1, d, eps, tmp);
             rope_row(tmp, posb ? posb[t] : (double)t, d, rd, base, qr);
             const double* vb = v + ((int64_t)b * S * G + g) * d;
@@ -234,9 +243,10 @@ void oracle_prefill_rows(const double* q, const double* k, const double* v, cons
             else if (gate_mode == ORACLE_GATE_HEADWISE)
                 apply_gate(o, gate + ((int64_t)b * S + t) * H + h, d, gate_mode);
             memcpy(out + (int64_t)i * H * d + (int64_t)h * d, o, sizeof(double) * (size_t)d);
-            free(kr); free(qr); free(tmp); free(o); free(scratch);
+            free(qr); free(tmp); free(o); free(scratch);
         }
     }
+    free(kr_all);
 }
 
 /* Decode step against a KV cache.

@@ -1,0 +1,126 @@
+"""C ABI checks that need no GPU: the library loads, exports every entry point
+include/gattn.h declares, and rejects bad arguments on the host before any
+CUDA call (so fake, never-dereferenced pointer values are safe here)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import __graft_entry__
+from gated_softmax_attention_gqa_gb300 import _lib
+from gated_softmax_attention_gqa_gb300.workloads import prefill_flops
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+OK, INVALID, UNSUPPORTED, CUDA, WORKSPACE, DEVICE = range(6)
+FAKE = 0x7F0000000000  # 256-byte aligned, never dereferenced by argument checks
+
+
+@pytest.fixture(scope="module")
+def lib():
+    __graft_entry__.build_library()
+    return _lib.load()
+
+
+def declared_symbols():
+    text = open(os.path.join(ROOT, "include", "gattn.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(gattn_[a-z_]+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_symbols()
+    assert set(names) == set(_lib.EXPORTS), names
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_strerror_covers_every_status(lib):
+    for s in range(6):
+        assert lib.gattn_strerror(s).decode().startswith("GATTN_")
+    assert b"unknown" in lib.gattn_strerror(99)
+
+
+def P(off=0):
+    return ctypes.c_void_p(FAKE + off)
+
+
+def prefill(lib, **kw):
+    a = dict(q=P(), k=P(), v=P(), gate=P(), qw=P(), kw=P(), pos=None, B=1, S=16, H=8, G=2, d=128, rd=64,
+             base=1e6, eps=1e-6, gm=1, qts=0, qhs=0, gts=0, ghs=0, dt=0, ws=P(), wsb=1 << 40, out=P(1 << 20))
+    a.update(kw)
+    return lib.gattn_prefill(a["q"], a["k"], a["v"], a["gate"], a["qw"], a["kw"], a["pos"], a["B"], a["S"], a["H"],
+                             a["G"], a["d"], a["rd"], a["base"], a["eps"], a["gm"], a["qts"], a["qhs"], a["gts"],
+                             a["ghs"], a["dt"], a["ws"], a["wsb"], a["out"], None)
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(q=None), INVALID),
+    (dict(out=None), INVALID),
+    (dict(gate=None), INVALID),
+    (dict(H=6, G=4), INVALID),           # H % G != 0
+    (dict(S=0), INVALID),
+    (dict(B=0), INVALID),
+    (dict(rd=63), INVALID),              # odd rotary_dim
+    (dict(rd=130), INVALID),             # rotary_dim > d
+    (dict(base=-1.0), INVALID),
+    (dict(eps=float("nan")), INVALID),
+    (dict(gm=3), INVALID),
+    (dict(dt=7), INVALID),
+    (dict(d=96), UNSUPPORTED),           # no bf16 kernel for head_dim 96
+    (dict(d=32, rd=16), UNSUPPORTED),    # bf16 needs d >= 64
+    (dict(rd=24), UNSUPPORTED),          # bf16 needs rotary_dim % 16 == 0
+    (dict(q=P(2)), INVALID),             # misaligned q
+    (dict(qts=1028), INVALID),           # token stride not a multiple of 8 elements
+    (dict(ws=None), WORKSPACE),
+    (dict(ws=P(16)), WORKSPACE),         # workspace not 256-byte aligned
+    (dict(wsb=1024), WORKSPACE),         # workspace too small
+])
+def test_prefill_rejects_bad_arguments(lib, kw, expect):
+    assert prefill(lib, **kw) == expect
+
+
+def test_fp32_accepts_other_shapes_only_where_supported(lib):
+    assert prefill(lib, dt=1, d=96) == UNSUPPORTED
+    assert prefill(lib, dt=1, d=32, rd=8, wsb=16) == WORKSPACE  # d=32 and rd=8 are fine in fp32
+
+
+def decode(lib, **kw):
+    a = dict(q=P(), kv=P(), sl=P(), gate=P(), qw=P(), B=4, H=8, G=2, d=256, L=1024, rd=64, base=1e7, eps=1e-6, gm=1,
+             ws=P(), wsb=1 << 40, out=P(1 << 20))
+    a.update(kw)
+    return lib.gattn_decode(a["q"], a["kv"], a["sl"], a["gate"], a["qw"], a["B"], a["H"], a["G"], a["d"], a["L"],
+                            a["rd"], a["base"], a["eps"], a["gm"], a["ws"], a["wsb"], a["out"], None)
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(kv=None), INVALID),
+    (dict(sl=None), INVALID),
+    (dict(H=8, G=3), INVALID),
+    (dict(L=0), INVALID),
+    (dict(rd=7), INVALID),
+    (dict(d=96), UNSUPPORTED),
+    (dict(H=32, G=2), UNSUPPORTED),      # more than 8 query heads per group
+    (dict(B=100000), UNSUPPORTED),
+    (dict(rd=40), UNSUPPORTED),
+    (dict(kv=P(8)), INVALID),            # cache must be 16-byte aligned for TMA
+])
+def test_decode_rejects_bad_arguments(lib, kw, expect):
+    assert decode(lib, **kw) == expect
+
+
+def test_prefill_workspace_sizes(lib):
+    assert lib.gattn_prefill_workspace_size(1, 4096, 8, 2, 256, 0) == 4096 * 2 * 256 * 2
+    assert lib.gattn_prefill_workspace_size(1, 64, 2, 1, 32, 1) == (64 * 2 * 32 + 64 * 32) * 4
+    assert lib.gattn_prefill_workspace_size(0, 64, 2, 1, 32, 1) == 0
+
+
+def test_flop_accounting_matches_the_causal_triangle():
+    # c2, c3, c4 algorithmic FLOPs (QK^T and PV over the causal triangle incl. the diagonal)
+    assert prefill_flops(1, 4096, 8, 256) == 68_736_253_952
+    assert prefill_flops(8, 2048, 16, 128) == 137_506_062_336
+    assert prefill_flops(2, 8192, 32, 128) == 1_099_645_845_504
+    # brute force on a tiny case: count multiply-adds of both contractions
+    B, S, H, d = 2, 5, 3, 4
+    madds = sum(2 * d for b in range(B) for h in range(H) for t in range(S) for j in range(t + 1))
+    assert prefill_flops(B, S, H, d) == 2 * madds

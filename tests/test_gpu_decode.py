@@ -1,0 +1,129 @@
+"""GPU decode parity: split-KV decode (through the C ABI) against the fp64 oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gated_softmax_attention_gqa_gb300 import gattn_decode, gattn_get_device_status, gattn_prefill
+from gated_softmax_attention_gqa_gb300.workloads import WORKLOADS, Workload, make_decode_inputs, make_prefill_inputs
+from tests.parity import assert_close_to_oracle
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+BAD_SEQLEN = 0x1
+
+
+def dec_workload(B, H, G, d, rd, base, gate_mode, Lmax, lo, hi, seed):
+    return Workload("dec", "decode", B=B, H=H, G=G, d=d, rotary_dim=rd, rope_base=base, gate_mode=gate_mode,
+                    dtype="bf16", seed=seed, Lmax=Lmax, seqlen_range=(lo, hi))
+
+
+def run_gpu(inp, w, out=None):
+    dev = {k: v.to(DEV) for k, v in inp.items()}
+    return gattn_decode(dev["q_new"], dev["kv_cache"], dev["seqlens"],
+                        dev["gate"] if w.gate_mode != "none" else None, dev["qnorm_w"], rotary_dim=w.rotary_dim,
+                        rope_base=w.rope_base, eps=w.eps, gate_mode=w.gate_mode, out=out)
+
+
+def run_oracle(inp, w, rows=None):
+    idx = slice(None) if rows is None else rows
+    cache = inp["kv_cache"]
+    sl = inp["seqlens"][idx]
+    lmax = int(sl.max())
+    return oracle.decode(inp["q_new"][idx], cache[0][idx][:, :, :lmax], cache[1][idx][:, :, :lmax], sl,
+                         inp["gate"][idx], inp["qnorm_w"], w.rotary_dim, w.rope_base, w.eps, w.gate_mode)
+
+
+SHAPES = [
+    # B, H, G, d, rd, base, gate, Lmax, lo, hi
+    (3, 8, 2, 256, 64, 1e7, "elementwise", 300, 1, 300),
+    (5, 16, 8, 128, 128, 1e6, "headwise", 700, 1, 700),
+    (4, 32, 4, 128, 64, 1e6, "elementwise", 1000, 500, 1000),
+    (2, 4, 4, 64, 32, 1e4, "none", 129, 63, 129),
+    (7, 8, 1, 128, 16, 1e4, "elementwise", 2048, 1, 2048),
+]
+
+
+@pytest.mark.parametrize("shape", SHAPES, ids=[str(s) for s in SHAPES])
+def test_decode_parity_small(shape):
+    B, H, G, d, rd, base, gm, Lmax, lo, hi = shape
+    w = dec_workload(B, H, G, d, rd, base, gm, Lmax, lo, hi, seed=B * 100 + d)
+    inp = make_decode_inputs(w)
+    out = run_gpu(inp, w)
+    torch.cuda.synchronize()
+    assert gattn_get_device_status() == 0
+    assert_close_to_oracle(out, run_oracle(inp, w), torch.bfloat16, str(shape))
+
+
+def test_decode_ignores_cache_entries_past_each_sequence():
+    """Tokens at or after seqlens[b] may hold anything, NaN included."""
+    w = dec_workload(4, 8, 2, 256, 64, 1e7, "elementwise", 512, 1, 500, seed=21)
+    inp = make_decode_inputs(w)
+    poisoned = inp["kv_cache"].clone()
+    for b, L in enumerate(inp["seqlens"].tolist()):
+        poisoned[:, b, :, L:] = float("nan")
+    out = run_gpu(dict(inp, kv_cache=poisoned), w)
+    torch.cuda.synchronize()
+    assert_close_to_oracle(out, run_oracle(inp, w), torch.bfloat16, "poisoned tail")
+
+
+def test_decode_full_size_sampled_sequences():
+    """The benchmark's decode workload at full size (64 sequences, 16k-32k cached
+    tokens); the oracle checks six seeded sequences in full, all heads."""
+    w = WORKLOADS["qwen35_08b_decode"]
+    inp = make_decode_inputs(w)
+    out = run_gpu(inp, w)
+    torch.cuda.synchronize()
+    assert gattn_get_device_status() == 0
+    rows = np.sort(np.random.default_rng(w.seed).choice(w.B, size=6, replace=False))
+    ref = run_oracle(inp, w, rows=torch.from_numpy(rows).long())
+    assert_close_to_oracle(out[torch.from_numpy(rows).long()], ref, torch.bfloat16, "decode full size")
+    assert torch.isfinite(out).all()
+
+
+def test_decode_equals_last_prefill_row():
+    """Decode with a cache holding the normed, rotated keys of a prefix equals row
+    L-1 of prefill over that prefix (both computed on the GPU)."""
+    H, G, d, rd, base, eps = 8, 2, 256, 64, 1e7, 1e-6
+    wp = Workload("p", "prefill", B=1, S=700, H=H, G=G, d=d, rotary_dim=rd, rope_base=base,
+                  gate_mode="elementwise", dtype="bf16", seed=31)
+    inp = make_prefill_inputs(wp)
+    dev = {k: v.to(DEV) for k, v in inp.items()}
+    full = gattn_prefill(dev["q"], dev["k"], dev["v"], dev["gate"], dev["qnorm_w"], dev["knorm_w"], rotary_dim=rd,
+                         rope_base=base, eps=eps, gate_mode="elementwise").view(1, wp.S, H * d)
+    lens = [1, 128, 129, 700]
+    Lmax = 704
+    kn = oracle.rmsnorm(inp["k"][0], inp["knorm_w"], eps)
+    kr = oracle.rope(kn, np.arange(wp.S)[:, None], rd, base)  # [S,G,d]
+    cache = torch.zeros((2, len(lens), G, Lmax, d), dtype=torch.bfloat16)
+    for i, L in enumerate(lens):
+        cache[0, i, :, :L] = torch.from_numpy(kr[:L]).permute(1, 0, 2).to(torch.bfloat16)
+        cache[1, i, :, :L] = inp["v"][0, :L].permute(1, 0, 2)
+    q_new = torch.stack([inp["q"][0, L - 1] for L in lens])
+    gate = torch.stack([inp["gate"][0, L - 1] for L in lens])
+    out = gattn_decode(q_new.to(DEV), cache.to(DEV), torch.tensor(lens, dtype=torch.int32, device=DEV),
+                       gate.to(DEV), dev["qnorm_w"], rotary_dim=rd, rope_base=base, eps=eps)
+    torch.cuda.synchronize()
+    for i, L in enumerate(lens):
+        diff = (out[i].double() - full[0, L - 1].double()).abs()
+        assert diff.max().item() <= 2e-2 and diff.mean().item() <= 2e-3, (L, diff.max().item())
+
+
+def test_bad_seqlen_is_reported_and_skipped():
+    w = dec_workload(4, 8, 2, 128, 64, 1e6, "elementwise", 256, 10, 256, seed=41)
+    inp = make_decode_inputs(w)
+    sl = inp["seqlens"].clone()
+    sl[1] = 0
+    sl[2] = 257  # beyond Lmax
+    bad = dict(inp, seqlens=sl)
+    out = torch.full((4, 8 * 128), 3.0, dtype=torch.bfloat16, device=DEV)
+    gattn_get_device_status()
+    run_gpu(bad, w, out=out)
+    torch.cuda.synchronize()
+    assert gattn_get_device_status() & BAD_SEQLEN
+    assert (out[1] == 3.0).all() and (out[2] == 3.0).all()
+    good = torch.tensor([0, 3])
+    ref = run_oracle(inp, w, rows=good)
+    assert_close_to_oracle(out[good], ref, torch.bfloat16, "good rows next to bad ones")
+    assert gattn_get_device_status() == 0

@@ -1,0 +1,167 @@
+"""GPU prefill parity: the CUDA path (through the C ABI) against the fp64 oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gated_softmax_attention_gqa_gb300 import gattn_get_device_status, gattn_prefill, workloads
+from gated_softmax_attention_gqa_gb300.workloads import WORKLOADS, Workload, make_prefill_inputs
+from tests.parity import assert_close_to_oracle, sample_rows
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+
+
+def run_gpu(inp, w, pos=None, out=None):
+    dev = {k: v.to(DEV) for k, v in inp.items()}
+    return gattn_prefill(dev["q"], dev["k"], dev["v"], dev["gate"] if w.gate_mode != "none" else None,
+                         dev["qnorm_w"], dev["knorm_w"], None if pos is None else pos.to(DEV),
+                         rotary_dim=w.rotary_dim, rope_base=w.rope_base, eps=w.eps, gate_mode=w.gate_mode, out=out)
+
+
+def run_oracle(inp, w, pos=None):
+    return oracle.prefill(inp["q"], inp["k"], inp["v"], inp["gate"], inp["qnorm_w"], inp["knorm_w"],
+                          None if pos is None else pos.double(), w.rotary_dim, w.rope_base, w.eps, w.gate_mode)
+
+
+def small(name, B, S, H, G, d, rd, base, gate_mode, dtype="bf16", seed=11, gate_std=1.0):
+    return Workload(name, "prefill", B=B, S=S, H=H, G=G, d=d, rotary_dim=rd, rope_base=base, gate_mode=gate_mode,
+                    dtype=dtype, seed=seed, gate_std=gate_std)
+
+
+def test_tiny_fp32_workload_full():
+    w = WORKLOADS["tiny_fp32"]
+    inp = make_prefill_inputs(w)
+    out = run_gpu(inp, w)
+    torch.cuda.synchronize()
+    ref = run_oracle(inp, w)
+    assert_close_to_oracle(out, ref, torch.float32, "tiny fp32")
+    assert gattn_get_device_status() == 0
+
+
+@pytest.mark.parametrize("shape", [
+    (1, 1, 2, 1, 32, 8, 1e4, "elementwise"),
+    (2, 37, 4, 2, 64, 6, 1e4, "headwise"),
+    (1, 130, 2, 2, 128, 128, 1e6, "none"),
+    (1, 77, 4, 1, 256, 64, 1e7, "elementwise"),
+])
+def test_fp32_variants(shape):
+    B, S, H, G, d, rd, base, gm = shape
+    w = small("f32", B, S, H, G, d, rd, base, gm, dtype="fp32", seed=S)
+    inp = make_prefill_inputs(w)
+    out = run_gpu(inp, w)
+    torch.cuda.synchronize()
+    assert_close_to_oracle(out, run_oracle(inp, w), torch.float32, str(shape))
+
+
+BF16_SHAPES = [
+    # B, S, H, G, d, rd, base, gate
+    (1, 1, 2, 1, 128, 64, 1e4, "elementwise"),      # single token
+    (1, 17, 4, 2, 64, 32, 1e4, "headwise"),         # shorter than one tile
+    (2, 129, 8, 2, 256, 64, 1e7, "elementwise"),    # ragged tail, two query tiles, d=256
+    (1, 300, 4, 4, 128, 128, 1e6, "headwise"),      # G = H (MHA), full rotary
+    (1, 384, 8, 1, 128, 64, 1e6, "none"),           # MQA, no gate, exact tile multiple
+    (2, 255, 16, 8, 128, 128, 1e6, "headwise"),     # Qwen3-0.6B head layout
+    (1, 513, 4, 1, 256, 64, 1e7, "elementwise"),    # d=256 with 64-key tiles, ragged
+    (1, 640, 32, 4, 128, 64, 1e6, "elementwise"),   # paper MoE head layout
+    (1, 200, 2, 1, 64, 0, 1e4, "elementwise"),      # no rotary features
+    (1, 256, 2, 1, 128, 16, 1e4, "elementwise"),    # small rotary block
+]
+
+
+@pytest.mark.parametrize("shape", BF16_SHAPES, ids=[str(s) for s in BF16_SHAPES])
+def test_bf16_parity_small(shape):
+    B, S, H, G, d, rd, base, gm = shape
+    w = small("bf16", B, S, H, G, d, rd, base, gm, seed=S + d)
+    inp = make_prefill_inputs(w)
+    out = run_gpu(inp, w)
+    torch.cuda.synchronize()
+    assert_close_to_oracle(out, run_oracle(inp, w), torch.bfloat16, str(shape))
+    assert gattn_get_device_status() == 0
+
+
+def test_bf16_packed_qproj_layout_and_positions():
+    """q and the gate as the two halves of the packed q_proj output [B,S,H,2d]
+    (the handbook's interleaved layout), with explicit RoPE positions."""
+    B, S, H, G, d = 2, 200, 8, 2, 128
+    w = small("packed", B, S, H, G, d, 64, 1e6, "elementwise", seed=5)
+    inp = make_prefill_inputs(w)
+    packed = torch.cat([inp["q"], inp["gate"]], dim=-1)  # [B,S,H,2d]
+    pos = (torch.arange(S, dtype=torch.int32)[None] * 3 + torch.tensor([[0], [1000]], dtype=torch.int32))
+    dev = packed.to(DEV)
+    out = gattn_prefill(dev[..., :d], inp["k"].to(DEV), inp["v"].to(DEV), dev[..., d:], inp["qnorm_w"].to(DEV),
+                        inp["knorm_w"].to(DEV), pos.to(DEV), rotary_dim=64, rope_base=1e6, gate_mode="elementwise")
+    torch.cuda.synchronize()
+    ref = run_oracle(inp, w, pos)
+    assert_close_to_oracle(out, ref, torch.bfloat16, "packed q_proj")
+
+
+@pytest.mark.parametrize("name", ["qwen35_08b_prefill", "qwen3_06b_prefill", "paper_moe_prefill"])
+def test_bf16_full_size_sampled_rows(name):
+    """The benchmark's workloads at full size; the oracle checks a seeded sample of
+    query rows (first/last 64, both sides of every tile boundary, 256 random) for
+    every batch and head."""
+    w = WORKLOADS[name]
+    inp = make_prefill_inputs(w)
+    out = run_gpu(inp, w)
+    torch.cuda.synchronize()
+    assert gattn_get_device_status() == 0
+    rb, rt = sample_rows(w.S, w.B, seed=w.seed)
+    ref = oracle.prefill_rows(inp["q"], inp["k"], inp["v"], inp["gate"], inp["qnorm_w"], inp["knorm_w"], None,
+                              w.rotary_dim, w.rope_base, w.eps, w.gate_mode, rb, rt)
+    got = out.view(w.B, w.S, -1)[torch.from_numpy(rb).long(), torch.from_numpy(rt).long()]
+    assert_close_to_oracle(got, ref, torch.bfloat16, name)
+    assert torch.isfinite(out).all()
+
+
+def test_every_output_written_and_guard_band_untouched():
+    B, S, H, G, d = 1, 333, 4, 2, 128
+    w = small("guard", B, S, H, G, d, 64, 1e6, "elementwise", seed=9)
+    inp = make_prefill_inputs(w)
+    n = B * S * H * d
+    buf = torch.full((n + 4096,), float("nan"), dtype=torch.bfloat16, device=DEV)
+    buf[n:] = 7.0
+    out = buf[:n].view(B, S, H * d)
+    run_gpu(inp, w, out=out)
+    torch.cuda.synchronize()
+    assert torch.isfinite(out).all(), "some output element was never written"
+    assert (buf[n:] == 7.0).all(), "kernel wrote past the end of the output"
+
+
+def test_headwise_gate_equals_broadcast_elementwise():
+    B, S, H, G, d = 1, 260, 8, 2, 128
+    w = small("hw", B, S, H, G, d, 64, 1e6, "headwise", seed=4)
+    inp = make_prefill_inputs(w)
+    a = run_gpu(inp, w)
+    we = small("ew", B, S, H, G, d, 64, 1e6, "elementwise", seed=4)
+    inp_e = dict(inp, gate=inp["gate"][..., None].expand(B, S, H, d).contiguous())
+    b = run_gpu(inp_e, we)
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
+
+
+def test_zero_gate_logits_halve_the_ungated_output():
+    """sigmoid(0) = 1/2 exactly, and halving commutes with bf16 rounding."""
+    B, S, H, G, d = 1, 190, 4, 1, 256
+    w = small("z", B, S, H, G, d, 64, 1e7, "elementwise", seed=3)
+    inp = make_prefill_inputs(w)
+    plain = run_gpu(inp, small("n", B, S, H, G, d, 64, 1e7, "none"))
+    half = run_gpu(dict(inp, gate=torch.zeros_like(inp["gate"])), w)
+    torch.cuda.synchronize()
+    assert torch.equal(half, plain * 0.5)
+
+
+def test_gqa_equals_mha_with_replicated_kv():
+    """Head h reads group floor(h/(H/G)): replicating each group's K and V to its
+    H/G heads and running with G = H gives the same output."""
+    B, S, H, G, d = 1, 150, 8, 2, 128
+    w = small("gqa", B, S, H, G, d, 64, 1e6, "elementwise", seed=8)
+    inp = make_prefill_inputs(w)
+    a = run_gpu(inp, w)
+    rep = H // G
+    inp_m = dict(inp, k=inp["k"].repeat_interleave(rep, dim=2).contiguous(),
+                 v=inp["v"].repeat_interleave(rep, dim=2).contiguous())
+    b = run_gpu(inp_m, small("mha", B, S, H, H, d, 64, 1e6, "elementwise"))
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
