@@ -20,6 +20,7 @@ Under torchrun (N > 1) every rank runs the same workload on its own GPU (replica
 the path has no exchange step); times are maxed over ranks.
 """
 import argparse
+import dataclasses
 import hashlib
 import json
 import os
@@ -45,6 +46,10 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--prefill", default=PREFILL, help="prefill workload name (parity/tuning runs)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only", choices=["prefill", "decode"], default=None,
+                    help="run one half of the path only (profiling runs; not a bench line)")
+    ap.add_argument("--decode-batch", type=int, default=None,
+                    help="override the decode batch (smaller profiling case; not a bench line)")
     ap.add_argument("--cpu-budget-s", type=float, default=12.0)
     return ap.parse_args()
 
@@ -136,29 +141,35 @@ class ClockSampler:
 
 def cpu_baseline(w, inputs, budget_s):
     """The fp64 oracle, as it stands, on a bounded sample of the prefill workload:
-    all heads of a seeded set of query rows; TFLOP/s over the causal FLOPs of
-    those rows.  Grows the sample until it takes about budget_s seconds."""
+    all heads of a seeded set of query rows (the whole workload when that fits the
+    budget); TFLOP/s over the causal FLOPs of the rows computed."""
     import numpy as np
 
     import oracle
-    from gated_softmax_attention_gqa_gb300.workloads import prefill_flops  # noqa: F401
+    from gated_softmax_attention_gqa_gb300.workloads import prefill_flops
 
     rng = np.random.default_rng(1234)
     n = 16
     while True:
-        rt = np.sort(rng.integers(0, w.S, size=n)).astype(np.int32)
-        rb = np.zeros(n, dtype=np.int32)
+        full = n >= w.B * w.S
+        if full:
+            rb = np.repeat(np.arange(w.B, dtype=np.int32), w.S)
+            rt = np.tile(np.arange(w.S, dtype=np.int32), w.B)
+        else:
+            rt = np.sort(rng.choice(w.S, size=n, replace=False)).astype(np.int32)
+            rb = rng.integers(0, w.B, size=n).astype(np.int32)
         t0 = time.perf_counter()
         oracle.prefill_rows(inputs["q"], inputs["k"], inputs["v"], inputs["gate"], inputs["qnorm_w"],
                             inputs["knorm_w"], None, w.rotary_dim, w.rope_base, w.eps, w.gate_mode, rb, rt)
         dt = time.perf_counter() - t0
-        flops = sum(4 * w.H * w.d * (int(t) + 1) for t in rt)
-        if dt >= budget_s * 0.5 or n >= 4096:
+        flops = prefill_flops(w.B, w.S, w.H, w.d) if full else sum(4 * w.H * w.d * (int(t) + 1) for t in rt)
+        if dt >= budget_s * 0.5 or full:
+            what = "every query row" if full else f"{n} seeded query rows"
             return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": oracle.threads_used(), "kind": "oracle",
-                    "sample": f"{n} seeded query rows x all {w.H} heads of {w.name} (B{w.B} S{w.S} H{w.H} G{w.G} "
-                              f"d{w.d}); fp64 C loops, OpenMP; {dt:.1f} s",
+                    "sample": f"{what} x all {w.H} heads of {w.name} (B{w.B} S{w.S} H{w.H} G{w.G} d{w.d}); "
+                              f"fp64 C loops, OpenMP; {dt:.1f} s",
                     "seconds": dt}
-        n = min(4096, int(n * max(2.0, budget_s / max(dt, 1e-3))))
+        n = min(w.B * w.S, int(n * max(2.0, budget_s / max(dt, 1e-3))))
 
 
 def run_reference(args):
@@ -214,12 +225,15 @@ def main():
     stream = torch.cuda.current_stream(dev)
     hbm_peak, bf16_peak, peak_kind = peaks()
 
+    do_p, do_d = args.only in (None, "prefill"), args.only in (None, "decode")
     wp, wd = WORKLOADS[args.prefill], WORKLOADS[DECODE]
+    if args.decode_batch:
+        wd = dataclasses.replace(wd, B=args.decode_batch)
     pin = make_prefill_inputs(wp)
-    p_dev = {k: v.to(dev) for k, v in pin.items()}
-    din = make_decode_inputs(wd)
-    d_dev = {k: v.to(dev) for k, v in din.items()}
-    seqlens = din["seqlens"].tolist()
+    p_dev = {k: v.to(dev) for k, v in pin.items()} if do_p else {}
+    din = make_decode_inputs(wd) if do_d else None
+    d_dev = {k: v.to(dev) for k, v in din.items()} if do_d else {}
+    seqlens = din["seqlens"].tolist() if do_d else [1]
     p_out = torch.empty((wp.B, wp.S, wp.H * wp.d), dtype=torch.bfloat16, device=dev)
     p_ws = torch.empty(ga.gattn_prefill_workspace_size(wp.B, wp.S, wp.H, wp.G, wp.d), dtype=torch.uint8, device=dev)
     d_out = torch.empty((wd.B, wd.H * wd.d), dtype=torch.bfloat16, device=dev)
@@ -228,11 +242,15 @@ def main():
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
 
     def prefill():
+        if not do_p:
+            return
         ga.gattn_prefill(p_dev["q"], p_dev["k"], p_dev["v"], p_dev["gate"], p_dev["qnorm_w"], p_dev["knorm_w"],
                          rotary_dim=wp.rotary_dim, rope_base=wp.rope_base, eps=wp.eps, gate_mode=wp.gate_mode,
                          out=p_out, workspace=p_ws)
 
     def decode():
+        if not do_d:
+            return
         ga.gattn_decode(d_dev["q_new"], d_dev["kv_cache"], d_dev["seqlens"], d_dev["gate"], d_dev["qnorm_w"],
                         rotary_dim=wd.rotary_dim, rope_base=wd.rope_base, eps=wd.eps, gate_mode=wd.gate_mode,
                         out=d_out, workspace=d_ws)
@@ -251,6 +269,10 @@ def main():
 
     K = args.steps
     evs = {k: [(ev(), ev()) for _ in range(K)] for k in ("p", "pk", "d", "dk")}
+    for pairs in evs.values():  # create every event before the timed region
+        for a, b in pairs:
+            a.record(stream)
+            b.record(stream)
     sampler = ClockSampler(dev.index)
     time.sleep(0.1)
     if world > 1:
@@ -278,7 +300,7 @@ def main():
     def ms(key):
         return [a.elapsed_time(b) for a, b in evs[key]]
 
-    t = {k: statistics.mean(ms(k)) for k in evs}
+    t = {k: statistics.mean(ms(k)) if (do_p if k[0] == "p" else do_d) else float("nan") for k in evs}
     if world > 1:
         vec = torch.tensor([t["p"], t["pk"], t["d"], t["dk"]], dtype=torch.float64, device=dev)
         dist.all_reduce(vec, op=dist.ReduceOp.MAX)
@@ -287,10 +309,10 @@ def main():
 
     flops = prefill_flops(wp.B, wp.S, wp.H, wp.d)
     dbytes = decode_io_bytes(seqlens, wd.H, wd.G, wd.d, wd.gate_mode)
-    value = world * flops / (t["p"] * 1e-3) / 1e12
-    kern_tflops = flops / (t["pk"] * 1e-3) / 1e12
-    dec_gbs = world * dbytes / (t["d"] * 1e-3) / 1e9
-    dec_kern_gbs = dbytes / (t["dk"] * 1e-3) / 1e9
+    value = world * flops / (t["p"] * 1e-3) / 1e12 if do_p else float("nan")
+    kern_tflops = flops / (t["pk"] * 1e-3) / 1e12 if do_p else float("nan")
+    dec_gbs = world * dbytes / (t["d"] * 1e-3) / 1e9 if do_d else float("nan")
+    dec_kern_gbs = dbytes / (t["dk"] * 1e-3) / 1e9 if do_d else float("nan")
 
     # ---- end to end through the public API: pinned host -> device, prefill, device -> host
     host_in = {k: v.pin_memory() for k, v in pin.items()}
@@ -307,12 +329,12 @@ def main():
                          gate_mode=wp.gate_mode, out=p_out, workspace=p_ws)
         host_out.copy_(p_out, non_blocking=True)
 
-    for _ in range(3):
+    for _ in range(3 if do_p else 0):
         e2e_step()
     torch.cuda.synchronize()
     e0, e1 = ev(), ev()
     e0.record(stream)
-    for _ in range(K):
+    for _ in range(K if do_p else 0):
         e2e_step()
     e1.record(stream)
     torch.cuda.synchronize()
@@ -321,7 +343,7 @@ def main():
         vec = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
         dist.all_reduce(vec, op=dist.ReduceOp.MAX)
         e2e_ms = vec.item()
-    e2e_val = world * flops / (e2e_ms * 1e-3) / 1e12
+    e2e_val = world * flops / (e2e_ms * 1e-3) / 1e12 if do_p and e2e_ms > 0 else float("nan")
 
     if rank == 0:
         tc_src = ["prefill_tc.cu", "common.cuh", "internal.h"]
@@ -354,7 +376,11 @@ def main():
             "clocks": clocks,
             "device_status": status,
         }
-        if not args.no_cpu_baseline:
+        if args.only or args.decode_batch:
+            line = {"profiling_run": True, "only": args.only, "decode_batch": wd.B, "prefill_ms": t["p"],
+                    "prefill_kernel_ms": t["pk"], "decode_ms": t["d"], "decode_kernel_ms": t["dk"],
+                    "prefill_kernel_tflops": kern_tflops, "decode_kernel_gbs": dec_kern_gbs, "clocks": clocks}
+        elif not args.no_cpu_baseline:
             cb = cpu_baseline(wp, pin, args.cpu_budget_s)
             cb.pop("seconds", None)
             line["cpu_baseline"] = cb

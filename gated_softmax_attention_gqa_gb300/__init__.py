@@ -51,6 +51,9 @@ def gattn_decode_workspace_size(B, H, G, d, Lmax) -> int:
 def gattn_set_profile_events(start=None, stop=None):
     """Record `start`/`stop` (torch.cuda.Event) around the main attention kernel of
     every later call; None, None switches it off."""
+    for e in (start, stop):
+        if e is not None and e.cuda_event == 0:
+            e.record()  # torch creates the underlying cudaEvent lazily, on first record
     _lib.load().gattn_set_profile_events(ctypes.c_void_p(start.cuda_event) if start is not None else None,
                                          ctypes.c_void_p(stop.cuda_event) if stop is not None else None)
 

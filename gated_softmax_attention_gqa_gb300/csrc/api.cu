@@ -10,10 +10,6 @@
 #include "common.cuh"
 #include "internal.h"
 
-namespace gattn {
-int decode_max_batch();
-}
-
 using namespace gattn;
 
 namespace {
@@ -175,15 +171,29 @@ gattn_status gattn_prefill(const void* q, const void* k, const void* v, const vo
     if (bf) {
         kp.dst = workspace;
         if (launch_prologue(kp, true, true, stream) != cudaSuccess) return GATTN_ERR_CUDA;
-        CUtensorMap tmK, tmV;
+        PrefillMaps maps;
+        const uint32_t bn = (uint32_t)prefill_block_n(d);
         const uint64_t kdims[3] = {(uint64_t)d, (uint64_t)S, (uint64_t)B * G};
         const uint64_t kstr[2] = {(uint64_t)d * 2, (uint64_t)S * d * 2};
-        const uint32_t kbox[3] = {64, (uint32_t)prefill_block_n(d), 1};
+        const uint32_t kbox[3] = {64, bn, 1};
         const uint64_t vdims[4] = {(uint64_t)d, (uint64_t)G, (uint64_t)S, (uint64_t)B};
         const uint64_t vstr[3] = {(uint64_t)d * 2, (uint64_t)G * d * 2, (uint64_t)S * G * d * 2};
-        const uint32_t vbox[4] = {64, 1, (uint32_t)prefill_block_n(d), 1};
-        if (!encode_bf16_map(&tmK, workspace, 3, kdims, kstr, kbox)) return GATTN_ERR_CUDA;
-        if (!encode_bf16_map(&tmV, v, 4, vdims, vstr, vbox)) return GATTN_ERR_CUDA;
+        const uint32_t vbox[4] = {64, 1, bn, 1};
+        // raw q and gate: [B,S,H,d] views with token/head strides; 128-token boxes
+        const uint64_t hdims[4] = {(uint64_t)d, (uint64_t)H, (uint64_t)S, (uint64_t)B};
+        const uint64_t qstr[3] = {(uint64_t)q_head_stride * 2, (uint64_t)q_tok_stride * 2,
+                                  (uint64_t)S * q_tok_stride * 2};
+        const uint32_t rbox[4] = {64, 1, 128, 1};
+        if (!encode_bf16_map(&maps.k, workspace, 3, kdims, kstr, kbox)) return GATTN_ERR_CUDA;
+        if (!encode_bf16_map(&maps.v, v, 4, vdims, vstr, vbox)) return GATTN_ERR_CUDA;
+        if (!encode_bf16_map(&maps.q, q, 4, hdims, qstr, rbox)) return GATTN_ERR_CUDA;
+        if (gate_mode == GATTN_GATE_ELEMENTWISE) {
+            const uint64_t gstr[3] = {(uint64_t)gate_head_stride * 2, (uint64_t)gate_tok_stride * 2,
+                                      (uint64_t)S * gate_tok_stride * 2};
+            if (!encode_bf16_map(&maps.gate, gate, 4, hdims, gstr, rbox)) return GATTN_ERR_CUDA;
+        } else {
+            maps.gate = maps.q;  // never read
+        }
         PrefillParams pp;
         std::memset(&pp, 0, sizeof(pp));
         pp.q = q;
@@ -207,7 +217,7 @@ gattn_status gattn_prefill(const void* q, const void* k, const void* v, const vo
         pp.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)d));
         pp.status = status;
         std::memcpy(pp.inv_freq, kp.inv_freq, sizeof(pp.inv_freq));
-        if (launch_prefill_tc(pp, tmK, tmV, stream, g_prof_start, g_prof_stop) != cudaSuccess) return GATTN_ERR_CUDA;
+        if (launch_prefill_tc(pp, maps, stream, g_prof_start, g_prof_stop) != cudaSuccess) return GATTN_ERR_CUDA;
         return GATTN_OK;
     }
 

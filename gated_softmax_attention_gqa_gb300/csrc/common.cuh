@@ -46,7 +46,17 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
 
-__device__ __forceinline__ float sigmoidf_dev(float z) { return 1.0f / (1.0f + __expf(-z)); }
+__device__ __forceinline__ float rcp_approx(float x) {
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// sigmoid(z) = 1 / (1 + 2^(-z log2 e)) with the hardware exp2 and reciprocal
+// approximations (relative error a few ulp; z -> -inf gives 0, z -> +inf gives 1).
+__device__ __forceinline__ float sigmoidf_dev(float z) {
+    return rcp_approx(1.0f + ex2_approx(-1.4426950408889634f * z));
+}
 
 // ------------------------------------------------------------------ mbarrier
 
@@ -141,6 +151,13 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map
         "%5, %6}], [%2];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
         : "memory");
+}
+
+// 1-D bulk copy global -> shared (16-byte aligned addresses, size a multiple of 16).
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                 "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+                 : "memory");
 }
 
 // Order this thread's generic-proxy shared-memory writes before later

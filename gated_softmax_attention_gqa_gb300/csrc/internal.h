@@ -63,9 +63,15 @@ struct DecodeParams {
     float inv_freq[kMaxRotaryHalf];
 };
 
+// TMA descriptors of the tcgen05 prefill: normed keys (workspace), raw V, raw Q
+// and (elementwise gate only) the gate logits; all bf16, 64-element inner boxes.
+struct PrefillMaps {
+    CUtensorMap k, v, q, gate;
+};
+
 cudaError_t launch_prologue(const ProloguePlan& p, bool bf16_in, bool bf16_out, cudaStream_t stream);
-cudaError_t launch_prefill_tc(const PrefillParams& p, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
-                              cudaStream_t stream, cudaEvent_t ev_start, cudaEvent_t ev_stop);
+cudaError_t launch_prefill_tc(const PrefillParams& p, const PrefillMaps& maps, cudaStream_t stream,
+                              cudaEvent_t ev_start, cudaEvent_t ev_stop);
 cudaError_t launch_prefill_f32(const PrefillF32Params& p, cudaStream_t stream, cudaEvent_t ev_start,
                                cudaEvent_t ev_stop);
 cudaError_t launch_decode(const DecodeParams& p, const CUtensorMap& tm_kv, cudaStream_t stream,
@@ -73,6 +79,8 @@ cudaError_t launch_decode(const DecodeParams& p, const CUtensorMap& tm_kv, cudaS
 
 // Prefill tile geometry for the tcgen05 kernel, per head_dim.
 int prefill_block_n(int d);
+
+int decode_max_batch();
 
 // Decode work split: the size of one partial-state slot in floats and the
 // number of slots the workspace must hold.

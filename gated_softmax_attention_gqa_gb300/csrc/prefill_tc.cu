@@ -10,18 +10,23 @@
 // "门放在哪里？".)
 //
 // Roles (6 warps):
-//   warp 0      TMA producer: K' tiles (normed+rotated keys from the pre-pass) and
-//               raw V tiles into a 3-stage shared-memory ring, 128 B swizzle.
+//   warp 0      TMA producer: the raw Q tile once, then K' tiles (keys normed and
+//               rotated by the pre-pass) and raw V tiles into 3-stage rings (128 B
+//               swizzle), K and V issued independently; at the end the gate tile.
 //   warp 1      TMEM owner and MMA issuer (one elected lane): S = Q'K'^T and
 //               O += P V with tcgen05.mma, A operand read from TMEM.
-//   warps 2..5  one thread per query row: the fused Q prologue (RMSNorm + RoPE
-//               of the raw query row, written as bf16 straight into TMEM), the
-//               online softmax, and the gate epilogue.
+//   warps 2..5  one thread per query row: the fused Q prologue (RMSNorm + RoPE of
+//               the raw query row, read from shared memory, written as bf16
+//               straight into TMEM), the online softmax, and the gate epilogue.
+//
+// Shared memory: K ring | V ring.  Before any V tile is loaded the V ring holds
+// the raw Q tile; once every K tile has been consumed the K ring receives the
+// gate tile.  Both reuses are ordered by mbarriers.
 //
 // TMEM (512 columns x 128 lanes, lane = query row):
-//   [0, d)            O accumulator, fp32
-//   [d, d+BN)         S buffer 0 (fp32 scores; overwritten in place by bf16 P)
-//   [d+BN, d+2BN)     S buffer 1
+//   [0, d)             O accumulator, fp32
+//   [d, d+BN)          S buffer 0 (fp32 scores; overwritten in place by bf16 P)
+//   [d+BN, d+2BN)      S buffer 1
 //   [d+2BN, d+2BN+d/2) Q' as packed bf16 pairs (A operand of S = Q'K'^T)
 //
 // Pipeline: while the softmax threads turn S_j into P_j, the tensor core already
@@ -42,8 +47,11 @@ struct PfCfg {
     static constexpr int BN = (D == 256) ? 64 : 128;
     static constexpr int NS = 3;
     static constexpr int KCH = D / 64;               // 128-byte chunks along head_dim
-    static constexpr int CHUNK_BYTES = BN * 128;     // one TMA box: BN rows x 64 bf16
+    static constexpr int CHUNK_BYTES = BN * 128;     // one K/V TMA box: BN rows x 64 bf16
     static constexpr int TILE_BYTES = BN * D * 2;
+    static constexpr int ROWBOX_BYTES = BM * 128;    // one Q/gate TMA box: 128 rows x 64 bf16
+    static constexpr int QTILE_BYTES = BM * D * 2;
+    static_assert(QTILE_BYTES <= NS * TILE_BYTES, "raw Q / gate tile must fit a ring");
     static constexpr int TM_O = 0;
     static constexpr int TM_S0 = D;
     static constexpr int TM_S1 = D + BN;
@@ -53,9 +61,10 @@ struct PfCfg {
     static constexpr int OFF_K = 0;
     static constexpr int OFF_V = NS * TILE_BYTES;
     static constexpr int OFF_BAR = 2 * NS * TILE_BYTES;
-    static constexpr int NBAR = 4 * NS + 8;
+    static constexpr int NBAR = 4 * NS + 10;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
-    static constexpr int SMEM_BYTES = OFF_MISC + 16;
+    static constexpr int OFF_W = (OFF_MISC + 16 + 127) & ~127;  // qnorm weights, D bf16
+    static constexpr int SMEM_BYTES = OFF_W + D * 2;
     // + slack for 1024-byte alignment; never less than 120 KB, so that a second CTA
     // can never share the SM (each CTA allocates all 512 TMEM columns).
     static constexpr int SMEM_ALLOC = (SMEM_BYTES + 1024) > 122880 ? (SMEM_BYTES + 1024) : 122880;
@@ -76,15 +85,15 @@ struct Bars {
     __device__ uint32_t p_full(int i) const { return base + 8u * (4 * ns + 2 + i); }
     __device__ uint32_t o_done() const { return base + 8u * (4 * ns + 4); }
     __device__ uint32_t o_final() const { return base + 8u * (4 * ns + 5); }
-    __device__ uint32_t q_ready() const { return base + 8u * (4 * ns + 6); }
+    __device__ uint32_t q_ready() const { return base + 8u * (4 * ns + 6); }  // Q' in TMEM, raw Q no longer read
     __device__ uint32_t drain() const { return base + 8u * (4 * ns + 7); }
+    __device__ uint32_t q_full() const { return base + 8u * (4 * ns + 8); }   // raw Q tile landed
+    __device__ uint32_t g_full() const { return base + 8u * (4 * ns + 9); }   // gate tile landed
 };
 
-__device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
+__device__ __forceinline__ uint4 lds_v4(uint32_t addr) {
     uint4 r;
-    asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-                 : "l"(p));
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "r"(addr));
     return r;
 }
 
@@ -95,36 +104,91 @@ __device__ __forceinline__ void unpack8(const uint4& v, float (&f)[8]) {
     f[6] = bf16_lo(v.w); f[7] = bf16_hi(v.w);
 }
 
+// Shared-memory address of elements e0..e0+7 of row `row` in a tile stored as
+// 128-byte-swizzled TMA boxes of [128 rows x 64 bf16].
+__device__ __forceinline__ uint32_t rowtile_addr(uint32_t base, int row, int e0) {
+    return base + (uint32_t)(e0 >> 6) * (128u * 128u) + sw128_offset((uint32_t)row, (uint32_t)((e0 >> 3) & 7));
+}
+
 // ----------------------------------------------------------------- producer
 
 template <int D>
-__device__ void run_producer(const CUtensorMap* tmK, const CUtensorMap* tmV, const Bars& bars, uint32_t sbase,
-                             int n_kv, int b, int g, int G, volatile int* abort_flag, unsigned int* status) {
+__device__ void run_producer(const CUtensorMap* tmK, const CUtensorMap* tmV, const CUtensorMap* tmQ,
+                             const CUtensorMap* tmG, const void* qnorm_w, const Bars& bars, uint32_t sbase, int n_kv,
+                             int b, int g, int h,
+                             int qt, int G, bool gate_tile, volatile int* abort_flag, unsigned int* status) {
     using C = PfCfg<D>;
+    // raw Q tile into the (still unused) V ring, the q norm weights next to it
+    mbar_arrive_expect_tx(bars.q_full(), C::QTILE_BYTES + D * 2);
+    bulk_load(sbase + C::OFF_W, qnorm_w, D * 2, bars.q_full());
+#pragma unroll
+    for (int c = 0; c < C::KCH; ++c)
+        tma_load_4d(sbase + C::OFF_V + c * C::ROWBOX_BYTES, tmQ, bars.q_full(), c * 64, h, qt * C::BM, b);
+
+    // K and V tiles, each stream as soon as its own stage frees up
     int nk = 0, nv = 0;
-    for (int j = 0; j < n_kv; ++j) {
-        const int st = j % C::NS;
-        const uint32_t ph = (uint32_t)(j / C::NS) & 1u;
-        if (j >= C::NS && !mbar_wait(bars.k_empty(st), ph ^ 1u, abort_flag, status)) break;
-        mbar_arrive_expect_tx(bars.k_full(st), C::TILE_BYTES);
-        const uint32_t kdst = sbase + C::OFF_K + st * C::TILE_BYTES;
+    bool v_open = false;  // the V ring is free once the raw Q tile has been read
+    const unsigned long long t0 = global_timer_ns();
+    uint32_t spins = 0;
+    while (nk < n_kv || nv < n_kv) {
+        bool progressed = false;
+        if (nk < n_kv &&
+            (nk < C::NS || mbar_try_wait(bars.k_empty(nk % C::NS), ((uint32_t)(nk / C::NS) & 1u) ^ 1u))) {
+            const int st = nk % C::NS;
+            mbar_arrive_expect_tx(bars.k_full(st), C::TILE_BYTES);
+            const uint32_t kdst = sbase + C::OFF_K + st * C::TILE_BYTES;
 #pragma unroll
-        for (int c = 0; c < C::KCH; ++c)
-            tma_load_3d(kdst + c * C::CHUNK_BYTES, tmK, bars.k_full(st), c * 64, j * C::BN, b * G + g);
-        ++nk;
-        if (j >= C::NS && !mbar_wait(bars.v_empty(st), ph ^ 1u, abort_flag, status)) break;
-        mbar_arrive_expect_tx(bars.v_full(st), C::TILE_BYTES);
-        const uint32_t vdst = sbase + C::OFF_V + st * C::TILE_BYTES;
+            for (int c = 0; c < C::KCH; ++c)
+                tma_load_3d(kdst + c * C::CHUNK_BYTES, tmK, bars.k_full(st), c * 64, nk * C::BN, b * G + g);
+            ++nk;
+            progressed = true;
+        }
+        if (!v_open) v_open = mbar_try_wait(bars.q_ready(), 0);
+        if (v_open && nv < n_kv &&
+            (nv < C::NS || mbar_try_wait(bars.v_empty(nv % C::NS), ((uint32_t)(nv / C::NS) & 1u) ^ 1u))) {
+            const int st = nv % C::NS;
+            mbar_arrive_expect_tx(bars.v_full(st), C::TILE_BYTES);
+            const uint32_t vdst = sbase + C::OFF_V + st * C::TILE_BYTES;
 #pragma unroll
-        for (int c = 0; c < C::KCH; ++c)
-            tma_load_4d(vdst + c * C::CHUNK_BYTES, tmV, bars.v_full(st), c * 64, g, j * C::BN, b);
-        ++nv;
+            for (int c = 0; c < C::KCH; ++c)
+                tma_load_4d(vdst + c * C::CHUNK_BYTES, tmV, bars.v_full(st), c * 64, g, nv * C::BN, b);
+            ++nv;
+            progressed = true;
+        }
+        if (progressed) {
+            spins = 0;
+            continue;
+        }
+        if ((++spins & 63u) == 0) {
+            if (*abort_flag) break;
+            if (global_timer_ns() - t0 > 4 * kWaitLimitNs) {
+                *abort_flag = 1;
+                atomicOr(status, GATTN_DEVICE_TIMEOUT);
+                break;
+            }
+        }
+    }
+    // gate tile into the K ring once every K stage has been consumed for the last time
+    bool g_issued = false;
+    if (gate_tile && nk == n_kv) {
+        bool ok = true;
+        for (int j = n_kv > C::NS ? n_kv - C::NS : 0; ok && j < n_kv; ++j)
+            ok = mbar_wait(bars.k_empty(j % C::NS), (uint32_t)(j / C::NS) & 1u, abort_flag, status);
+        if (ok) {
+            mbar_arrive_expect_tx(bars.g_full(), C::QTILE_BYTES);
+#pragma unroll
+            for (int c = 0; c < C::KCH; ++c)
+                tma_load_4d(sbase + C::OFF_K + c * C::ROWBOX_BYTES, tmG, bars.g_full(), c * 64, h, qt * C::BM, b);
+            g_issued = true;
+        }
     }
     // Drain: every copy this thread started must land before the CTA can exit.
+    mbar_wait_drain(bars.q_full(), 0, status);
     for (int j = nk > C::NS ? nk - C::NS : 0; j < nk; ++j)
         mbar_wait_drain(bars.k_full(j % C::NS), (uint32_t)(j / C::NS) & 1u, status);
     for (int j = nv > C::NS ? nv - C::NS : 0; j < nv; ++j)
         mbar_wait_drain(bars.v_full(j % C::NS), (uint32_t)(j / C::NS) & 1u, status);
+    if (g_issued) mbar_wait_drain(bars.g_full(), 0, status);
 }
 
 // ----------------------------------------------------------------- MMA issuer
@@ -135,18 +199,20 @@ __device__ void run_mma(const Bars& bars, uint32_t sbase, uint32_t tm, int n_kv,
     using C = PfCfg<D>;
     bool ok = mbar_wait(bars.q_ready(), 0, abort_flag, status);
     tc_fence_after();
+    // descriptors of stage 0; stage s adds s * TILE_BYTES to the start address
+    const uint64_t kdesc0 = make_sdesc_sw128(sbase + C::OFF_K, 16, 1024);
+    const uint64_t vdesc0 = make_sdesc_sw128(sbase + C::OFF_V, C::CHUNK_BYTES, 1024);
 
     auto issue_qk = [&](int j) -> bool {
         const int st = j % C::NS;
         if (!mbar_wait(bars.k_full(st), (uint32_t)(j / C::NS) & 1u, abort_flag, status)) return false;
         tc_fence_after();
         const uint32_t d_tmem = tm + ((j & 1) ? C::TM_S1 : C::TM_S0);
-        const uint32_t kbase = sbase + C::OFF_K + st * C::TILE_BYTES;
+        const uint64_t kd = kdesc0 + (uint64_t)((st * C::TILE_BYTES) >> 4);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-            const uint64_t bdesc = make_sdesc_sw128(kbase + (kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32, 16, 1024);
-            mma_ts(d_tmem, tm + C::TM_Q + kk * 8, bdesc, C::IDESC_QK, kk > 0 ? 1u : 0u);
-        }
+        for (int kk = 0; kk < D / 16; ++kk)
+            mma_ts(d_tmem, tm + C::TM_Q + kk * 8, kd + (uint64_t)(((kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32) >> 4),
+                   C::IDESC_QK, kk > 0 ? 1u : 0u);
         tc_commit(bars.k_empty(st));
         tc_commit(bars.s_full(j & 1));
         return true;
@@ -161,12 +227,11 @@ __device__ void run_mma(const Bars& bars, uint32_t sbase, uint32_t tm, int n_kv,
         if (!mbar_wait(bars.v_full(st), (uint32_t)(j / C::NS) & 1u, abort_flag, status)) { ok = false; break; }
         tc_fence_after();
         const uint32_t p_tmem = tm + ((j & 1) ? C::TM_S1 : C::TM_S0);
-        const uint32_t vbase = sbase + C::OFF_V + st * C::TILE_BYTES;
+        const uint64_t vd = vdesc0 + (uint64_t)((st * C::TILE_BYTES) >> 4);
 #pragma unroll
-        for (int kk = 0; kk < C::BN / 16; ++kk) {
-            const uint64_t bdesc = make_sdesc_sw128(vbase + kk * 16 * 128, C::CHUNK_BYTES, 1024);
-            mma_ts(tm + C::TM_O, p_tmem + kk * 8, bdesc, C::IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
-        }
+        for (int kk = 0; kk < C::BN / 16; ++kk)
+            mma_ts(tm + C::TM_O, p_tmem + kk * 8, vd + (uint64_t)((kk * 16 * 128) >> 4), C::IDESC_PV,
+                   (j > 0 || kk > 0) ? 1u : 0u);
         tc_commit(bars.v_empty(st));
         tc_commit(bars.o_done());
     }
@@ -179,8 +244,8 @@ __device__ void run_mma(const Bars& bars, uint32_t sbase, uint32_t tm, int n_kv,
 // ----------------------------------------------------------------- softmax / prologue / epilogue
 
 template <int D>
-__device__ void run_softmax(const PrefillParams& p, const Bars& bars, uint32_t tm, int quarter, int lane, int qt,
-                            int b, int h, int n_kv, volatile int* abort_flag) {
+__device__ void run_softmax(const PrefillParams& p, const Bars& bars, uint32_t sbase, uint32_t tm, int quarter,
+                            int lane, int qt, int b, int h, int n_kv, volatile int* abort_flag) {
     using C = PfCfg<D>;
     const int row = quarter * 32 + lane;
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
@@ -188,36 +253,34 @@ __device__ void run_softmax(const PrefillParams& p, const Bars& bars, uint32_t t
     const int t = qt * C::BM + row;
     const bool valid = t < p.S;
     const int64_t tok = (int64_t)b * p.S + (valid ? t : 0);
+    const bf16* grow = static_cast<const bf16*>(p.gate) + tok * p.gate_tok_stride + (int64_t)h * p.gate_head_stride;
+    float gate_head = 1.f;
+    if (p.gate_mode == GATTN_GATE_HEADWISE && valid) gate_head = sigmoidf_dev(__bfloat162float(grow[0]));
 
-    // ---- fused Q prologue: rmsnorm then partial rotate-half RoPE, bf16 into TMEM
+    // ---- fused Q prologue: rmsnorm then partial rotate-half RoPE, bf16 into TMEM.
+    // The raw row is read from the Q tile the producer placed in the V ring
+    // (rows past the sequence end were zero-filled by TMA).
+    if (!__all_sync(0xffffffffu, mbar_wait(bars.q_full(), 0, abort_flag, p.status))) return;
     {
-        const bf16* qrow = static_cast<const bf16*>(p.q) + tok * p.q_tok_stride + (int64_t)h * p.q_head_stride;
-        const bf16* wq = static_cast<const bf16*>(p.qnorm_w);
-        float ss = 0.f;
-        if (valid) {
-#pragma unroll 4
-            for (int c = 0; c < D / 8; ++c) {
-                float f[8];
-                unpack8(ldg_nc_v4(qrow + 8 * c), f);
+        const uint32_t qbase = sbase + C::OFF_V;
+        const uint32_t wbase = sbase + C::OFF_W;
+        float ss[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                for (int e = 0; e < 8; ++e) ss = fmaf(f[e], f[e], ss);
-            }
+        for (int c = 0; c < D / 8; ++c) {
+            float f[8];
+            unpack8(lds_v4(rowtile_addr(qbase, row, 8 * c)), f);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) ss[e & 3] = fmaf(f[e], f[e], ss[e & 3]);
         }
-        const float rinv = rsqrtf(ss / (float)D + p.eps);
+        const float rinv = rsqrtf(((ss[0] + ss[1]) + (ss[2] + ss[3])) / (float)D + p.eps);
         const float posf = valid ? (p.pos ? (float)p.pos[tok] : (float)t) : 0.f;
         const int half = p.rd >> 1;
         for (int i0 = 0; i0 < half; i0 += 8) {
             float xa[8], xb[8], wa[8], wb[8];
-            if (valid) {
-                unpack8(ldg_nc_v4(qrow + i0), xa);
-                unpack8(ldg_nc_v4(qrow + i0 + half), xb);
-            } else {
-#pragma unroll
-                for (int e = 0; e < 8; ++e) xa[e] = xb[e] = 0.f;
-            }
-            unpack8(ldg_nc_v4(wq + i0), wa);
-            unpack8(ldg_nc_v4(wq + i0 + half), wb);
-            __syncwarp();
+            unpack8(lds_v4(rowtile_addr(qbase, row, i0)), xa);
+            unpack8(lds_v4(rowtile_addr(qbase, row, i0 + half)), xb);
+            unpack8(lds_v4(wbase + 2 * i0), wa);
+            unpack8(lds_v4(wbase + 2 * (i0 + half)), wb);
             uint32_t lo[4], hi[4];
 #pragma unroll
             for (int e = 0; e < 8; e += 2) {
@@ -229,24 +292,21 @@ __device__ void run_softmax(const PrefillParams& p, const Bars& bars, uint32_t t
                 lo[e >> 1] = pack_bf16x2((a0 * c0 - b0 * s0) * rinv, (a1 * c1 - b1 * s1) * rinv);
                 hi[e >> 1] = pack_bf16x2((b0 * c0 + a0 * s0) * rinv, (b1 * c1 + a1 * s1) * rinv);
             }
+            __syncwarp();
             tmem_st4(tl + C::TM_Q + (i0 >> 1), lo[0], lo[1], lo[2], lo[3]);
             tmem_st4(tl + C::TM_Q + ((i0 + half) >> 1), hi[0], hi[1], hi[2], hi[3]);
         }
         for (int e0 = p.rd; e0 < D; e0 += 8) {
             float x[8], w[8];
-            if (valid) {
-                unpack8(ldg_nc_v4(qrow + e0), x);
-            } else {
-#pragma unroll
-                for (int e = 0; e < 8; ++e) x[e] = 0.f;
-            }
-            unpack8(ldg_nc_v4(wq + e0), w);
+            unpack8(lds_v4(rowtile_addr(qbase, row, e0)), x);
+            unpack8(lds_v4(wbase + 2 * e0), w);
             __syncwarp();
             tmem_st4(tl + C::TM_Q + (e0 >> 1), pack_bf16x2(x[0] * w[0] * rinv, x[1] * w[1] * rinv),
                      pack_bf16x2(x[2] * w[2] * rinv, x[3] * w[3] * rinv),
                      pack_bf16x2(x[4] * w[4] * rinv, x[5] * w[5] * rinv),
                      pack_bf16x2(x[6] * w[6] * rinv, x[7] * w[7] * rinv));
         }
+        fence_proxy_async_smem();  // our reads of the V ring happen before the V tiles overwrite it
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
@@ -258,14 +318,11 @@ __device__ void run_softmax(const PrefillParams& p, const Bars& bars, uint32_t t
     const int row_min = qt * C::BM;
     float m_ref = -INFINITY;  // reference max (log2 domain) shared by O and l
     float l = 0.f;
-    bool ok = true;
     for (int j = 0; j < n_kv; ++j) {
         const int sb = j & 1;
         const uint32_t s_col = sb ? C::TM_S1 : C::TM_S0;
-        if (!__all_sync(0xffffffffu, mbar_wait(bars.s_full(sb), (uint32_t)(j >> 1) & 1u, abort_flag, p.status))) {
-            ok = false;
-            break;
-        }
+        if (!__all_sync(0xffffffffu, mbar_wait(bars.s_full(sb), (uint32_t)(j >> 1) & 1u, abort_flag, p.status)))
+            return;
         tc_fence_after();
         float s[C::BN];
         {
@@ -283,9 +340,13 @@ __device__ void run_softmax(const PrefillParams& p, const Bars& bars, uint32_t t
             for (int c = 0; c < C::BN; ++c)
                 if (key0 + c > t) s[c] = -INFINITY;
         }
-        float mt = s[0];
+        float mx[8];
 #pragma unroll
-        for (int c = 1; c < C::BN; ++c) mt = fmaxf(mt, s[c]);
+        for (int i = 0; i < 8; ++i) mx[i] = s[i];
+#pragma unroll
+        for (int c = 8; c < C::BN; ++c) mx[c & 7] = fmaxf(mx[c & 7], s[c]);
+        const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
         const float m_new = fmaxf(m_ref, mt * sl2);
         const bool need = (m_new - m_ref) > C::RESCALE_THRESHOLD;
         if (j == 0) {
@@ -298,10 +359,8 @@ __device__ void run_softmax(const PrefillParams& p, const Bars& bars, uint32_t t
             }
             __syncwarp();
             // O is only touched once the previous P V has landed.
-            if (!__all_sync(0xffffffffu, mbar_wait(bars.o_done(), (uint32_t)(j - 1) & 1u, abort_flag, p.status))) {
-                ok = false;
-                break;
-            }
+            if (!__all_sync(0xffffffffu, mbar_wait(bars.o_done(), (uint32_t)(j - 1) & 1u, abort_flag, p.status)))
+                return;
             tc_fence_after();
 #pragma unroll 1
             for (int c = 0; c < D; c += 32) {
@@ -313,7 +372,7 @@ __device__ void run_softmax(const PrefillParams& p, const Bars& bars, uint32_t t
             }
         }
         // P = exp2(s * scale * log2e - m_ref), packed bf16, written over S in TMEM
-        float rs = 0.f;
+        float rs[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
         const float mref = m_ref;
 #pragma unroll
         for (int c = 0; c < C::BN; c += 64) {
@@ -322,27 +381,27 @@ __device__ void run_softmax(const PrefillParams& p, const Bars& bars, uint32_t t
             for (int e = 0; e < 32; ++e) {
                 const float p0 = ex2_approx(fmaf(s[c + 2 * e], sl2, -mref));
                 const float p1 = ex2_approx(fmaf(s[c + 2 * e + 1], sl2, -mref));
-                rs += p0 + p1;
+                rs[e & 7] += p0 + p1;
                 pk[e] = pack_bf16x2(p0, p1);
             }
             tmem_st32(tl + s_col + (c >> 1), pk);
         }
-        l += rs;
+        l += ((rs[0] + rs[1]) + (rs[2] + rs[3])) + ((rs[4] + rs[5]) + (rs[6] + rs[7]));
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bars.p_full(sb));
     }
-    if (!ok) return;
 
     // ---- epilogue: O / l * sigmoid(gate) -> bf16 [B,S,H*d]
     if (!__all_sync(0xffffffffu, mbar_wait(bars.o_final(), 0, abort_flag, p.status))) return;
+    const bool elementwise = p.gate_mode == GATTN_GATE_ELEMENTWISE;
+    if (elementwise && !__all_sync(0xffffffffu, mbar_wait(bars.g_full(), 0, abort_flag, p.status))) return;
     tc_fence_after();
     const float inv_l = 1.f / l;
+    const float gh = inv_l * gate_head;
     bf16* orow = static_cast<bf16*>(p.out) + (tok * p.H + h) * D;
-    const bf16* grow = static_cast<const bf16*>(p.gate) + tok * p.gate_tok_stride + (int64_t)h * p.gate_head_stride;
-    float gh = inv_l;
-    if (p.gate_mode == GATTN_GATE_HEADWISE && valid) gh = inv_l * sigmoidf_dev(__bfloat162float(grow[0]));
+    const uint32_t gbase = sbase + C::OFF_K;
 #pragma unroll 1
     for (int c = 0; c < D; c += 32) {
         uint32_t r[32];
@@ -350,11 +409,11 @@ __device__ void run_softmax(const PrefillParams& p, const Bars& bars, uint32_t t
         tmem_ld32(tl + C::TM_O + c, r);
         if (!valid) continue;
         float gv[32];
-        if (p.gate_mode == GATTN_GATE_ELEMENTWISE) {
+        if (elementwise) {
 #pragma unroll
             for (int q4 = 0; q4 < 4; ++q4) {
                 float f[8];
-                unpack8(ldg_nc_v4(grow + c + 8 * q4), f);
+                unpack8(lds_v4(rowtile_addr(gbase, row, c + 8 * q4)), f);
 #pragma unroll
                 for (int e = 0; e < 8; ++e) gv[8 * q4 + e] = inv_l * sigmoidf_dev(f[e]);
             }
@@ -380,6 +439,7 @@ __device__ void run_softmax(const PrefillParams& p, const Bars& bars, uint32_t t
 template <int D>
 __global__ void __launch_bounds__(PfCfg<D>::THREADS, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                      const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmG,
                       const __grid_constant__ PrefillParams p) {
     using C = PfCfg<D>;
     extern __shared__ uint8_t smem_raw[];
@@ -413,10 +473,13 @@ __global__ void __launch_bounds__(PfCfg<D>::THREADS, 1)
         mbar_init(bars.o_final(), 1);
         mbar_init(bars.q_ready(), 4);
         mbar_init(bars.drain(), 1);
+        mbar_init(bars.q_full(), 1);
+        mbar_init(bars.g_full(), 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
     if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmQ);
         tma_prefetch_desc(&tmK);
         tma_prefetch_desc(&tmV);
     }
@@ -430,13 +493,15 @@ __global__ void __launch_bounds__(PfCfg<D>::THREADS, 1)
     const uint32_t tm = *tmem_slot;
 
     if (warp == 0) {
-        if (lane == 0) run_producer<D>(&tmK, &tmV, bars, sbase, n_kv, b, g, p.G, abort_flag, p.status);
+        if (lane == 0)
+            run_producer<D>(&tmK, &tmV, &tmQ, &tmG, p.qnorm_w, bars, sbase, n_kv, b, g, h, qt, p.G,
+                            p.gate_mode == GATTN_GATE_ELEMENTWISE, abort_flag, p.status);
         __syncwarp();
     } else if (warp == 1) {
         if (lane == 0) run_mma<D>(bars, sbase, tm, n_kv, abort_flag, p.status);
         __syncwarp();
     } else {
-        run_softmax<D>(p, bars, tm, warp & 3, lane, qt, b, h, n_kv, abort_flag);
+        run_softmax<D>(p, bars, sbase, tm, warp & 3, lane, qt, b, h, n_kv, abort_flag);
     }
     tc_fence_before();
     __syncthreads();
@@ -447,8 +512,8 @@ __global__ void __launch_bounds__(PfCfg<D>::THREADS, 1)
 }
 
 template <int D>
-cudaError_t launch_d(const PrefillParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV, cudaStream_t stream,
-                     cudaEvent_t ev_start, cudaEvent_t ev_stop) {
+cudaError_t launch_d(const PrefillParams& p, const PrefillMaps& maps, cudaStream_t stream, cudaEvent_t ev_start,
+                     cudaEvent_t ev_stop) {
     using C = PfCfg<D>;
     cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::SMEM_ALLOC);
@@ -456,7 +521,8 @@ cudaError_t launch_d(const PrefillParams& p, const CUtensorMap& tmK, const CUten
     const long long blocks = (long long)p.n_qtiles * p.B * p.H;
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
     if (ev_start) cudaEventRecord(ev_start, stream);
-    prefill_tc_kernel<D><<<(unsigned)blocks, C::THREADS, C::SMEM_ALLOC, stream>>>(tmK, tmV, p);
+    prefill_tc_kernel<D><<<(unsigned)blocks, C::THREADS, C::SMEM_ALLOC, stream>>>(maps.k, maps.v, maps.q, maps.gate,
+                                                                                    p);
     cudaError_t err = cudaGetLastError();
     if (ev_stop) cudaEventRecord(ev_stop, stream);
     return err;
@@ -466,12 +532,12 @@ cudaError_t launch_d(const PrefillParams& p, const CUtensorMap& tmK, const CUten
 
 int prefill_block_n(int d) { return d == 256 ? PfCfg<256>::BN : d == 128 ? PfCfg<128>::BN : PfCfg<64>::BN; }
 
-cudaError_t launch_prefill_tc(const PrefillParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV,
-                              cudaStream_t stream, cudaEvent_t ev_start, cudaEvent_t ev_stop) {
+cudaError_t launch_prefill_tc(const PrefillParams& p, const PrefillMaps& maps, cudaStream_t stream,
+                              cudaEvent_t ev_start, cudaEvent_t ev_stop) {
     switch (p.d) {
-        case 64: return launch_d<64>(p, tmK, tmV, stream, ev_start, ev_stop);
-        case 128: return launch_d<128>(p, tmK, tmV, stream, ev_start, ev_stop);
-        case 256: return launch_d<256>(p, tmK, tmV, stream, ev_start, ev_stop);
+        case 64: return launch_d<64>(p, maps, stream, ev_start, ev_stop);
+        case 128: return launch_d<128>(p, maps, stream, ev_start, ev_stop);
+        case 256: return launch_d<256>(p, maps, stream, ev_start, ev_stop);
         default: return cudaErrorInvalidValue;
     }
 }
