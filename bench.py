@@ -38,6 +38,19 @@ DECODE = "qwen35_08b_decode"
 L2_FLUSH_BYTES = 256 << 20
 
 
+def reduce_max(values, device=None):
+    """Element-wise max of a list of floats over all ranks (the slowest rank sets
+    every timing); identity when torch.distributed is not initialised."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return list(values)
+    t = torch.tensor(list(values), dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -301,10 +314,7 @@ def main():
         return [a.elapsed_time(b) for a, b in evs[key]]
 
     t = {k: statistics.mean(ms(k)) if (do_p if k[0] == "p" else do_d) else float("nan") for k in evs}
-    if world > 1:
-        vec = torch.tensor([t["p"], t["pk"], t["d"], t["dk"]], dtype=torch.float64, device=dev)
-        dist.all_reduce(vec, op=dist.ReduceOp.MAX)
-        t = dict(zip(("p", "pk", "d", "dk"), vec.tolist()))
+    t = dict(zip(("p", "pk", "d", "dk"), reduce_max([t["p"], t["pk"], t["d"], t["dk"]], dev)))
     status = ga.gattn_get_device_status()
 
     flops = prefill_flops(wp.B, wp.S, wp.H, wp.d)
@@ -339,10 +349,7 @@ def main():
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / K
-    if world > 1:
-        vec = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(vec, op=dist.ReduceOp.MAX)
-        e2e_ms = vec.item()
+    e2e_ms = reduce_max([e2e_ms], dev)[0]
     e2e_val = world * flops / (e2e_ms * 1e-3) / 1e12 if do_p and e2e_ms > 0 else float("nan")
 
     if rank == 0:
