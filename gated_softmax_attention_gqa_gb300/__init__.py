@@ -19,7 +19,7 @@ from ._lib import GattnError, check
 GATE_MODES = {"none": 0, "elementwise": 1, "headwise": 2}
 DTYPES = {torch.bfloat16: 0, torch.float32: 1}
 
-__all__ = ["gattn_prefill", "gattn_decode", "gattn_prefill_workspace_size", "gattn_decode_workspace_size",
+__all__ = ["gattn_prefill", "gattn_decode", "gattn_decode_noalloc", "gattn_prefill_workspace_size", "gattn_decode_workspace_size",
            "gattn_get_device_status", "gattn_set_profile_events", "gattn_strerror", "GattnError", "GATE_MODES"]
 
 
@@ -140,4 +140,22 @@ def gattn_decode(q_new, kv_cache, seqlens, gate, qnorm_w, *, rotary_dim, rope_ba
         Lmax, int(rotary_dim), float(rope_base), float(eps), mode, _ptr(workspace),
         workspace.numel() * workspace.element_size(), _ptr(out), _stream_handle(stream, q_new.device))
     check(st, "gattn_decode")
+    return out
+
+
+def gattn_decode_noalloc(q_new, kv_cache, seqlens, gate, qnorm_w, *, rotary_dim, rope_base, eps=1e-6,
+                         gate_mode="elementwise", out=None, stream=None):
+    """gattn_decode without a workspace: the partial states live in the library's
+    own fixed device array (GATTN_DECODE_NOALLOC_SCRATCH_BYTES).  For callers that
+    must not allocate device memory while decoding; pass `out` to allocate nothing
+    here either.  Calls that overlap on the GPU race on that array."""
+    mode = _mode(gate_mode)
+    B, H, d = q_new.shape
+    G, Lmax = kv_cache.shape[2], kv_cache.shape[3]
+    if out is None:
+        out = torch.empty((B, H * d), dtype=q_new.dtype, device=q_new.device)
+    st = _lib.load().gattn_decode_noalloc(
+        _ptr(q_new), _ptr(kv_cache), _ptr(seqlens), _ptr(gate if mode != 0 else None), _ptr(qnorm_w), B, H, G, d,
+        Lmax, int(rotary_dim), float(rope_base), float(eps), mode, _ptr(out), _stream_handle(stream, q_new.device))
+    check(st, "gattn_decode_noalloc")
     return out

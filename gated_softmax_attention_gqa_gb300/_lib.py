@@ -12,6 +12,7 @@ EXPORTS = (
     "gattn_prefill",
     "gattn_decode_workspace_size",
     "gattn_decode",
+    "gattn_decode_noalloc",
     "gattn_get_device_status",
     "gattn_set_profile_events",
 )
@@ -47,6 +48,8 @@ def load():
     lib.gattn_decode_workspace_size.argtypes = [_i, _i, _i, _i, _i]
     lib.gattn_decode.restype = _i
     lib.gattn_decode.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _d, _f, _i, _vp, _sz, _vp, _vp]
+    lib.gattn_decode_noalloc.restype = _i
+    lib.gattn_decode_noalloc.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _d, _f, _i, _vp, _vp]
     lib.gattn_get_device_status.restype = _i
     lib.gattn_get_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint), _vp]
     lib.gattn_set_profile_events.restype = None

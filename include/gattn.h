@@ -142,6 +142,34 @@ gattn_status gattn_decode(const void* q_new, const void* kv_cache, const int32_t
                           void* out, void* stream);
 
 /*
+ * One decode step exactly like gattn_decode, for callers that cannot allocate
+ * device memory when they run it -- for example a serving loop that must not call
+ * cudaMalloc while requests are in flight (it can synchronise the whole device),
+ * or a host framework that hands a plugin its buffers and forbids it to allocate
+ * any of its own.  The source pages have no counterpart to this entry point: it
+ * exists only to spare such callers the workspace.
+ *
+ * Arguments, layouts and errors are those of gattn_decode minus the workspace.
+ * The partial softmax states live instead in one fixed array of device memory
+ * inside the library, GATTN_DECODE_NOALLOC_SCRATCH_BYTES (8 MiB) long, that every
+ * GPU which loads the library holds until the process exits.  A problem whose
+ * gattn_decode_workspace_size() exceeds that limit is rejected with
+ * GATTN_ERR_WORKSPACE before anything is launched.  The entry point itself calls
+ * no cudaMalloc, cudaFree or other allocating routine.
+ *
+ * Set-up: the first call with a given device current looks up the array's device
+ * address (cudaGetSymbolAddress) and caches it; make that first call before any
+ * stream capture.  All calls share the one array and it keeps the last call's
+ * contents; nothing in it needs to start at zero.  Calls whose executions overlap
+ * on the GPU (on different streams, say) race on the array and give wrong
+ * results: serialise them.
+ */
+#define GATTN_DECODE_NOALLOC_SCRATCH_BYTES ((size_t)8 << 20)
+gattn_status gattn_decode_noalloc(const void* q_new, const void* kv_cache, const int32_t* seqlens, const void* gate,
+                                  const void* qnorm_w, int B, int H, int G, int d, int Lmax, int rotary_dim,
+                                  double rope_base, float eps, int gate_mode, void* out, void* stream);
+
+/*
  * Read (synchronously on `stream`) and clear the device status word.  Writes the
  * GATTN_DEVICE_* bits seen since the last call to *bits (may be NULL) and returns
  * GATTN_ERR_DEVICE if any bit was set, GATTN_OK otherwise.
