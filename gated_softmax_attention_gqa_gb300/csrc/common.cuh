@@ -58,6 +58,23 @@ __device__ __forceinline__ float sigmoidf_dev(float z) {
     return rcp_approx(1.0f + ex2_approx(-1.4426950408889634f * z));
 }
 
+// sin and cos of a RoPE angle.  Cody-Waite reduction by 2*pi (the constant split
+// into a float head and a float tail, k = round(x / 2pi)) brings x into
+// [-pi, pi], where the hardware sine/cosine approximations are accurate to about
+// 2^-21 absolute; the reduction adds ~1e-7 rad for |x| up to 1e5.  Angles here
+// are pos * inv_freq with pos < 2^24, whose own fp32 rounding (ulp(x)/2) is the
+// larger error.
+__device__ __forceinline__ void rope_sincos(float x, float* s, float* c) {
+    constexpr float kInv2Pi = 0.15915494309189535f;
+    constexpr float k2PiHi = 6.28318548202514648f;      // 2*pi rounded to float
+    constexpr float k2PiLo = -1.7484556000744487e-07f;  // 2*pi - k2PiHi
+    const float k = rintf(x * kInv2Pi);
+    float r = fmaf(-k, k2PiHi, x);
+    r = fmaf(-k, k2PiLo, r);
+    *s = __sinf(r);
+    *c = __cosf(r);
+}
+
 // ------------------------------------------------------------------ mbarrier
 
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
@@ -120,6 +137,11 @@ __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, u
         }
     }
 }
+
+// Programmatic dependent launch: let the next kernel on the stream start its
+// independent prologue early / wait until the previous kernel's results are visible.
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait_prerequisites() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 // ------------------------------------------------------------------ TMA
 
@@ -195,8 +217,7 @@ __device__ __forceinline__ void tc_fence_after() {
 
 // Arrive once on `bar` when every tcgen05 operation this thread issued so far completes.
 __device__ __forceinline__ void tc_commit(uint32_t bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-                 : "memory");
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar));
 }
 
 // D(tmem) (+)= A(tmem) * B(smem), kind::f16 (bf16 inputs, fp32 accumulate).
@@ -206,8 +227,17 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
         "{\n\t.reg .pred p;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate));
+}
+
+// D(tmem) (+)= A(smem) * B(smem), kind::f16.
+__device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                       uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate));
 }
 
 // Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, dense.

@@ -204,8 +204,8 @@ __global__ void __launch_bounds__(DecCfg<D>::THREADS, 1)
                         const int fp = first ? f + hf : f - hf;
                         const int i0 = first ? e0 : e0 - half;
                         float s0, c0, s1, c1;
-                        sincosf(posf * p.inv_freq[i0], &s0, &c0);
-                        sincosf(posf * p.inv_freq[i0 + 1], &s1, &c1);
+                        rope_sincos(posf * p.inv_freq[i0], &s0, &c0);
+                        rope_sincos(posf * p.inv_freq[i0 + 1], &s1, &c1);
                         float q0 = 0.f, q1 = 0.f;
 #pragma unroll
                         for (int ff = 0; ff < D / 8; ++ff)

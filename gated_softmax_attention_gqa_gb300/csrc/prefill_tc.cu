@@ -9,13 +9,14 @@
 // scaling and stable softmax matter"; "Gated Attention" deep-dive, section
 // "门放在哪里？".)
 //
-// Roles (6 warps):
+// Roles (7 warps):
 //   warp 0      TMA producer: the raw Q tile once, then K' tiles (keys normed and
 //               rotated by the pre-pass) and raw V tiles into 3-stage rings (128 B
 //               swizzle), K and V issued independently; at the end the gate tile.
-//   warp 1      TMEM owner and MMA issuer (one elected lane): S = Q'K'^T and
-//               O += P V with tcgen05.mma, A operand read from TMEM.
-//   warps 2..5  one thread per query row: the fused Q prologue (RMSNorm + RoPE of
+//   warps 1, 2  MMA issuers (warp 1 also owns TMEM): warp 1 + i issues S = Q'K'^T
+//               (tcgen05.mma, A read from TMEM) and O += P V of the KV tiles j
+//               with j % 2 == i.
+//   warps 3..6  one thread per query row: the fused Q prologue (RMSNorm + RoPE of
 //               the raw query row, read from shared memory, written as bf16
 //               straight into TMEM), the online softmax, and the gate epilogue.
 //
@@ -44,31 +45,41 @@ namespace {
 template <int D>
 struct PfCfg {
     static constexpr int BM = 128;
+    // d = 256: 64-key tiles (TMEM: O 256 + two S 64 + Q' 128 columns) and P goes to
+    // shared memory, so a score buffer is free again as soon as the softmax has read
+    // it.  d <= 128: 128-key tiles, P overwrites S in TMEM.
     static constexpr int BN = (D == 256) ? 64 : 128;
-    static constexpr int NS = 3;
+    static constexpr bool PSMEM = (D == 256);
+    static constexpr int NSB = 2;  // score buffers in TMEM: tile j uses buffer j % 2
+    static constexpr int NPB = PSMEM ? 2 : 0;  // P buffers in shared memory
+    static constexpr int NSK = 3;  // K ring stages
+    static constexpr int NSV = 3;  // V ring stages
     static constexpr int KCH = D / 64;               // 128-byte chunks along head_dim
     static constexpr int CHUNK_BYTES = BN * 128;     // one K/V TMA box: BN rows x 64 bf16
     static constexpr int TILE_BYTES = BN * D * 2;
     static constexpr int ROWBOX_BYTES = BM * 128;    // one Q/gate TMA box: 128 rows x 64 bf16
     static constexpr int QTILE_BYTES = BM * D * 2;
-    static_assert(QTILE_BYTES <= NS * TILE_BYTES, "raw Q / gate tile must fit a ring");
+    static_assert(QTILE_BYTES <= NSV * TILE_BYTES && QTILE_BYTES <= NSK * TILE_BYTES,
+                  "raw Q and gate tiles must fit the V and K rings");
+    static constexpr int P_BUF_BYTES = PSMEM ? BM * BN * 2 : 0;  // [BN/64 chunks][128 rows][128 B]
     static constexpr int TM_O = 0;
-    static constexpr int TM_S0 = D;
-    static constexpr int TM_S1 = D + BN;
-    static constexpr int TM_Q = D + 2 * BN;
+    static constexpr int TM_S = D;                   // score buffer b at TM_S + b * BN
+    static constexpr int TM_Q = D + NSB * BN;
     static constexpr int TM_COLS = 512;
     static_assert(TM_Q + D / 2 <= TM_COLS, "TMEM budget");
     static constexpr int OFF_K = 0;
-    static constexpr int OFF_V = NS * TILE_BYTES;
-    static constexpr int OFF_BAR = 2 * NS * TILE_BYTES;
-    static constexpr int NBAR = 4 * NS + 10;
+    static constexpr int OFF_V = NSK * TILE_BYTES;
+    static constexpr int OFF_P = OFF_V + NSV * TILE_BYTES;
+    static constexpr int OFF_BAR = OFF_P + NPB * P_BUF_BYTES;
+    static constexpr int NBAR = 2 * NSK + 2 * NSV + 13;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr int OFF_W = (OFF_MISC + 16 + 127) & ~127;  // qnorm weights, D bf16
     static constexpr int SMEM_BYTES = OFF_W + D * 2;
     // + slack for 1024-byte alignment; never less than 120 KB, so that a second CTA
     // can never share the SM (each CTA allocates all 512 TMEM columns).
     static constexpr int SMEM_ALLOC = (SMEM_BYTES + 1024) > 122880 ? (SMEM_BYTES + 1024) : 122880;
-    static constexpr int THREADS = 192;
+    static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
+    static constexpr int THREADS = 224;
     static constexpr uint32_t IDESC_QK = make_idesc_bf16(128, BN, false);
     static constexpr uint32_t IDESC_PV = make_idesc_bf16(128, D, true);
     static constexpr float RESCALE_THRESHOLD = 8.0f;  // log2 domain: rescale when the max grows by > 2^8
@@ -76,19 +87,22 @@ struct PfCfg {
 
 struct Bars {
     uint32_t base;
-    int ns;
-    __device__ uint32_t k_full(int s) const { return base + 8u * s; }
-    __device__ uint32_t k_empty(int s) const { return base + 8u * (ns + s); }
-    __device__ uint32_t v_full(int s) const { return base + 8u * (2 * ns + s); }
-    __device__ uint32_t v_empty(int s) const { return base + 8u * (3 * ns + s); }
-    __device__ uint32_t s_full(int i) const { return base + 8u * (4 * ns + i); }
-    __device__ uint32_t p_full(int i) const { return base + 8u * (4 * ns + 2 + i); }
-    __device__ uint32_t o_done() const { return base + 8u * (4 * ns + 4); }
-    __device__ uint32_t o_final() const { return base + 8u * (4 * ns + 5); }
-    __device__ uint32_t q_ready() const { return base + 8u * (4 * ns + 6); }  // Q' in TMEM, raw Q no longer read
-    __device__ uint32_t drain() const { return base + 8u * (4 * ns + 7); }
-    __device__ uint32_t q_full() const { return base + 8u * (4 * ns + 8); }   // raw Q tile landed
-    __device__ uint32_t g_full() const { return base + 8u * (4 * ns + 9); }   // gate tile landed
+    int nsk, nsv;
+    __device__ uint32_t at(int i) const { return base + 8u * (uint32_t)i; }
+    __device__ uint32_t k_full(int s) const { return at(s); }
+    __device__ uint32_t k_empty(int s) const { return at(nsk + s); }
+    __device__ uint32_t v_full(int s) const { return at(2 * nsk + s); }
+    __device__ uint32_t v_empty(int s) const { return at(2 * nsk + nsv + s); }
+    __device__ int r() const { return 2 * nsk + 2 * nsv; }
+    __device__ uint32_t s_full(int i) const { return at(r() + i); }        // S of a tile in buffer i
+    __device__ uint32_t s_free(int i) const { return at(r() + 2 + i); }    // S of a tile read out of buffer i
+    __device__ uint32_t p_full(int i) const { return at(r() + 4 + i); }    // P_j ready, j % 2 == i
+    __device__ uint32_t pv_done(int i) const { return at(r() + 6 + i); }   // PV_j complete, j % 2 == i
+    __device__ uint32_t o_final() const { return at(r() + 8); }
+    __device__ uint32_t q_ready() const { return at(r() + 9); }   // Q' in TMEM, raw Q no longer read
+    __device__ uint32_t drain() const { return at(r() + 10); }
+    __device__ uint32_t q_full() const { return at(r() + 11); }   // raw Q tile landed
+    __device__ uint32_t g_full() const { return at(r() + 12); }   // gate tile landed
 };
 
 __device__ __forceinline__ uint4 lds_v4(uint32_t addr) {
@@ -125,6 +139,10 @@ __device__ void run_producer(const CUtensorMap* tmK, const CUtensorMap* tmV, con
     for (int c = 0; c < C::KCH; ++c)
         tma_load_4d(sbase + C::OFF_V + c * C::ROWBOX_BYTES, tmQ, bars.q_full(), c * 64, h, qt * C::BM, b);
 
+    // K' is written by the pre-pass kernel just before this one (programmatic
+    // dependent launch): wait for it to finish before the first K' load.
+    pdl_wait_prerequisites();
+
     // K and V tiles, each stream as soon as its own stage frees up
     int nk = 0, nv = 0;
     bool v_open = false;  // the V ring is free once the raw Q tile has been read
@@ -133,8 +151,8 @@ __device__ void run_producer(const CUtensorMap* tmK, const CUtensorMap* tmV, con
     while (nk < n_kv || nv < n_kv) {
         bool progressed = false;
         if (nk < n_kv &&
-            (nk < C::NS || mbar_try_wait(bars.k_empty(nk % C::NS), ((uint32_t)(nk / C::NS) & 1u) ^ 1u))) {
-            const int st = nk % C::NS;
+            (nk < C::NSK || mbar_try_wait(bars.k_empty(nk % C::NSK), ((uint32_t)(nk / C::NSK) & 1u) ^ 1u))) {
+            const int st = nk % C::NSK;
             mbar_arrive_expect_tx(bars.k_full(st), C::TILE_BYTES);
             const uint32_t kdst = sbase + C::OFF_K + st * C::TILE_BYTES;
 #pragma unroll
@@ -145,8 +163,8 @@ __device__ void run_producer(const CUtensorMap* tmK, const CUtensorMap* tmV, con
         }
         if (!v_open) v_open = mbar_try_wait(bars.q_ready(), 0);
         if (v_open && nv < n_kv &&
-            (nv < C::NS || mbar_try_wait(bars.v_empty(nv % C::NS), ((uint32_t)(nv / C::NS) & 1u) ^ 1u))) {
-            const int st = nv % C::NS;
+            (nv < C::NSV || mbar_try_wait(bars.v_empty(nv % C::NSV), ((uint32_t)(nv / C::NSV) & 1u) ^ 1u))) {
+            const int st = nv % C::NSV;
             mbar_arrive_expect_tx(bars.v_full(st), C::TILE_BYTES);
             const uint32_t vdst = sbase + C::OFF_V + st * C::TILE_BYTES;
 #pragma unroll
@@ -172,8 +190,8 @@ __device__ void run_producer(const CUtensorMap* tmK, const CUtensorMap* tmV, con
     bool g_issued = false;
     if (gate_tile && nk == n_kv) {
         bool ok = true;
-        for (int j = n_kv > C::NS ? n_kv - C::NS : 0; ok && j < n_kv; ++j)
-            ok = mbar_wait(bars.k_empty(j % C::NS), (uint32_t)(j / C::NS) & 1u, abort_flag, status);
+        for (int j = n_kv > C::NSK ? n_kv - C::NSK : 0; ok && j < n_kv; ++j)
+            ok = mbar_wait(bars.k_empty(j % C::NSK), (uint32_t)(j / C::NSK) & 1u, abort_flag, status);
         if (ok) {
             mbar_arrive_expect_tx(bars.g_full(), C::QTILE_BYTES);
 #pragma unroll
@@ -184,61 +202,104 @@ __device__ void run_producer(const CUtensorMap* tmK, const CUtensorMap* tmV, con
     }
     // Drain: every copy this thread started must land before the CTA can exit.
     mbar_wait_drain(bars.q_full(), 0, status);
-    for (int j = nk > C::NS ? nk - C::NS : 0; j < nk; ++j)
-        mbar_wait_drain(bars.k_full(j % C::NS), (uint32_t)(j / C::NS) & 1u, status);
-    for (int j = nv > C::NS ? nv - C::NS : 0; j < nv; ++j)
-        mbar_wait_drain(bars.v_full(j % C::NS), (uint32_t)(j / C::NS) & 1u, status);
+    for (int j = nk > C::NSK ? nk - C::NSK : 0; j < nk; ++j)
+        mbar_wait_drain(bars.k_full(j % C::NSK), (uint32_t)(j / C::NSK) & 1u, status);
+    for (int j = nv > C::NSV ? nv - C::NSV : 0; j < nv; ++j)
+        mbar_wait_drain(bars.v_full(j % C::NSV), (uint32_t)(j / C::NSV) & 1u, status);
     if (g_issued) mbar_wait_drain(bars.g_full(), 0, status);
 }
 
 // ----------------------------------------------------------------- MMA issuer
 
+// Two threads issue MMAs: a single thread can issue one tcgen05.mma only every
+// ~54 cycles whatever its size (measured on GB300), which at d = 256 (D/16 narrow
+// QK^T MMAs per 64-key tile) is slower than the tensor pipe executes them.  So
+// there is one issuer per tile parity: issuer i issues QK^T and PV of the tiles j
+// with j % 2 == i, each issuing half the MMAs; their MMAs interleave freely in the
+// pipe.  PV_j waits for PV_{j-1} to complete, so O sums the tiles in the same
+// order on every run (the result is deterministic).
 template <int D>
-__device__ void run_mma(const Bars& bars, uint32_t sbase, uint32_t tm, int n_kv, volatile int* abort_flag,
-                        unsigned int* status) {
+__device__ __forceinline__ bool issue_qk(int j, const Bars& bars, uint32_t tm, uint64_t kdesc0,
+                                         volatile int* abort_flag, unsigned int* status) {
     using C = PfCfg<D>;
-    bool ok = mbar_wait(bars.q_ready(), 0, abort_flag, status);
+    const int sb = j & 1;
+    // score buffer sb was last used by tile j-2: with P in shared memory it is free
+    // once the softmax has read S_{j-2}; with P in TMEM this issuer already issued
+    // PV_{j-2} (which reads P_{j-2} there) before this QK, and the pipe runs in order.
+    if (C::PSMEM && j >= 2 && !mbar_wait(bars.s_free(sb), (uint32_t)((j >> 1) - 1) & 1u, abort_flag, status))
+        return false;
+    const int st = j % C::NSK;
+    if (!mbar_wait(bars.k_full(st), (uint32_t)(j / C::NSK) & 1u, abort_flag, status)) return false;
     tc_fence_after();
-    // descriptors of stage 0; stage s adds s * TILE_BYTES to the start address
-    const uint64_t kdesc0 = make_sdesc_sw128(sbase + C::OFF_K, 16, 1024);
-    const uint64_t vdesc0 = make_sdesc_sw128(sbase + C::OFF_V, C::CHUNK_BYTES, 1024);
-
-    auto issue_qk = [&](int j) -> bool {
-        const int st = j % C::NS;
-        if (!mbar_wait(bars.k_full(st), (uint32_t)(j / C::NS) & 1u, abort_flag, status)) return false;
-        tc_fence_after();
-        const uint32_t d_tmem = tm + ((j & 1) ? C::TM_S1 : C::TM_S0);
-        const uint64_t kd = kdesc0 + (uint64_t)((st * C::TILE_BYTES) >> 4);
+    const uint32_t d_tmem = tm + C::TM_S + sb * C::BN;
+    const uint64_t kd = kdesc0 + (uint64_t)((st * C::TILE_BYTES) >> 4);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-            mma_ts(d_tmem, tm + C::TM_Q + kk * 8, kd + (uint64_t)(((kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32) >> 4),
-                   C::IDESC_QK, kk > 0 ? 1u : 0u);
-        tc_commit(bars.k_empty(st));
-        tc_commit(bars.s_full(j & 1));
-        return true;
-    };
+    for (int kk = 0; kk < D / 16; ++kk)
+        mma_ts(d_tmem, tm + C::TM_Q + kk * 8, kd + (uint64_t)(((kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32) >> 4),
+               C::IDESC_QK, kk > 0 ? 1u : 0u);
+    tc_commit(bars.k_empty(st));
+    tc_commit(bars.s_full(sb));
+    return true;
+}
 
-    if (ok) ok = issue_qk(0);
-    for (int j = 0; ok && j < n_kv; ++j) {
-        if (j + 1 < n_kv && !issue_qk(j + 1)) { ok = false; break; }
-        if (!mbar_wait(bars.p_full(j & 1), (uint32_t)(j >> 1) & 1u, abort_flag, status)) { ok = false; break; }
-        tc_fence_after();
-        const int st = j % C::NS;
-        if (!mbar_wait(bars.v_full(st), (uint32_t)(j / C::NS) & 1u, abort_flag, status)) { ok = false; break; }
-        tc_fence_after();
-        const uint32_t p_tmem = tm + ((j & 1) ? C::TM_S1 : C::TM_S0);
-        const uint64_t vd = vdesc0 + (uint64_t)((st * C::TILE_BYTES) >> 4);
+template <int D>
+__device__ __forceinline__ bool issue_pv(int j, const Bars& bars, uint32_t tm, uint64_t vdesc0, uint64_t pdesc0,
+                                         volatile int* abort_flag, unsigned int* status) {
+    using C = PfCfg<D>;
+    if (!mbar_wait(bars.p_full(j & 1), (uint32_t)(j >> 1) & 1u, abort_flag, status)) return false;
+    // O accumulates the PVs in tile order, run after run: PV_j starts once the
+    // other issuer's PV_{j-1} has completed (its QKs keep the pipe busy meanwhile).
+    if (j >= 1 && !mbar_wait(bars.pv_done((j - 1) & 1), (uint32_t)((j - 1) >> 1) & 1u, abort_flag, status))
+        return false;
+    tc_fence_after();
+    const int st = j % C::NSV;
+    if (!mbar_wait(bars.v_full(st), (uint32_t)(j / C::NSV) & 1u, abort_flag, status)) return false;
+    tc_fence_after();
+    const uint64_t vd = vdesc0 + (uint64_t)((st * C::TILE_BYTES) >> 4);
+    if constexpr (C::PSMEM) {
+        const uint64_t pd = pdesc0 + (uint64_t)(((j & 1) * C::P_BUF_BYTES) >> 4);
 #pragma unroll
         for (int kk = 0; kk < C::BN / 16; ++kk)
-            mma_ts(tm + C::TM_O, p_tmem + kk * 8, vd + (uint64_t)((kk * 16 * 128) >> 4), C::IDESC_PV,
-                   (j > 0 || kk > 0) ? 1u : 0u);
-        tc_commit(bars.v_empty(st));
-        tc_commit(bars.o_done());
+            mma_ss(tm + C::TM_O, pd + (uint64_t)(((kk >> 2) * (C::BM * 128) + (kk & 3) * 32) >> 4),
+                   vd + (uint64_t)((kk * 16 * 128) >> 4), C::IDESC_PV, 1u);
+    } else {
+        const uint32_t p_tmem = tm + C::TM_S + (j & 1) * C::BN;
+#pragma unroll
+        for (int kk = 0; kk < C::BN / 16; ++kk)
+            mma_ts(tm + C::TM_O, p_tmem + kk * 8, vd + (uint64_t)((kk * 16 * 128) >> 4), C::IDESC_PV, 1u);
     }
-    if (ok) tc_commit(bars.o_final());
-    // Whatever happened, no MMA may still be in flight when TMEM is released.
+    tc_commit(bars.v_empty(st));
+    tc_commit(bars.pv_done(j & 1));
+    return true;
+}
+
+template <int D>
+__device__ void run_mma(int parity, const Bars& bars, uint32_t sbase, uint32_t tm, int n_kv,
+                        volatile int* abort_flag, unsigned int* status) {
+    using C = PfCfg<D>;
+    bool ok = mbar_wait(bars.q_ready(), 0, abort_flag, status);  // Q' in TMEM, O zeroed
+    tc_fence_after();
+    const uint64_t kdesc0 = make_sdesc_sw128(sbase + C::OFF_K, 16, 1024);
+    const uint64_t vdesc0 = make_sdesc_sw128(sbase + C::OFF_V, C::CHUNK_BYTES, 1024);
+    const uint64_t pdesc0 = make_sdesc_sw128(sbase + C::OFF_P, 16, 1024);
+    if (C::PSMEM) {
+        // QK of the next own tile goes out as soon as its score buffer is free,
+        // ahead of the PV that is still waiting for its P.
+        if (ok && parity < n_kv) ok = issue_qk<D>(parity, bars, tm, kdesc0, abort_flag, status);
+        for (int j = parity; ok && j < n_kv; j += 2) {
+            if (j + 2 < n_kv && !issue_qk<D>(j + 2, bars, tm, kdesc0, abort_flag, status)) { ok = false; break; }
+            if (!issue_pv<D>(j, bars, tm, vdesc0, pdesc0, abort_flag, status)) { ok = false; break; }
+        }
+    } else {
+        // P_j lives in score buffer j%2: PV_j must be issued before QK_{j+2} overwrites it.
+        if (ok && parity < n_kv) ok = issue_qk<D>(parity, bars, tm, kdesc0, abort_flag, status);
+        for (int j = parity; ok && j < n_kv; j += 2) {
+            if (!issue_pv<D>(j, bars, tm, vdesc0, pdesc0, abort_flag, status)) { ok = false; break; }
+            if (j + 2 < n_kv && !issue_qk<D>(j + 2, bars, tm, kdesc0, abort_flag, status)) { ok = false; break; }
+        }
+    }
+    if (ok) tc_commit(bars.o_final());  // count 2: both issuers' PVs complete
     tc_commit(bars.drain());
-    mbar_wait_drain(bars.drain(), 0, status);
 }
 
 // ----------------------------------------------------------------- softmax / prologue / epilogue
@@ -285,8 +346,8 @@ __device__ void run_softmax(const PrefillParams& p, const Bars& bars, uint32_t s
 #pragma unroll
             for (int e = 0; e < 8; e += 2) {
                 float s0, c0, s1, c1;
-                sincosf(posf * p.inv_freq[i0 + e], &s0, &c0);
-                sincosf(posf * p.inv_freq[i0 + e + 1], &s1, &c1);
+                rope_sincos(posf * p.inv_freq[i0 + e], &s0, &c0);
+                rope_sincos(posf * p.inv_freq[i0 + e + 1], &s1, &c1);
                 const float a0 = xa[e] * wa[e], b0 = xb[e] * wb[e];
                 const float a1 = xa[e + 1] * wa[e + 1], b1 = xb[e + 1] * wb[e + 1];
                 lo[e >> 1] = pack_bf16x2((a0 * c0 - b0 * s0) * rinv, (a1 * c1 - b1 * s1) * rinv);
@@ -306,6 +367,14 @@ __device__ void run_softmax(const PrefillParams& p, const Bars& bars, uint32_t s
                      pack_bf16x2(x[4] * w[4] * rinv, x[5] * w[5] * rinv),
                      pack_bf16x2(x[6] * w[6] * rinv, x[7] * w[7] * rinv));
         }
+        // O starts at zero and every PV accumulates into it
+        {
+            uint32_t z[32];
+#pragma unroll
+            for (int e = 0; e < 32; ++e) z[e] = 0u;
+#pragma unroll
+            for (int c = 0; c < D; c += 32) tmem_st32(tl + C::TM_O + c, z);
+        }
         fence_proxy_async_smem();  // our reads of the V ring happen before the V tiles overwrite it
         tmem_wait_st();
         tc_fence_before();
@@ -319,9 +388,9 @@ __device__ void run_softmax(const PrefillParams& p, const Bars& bars, uint32_t s
     float m_ref = -INFINITY;  // reference max (log2 domain) shared by O and l
     float l = 0.f;
     for (int j = 0; j < n_kv; ++j) {
-        const int sb = j & 1;
-        const uint32_t s_col = sb ? C::TM_S1 : C::TM_S0;
-        if (!__all_sync(0xffffffffu, mbar_wait(bars.s_full(sb), (uint32_t)(j >> 1) & 1u, abort_flag, p.status)))
+        const int sb = j % C::NSB;
+        const uint32_t s_col = C::TM_S + sb * C::BN;
+        if (!__all_sync(0xffffffffu, mbar_wait(bars.s_full(sb), (uint32_t)(j / C::NSB) & 1u, abort_flag, p.status)))
             return;
         tc_fence_after();
         float s[C::BN];
@@ -333,6 +402,11 @@ __device__ void run_softmax(const PrefillParams& p, const Bars& bars, uint32_t s
 #pragma unroll
                 for (int e = 0; e < 64; ++e) s[c + e] = __uint_as_float(r[e]);
             }
+        }
+        if constexpr (C::PSMEM) {  // S_j is in registers: its buffer may take the next tile's scores
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bars.s_free(sb));
         }
         const int key0 = j * C::BN;
         if (key0 + C::BN - 1 > row_min) {
@@ -358,8 +432,13 @@ __device__ void run_softmax(const PrefillParams& p, const Bars& bars, uint32_t s
                 m_ref = m_new;
             }
             __syncwarp();
-            // O is only touched once the previous P V has landed.
-            if (!__all_sync(0xffffffffu, mbar_wait(bars.o_done(), (uint32_t)(j - 1) & 1u, abort_flag, p.status)))
+            // O is only touched once every earlier P V has landed (the two issuers'
+            // PVs may complete in either order).
+            if (!__all_sync(0xffffffffu, mbar_wait(bars.pv_done((j - 1) & 1), (uint32_t)((j - 1) >> 1) & 1u,
+                                                   abort_flag, p.status)))
+                return;
+            if (j >= 2 && !__all_sync(0xffffffffu, mbar_wait(bars.pv_done(j & 1), (uint32_t)((j - 2) >> 1) & 1u,
+                                                              abort_flag, p.status)))
                 return;
             tc_fence_after();
 #pragma unroll 1
@@ -371,26 +450,56 @@ __device__ void run_softmax(const PrefillParams& p, const Bars& bars, uint32_t s
                 tmem_st32(tl + C::TM_O + c, r);
             }
         }
-        // P = exp2(s * scale * log2e - m_ref), packed bf16, written over S in TMEM
+        // P = exp2(s * scale * log2e - m_ref), packed bf16: written over S in TMEM, or
+        // (PSMEM) as this thread's 128-byte-swizzled row of P buffer j%2.
         float rs[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
         const float mref = m_ref;
+        if constexpr (C::PSMEM) {
+            // P buffer j%2 held P_{j-2}: PV_{j-2} must have finished reading it
+            if (j >= 2 && !__all_sync(0xffffffffu, mbar_wait(bars.pv_done(j & 1), (uint32_t)((j - 2) >> 1) & 1u,
+                                                              abort_flag, p.status)))
+                return;
+            const uint32_t pbase = sbase + C::OFF_P + (j & 1) * C::P_BUF_BYTES;
 #pragma unroll
-        for (int c = 0; c < C::BN; c += 64) {
-            uint32_t pk[32];
+            for (int c8 = 0; c8 < C::BN / 8; ++c8) {
+                uint32_t pk[4];
 #pragma unroll
-            for (int e = 0; e < 32; ++e) {
-                const float p0 = ex2_approx(fmaf(s[c + 2 * e], sl2, -mref));
-                const float p1 = ex2_approx(fmaf(s[c + 2 * e + 1], sl2, -mref));
-                rs[e & 7] += p0 + p1;
-                pk[e] = pack_bf16x2(p0, p1);
+                for (int e = 0; e < 4; ++e) {
+                    const float p0 = ex2_approx(fmaf(s[8 * c8 + 2 * e], sl2, -mref));
+                    const float p1 = ex2_approx(fmaf(s[8 * c8 + 2 * e + 1], sl2, -mref));
+                    rs[(2 * c8 + (e >> 1)) & 7] += p0 + p1;
+                    pk[e] = pack_bf16x2(p0, p1);
+                }
+                const uint32_t addr = pbase + (uint32_t)(c8 >> 3) * (C::BM * 128) + sw128_offset(row, c8 & 7);
+                asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(pk[0]), "r"(pk[1]), "r"(pk[2]),
+                             "r"(pk[3])
+                             : "memory");
             }
-            tmem_st32(tl + s_col + (c >> 1), pk);
+            l += ((rs[0] + rs[1]) + (rs[2] + rs[3])) + ((rs[4] + rs[5]) + (rs[6] + rs[7]));
+            fence_proxy_async_smem();  // the tensor core reads P through the async proxy
+            tmem_wait_st();            // an O rescale above, if any, has landed
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bars.p_full(j & 1));
+        } else {
+#pragma unroll
+            for (int c = 0; c < C::BN; c += 64) {
+                uint32_t pk[32];
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                    const float p0 = ex2_approx(fmaf(s[c + 2 * e], sl2, -mref));
+                    const float p1 = ex2_approx(fmaf(s[c + 2 * e + 1], sl2, -mref));
+                    rs[e & 7] += p0 + p1;
+                    pk[e] = pack_bf16x2(p0, p1);
+                }
+                tmem_st32(tl + s_col + (c >> 1), pk);
+            }
+            l += ((rs[0] + rs[1]) + (rs[2] + rs[3])) + ((rs[4] + rs[5]) + (rs[6] + rs[7]));
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bars.p_full(j & 1));
         }
-        l += ((rs[0] + rs[1]) + (rs[2] + rs[3])) + ((rs[4] + rs[5]) + (rs[6] + rs[7]));
-        tmem_wait_st();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bars.p_full(sb));
     }
 
     // ---- epilogue: O / l * sigmoid(gate) -> bf16 [B,S,H*d]
@@ -446,7 +555,7 @@ __global__ void __launch_bounds__(PfCfg<D>::THREADS, 1)
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const Bars bars{sbase + C::OFF_BAR, C::NS};
+    const Bars bars{sbase + C::OFF_BAR, C::NSK, C::NSV};
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
 
@@ -459,20 +568,23 @@ __global__ void __launch_bounds__(PfCfg<D>::THREADS, 1)
     const int n_kv = (q_end + C::BN - 1) / C::BN;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < C::NS; ++s) {
+        for (int s = 0; s < C::NSK; ++s) {
             mbar_init(bars.k_full(s), 1);
             mbar_init(bars.k_empty(s), 1);
+        }
+        for (int s = 0; s < C::NSV; ++s) {
             mbar_init(bars.v_full(s), 1);
             mbar_init(bars.v_empty(s), 1);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(bars.s_full(i), 1);
+            mbar_init(bars.s_free(i), 4);
             mbar_init(bars.p_full(i), 4);
+            mbar_init(bars.pv_done(i), 1);
         }
-        mbar_init(bars.o_done(), 1);
-        mbar_init(bars.o_final(), 1);
+        mbar_init(bars.o_final(), 2);
         mbar_init(bars.q_ready(), 4);
-        mbar_init(bars.drain(), 1);
+        mbar_init(bars.drain(), 2);
         mbar_init(bars.q_full(), 1);
         mbar_init(bars.g_full(), 1);
         *abort_flag = 0;
@@ -498,7 +610,14 @@ __global__ void __launch_bounds__(PfCfg<D>::THREADS, 1)
                             p.gate_mode == GATTN_GATE_ELEMENTWISE, abort_flag, p.status);
         __syncwarp();
     } else if (warp == 1) {
-        if (lane == 0) run_mma<D>(bars, sbase, tm, n_kv, abort_flag, p.status);
+        if (lane == 0) run_mma<D>(0, bars, sbase, tm, n_kv, abort_flag, p.status);
+        __syncwarp();
+    } else if (warp == 2) {
+        if (lane == 0) {
+            run_mma<D>(1, bars, sbase, tm, n_kv, abort_flag, p.status);
+            // Whatever happened, no MMA of either issuer may still be in flight when TMEM is released.
+            mbar_wait_drain(bars.drain(), 0, p.status);
+        }
         __syncwarp();
     } else {
         run_softmax<D>(p, bars, sbase, tm, warp & 3, lane, qt, b, h, n_kv, abort_flag);
@@ -521,9 +640,17 @@ cudaError_t launch_d(const PrefillParams& p, const PrefillMaps& maps, cudaStream
     const long long blocks = (long long)p.n_qtiles * p.B * p.H;
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
     if (ev_start) cudaEventRecord(ev_start, stream);
-    prefill_tc_kernel<D><<<(unsigned)blocks, C::THREADS, C::SMEM_ALLOC, stream>>>(maps.k, maps.v, maps.q, maps.gate,
-                                                                                    p);
-    cudaError_t err = cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)blocks);
+    cfg.blockDim = dim3(C::THREADS);
+    cfg.dynamicSmemBytes = C::SMEM_ALLOC;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t err = cudaLaunchKernelEx(&cfg, prefill_tc_kernel<D>, maps.k, maps.v, maps.q, maps.gate, p);
     if (ev_stop) cudaEventRecord(ev_stop, stream);
     return err;
 }

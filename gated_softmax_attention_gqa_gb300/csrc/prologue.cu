@@ -31,6 +31,7 @@ constexpr int kWarpsPerBlock = 8;
 template <typename Tin, typename Tout>
 __global__ void __launch_bounds__(kWarpsPerBlock * 32) qk_prologue_kernel(const __grid_constant__ ProloguePlan p) {
     extern __shared__ float rows[];
+    pdl_launch_dependents();  // the attention kernel may start its own prologue now
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t r = (int64_t)blockIdx.x * kWarpsPerBlock + warp;
     const int64_t n_rows = (int64_t)p.B * p.S * p.n_heads;
@@ -63,12 +64,12 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) qk_prologue_kernel(const 
         float y = row[e];
         if (e < half) {
             float s, c;
-            sincosf(posf * p.inv_freq[e], &s, &c);
+            rope_sincos(posf * p.inv_freq[e], &s, &c);
             y = row[e] * c - row[e + half] * s;
         } else if (e < p.rd) {
             const int i = e - half;
             float s, c;
-            sincosf(posf * p.inv_freq[i], &s, &c);
+            rope_sincos(posf * p.inv_freq[i], &s, &c);
             y = row[e] * c + row[i] * s;
         }
         dst[e] = from_f<Tout>(y);

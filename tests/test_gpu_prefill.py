@@ -165,3 +165,32 @@ def test_gqa_equals_mha_with_replicated_kv():
     b = run_gpu(inp_m, small("mha", B, S, H, H, d, 64, 1e6, "elementwise"))
     torch.cuda.synchronize()
     assert torch.equal(a, b)
+
+
+def test_rope_rotation_error_bound_at_long_positions():
+    """The rotated keys the pre-pass leaves in the workspace (fp32 path) against a
+    fp64 rotation by the same fp32 angle pos * inv_freq: checks the kernels' own
+    sine/cosine range reduction to ~1e-5 for angles up to 32k rad."""
+    B, S, H, G, d, rd, base = 1, 96, 2, 2, 128, 128, 1e4
+    w = small("rope", B, S, H, G, d, rd, base, "none", dtype="fp32", seed=12)
+    inp = make_prefill_inputs(w)
+    pos = torch.randint(0, 32768, (B, S), generator=torch.Generator().manual_seed(3), dtype=torch.int32)
+    pos[0, :4] = torch.tensor([0, 1, 32767, 31416], dtype=torch.int32)
+    from gated_softmax_attention_gqa_gb300 import gattn_prefill_workspace_size
+
+    ws = torch.zeros(gattn_prefill_workspace_size(B, S, H, G, d, torch.float32), dtype=torch.uint8, device=DEV)
+    dev = {k: v.to(DEV) for k, v in inp.items()}
+    gattn_prefill(dev["q"], dev["k"], dev["v"], None, dev["qnorm_w"], dev["knorm_w"], pos.to(DEV), rotary_dim=rd,
+                  rope_base=base, eps=w.eps, gate_mode="none", workspace=ws)
+    torch.cuda.synchronize()
+    q_bytes = ((B * H * S * d * 4 + 255) // 256) * 256
+    kr = ws[q_bytes:q_bytes + B * G * S * d * 4].view(torch.float32).view(B, G, S, d).double().cpu().numpy()
+    kn = oracle.rmsnorm(inp["k"], inp["knorm_w"], w.eps)  # [B,S,G,d] fp64
+    half = rd // 2
+    inv = (base ** (-2.0 * np.arange(half) / rd)).astype(np.float32)
+    ang = (pos.numpy().astype(np.float32)[..., None] * inv[None, None, :]).astype(np.float64)  # fp32 product
+    c, s = np.cos(ang)[:, :, None, :], np.sin(ang)[:, :, None, :]
+    a, b_ = kn[..., :half], kn[..., half:rd]
+    ref = np.concatenate([a * c - b_ * s, b_ * c + a * s, kn[..., rd:]], axis=-1).transpose(0, 2, 1, 3)
+    err = np.abs(kr - ref)
+    assert err.max() < 2e-5, err.max()
