@@ -292,17 +292,26 @@ def main():
         dist.barrier()
     torch.cuda.synchronize()
     sampler.mark_start()
+    # Timed region 1: the calls exactly as a user makes them (the headline numbers).
     for i in range(K):
         flush.zero_()
-        ga.gattn_set_profile_events(*evs["pk"][i])
         evs["p"][i][0].record(stream)
         prefill()
         evs["p"][i][1].record(stream)
         flush.zero_()
-        ga.gattn_set_profile_events(*evs["dk"][i])
         evs["d"][i][0].record(stream)
         decode()
         evs["d"][i][1].record(stream)
+    # Timed region 2: the same calls with the library recording events around its
+    # main attention kernel (the roofline numbers).  Kept separate because an event
+    # between the K pre-pass and the attention kernel stops them from overlapping.
+    for i in range(K):
+        flush.zero_()
+        ga.gattn_set_profile_events(*evs["pk"][i])
+        prefill()
+        flush.zero_()
+        ga.gattn_set_profile_events(*evs["dk"][i])
+        decode()
     torch.cuda.synchronize()
     sampler.mark_end()
     if world > 1:
@@ -379,7 +388,7 @@ def main():
                                     "traffic": profiled_traffic("decode_split_qwen35_08b.md", dec_src)}},
             "e2e": {"value": e2e_val, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "ms_per_step": e2e_ms},
-            "gpu_launches": 4 * K,
+            "gpu_launches": 8 * K,
             "clocks": clocks,
             "device_status": status,
         }

@@ -48,9 +48,12 @@ unsigned int* status_ptr() {
 }
 
 int sm_count() {
+    static int cached[64] = {};
     int dev = 0, n = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (dev >= 0 && dev < 64 && cached[dev] > 0) return cached[dev];
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    if (dev >= 0 && dev < 64) cached[dev] = n;
     return n;
 }
 
@@ -63,9 +66,57 @@ void fill_inv_freq(float* dst, int rd, double base) {
         dst[i] = (i < rd / 2) ? (float)std::pow(base, -2.0 * (double)i / (double)rd) : 0.f;
 }
 
+// Recently encoded tensor maps, so that repeated calls on the same buffers skip
+// the host-side encoding.  A map depends only on the arguments below.
+struct MapKey {
+    const void* base;
+    int rank;
+    uint64_t dims[5], strides[4];
+    uint32_t box[5];
+    bool operator==(const MapKey& o) const { return std::memcmp(this, &o, sizeof(MapKey)) == 0; }
+};
+struct MapCache {
+    static constexpr int kEntries = 16;
+    MapKey key[kEntries];
+    CUtensorMap map[kEntries];
+    bool used[kEntries] = {};
+    int next = 0;
+    std::mutex mu;
+};
+MapCache g_maps;
+
+bool encode_bf16_map_uncached(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
+                              const uint64_t* strides_bytes, const uint32_t* box);
+
 // bf16 tensor map with a 64-element (128 B) inner box and 128 B swizzle.
 bool encode_bf16_map(CUtensorMap* map, const void* base, int rank, const uint64_t* dims, const uint64_t* strides_bytes,
                      const uint32_t* box) {
+    MapKey k;
+    std::memset(&k, 0, sizeof(k));
+    k.base = base;
+    k.rank = rank;
+    for (int i = 0; i < rank; ++i) {
+        k.dims[i] = dims[i];
+        k.box[i] = box[i];
+        if (i + 1 < rank) k.strides[i] = strides_bytes[i];
+    }
+    std::lock_guard<std::mutex> lock(g_maps.mu);
+    for (int i = 0; i < MapCache::kEntries; ++i)
+        if (g_maps.used[i] && g_maps.key[i] == k) {
+            *map = g_maps.map[i];
+            return true;
+        }
+    if (!encode_bf16_map_uncached(map, base, rank, dims, strides_bytes, box)) return false;
+    const int slot = g_maps.next;
+    g_maps.next = (slot + 1) % MapCache::kEntries;
+    g_maps.key[slot] = k;
+    g_maps.map[slot] = *map;
+    g_maps.used[slot] = true;
+    return true;
+}
+
+bool encode_bf16_map_uncached(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
+                              const uint64_t* strides_bytes, const uint32_t* box) {
     auto fn = get_encode_fn();
     if (!fn) return false;
     cuuint32_t elem_strides[5] = {1, 1, 1, 1, 1};

@@ -75,6 +75,26 @@ __device__ __forceinline__ void rope_sincos(float x, float* s, float* c) {
     *c = __cosf(r);
 }
 
+// Raise a kernel's dynamic shared-memory limit once per device (host side).
+// `func` identifies the kernel; up to 8 kernels per device are remembered.
+inline cudaError_t set_smem_once(const void* func, int bytes) {
+    static const void* seen[64][8] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64)
+        for (int i = 0; i < 8; ++i)
+            if (seen[dev][i] == func) return cudaSuccess;
+    e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e != cudaSuccess || dev < 0 || dev >= 64) return e;
+    for (int i = 0; i < 8; ++i)
+        if (!seen[dev][i]) {
+            seen[dev][i] = func;
+            break;
+        }
+    return cudaSuccess;
+}
+
 // ------------------------------------------------------------------ mbarrier
 
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
@@ -354,6 +374,29 @@ __device__ __forceinline__ void mma_bf16_16816(float (&c)[4], uint32_t a0, uint3
 // 128-byte rows written by TMA with 128-byte swizzle.
 __device__ __forceinline__ uint32_t sw128_offset(uint32_t row, uint32_t chunk) {
     return row * 128u + ((chunk ^ (row & 7u)) << 4);
+}
+
+__device__ __forceinline__ uint4 lds_v4(uint32_t addr) {
+    uint4 r;
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "r"(addr));
+    return r;
+}
+
+__device__ __forceinline__ void sts_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
+__device__ __forceinline__ void unpack8(const uint4& v, float (&f)[8]) {
+    f[0] = bf16_lo(v.x); f[1] = bf16_hi(v.x);
+    f[2] = bf16_lo(v.y); f[3] = bf16_hi(v.y);
+    f[4] = bf16_lo(v.z); f[5] = bf16_hi(v.z);
+    f[6] = bf16_lo(v.w); f[7] = bf16_hi(v.w);
+}
+
+// Shared-memory address of elements e0..e0+7 of row `row` in a tile stored as
+// 128-byte-swizzled TMA boxes of [128 rows x 64 bf16].
+__device__ __forceinline__ uint32_t rowtile_addr(uint32_t base, int row, int e0) {
+    return base + (uint32_t)(e0 >> 6) * (128u * 128u) + sw128_offset((uint32_t)row, (uint32_t)((e0 >> 3) & 7));
 }
 
 }  // namespace gattn

@@ -338,10 +338,16 @@ __global__ void __launch_bounds__(DecCfg<D>::THREADS, 1)
     __syncthreads();
 }
 
-// Merge the partial states of one (sequence, group) and apply the gate.
+// Merge the partial states of one (sequence, group) and apply the gate.  The
+// CTAs whose tile ranges overlap this (sequence, group) each left one partial
+// state per consumer warp; their (max, sum) pairs are first turned into merge
+// weights w_s = 2^(m_s - max_s m_s) in shared memory, then every output element is
+// sum_s w_s O_s / sum_s w_s l_s -- independent, coalesced loads across the slots.
 template <int D>
 __global__ void __launch_bounds__(256) decode_combine_kernel(const __grid_constant__ DecodeParams p) {
+    extern __shared__ float cw[];  // [n_slots][r] merge weights
     __shared__ int red[2][8];
+    __shared__ float den[8];
     const int b = blockIdx.x / p.G, g = blockIdx.x % p.G;
     const int r = p.H / p.G;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -379,27 +385,47 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(const __grid_consta
         const int64_t c = ((x + 1) * N - 1) / T;
         return c < N - 1 ? c : N - 1;
     };
-    const int64_t c_first = cmax(u0), c_last = cmax(u1);
+    const int64_t c_first = cmax(u0);
+    const int n_c = (int)(cmax(u1) - c_first + 1);
+    const int n_slots = n_c * NCW;
     const int64_t seg = (int64_t)b * p.G + g;
     const int slot_floats = 2 * r + r * D;
+    const float* part0 = p.part + (c_first + seg) * NCW * (int64_t)slot_floats;  // slot s at part0 + s*slot_floats
+
+    // 1. each slot's max, or -inf when its CTA covered no tile of this (sequence, group)
+    for (int i = tid; i < n_slots * r; i += blockDim.x) {
+        const int sl = i / r, hl = i % r;
+        const int64_t c = c_first + sl / NCW;
+        const int64_t s0 = c * T / N, s1 = (c + 1) * T / N;
+        const bool covers = s0 < s1 && s0 <= u1 && s1 > u0;
+        cw[i] = covers ? part0[(int64_t)sl * slot_floats + hl] : -INFINITY;
+    }
+    __syncthreads();
+    // 2. one warp per head: the common max, the weights and the merged sum
+    if (warp < r) {
+        float mx = -INFINITY;
+        for (int sl = lane; sl < n_slots; sl += 32) mx = fmaxf(mx, cw[sl * r + warp]);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        float dsum = 0.f;
+        for (int sl = lane; sl < n_slots; sl += 32) {
+            const float m = cw[sl * r + warp];
+            const float wgt = m == -INFINITY ? 0.f : ex2_approx(m - mx);
+            cw[sl * r + warp] = wgt;
+            if (wgt != 0.f) dsum += wgt * part0[(int64_t)sl * slot_floats + r + warp];
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) dsum += __shfl_xor_sync(0xffffffffu, dsum, o);
+        if (lane == 0) den[warp] = dsum;
+    }
+    __syncthreads();
+    // 3. outputs: o = sum_s w_s O_s / sum_s w_s l_s, times the gate
     for (int idx = tid; idx < r * D; idx += blockDim.x) {
         const int hl = idx / D, e = idx % D;
-        float mstar = -INFINITY;
-        for (int64_t c = c_first; c <= c_last; ++c) {
-            const int64_t s0 = c * T / N, s1 = (c + 1) * T / N;
-            if (s0 >= s1 || s0 > u1 || s1 <= u0) continue;
-            for (int w = 0; w < NCW; ++w) mstar = fmaxf(mstar, p.part[((c + seg) * NCW + w) * slot_floats + hl]);
-        }
-        float num = 0.f, den = 0.f;
-        for (int64_t c = c_first; c <= c_last; ++c) {
-            const int64_t s0 = c * T / N, s1 = (c + 1) * T / N;
-            if (s0 >= s1 || s0 > u1 || s1 <= u0) continue;
-            for (int w = 0; w < NCW; ++w) {
-                const float* ps = p.part + ((c + seg) * NCW + w) * slot_floats;
-                const float wgt = ex2_approx(ps[hl] - mstar);
-                num += wgt * ps[2 * r + hl * D + e];
-                den += wgt * ps[r + hl];
-            }
+        float num = 0.f;
+        for (int sl = 0; sl < n_slots; ++sl) {
+            const float wgt = cw[sl * r + hl];
+            if (wgt != 0.f) num += wgt * part0[(int64_t)sl * slot_floats + 2 * r + hl * D + e];
         }
         const int h = g * r + hl;
         float gv = 1.f;
@@ -407,7 +433,7 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(const __grid_consta
             gv = sigmoidf_dev(__bfloat162float(static_cast<const bf16*>(p.gate)[((int64_t)b * p.H + h) * D + e]));
         else if (p.gate_mode == GATTN_GATE_HEADWISE)
             gv = sigmoidf_dev(__bfloat162float(static_cast<const bf16*>(p.gate)[(int64_t)b * p.H + h]));
-        static_cast<bf16*>(p.out)[((int64_t)b * p.H + h) * D + e] = __float2bfloat16_rn(num / den * gv);
+        static_cast<bf16*>(p.out)[((int64_t)b * p.H + h) * D + e] = __float2bfloat16_rn(num / den[hl] * gv);
     }
 }
 
@@ -415,15 +441,20 @@ template <int D>
 cudaError_t launch_dec(const DecodeParams& p, const CUtensorMap& tm, cudaStream_t stream, cudaEvent_t ev_start,
                        cudaEvent_t ev_stop) {
     using C = DecCfg<D>;
-    cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         C::SMEM_ALLOC);
+    cudaError_t e = set_smem_once(reinterpret_cast<const void*>(decode_split_kernel<D>), C::SMEM_ALLOC);
     if (e != cudaSuccess) return e;
     if (ev_start) cudaEventRecord(ev_start, stream);
     decode_split_kernel<D><<<p.n_ctas, C::THREADS, C::SMEM_ALLOC, stream>>>(tm, p);
     e = cudaGetLastError();
     if (ev_stop) cudaEventRecord(ev_stop, stream);
     if (e != cudaSuccess) return e;
-    decode_combine_kernel<D><<<p.B * p.G, 256, 0, stream>>>(p);
+    // merge weights: at most (n_ctas + 1) CTAs cover one (sequence, group)
+    const size_t cw_bytes = (size_t)(p.n_ctas + 1) * NCW * (p.H / p.G) * sizeof(float);
+    if (cw_bytes > 48 * 1024) {
+        e = cudaFuncSetAttribute(decode_combine_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)cw_bytes);
+        if (e != cudaSuccess) return e;
+    }
+    decode_combine_kernel<D><<<p.B * p.G, 256, cw_bytes, stream>>>(p);
     return cudaGetLastError();
 }
 

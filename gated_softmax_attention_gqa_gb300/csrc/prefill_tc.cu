@@ -105,25 +105,6 @@ struct Bars {
     __device__ uint32_t g_full() const { return at(r() + 12); }   // gate tile landed
 };
 
-__device__ __forceinline__ uint4 lds_v4(uint32_t addr) {
-    uint4 r;
-    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "r"(addr));
-    return r;
-}
-
-__device__ __forceinline__ void unpack8(const uint4& v, float (&f)[8]) {
-    f[0] = bf16_lo(v.x); f[1] = bf16_hi(v.x);
-    f[2] = bf16_lo(v.y); f[3] = bf16_hi(v.y);
-    f[4] = bf16_lo(v.z); f[5] = bf16_hi(v.z);
-    f[6] = bf16_lo(v.w); f[7] = bf16_hi(v.w);
-}
-
-// Shared-memory address of elements e0..e0+7 of row `row` in a tile stored as
-// 128-byte-swizzled TMA boxes of [128 rows x 64 bf16].
-__device__ __forceinline__ uint32_t rowtile_addr(uint32_t base, int row, int e0) {
-    return base + (uint32_t)(e0 >> 6) * (128u * 128u) + sw128_offset((uint32_t)row, (uint32_t)((e0 >> 3) & 7));
-}
-
 // ----------------------------------------------------------------- producer
 
 template <int D>
@@ -634,8 +615,7 @@ template <int D>
 cudaError_t launch_d(const PrefillParams& p, const PrefillMaps& maps, cudaStream_t stream, cudaEvent_t ev_start,
                      cudaEvent_t ev_stop) {
     using C = PfCfg<D>;
-    cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         C::SMEM_ALLOC);
+    cudaError_t e = set_smem_once(reinterpret_cast<const void*>(prefill_tc_kernel<D>), C::SMEM_ALLOC);
     if (e != cudaSuccess) return e;
     const long long blocks = (long long)p.n_qtiles * p.B * p.H;
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
