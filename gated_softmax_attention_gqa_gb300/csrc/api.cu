@@ -217,6 +217,7 @@ gattn_status gattn_prefill(const void* q, const void* k, const void* v, const vo
     kp.d = d;
     kp.rd = rotary_dim;
     kp.eps = eps;
+    kp.status = status;
     fill_inv_freq(kp.inv_freq, rotary_dim, rope_base);
 
     if (bf) {

@@ -76,18 +76,19 @@ __device__ __forceinline__ void rope_sincos(float x, float* s, float* c) {
 }
 
 // Raise a kernel's dynamic shared-memory limit once per device (host side).
-// `func` identifies the kernel; up to 8 kernels per device are remembered.
+// `func` identifies the kernel; up to 16 kernels per device are remembered
+// (beyond that the attribute is simply set again on every call).
 inline cudaError_t set_smem_once(const void* func, int bytes) {
-    static const void* seen[64][8] = {};
+    static const void* seen[64][16] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64)
-        for (int i = 0; i < 8; ++i)
+        for (int i = 0; i < 16; ++i)
             if (seen[dev][i] == func) return cudaSuccess;
     e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
     if (e != cudaSuccess || dev < 0 || dev >= 64) return e;
-    for (int i = 0; i < 8; ++i)
+    for (int i = 0; i < 16; ++i)
         if (!seen[dev][i]) {
             seen[dev][i] = func;
             break;

@@ -30,6 +30,7 @@ namespace {
 constexpr int BT = kDecodeTileKeys;  // keys per tile
 constexpr int NCW = kDecodeConsumerWarps;
 constexpr int MAXB = 2048;           // sequences per call
+constexpr int kCombineThreads = 512;
 
 template <int D>
 struct DecCfg {
@@ -111,6 +112,7 @@ __global__ void __launch_bounds__(DecCfg<D>::THREADS, 1)
     int* pb = reinterpret_cast<int*>(smem + C::OFF_PB);
     const uint32_t bar_full = sbase + C::OFF_BAR, bar_empty = bar_full + 8 * C::NS;
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC);
+    pdl_launch_dependents();  // the combine kernel may become resident; it waits for this grid to finish
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::NS; ++s) {
@@ -344,9 +346,9 @@ __global__ void __launch_bounds__(DecCfg<D>::THREADS, 1)
 // weights w_s = 2^(m_s - max_s m_s) in shared memory, then every output element is
 // sum_s w_s O_s / sum_s w_s l_s -- independent, coalesced loads across the slots.
 template <int D>
-__global__ void __launch_bounds__(256) decode_combine_kernel(const __grid_constant__ DecodeParams p) {
+__global__ void __launch_bounds__(kCombineThreads) decode_combine_kernel(const __grid_constant__ DecodeParams p) {
     extern __shared__ float cw[];  // [n_slots][r] merge weights
-    __shared__ int red[2][8];
+    __shared__ int red[2][kCombineThreads / 32];
     __shared__ float den[8];
     const int b = blockIdx.x / p.G, g = blockIdx.x % p.G;
     const int r = p.H / p.G;
@@ -392,6 +394,8 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(const __grid_consta
     const int slot_floats = 2 * r + r * D;
     const float* part0 = p.part + (c_first + seg) * NCW * (int64_t)slot_floats;  // slot s at part0 + s*slot_floats
 
+    // everything above reads only the inputs; the partial states come from the split kernel
+    pdl_wait_prerequisites();
     // 1. each slot's max, or -inf when its CTA covered no tile of this (sequence, group)
     for (int i = tid; i < n_slots * r; i += blockDim.x) {
         const int sl = i / r, hl = i % r;
@@ -412,27 +416,40 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(const __grid_consta
             const float m = cw[sl * r + warp];
             const float wgt = m == -INFINITY ? 0.f : ex2_approx(m - mx);
             cw[sl * r + warp] = wgt;
-            if (wgt != 0.f) dsum += wgt * part0[(int64_t)sl * slot_floats + r + warp];
+            const float l = part0[(int64_t)sl * slot_floats + r + warp];
+            dsum += wgt != 0.f ? wgt * l : 0.f;
         }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) dsum += __shfl_xor_sync(0xffffffffu, dsum, o);
         if (lane == 0) den[warp] = dsum;
     }
     __syncthreads();
-    // 3. outputs: o = sum_s w_s O_s / sum_s w_s l_s, times the gate
+    // 3. outputs: o = sum_s w_s O_s / sum_s w_s l_s, times the gate.  The slots are
+    // read eight at a time with no branch between the loads, so they are in flight
+    // together; a slot with weight 0 (its CTA covered none of this sequence) may
+    // hold stale data and is dropped by a select, never multiplied.
+    constexpr int CH = 8;
     for (int idx = tid; idx < r * D; idx += blockDim.x) {
         const int hl = idx / D, e = idx % D;
-        float num = 0.f;
-        for (int sl = 0; sl < n_slots; ++sl) {
-            const float wgt = cw[sl * r + hl];
-            if (wgt != 0.f) num += wgt * part0[(int64_t)sl * slot_floats + 2 * r + hl * D + e];
-        }
         const int h = g * r + hl;
-        float gv = 1.f;
+        float gl = 0.f;
         if (p.gate_mode == GATTN_GATE_ELEMENTWISE)
-            gv = sigmoidf_dev(__bfloat162float(static_cast<const bf16*>(p.gate)[((int64_t)b * p.H + h) * D + e]));
+            gl = __bfloat162float(static_cast<const bf16*>(p.gate)[((int64_t)b * p.H + h) * D + e]);
         else if (p.gate_mode == GATTN_GATE_HEADWISE)
-            gv = sigmoidf_dev(__bfloat162float(static_cast<const bf16*>(p.gate)[(int64_t)b * p.H + h]));
+            gl = __bfloat162float(static_cast<const bf16*>(p.gate)[(int64_t)b * p.H + h]);
+        const float* src = part0 + 2 * r + hl * D + e;
+        float num = 0.f;
+        for (int sl0 = 0; sl0 < n_slots; sl0 += CH) {
+            float v[CH];
+#pragma unroll
+            for (int j = 0; j < CH; ++j) v[j] = sl0 + j < n_slots ? src[(int64_t)(sl0 + j) * slot_floats] : 0.f;
+#pragma unroll
+            for (int j = 0; j < CH; ++j) {
+                const float wgt = sl0 + j < n_slots ? cw[(sl0 + j) * r + hl] : 0.f;
+                num += wgt != 0.f ? wgt * v[j] : 0.f;
+            }
+        }
+        const float gv = p.gate_mode == GATTN_GATE_NONE ? 1.f : sigmoidf_dev(gl);
         static_cast<bf16*>(p.out)[((int64_t)b * p.H + h) * D + e] = __float2bfloat16_rn(num / den[hl] * gv);
     }
 }
@@ -454,8 +471,19 @@ cudaError_t launch_dec(const DecodeParams& p, const CUtensorMap& tm, cudaStream_
         e = cudaFuncSetAttribute(decode_combine_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)cw_bytes);
         if (e != cudaSuccess) return e;
     }
-    decode_combine_kernel<D><<<p.B * p.G, 256, cw_bytes, stream>>>(p);
-    return cudaGetLastError();
+    // programmatic serialisation: the combine CTAs become resident while the split
+    // kernel drains and wait on its completion inside the kernel
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(p.B * p.G));
+    cfg.blockDim = dim3(kCombineThreads);
+    cfg.dynamicSmemBytes = cw_bytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, decode_combine_kernel<D>, p);
 }
 
 }  // namespace

@@ -20,6 +20,7 @@ struct ProloguePlan {
     void* dst;
     int B, S, n_heads, d, rd;
     float eps;
+    unsigned int* status;  // device status word (bounded-wait expiry)
     float inv_freq[kMaxRotaryHalf];
 };
 

@@ -76,87 +76,128 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) qk_prologue_kernel(const 
     }
 }
 
-// bf16 -> bf16 with rotary_dim % 16 == 0 (the tensor-core path): a row of d
-// elements is spread over d/8 lanes, one 16-byte load and one 16-byte store each,
-// so a warp holds 32*8/d whole rows.  The RMS is a shuffle reduction inside the
-// row's lanes, and the rotation partner of a lane's 8 elements (e +- rd/2) sits in
-// the lane rd/16 away within the same row.
+// bf16 -> bf16 with rotary_dim % 16 == 0 (the tensor-core path).
+//
+// A row of D elements is spread over D/8 lanes, one 16-byte load and one 16-byte
+// store each, so a warp holds RPW = 32*8/D whole rows at a time.  The RMS is a
+// shuffle reduction inside the row's lanes, and the rotation partner of a lane's
+// 8 elements (e +- rd/2) sits in the lane rd/16 away within the same row.
+//
+// Each warp owns one RoPE position and up to U*RPW of the rows rotated by it:
+// with default positions (pos == NULL) that is token t of every batch and head,
+// otherwise token t of one batch, every head.  The lane's 8 (cos, sin) pairs are
+// computed once and reused for all of those rows, so the sine/cosine work is per
+// position rather than per row; the U row loads are issued together before any
+// arithmetic.
 template <int D>
-__global__ void __launch_bounds__(256) qk_prologue_bf16_kernel(const __grid_constant__ ProloguePlan p) {
+__global__ void __launch_bounds__(256) qk_prologue_bf16_kernel(const __grid_constant__ ProloguePlan p,
+                                                               uint32_t n_items, uint32_t n_tau, int nb) {
+    constexpr int LPR = D / 8;        // lanes per row
+    constexpr int RPW = 32 / LPR;     // rows per warp step
+    constexpr int U = 4;              // warp steps per item
     pdl_launch_dependents();  // the attention kernel may start its own prologue now
     // lanes read different frequencies: from shared memory, not the (serialising) parameter bank
     __shared__ float inv_freq[kMaxRotaryHalf];
     if (threadIdx.x < kMaxRotaryHalf) inv_freq[threadIdx.x] = p.inv_freq[threadIdx.x];
     __syncthreads();
-    constexpr int LPR = D / 8;        // lanes per row
-    constexpr int RPW = 32 / LPR;     // rows per warp
     const int lane = threadIdx.x & 31;
     const int sub = lane % LPR;       // this lane's 8-element block within the row
-    const int64_t r = ((int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5)) * RPW + lane / LPR;
-    const int64_t n_rows = (int64_t)p.B * p.S * p.n_heads;
-    const bool live = r < n_rows;
-    const int64_t rr = live ? r : 0;
-    const int hd = (int)(rr % p.n_heads);
-    const int64_t bt = rr / p.n_heads;  // b*S + t
-    const int t = (int)(bt % p.S);
-    const int b = (int)(bt / p.S);
-    const bf16* x = static_cast<const bf16*>(p.x) + bt * p.tok_stride + (int64_t)hd * p.head_stride + 8 * sub;
-    const uint4 xv = live ? *reinterpret_cast<const uint4*>(x) : make_uint4(0, 0, 0, 0);
-    const uint4 wv = *reinterpret_cast<const uint4*>(static_cast<const bf16*>(p.w) + 8 * sub);
-    const uint32_t xs[4] = {xv.x, xv.y, xv.z, xv.w}, ws[4] = {wv.x, wv.y, wv.z, wv.w};
-    float y[8];
-    float ss = 0.f;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const float a = bf16_lo(xs[i]), c = bf16_hi(xs[i]);
-        ss = fmaf(a, a, fmaf(c, c, ss));
-        y[2 * i] = a * bf16_lo(ws[i]);
-        y[2 * i + 1] = c * bf16_hi(ws[i]);
-    }
-#pragma unroll
-    for (int o = LPR / 2; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-    const float rinv = rsqrtf(ss / (float)D + p.eps);
-    // rotation: block e0 = 8*sub pairs with e0 + half (first half) or e0 - half (second half)
-    const int half = p.rd >> 1, dl = half >> 3;  // partner distance in lanes
     const int e0 = 8 * sub;
+    const uint32_t item = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    const bool warp_live = item < n_items;
+    // the position this warp rotates by: tau = t (default positions) or b*S + t.
+    // Consecutive warps take consecutive positions of the same chunk of rows, so a
+    // CTA reads and writes contiguous runs of every (batch, head) plane.
+    const uint32_t chunk = warp_live ? item / n_tau : 0u;
+    const uint32_t tau = warp_live ? item - chunk * n_tau : 0u;
+    const int t = p.pos ? (int)(tau % (uint32_t)p.S) : (int)tau;
+    const int b_fixed = p.pos ? (int)(tau / (uint32_t)p.S) : 0;
+    const float posf = p.pos ? (float)p.pos[tau] : (float)tau;
+    const int half = p.rd >> 1, dl = half >> 3;  // rotation partner distance in lanes
     const bool first = e0 < half, rot = e0 < p.rd;
     const int src = lane + (first ? dl : -dl);
-    float q[8];
+    float cs[8], sn[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) q[i] = __shfl_sync(0xffffffffu, y[i], rot ? src : lane);
-    const float posf = live ? (p.pos ? (float)p.pos[bt] : (float)t) : 0.f;
-    uint32_t o[4];
+    for (int i = 0; i < 8; ++i) {
+        cs[i] = 1.f;
+        sn[i] = 0.f;
+        if (rot) rope_sincos(posf * inv_freq[(first ? e0 : e0 - half) + i], &sn[i], &cs[i]);
+    }
+    const uint4 wv = *reinterpret_cast<const uint4*>(static_cast<const bf16*>(p.w) + e0);
+    const uint32_t ws[4] = {wv.x, wv.y, wv.z, wv.w};
+    const uint32_t n_rows = (uint32_t)nb * (uint32_t)p.n_heads;  // rows sharing this position
+    uint4 xv[U];
+    int rb[U], rh[U];
+    bool live[U];
 #pragma unroll
-    for (int i = 0; i < 8; i += 2) {
-        float v0 = y[i], v1 = y[i + 1];
-        if (rot) {
-            const int f = (first ? e0 : e0 - half) + i;
-            float s0, c0, s1, c1;
-            rope_sincos(posf * inv_freq[f], &s0, &c0);
-            rope_sincos(posf * inv_freq[f + 1], &s1, &c1);
-            v0 = first ? y[i] * c0 - q[i] * s0 : y[i] * c0 + q[i] * s0;
-            v1 = first ? y[i + 1] * c1 - q[i + 1] * s1 : y[i + 1] * c1 + q[i + 1] * s1;
+    for (int u = 0; u < U; ++u) {
+        const uint32_t r = (chunk * U + u) * RPW + (uint32_t)(lane / LPR);
+        live[u] = warp_live && r < n_rows;
+        const uint32_t rr = live[u] ? r : 0u;
+        rh[u] = (int)(rr % (uint32_t)p.n_heads);
+        rb[u] = p.pos ? b_fixed : (int)(rr / (uint32_t)p.n_heads);
+        const bf16* x = static_cast<const bf16*>(p.x) + ((int64_t)rb[u] * p.S + t) * p.tok_stride +
+                        (int64_t)rh[u] * p.head_stride + e0;
+        xv[u] = live[u] ? __ldcs(reinterpret_cast<const uint4*>(x)) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        const uint32_t xs[4] = {xv[u].x, xv[u].y, xv[u].z, xv[u].w};
+        float y[8];
+        float ss = 0.f;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float a = bf16_lo(xs[i]), c = bf16_hi(xs[i]);
+            ss = fmaf(a, a, fmaf(c, c, ss));
+            y[2 * i] = a * bf16_lo(ws[i]);
+            y[2 * i + 1] = c * bf16_hi(ws[i]);
         }
-        o[i >> 1] = pack_bf16x2(v0 * rinv, v1 * rinv);
+#pragma unroll
+        for (int o = LPR / 2; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+        const float rinv = rsqrtf(ss / (float)D + p.eps);
+        float q[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) q[i] = __shfl_sync(0xffffffffu, y[i], rot ? src : lane);
+        uint32_t o[4];
+#pragma unroll
+        for (int i = 0; i < 8; i += 2) {
+            // first half: x*cos - partner*sin; second half: x*cos + partner*sin (cs=1, sn=0 past rd)
+            const float s0 = first ? -sn[i] : sn[i], s1 = first ? -sn[i + 1] : sn[i + 1];
+            const float v0 = fmaf(y[i], cs[i], q[i] * s0);
+            const float v1 = fmaf(y[i + 1], cs[i + 1], q[i + 1] * s1);
+            o[i >> 1] = pack_bf16x2(v0 * rinv, v1 * rinv);
+        }
+        if (live[u]) {
+            bf16* dst = static_cast<bf16*>(p.dst) + (((int64_t)rb[u] * p.n_heads + rh[u]) * p.S + t) * D + e0;
+            *reinterpret_cast<uint4*>(dst) = make_uint4(o[0], o[1], o[2], o[3]);
+        }
     }
-    if (live) {
-        bf16* dst = static_cast<bf16*>(p.dst) + (((int64_t)b * p.n_heads + hd) * p.S + t) * D + 8 * sub;
-        *reinterpret_cast<uint4*>(dst) = make_uint4(o[0], o[1], o[2], o[3]);
-    }
+}
+
+template <int D>
+cudaError_t launch_bf16(const ProloguePlan& p, cudaStream_t stream) {
+    constexpr int RPW = 32 / (D / 8);
+    constexpr int U = 4;
+    const int64_t n_tau = p.pos ? (int64_t)p.B * p.S : (int64_t)p.S;
+    const int64_t rows_per_tau = p.pos ? (int64_t)p.n_heads : (int64_t)p.B * p.n_heads;
+    const int64_t n_chunks = (rows_per_tau + U * RPW - 1) / (U * RPW);
+    const int64_t n_items = n_tau * n_chunks;
+    if (rows_per_tau >= 0x7fffffffLL || n_items + 8 >= 0x7fffffffLL) return cudaErrorInvalidValue;
+    const int64_t blocks = (n_items + 7) / 8;
+    qk_prologue_bf16_kernel<D><<<(unsigned)blocks, 256, 0, stream>>>(p, (uint32_t)n_items, (uint32_t)n_tau,
+                                                                        p.pos ? 1 : p.B);
+    return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_prologue(const ProloguePlan& p, bool bf16_in, bool bf16_out, cudaStream_t stream) {
     const int64_t n_rows = (int64_t)p.B * p.S * p.n_heads;
-    if (bf16_in && bf16_out && p.rd % 16 == 0 && (p.d == 64 || p.d == 128 || p.d == 256)) {
-        const int64_t rows_per_block = 8 * (256 / p.d);  // 8 warps, 32*8/d rows each
-        const int64_t nb = (n_rows + rows_per_block - 1) / rows_per_block;
-        if (nb > 0x7fffffff) return cudaErrorInvalidValue;
-        if (p.d == 64) qk_prologue_bf16_kernel<64><<<(unsigned)nb, 256, 0, stream>>>(p);
-        else if (p.d == 128) qk_prologue_bf16_kernel<128><<<(unsigned)nb, 256, 0, stream>>>(p);
-        else qk_prologue_bf16_kernel<256><<<(unsigned)nb, 256, 0, stream>>>(p);
-        return cudaGetLastError();
+    if (n_rows == 0) return cudaSuccess;
+    if (bf16_in && bf16_out && p.rd % 16 == 0 && n_rows < 0x40000000LL) {
+        if (p.d == 64) return launch_bf16<64>(p, stream);
+        if (p.d == 128) return launch_bf16<128>(p, stream);
+        if (p.d == 256) return launch_bf16<256>(p, stream);
     }
     const int64_t blocks = (n_rows + kWarpsPerBlock - 1) / kWarpsPerBlock;
     if (blocks > 0x7fffffff) return cudaErrorInvalidValue;
