@@ -362,7 +362,7 @@ def main():
     e2e_val = world * flops / (e2e_ms * 1e-3) / 1e12 if do_p and e2e_ms > 0 else float("nan")
 
     if rank == 0:
-        tc_src = ["prefill_tc.cu", "common.cuh", "internal.h"]
+        tc_src = ["prefill_pair.cu", "common.cuh", "internal.h"]
         dec_src = ["decode.cu", "common.cuh", "internal.h"]
         line = {
             "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": K,
@@ -378,8 +378,8 @@ def main():
             "prefill_ms": t["p"], "prefill_kernel_ms": t["pk"],
             "roofline": {"bound": "tensor", "achieved": kern_tflops, "peak": bf16_peak, "unit": "TFLOP/s",
                          "frac": kern_tflops / bf16_peak, "peak_kind": f"{peak_kind} bf16 dense (burst)",
-                         "kernel": "prefill_tc_kernel<256>",
-                         "traffic": profiled_traffic("prefill_tc_qwen35_08b.md", tc_src)},
+                         "kernel": "prefill_pair_kernel<256>",
+                         "traffic": profiled_traffic("prefill_pair_qwen35_08b.md", tc_src)},
             "decode": {"value": dec_gbs, "unit": "GB/s", "ms": t["d"], "kernel_ms": t["dk"],
                        "bytes_per_step": dbytes,
                        "roofline": {"bound": "hbm", "achieved": dec_kern_gbs, "peak": hbm_peak, "unit": "GB/s",

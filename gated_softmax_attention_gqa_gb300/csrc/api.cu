@@ -224,13 +224,16 @@ gattn_status gattn_prefill(const void* q, const void* k, const void* v, const vo
         kp.dst = workspace;
         if (launch_prologue(kp, true, true, stream) != cudaSuccess) return GATTN_ERR_CUDA;
         PrefillMaps maps;
-        const uint32_t bn = (uint32_t)prefill_block_n(d);
+        // two heads of a KV group per CTA pair when H/G is even, else one head per CTA
+        const bool pair = prefill_pair_supported(d, H, G);
+        const uint32_t kbn = pair ? (uint32_t)prefill_pair_key_rows() : (uint32_t)prefill_block_n(d);
+        const uint32_t vbn = pair ? (uint32_t)prefill_pair_value_rows() : (uint32_t)prefill_block_n(d);
         const uint64_t kdims[3] = {(uint64_t)d, (uint64_t)S, (uint64_t)B * G};
         const uint64_t kstr[2] = {(uint64_t)d * 2, (uint64_t)S * d * 2};
-        const uint32_t kbox[3] = {64, bn, 1};
+        const uint32_t kbox[3] = {64, kbn, 1};
         const uint64_t vdims[4] = {(uint64_t)d, (uint64_t)G, (uint64_t)S, (uint64_t)B};
         const uint64_t vstr[3] = {(uint64_t)d * 2, (uint64_t)G * d * 2, (uint64_t)S * G * d * 2};
-        const uint32_t vbox[4] = {64, 1, bn, 1};
+        const uint32_t vbox[4] = {64, 1, vbn, 1};
         // raw q and gate: [B,S,H,d] views with token/head strides; 128-token boxes
         const uint64_t hdims[4] = {(uint64_t)d, (uint64_t)H, (uint64_t)S, (uint64_t)B};
         const uint64_t qstr[3] = {(uint64_t)q_head_stride * 2, (uint64_t)q_tok_stride * 2,
@@ -269,7 +272,9 @@ gattn_status gattn_prefill(const void* q, const void* k, const void* v, const vo
         pp.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)d));
         pp.status = status;
         std::memcpy(pp.inv_freq, kp.inv_freq, sizeof(pp.inv_freq));
-        if (launch_prefill_tc(pp, maps, stream, g_prof_start, g_prof_stop) != cudaSuccess) return GATTN_ERR_CUDA;
+        const cudaError_t le = pair ? launch_prefill_pair(pp, maps, stream, g_prof_start, g_prof_stop)
+                                    : launch_prefill_tc(pp, maps, stream, g_prof_start, g_prof_stop);
+        if (le != cudaSuccess) return GATTN_ERR_CUDA;
         return GATTN_OK;
     }
 

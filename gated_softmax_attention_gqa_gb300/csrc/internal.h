@@ -73,6 +73,12 @@ struct PrefillMaps {
 cudaError_t launch_prologue(const ProloguePlan& p, bool bf16_in, bool bf16_out, cudaStream_t stream);
 cudaError_t launch_prefill_tc(const PrefillParams& p, const PrefillMaps& maps, cudaStream_t stream,
                               cudaEvent_t ev_start, cudaEvent_t ev_stop);
+// CTA-pair (cta_group::2) tcgen05 prefill: two heads of one KV group per cluster.
+bool prefill_pair_supported(int d, int H, int G);
+int prefill_pair_key_rows();    // K' rows per TMA box
+int prefill_pair_value_rows();  // V rows per TMA box
+cudaError_t launch_prefill_pair(const PrefillParams& p, const PrefillMaps& maps, cudaStream_t stream,
+                                cudaEvent_t ev_start, cudaEvent_t ev_stop);
 cudaError_t launch_prefill_f32(const PrefillF32Params& p, cudaStream_t stream, cudaEvent_t ev_start,
                                cudaEvent_t ev_stop);
 cudaError_t launch_decode(const DecodeParams& p, const CUtensorMap& tm_kv, cudaStream_t stream,

@@ -1,0 +1,643 @@
+// prefill_pair.cu -- bf16 causal gated GQA attention on CTA pairs (cta_group::2).
+//
+// Computes, like prefill_tc.cu,
+//   out[b, t, h*d:(h+1)*d] = sigmoid(z) * sum_{j<=t} softmax_j(q'_t . k'_j / sqrt(d)) v_j
+// with q' = rope(rmsnorm(q)), k' = rope(rmsnorm(k)) and head h reading KV group
+// g = floor(h / (H/G)).  ("Gated attention" handbook chapter, sections "The
+// formula" and "Four things Qwen3.5 adds to the textbook"; "Attention, worked all
+// the way through", section "Why scaling and stable softmax matter"; "Gated
+// Attention" deep-dive, section "门放在哪里？".)
+//
+// A cluster of two CTAs takes one 128-row query tile of two heads 2p and 2p+1,
+// which share their KV group whenever H/G is even; CTA rank c owns head 2p + c.
+// The two heads' query rows stack into one M = 256 tensor-core operand, so each
+// MMA (issued once, by the even CTA) serves both heads, while each CTA keeps only
+// half of every K/V tile in its shared memory: keys [64c, 64c+64) of a 128-key K'
+// tile (the B operand of S = Q'K'^T is split along N) and value columns
+// [c d/2, (c+1) d/2) of the V tile (the B operand of O += P V, split along N = d).
+// That halved footprint is what buys 128-key tiles at d = 256.
+//
+// Roles per CTA (10 warps):
+//   warp 0      TMA producer of this CTA's halves: the raw Q tile of its own head
+//               once, K' and V halves into rings, its gate tile at the end.
+//   warp 1      allocates TMEM for the pair.  Even CTA: issues every MMA.  Odd CTA:
+//               forwards the landing of its K'/V halves to the even CTA's barriers.
+//   warps 2..9  two threads per query row of this CTA's head, each owning half of
+//               the row's keys in every tile (and half of its O columns): the fused
+//               Q prologue (warps 2..5: Q' = rope(rmsnorm(q)) written over the raw
+//               Q tile in shared memory), the online softmax and the gate epilogue.
+//               The two halves of a row swap tile maxima through shared memory;
+//               their row sums are added once, in the epilogue.
+//
+// TMEM (per CTA, lane = query row): O [0, d) | S0 [d, d+128) | S1 [d+128, d+256).
+// Key tile j's scores go to S_{j%2}, and its probabilities P_j overwrite them in
+// place as bf16 pairs, which the PV MMA reads straight from TMEM.
+// Shared memory (per CTA): Q' tile | K' ring | V ring | barriers | q norm weights |
+// row-half exchange.  The gate tile finally lands in the K' ring.
+//
+// Issue order (one issuer, the tensor pipe runs in order): QK(0), QK(1), then per
+// tile PV(j), QK(j+2).  QK(j+2) reuses S_{j%2} right behind the PV that reads P_j
+// from it, so while the softmax turns S_j into P_j the tensor core runs PV(j-1)
+// and QK(j+1): the softmax has a whole tile period.  The running max is refreshed
+// (and O rescaled in TMEM) only when it grows by more than 2^8, so O and l always
+// share one reference max.
+//
+// Cross-CTA signalling: tensor-core completions are multicast to both CTAs by
+// tcgen05.commit.  The odd CTA's threads arrive on the even CTA's barriers; every
+// such arrival announces work that has already completed (a TMA copy whose
+// barrier was observed, tcgen05 stores waited on, tcgen05 loads in registers), so
+// CTA-scope arrivals suffice, except for Q', which is written by ordinary stores
+// and announced once with a cluster-scope release.
+#include "common.cuh"
+#include "internal.h"
+
+namespace gattn {
+namespace {
+
+template <int D>
+struct PairCfg {
+    static constexpr int BM = 128;        // query rows per CTA
+    static constexpr int BN = 128;        // keys per tile
+    static constexpr int KH = BN / 2;     // keys of a K' tile held by one CTA
+    static constexpr int DH = D / 2;      // value columns held by one CTA
+    static constexpr int NSK = D == 256 ? 2 : 4;  // K' ring stages
+    static constexpr int NSV = D == 256 ? 2 : 4;  // V ring stages
+    static constexpr int KCH = D / 64;    // 128-byte chunks of a K' row
+    static constexpr int K_CHUNK = KH * 128;
+    static constexpr int K_TILE = KCH * K_CHUNK;
+    static constexpr int VCH = DH / 64;   // 128-byte chunks of a V half-row
+    static constexpr int V_CHUNK = BN * 128;
+    static constexpr int V_TILE = VCH * V_CHUNK;
+    static constexpr int ROWBOX_BYTES = BM * 128;  // one Q/gate TMA box: 128 rows x 64 bf16
+    static constexpr int QTILE_BYTES = BM * D * 2;
+    static_assert(QTILE_BYTES <= NSK * K_TILE, "the gate tile must fit the K' ring");
+    static constexpr int TM_O = 0;
+    static constexpr int TM_S = D;                // score buffer b at TM_S + b * BN
+    static constexpr int TM_COLS = 512;
+    static_assert(TM_S + 2 * BN <= TM_COLS, "TMEM budget");
+    static constexpr int OFF_Q = 0;
+    static constexpr int OFF_K = QTILE_BYTES;
+    static constexpr int OFF_V = OFF_K + NSK * K_TILE;
+    static constexpr int OFF_BAR = OFF_V + NSV * V_TILE;
+    static constexpr int NBAR = 2 * NSK + 2 * NSV + 14;
+    static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+    static constexpr int OFF_W = (OFF_MISC + 16 + 127) & ~127;
+    // row-half exchange: tile maxima [2 buffers][2 halves][BM] and row sums [2 halves][BM]
+    static constexpr int OFF_X = OFF_W + D * 2;
+    static constexpr int SMEM_BYTES = OFF_X + (2 * 2 * BM + 2 * BM) * 4;
+    // never less than 120 KB, so that no second CTA (and TMEM allocation) shares the SM
+    static constexpr int SMEM_ALLOC = (SMEM_BYTES + 1024) > 122880 ? (SMEM_BYTES + 1024) : 122880;
+    static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
+    static constexpr int SOFTMAX_WARPS = 8;  // two per row quarter: each thread takes half a row
+    static constexpr int THREADS = 64 + 32 * SOFTMAX_WARPS;
+    static constexpr int P_ARRIVALS = 2 * SOFTMAX_WARPS;   // P_j: every softmax warp of both CTAs
+    static constexpr int Q_ARRIVALS = SOFTMAX_WARPS;       // Q': the first-half warps of both CTAs
+    static constexpr uint32_t IDESC_QK = make_idesc_bf16(256, BN, false);
+    static constexpr uint32_t IDESC_PV = make_idesc_bf16(256, D, true);
+    static constexpr float RESCALE_THRESHOLD = 8.0f;  // log2 domain
+};
+
+struct PairBars {
+    uint32_t base;
+    int nsk, nsv;
+    __device__ uint32_t at(int i) const { return base + 8u * (uint32_t)i; }
+    // k_full / v_full: in the even CTA they expect two arrivals (its own producer's,
+    // carrying the bytes, and the odd CTA's forward); in the odd CTA one.
+    __device__ uint32_t k_full(int s) const { return at(s); }
+    __device__ uint32_t k_empty(int s) const { return at(nsk + s); }
+    __device__ uint32_t v_full(int s) const { return at(2 * nsk + s); }
+    __device__ uint32_t v_empty(int s) const { return at(2 * nsk + nsv + s); }
+    __device__ int r() const { return 2 * nsk + 2 * nsv; }
+    __device__ uint32_t s_full(int i) const { return at(r() + i); }      // S_j in buffer i = j % 2 (both CTAs)
+    __device__ uint32_t p_full(int i) const { return at(r() + 2 + i); }  // P_j of both CTAs in buffer i (even CTA)
+    __device__ uint32_t pv_done() const { return at(r() + 4); }          // PV_j complete (both CTAs)
+    __device__ uint32_t o_final() const { return at(r() + 5); }          // every PV complete (both CTAs)
+    __device__ uint32_t q_ready() const { return at(r() + 6); }          // Q' of both CTAs written (even CTA)
+    __device__ uint32_t q_full() const { return at(r() + 7); }           // raw Q tile + weights landed
+    __device__ uint32_t g_full() const { return at(r() + 8); }           // gate tile landed
+    __device__ uint32_t drain() const { return at(r() + 9); }            // the issuer's MMAs all complete
+    __device__ uint32_t xchg(int q) const { return at(r() + 10 + q); }   // both halves of row quarter q posted
+};
+
+// Arrive on the even CTA's copy of barrier `bar`: locally from the even CTA, at
+// CTA scope from the odd one (what is announced has already completed).
+__device__ __forceinline__ void arrive_even(uint32_t bar, uint32_t cr) {
+    if (cr == 0) mbar_arrive(bar);
+    else mbar_arrive_remote_cta(mapa_shared(bar, 0));
+}
+
+// ----------------------------------------------------------------- producer
+
+template <int D>
+__device__ void pair_producer(const CUtensorMap* tmK, const CUtensorMap* tmV, const CUtensorMap* tmQ,
+                              const CUtensorMap* tmG, const void* qnorm_w, const PairBars& bars, uint32_t sbase,
+                              int n_kv, int b, int g, int h, int qt, int G, uint32_t cr, bool gate_tile,
+                              volatile int* abort_flag, unsigned int* status) {
+    using C = PairCfg<D>;
+    // raw Q tile of this CTA's head (normalised in place later), the weights next to it
+    mbar_arrive_expect_tx(bars.q_full(), C::QTILE_BYTES + D * 2);
+    bulk_load(sbase + C::OFF_W, qnorm_w, D * 2, bars.q_full());
+#pragma unroll
+    for (int c = 0; c < C::KCH; ++c)
+        tma_load_4d(sbase + C::OFF_Q + c * C::ROWBOX_BYTES, tmQ, bars.q_full(), c * 64, h, qt * C::BM, b);
+
+    // K' comes from the pre-pass kernel launched just before this one
+    pdl_wait_prerequisites();
+
+    int nk = 0, nv = 0;
+    const unsigned long long t0 = global_timer_ns();
+    uint32_t spins = 0;
+    while (nk < n_kv || nv < n_kv) {
+        bool progressed = false;
+        if (nk < n_kv &&
+            (nk < C::NSK || mbar_try_wait(bars.k_empty(nk % C::NSK), ((uint32_t)(nk / C::NSK) & 1u) ^ 1u))) {
+            const int st = nk % C::NSK;
+            mbar_arrive_expect_tx(bars.k_full(st), C::K_TILE);
+            const uint32_t kdst = sbase + C::OFF_K + st * C::K_TILE;
+#pragma unroll
+            for (int c = 0; c < C::KCH; ++c)
+                tma_load_3d(kdst + c * C::K_CHUNK, tmK, bars.k_full(st), c * 64, nk * C::BN + (int)cr * C::KH,
+                            b * G + g);
+            ++nk;
+            progressed = true;
+        }
+        if (nv < n_kv &&
+            (nv < C::NSV || mbar_try_wait(bars.v_empty(nv % C::NSV), ((uint32_t)(nv / C::NSV) & 1u) ^ 1u))) {
+            const int st = nv % C::NSV;
+            mbar_arrive_expect_tx(bars.v_full(st), C::V_TILE);
+            const uint32_t vdst = sbase + C::OFF_V + st * C::V_TILE;
+#pragma unroll
+            for (int c = 0; c < C::VCH; ++c)
+                tma_load_4d(vdst + c * C::V_CHUNK, tmV, bars.v_full(st), (int)cr * C::DH + c * 64, g, nv * C::BN, b);
+            ++nv;
+            progressed = true;
+        }
+        if (progressed) {
+            spins = 0;
+            continue;
+        }
+        if ((++spins & 63u) == 0) {
+            if (*abort_flag) break;
+            if (global_timer_ns() - t0 > 4 * kWaitLimitNs) {
+                *abort_flag = 1;
+                atomicOr(status, GATTN_DEVICE_TIMEOUT);
+                break;
+            }
+        }
+    }
+    // gate tile into the K' ring once its last K' tile has been consumed
+    bool g_issued = false;
+    if (gate_tile && nk == n_kv) {
+        bool ok = true;
+        for (int j = n_kv > C::NSK ? n_kv - C::NSK : 0; ok && j < n_kv; ++j)
+            ok = mbar_wait(bars.k_empty(j % C::NSK), (uint32_t)(j / C::NSK) & 1u, abort_flag, status);
+        if (ok) {
+            mbar_arrive_expect_tx(bars.g_full(), C::QTILE_BYTES);
+#pragma unroll
+            for (int c = 0; c < C::KCH; ++c)
+                tma_load_4d(sbase + C::OFF_K + c * C::ROWBOX_BYTES, tmG, bars.g_full(), c * 64, h, qt * C::BM, b);
+            g_issued = true;
+        }
+    }
+    // every copy this thread started lands before the CTA can exit
+    mbar_wait_drain(bars.q_full(), 0, status);
+    for (int j = nk > C::NSK ? nk - C::NSK : 0; j < nk; ++j)
+        mbar_wait_drain(bars.k_full(j % C::NSK), (uint32_t)(j / C::NSK) & 1u, status);
+    for (int j = nv > C::NSV ? nv - C::NSV : 0; j < nv; ++j)
+        mbar_wait_drain(bars.v_full(j % C::NSV), (uint32_t)(j / C::NSV) & 1u, status);
+    if (g_issued) mbar_wait_drain(bars.g_full(), 0, status);
+}
+
+// Odd CTA: tell the even CTA's issuer, in order, that each K'/V half has landed here.
+template <int D>
+__device__ void pair_forwarder(const PairBars& bars, int n_kv, volatile int* abort_flag, unsigned int* status) {
+    using C = PairCfg<D>;
+    int fk = 0, fv = 0;
+    const unsigned long long t0 = global_timer_ns();
+    uint32_t spins = 0;
+    while (fk < n_kv || fv < n_kv) {
+        bool progressed = false;
+        if (fk < n_kv && mbar_try_wait(bars.k_full(fk % C::NSK), (uint32_t)(fk / C::NSK) & 1u)) {
+            arrive_even(bars.k_full(fk % C::NSK), 1);
+            ++fk;
+            progressed = true;
+        }
+        if (fv < n_kv && mbar_try_wait(bars.v_full(fv % C::NSV), (uint32_t)(fv / C::NSV) & 1u)) {
+            arrive_even(bars.v_full(fv % C::NSV), 1);
+            ++fv;
+            progressed = true;
+        }
+        if (progressed) {
+            spins = 0;
+            continue;
+        }
+        if ((++spins & 63u) == 0) {
+            if (*abort_flag) break;
+            if (global_timer_ns() - t0 > 4 * kWaitLimitNs) {
+                *abort_flag = 1;
+                atomicOr(status, GATTN_DEVICE_TIMEOUT);
+                break;
+            }
+        }
+    }
+}
+
+// ----------------------------------------------------------------- MMA issuer (even CTA)
+
+template <int D>
+__device__ void pair_mma(const PairBars& bars, uint32_t sbase, uint32_t tm, int n_kv, volatile int* abort_flag,
+                         unsigned int* status) {
+    using C = PairCfg<D>;
+    const uint64_t qdesc0 = make_sdesc_sw128(sbase + C::OFF_Q, 16, 1024);
+    const uint64_t kdesc0 = make_sdesc_sw128(sbase + C::OFF_K, 16, 1024);
+    const uint64_t vdesc0 = make_sdesc_sw128(sbase + C::OFF_V, C::V_CHUNK, 1024);
+    // S_j = Q' K'_j^T into score buffer j % 2
+    auto issue_qk = [&](int j) -> bool {
+        const int st = j % C::NSK;
+        if (!mbar_wait(bars.k_full(st), (uint32_t)(j / C::NSK) & 1u, abort_flag, status)) return false;
+        tc_fence_after();
+        const uint64_t kd = kdesc0 + (uint64_t)((st * C::K_TILE) >> 4);
+        const uint32_t d_tmem = tm + C::TM_S + (uint32_t)(j & 1) * C::BN;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+            mma2_ss(d_tmem, qdesc0 + (uint64_t)(((kk >> 2) * C::ROWBOX_BYTES + (kk & 3) * 32) >> 4),
+                    kd + (uint64_t)(((kk >> 2) * C::K_CHUNK + (kk & 3) * 32) >> 4), C::IDESC_QK, kk > 0 ? 1u : 0u);
+        tc_commit2(bars.k_empty(st), 3);
+        tc_commit2(bars.s_full(j & 1), 3);
+        return true;
+    };
+    // O += P_j V_j, P_j read from TMEM where it overwrote S_j
+    auto issue_pv = [&](int j) -> bool {
+        if (!mbar_wait(bars.p_full(j & 1), (uint32_t)(j >> 1) & 1u, abort_flag, status)) return false;
+        const int st = j % C::NSV;
+        if (!mbar_wait(bars.v_full(st), (uint32_t)(j / C::NSV) & 1u, abort_flag, status)) return false;
+        tc_fence_after();
+        const uint64_t vd = vdesc0 + (uint64_t)((st * C::V_TILE) >> 4);
+        const uint32_t p_tmem = tm + C::TM_S + (uint32_t)(j & 1) * C::BN;
+#pragma unroll
+        for (int kk = 0; kk < C::BN / 16; ++kk)
+            mma2_ts(tm + C::TM_O, p_tmem + kk * 8, vd + (uint64_t)((kk * 16 * 128) >> 4), C::IDESC_PV,
+                    (j > 0 || kk > 0) ? 1u : 0u);
+        tc_commit2(bars.v_empty(st), 3);
+        tc_commit2(bars.pv_done(), 3);
+        return true;
+    };
+    bool ok = mbar_wait(bars.q_ready(), 0, abort_flag, status);  // Q' of both heads in shared memory
+    tc_fence_after();
+    if (ok && n_kv > 0) ok = issue_qk(0);
+    if (ok && n_kv > 1) ok = issue_qk(1);
+    for (int j = 0; ok && j < n_kv; ++j) {
+        if (!issue_pv(j)) { ok = false; break; }
+        // S_{j%2} is free again behind PV(j), which reads P_j from it
+        if (j + 2 < n_kv && !issue_qk(j + 2)) { ok = false; break; }
+    }
+    if (ok) tc_commit2(bars.o_final(), 3);
+    tc_commit2(bars.drain(), 1);
+    // no MMA of the pair may still be running when the CTAs tear down
+    mbar_wait_drain(bars.drain(), 0, status);
+}
+
+// ----------------------------------------------------------------- softmax / prologue / epilogue
+
+template <int D>
+__device__ void pair_softmax(const PrefillParams& p, const PairBars& bars, uint32_t sbase, uint8_t* smem_x, uint32_t tm,
+                             uint32_t cr, int quarter, int hf, int lane, int qt, int b, int h, int n_kv,
+                             volatile int* abort_flag) {
+    using C = PairCfg<D>;
+    constexpr int HB = C::BN / 2;  // keys of a tile owned by this thread
+    const int row = quarter * 32 + lane;
+    const uint32_t tl = tm + ((uint32_t)(quarter * 32) << 16);
+    const int t = qt * C::BM + row;
+    const bool valid = t < p.S;
+    const int64_t tok = (int64_t)b * p.S + (valid ? t : 0);
+    const bf16* grow = static_cast<const bf16*>(p.gate) + tok * p.gate_tok_stride + (int64_t)h * p.gate_head_stride;
+    float gate_head = 1.f;
+    if (p.gate_mode == GATTN_GATE_HEADWISE && valid) gate_head = sigmoidf_dev(__bfloat162float(grow[0]));
+
+    // ---- fused Q prologue (first-half threads): rmsnorm then partial rotate-half
+    // RoPE, written as bf16 over the raw row in the Q tile (the A operand of
+    // S = Q'K'^T).  Rows past the sequence end were zero-filled by TMA.
+    if (hf == 0) {
+        if (!__all_sync(0xffffffffu, mbar_wait(bars.q_full(), 0, abort_flag, p.status))) return;
+        const uint32_t qbase = sbase + C::OFF_Q;
+        const uint32_t wbase = sbase + C::OFF_W;
+        float ss[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int c = 0; c < D / 8; ++c) {
+            float f[8];
+            unpack8(lds_v4(rowtile_addr(qbase, row, 8 * c)), f);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) ss[e & 3] = fmaf(f[e], f[e], ss[e & 3]);
+        }
+        const float rinv = rsqrtf(((ss[0] + ss[1]) + (ss[2] + ss[3])) / (float)D + p.eps);
+        const float posf = valid ? (p.pos ? (float)p.pos[tok] : (float)t) : 0.f;
+        const int half = p.rd >> 1;
+        for (int i0 = 0; i0 < half; i0 += 8) {
+            float xa[8], xb[8], wa[8], wb[8];
+            unpack8(lds_v4(rowtile_addr(qbase, row, i0)), xa);
+            unpack8(lds_v4(rowtile_addr(qbase, row, i0 + half)), xb);
+            unpack8(lds_v4(wbase + 2 * i0), wa);
+            unpack8(lds_v4(wbase + 2 * (i0 + half)), wb);
+            uint32_t lo[4], hi[4];
+#pragma unroll
+            for (int e = 0; e < 8; e += 2) {
+                float s0, c0, s1, c1;
+                rope_sincos(posf * p.inv_freq[i0 + e], &s0, &c0);
+                rope_sincos(posf * p.inv_freq[i0 + e + 1], &s1, &c1);
+                const float a0 = xa[e] * wa[e], b0 = xb[e] * wb[e];
+                const float a1 = xa[e + 1] * wa[e + 1], b1 = xb[e + 1] * wb[e + 1];
+                lo[e >> 1] = pack_bf16x2((a0 * c0 - b0 * s0) * rinv, (a1 * c1 - b1 * s1) * rinv);
+                hi[e >> 1] = pack_bf16x2((b0 * c0 + a0 * s0) * rinv, (b1 * c1 + a1 * s1) * rinv);
+            }
+            sts_v4(rowtile_addr(qbase, row, i0), lo[0], lo[1], lo[2], lo[3]);
+            sts_v4(rowtile_addr(qbase, row, i0 + half), hi[0], hi[1], hi[2], hi[3]);
+        }
+        for (int e0 = p.rd; e0 < D; e0 += 8) {
+            float x[8], w[8];
+            unpack8(lds_v4(rowtile_addr(qbase, row, e0)), x);
+            unpack8(lds_v4(wbase + 2 * e0), w);
+            sts_v4(rowtile_addr(qbase, row, e0), pack_bf16x2(x[0] * w[0] * rinv, x[1] * w[1] * rinv),
+                   pack_bf16x2(x[2] * w[2] * rinv, x[3] * w[3] * rinv),
+                   pack_bf16x2(x[4] * w[4] * rinv, x[5] * w[5] * rinv),
+                   pack_bf16x2(x[6] * w[6] * rinv, x[7] * w[7] * rinv));
+        }
+        fence_proxy_async_smem();  // the tensor core reads Q' through the async proxy
+        __syncwarp();
+        if (lane == 0) mbar_arrive_remote(mapa_shared(bars.q_ready(), 0));  // ordinary stores: cluster release
+    }
+
+    // ---- main loop: online softmax over the KV tiles this query tile can see.
+    // This thread owns keys [64 hf, 64 hf + 64) of every tile and O columns
+    // [hf D/2, (hf+1) D/2); its partner (same row, other half) runs in warp +- 4.
+    const float sl2 = p.scale_log2;
+    const int row_min = qt * C::BM;
+    float* xmax = reinterpret_cast<float*>(smem_x);          // [2][2][BM]
+    float* xsum = xmax + 2 * 2 * C::BM;                      // [2][BM]
+    // the two warps of a row quarter post to shared memory, then meet on an
+    // mbarrier (one phase per tile, one more for the row sums; bounded wait)
+    const uint32_t xbar = bars.xchg(quarter);
+    auto meet = [&](int phase) -> bool {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(xbar);
+        return __all_sync(0xffffffffu, mbar_wait(xbar, (uint32_t)phase & 1u, abort_flag, p.status));
+    };
+    float m_ref = -INFINITY;  // reference max (log2 domain) shared by O and l
+    float l = 0.f;            // this half's share of the row sum
+    for (int j = 0; j < n_kv; ++j) {
+        const uint32_t s_col = C::TM_S + (uint32_t)(j & 1) * C::BN;
+        if (!__all_sync(0xffffffffu, mbar_wait(bars.s_full(j & 1), (uint32_t)(j >> 1) & 1u, abort_flag, p.status)))
+            return;
+        tc_fence_after();
+        float s[HB];
+        {
+            uint32_t r[64];
+            tmem_ld64(tl + s_col + hf * HB, r);
+#pragma unroll
+            for (int e = 0; e < 64; ++e) s[e] = __uint_as_float(r[e]);
+        }
+        const int key0 = j * C::BN + hf * HB;
+        if (key0 + HB - 1 > row_min) {
+#pragma unroll
+            for (int c = 0; c < HB; ++c)
+                if (key0 + c > t) s[c] = -INFINITY;
+        }
+        float mx[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) mx[i] = s[i];
+#pragma unroll
+        for (int c = 8; c < HB; ++c) mx[c & 7] = fmaxf(mx[c & 7], s[c]);
+        float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+        // the row's maximum over the whole tile: swap halves (buffer j%2, so a slow
+        // partner still reading tile j-1 is never overwritten).  Passing the meet also
+        // means the partner has read its S columns, which P overwrites below.
+        xmax[((j & 1) * 2 + hf) * C::BM + row] = mt;
+        if (!meet(j)) return;
+        mt = fmaxf(mt, xmax[((j & 1) * 2 + (hf ^ 1)) * C::BM + row]);
+        const float m_new = fmaxf(m_ref, mt * sl2);
+        const bool need = (m_new - m_ref) > C::RESCALE_THRESHOLD;
+        if (j == 0) {
+            m_ref = m_new;
+        } else if (__any_sync(0xffffffffu, need)) {
+            const float alpha = need ? ex2_approx(m_ref - m_new) : 1.f;
+            if (need) {
+                l *= alpha;
+                m_ref = m_new;
+            }
+            __syncwarp();
+            // O is touched only once PV(j-1) has landed (PV(j-2) already had: QK(j)
+            // was issued behind it)
+            if (!__all_sync(0xffffffffu, mbar_wait(bars.pv_done(), (uint32_t)(j - 1) & 1u, abort_flag, p.status)))
+                return;
+            tc_fence_after();
+#pragma unroll 1
+            for (int c = hf * (D / 2); c < (hf + 1) * (D / 2); c += 32) {
+                uint32_t r[32];
+                tmem_ld32(tl + C::TM_O + c, r);
+#pragma unroll
+                for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
+                tmem_st32(tl + C::TM_O + c, r);
+            }
+        }
+        // P = exp2(s * scale * log2e - m_ref) as bf16 pairs over this thread's keys:
+        // columns [32 hf, 32 hf + 32) of the score buffer
+        float rs[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        const float mref = m_ref;
+        uint32_t pk[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+            const float p0 = ex2_approx(fmaf(s[2 * e], sl2, -mref));
+            const float p1 = ex2_approx(fmaf(s[2 * e + 1], sl2, -mref));
+            rs[e & 7] += p0 + p1;
+            pk[e] = pack_bf16x2(p0, p1);
+        }
+        tmem_st32(tl + s_col + hf * (HB / 2), pk);
+        l += ((rs[0] + rs[1]) + (rs[2] + rs[3])) + ((rs[4] + rs[5]) + (rs[6] + rs[7]));
+        tmem_wait_st();  // P (and an O rescale above, if any) has landed
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) arrive_even(bars.p_full(j & 1), cr);
+    }
+
+    // ---- epilogue: O / l * sigmoid(gate) -> bf16 [B,S,H*d], this thread's half of the columns
+    xsum[hf * C::BM + row] = l;
+    if (!meet(n_kv)) return;
+    const float l_row = xsum[row] + xsum[C::BM + row];
+    if (!__all_sync(0xffffffffu, mbar_wait(bars.o_final(), 0, abort_flag, p.status))) return;
+    const bool elementwise = p.gate_mode == GATTN_GATE_ELEMENTWISE;
+    if (elementwise && !__all_sync(0xffffffffu, mbar_wait(bars.g_full(), 0, abort_flag, p.status))) return;
+    tc_fence_after();
+    const float inv_l = 1.f / l_row;
+    const float gh = inv_l * gate_head;
+    bf16* orow = static_cast<bf16*>(p.out) + (tok * p.H + h) * D;
+    const uint32_t gbase = sbase + C::OFF_K;
+#pragma unroll 1
+    for (int c = hf * (D / 2); c < (hf + 1) * (D / 2); c += 32) {
+        uint32_t r[32];
+        __syncwarp();
+        tmem_ld32(tl + C::TM_O + c, r);
+        if (!valid) continue;
+        float gv[32];
+        if (elementwise) {
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+                float f[8];
+                unpack8(lds_v4(rowtile_addr(gbase, row, c + 8 * q4)), f);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) gv[8 * q4 + e] = inv_l * sigmoidf_dev(f[e]);
+            }
+        } else {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) gv[e] = gh;
+        }
+        uint4* dst = reinterpret_cast<uint4*>(orow + c);
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+            uint4 v;
+            v.x = pack_bf16x2(__uint_as_float(r[8 * q4 + 0]) * gv[8 * q4 + 0], __uint_as_float(r[8 * q4 + 1]) * gv[8 * q4 + 1]);
+            v.y = pack_bf16x2(__uint_as_float(r[8 * q4 + 2]) * gv[8 * q4 + 2], __uint_as_float(r[8 * q4 + 3]) * gv[8 * q4 + 3]);
+            v.z = pack_bf16x2(__uint_as_float(r[8 * q4 + 4]) * gv[8 * q4 + 4], __uint_as_float(r[8 * q4 + 5]) * gv[8 * q4 + 5]);
+            v.w = pack_bf16x2(__uint_as_float(r[8 * q4 + 6]) * gv[8 * q4 + 6], __uint_as_float(r[8 * q4 + 7]) * gv[8 * q4 + 7]);
+            dst[q4] = v;
+        }
+    }
+}
+
+// ----------------------------------------------------------------- kernel
+
+template <int D>
+__global__ void __launch_bounds__(PairCfg<D>::THREADS, 1)
+    prefill_pair_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                        const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmG,
+                        const __grid_constant__ PrefillParams p) {
+    using C = PairCfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = smem_u32(smem);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const PairBars bars{sbase + C::OFF_BAR, C::NSK, C::NSV};
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
+    const uint32_t cr = cluster_ctarank();
+
+    // one cluster per (query tile, batch, head pair), heaviest query tiles first
+    const int n_hp = p.H / 2;
+    const int pairs = p.B * n_hp;
+    const int u = (int)(blockIdx.x >> 1);
+    const int qt = p.n_qtiles - 1 - u / pairs;
+    const int bp = u % pairs;
+    const int b = bp / n_hp;
+    const int h = 2 * (bp % n_hp) + (int)cr;
+    const int g = h / (p.H / p.G);
+    const int q_end = min(p.S, (qt + 1) * C::BM);
+    const int n_kv = (q_end + C::BN - 1) / C::BN;
+
+    if (threadIdx.x == 0) {
+        const uint32_t full_count = cr == 0 ? 2u : 1u;
+        for (int s = 0; s < C::NSK; ++s) {
+            mbar_init(bars.k_full(s), full_count);
+            mbar_init(bars.k_empty(s), 1);
+        }
+        for (int s = 0; s < C::NSV; ++s) {
+            mbar_init(bars.v_full(s), full_count);
+            mbar_init(bars.v_empty(s), 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(bars.s_full(i), 1);
+            mbar_init(bars.p_full(i), C::P_ARRIVALS);
+        }
+        mbar_init(bars.pv_done(), 1);
+        mbar_init(bars.o_final(), 1);
+        mbar_init(bars.q_ready(), C::Q_ARRIVALS);
+        mbar_init(bars.q_full(), 1);
+        mbar_init(bars.g_full(), 1);
+        mbar_init(bars.drain(), 1);
+        for (int q = 0; q < 4; ++q) mbar_init(bars.xchg(q), 2);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmQ);
+        tma_prefetch_desc(&tmK);
+        tma_prefetch_desc(&tmV);
+    }
+    if (warp == 1) {
+        tmem_alloc2(smem_u32(tmem_slot), C::TM_COLS);
+        tmem_relinquish2();
+    }
+    // both CTAs' barriers are initialised and the pair's TMEM allocated before any
+    // cross-CTA arrival or MMA
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync_all();
+    tc_fence_after();
+    const uint32_t tm = *tmem_slot;
+
+    if (warp == 0) {
+        if (lane == 0)
+            pair_producer<D>(&tmK, &tmV, &tmQ, &tmG, p.qnorm_w, bars, sbase, n_kv, b, g, h, qt, p.G, cr,
+                             p.gate_mode == GATTN_GATE_ELEMENTWISE, abort_flag, p.status);
+        __syncwarp();
+    } else if (warp == 1) {
+        if (lane == 0) {
+            if (cr == 0) pair_mma<D>(bars, sbase, tm, n_kv, abort_flag, p.status);
+            else pair_forwarder<D>(bars, n_kv, abort_flag, p.status);
+        }
+        __syncwarp();
+    } else {
+        pair_softmax<D>(p, bars, sbase, smem + C::OFF_X, tm, cr, warp & 3, (warp - 2) >> 2, lane, qt, b, h, n_kv,
+                        abort_flag);
+    }
+    // both CTAs are done with the pair's TMEM (the issuer drained every MMA) before it is released
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync_all();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc2(tm, C::TM_COLS);
+    }
+}
+
+template <int D>
+cudaError_t launch_pair_d(const PrefillParams& p, const PrefillMaps& maps, cudaStream_t stream, cudaEvent_t ev_start,
+                          cudaEvent_t ev_stop) {
+    using C = PairCfg<D>;
+    cudaError_t e = set_smem_once(reinterpret_cast<const void*>(prefill_pair_kernel<D>), C::SMEM_ALLOC);
+    if (e != cudaSuccess) return e;
+    const long long blocks = 2LL * p.n_qtiles * p.B * (p.H / 2);
+    if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
+    if (ev_start) cudaEventRecord(ev_start, stream);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)blocks);
+    cfg.blockDim = dim3(C::THREADS);
+    cfg.dynamicSmemBytes = C::SMEM_ALLOC;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    cudaError_t err = cudaLaunchKernelEx(&cfg, prefill_pair_kernel<D>, maps.k, maps.v, maps.q, maps.gate, p);
+    if (ev_stop) cudaEventRecord(ev_stop, stream);
+    return err;
+}
+
+}  // namespace
+
+// d = 256 only: at d = 128 the one-head kernel (64-column P and S in TMEM, two
+// score buffers) is faster, the softmax rather than K/V traffic being its bound.
+bool prefill_pair_supported(int d, int H, int G) { return d == 256 && ((H / G) % 2 == 0); }
+int prefill_pair_key_rows() { return PairCfg<256>::KH; }
+int prefill_pair_value_rows() { return PairCfg<256>::BN; }
+
+cudaError_t launch_prefill_pair(const PrefillParams& p, const PrefillMaps& maps, cudaStream_t stream,
+                                cudaEvent_t ev_start, cudaEvent_t ev_stop) {
+    if (p.d == 256) return launch_pair_d<256>(p, maps, stream, ev_start, ev_stop);
+    if (p.d == 128) return launch_pair_d<128>(p, maps, stream, ev_start, ev_stop);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace gattn
