@@ -54,14 +54,37 @@
 namespace gattn {
 namespace {
 
+struct PairBars {
+    uint32_t base;
+    __device__ uint32_t at(int i) const { return base + 8u * (uint32_t)i; }
+    // k_full / v_full: in the even CTA they expect two arrivals (its own producer's,
+    // carrying the bytes, and the odd CTA's forward); in the odd CTA one.
+    __device__ uint32_t k_full(int s) const { return at(s); }
+    __device__ uint32_t v_full(int s) const { return at(2 + s); }
+    // QK(j) complete, j % 2 == i (both CTAs): S_j is in score buffer i and K' stage i is free
+    __device__ uint32_t s_full(int i) const { return at(4 + i); }
+    __device__ uint32_t p_full(int i) const { return at(6 + i); }   // P_j of both CTAs in buffer i (even CTA)
+    // PV(j) complete, j % 2 == i (both CTAs): V stage i is free, O holds the tiles up to j
+    __device__ uint32_t pv_done(int i) const { return at(8 + i); }
+    __device__ uint32_t o_final() const { return at(10); }          // every PV complete (both CTAs)
+    __device__ uint32_t q_ready() const { return at(11); }          // Q' of both CTAs written (even CTA)
+    __device__ uint32_t q_full() const { return at(12); }           // raw Q tile + weights landed
+    __device__ uint32_t g_full() const { return at(13); }           // gate tile landed
+    __device__ uint32_t drain() const { return at(14); }            // the issuer's MMAs all complete
+    __device__ uint32_t xchg(int q) const { return at(15 + q); }    // both halves of row quarter q posted
+    static constexpr int COUNT = 19;
+};
+
 template <int D>
 struct PairCfg {
     static constexpr int BM = 128;        // query rows per CTA
     static constexpr int BN = 128;        // keys per tile
     static constexpr int KH = BN / 2;     // keys of a K' tile held by one CTA
     static constexpr int DH = D / 2;      // value columns held by one CTA
-    static constexpr int NSK = D == 256 ? 2 : 4;  // K' ring stages
-    static constexpr int NSV = D == 256 ? 2 : 4;  // V ring stages
+    // two stages each: stage j % 2 is released by the completion of QK(j) / PV(j),
+    // the same commits that hand S_j to the softmax and close O's tile j
+    static constexpr int NSK = 2;  // K' ring stages
+    static constexpr int NSV = 2;  // V ring stages
     static constexpr int KCH = D / 64;    // 128-byte chunks of a K' row
     static constexpr int K_CHUNK = KH * 128;
     static constexpr int K_TILE = KCH * K_CHUNK;
@@ -79,7 +102,7 @@ struct PairCfg {
     static constexpr int OFF_K = QTILE_BYTES;
     static constexpr int OFF_V = OFF_K + NSK * K_TILE;
     static constexpr int OFF_BAR = OFF_V + NSV * V_TILE;
-    static constexpr int NBAR = 2 * NSK + 2 * NSV + 14;
+    static constexpr int NBAR = PairBars::COUNT;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr int OFF_W = (OFF_MISC + 16 + 127) & ~127;
     // row-half exchange: tile maxima [2 buffers][2 halves][BM] and row sums [2 halves][BM]
@@ -95,28 +118,6 @@ struct PairCfg {
     static constexpr uint32_t IDESC_QK = make_idesc_bf16(256, BN, false);
     static constexpr uint32_t IDESC_PV = make_idesc_bf16(256, D, true);
     static constexpr float RESCALE_THRESHOLD = 8.0f;  // log2 domain
-};
-
-struct PairBars {
-    uint32_t base;
-    int nsk, nsv;
-    __device__ uint32_t at(int i) const { return base + 8u * (uint32_t)i; }
-    // k_full / v_full: in the even CTA they expect two arrivals (its own producer's,
-    // carrying the bytes, and the odd CTA's forward); in the odd CTA one.
-    __device__ uint32_t k_full(int s) const { return at(s); }
-    __device__ uint32_t k_empty(int s) const { return at(nsk + s); }
-    __device__ uint32_t v_full(int s) const { return at(2 * nsk + s); }
-    __device__ uint32_t v_empty(int s) const { return at(2 * nsk + nsv + s); }
-    __device__ int r() const { return 2 * nsk + 2 * nsv; }
-    __device__ uint32_t s_full(int i) const { return at(r() + i); }      // S_j in buffer i = j % 2 (both CTAs)
-    __device__ uint32_t p_full(int i) const { return at(r() + 2 + i); }  // P_j of both CTAs in buffer i (even CTA)
-    __device__ uint32_t pv_done() const { return at(r() + 4); }          // PV_j complete (both CTAs)
-    __device__ uint32_t o_final() const { return at(r() + 5); }          // every PV complete (both CTAs)
-    __device__ uint32_t q_ready() const { return at(r() + 6); }          // Q' of both CTAs written (even CTA)
-    __device__ uint32_t q_full() const { return at(r() + 7); }           // raw Q tile + weights landed
-    __device__ uint32_t g_full() const { return at(r() + 8); }           // gate tile landed
-    __device__ uint32_t drain() const { return at(r() + 9); }            // the issuer's MMAs all complete
-    __device__ uint32_t xchg(int q) const { return at(r() + 10 + q); }   // both halves of row quarter q posted
 };
 
 // Arrive on the even CTA's copy of barrier `bar`: locally from the even CTA, at
@@ -141,6 +142,12 @@ __device__ void pair_producer(const CUtensorMap* tmK, const CUtensorMap* tmV, co
     for (int c = 0; c < C::KCH; ++c)
         tma_load_4d(sbase + C::OFF_Q + c * C::ROWBOX_BYTES, tmQ, bars.q_full(), c * 64, h, qt * C::BM, b);
 
+    // the gate tile is read at the very end: start it on its way to L2 now
+    if (gate_tile) {
+#pragma unroll
+        for (int c = 0; c < C::KCH; ++c) tma_prefetch_l2_4d(tmG, c * 64, h, qt * C::BM, b);
+    }
+
     // K' comes from the pre-pass kernel launched just before this one
     pdl_wait_prerequisites();
 
@@ -150,7 +157,7 @@ __device__ void pair_producer(const CUtensorMap* tmK, const CUtensorMap* tmV, co
     while (nk < n_kv || nv < n_kv) {
         bool progressed = false;
         if (nk < n_kv &&
-            (nk < C::NSK || mbar_try_wait(bars.k_empty(nk % C::NSK), ((uint32_t)(nk / C::NSK) & 1u) ^ 1u))) {
+            (nk < C::NSK || mbar_try_wait(bars.s_full(nk % C::NSK), ((uint32_t)(nk / C::NSK) & 1u) ^ 1u))) {
             const int st = nk % C::NSK;
             mbar_arrive_expect_tx(bars.k_full(st), C::K_TILE);
             const uint32_t kdst = sbase + C::OFF_K + st * C::K_TILE;
@@ -162,7 +169,7 @@ __device__ void pair_producer(const CUtensorMap* tmK, const CUtensorMap* tmV, co
             progressed = true;
         }
         if (nv < n_kv &&
-            (nv < C::NSV || mbar_try_wait(bars.v_empty(nv % C::NSV), ((uint32_t)(nv / C::NSV) & 1u) ^ 1u))) {
+            (nv < C::NSV || mbar_try_wait(bars.pv_done(nv % C::NSV), ((uint32_t)(nv / C::NSV) & 1u) ^ 1u))) {
             const int st = nv % C::NSV;
             mbar_arrive_expect_tx(bars.v_full(st), C::V_TILE);
             const uint32_t vdst = sbase + C::OFF_V + st * C::V_TILE;
@@ -190,7 +197,7 @@ __device__ void pair_producer(const CUtensorMap* tmK, const CUtensorMap* tmV, co
     if (gate_tile && nk == n_kv) {
         bool ok = true;
         for (int j = n_kv > C::NSK ? n_kv - C::NSK : 0; ok && j < n_kv; ++j)
-            ok = mbar_wait(bars.k_empty(j % C::NSK), (uint32_t)(j / C::NSK) & 1u, abort_flag, status);
+            ok = mbar_wait(bars.s_full(j % C::NSK), (uint32_t)(j / C::NSK) & 1u, abort_flag, status);
         if (ok) {
             mbar_arrive_expect_tx(bars.g_full(), C::QTILE_BYTES);
 #pragma unroll
@@ -244,52 +251,81 @@ __device__ void pair_forwarder(const PairBars& bars, int n_kv, volatile int* abo
 
 // ----------------------------------------------------------------- MMA issuer (even CTA)
 
+// Issue order QK(0), QK(1), then per tile PV(j), QK(j+2).  One thread can put an
+// MMA into the tensor queue only every ~47 cycles, and the queue is mostly full,
+// so the issuer runs almost in step with the pipe: the inputs of the next MMA
+// group are polled while the tail of the current one is still queued, so that
+// the commits and waits between groups do not leave the pipe idle.
 template <int D>
 __device__ void pair_mma(const PairBars& bars, uint32_t sbase, uint32_t tm, int n_kv, volatile int* abort_flag,
                          unsigned int* status) {
     using C = PairCfg<D>;
+    constexpr int QK_MMAS = D / 16, PV_MMAS = C::BN / 16;
+    constexpr int QK_HEAD = QK_MMAS - 4, PV_HEAD = PV_MMAS - 2;  // issued before polling the next group's inputs
     const uint64_t qdesc0 = make_sdesc_sw128(sbase + C::OFF_Q, 16, 1024);
     const uint64_t kdesc0 = make_sdesc_sw128(sbase + C::OFF_K, 16, 1024);
     const uint64_t vdesc0 = make_sdesc_sw128(sbase + C::OFF_V, C::V_CHUNK, 1024);
-    // S_j = Q' K'_j^T into score buffer j % 2
-    auto issue_qk = [&](int j) -> bool {
-        const int st = j % C::NSK;
-        if (!mbar_wait(bars.k_full(st), (uint32_t)(j / C::NSK) & 1u, abort_flag, status)) return false;
-        tc_fence_after();
-        const uint64_t kd = kdesc0 + (uint64_t)((st * C::K_TILE) >> 4);
+    // S_j = Q' K'_j^T into score buffer j % 2, MMAs [k0, k1) of the group
+    auto qk = [&](int j, int k0, int k1) {
+        const uint64_t kd = kdesc0 + (uint64_t)(((j % C::NSK) * C::K_TILE) >> 4);
         const uint32_t d_tmem = tm + C::TM_S + (uint32_t)(j & 1) * C::BN;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-            mma2_ss(d_tmem, qdesc0 + (uint64_t)(((kk >> 2) * C::ROWBOX_BYTES + (kk & 3) * 32) >> 4),
-                    kd + (uint64_t)(((kk >> 2) * C::K_CHUNK + (kk & 3) * 32) >> 4), C::IDESC_QK, kk > 0 ? 1u : 0u);
-        tc_commit2(bars.k_empty(st), 3);
-        tc_commit2(bars.s_full(j & 1), 3);
-        return true;
+        for (int kk = 0; kk < QK_MMAS; ++kk)
+            if (kk >= k0 && kk < k1)
+                mma2_ss(d_tmem, qdesc0 + (uint64_t)(((kk >> 2) * C::ROWBOX_BYTES + (kk & 3) * 32) >> 4),
+                        kd + (uint64_t)(((kk >> 2) * C::K_CHUNK + (kk & 3) * 32) >> 4), C::IDESC_QK, kk > 0 ? 1u : 0u);
     };
     // O += P_j V_j, P_j read from TMEM where it overwrote S_j
-    auto issue_pv = [&](int j) -> bool {
-        if (!mbar_wait(bars.p_full(j & 1), (uint32_t)(j >> 1) & 1u, abort_flag, status)) return false;
-        const int st = j % C::NSV;
-        if (!mbar_wait(bars.v_full(st), (uint32_t)(j / C::NSV) & 1u, abort_flag, status)) return false;
-        tc_fence_after();
-        const uint64_t vd = vdesc0 + (uint64_t)((st * C::V_TILE) >> 4);
+    auto pv = [&](int j, int k0, int k1) {
+        const uint64_t vd = vdesc0 + (uint64_t)(((j % C::NSV) * C::V_TILE) >> 4);
         const uint32_t p_tmem = tm + C::TM_S + (uint32_t)(j & 1) * C::BN;
 #pragma unroll
-        for (int kk = 0; kk < C::BN / 16; ++kk)
-            mma2_ts(tm + C::TM_O, p_tmem + kk * 8, vd + (uint64_t)((kk * 16 * 128) >> 4), C::IDESC_PV,
-                    (j > 0 || kk > 0) ? 1u : 0u);
-        tc_commit2(bars.v_empty(st), 3);
-        tc_commit2(bars.pv_done(), 3);
-        return true;
+        for (int kk = 0; kk < PV_MMAS; ++kk)
+            if (kk >= k0 && kk < k1)
+                mma2_ts(tm + C::TM_O, p_tmem + kk * 8, vd + (uint64_t)((kk * 16 * 128) >> 4), C::IDESC_PV,
+                        (j > 0 || kk > 0) ? 1u : 0u);
     };
+    auto k_ready = [&](int j) { return mbar_try_wait(bars.k_full(j % C::NSK), (uint32_t)(j / C::NSK) & 1u); };
+    auto k_wait = [&](int j) { return mbar_wait(bars.k_full(j % C::NSK), (uint32_t)(j / C::NSK) & 1u, abort_flag, status); };
+    auto pv_ready = [&](int j) {
+        return mbar_try_wait(bars.p_full(j & 1), (uint32_t)(j >> 1) & 1u) &&
+               mbar_try_wait(bars.v_full(j % C::NSV), (uint32_t)(j / C::NSV) & 1u);
+    };
+    auto pv_wait = [&](int j) {
+        return mbar_wait(bars.p_full(j & 1), (uint32_t)(j >> 1) & 1u, abort_flag, status) &&
+               mbar_wait(bars.v_full(j % C::NSV), (uint32_t)(j / C::NSV) & 1u, abort_flag, status);
+    };
+
     bool ok = mbar_wait(bars.q_ready(), 0, abort_flag, status);  // Q' of both heads in shared memory
-    tc_fence_after();
-    if (ok && n_kv > 0) ok = issue_qk(0);
-    if (ok && n_kv > 1) ok = issue_qk(1);
+    for (int j = 0; ok && j < 2 && j < n_kv; ++j) {
+        ok = k_wait(j);
+        if (!ok) break;
+        tc_fence_after();
+        qk(j, 0, QK_MMAS);
+        tc_commit2(bars.s_full(j & 1), 3);
+    }
+    if (ok && n_kv > 0) ok = pv_wait(0);
     for (int j = 0; ok && j < n_kv; ++j) {
-        if (!issue_pv(j)) { ok = false; break; }
-        // S_{j%2} is free again behind PV(j), which reads P_j from it
-        if (j + 2 < n_kv && !issue_qk(j + 2)) { ok = false; break; }
+        // ---- PV(j): its inputs were checked before
+        tc_fence_after();
+        pv(j, 0, PV_HEAD);
+        const bool more = j + 2 < n_kv;
+        const bool kr = more && k_ready(j + 2);
+        pv(j, PV_HEAD, PV_MMAS);
+        tc_commit2(bars.pv_done(j & 1), 3);
+        // ---- QK(j+2) into the buffer PV(j) has just been queued to read
+        if (more) {
+            if (!kr && !k_wait(j + 2)) { ok = false; break; }
+            tc_fence_after();
+            qk(j + 2, 0, QK_HEAD);
+        }
+        const bool next = j + 1 < n_kv;
+        const bool pr = next && pv_ready(j + 1);
+        if (more) {
+            qk(j + 2, QK_HEAD, QK_MMAS);
+            tc_commit2(bars.s_full(j & 1), 3);
+        }
+        if (next && !pr && !pv_wait(j + 1)) { ok = false; break; }
     }
     if (ok) tc_commit2(bars.o_final(), 3);
     tc_commit2(bars.drain(), 1);
@@ -313,6 +349,18 @@ __device__ void pair_softmax(const PrefillParams& p, const PairBars& bars, uint3
     const bf16* grow = static_cast<const bf16*>(p.gate) + tok * p.gate_tok_stride + (int64_t)h * p.gate_head_stride;
     float gate_head = 1.f;
     if (p.gate_mode == GATTN_GATE_HEADWISE && valid) gate_head = sigmoidf_dev(__bfloat162float(grow[0]));
+
+    // the two threads of a row swap values through shared memory and then meet on
+    // an mbarrier (one phase per use: the prologue, every tile, the row sums)
+    float* xmax = reinterpret_cast<float*>(smem_x);          // [2][2][BM]
+    float* xsum = xmax + 2 * 2 * C::BM;                      // [2][BM]
+    const uint32_t xbar = bars.xchg(quarter);
+    int xphase = 0;
+    auto meet = [&]() -> bool {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(xbar);
+        return __all_sync(0xffffffffu, mbar_wait(xbar, (uint32_t)(xphase++) & 1u, abort_flag, p.status));
+    };
 
     // ---- fused Q prologue (first-half threads): rmsnorm then partial rotate-half
     // RoPE, written as bf16 over the raw row in the Q tile (the A operand of
@@ -371,16 +419,6 @@ __device__ void pair_softmax(const PrefillParams& p, const PairBars& bars, uint3
     // [hf D/2, (hf+1) D/2); its partner (same row, other half) runs in warp +- 4.
     const float sl2 = p.scale_log2;
     const int row_min = qt * C::BM;
-    float* xmax = reinterpret_cast<float*>(smem_x);          // [2][2][BM]
-    float* xsum = xmax + 2 * 2 * C::BM;                      // [2][BM]
-    // the two warps of a row quarter post to shared memory, then meet on an
-    // mbarrier (one phase per tile, one more for the row sums; bounded wait)
-    const uint32_t xbar = bars.xchg(quarter);
-    auto meet = [&](int phase) -> bool {
-        __syncwarp();
-        if (lane == 0) mbar_arrive(xbar);
-        return __all_sync(0xffffffffu, mbar_wait(xbar, (uint32_t)phase & 1u, abort_flag, p.status));
-    };
     float m_ref = -INFINITY;  // reference max (log2 domain) shared by O and l
     float l = 0.f;            // this half's share of the row sum
     for (int j = 0; j < n_kv; ++j) {
@@ -411,7 +449,7 @@ __device__ void pair_softmax(const PrefillParams& p, const PairBars& bars, uint3
         // partner still reading tile j-1 is never overwritten).  Passing the meet also
         // means the partner has read its S columns, which P overwrites below.
         xmax[((j & 1) * 2 + hf) * C::BM + row] = mt;
-        if (!meet(j)) return;
+        if (!meet()) return;
         mt = fmaxf(mt, xmax[((j & 1) * 2 + (hf ^ 1)) * C::BM + row]);
         const float m_new = fmaxf(m_ref, mt * sl2);
         const bool need = (m_new - m_ref) > C::RESCALE_THRESHOLD;
@@ -426,7 +464,8 @@ __device__ void pair_softmax(const PrefillParams& p, const PairBars& bars, uint3
             __syncwarp();
             // O is touched only once PV(j-1) has landed (PV(j-2) already had: QK(j)
             // was issued behind it)
-            if (!__all_sync(0xffffffffu, mbar_wait(bars.pv_done(), (uint32_t)(j - 1) & 1u, abort_flag, p.status)))
+            if (!__all_sync(0xffffffffu, mbar_wait(bars.pv_done((j - 1) & 1), (uint32_t)((j - 1) >> 1) & 1u,
+                                                   abort_flag, p.status)))
                 return;
             tc_fence_after();
 #pragma unroll 1
@@ -460,7 +499,7 @@ __device__ void pair_softmax(const PrefillParams& p, const PairBars& bars, uint3
 
     // ---- epilogue: O / l * sigmoid(gate) -> bf16 [B,S,H*d], this thread's half of the columns
     xsum[hf * C::BM + row] = l;
-    if (!meet(n_kv)) return;
+    if (!meet()) return;
     const float l_row = xsum[row] + xsum[C::BM + row];
     if (!__all_sync(0xffffffffu, mbar_wait(bars.o_final(), 0, abort_flag, p.status))) return;
     const bool elementwise = p.gate_mode == GATTN_GATE_ELEMENTWISE;
@@ -483,7 +522,7 @@ __device__ void pair_softmax(const PrefillParams& p, const PairBars& bars, uint3
                 float f[8];
                 unpack8(lds_v4(rowtile_addr(gbase, row, c + 8 * q4)), f);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) gv[8 * q4 + e] = inv_l * sigmoidf_dev(f[e]);
+                for (int e = 0; e < 8; ++e) gv[8 * q4 + e] = inv_l * sigmoid_tanh(f[e]);
             }
         } else {
 #pragma unroll
@@ -514,7 +553,7 @@ __global__ void __launch_bounds__(PairCfg<D>::THREADS, 1)
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const PairBars bars{sbase + C::OFF_BAR, C::NSK, C::NSV};
+    const PairBars bars{sbase + C::OFF_BAR};
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
     const uint32_t cr = cluster_ctarank();
@@ -533,19 +572,13 @@ __global__ void __launch_bounds__(PairCfg<D>::THREADS, 1)
 
     if (threadIdx.x == 0) {
         const uint32_t full_count = cr == 0 ? 2u : 1u;
-        for (int s = 0; s < C::NSK; ++s) {
-            mbar_init(bars.k_full(s), full_count);
-            mbar_init(bars.k_empty(s), 1);
-        }
-        for (int s = 0; s < C::NSV; ++s) {
-            mbar_init(bars.v_full(s), full_count);
-            mbar_init(bars.v_empty(s), 1);
-        }
         for (int i = 0; i < 2; ++i) {
+            mbar_init(bars.k_full(i), full_count);
+            mbar_init(bars.v_full(i), full_count);
             mbar_init(bars.s_full(i), 1);
             mbar_init(bars.p_full(i), C::P_ARRIVALS);
+            mbar_init(bars.pv_done(i), 1);
         }
-        mbar_init(bars.pv_done(), 1);
         mbar_init(bars.o_final(), 1);
         mbar_init(bars.q_ready(), C::Q_ARRIVALS);
         mbar_init(bars.q_full(), 1);
