@@ -249,6 +249,9 @@ gattn_status gattn_prefill(const void* q, const void* k, const void* v, const vo
         } else {
             maps.gate = maps.q;  // never read
         }
+        // out [B,S,H*d] seen as (d, H, S, B)
+        const uint64_t ostr[3] = {(uint64_t)d * 2, (uint64_t)H * d * 2, (uint64_t)S * H * d * 2};
+        if (!encode_bf16_map(&maps.out, out, 4, hdims, ostr, rbox)) return GATTN_ERR_CUDA;
         PrefillParams pp;
         std::memset(&pp, 0, sizeof(pp));
         pp.q = q;
@@ -268,6 +271,7 @@ gattn_status gattn_prefill(const void* q, const void* k, const void* v, const vo
         pp.rd = rotary_dim;
         pp.gate_mode = gate_mode;
         pp.n_qtiles = (S + 127) / 128;
+        pp.n_sms = sm_count();
         pp.eps = eps;
         pp.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)d));
         pp.status = status;

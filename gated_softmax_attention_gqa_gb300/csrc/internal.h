@@ -33,6 +33,7 @@ struct PrefillParams {
     void* out;
     int64_t q_tok_stride, q_head_stride, gate_tok_stride, gate_head_stride;
     int B, S, H, G, d, rd, gate_mode, n_qtiles;
+    int n_sms;  // multiprocessors of the device (persistent grids)
     float eps, scale_log2;
     unsigned int* status;
     float inv_freq[kMaxRotaryHalf];
@@ -64,10 +65,10 @@ struct DecodeParams {
     float inv_freq[kMaxRotaryHalf];
 };
 
-// TMA descriptors of the tcgen05 prefill: normed keys (workspace), raw V, raw Q
-// and (elementwise gate only) the gate logits; all bf16, 64-element inner boxes.
+// TMA descriptors of the tcgen05 prefill: normed keys (workspace), raw V, raw Q,
+// (elementwise gate only) the gate logits and the output; all bf16, 64-element inner boxes.
 struct PrefillMaps {
-    CUtensorMap k, v, q, gate;
+    CUtensorMap k, v, q, gate, out;  // out: [B,S,H*d] as (d, H, S, B), written by TMA stores (pair kernel)
 };
 
 cudaError_t launch_prologue(const ProloguePlan& p, bool bf16_in, bool bf16_out, cudaStream_t stream);

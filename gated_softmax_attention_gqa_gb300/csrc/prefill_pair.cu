@@ -72,7 +72,10 @@ struct PairBars {
     __device__ uint32_t g_full() const { return at(13); }           // gate tile landed
     __device__ uint32_t drain() const { return at(14); }            // the issuer's MMAs all complete
     __device__ uint32_t xchg(int q) const { return at(15 + q); }    // both halves of row quarter q posted
-    static constexpr int COUNT = 19;
+    __device__ uint32_t o_free() const { return at(19); }   // an item's epilogue has read O (even CTA, both CTAs arrive)
+    __device__ uint32_t e_done() const { return at(20); }   // (unused)
+    __device__ uint32_t o_staged() const { return at(21); } // every softmax warp staged its output rows (this CTA)
+    static constexpr int COUNT = 22;
 };
 
 template <int D>
@@ -127,98 +130,165 @@ __device__ __forceinline__ void arrive_even(uint32_t bar, uint32_t cr) {
     else mbar_arrive_remote_cta(mapa_shared(bar, 0));
 }
 
+// ----------------------------------------------------------------- work items
+
+// The grid is persistent: one cluster per pair of SMs at most.  Work item u is
+// query tile n_qtiles - 1 - u / (B*H/2) (heaviest first) of batch and head pair
+// u % (B*H/2); cluster cl of ncl takes items cl, 2 ncl - 1 - cl, 2 ncl + cl, ...
+// (a snake over rounds, so that heavy and light tiles share a cluster).  Every
+// role walks the same list; ring stages, score buffers and barrier phases run on
+// a tile counter that continues across items.
+struct PairItem {
+    int qt, b, hp, n_kv;
+};
+
+__device__ __forceinline__ bool pair_item(const PrefillParams& p, int cl, int ncl, int r, PairItem& it) {
+    const int n_hp = p.H / 2, pairs = p.B * n_hp;
+    const long long u = (long long)r * ncl + ((r & 1) ? ncl - 1 - cl : cl);
+    if (u >= (long long)p.n_qtiles * pairs) return false;
+    it.qt = p.n_qtiles - 1 - (int)(u / pairs);
+    const int bp = (int)(u % pairs);
+    it.b = bp / n_hp;
+    it.hp = bp % n_hp;
+    it.n_kv = (min(p.S, (it.qt + 1) * 128) + 127) / 128;
+    return true;
+}
+
 // ----------------------------------------------------------------- producer
 
 template <int D>
 __device__ void pair_producer(const CUtensorMap* tmK, const CUtensorMap* tmV, const CUtensorMap* tmQ,
-                              const CUtensorMap* tmG, const void* qnorm_w, const PairBars& bars, uint32_t sbase,
-                              int n_kv, int b, int g, int h, int qt, int G, uint32_t cr, bool gate_tile,
-                              volatile int* abort_flag, unsigned int* status) {
+                              const CUtensorMap* tmG, const CUtensorMap* tmO, const PrefillParams& p,
+                              const PairBars& bars, uint32_t sbase, int cl, int ncl, uint32_t cr, volatile int* abort_flag,
+                              unsigned int* status) {
     using C = PairCfg<D>;
-    // raw Q tile of this CTA's head (normalised in place later), the weights next to it
-    mbar_arrive_expect_tx(bars.q_full(), C::QTILE_BYTES + D * 2);
-    bulk_load(sbase + C::OFF_W, qnorm_w, D * 2, bars.q_full());
+    const bool gate_tile = p.gate_mode == GATTN_GATE_ELEMENTWISE;
+    int nk = 0, nv = 0;  // K' / V tiles issued, over all items
+    int jb = 0;          // tiles of the items before the current one
+    int n_it = 0, n_g = 0;
+    bool ok = true;
+    PairItem it;
+    int prev_h = 0, prev_qt = 0, prev_b = 0;
+    // the softmax warps staged item k's output rows in the K' ring: write them out
+    // (TMA stores, rows past the end clipped) and wait until the copies have read
+    // shared memory, after which the K' ring may be refilled
+    auto store_output = [&](int k, int h, int qt, int b) -> bool {
+        if (!mbar_wait(bars.o_staged(), (uint32_t)k & 1u, abort_flag, status)) return false;
 #pragma unroll
-    for (int c = 0; c < C::KCH; ++c)
-        tma_load_4d(sbase + C::OFF_Q + c * C::ROWBOX_BYTES, tmQ, bars.q_full(), c * 64, h, qt * C::BM, b);
-
-    // the gate tile is read at the very end: start it on its way to L2 now
-    if (gate_tile) {
+        for (int c = 0; c < C::KCH; ++c)
+            tma_store_4d(tmO, sbase + C::OFF_K + c * C::ROWBOX_BYTES, c * 64, h, qt * C::BM, b);
+        bulk_commit_group();
+        bulk_wait_group_read0();
+        return true;
+    };
+    for (int r = 0; ok && pair_item(p, cl, ncl, r, it); ++r) {
+        const int h = 2 * it.hp + (int)cr, g = h / (p.H / p.G);
+        // raw Q tile of this CTA's head (normalised in place later): the Q buffer is
+        // free once every QK of the previous item has completed
+        if (n_it > 0 && !(ok = mbar_wait(bars.s_full((jb - 1) & 1), (uint32_t)((jb - 1) >> 1) & 1u, abort_flag, status)))
+            break;
+        mbar_arrive_expect_tx(bars.q_full(), C::QTILE_BYTES + (n_it == 0 ? D * 2 : 0));
+        if (n_it == 0) bulk_load(sbase + C::OFF_W, p.qnorm_w, D * 2, bars.q_full());
 #pragma unroll
-        for (int c = 0; c < C::KCH; ++c) tma_prefetch_l2_4d(tmG, c * 64, h, qt * C::BM, b);
-    }
-
-    // K' comes from the pre-pass kernel launched just before this one
-    pdl_wait_prerequisites();
-
-    int nk = 0, nv = 0;
-    const unsigned long long t0 = global_timer_ns();
-    uint32_t spins = 0;
-    while (nk < n_kv || nv < n_kv) {
-        bool progressed = false;
-        if (nk < n_kv &&
-            (nk < C::NSK || mbar_try_wait(bars.s_full(nk % C::NSK), ((uint32_t)(nk / C::NSK) & 1u) ^ 1u))) {
-            const int st = nk % C::NSK;
-            mbar_arrive_expect_tx(bars.k_full(st), C::K_TILE);
-            const uint32_t kdst = sbase + C::OFF_K + st * C::K_TILE;
+        for (int c = 0; c < C::KCH; ++c)
+            tma_load_4d(sbase + C::OFF_Q + c * C::ROWBOX_BYTES, tmQ, bars.q_full(), c * 64, h, it.qt * C::BM, it.b);
+        ++n_it;
+        // the gate tile is read at the very end of the item: start it on its way to L2 now
+        if (gate_tile) {
 #pragma unroll
-            for (int c = 0; c < C::KCH; ++c)
-                tma_load_3d(kdst + c * C::K_CHUNK, tmK, bars.k_full(st), c * 64, nk * C::BN + (int)cr * C::KH,
-                            b * G + g);
-            ++nk;
-            progressed = true;
+            for (int c = 0; c < C::KCH; ++c) tma_prefetch_l2_4d(tmG, c * 64, h, it.qt * C::BM, it.b);
         }
-        if (nv < n_kv &&
-            (nv < C::NSV || mbar_try_wait(bars.pv_done(nv % C::NSV), ((uint32_t)(nv / C::NSV) & 1u) ^ 1u))) {
-            const int st = nv % C::NSV;
-            mbar_arrive_expect_tx(bars.v_full(st), C::V_TILE);
-            const uint32_t vdst = sbase + C::OFF_V + st * C::V_TILE;
+        // K' comes from the pre-pass kernel launched just before this one
+        if (n_it == 1) pdl_wait_prerequisites();
+
+        // K' and V tiles, each stream as soon as its own stage frees up; the K' ring
+        // holds the previous item's gate and output tiles until they are written out
+        bool k_open = n_it == 1;
+        const int ke = nk + it.n_kv, ve = nv + it.n_kv;
+        const unsigned long long t0 = global_timer_ns();
+        uint32_t spins = 0;
+        while (nk < ke || nv < ve) {
+            bool progressed = false;
+            if (!k_open && mbar_try_wait(bars.o_staged(), (uint32_t)(n_it - 2) & 1u)) {
+                if (!store_output(n_it - 2, prev_h, prev_qt, prev_b)) break;
+                k_open = true;
+            }
+            if (k_open && nk < ke &&
+                (nk < C::NSK || mbar_try_wait(bars.s_full(nk % C::NSK), ((uint32_t)(nk / C::NSK) & 1u) ^ 1u))) {
+                const int st = nk % C::NSK;
+                mbar_arrive_expect_tx(bars.k_full(st), C::K_TILE);
+                const uint32_t kdst = sbase + C::OFF_K + st * C::K_TILE;
 #pragma unroll
-            for (int c = 0; c < C::VCH; ++c)
-                tma_load_4d(vdst + c * C::V_CHUNK, tmV, bars.v_full(st), (int)cr * C::DH + c * 64, g, nv * C::BN, b);
-            ++nv;
-            progressed = true;
-        }
-        if (progressed) {
-            spins = 0;
-            continue;
-        }
-        if ((++spins & 63u) == 0) {
-            if (*abort_flag) break;
-            if (global_timer_ns() - t0 > 4 * kWaitLimitNs) {
-                *abort_flag = 1;
-                atomicOr(status, GATTN_DEVICE_TIMEOUT);
-                break;
+                for (int c = 0; c < C::KCH; ++c)
+                    tma_load_3d(kdst + c * C::K_CHUNK, tmK, bars.k_full(st), c * 64,
+                                (nk - jb) * C::BN + (int)cr * C::KH, it.b * p.G + g);
+                ++nk;
+                progressed = true;
+            }
+            if (nv < ve &&
+                (nv < C::NSV || mbar_try_wait(bars.pv_done(nv % C::NSV), ((uint32_t)(nv / C::NSV) & 1u) ^ 1u))) {
+                const int st = nv % C::NSV;
+                mbar_arrive_expect_tx(bars.v_full(st), C::V_TILE);
+                const uint32_t vdst = sbase + C::OFF_V + st * C::V_TILE;
+#pragma unroll
+                for (int c = 0; c < C::VCH; ++c)
+                    tma_load_4d(vdst + c * C::V_CHUNK, tmV, bars.v_full(st), (int)cr * C::DH + c * 64, g,
+                                (nv - jb) * C::BN, it.b);
+                ++nv;
+                progressed = true;
+            }
+            if (progressed) {
+                spins = 0;
+                continue;
+            }
+            if ((++spins & 63u) == 0) {
+                if (*abort_flag) break;
+                if (global_timer_ns() - t0 > 4 * kWaitLimitNs) {
+                    *abort_flag = 1;
+                    atomicOr(status, GATTN_DEVICE_TIMEOUT);
+                    break;
+                }
             }
         }
-    }
-    // gate tile into the K' ring once its last K' tile has been consumed
-    bool g_issued = false;
-    if (gate_tile && nk == n_kv) {
-        bool ok = true;
-        for (int j = n_kv > C::NSK ? n_kv - C::NSK : 0; ok && j < n_kv; ++j)
-            ok = mbar_wait(bars.s_full(j % C::NSK), (uint32_t)(j / C::NSK) & 1u, abort_flag, status);
-        if (ok) {
+        if (nk != ke || nv != ve || !k_open) { ok = false; break; }
+        // gate tile into the K' ring once this item's last K' tiles have been consumed
+        if (gate_tile) {
+            for (int j = ke - C::NSK > jb ? ke - C::NSK : jb; ok && j < ke; ++j)
+                ok = mbar_wait(bars.s_full(j % C::NSK), (uint32_t)(j / C::NSK) & 1u, abort_flag, status);
+            if (!ok) break;
             mbar_arrive_expect_tx(bars.g_full(), C::QTILE_BYTES);
 #pragma unroll
             for (int c = 0; c < C::KCH; ++c)
-                tma_load_4d(sbase + C::OFF_K + c * C::ROWBOX_BYTES, tmG, bars.g_full(), c * 64, h, qt * C::BM, b);
-            g_issued = true;
+                tma_load_4d(sbase + C::OFF_K + c * C::ROWBOX_BYTES, tmG, bars.g_full(), c * 64, h, it.qt * C::BM, it.b);
+            ++n_g;
         }
+        jb += it.n_kv;
+        prev_h = h;
+        prev_qt = it.qt;
+        prev_b = it.b;
+    }
+    // the last item's output
+    if (ok && n_it > 0) {
+        store_output(n_it - 1, prev_h, prev_qt, prev_b);
+        bulk_wait_group0();
     }
     // every copy this thread started lands before the CTA can exit
-    mbar_wait_drain(bars.q_full(), 0, status);
+    if (n_it > 0) mbar_wait_drain(bars.q_full(), (uint32_t)(n_it - 1) & 1u, status);
     for (int j = nk > C::NSK ? nk - C::NSK : 0; j < nk; ++j)
         mbar_wait_drain(bars.k_full(j % C::NSK), (uint32_t)(j / C::NSK) & 1u, status);
     for (int j = nv > C::NSV ? nv - C::NSV : 0; j < nv; ++j)
         mbar_wait_drain(bars.v_full(j % C::NSV), (uint32_t)(j / C::NSV) & 1u, status);
-    if (g_issued) mbar_wait_drain(bars.g_full(), 0, status);
+    if (n_g > 0) mbar_wait_drain(bars.g_full(), (uint32_t)(n_g - 1) & 1u, status);
 }
 
 // Odd CTA: tell the even CTA's issuer, in order, that each K'/V half has landed here.
 template <int D>
-__device__ void pair_forwarder(const PairBars& bars, int n_kv, volatile int* abort_flag, unsigned int* status) {
+__device__ void pair_forwarder(const PrefillParams& p, const PairBars& bars, int cl, int ncl, volatile int* abort_flag,
+                               unsigned int* status) {
     using C = PairCfg<D>;
+    int n_kv = 0;  // tiles over all of this cluster's items
+    PairItem it;
+    for (int r = 0; pair_item(p, cl, ncl, r, it); ++r) n_kv += it.n_kv;
     int fk = 0, fv = 0;
     const unsigned long long t0 = global_timer_ns();
     uint32_t spins = 0;
@@ -257,15 +327,15 @@ __device__ void pair_forwarder(const PairBars& bars, int n_kv, volatile int* abo
 // group are polled while the tail of the current one is still queued, so that
 // the commits and waits between groups do not leave the pipe idle.
 template <int D>
-__device__ void pair_mma(const PairBars& bars, uint32_t sbase, uint32_t tm, int n_kv, volatile int* abort_flag,
-                         unsigned int* status) {
+__device__ void pair_mma(const PrefillParams& p, const PairBars& bars, uint32_t sbase, uint32_t tm, int cl, int ncl,
+                         volatile int* abort_flag, unsigned int* status) {
     using C = PairCfg<D>;
     constexpr int QK_MMAS = D / 16, PV_MMAS = C::BN / 16;
     constexpr int QK_HEAD = QK_MMAS - 4, PV_HEAD = PV_MMAS - 2;  // issued before polling the next group's inputs
     const uint64_t qdesc0 = make_sdesc_sw128(sbase + C::OFF_Q, 16, 1024);
     const uint64_t kdesc0 = make_sdesc_sw128(sbase + C::OFF_K, 16, 1024);
     const uint64_t vdesc0 = make_sdesc_sw128(sbase + C::OFF_V, C::V_CHUNK, 1024);
-    // S_j = Q' K'_j^T into score buffer j % 2, MMAs [k0, k1) of the group
+    // S_j = Q' K'_j^T into score buffer j % 2, MMAs [k0, k1) of the group (j counts tiles over all items)
     auto qk = [&](int j, int k0, int k1) {
         const uint64_t kd = kdesc0 + (uint64_t)(((j % C::NSK) * C::K_TILE) >> 4);
         const uint32_t d_tmem = tm + C::TM_S + (uint32_t)(j & 1) * C::BN;
@@ -275,15 +345,15 @@ __device__ void pair_mma(const PairBars& bars, uint32_t sbase, uint32_t tm, int 
                 mma2_ss(d_tmem, qdesc0 + (uint64_t)(((kk >> 2) * C::ROWBOX_BYTES + (kk & 3) * 32) >> 4),
                         kd + (uint64_t)(((kk >> 2) * C::K_CHUNK + (kk & 3) * 32) >> 4), C::IDESC_QK, kk > 0 ? 1u : 0u);
     };
-    // O += P_j V_j, P_j read from TMEM where it overwrote S_j
-    auto pv = [&](int j, int k0, int k1) {
+    // O += P_j V_j, P_j read from TMEM where it overwrote S_j; the first tile of an item overwrites O
+    auto pv = [&](int j, bool first, int k0, int k1) {
         const uint64_t vd = vdesc0 + (uint64_t)(((j % C::NSV) * C::V_TILE) >> 4);
         const uint32_t p_tmem = tm + C::TM_S + (uint32_t)(j & 1) * C::BN;
 #pragma unroll
         for (int kk = 0; kk < PV_MMAS; ++kk)
             if (kk >= k0 && kk < k1)
                 mma2_ts(tm + C::TM_O, p_tmem + kk * 8, vd + (uint64_t)((kk * 16 * 128) >> 4), C::IDESC_PV,
-                        (j > 0 || kk > 0) ? 1u : 0u);
+                        (!first || kk > 0) ? 1u : 0u);
     };
     auto k_ready = [&](int j) { return mbar_try_wait(bars.k_full(j % C::NSK), (uint32_t)(j / C::NSK) & 1u); };
     auto k_wait = [&](int j) { return mbar_wait(bars.k_full(j % C::NSK), (uint32_t)(j / C::NSK) & 1u, abort_flag, status); };
@@ -296,38 +366,48 @@ __device__ void pair_mma(const PairBars& bars, uint32_t sbase, uint32_t tm, int 
                mbar_wait(bars.v_full(j % C::NSV), (uint32_t)(j / C::NSV) & 1u, abort_flag, status);
     };
 
-    bool ok = mbar_wait(bars.q_ready(), 0, abort_flag, status);  // Q' of both heads in shared memory
-    for (int j = 0; ok && j < 2 && j < n_kv; ++j) {
-        ok = k_wait(j);
-        if (!ok) break;
-        tc_fence_after();
-        qk(j, 0, QK_MMAS);
-        tc_commit2(bars.s_full(j & 1), 3);
-    }
-    if (ok && n_kv > 0) ok = pv_wait(0);
-    for (int j = 0; ok && j < n_kv; ++j) {
-        // ---- PV(j): its inputs were checked before
-        tc_fence_after();
-        pv(j, 0, PV_HEAD);
-        const bool more = j + 2 < n_kv;
-        const bool kr = more && k_ready(j + 2);
-        pv(j, PV_HEAD, PV_MMAS);
-        tc_commit2(bars.pv_done(j & 1), 3);
-        // ---- QK(j+2) into the buffer PV(j) has just been queued to read
-        if (more) {
-            if (!kr && !k_wait(j + 2)) { ok = false; break; }
+    bool ok = true;
+    int jb = 0, n_it = 0;
+    PairItem it;
+    for (int r = 0; ok && pair_item(p, cl, ncl, r, it); ++r, ++n_it) {
+        const int n = it.n_kv;
+        ok = mbar_wait(bars.q_ready(), (uint32_t)n_it & 1u, abort_flag, status);  // Q' of both heads ready
+        for (int j = 0; ok && j < 2 && j < n; ++j) {
+            ok = k_wait(jb + j);
+            if (!ok) break;
             tc_fence_after();
-            qk(j + 2, 0, QK_HEAD);
+            qk(jb + j, 0, QK_MMAS);
+            tc_commit2(bars.s_full((jb + j) & 1), 3);
         }
-        const bool next = j + 1 < n_kv;
-        const bool pr = next && pv_ready(j + 1);
-        if (more) {
-            qk(j + 2, QK_HEAD, QK_MMAS);
-            tc_commit2(bars.s_full(j & 1), 3);
+        // PV(0) overwrites O: the previous item's epilogue (both CTAs) must have read it
+        if (ok && n_it > 0) ok = mbar_wait(bars.o_free(), (uint32_t)(n_it - 1) & 1u, abort_flag, status);
+        if (ok && n > 0) ok = pv_wait(jb);
+        for (int j = 0; ok && j < n; ++j) {
+            const int jg = jb + j;
+            // ---- PV(j): its inputs were checked before
+            tc_fence_after();
+            pv(jg, j == 0, 0, PV_HEAD);
+            const bool more = j + 2 < n;
+            const bool kr = more && k_ready(jg + 2);
+            pv(jg, j == 0, PV_HEAD, PV_MMAS);
+            tc_commit2(bars.pv_done(jg & 1), 3);
+            // ---- QK(j+2) into the buffer PV(j) has just been queued to read
+            if (more) {
+                if (!kr && !k_wait(jg + 2)) { ok = false; break; }
+                tc_fence_after();
+                qk(jg + 2, 0, QK_HEAD);
+            }
+            const bool next = j + 1 < n;
+            const bool pr = next && pv_ready(jg + 1);
+            if (more) {
+                qk(jg + 2, QK_HEAD, QK_MMAS);
+                tc_commit2(bars.s_full(jg & 1), 3);
+            }
+            if (next && !pr && !pv_wait(jg + 1)) { ok = false; break; }
         }
-        if (next && !pr && !pv_wait(j + 1)) { ok = false; break; }
+        if (ok) tc_commit2(bars.o_final(), 3);
+        jb += n;
     }
-    if (ok) tc_commit2(bars.o_final(), 3);
     tc_commit2(bars.drain(), 1);
     // no MMA of the pair may still be running when the CTAs tear down
     mbar_wait_drain(bars.drain(), 0, status);
@@ -337,21 +417,13 @@ __device__ void pair_mma(const PairBars& bars, uint32_t sbase, uint32_t tm, int 
 
 template <int D>
 __device__ void pair_softmax(const PrefillParams& p, const PairBars& bars, uint32_t sbase, uint8_t* smem_x, uint32_t tm,
-                             uint32_t cr, int quarter, int hf, int lane, int qt, int b, int h, int n_kv,
-                             volatile int* abort_flag) {
+                             uint32_t cr, int quarter, int hf, int lane, int cl, int ncl, volatile int* abort_flag) {
     using C = PairCfg<D>;
     constexpr int HB = C::BN / 2;  // keys of a tile owned by this thread
     const int row = quarter * 32 + lane;
     const uint32_t tl = tm + ((uint32_t)(quarter * 32) << 16);
-    const int t = qt * C::BM + row;
-    const bool valid = t < p.S;
-    const int64_t tok = (int64_t)b * p.S + (valid ? t : 0);
-    const bf16* grow = static_cast<const bf16*>(p.gate) + tok * p.gate_tok_stride + (int64_t)h * p.gate_head_stride;
-    float gate_head = 1.f;
-    if (p.gate_mode == GATTN_GATE_HEADWISE && valid) gate_head = sigmoidf_dev(__bfloat162float(grow[0]));
-
     // the two threads of a row swap values through shared memory and then meet on
-    // an mbarrier (one phase per use: the prologue, every tile, the row sums)
+    // an mbarrier (one phase per use: every tile, and the row sums of every item)
     float* xmax = reinterpret_cast<float*>(smem_x);          // [2][2][BM]
     float* xsum = xmax + 2 * 2 * C::BM;                      // [2][BM]
     const uint32_t xbar = bars.xchg(quarter);
@@ -361,183 +433,200 @@ __device__ void pair_softmax(const PrefillParams& p, const PairBars& bars, uint3
         if (lane == 0) mbar_arrive(xbar);
         return __all_sync(0xffffffffu, mbar_wait(xbar, (uint32_t)(xphase++) & 1u, abort_flag, p.status));
     };
+    int jb = 0, n_it = 0;
+    PairItem item;
+    for (int r = 0; pair_item(p, cl, ncl, r, item); ++r, ++n_it) {
+        const int qt = item.qt, b = item.b, h = 2 * item.hp + (int)cr, n_kv = item.n_kv;
+        const int t = qt * C::BM + row;
+        const bool valid = t < p.S;
+        const int64_t tok = (int64_t)b * p.S + (valid ? t : 0);
+        const bf16* grow = static_cast<const bf16*>(p.gate) + tok * p.gate_tok_stride + (int64_t)h * p.gate_head_stride;
+        float gate_head = 1.f;
+        if (p.gate_mode == GATTN_GATE_HEADWISE && valid) gate_head = sigmoidf_dev(__bfloat162float(grow[0]));
 
-    // ---- fused Q prologue (first-half threads): rmsnorm then partial rotate-half
-    // RoPE, written as bf16 over the raw row in the Q tile (the A operand of
-    // S = Q'K'^T).  Rows past the sequence end were zero-filled by TMA.
-    if (hf == 0) {
-        if (!__all_sync(0xffffffffu, mbar_wait(bars.q_full(), 0, abort_flag, p.status))) return;
-        const uint32_t qbase = sbase + C::OFF_Q;
-        const uint32_t wbase = sbase + C::OFF_W;
-        float ss[4] = {0.f, 0.f, 0.f, 0.f};
+        // ---- fused Q prologue (first-half threads): rmsnorm then partial rotate-half
+        // RoPE, written as bf16 over the raw row in the Q tile (the A operand of
+        // S = Q'K'^T).  Rows past the sequence end were zero-filled by TMA.
+        if (hf == 0) {
+            if (!__all_sync(0xffffffffu, mbar_wait(bars.q_full(), (uint32_t)n_it & 1u, abort_flag, p.status))) return;
+            const uint32_t qbase = sbase + C::OFF_Q;
+            const uint32_t wbase = sbase + C::OFF_W;
+            float ss[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int c = 0; c < D / 8; ++c) {
-            float f[8];
-            unpack8(lds_v4(rowtile_addr(qbase, row, 8 * c)), f);
+            for (int c = 0; c < D / 8; ++c) {
+                float f[8];
+                unpack8(lds_v4(rowtile_addr(qbase, row, 8 * c)), f);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) ss[e & 3] = fmaf(f[e], f[e], ss[e & 3]);
-        }
-        const float rinv = rsqrtf(((ss[0] + ss[1]) + (ss[2] + ss[3])) / (float)D + p.eps);
-        const float posf = valid ? (p.pos ? (float)p.pos[tok] : (float)t) : 0.f;
-        const int half = p.rd >> 1;
-        for (int i0 = 0; i0 < half; i0 += 8) {
-            float xa[8], xb[8], wa[8], wb[8];
-            unpack8(lds_v4(rowtile_addr(qbase, row, i0)), xa);
-            unpack8(lds_v4(rowtile_addr(qbase, row, i0 + half)), xb);
-            unpack8(lds_v4(wbase + 2 * i0), wa);
-            unpack8(lds_v4(wbase + 2 * (i0 + half)), wb);
-            uint32_t lo[4], hi[4];
-#pragma unroll
-            for (int e = 0; e < 8; e += 2) {
-                float s0, c0, s1, c1;
-                rope_sincos(posf * p.inv_freq[i0 + e], &s0, &c0);
-                rope_sincos(posf * p.inv_freq[i0 + e + 1], &s1, &c1);
-                const float a0 = xa[e] * wa[e], b0 = xb[e] * wb[e];
-                const float a1 = xa[e + 1] * wa[e + 1], b1 = xb[e + 1] * wb[e + 1];
-                lo[e >> 1] = pack_bf16x2((a0 * c0 - b0 * s0) * rinv, (a1 * c1 - b1 * s1) * rinv);
-                hi[e >> 1] = pack_bf16x2((b0 * c0 + a0 * s0) * rinv, (b1 * c1 + a1 * s1) * rinv);
+                for (int e = 0; e < 8; ++e) ss[e & 3] = fmaf(f[e], f[e], ss[e & 3]);
             }
-            sts_v4(rowtile_addr(qbase, row, i0), lo[0], lo[1], lo[2], lo[3]);
-            sts_v4(rowtile_addr(qbase, row, i0 + half), hi[0], hi[1], hi[2], hi[3]);
-        }
-        for (int e0 = p.rd; e0 < D; e0 += 8) {
-            float x[8], w[8];
-            unpack8(lds_v4(rowtile_addr(qbase, row, e0)), x);
-            unpack8(lds_v4(wbase + 2 * e0), w);
-            sts_v4(rowtile_addr(qbase, row, e0), pack_bf16x2(x[0] * w[0] * rinv, x[1] * w[1] * rinv),
-                   pack_bf16x2(x[2] * w[2] * rinv, x[3] * w[3] * rinv),
-                   pack_bf16x2(x[4] * w[4] * rinv, x[5] * w[5] * rinv),
-                   pack_bf16x2(x[6] * w[6] * rinv, x[7] * w[7] * rinv));
-        }
-        fence_proxy_async_smem();  // the tensor core reads Q' through the async proxy
-        __syncwarp();
-        if (lane == 0) mbar_arrive_remote(mapa_shared(bars.q_ready(), 0));  // ordinary stores: cluster release
-    }
-
-    // ---- main loop: online softmax over the KV tiles this query tile can see.
-    // This thread owns keys [64 hf, 64 hf + 64) of every tile and O columns
-    // [hf D/2, (hf+1) D/2); its partner (same row, other half) runs in warp +- 4.
-    const float sl2 = p.scale_log2;
-    const int row_min = qt * C::BM;
-    float m_ref = -INFINITY;  // reference max (log2 domain) shared by O and l
-    float l = 0.f;            // this half's share of the row sum
-    for (int j = 0; j < n_kv; ++j) {
-        const uint32_t s_col = C::TM_S + (uint32_t)(j & 1) * C::BN;
-        if (!__all_sync(0xffffffffu, mbar_wait(bars.s_full(j & 1), (uint32_t)(j >> 1) & 1u, abort_flag, p.status)))
-            return;
-        tc_fence_after();
-        float s[HB];
-        {
-            uint32_t r[64];
-            tmem_ld64(tl + s_col + hf * HB, r);
+            const float rinv = rsqrtf(((ss[0] + ss[1]) + (ss[2] + ss[3])) / (float)D + p.eps);
+            const float posf = valid ? (p.pos ? (float)p.pos[tok] : (float)t) : 0.f;
+            const int half = p.rd >> 1;
+            for (int i0 = 0; i0 < half; i0 += 8) {
+                float xa[8], xb[8], wa[8], wb[8];
+                unpack8(lds_v4(rowtile_addr(qbase, row, i0)), xa);
+                unpack8(lds_v4(rowtile_addr(qbase, row, i0 + half)), xb);
+                unpack8(lds_v4(wbase + 2 * i0), wa);
+                unpack8(lds_v4(wbase + 2 * (i0 + half)), wb);
+                uint32_t lo[4], hi[4];
 #pragma unroll
-            for (int e = 0; e < 64; ++e) s[e] = __uint_as_float(r[e]);
-        }
-        const int key0 = j * C::BN + hf * HB;
-        if (key0 + HB - 1 > row_min) {
-#pragma unroll
-            for (int c = 0; c < HB; ++c)
-                if (key0 + c > t) s[c] = -INFINITY;
-        }
-        float mx[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) mx[i] = s[i];
-#pragma unroll
-        for (int c = 8; c < HB; ++c) mx[c & 7] = fmaxf(mx[c & 7], s[c]);
-        float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
-        // the row's maximum over the whole tile: swap halves (buffer j%2, so a slow
-        // partner still reading tile j-1 is never overwritten).  Passing the meet also
-        // means the partner has read its S columns, which P overwrites below.
-        xmax[((j & 1) * 2 + hf) * C::BM + row] = mt;
-        if (!meet()) return;
-        mt = fmaxf(mt, xmax[((j & 1) * 2 + (hf ^ 1)) * C::BM + row]);
-        const float m_new = fmaxf(m_ref, mt * sl2);
-        const bool need = (m_new - m_ref) > C::RESCALE_THRESHOLD;
-        if (j == 0) {
-            m_ref = m_new;
-        } else if (__any_sync(0xffffffffu, need)) {
-            const float alpha = need ? ex2_approx(m_ref - m_new) : 1.f;
-            if (need) {
-                l *= alpha;
-                m_ref = m_new;
+                for (int e = 0; e < 8; e += 2) {
+                    float s0, c0, s1, c1;
+                    rope_sincos(posf * p.inv_freq[i0 + e], &s0, &c0);
+                    rope_sincos(posf * p.inv_freq[i0 + e + 1], &s1, &c1);
+                    const float a0 = xa[e] * wa[e], b0 = xb[e] * wb[e];
+                    const float a1 = xa[e + 1] * wa[e + 1], b1 = xb[e + 1] * wb[e + 1];
+                    lo[e >> 1] = pack_bf16x2((a0 * c0 - b0 * s0) * rinv, (a1 * c1 - b1 * s1) * rinv);
+                    hi[e >> 1] = pack_bf16x2((b0 * c0 + a0 * s0) * rinv, (b1 * c1 + a1 * s1) * rinv);
+                }
+                sts_v4(rowtile_addr(qbase, row, i0), lo[0], lo[1], lo[2], lo[3]);
+                sts_v4(rowtile_addr(qbase, row, i0 + half), hi[0], hi[1], hi[2], hi[3]);
             }
+            for (int e0 = p.rd; e0 < D; e0 += 8) {
+                float x[8], w[8];
+                unpack8(lds_v4(rowtile_addr(qbase, row, e0)), x);
+                unpack8(lds_v4(wbase + 2 * e0), w);
+                sts_v4(rowtile_addr(qbase, row, e0), pack_bf16x2(x[0] * w[0] * rinv, x[1] * w[1] * rinv),
+                       pack_bf16x2(x[2] * w[2] * rinv, x[3] * w[3] * rinv),
+                       pack_bf16x2(x[4] * w[4] * rinv, x[5] * w[5] * rinv),
+                       pack_bf16x2(x[6] * w[6] * rinv, x[7] * w[7] * rinv));
+            }
+            fence_proxy_async_smem();  // the tensor core reads Q' through the async proxy
             __syncwarp();
-            // O is touched only once PV(j-1) has landed (PV(j-2) already had: QK(j)
-            // was issued behind it)
-            if (!__all_sync(0xffffffffu, mbar_wait(bars.pv_done((j - 1) & 1), (uint32_t)((j - 1) >> 1) & 1u,
-                                                   abort_flag, p.status)))
+            if (lane == 0) mbar_arrive_remote(mapa_shared(bars.q_ready(), 0));  // ordinary stores: cluster release
+        }
+
+        // ---- main loop: online softmax over the KV tiles this query tile can see.
+        // This thread owns keys [64 hf, 64 hf + 64) of every tile and O columns
+        // [hf D/2, (hf+1) D/2); its partner (same row, other half) runs in warp +- 4.
+        const float sl2 = p.scale_log2;
+        const int row_min = qt * C::BM;
+        float m_ref = -INFINITY;  // reference max (log2 domain) shared by O and l
+        float l = 0.f;            // this half's share of the row sum
+        for (int j = 0; j < n_kv; ++j) {
+            const int jg = jb + j;  // tile counter over all items: buffers and phases
+            const uint32_t s_col = C::TM_S + (uint32_t)(jg & 1) * C::BN;
+            if (!__all_sync(0xffffffffu, mbar_wait(bars.s_full(jg & 1), (uint32_t)(jg >> 1) & 1u, abort_flag, p.status)))
                 return;
             tc_fence_after();
-#pragma unroll 1
-            for (int c = hf * (D / 2); c < (hf + 1) * (D / 2); c += 32) {
-                uint32_t r[32];
-                tmem_ld32(tl + C::TM_O + c, r);
+            float s[HB];
+            {
+                uint32_t r[64];
+                tmem_ld64(tl + s_col + hf * HB, r);
 #pragma unroll
-                for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
-                tmem_st32(tl + C::TM_O + c, r);
+                for (int e = 0; e < 64; ++e) s[e] = __uint_as_float(r[e]);
             }
-        }
-        // P = exp2(s * scale * log2e - m_ref) as bf16 pairs over this thread's keys:
-        // columns [32 hf, 32 hf + 32) of the score buffer
-        float rs[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        const float mref = m_ref;
-        uint32_t pk[32];
+            const int key0 = j * C::BN + hf * HB;
+            if (key0 + HB - 1 > row_min) {
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-            const float p0 = ex2_approx(fmaf(s[2 * e], sl2, -mref));
-            const float p1 = ex2_approx(fmaf(s[2 * e + 1], sl2, -mref));
-            rs[e & 7] += p0 + p1;
-            pk[e] = pack_bf16x2(p0, p1);
-        }
-        tmem_st32(tl + s_col + hf * (HB / 2), pk);
-        l += ((rs[0] + rs[1]) + (rs[2] + rs[3])) + ((rs[4] + rs[5]) + (rs[6] + rs[7]));
-        tmem_wait_st();  // P (and an O rescale above, if any) has landed
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) arrive_even(bars.p_full(j & 1), cr);
-    }
-
-    // ---- epilogue: O / l * sigmoid(gate) -> bf16 [B,S,H*d], this thread's half of the columns
-    xsum[hf * C::BM + row] = l;
-    if (!meet()) return;
-    const float l_row = xsum[row] + xsum[C::BM + row];
-    if (!__all_sync(0xffffffffu, mbar_wait(bars.o_final(), 0, abort_flag, p.status))) return;
-    const bool elementwise = p.gate_mode == GATTN_GATE_ELEMENTWISE;
-    if (elementwise && !__all_sync(0xffffffffu, mbar_wait(bars.g_full(), 0, abort_flag, p.status))) return;
-    tc_fence_after();
-    const float inv_l = 1.f / l_row;
-    const float gh = inv_l * gate_head;
-    bf16* orow = static_cast<bf16*>(p.out) + (tok * p.H + h) * D;
-    const uint32_t gbase = sbase + C::OFF_K;
+                for (int c = 0; c < HB; ++c)
+                    if (key0 + c > t) s[c] = -INFINITY;
+            }
+            float mx[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) mx[i] = s[i];
+#pragma unroll
+            for (int c = 8; c < HB; ++c) mx[c & 7] = fmaxf(mx[c & 7], s[c]);
+            float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+            // the row's maximum over the whole tile: swap halves (buffer j%2, so a slow
+            // partner still reading tile j-1 is never overwritten).  Passing the meet also
+            // means the partner has read its S columns, which P overwrites below.
+            xmax[((jg & 1) * 2 + hf) * C::BM + row] = mt;
+            if (!meet()) return;
+            mt = fmaxf(mt, xmax[((jg & 1) * 2 + (hf ^ 1)) * C::BM + row]);
+            const float m_new = fmaxf(m_ref, mt * sl2);
+            const bool need = (m_new - m_ref) > C::RESCALE_THRESHOLD;
+            if (j == 0) {
+                m_ref = m_new;
+            } else if (__any_sync(0xffffffffu, need)) {
+                const float alpha = need ? ex2_approx(m_ref - m_new) : 1.f;
+                if (need) {
+                    l *= alpha;
+                    m_ref = m_new;
+                }
+                __syncwarp();
+                // O is touched only once PV(j-1) has landed (PV(j-2) already had: QK(j)
+                // was issued behind it)
+                if (!__all_sync(0xffffffffu, mbar_wait(bars.pv_done((jg - 1) & 1), (uint32_t)((jg - 1) >> 1) & 1u,
+                                                       abort_flag, p.status)))
+                    return;
+                tc_fence_after();
 #pragma unroll 1
-    for (int c = hf * (D / 2); c < (hf + 1) * (D / 2); c += 32) {
-        uint32_t r[32];
-        __syncwarp();
-        tmem_ld32(tl + C::TM_O + c, r);
-        if (!valid) continue;
-        float gv[32];
-        if (elementwise) {
+                for (int c = hf * (D / 2); c < (hf + 1) * (D / 2); c += 32) {
+                    uint32_t r[32];
+                    tmem_ld32(tl + C::TM_O + c, r);
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
+                    tmem_st32(tl + C::TM_O + c, r);
+                }
+            }
+            // P = exp2(s * scale * log2e - m_ref) as bf16 pairs over this thread's keys:
+            // columns [32 hf, 32 hf + 32) of the score buffer
+            float rs[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            const float mref = m_ref;
+            uint32_t pk[32];
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+                const float p0 = ex2_approx(fmaf(s[2 * e], sl2, -mref));
+                const float p1 = ex2_approx(fmaf(s[2 * e + 1], sl2, -mref));
+                rs[e & 7] += p0 + p1;
+                pk[e] = pack_bf16x2(p0, p1);
+            }
+            tmem_st32(tl + s_col + hf * (HB / 2), pk);
+            l += ((rs[0] + rs[1]) + (rs[2] + rs[3])) + ((rs[4] + rs[5]) + (rs[6] + rs[7]));
+            tmem_wait_st();  // P (and an O rescale above, if any) has landed
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) arrive_even(bars.p_full(jg & 1), cr);
+        }
+
+        // ---- epilogue: O / l * sigmoid(gate), this thread's half of the columns, as bf16
+        // into the staging tile in the K' ring (the gate tile's own slots when there
+        // is one: each thread overwrites only what it has just read); the producer
+        // then writes the tile to [B,S,H*d] with TMA stores (rows past the end clipped)
+        xsum[hf * C::BM + row] = l;
+        if (!meet()) return;
+        const float l_row = xsum[row] + xsum[C::BM + row];
+        if (!__all_sync(0xffffffffu, mbar_wait(bars.o_final(), (uint32_t)n_it & 1u, abort_flag, p.status))) return;
+        const bool elementwise = p.gate_mode == GATTN_GATE_ELEMENTWISE;
+        if (elementwise && !__all_sync(0xffffffffu, mbar_wait(bars.g_full(), (uint32_t)n_it & 1u, abort_flag, p.status)))
+            return;
+        tc_fence_after();
+        const float inv_l = 1.f / l_row;
+        const float gh = inv_l * gate_head;
+        const uint32_t gbase = sbase + C::OFF_K;
+#pragma unroll 1
+        for (int c = hf * (D / 2); c < (hf + 1) * (D / 2); c += 32) {
+            uint32_t r[32];
+            __syncwarp();
+            tmem_ld32(tl + C::TM_O + c, r);
 #pragma unroll
             for (int q4 = 0; q4 < 4; ++q4) {
-                float f[8];
-                unpack8(lds_v4(rowtile_addr(gbase, row, c + 8 * q4)), f);
+                const uint32_t addr = rowtile_addr(gbase, row, c + 8 * q4);
+                float gv[8];
+                if (elementwise) {
+                    float f[8];
+                    unpack8(lds_v4(addr), f);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) gv[8 * q4 + e] = inv_l * sigmoid_tanh(f[e]);
+                    for (int e = 0; e < 8; ++e) gv[e] = inv_l * sigmoid_tanh(f[e]);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) gv[e] = gh;
+                }
+                const float* o = reinterpret_cast<const float*>(r + 8 * q4);
+                sts_v4(addr, pack_bf16x2(o[0] * gv[0], o[1] * gv[1]), pack_bf16x2(o[2] * gv[2], o[3] * gv[3]),
+                       pack_bf16x2(o[4] * gv[4], o[5] * gv[5]), pack_bf16x2(o[6] * gv[6], o[7] * gv[7]));
             }
-        } else {
-#pragma unroll
-            for (int e = 0; e < 32; ++e) gv[e] = gh;
         }
-        uint4* dst = reinterpret_cast<uint4*>(orow + c);
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-            uint4 v;
-            v.x = pack_bf16x2(__uint_as_float(r[8 * q4 + 0]) * gv[8 * q4 + 0], __uint_as_float(r[8 * q4 + 1]) * gv[8 * q4 + 1]);
-            v.y = pack_bf16x2(__uint_as_float(r[8 * q4 + 2]) * gv[8 * q4 + 2], __uint_as_float(r[8 * q4 + 3]) * gv[8 * q4 + 3]);
-            v.z = pack_bf16x2(__uint_as_float(r[8 * q4 + 4]) * gv[8 * q4 + 4], __uint_as_float(r[8 * q4 + 5]) * gv[8 * q4 + 5]);
-            v.w = pack_bf16x2(__uint_as_float(r[8 * q4 + 6]) * gv[8 * q4 + 6], __uint_as_float(r[8 * q4 + 7]) * gv[8 * q4 + 7]);
-            dst[q4] = v;
+        // O has been read: the next item's first PV may overwrite it
+        tc_fence_before();
+        fence_proxy_async_smem();  // the TMA store reads the staged rows through the async proxy
+        __syncwarp();
+        if (lane == 0) {
+            arrive_even(bars.o_free(), cr);
+            mbar_arrive(bars.o_staged());
         }
+        jb += n_kv;
     }
 }
 
@@ -547,7 +636,7 @@ template <int D>
 __global__ void __launch_bounds__(PairCfg<D>::THREADS, 1)
     prefill_pair_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                         const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmG,
-                        const __grid_constant__ PrefillParams p) {
+                        const __grid_constant__ CUtensorMap tmO, const __grid_constant__ PrefillParams p) {
     using C = PairCfg<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -558,17 +647,8 @@ __global__ void __launch_bounds__(PairCfg<D>::THREADS, 1)
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
     const uint32_t cr = cluster_ctarank();
 
-    // one cluster per (query tile, batch, head pair), heaviest query tiles first
-    const int n_hp = p.H / 2;
-    const int pairs = p.B * n_hp;
-    const int u = (int)(blockIdx.x >> 1);
-    const int qt = p.n_qtiles - 1 - u / pairs;
-    const int bp = u % pairs;
-    const int b = bp / n_hp;
-    const int h = 2 * (bp % n_hp) + (int)cr;
-    const int g = h / (p.H / p.G);
-    const int q_end = min(p.S, (qt + 1) * C::BM);
-    const int n_kv = (q_end + C::BN - 1) / C::BN;
+    // cluster cl of ncl walks its list of work items (see pair_item)
+    const int cl = (int)(blockIdx.x >> 1), ncl = (int)(gridDim.x >> 1);
 
     if (threadIdx.x == 0) {
         const uint32_t full_count = cr == 0 ? 2u : 1u;
@@ -585,6 +665,9 @@ __global__ void __launch_bounds__(PairCfg<D>::THREADS, 1)
         mbar_init(bars.g_full(), 1);
         mbar_init(bars.drain(), 1);
         for (int q = 0; q < 4; ++q) mbar_init(bars.xchg(q), 2);
+        mbar_init(bars.o_free(), C::P_ARRIVALS);
+        mbar_init(bars.e_done(), 1);
+        mbar_init(bars.o_staged(), C::SOFTMAX_WARPS);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -592,6 +675,7 @@ __global__ void __launch_bounds__(PairCfg<D>::THREADS, 1)
         tma_prefetch_desc(&tmQ);
         tma_prefetch_desc(&tmK);
         tma_prefetch_desc(&tmV);
+        tma_prefetch_desc(&tmO);
     }
     if (warp == 1) {
         tmem_alloc2(smem_u32(tmem_slot), C::TM_COLS);
@@ -607,18 +691,16 @@ __global__ void __launch_bounds__(PairCfg<D>::THREADS, 1)
 
     if (warp == 0) {
         if (lane == 0)
-            pair_producer<D>(&tmK, &tmV, &tmQ, &tmG, p.qnorm_w, bars, sbase, n_kv, b, g, h, qt, p.G, cr,
-                             p.gate_mode == GATTN_GATE_ELEMENTWISE, abort_flag, p.status);
+            pair_producer<D>(&tmK, &tmV, &tmQ, &tmG, &tmO, p, bars, sbase, cl, ncl, cr, abort_flag, p.status);
         __syncwarp();
     } else if (warp == 1) {
         if (lane == 0) {
-            if (cr == 0) pair_mma<D>(bars, sbase, tm, n_kv, abort_flag, p.status);
-            else pair_forwarder<D>(bars, n_kv, abort_flag, p.status);
+            if (cr == 0) pair_mma<D>(p, bars, sbase, tm, cl, ncl, abort_flag, p.status);
+            else pair_forwarder<D>(p, bars, cl, ncl, abort_flag, p.status);
         }
         __syncwarp();
     } else {
-        pair_softmax<D>(p, bars, sbase, smem + C::OFF_X, tm, cr, warp & 3, (warp - 2) >> 2, lane, qt, b, h, n_kv,
-                        abort_flag);
+        pair_softmax<D>(p, bars, sbase, smem + C::OFF_X, tm, cr, warp & 3, (warp - 2) >> 2, lane, cl, ncl, abort_flag);
     }
     // both CTAs are done with the pair's TMEM (the issuer drained every MMA) before it is released
     tc_fence_before();
@@ -636,8 +718,10 @@ cudaError_t launch_pair_d(const PrefillParams& p, const PrefillMaps& maps, cudaS
     using C = PairCfg<D>;
     cudaError_t e = set_smem_once(reinterpret_cast<const void*>(prefill_pair_kernel<D>), C::SMEM_ALLOC);
     if (e != cudaSuccess) return e;
-    const long long blocks = 2LL * p.n_qtiles * p.B * (p.H / 2);
-    if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
+    const long long n_items = (long long)p.n_qtiles * p.B * (p.H / 2);
+    const long long max_clusters = p.n_sms >= 2 ? p.n_sms / 2 : 1;
+    const long long blocks = 2 * (n_items < max_clusters ? n_items : max_clusters);
+    if (n_items * 2 > 0x7fffffffLL || blocks < 2) return cudaErrorInvalidValue;
     if (ev_start) cudaEventRecord(ev_start, stream);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)blocks);
@@ -653,7 +737,7 @@ cudaError_t launch_pair_d(const PrefillParams& p, const PrefillMaps& maps, cudaS
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    cudaError_t err = cudaLaunchKernelEx(&cfg, prefill_pair_kernel<D>, maps.k, maps.v, maps.q, maps.gate, p);
+    cudaError_t err = cudaLaunchKernelEx(&cfg, prefill_pair_kernel<D>, maps.k, maps.v, maps.q, maps.gate, maps.out, p);
     if (ev_stop) cudaEventRecord(ev_stop, stream);
     return err;
 }
