@@ -18,22 +18,31 @@
 // That halved footprint is what buys 128-key tiles at d = 256.
 //
 // Roles per CTA (10 warps):
-//   warp 0      TMA producer of this CTA's halves: the raw Q tile of its own head
-//               once, K' and V halves into rings, its gate tile at the end.
+//   warp 0      TMA producer of this CTA's halves: per work item the raw Q tile of its
+//               own head, K' and V halves into rings, at the end its gate tile into
+//               the idle V ring, and finally the staged output tile back to global
+//               memory with TMA stores.
 //   warp 1      allocates TMEM for the pair.  Even CTA: issues every MMA.  Odd CTA:
 //               forwards the landing of its K'/V halves to the even CTA's barriers.
 //   warps 2..9  two threads per query row of this CTA's head, each owning half of
 //               the row's keys in every tile (and half of its O columns): the fused
-//               Q prologue (warps 2..5: Q' = rope(rmsnorm(q)) written over the raw
-//               Q tile in shared memory), the online softmax and the gate epilogue.
-//               The two halves of a row swap tile maxima through shared memory;
-//               their row sums are added once, in the epilogue.
+//               Q prologue (Q' = rope(rmsnorm(q)) written over the raw Q tile in
+//               shared memory), the online softmax and the gate epilogue.  The two
+//               halves of a row swap tile maxima through shared memory; their row
+//               sums are added once, in the epilogue.
 //
 // TMEM (per CTA, lane = query row): O [0, d) | S0 [d, d+128) | S1 [d+128, d+256).
 // Key tile j's scores go to S_{j%2}, and its probabilities P_j overwrite them in
 // place as bf16 pairs, which the PV MMA reads straight from TMEM.
 // Shared memory (per CTA): Q' tile | K' ring | V ring | barriers | q norm weights |
-// row-half exchange.  The gate tile finally lands in the K' ring.
+// row-half exchange.  Once an item's last PV is done, the V ring holds its gate
+// tile, which the epilogue overwrites with the output tile.
+//
+// Work items follow one another without a gap in the tensor pipe's inputs: the
+// next item's Q tile lands as soon as the last QK has read the Q buffer, its K'
+// tiles as soon as the ring frees up, and the softmax warps normalise it before
+// running the current item's epilogue, so that the next item's first QK MMAs run
+// meanwhile; its V tiles follow the output tile out of the V ring.
 //
 // Issue order (one issuer, the tensor pipe runs in order): QK(0), QK(1), then per
 // tile PV(j), QK(j+2).  QK(j+2) reuses S_{j%2} right behind the PV that reads P_j
@@ -69,13 +78,12 @@ struct PairBars {
     __device__ uint32_t o_final() const { return at(10); }          // every PV complete (both CTAs)
     __device__ uint32_t q_ready() const { return at(11); }          // Q' of both CTAs written (even CTA)
     __device__ uint32_t q_full() const { return at(12); }           // raw Q tile + weights landed
-    __device__ uint32_t g_full() const { return at(13); }           // gate tile landed
+    __device__ uint32_t g_full() const { return at(13); }           // gate tile landed (in the V ring)
     __device__ uint32_t drain() const { return at(14); }            // the issuer's MMAs all complete
     __device__ uint32_t xchg(int q) const { return at(15 + q); }    // both halves of row quarter q posted
     __device__ uint32_t o_free() const { return at(19); }   // an item's epilogue has read O (even CTA, both CTAs arrive)
-    __device__ uint32_t e_done() const { return at(20); }   // (unused)
-    __device__ uint32_t o_staged() const { return at(21); } // every softmax warp staged its output rows (this CTA)
-    static constexpr int COUNT = 22;
+    __device__ uint32_t o_staged() const { return at(20); } // every softmax warp staged its output rows (this CTA)
+    static constexpr int COUNT = 21;
 };
 
 template <int D>
@@ -96,7 +104,7 @@ struct PairCfg {
     static constexpr int V_TILE = VCH * V_CHUNK;
     static constexpr int ROWBOX_BYTES = BM * 128;  // one Q/gate TMA box: 128 rows x 64 bf16
     static constexpr int QTILE_BYTES = BM * D * 2;
-    static_assert(QTILE_BYTES <= NSK * K_TILE, "the gate tile must fit the K' ring");
+    static_assert(QTILE_BYTES == NSV * V_TILE, "the gate / output tile fills the V ring");
     static constexpr int TM_O = 0;
     static constexpr int TM_S = D;                // score buffer b at TM_S + b * BN
     static constexpr int TM_COLS = 512;
@@ -108,16 +116,17 @@ struct PairCfg {
     static constexpr int NBAR = PairBars::COUNT;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr int OFF_W = (OFF_MISC + 16 + 127) & ~127;
-    // row-half exchange: tile maxima [2 buffers][2 halves][BM] and row sums [2 halves][BM]
+    // row-half exchange: tile maxima [2 buffers][2 halves][BM], row sums and sums of
+    // squares of q [2 halves][BM] each
     static constexpr int OFF_X = OFF_W + D * 2;
-    static constexpr int SMEM_BYTES = OFF_X + (2 * 2 * BM + 2 * BM) * 4;
+    static constexpr int SMEM_BYTES = OFF_X + (2 * 2 * BM + 2 * 2 * BM) * 4;
     // never less than 120 KB, so that no second CTA (and TMEM allocation) shares the SM
     static constexpr int SMEM_ALLOC = (SMEM_BYTES + 1024) > 122880 ? (SMEM_BYTES + 1024) : 122880;
     static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
     static constexpr int SOFTMAX_WARPS = 8;  // two per row quarter: each thread takes half a row
     static constexpr int THREADS = 64 + 32 * SOFTMAX_WARPS;
     static constexpr int P_ARRIVALS = 2 * SOFTMAX_WARPS;   // P_j: every softmax warp of both CTAs
-    static constexpr int Q_ARRIVALS = SOFTMAX_WARPS;       // Q': the first-half warps of both CTAs
+    static constexpr int Q_ARRIVALS = 2 * SOFTMAX_WARPS;   // Q': every softmax warp of both CTAs
     static constexpr uint32_t IDESC_QK = make_idesc_bf16(256, BN, false);
     static constexpr uint32_t IDESC_PV = make_idesc_bf16(256, D, true);
     static constexpr float RESCALE_THRESHOLD = 8.0f;  // log2 domain
@@ -168,18 +177,32 @@ __device__ void pair_producer(const CUtensorMap* tmK, const CUtensorMap* tmV, co
     int n_it = 0, n_g = 0;
     bool ok = true;
     PairItem it;
+    // the previous item, whose output still occupies the V ring
     int prev_h = 0, prev_qt = 0, prev_b = 0;
-    // the softmax warps staged item k's output rows in the K' ring: write them out
-    // (TMA stores, rows past the end clipped) and wait until the copies have read
-    // shared memory, after which the K' ring may be refilled
-    auto store_output = [&](int k, int h, int qt, int b) -> bool {
-        if (!mbar_wait(bars.o_staged(), (uint32_t)k & 1u, abort_flag, status)) return false;
+    // the V ring is free once every PV of the previous item has completed
+    auto v_ring_idle = [&]() -> bool {
+        for (int j = jb - C::NSV > 0 ? jb - C::NSV : 0; j < jb; ++j)
+            if (!mbar_try_wait(bars.pv_done(j % C::NSV), (uint32_t)(j / C::NSV) & 1u)) return false;
+        return true;
+    };
+    // the previous item's gate tile, read by its epilogue, goes into the idle V ring
+    auto load_gate = [&]() {
+        mbar_arrive_expect_tx(bars.g_full(), C::QTILE_BYTES);
 #pragma unroll
         for (int c = 0; c < C::KCH; ++c)
-            tma_store_4d(tmO, sbase + C::OFF_K + c * C::ROWBOX_BYTES, c * 64, h, qt * C::BM, b);
+            tma_load_4d(sbase + C::OFF_V + c * C::ROWBOX_BYTES, tmG, bars.g_full(), c * 64, prev_h, prev_qt * C::BM,
+                        prev_b);
+        ++n_g;
+    };
+    // the softmax warps staged the previous item's output rows in the V ring (over
+    // the gate tile): write them out (TMA stores, rows past the end clipped) and wait
+    // until the copies have read shared memory, after which the ring may be refilled
+    auto store_output = [&]() {
+#pragma unroll
+        for (int c = 0; c < C::KCH; ++c)
+            tma_store_4d(tmO, sbase + C::OFF_V + c * C::ROWBOX_BYTES, c * 64, prev_h, prev_qt * C::BM, prev_b);
         bulk_commit_group();
         bulk_wait_group_read0();
-        return true;
     };
     for (int r = 0; ok && pair_item(p, cl, ncl, r, it); ++r) {
         const int h = 2 * it.hp + (int)cr, g = h / (p.H / p.G);
@@ -201,20 +224,24 @@ __device__ void pair_producer(const CUtensorMap* tmK, const CUtensorMap* tmV, co
         // K' comes from the pre-pass kernel launched just before this one
         if (n_it == 1) pdl_wait_prerequisites();
 
-        // K' and V tiles, each stream as soon as its own stage frees up; the K' ring
-        // holds the previous item's gate and output tiles until they are written out
-        bool k_open = n_it == 1;
+        // K' and V tiles, each stream as soon as its own stage frees up.  Meanwhile the
+        // previous item finishes in the V ring: its gate tile once the ring is idle,
+        // then its output once staged; this item's V tiles follow.
+        bool g_sent = n_it == 1 || !gate_tile, v_open = n_it == 1;
         const int ke = nk + it.n_kv, ve = nv + it.n_kv;
         const unsigned long long t0 = global_timer_ns();
         uint32_t spins = 0;
         while (nk < ke || nv < ve) {
             bool progressed = false;
-            if (!k_open && mbar_try_wait(bars.o_staged(), (uint32_t)(n_it - 2) & 1u)) {
-                if (!store_output(n_it - 2, prev_h, prev_qt, prev_b)) break;
-                k_open = true;
+            if (!g_sent && v_ring_idle()) {
+                load_gate();
+                g_sent = progressed = true;
             }
-            if (k_open && nk < ke &&
-                (nk < C::NSK || mbar_try_wait(bars.s_full(nk % C::NSK), ((uint32_t)(nk / C::NSK) & 1u) ^ 1u))) {
+            if (g_sent && !v_open && mbar_try_wait(bars.o_staged(), (uint32_t)(n_it - 2) & 1u)) {
+                store_output();
+                v_open = progressed = true;
+            }
+            if (nk < ke && (nk < C::NSK || mbar_try_wait(bars.s_full(nk % C::NSK), ((uint32_t)(nk / C::NSK) & 1u) ^ 1u))) {
                 const int st = nk % C::NSK;
                 mbar_arrive_expect_tx(bars.k_full(st), C::K_TILE);
                 const uint32_t kdst = sbase + C::OFF_K + st * C::K_TILE;
@@ -225,7 +252,7 @@ __device__ void pair_producer(const CUtensorMap* tmK, const CUtensorMap* tmV, co
                 ++nk;
                 progressed = true;
             }
-            if (nv < ve &&
+            if (v_open && nv < ve &&
                 (nv < C::NSV || mbar_try_wait(bars.pv_done(nv % C::NSV), ((uint32_t)(nv / C::NSV) & 1u) ^ 1u))) {
                 const int st = nv % C::NSV;
                 mbar_arrive_expect_tx(bars.v_full(st), C::V_TILE);
@@ -250,26 +277,20 @@ __device__ void pair_producer(const CUtensorMap* tmK, const CUtensorMap* tmV, co
                 }
             }
         }
-        if (nk != ke || nv != ve || !k_open) { ok = false; break; }
-        // gate tile into the K' ring once this item's last K' tiles have been consumed
-        if (gate_tile) {
-            for (int j = ke - C::NSK > jb ? ke - C::NSK : jb; ok && j < ke; ++j)
-                ok = mbar_wait(bars.s_full(j % C::NSK), (uint32_t)(j / C::NSK) & 1u, abort_flag, status);
-            if (!ok) break;
-            mbar_arrive_expect_tx(bars.g_full(), C::QTILE_BYTES);
-#pragma unroll
-            for (int c = 0; c < C::KCH; ++c)
-                tma_load_4d(sbase + C::OFF_K + c * C::ROWBOX_BYTES, tmG, bars.g_full(), c * 64, h, it.qt * C::BM, it.b);
-            ++n_g;
-        }
+        if (nk != ke || nv != ve) { ok = false; break; }
         jb += it.n_kv;
         prev_h = h;
         prev_qt = it.qt;
         prev_b = it.b;
     }
-    // the last item's output
+    // the last item's gate and output
     if (ok && n_it > 0) {
-        store_output(n_it - 1, prev_h, prev_qt, prev_b);
+        if (gate_tile) {
+            for (int j = jb - C::NSV > 0 ? jb - C::NSV : 0; ok && j < jb; ++j)
+                ok = mbar_wait(bars.pv_done(j % C::NSV), (uint32_t)(j / C::NSV) & 1u, abort_flag, status);
+            if (ok) load_gate();
+        }
+        if (ok && mbar_wait(bars.o_staged(), (uint32_t)(n_it - 1) & 1u, abort_flag, status)) store_output();
         bulk_wait_group0();
     }
     // every copy this thread started lands before the CTA can exit
@@ -423,9 +444,10 @@ __device__ void pair_softmax(const PrefillParams& p, const PairBars& bars, uint3
     const int row = quarter * 32 + lane;
     const uint32_t tl = tm + ((uint32_t)(quarter * 32) << 16);
     // the two threads of a row swap values through shared memory and then meet on
-    // an mbarrier (one phase per use: every tile, and the row sums of every item)
-    float* xmax = reinterpret_cast<float*>(smem_x);          // [2][2][BM]
-    float* xsum = xmax + 2 * 2 * C::BM;                      // [2][BM]
+    // an mbarrier (one phase per use: every tile, and twice per item)
+    float* xmax = reinterpret_cast<float*>(smem_x);          // [2][2][BM] tile maxima
+    float* xsum = xmax + 2 * 2 * C::BM;                      // [2][BM] row sums
+    float* xss = xsum + 2 * C::BM;                           // [2][BM] sums of squares of q
     const uint32_t xbar = bars.xchg(quarter);
     int xphase = 0;
     auto meet = [&]() -> bool {
@@ -433,67 +455,79 @@ __device__ void pair_softmax(const PrefillParams& p, const PairBars& bars, uint3
         if (lane == 0) mbar_arrive(xbar);
         return __all_sync(0xffffffffu, mbar_wait(xbar, (uint32_t)(xphase++) & 1u, abort_flag, p.status));
     };
+
+    // ---- fused Q prologue of item k: rmsnorm then partial rotate-half RoPE, written
+    // as bf16 over the raw row in the Q tile (the A operand of S = Q'K'^T).  The two
+    // threads of a row each sum the squares of their half of it; the 8-column chunks
+    // are then shared out alternately, a rotated pair (i, i + rd/2) going with the
+    // chunk of i.  Rows past the sequence end were zero-filled by TMA.
+    auto q_prologue = [&](const PairItem& it, int k) -> bool {
+        const int t = it.qt * C::BM + row;
+        const bool valid = t < p.S;
+        if (!__all_sync(0xffffffffu, mbar_wait(bars.q_full(), (uint32_t)k & 1u, abort_flag, p.status))) return false;
+        const uint32_t qbase = sbase + C::OFF_Q;
+        const uint32_t wbase = sbase + C::OFF_W;
+        float ss[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int c = 0; c < D / 16; ++c) {
+            float f[8];
+            unpack8(lds_v4(rowtile_addr(qbase, row, hf * (D / 2) + 8 * c)), f);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) ss[e & 3] = fmaf(f[e], f[e], ss[e & 3]);
+        }
+        xss[hf * C::BM + row] = (ss[0] + ss[1]) + (ss[2] + ss[3]);
+        // past the meet both halves have read the raw row: the writes below may begin
+        if (!meet()) return false;
+        const float rinv = rsqrtf((xss[row] + xss[C::BM + row]) / (float)D + p.eps);
+        const float posf = valid ? (p.pos ? (float)p.pos[(int64_t)it.b * p.S + t] : (float)t) : 0.f;
+        const int half = p.rd >> 1;
+        for (int i0 = 8 * hf; i0 < half; i0 += 16) {
+            float xa[8], xb[8], wa[8], wb[8];
+            unpack8(lds_v4(rowtile_addr(qbase, row, i0)), xa);
+            unpack8(lds_v4(rowtile_addr(qbase, row, i0 + half)), xb);
+            unpack8(lds_v4(wbase + 2 * i0), wa);
+            unpack8(lds_v4(wbase + 2 * (i0 + half)), wb);
+            uint32_t lo[4], hi[4];
+#pragma unroll
+            for (int e = 0; e < 8; e += 2) {
+                float s0, c0, s1, c1;
+                rope_sincos(posf * p.inv_freq[i0 + e], &s0, &c0);
+                rope_sincos(posf * p.inv_freq[i0 + e + 1], &s1, &c1);
+                const float a0 = xa[e] * wa[e], b0 = xb[e] * wb[e];
+                const float a1 = xa[e + 1] * wa[e + 1], b1 = xb[e + 1] * wb[e + 1];
+                lo[e >> 1] = pack_bf16x2((a0 * c0 - b0 * s0) * rinv, (a1 * c1 - b1 * s1) * rinv);
+                hi[e >> 1] = pack_bf16x2((b0 * c0 + a0 * s0) * rinv, (b1 * c1 + a1 * s1) * rinv);
+            }
+            sts_v4(rowtile_addr(qbase, row, i0), lo[0], lo[1], lo[2], lo[3]);
+            sts_v4(rowtile_addr(qbase, row, i0 + half), hi[0], hi[1], hi[2], hi[3]);
+        }
+        for (int e0 = p.rd + 8 * hf; e0 < D; e0 += 16) {
+            float x[8], w[8];
+            unpack8(lds_v4(rowtile_addr(qbase, row, e0)), x);
+            unpack8(lds_v4(wbase + 2 * e0), w);
+            sts_v4(rowtile_addr(qbase, row, e0), pack_bf16x2(x[0] * w[0] * rinv, x[1] * w[1] * rinv),
+                   pack_bf16x2(x[2] * w[2] * rinv, x[3] * w[3] * rinv), pack_bf16x2(x[4] * w[4] * rinv, x[5] * w[5] * rinv),
+                   pack_bf16x2(x[6] * w[6] * rinv, x[7] * w[7] * rinv));
+        }
+        fence_proxy_async_smem();  // the tensor core reads Q' through the async proxy
+        __syncwarp();
+        if (lane == 0) mbar_arrive_remote(mapa_shared(bars.q_ready(), 0));  // ordinary stores: cluster release
+        return true;
+    };
+
     int jb = 0, n_it = 0;
-    PairItem item;
-    for (int r = 0; pair_item(p, cl, ncl, r, item); ++r, ++n_it) {
+    PairItem item, next;
+    bool have = pair_item(p, cl, ncl, 0, item);
+    if (have && !q_prologue(item, 0)) return;
+    for (int r = 0; have; ++r, ++n_it) {
         const int qt = item.qt, b = item.b, h = 2 * item.hp + (int)cr, n_kv = item.n_kv;
         const int t = qt * C::BM + row;
         const bool valid = t < p.S;
-        const int64_t tok = (int64_t)b * p.S + (valid ? t : 0);
-        const bf16* grow = static_cast<const bf16*>(p.gate) + tok * p.gate_tok_stride + (int64_t)h * p.gate_head_stride;
         float gate_head = 1.f;
-        if (p.gate_mode == GATTN_GATE_HEADWISE && valid) gate_head = sigmoidf_dev(__bfloat162float(grow[0]));
-
-        // ---- fused Q prologue (first-half threads): rmsnorm then partial rotate-half
-        // RoPE, written as bf16 over the raw row in the Q tile (the A operand of
-        // S = Q'K'^T).  Rows past the sequence end were zero-filled by TMA.
-        if (hf == 0) {
-            if (!__all_sync(0xffffffffu, mbar_wait(bars.q_full(), (uint32_t)n_it & 1u, abort_flag, p.status))) return;
-            const uint32_t qbase = sbase + C::OFF_Q;
-            const uint32_t wbase = sbase + C::OFF_W;
-            float ss[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int c = 0; c < D / 8; ++c) {
-                float f[8];
-                unpack8(lds_v4(rowtile_addr(qbase, row, 8 * c)), f);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) ss[e & 3] = fmaf(f[e], f[e], ss[e & 3]);
-            }
-            const float rinv = rsqrtf(((ss[0] + ss[1]) + (ss[2] + ss[3])) / (float)D + p.eps);
-            const float posf = valid ? (p.pos ? (float)p.pos[tok] : (float)t) : 0.f;
-            const int half = p.rd >> 1;
-            for (int i0 = 0; i0 < half; i0 += 8) {
-                float xa[8], xb[8], wa[8], wb[8];
-                unpack8(lds_v4(rowtile_addr(qbase, row, i0)), xa);
-                unpack8(lds_v4(rowtile_addr(qbase, row, i0 + half)), xb);
-                unpack8(lds_v4(wbase + 2 * i0), wa);
-                unpack8(lds_v4(wbase + 2 * (i0 + half)), wb);
-                uint32_t lo[4], hi[4];
-#pragma unroll
-                for (int e = 0; e < 8; e += 2) {
-                    float s0, c0, s1, c1;
-                    rope_sincos(posf * p.inv_freq[i0 + e], &s0, &c0);
-                    rope_sincos(posf * p.inv_freq[i0 + e + 1], &s1, &c1);
-                    const float a0 = xa[e] * wa[e], b0 = xb[e] * wb[e];
-                    const float a1 = xa[e + 1] * wa[e + 1], b1 = xb[e + 1] * wb[e + 1];
-                    lo[e >> 1] = pack_bf16x2((a0 * c0 - b0 * s0) * rinv, (a1 * c1 - b1 * s1) * rinv);
-                    hi[e >> 1] = pack_bf16x2((b0 * c0 + a0 * s0) * rinv, (b1 * c1 + a1 * s1) * rinv);
-                }
-                sts_v4(rowtile_addr(qbase, row, i0), lo[0], lo[1], lo[2], lo[3]);
-                sts_v4(rowtile_addr(qbase, row, i0 + half), hi[0], hi[1], hi[2], hi[3]);
-            }
-            for (int e0 = p.rd; e0 < D; e0 += 8) {
-                float x[8], w[8];
-                unpack8(lds_v4(rowtile_addr(qbase, row, e0)), x);
-                unpack8(lds_v4(wbase + 2 * e0), w);
-                sts_v4(rowtile_addr(qbase, row, e0), pack_bf16x2(x[0] * w[0] * rinv, x[1] * w[1] * rinv),
-                       pack_bf16x2(x[2] * w[2] * rinv, x[3] * w[3] * rinv),
-                       pack_bf16x2(x[4] * w[4] * rinv, x[5] * w[5] * rinv),
-                       pack_bf16x2(x[6] * w[6] * rinv, x[7] * w[7] * rinv));
-            }
-            fence_proxy_async_smem();  // the tensor core reads Q' through the async proxy
-            __syncwarp();
-            if (lane == 0) mbar_arrive_remote(mapa_shared(bars.q_ready(), 0));  // ordinary stores: cluster release
+        if (p.gate_mode == GATTN_GATE_HEADWISE && valid) {
+            const int64_t tok = (int64_t)b * p.S + t;
+            const bf16* grow = static_cast<const bf16*>(p.gate) + tok * p.gate_tok_stride + (int64_t)h * p.gate_head_stride;
+            gate_head = sigmoidf_dev(__bfloat162float(grow[0]));
         }
 
         // ---- main loop: online softmax over the KV tiles this query tile can see.
@@ -580,10 +614,14 @@ __device__ void pair_softmax(const PrefillParams& p, const PairBars& bars, uint3
             if (lane == 0) arrive_even(bars.p_full(jg & 1), cr);
         }
 
+        // ---- the next item's Q prologue: its QK MMAs then run during this epilogue
+        const bool more = pair_item(p, cl, ncl, r + 1, next);
+        if (more && !q_prologue(next, n_it + 1)) return;
+
         // ---- epilogue: O / l * sigmoid(gate), this thread's half of the columns, as bf16
-        // into the staging tile in the K' ring (the gate tile's own slots when there
-        // is one: each thread overwrites only what it has just read); the producer
-        // then writes the tile to [B,S,H*d] with TMA stores (rows past the end clipped)
+        // into the staging tile in the V ring (the gate tile's own slots when there is
+        // one: each thread overwrites only what it has just read); the producer then
+        // writes the tile to [B,S,H*d] with TMA stores (rows past the end clipped)
         xsum[hf * C::BM + row] = l;
         if (!meet()) return;
         const float l_row = xsum[row] + xsum[C::BM + row];
@@ -594,7 +632,7 @@ __device__ void pair_softmax(const PrefillParams& p, const PairBars& bars, uint3
         tc_fence_after();
         const float inv_l = 1.f / l_row;
         const float gh = inv_l * gate_head;
-        const uint32_t gbase = sbase + C::OFF_K;
+        const uint32_t gbase = sbase + C::OFF_V;
 #pragma unroll 1
         for (int c = hf * (D / 2); c < (hf + 1) * (D / 2); c += 32) {
             uint32_t r[32];
@@ -627,6 +665,8 @@ __device__ void pair_softmax(const PrefillParams& p, const PairBars& bars, uint3
             mbar_arrive(bars.o_staged());
         }
         jb += n_kv;
+        item = next;
+        have = more;
     }
 }
 
@@ -666,7 +706,6 @@ __global__ void __launch_bounds__(PairCfg<D>::THREADS, 1)
         mbar_init(bars.drain(), 1);
         for (int q = 0; q < 4; ++q) mbar_init(bars.xchg(q), 2);
         mbar_init(bars.o_free(), C::P_ARRIVALS);
-        mbar_init(bars.e_done(), 1);
         mbar_init(bars.o_staged(), C::SOFTMAX_WARPS);
         *abort_flag = 0;
         fence_mbar_init();
