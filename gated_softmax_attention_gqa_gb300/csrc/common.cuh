@@ -135,6 +135,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// Non-blocking test of a phase (mbarrier.test_wait).  try_wait may suspend the
+// thread for a while when the phase is not complete yet, which a thread that polls
+// several barriers in turn (or looks ahead between MMA groups) cannot afford.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // Wait for the phase with the given parity to complete.  Gives up when another
 // thread of the CTA raised *abort, or after kWaitLimitNs; on a timeout it
 // raises *abort and the device status bit.  Returns true iff the phase completed.

@@ -182,7 +182,7 @@ __device__ void pair_producer(const CUtensorMap* tmK, const CUtensorMap* tmV, co
     // the V ring is free once every PV of the previous item has completed
     auto v_ring_idle = [&]() -> bool {
         for (int j = jb - C::NSV > 0 ? jb - C::NSV : 0; j < jb; ++j)
-            if (!mbar_try_wait(bars.pv_done(j % C::NSV), (uint32_t)(j / C::NSV) & 1u)) return false;
+            if (!mbar_test_wait(bars.pv_done(j % C::NSV), (uint32_t)(j / C::NSV) & 1u)) return false;
         return true;
     };
     // the previous item's gate tile, read by its epilogue, goes into the idle V ring
@@ -237,11 +237,11 @@ __device__ void pair_producer(const CUtensorMap* tmK, const CUtensorMap* tmV, co
                 load_gate();
                 g_sent = progressed = true;
             }
-            if (g_sent && !v_open && mbar_try_wait(bars.o_staged(), (uint32_t)(n_it - 2) & 1u)) {
+            if (g_sent && !v_open && mbar_test_wait(bars.o_staged(), (uint32_t)(n_it - 2) & 1u)) {
                 store_output();
                 v_open = progressed = true;
             }
-            if (nk < ke && (nk < C::NSK || mbar_try_wait(bars.s_full(nk % C::NSK), ((uint32_t)(nk / C::NSK) & 1u) ^ 1u))) {
+            if (nk < ke && (nk < C::NSK || mbar_test_wait(bars.s_full(nk % C::NSK), ((uint32_t)(nk / C::NSK) & 1u) ^ 1u))) {
                 const int st = nk % C::NSK;
                 mbar_arrive_expect_tx(bars.k_full(st), C::K_TILE);
                 const uint32_t kdst = sbase + C::OFF_K + st * C::K_TILE;
@@ -253,7 +253,7 @@ __device__ void pair_producer(const CUtensorMap* tmK, const CUtensorMap* tmV, co
                 progressed = true;
             }
             if (v_open && nv < ve &&
-                (nv < C::NSV || mbar_try_wait(bars.pv_done(nv % C::NSV), ((uint32_t)(nv / C::NSV) & 1u) ^ 1u))) {
+                (nv < C::NSV || mbar_test_wait(bars.pv_done(nv % C::NSV), ((uint32_t)(nv / C::NSV) & 1u) ^ 1u))) {
                 const int st = nv % C::NSV;
                 mbar_arrive_expect_tx(bars.v_full(st), C::V_TILE);
                 const uint32_t vdst = sbase + C::OFF_V + st * C::V_TILE;
@@ -315,12 +315,12 @@ __device__ void pair_forwarder(const PrefillParams& p, const PairBars& bars, int
     uint32_t spins = 0;
     while (fk < n_kv || fv < n_kv) {
         bool progressed = false;
-        if (fk < n_kv && mbar_try_wait(bars.k_full(fk % C::NSK), (uint32_t)(fk / C::NSK) & 1u)) {
+        if (fk < n_kv && mbar_test_wait(bars.k_full(fk % C::NSK), (uint32_t)(fk / C::NSK) & 1u)) {
             arrive_even(bars.k_full(fk % C::NSK), 1);
             ++fk;
             progressed = true;
         }
-        if (fv < n_kv && mbar_try_wait(bars.v_full(fv % C::NSV), (uint32_t)(fv / C::NSV) & 1u)) {
+        if (fv < n_kv && mbar_test_wait(bars.v_full(fv % C::NSV), (uint32_t)(fv / C::NSV) & 1u)) {
             arrive_even(bars.v_full(fv % C::NSV), 1);
             ++fv;
             progressed = true;
@@ -376,11 +376,11 @@ __device__ void pair_mma(const PrefillParams& p, const PairBars& bars, uint32_t 
                 mma2_ts(tm + C::TM_O, p_tmem + kk * 8, vd + (uint64_t)((kk * 16 * 128) >> 4), C::IDESC_PV,
                         (!first || kk > 0) ? 1u : 0u);
     };
-    auto k_ready = [&](int j) { return mbar_try_wait(bars.k_full(j % C::NSK), (uint32_t)(j / C::NSK) & 1u); };
+    auto k_ready = [&](int j) { return mbar_test_wait(bars.k_full(j % C::NSK), (uint32_t)(j / C::NSK) & 1u); };
     auto k_wait = [&](int j) { return mbar_wait(bars.k_full(j % C::NSK), (uint32_t)(j / C::NSK) & 1u, abort_flag, status); };
     auto pv_ready = [&](int j) {
-        return mbar_try_wait(bars.p_full(j & 1), (uint32_t)(j >> 1) & 1u) &&
-               mbar_try_wait(bars.v_full(j % C::NSV), (uint32_t)(j / C::NSV) & 1u);
+        return mbar_test_wait(bars.p_full(j & 1), (uint32_t)(j >> 1) & 1u) &&
+               mbar_test_wait(bars.v_full(j % C::NSV), (uint32_t)(j / C::NSV) & 1u);
     };
     auto pv_wait = [&](int j) {
         return mbar_wait(bars.p_full(j & 1), (uint32_t)(j >> 1) & 1u, abort_flag, status) &&

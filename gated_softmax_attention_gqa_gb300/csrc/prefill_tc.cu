@@ -132,7 +132,7 @@ __device__ void run_producer(const CUtensorMap* tmK, const CUtensorMap* tmV, con
     while (nk < n_kv || nv < n_kv) {
         bool progressed = false;
         if (nk < n_kv &&
-            (nk < C::NSK || mbar_try_wait(bars.k_empty(nk % C::NSK), ((uint32_t)(nk / C::NSK) & 1u) ^ 1u))) {
+            (nk < C::NSK || mbar_test_wait(bars.k_empty(nk % C::NSK), ((uint32_t)(nk / C::NSK) & 1u) ^ 1u))) {
             const int st = nk % C::NSK;
             mbar_arrive_expect_tx(bars.k_full(st), C::TILE_BYTES);
             const uint32_t kdst = sbase + C::OFF_K + st * C::TILE_BYTES;
@@ -142,9 +142,9 @@ __device__ void run_producer(const CUtensorMap* tmK, const CUtensorMap* tmV, con
             ++nk;
             progressed = true;
         }
-        if (!v_open) v_open = mbar_try_wait(bars.q_ready(), 0);
+        if (!v_open) v_open = mbar_test_wait(bars.q_ready(), 0);
         if (v_open && nv < n_kv &&
-            (nv < C::NSV || mbar_try_wait(bars.v_empty(nv % C::NSV), ((uint32_t)(nv / C::NSV) & 1u) ^ 1u))) {
+            (nv < C::NSV || mbar_test_wait(bars.v_empty(nv % C::NSV), ((uint32_t)(nv / C::NSV) & 1u) ^ 1u))) {
             const int st = nv % C::NSV;
             mbar_arrive_expect_tx(bars.v_full(st), C::TILE_BYTES);
             const uint32_t vdst = sbase + C::OFF_V + st * C::TILE_BYTES;
