@@ -21,8 +21,18 @@ import numpy as np
 
 from . import build as _build
 
-GATE_NONE, GATE_ELEMENTWISE, GATE_HEADWISE = 0, 1, 2
-_GATE_MODES = {"none": GATE_NONE, "elementwise": GATE_ELEMENTWISE, "headwise": GATE_HEADWISE}
+# gate_mode = layout | activation << 4 | ADDITIVE (the encoding of gattn_oracle.c)
+GATE_NONE, GATE_ELEMENTWISE, GATE_HEADWISE, GATE_HEAD_SHARED = 0, 1, 2, 3
+_GATE_MODES = {"none": GATE_NONE, "elementwise": GATE_ELEMENTWISE, "headwise": GATE_HEADWISE,
+               "head_shared": GATE_HEAD_SHARED}
+_GATE_ACTS = {"sigmoid": 0, "ns_sigmoid": 1, "silu": 2}
+GATE_ADDITIVE = 256
+
+
+def gate_code(layout, act="sigmoid", additive=False):
+    """The oracle's gate_mode for a layout name, an activation name and the
+    additive flag (Y + act(z) instead of Y * act(z))."""
+    return _GATE_MODES[layout] | (_GATE_ACTS[act] << 4) | (GATE_ADDITIVE if additive else 0)
 
 _lib = None
 _D = ctypes.POINTER(ctypes.c_double)
@@ -37,6 +47,8 @@ def _load():
         lib = ctypes.CDLL(path)
         lib.oracle_sigmoid.restype = ctypes.c_double
         lib.oracle_sigmoid.argtypes = [_dbl]
+        lib.oracle_gate_act.restype = ctypes.c_double
+        lib.oracle_gate_act.argtypes = [_dbl, _int]
         lib.oracle_rmsnorm.argtypes = [_D, _D, ctypes.c_int64, _int, _dbl, _D]
         lib.oracle_rope.argtypes = [_D, _D, ctypes.c_int64, _int, _int, _dbl, _D]
         lib.oracle_gate.argtypes = [_D, _D, _int, _int, _int, _D]
@@ -71,6 +83,11 @@ def sigmoid(z: float) -> float:
     return _load().oracle_sigmoid(float(z))
 
 
+def gate_act(z: float, act) -> float:
+    """The gate activation of one logit (act: "sigmoid", "ns_sigmoid", "silu")."""
+    return _load().oracle_gate_act(float(z), _GATE_ACTS[act] if isinstance(act, str) else int(act))
+
+
 def rmsnorm(x, w, eps):
     x, w = _f64(x), _f64(w)
     d = x.shape[-1]
@@ -90,7 +107,8 @@ def rope(x, pos, rotary_dim, base):
 
 
 def gate(y, z, gate_mode):
-    """y [n_heads, d]; z [n_heads, d] (elementwise) or [n_heads] (headwise)."""
+    """y [n_heads, d]; z [n_heads, d] (elementwise), [n_heads] (headwise) or [d]
+    (head-shared)."""
     y = _f64(y)
     n_heads, d = y.shape
     mode = _gate_mode(gate_mode)
@@ -107,7 +125,7 @@ def sdpa_gate(q, k, v, gate_logits, gate_mode, want_attn=False):
     B, S, H, d = q.shape
     G = k.shape[2]
     mode = _gate_mode(gate_mode)
-    z = _f64(gate_logits) if mode != GATE_NONE else np.zeros(1)
+    z = _f64(gate_logits) if (mode & 15) != GATE_NONE else np.zeros(1)
     out = np.empty((B, S, H * d))
     attn = np.empty((B, H, S, S)) if want_attn else None
     _load().oracle_sdpa_gate(_p(q), _p(k), _p(v), _p(z), B, S, H, G, d, mode, _p(out), _p(attn))
@@ -120,7 +138,7 @@ def prefill(q, k, v, gate_logits, qnorm_w, knorm_w, pos, rotary_dim, rope_base, 
     B, S, H, d = q.shape
     G = k.shape[2]
     mode = _gate_mode(gate_mode)
-    z = _f64(gate_logits) if mode != GATE_NONE else np.zeros(1)
+    z = _f64(gate_logits) if (mode & 15) != GATE_NONE else np.zeros(1)
     p = _f64(pos)
     out = np.empty((B, S, H * d))
     _load().oracle_prefill(_p(q), _p(k), _p(v), _p(z), _p(qw), _p(kw), _p(p), B, S, H, G, d, int(rotary_dim),
@@ -135,7 +153,7 @@ def prefill_rows(q, k, v, gate_logits, qnorm_w, knorm_w, pos, rotary_dim, rope_b
     B, S, H, d = q.shape
     G = k.shape[2]
     mode = _gate_mode(gate_mode)
-    z = _f64(gate_logits) if mode != GATE_NONE else np.zeros(1)
+    z = _f64(gate_logits) if (mode & 15) != GATE_NONE else np.zeros(1)
     p = _f64(pos)
     rb = np.ascontiguousarray(row_b, dtype=np.int32)
     rt = np.ascontiguousarray(row_t, dtype=np.int32)
@@ -152,7 +170,7 @@ def decode(q_new, kcache, vcache, seqlens, gate_logits, qnorm_w, rotary_dim, rop
     B, H, d = q.shape
     G, Lmax = kc.shape[1], kc.shape[2]
     mode = _gate_mode(gate_mode)
-    z = _f64(gate_logits) if mode != GATE_NONE else np.zeros(1)
+    z = _f64(gate_logits) if (mode & 15) != GATE_NONE else np.zeros(1)
     sl = np.ascontiguousarray(np.asarray(seqlens if not hasattr(seqlens, "cpu") else seqlens.cpu().numpy()),
                               dtype=np.int32)
     out = np.empty((B, H * d))

@@ -15,7 +15,11 @@
  *   multiplied by sigmoid(gate logits) before o_proj.
  *   "Gated Attention" deep-dive (cooking-agi, section "门放在哪里？"): the gate
  *   is G_h = sigmoid(X W_g,h) applied to O_h after SDPA and before W_O; headwise
- *   = one logit per token per head, elementwise = one per dimension.
+ *   = one logit per token per head, elementwise = one per dimension.  The same
+ *   section lists the variants the paper compares: head-shared scores (one
+ *   vector for all heads), an additive gate Y' = Y + sigmoid(X W), and SiLU in
+ *   place of sigmoid; section "第二条机制线索" defines the non-sparse control
+ *   NS-sigmoid(x) = 0.5 + 0.5 sigmoid(x).
  *   "Attention, worked all the way through" (curtisalexander.github.io, section
  *   "Why scaling and stable softmax matter"): softmax subtracts the row max
  *   before exp; a masked -inf becomes weight 0.  Section "Qwen3's exact order":
@@ -34,10 +38,16 @@
  *     positions only feed RoPE.
  *   - Decode: the cache holds already-normed, already-rotated K and raw V; the
  *     new query sits at position seqlen-1 and sees keys 0..seqlen-1.
+ *   - SiLU is not printed: silu(z) = z * sigmoid(z).  An additive gate with
+ *     SiLU adds silu(z).  A head-shared gate is elementwise over head_dim.
  *
  * Everything is double precision.  Layouts (all contiguous, row-major):
- *   q [B,S,H,d]   k,v [B,S,G,d]   gate [B,S,H,d] (elementwise) or [B,S,H] (headwise)
- *   out [B,S,H*d]   pos [B,S] (NULL means 0..S-1)
+ *   q [B,S,H,d]   k,v [B,S,G,d]   gate [B,S,H,d] (elementwise), [B,S,H] (headwise)
+ *   or [B,S,d] (head-shared)   out [B,S,H*d]   pos [B,S] (NULL means 0..S-1)
+ *
+ * gate_mode = layout | activation << 4 | (256 if additive): layout 0 none,
+ * 1 elementwise, 2 headwise, 3 head-shared; activation 0 sigmoid, 1 NS-sigmoid,
+ * 2 SiLU.
  */
 #include <math.h>
 #include <stddef.h>
@@ -48,6 +58,11 @@
 #define ORACLE_GATE_NONE 0
 #define ORACLE_GATE_ELEMENTWISE 1
 #define ORACLE_GATE_HEADWISE 2
+#define ORACLE_GATE_HEAD_SHARED 3
+#define ORACLE_GATE_ACT_SIGMOID 0
+#define ORACLE_GATE_ACT_NS_SIGMOID 1
+#define ORACLE_GATE_ACT_SILU 2
+#define ORACLE_GATE_ADDITIVE 256
 
 /* sigmoid(z) = 1 / (1 + e^-z), evaluated so that neither branch overflows
  * (the deep-dive's `sigmoid` helper takes the same two branches). */
@@ -114,23 +129,44 @@ static void attend_row(const double* q, const double* kr, int64_t key_stride, co
     }
 }
 
-/* Multiply a head's attention output by sigmoid of its gate logits. */
+/* The gate's activation of one logit: sigmoid, NS-sigmoid = 0.5 + 0.5 sigmoid,
+ * or SiLU = z sigmoid(z). */
+double oracle_gate_act(double z, int act) {
+    double s = oracle_sigmoid(z);
+    if (act == ORACLE_GATE_ACT_NS_SIGMOID) return 0.5 + 0.5 * s;
+    if (act == ORACLE_GATE_ACT_SILU) return z * s;
+    return s;
+}
+
+/* Gate a head's attention output: o * act(z) (multiplicative, the default) or
+ * o + act(z) (additive).  z holds d logits, or one for a headwise gate. */
 static void apply_gate(double* o, const double* z, int d, int gate_mode) {
-    if (gate_mode == ORACLE_GATE_ELEMENTWISE) {
-        for (int e = 0; e < d; ++e) o[e] *= oracle_sigmoid(z[e]);
-    } else if (gate_mode == ORACLE_GATE_HEADWISE) {
-        double g = oracle_sigmoid(z[0]);
-        for (int e = 0; e < d; ++e) o[e] *= g;
+    int layout = gate_mode & 15, act = (gate_mode >> 4) & 15;
+    int additive = (gate_mode & ORACLE_GATE_ADDITIVE) != 0;
+    if (layout == ORACLE_GATE_NONE) return;
+    for (int e = 0; e < d; ++e) {
+        double g = oracle_gate_act(layout == ORACLE_GATE_HEADWISE ? z[0] : z[e], act);
+        o[e] = additive ? o[e] + g : o[e] * g;
     }
 }
 
-/* Gate one [n_heads, d] block: out = y * sigmoid(z) (elementwise z [n_heads,d],
- * headwise z [n_heads]). */
+/* The gate logits of token row `bt` (b*S + t in prefill, b in decode) for head h:
+ * elementwise [.., H, d], headwise [.., H], head-shared [.., d]. */
+static const double* gate_at(const double* gate, int gate_mode, int64_t bt, int H, int h, int d) {
+    switch (gate_mode & 15) {
+        case ORACLE_GATE_ELEMENTWISE: return gate + (bt * H + h) * d;
+        case ORACLE_GATE_HEADWISE: return gate + bt * H + h;
+        case ORACLE_GATE_HEAD_SHARED: return gate + bt * d;
+        default: return NULL;
+    }
+}
+
+/* Gate one [n_heads, d] block y with the logits z of one token (layout as
+ * gate_mode says: [n_heads, d], [n_heads] or [d]). */
 void oracle_gate(const double* y, const double* z, int n_heads, int d, int gate_mode, double* out) {
     for (int h = 0; h < n_heads; ++h) {
         for (int e = 0; e < d; ++e) out[h * d + e] = y[h * d + e];
-        const double* zh = gate_mode == ORACLE_GATE_HEADWISE ? z + h : z + (int64_t)h * d;
-        apply_gate(out + (int64_t)h * d, zh, d, gate_mode);
+        apply_gate(out + (int64_t)h * d, gate_at(z, gate_mode, 0, n_heads, h, d), d, gate_mode);
     }
 }
 
@@ -152,10 +188,7 @@ void oracle_sdpa_gate(const double* q, const double* k, const double* v, const d
                 double* arow = attn ? attn + (((int64_t)b * H + h) * S + t) * S : NULL;
                 attend_row(qt, kb, (int64_t)G * d, vb, (int64_t)G * d, t + 1, d, o, arow, scratch);
                 if (arow) for (int j = t + 1; j < S; ++j) arow[j] = 0.0;
-                if (gate_mode == ORACLE_GATE_ELEMENTWISE)
-                    apply_gate(o, gate + (((int64_t)b * S + t) * H + h) * d, d, gate_mode);
-                else if (gate_mode == ORACLE_GATE_HEADWISE)
-                    apply_gate(o, gate + ((int64_t)b * S + t) * H + h, d, gate_mode);
+                apply_gate(o, gate_at(gate, gate_mode, (int64_t)b * S + t, H, h, d), d, gate_mode);
                 memcpy(out + ((int64_t)b * S + t) * H * d + (int64_t)h * d, o, sizeof(double) * (size_t)d);
             }
             free(scratch);
@@ -174,7 +207,7 @@ static void prologue_head(const double* x, const double* w, const double* posb, 
     }
 }
 
-/* Full prefill: QK-RMSNorm, partial RoPE, causal GQA SDPA, sigmoid gate. */
+/* Full prefill: QK-RMSNorm, partial RoPE, causal GQA SDPA, gate. */
 void oracle_prefill(const double* q, const double* k, const double* v, const double* gate, const double* qnorm_w,
                     const double* knorm_w, const double* pos, int B, int S, int H, int G, int d, int rd,
                     double base, double eps, int gate_mode, double* out) {
@@ -194,10 +227,7 @@ void oracle_prefill(const double* q, const double* k, const double* v, const dou
             const double* vb = v + ((int64_t)b * S * G + g) * d;
             for (int t = 0; t < S; ++t) {
                 attend_row(qr + (int64_t)t * d, kr, d, vb, (int64_t)G * d, t + 1, d, o, NULL, scratch);
-                if (gate_mode == ORACLE_GATE_ELEMENTWISE)
-                    apply_gate(o, gate + (((int64_t)b * S + t) * H + h) * d, d, gate_mode);
-                else if (gate_mode == ORACLE_GATE_HEADWISE)
-                    apply_gate(o, gate + ((int64_t)b * S + t) * H + h, d, gate_mode);
+                apply_gate(o, gate_at(gate, gate_mode, (int64_t)b * S + t, H, h, d), d, gate_mode);
                 memcpy(out + ((int64_t)b * S + t) * H * d + (int64_t)h * d, o, sizeof(double) * (size_t)d);
             }
             free(qr); free(kr); free(tmp); free(o); free(scratch);
@@ -238,10 +268,7 @@ void oracle_prefill_rows(const double* q, const double* k, const double* v, cons
             rope_row(tmp, posb ? posb[t] : (double)t, d, rd, base, qr);
             const double* vb = v + ((int64_t)b * S * G + g) * d;
             attend_row(qr, kr, d, vb, (int64_t)G * d, t + 1, d, o, NULL, scratch);
-            if (gate_mode == ORACLE_GATE_ELEMENTWISE)
-                apply_gate(o, gate + (((int64_t)b * S + t) * H + h) * d, d, gate_mode);
-            else if (gate_mode == ORACLE_GATE_HEADWISE)
-                apply_gate(o, gate + ((int64_t)b * S + t) * H + h, d, gate_mode);
+            apply_gate(o, gate_at(gate, gate_mode, (int64_t)b * S + t, H, h, d), d, gate_mode);
             memcpy(out + (int64_t)i * H * d + (int64_t)h * d, o, sizeof(double) * (size_t)d);
             free(qr); free(tmp); free(o); free(scratch);
         }
@@ -252,7 +279,7 @@ void oracle_prefill_rows(const double* q, const double* k, const double* v, cons
 /* Decode step against a KV cache.
  *   q_new [B,H,d] raw; kcache, vcache [B,G,Lmax,d] (K already normed and rotated);
  *   seqlens [B] includes the new token; its query sits at position seqlens[b]-1.
- *   gate [B,H,d] or [B,H]; out [B,H*d]. */
+ *   gate [B,H,d], [B,H] or [B,d]; out [B,H*d]. */
 void oracle_decode(const double* q_new, const double* kcache, const double* vcache, const int32_t* seqlens,
                    const double* gate, const double* qnorm_w, int B, int H, int G, int d, int Lmax, int rd,
                    double base, double eps, int gate_mode, double* out) {
@@ -271,10 +298,7 @@ void oracle_decode(const double* q_new, const double* kcache, const double* vcac
             const double* kb = kcache + ((int64_t)b * G + g) * Lmax * d;
             const double* vb = vcache + ((int64_t)b * G + g) * Lmax * d;
             attend_row(qr, kb, d, vb, d, L, d, o, NULL, scratch);
-            if (gate_mode == ORACLE_GATE_ELEMENTWISE)
-                apply_gate(o, gate + ((int64_t)b * H + h) * d, d, gate_mode);
-            else if (gate_mode == ORACLE_GATE_HEADWISE)
-                apply_gate(o, gate + (int64_t)b * H + h, d, gate_mode);
+            apply_gate(o, gate_at(gate, gate_mode, b, H, h, d), d, gate_mode);
             memcpy(out + (int64_t)b * H * d + (int64_t)h * d, o, sizeof(double) * (size_t)d);
             free(tmp); free(qr); free(o); free(scratch);
         }

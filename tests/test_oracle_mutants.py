@@ -28,10 +28,9 @@ MUTANTS = {
     "rope_adjacent_pairs": ("double a = x[i], b = x[i + half];", "double a = x[2 * i], b = x[2 * i + 1];"),
     "causal_excludes_diagonal": ("attend_row(qt, kb, (int64_t)G * d, vb, (int64_t)G * d, t + 1,",
                                  "attend_row(qt, kb, (int64_t)G * d, vb, (int64_t)G * d, t > 0 ? t : 1,"),
-    "gate_negated": ("for (int e = 0; e < d; ++e) o[e] *= oracle_sigmoid(z[e]);",
-                     "for (int e = 0; e < d; ++e) o[e] *= oracle_sigmoid(-z[e]);"),
-    "gate_transposed_dim": ("for (int e = 0; e < d; ++e) o[e] *= oracle_sigmoid(z[e]);",
-                            "for (int e = 0; e < d; ++e) o[e] *= oracle_sigmoid(z[d - 1 - e]);"),
+    "gate_negated": ("double s = oracle_sigmoid(z);", "double s = oracle_sigmoid(-z);"),
+    "gate_transposed_dim": ("layout == ORACLE_GATE_HEADWISE ? z[0] : z[e], act);",
+                            "layout == ORACLE_GATE_HEADWISE ? z[0] : z[d - 1 - e], act);"),
     "rmsnorm_sum_not_mean": ("double inv = 1.0 / sqrt(ss / (double)d + eps);", "double inv = 1.0 / sqrt(ss + eps);"),
     "rmsnorm_eps_outside": ("double inv = 1.0 / sqrt(ss / (double)d + eps);",
                             "double inv = 1.0 / (sqrt(ss / (double)d) + eps);"),
@@ -42,8 +41,13 @@ MUTANTS = {
                                    "rope_row(tmp, (double)L, d, rd, base, qr);"),
     "prefill_k_uses_q_weight": ("prologue_head(k + (int64_t)b * S * G * d, knorm_w, posb, S, G, g,",
                                 "prologue_head(k + (int64_t)b * S * G * d, qnorm_w, posb, S, G, g,"),
-    "headwise_gate_index": ("apply_gate(o, gate + ((int64_t)b * S + t) * H + h, d, gate_mode);",
-                            "apply_gate(o, gate + ((int64_t)t * B + b) * H + h, d, gate_mode);"),
+    "headwise_gate_index": ("case ORACLE_GATE_HEADWISE: return gate + bt * H + h;",
+                            "case ORACLE_GATE_HEADWISE: return gate + bt * H;"),
+    "ns_sigmoid_without_offset": ("return 0.5 + 0.5 * s;", "return 0.5 * s;"),
+    "silu_is_sigmoid": ("return z * s;", "return s;"),
+    "additive_multiplies": ("o[e] = additive ? o[e] + g : o[e] * g;", "o[e] = o[e] * g;"),
+    "head_shared_previous_token": ("case ORACLE_GATE_HEAD_SHARED: return gate + bt * d;",
+                                   "case ORACLE_GATE_HEAD_SHARED: return gate + (bt > 0 ? bt - 1 : 0) * d;"),
 }
 
 
@@ -86,7 +90,7 @@ def test_pins_catch_mutant(mutant, tmp_path):
     libpath = _compile_mutant(tmp_path, old, new)
     real = oracle._load()
     mutant_lib = ctypes.CDLL(libpath)
-    for fname in ("oracle_sigmoid", "oracle_rmsnorm", "oracle_rope", "oracle_gate", "oracle_sdpa_gate",
+    for fname in ("oracle_sigmoid", "oracle_gate_act", "oracle_rmsnorm", "oracle_rope", "oracle_gate", "oracle_sdpa_gate",
                   "oracle_prefill", "oracle_prefill_rows", "oracle_decode"):
         getattr(mutant_lib, fname).argtypes = getattr(real, fname).argtypes
         getattr(mutant_lib, fname).restype = getattr(real, fname).restype

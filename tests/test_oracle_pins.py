@@ -328,6 +328,79 @@ def test_decode_equals_last_prefill_row():
         np.testing.assert_allclose(dec[b], full[b, seqlens[b] - 1], rtol=1e-12, atol=1e-13)
 
 
+# ---------------------------------------------------------------- gate variants
+# ("Gated Attention" deep-dive, section "门放在哪里？": head-shared scores, an additive
+# gate Y + sigmoid(XW), SiLU instead of sigmoid; section "第二条机制线索": the
+# non-sparse control NS-sigmoid(x) = 0.5 + 0.5 sigmoid(x).)
+
+def test_gate_activation_closed_forms():
+    # NS-sigmoid: 3/4 at 0, inside [1/2, 1], symmetric about 3/4, limits 1/2 and 1
+    assert oracle.gate_act(0.0, "ns_sigmoid") == 0.75
+    for x in (-30.0, -2.5, -0.3, 0.7, 4.0, 30.0):
+        ns = oracle.gate_act(x, "ns_sigmoid")
+        assert 0.5 <= ns <= 1.0
+        assert abs(ns + oracle.gate_act(-x, "ns_sigmoid") - 1.5) < 1e-15
+    assert abs(oracle.gate_act(40.0, "ns_sigmoid") - 1.0) < 1e-15
+    assert abs(oracle.gate_act(-40.0, "ns_sigmoid") - 0.5) < 1e-15
+    # SiLU: 0 at 0; silu(x) - silu(-x) = x; silu(ln 3) = (3/4) ln 3
+    assert oracle.gate_act(0.0, "silu") == 0.0
+    for x in (-7.0, -1.2, 0.4, 3.3):
+        assert abs(oracle.gate_act(x, "silu") - oracle.gate_act(-x, "silu") - x) < 1e-13
+    assert abs(oracle.gate_act(math.log(3.0), "silu") - 0.75 * math.log(3.0)) < 1e-15
+    assert abs(oracle.gate_act(math.log(3.0), "sigmoid") - 0.75) < 1e-15
+
+
+def test_silu_gate_matches_torch_silu():
+    z = torch.linspace(-12, 12, 97, dtype=torch.float64)
+    got = oracle.gate(np.ones((1, z.numel())), z.numpy().reshape(1, -1), oracle.gate_code("elementwise", "silu"))
+    np.testing.assert_allclose(got[0], torch.nn.functional.silu(z).numpy(), rtol=1e-14, atol=1e-15)
+
+
+@pytest.mark.parametrize("layout,act", [(lay, act) for lay in ("elementwise", "headwise", "head_shared")
+                                        for act in ("sigmoid", "ns_sigmoid", "silu")])
+def test_gate_layouts_and_combine_on_constant_values(layout, act):
+    # every row of v equal to c: attention returns c exactly, so the output is c*act(z)
+    # (multiplicative) or c + act(z) (additive), with z read per head, per head and
+    # dimension, or per dimension shared by all heads
+    rng = np.random.default_rng(7)
+    B, S, H, G, d = 2, 5, 4, 2, 8
+    q, k = rng.standard_normal((B, S, H, d)), rng.standard_normal((B, S, G, d))
+    c = rng.standard_normal((G, d))
+    v = np.broadcast_to(c[None, None], (B, S, G, d)).copy()
+    z = 2.0 * rng.standard_normal({"elementwise": (B, S, H, d), "headwise": (B, S, H),
+                                   "head_shared": (B, S, d)}[layout])
+    if layout == "elementwise":
+        zfull = z
+    elif layout == "headwise":
+        zfull = np.broadcast_to(z[..., None], (B, S, H, d))
+    else:
+        zfull = np.broadcast_to(z[:, :, None, :], (B, S, H, d))
+    g = np.vectorize(lambda x: oracle.gate_act(x, act))(zfull)
+    cv = np.repeat(c, H // G, axis=0)  # head h reads group h // (H/G)
+    for additive in (False, True):
+        out = oracle.sdpa_gate(q, k, v, z, oracle.gate_code(layout, act, additive)).reshape(B, S, H, d)
+        np.testing.assert_allclose(out, cv + g if additive else cv * g, rtol=1e-12, atol=1e-12)
+
+
+def test_decode_head_shared_additive_equals_last_prefill_row():
+    rng = np.random.default_rng(23)
+    B, S, H, G, d, rd, base, eps = 2, 10, 4, 2, 16, 8, 1e6, 1e-6
+    q, k, v, _, qw, kw = _full_inputs(rng, B, S, H, G, d)
+    z = rng.standard_normal((B, S, d))
+    mode = oracle.gate_code("head_shared", "ns_sigmoid", True)
+    full = oracle.prefill(q, k, v, z, qw, kw, None, rd, base, eps, mode)
+    kc, vc = np.zeros((B, G, S, d)), np.zeros((B, G, S, d))
+    for b in range(B):
+        kc[b] = oracle.rope(oracle.rmsnorm(k[b], kw, eps), np.arange(S)[:, None], rd, base).transpose(1, 0, 2)
+        vc[b] = v[b].transpose(1, 0, 2)
+    seqlens = [S, S - 3]
+    qn = np.stack([q[b, seqlens[b] - 1] for b in range(B)])
+    zn = np.stack([z[b, seqlens[b] - 1] for b in range(B)])
+    dec = oracle.decode(qn, kc, vc, seqlens, zn, qw, rd, base, eps, mode)
+    for b in range(B):
+        np.testing.assert_allclose(dec[b], full[b, seqlens[b] - 1], rtol=1e-12, atol=1e-13)
+
+
 def test_kv_cache_byte_accounting(golden):
     from gated_softmax_attention_gqa_gb300 import workloads
 
