@@ -16,11 +16,15 @@ import torch
 from . import _lib
 from ._lib import GattnError, check
 
-GATE_MODES = {"none": 0, "elementwise": 1, "headwise": 2}
+# gate_mode = layout | activation | additive (the bit fields of gattn_gate_mode in gattn.h)
+GATE_MODES = {"none": 0, "elementwise": 1, "headwise": 2, "head_shared": 3}
+GATE_ACTS = {"sigmoid": 0x00, "ns_sigmoid": 0x10, "silu": 0x20}
+GATE_ADDITIVE = 0x100
 DTYPES = {torch.bfloat16: 0, torch.float32: 1}
 
 __all__ = ["gattn_prefill", "gattn_decode", "gattn_decode_noalloc", "gattn_prefill_workspace_size", "gattn_decode_workspace_size",
-           "gattn_get_device_status", "gattn_set_profile_events", "gattn_strerror", "GattnError", "GATE_MODES"]
+           "gattn_get_device_status", "gattn_set_profile_events", "gattn_strerror", "GattnError", "GATE_MODES",
+           "GATE_ACTS", "GATE_ADDITIVE"]
 
 
 def _ptr(t):
@@ -32,8 +36,17 @@ def _stream_handle(stream, device):
     return ctypes.c_void_p(s.cuda_stream)
 
 
-def _mode(gate_mode):
-    return GATE_MODES[gate_mode] if isinstance(gate_mode, str) else int(gate_mode)
+def _mode(gate_mode, gate_act="sigmoid", gate_additive=False):
+    """The C gate_mode for a layout name, an activation name and the additive flag
+    (an int is passed through unchanged)."""
+    if not isinstance(gate_mode, str):
+        return int(gate_mode)
+    m = GATE_MODES[gate_mode]
+    if m == 0:
+        if gate_act != "sigmoid" or gate_additive:
+            raise ValueError("gate_act / gate_additive need a gate")
+        return 0
+    return m | GATE_ACTS[gate_act] | (GATE_ADDITIVE if gate_additive else 0)
 
 
 def gattn_strerror(status: int) -> str:
@@ -82,19 +95,28 @@ def _head_strides(t, name):
 
 
 def gattn_prefill(q, k, v, gate, qnorm_w, knorm_w, pos=None, *, rotary_dim, rope_base, eps=1e-6,
-                  gate_mode="elementwise", out=None, workspace=None, stream=None):
+                  gate_mode="elementwise", gate_act="sigmoid", gate_additive=False, out=None, workspace=None,
+                  stream=None):
     """Causal gated GQA attention over whole sequences.
 
     q [B,S,H,d] (may be a strided view, e.g. the query half of the packed q_proj
-    output [B,S,H,2d]); k, v [B,S,G,d] contiguous; gate [B,S,H,d] (elementwise)
-    or [B,S,H] (headwise) or None; qnorm_w, knorm_w [d]; pos [B,S] int32 or None.
+    output [B,S,H,2d]); k, v [B,S,G,d] contiguous; gate [B,S,H,d] (elementwise),
+    [B,S,H] (headwise), [B,S,d] (head_shared: one vector for every head) or None;
+    gate_act "sigmoid" | "ns_sigmoid" | "silu"; gate_additive: out = o + act(z)
+    instead of o * act(z); qnorm_w, knorm_w [d]; pos [B,S] int32 or None.
     All on one CUDA device, bf16 or fp32 (all the same).  Returns out [B,S,H*d]."""
-    mode = _mode(gate_mode)
+    mode = _mode(gate_mode, gate_act, gate_additive)
     B, S, H, d = q.shape
     G = k.shape[2]
     dt = DTYPES[q.dtype]
     qts, qhs = _head_strides(q, "q")
-    if mode != 0:
+    if (mode & 0x0F) == GATE_MODES["head_shared"]:
+        if gate.dim() != 3 or gate.stride(-1) != 1:
+            raise ValueError("gate: a head-shared gate is [B,S,d] with a contiguous last dimension")
+        if B > 1 and S > 1 and gate.stride(0) != S * gate.stride(1):
+            raise ValueError("gate: batches must be evenly spaced tokens (stride(0) == S * stride(1))")
+        gts, ghs = (gate.stride(1) if S > 1 else gate.stride(0)), 0
+    elif mode & 0x0F:
         gts, ghs = _head_strides(gate, "gate")
     else:
         gate, gts, ghs = None, 0, 0
@@ -116,17 +138,19 @@ def gattn_prefill(q, k, v, gate, qnorm_w, knorm_w, pos=None, *, rotary_dim, rope
 
 
 def gattn_decode(q_new, kv_cache, seqlens, gate, qnorm_w, *, rotary_dim, rope_base, eps=1e-6,
-                 gate_mode="elementwise", out=None, workspace=None, stream=None):
+                 gate_mode="elementwise", gate_act="sigmoid", gate_additive=False, out=None, workspace=None,
+                 stream=None):
     """One decode step.  q_new [B,H,d] raw; kv_cache [2,B,G,Lmax,d] (K normed and
-    rotated, V raw); seqlens [B] int32 including the new token; gate [B,H,d] or
-    [B,H] or None; qnorm_w [d].  bf16.  Returns out [B,H*d]."""
-    mode = _mode(gate_mode)
+    rotated, V raw); seqlens [B] int32 including the new token; gate [B,H,d]
+    (elementwise), [B,H] (headwise), [B,d] (head_shared) or None; gate_act and
+    gate_additive as for gattn_prefill; qnorm_w [d].  bf16.  Returns out [B,H*d]."""
+    mode = _mode(gate_mode, gate_act, gate_additive)
     B, H, d = q_new.shape
     G, Lmax = kv_cache.shape[2], kv_cache.shape[3]
     for name, t in (("q_new", q_new), ("kv_cache", kv_cache), ("seqlens", seqlens), ("qnorm_w", qnorm_w)):
         if not t.is_contiguous():
             raise ValueError(f"{name} must be contiguous")
-    if mode != 0 and not gate.is_contiguous():
+    if mode & 0x0F and not gate.is_contiguous():
         raise ValueError("gate must be contiguous")
     if seqlens.dtype != torch.int32:
         raise ValueError("seqlens must be int32")
@@ -136,7 +160,7 @@ def gattn_decode(q_new, kv_cache, seqlens, gate, qnorm_w, *, rotary_dim, rope_ba
     if workspace is None or workspace.numel() * workspace.element_size() < need:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q_new.device)
     st = _lib.load().gattn_decode(
-        _ptr(q_new), _ptr(kv_cache), _ptr(seqlens), _ptr(gate if mode != 0 else None), _ptr(qnorm_w), B, H, G, d,
+        _ptr(q_new), _ptr(kv_cache), _ptr(seqlens), _ptr(gate if mode & 0x0F else None), _ptr(qnorm_w), B, H, G, d,
         Lmax, int(rotary_dim), float(rope_base), float(eps), mode, _ptr(workspace),
         workspace.numel() * workspace.element_size(), _ptr(out), _stream_handle(stream, q_new.device))
     check(st, "gattn_decode")
@@ -144,18 +168,18 @@ def gattn_decode(q_new, kv_cache, seqlens, gate, qnorm_w, *, rotary_dim, rope_ba
 
 
 def gattn_decode_noalloc(q_new, kv_cache, seqlens, gate, qnorm_w, *, rotary_dim, rope_base, eps=1e-6,
-                         gate_mode="elementwise", out=None, stream=None):
+                         gate_mode="elementwise", gate_act="sigmoid", gate_additive=False, out=None, stream=None):
     """gattn_decode without a workspace: the partial states live in the library's
     own fixed device array (GATTN_DECODE_NOALLOC_SCRATCH_BYTES).  For callers that
     must not allocate device memory while decoding; pass `out` to allocate nothing
     here either.  Calls that overlap on the GPU race on that array."""
-    mode = _mode(gate_mode)
+    mode = _mode(gate_mode, gate_act, gate_additive)
     B, H, d = q_new.shape
     G, Lmax = kv_cache.shape[2], kv_cache.shape[3]
     if out is None:
         out = torch.empty((B, H * d), dtype=q_new.dtype, device=q_new.device)
     st = _lib.load().gattn_decode_noalloc(
-        _ptr(q_new), _ptr(kv_cache), _ptr(seqlens), _ptr(gate if mode != 0 else None), _ptr(qnorm_w), B, H, G, d,
+        _ptr(q_new), _ptr(kv_cache), _ptr(seqlens), _ptr(gate if mode & 0x0F else None), _ptr(qnorm_w), B, H, G, d,
         Lmax, int(rotary_dim), float(rope_base), float(eps), mode, _ptr(out), _stream_handle(stream, q_new.device))
     check(st, "gattn_decode_noalloc")
     return out

@@ -128,7 +128,14 @@ bool encode_bf16_map_uncached(CUtensorMap* map, const void* base, int rank, cons
     return r == CUDA_SUCCESS;
 }
 
-bool valid_gate_mode(int m) { return m == GATTN_GATE_NONE || m == GATTN_GATE_ELEMENTWISE || m == GATTN_GATE_HEADWISE; }
+// layout | activation | additive; no gate means no activation or combine bits either
+bool valid_gate_mode(int m) {
+    if (m < 0 || (m & ~0x1FF)) return false;
+    const int layout = m & 0x0F, act = m & 0xF0;
+    if (layout > GATTN_GATE_HEAD_SHARED) return false;
+    if (act != GATTN_GATE_ACT_SIGMOID && act != GATTN_GATE_ACT_NS_SIGMOID && act != GATTN_GATE_ACT_SILU) return false;
+    return layout != GATTN_GATE_NONE || m == GATTN_GATE_NONE;
+}
 
 size_t prefill_ws(int B, int S, int H, int G, int d, int dtype) {
     if (B < 1 || S < 1 || H < 1 || G < 1 || d < 1) return 0;
@@ -170,7 +177,8 @@ gattn_status gattn_prefill(const void* q, const void* k, const void* v, const vo
                            void* workspace, size_t workspace_bytes, void* out, void* stream_) {
     // ---- arguments
     if (!q || !k || !v || !qnorm_w || !knorm_w || !out) return GATTN_ERR_INVALID_ARG;
-    if (!valid_gate_mode(gate_mode) || (gate_mode != GATTN_GATE_NONE && !gate)) return GATTN_ERR_INVALID_ARG;
+    if (!valid_gate_mode(gate_mode) || (gate_layout(gate_mode) != GATTN_GATE_NONE && !gate))
+        return GATTN_ERR_INVALID_ARG;
     if (dtype != GATTN_BF16 && dtype != GATTN_FP32) return GATTN_ERR_INVALID_ARG;
     if (B < 1 || S < 1 || H < 1 || G < 1 || d < 1 || H % G != 0) return GATTN_ERR_INVALID_ARG;
     if (rotary_dim < 0 || rotary_dim > d || (rotary_dim & 1)) return GATTN_ERR_INVALID_ARG;
@@ -185,15 +193,17 @@ gattn_status gattn_prefill(const void* q, const void* k, const void* v, const vo
     if (bf && rotary_dim % 16 != 0) return GATTN_ERR_UNSUPPORTED;
     if (q_tok_stride == 0) q_tok_stride = (int64_t)H * d;
     if (q_head_stride == 0) q_head_stride = d;
-    const bool headwise = gate_mode == GATTN_GATE_HEADWISE;
-    if (gate_tok_stride == 0) gate_tok_stride = headwise ? H : (int64_t)H * d;
+    const int glayout = gate_layout(gate_mode);
+    const bool headwise = glayout == GATTN_GATE_HEADWISE, shared = glayout == GATTN_GATE_HEAD_SHARED;
+    if (gate_tok_stride == 0) gate_tok_stride = headwise ? H : shared ? d : (int64_t)H * d;
     if (gate_head_stride == 0) gate_head_stride = headwise ? 1 : d;
+    if (shared) gate_head_stride = 0;  // one vector of logits for every head
     if (q_tok_stride < 0 || q_head_stride < 0 || gate_tok_stride < 0 || gate_head_stride < 0)
         return GATTN_ERR_INVALID_ARG;
     const int64_t vec = 16 / elt;
     if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16)) return GATTN_ERR_INVALID_ARG;
     if (q_tok_stride % vec || q_head_stride % vec) return GATTN_ERR_INVALID_ARG;
-    if (gate_mode == GATTN_GATE_ELEMENTWISE && (!aligned(gate, 16) || gate_tok_stride % vec || gate_head_stride % vec))
+    if (gate_per_dim(gate_mode) && (!aligned(gate, 16) || gate_tok_stride % vec || gate_head_stride % vec))
         return GATTN_ERR_INVALID_ARG;
     if (bf && (!aligned(qnorm_w, 16) || !aligned(knorm_w, 16))) return GATTN_ERR_INVALID_ARG;
     const size_t need = prefill_ws(B, S, H, G, d, dtype);
@@ -242,10 +252,12 @@ gattn_status gattn_prefill(const void* q, const void* k, const void* v, const vo
         if (!encode_bf16_map(&maps.k, workspace, 3, kdims, kstr, kbox)) return GATTN_ERR_CUDA;
         if (!encode_bf16_map(&maps.v, v, 4, vdims, vstr, vbox)) return GATTN_ERR_CUDA;
         if (!encode_bf16_map(&maps.q, q, 4, hdims, qstr, rbox)) return GATTN_ERR_CUDA;
-        if (gate_mode == GATTN_GATE_ELEMENTWISE) {
-            const uint64_t gstr[3] = {(uint64_t)gate_head_stride * 2, (uint64_t)gate_tok_stride * 2,
-                                      (uint64_t)S * gate_tok_stride * 2};
-            if (!encode_bf16_map(&maps.gate, gate, 4, hdims, gstr, rbox)) return GATTN_ERR_CUDA;
+        if (gate_per_dim(gate_mode)) {
+            // (d, H, S, B); a head-shared gate has a single head (its stride is unused)
+            const uint64_t gdims[4] = {(uint64_t)d, shared ? 1u : (uint64_t)H, (uint64_t)S, (uint64_t)B};
+            const uint64_t gstr[3] = {(uint64_t)(shared ? gate_tok_stride : gate_head_stride) * 2,
+                                      (uint64_t)gate_tok_stride * 2, (uint64_t)S * gate_tok_stride * 2};
+            if (!encode_bf16_map(&maps.gate, gate, 4, gdims, gstr, rbox)) return GATTN_ERR_CUDA;
         } else {
             maps.gate = maps.q;  // never read
         }
@@ -327,7 +339,8 @@ gattn_status gattn_decode(const void* q_new, const void* kv_cache, const int32_t
                           double rope_base, float eps, int gate_mode, void* workspace, size_t workspace_bytes,
                           void* out, void* stream_) {
     if (!q_new || !kv_cache || !seqlens || !qnorm_w || !out) return GATTN_ERR_INVALID_ARG;
-    if (!valid_gate_mode(gate_mode) || (gate_mode != GATTN_GATE_NONE && !gate)) return GATTN_ERR_INVALID_ARG;
+    if (!valid_gate_mode(gate_mode) || (gate_layout(gate_mode) != GATTN_GATE_NONE && !gate))
+        return GATTN_ERR_INVALID_ARG;
     if (B < 1 || H < 1 || G < 1 || d < 1 || Lmax < 1 || H % G != 0) return GATTN_ERR_INVALID_ARG;
     if (rotary_dim < 0 || rotary_dim > d || (rotary_dim & 1)) return GATTN_ERR_INVALID_ARG;
     if (rotary_dim > 0 && !(rope_base > 0.0 && std::isfinite(rope_base))) return GATTN_ERR_INVALID_ARG;

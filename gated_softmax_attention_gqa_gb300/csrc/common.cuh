@@ -67,6 +67,23 @@ __device__ __forceinline__ float sigmoid_tanh(float z) {
     return fmaf(0.5f, t, 0.5f);
 }
 
+// Gate variants (gattn_gate_mode bit fields).  gate_plain: the default
+// multiplicative sigmoid gate, for which the epilogues keep their fast path.
+__host__ __device__ __forceinline__ int gate_layout(int mode) { return mode & 0x0F; }
+__host__ __device__ __forceinline__ bool gate_additive(int mode) { return (mode & 0x100) != 0; }
+__host__ __device__ __forceinline__ bool gate_plain(int mode) { return (mode & 0x1F0) == 0; }
+// Logits held per (token, head, dimension) -- elementwise, or head-shared [.., d].
+__host__ __device__ __forceinline__ bool gate_per_dim(int mode) {
+    return gate_layout(mode) == 1 || gate_layout(mode) == 3;
+}
+
+// The gate activation of logit z given s = sigmoid(z): sigmoid, NS-sigmoid
+// 0.5 + 0.5 sigmoid(z), or SiLU z sigmoid(z).
+__device__ __forceinline__ float gate_act(float z, float s, int mode) {
+    const int act = mode & 0xF0;
+    return act == 0x10 ? fmaf(0.5f, s, 0.5f) : act == 0x20 ? z * s : s;
+}
+
 // sin and cos of a RoPE angle.  Cody-Waite reduction by 2*pi (the constant split
 // into a float head and a float tail, k = round(x / 2pi)) brings x into
 // [-pi, pi], where the hardware sine/cosine approximations are accurate to about

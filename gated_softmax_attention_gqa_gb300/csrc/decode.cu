@@ -432,11 +432,15 @@ __global__ void __launch_bounds__(kCombineThreads) decode_combine_kernel(const _
     for (int idx = tid; idx < r * D; idx += blockDim.x) {
         const int hl = idx / D, e = idx % D;
         const int h = g * r + hl;
+        // gate logit: [B,H,d] elementwise, [B,H] headwise, [B,d] head-shared
+        const int layout = gate_layout(p.gate_mode);
         float gl = 0.f;
-        if (p.gate_mode == GATTN_GATE_ELEMENTWISE)
+        if (layout == GATTN_GATE_ELEMENTWISE)
             gl = __bfloat162float(static_cast<const bf16*>(p.gate)[((int64_t)b * p.H + h) * D + e]);
-        else if (p.gate_mode == GATTN_GATE_HEADWISE)
+        else if (layout == GATTN_GATE_HEADWISE)
             gl = __bfloat162float(static_cast<const bf16*>(p.gate)[(int64_t)b * p.H + h]);
+        else if (layout == GATTN_GATE_HEAD_SHARED)
+            gl = __bfloat162float(static_cast<const bf16*>(p.gate)[(int64_t)b * D + e]);
         const float* src = part0 + 2 * r + hl * D + e;
         float num = 0.f;
         for (int sl0 = 0; sl0 < n_slots; sl0 += CH) {
@@ -449,8 +453,10 @@ __global__ void __launch_bounds__(kCombineThreads) decode_combine_kernel(const _
                 num += wgt != 0.f ? wgt * v[j] : 0.f;
             }
         }
-        const float gv = p.gate_mode == GATTN_GATE_NONE ? 1.f : sigmoidf_dev(gl);
-        static_cast<bf16*>(p.out)[((int64_t)b * p.H + h) * D + e] = __float2bfloat16_rn(num / den[hl] * gv);
+        const float gv = layout == GATTN_GATE_NONE ? 1.f : gate_act(gl, sigmoidf_dev(gl), p.gate_mode);
+        const float o = num / den[hl];
+        static_cast<bf16*>(p.out)[((int64_t)b * p.H + h) * D + e] =
+            __float2bfloat16_rn(gate_additive(p.gate_mode) ? o + gv : o * gv);
     }
 }
 

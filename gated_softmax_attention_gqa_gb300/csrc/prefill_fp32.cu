@@ -59,21 +59,24 @@ __global__ void __launch_bounds__(kRowsPerBlock * 32) prefill_f32_kernel(const _
     const float inv_l = 1.f / l;
     const int64_t tok = (int64_t)b * p.S + t;
     float* out = p.out + (tok * p.H + h) * d;
+    // the gate's activation: one per head (headwise), else per dimension
+    // (elementwise, or head-shared with a head stride of 0); none: 1
     float gh = 1.f;
-    if (p.gate_mode == GATTN_GATE_HEADWISE) {
+    if (gate_layout(p.gate_mode) == GATTN_GATE_HEADWISE) {
         const float z = p.gate[tok * p.gate_tok_stride + (int64_t)h * p.gate_head_stride];
-        gh = 1.f / (1.f + expf(-z));
+        gh = gate_act(z, 1.f / (1.f + expf(-z)), p.gate_mode);
     }
+    const bool additive = gate_additive(p.gate_mode);
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         if (i >= ne) continue;
         const int e = lane + 32 * i;
         float gv = gh;
-        if (p.gate_mode == GATTN_GATE_ELEMENTWISE) {
+        if (gate_per_dim(p.gate_mode)) {
             const float z = p.gate[tok * p.gate_tok_stride + (int64_t)h * p.gate_head_stride + e];
-            gv = 1.f / (1.f + expf(-z));
+            gv = gate_act(z, 1.f / (1.f + expf(-z)), p.gate_mode);
         }
-        out[e] = o[i] * inv_l * gv;
+        out[e] = additive ? o[i] * inv_l + gv : o[i] * inv_l * gv;
     }
 }
 

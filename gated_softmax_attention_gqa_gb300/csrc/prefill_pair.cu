@@ -165,13 +165,16 @@ __device__ __forceinline__ bool pair_item(const PrefillParams& p, int cl, int nc
 
 // ----------------------------------------------------------------- producer
 
-template <int D>
+template <int D, bool GV>
 __device__ void pair_producer(const CUtensorMap* tmK, const CUtensorMap* tmV, const CUtensorMap* tmQ,
                               const CUtensorMap* tmG, const CUtensorMap* tmO, const PrefillParams& p,
                               const PairBars& bars, uint32_t sbase, int cl, int ncl, uint32_t cr, volatile int* abort_flag,
                               unsigned int* status) {
     using C = PairCfg<D>;
-    const bool gate_tile = p.gate_mode == GATTN_GATE_ELEMENTWISE;
+    // a gate tile per item when the logits vary over head_dim (elementwise, or one
+    // head-shared vector per token: the gate map then has a single head)
+    const bool gate_tile = GV ? gate_per_dim(p.gate_mode) : p.gate_mode == GATTN_GATE_ELEMENTWISE;
+    const bool shared = GV && gate_layout(p.gate_mode) == GATTN_GATE_HEAD_SHARED;
     int nk = 0, nv = 0;  // K' / V tiles issued, over all items
     int jb = 0;          // tiles of the items before the current one
     int n_it = 0, n_g = 0;
@@ -190,7 +193,8 @@ __device__ void pair_producer(const CUtensorMap* tmK, const CUtensorMap* tmV, co
         mbar_arrive_expect_tx(bars.g_full(), C::QTILE_BYTES);
 #pragma unroll
         for (int c = 0; c < C::KCH; ++c)
-            tma_load_4d(sbase + C::OFF_V + c * C::ROWBOX_BYTES, tmG, bars.g_full(), c * 64, prev_h, prev_qt * C::BM,
+            tma_load_4d(sbase + C::OFF_V + c * C::ROWBOX_BYTES, tmG, bars.g_full(), c * 64, shared ? 0 : prev_h,
+                        prev_qt * C::BM,
                         prev_b);
         ++n_g;
     };
@@ -219,7 +223,7 @@ __device__ void pair_producer(const CUtensorMap* tmK, const CUtensorMap* tmV, co
         // the gate tile is read at the very end of the item: start it on its way to L2 now
         if (gate_tile) {
 #pragma unroll
-            for (int c = 0; c < C::KCH; ++c) tma_prefetch_l2_4d(tmG, c * 64, h, it.qt * C::BM, it.b);
+            for (int c = 0; c < C::KCH; ++c) tma_prefetch_l2_4d(tmG, c * 64, shared ? 0 : h, it.qt * C::BM, it.b);
         }
         // K' comes from the pre-pass kernel launched just before this one
         if (n_it == 1) pdl_wait_prerequisites();
@@ -436,7 +440,10 @@ __device__ void pair_mma(const PrefillParams& p, const PairBars& bars, uint32_t 
 
 // ----------------------------------------------------------------- softmax / prologue / epilogue
 
-template <int D>
+// GV: the gate variants (head-shared logits, NS-sigmoid, SiLU, additive) -- a
+// second instance of the kernel, so that the default elementwise / headwise
+// multiplicative sigmoid gate compiles exactly as it would alone.
+template <int D, bool GV>
 __device__ void pair_softmax(const PrefillParams& p, const PairBars& bars, uint32_t sbase, uint8_t* smem_x, uint32_t tm,
                              uint32_t cr, int quarter, int hf, int lane, int cl, int ncl, volatile int* abort_flag) {
     using C = PairCfg<D>;
@@ -523,11 +530,12 @@ __device__ void pair_softmax(const PrefillParams& p, const PairBars& bars, uint3
         const int qt = item.qt, b = item.b, h = 2 * item.hp + (int)cr, n_kv = item.n_kv;
         const int t = qt * C::BM + row;
         const bool valid = t < p.S;
-        float gate_head = 1.f;
-        if (p.gate_mode == GATTN_GATE_HEADWISE && valid) {
+        float gate_head = 1.f;  // the activation of a headwise logit
+        if ((GV ? gate_layout(p.gate_mode) : p.gate_mode) == GATTN_GATE_HEADWISE && valid) {
             const int64_t tok = (int64_t)b * p.S + t;
             const bf16* grow = static_cast<const bf16*>(p.gate) + tok * p.gate_tok_stride + (int64_t)h * p.gate_head_stride;
-            gate_head = sigmoidf_dev(__bfloat162float(grow[0]));
+            const float z = __bfloat162float(grow[0]);
+            gate_head = GV ? gate_act(z, sigmoidf_dev(z), p.gate_mode) : sigmoidf_dev(z);
         }
 
         // ---- main loop: online softmax over the KV tiles this query tile can see.
@@ -618,7 +626,8 @@ __device__ void pair_softmax(const PrefillParams& p, const PairBars& bars, uint3
         const bool more = pair_item(p, cl, ncl, r + 1, next);
         if (more && !q_prologue(next, n_it + 1)) return;
 
-        // ---- epilogue: O / l * sigmoid(gate), this thread's half of the columns, as bf16
+        // ---- epilogue: O / l * act(gate) (or O / l + act(gate) for an additive gate),
+        // this thread's half of the columns, as bf16
         // into the staging tile in the V ring (the gate tile's own slots when there is
         // one: each thread overwrites only what it has just read); the producer then
         // writes the tile to [B,S,H*d] with TMA stores (rows past the end clipped)
@@ -626,12 +635,15 @@ __device__ void pair_softmax(const PrefillParams& p, const PairBars& bars, uint3
         if (!meet()) return;
         const float l_row = xsum[row] + xsum[C::BM + row];
         if (!__all_sync(0xffffffffu, mbar_wait(bars.o_final(), (uint32_t)n_it & 1u, abort_flag, p.status))) return;
-        const bool elementwise = p.gate_mode == GATTN_GATE_ELEMENTWISE;
+        const bool elementwise = GV ? gate_per_dim(p.gate_mode) : p.gate_mode == GATTN_GATE_ELEMENTWISE;
+        constexpr bool plain = !GV;
+        const bool additive = GV && gate_additive(p.gate_mode);
         if (elementwise && !__all_sync(0xffffffffu, mbar_wait(bars.g_full(), (uint32_t)n_it & 1u, abort_flag, p.status)))
             return;
         tc_fence_after();
         const float inv_l = 1.f / l_row;
-        const float gh = inv_l * gate_head;
+        // out = o * gm + ga
+        const float gh = additive ? inv_l : inv_l * gate_head, gha = additive ? gate_head : 0.f;
         const uint32_t gbase = sbase + C::OFF_V;
 #pragma unroll 1
         for (int c = hf * (D / 2); c < (hf + 1) * (D / 2); c += 32) {
@@ -641,19 +653,43 @@ __device__ void pair_softmax(const PrefillParams& p, const PairBars& bars, uint3
 #pragma unroll
             for (int q4 = 0; q4 < 4; ++q4) {
                 const uint32_t addr = rowtile_addr(gbase, row, c + 8 * q4);
-                float gv[8];
+                const float* o = reinterpret_cast<const float*>(r + 8 * q4);
+                if constexpr (plain) {  // the default multiplicative sigmoid gate
+                    float gv[8];
+                    if (elementwise) {
+                        float f[8];
+                        unpack8(lds_v4(addr), f);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) gv[e] = inv_l * sigmoid_tanh(f[e]);
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) gv[e] = gh;
+                    }
+                    sts_v4(addr, pack_bf16x2(o[0] * gv[0], o[1] * gv[1]), pack_bf16x2(o[2] * gv[2], o[3] * gv[3]),
+                           pack_bf16x2(o[4] * gv[4], o[5] * gv[5]), pack_bf16x2(o[6] * gv[6], o[7] * gv[7]));
+                } else {
+                float gv[8], ga[8];  // out = o * gv + ga
                 if (elementwise) {
                     float f[8];
                     unpack8(lds_v4(addr), f);
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) gv[e] = inv_l * sigmoid_tanh(f[e]);
+                    for (int e = 0; e < 8; ++e) {
+                        const float a = gate_act(f[e], sigmoid_tanh(f[e]), p.gate_mode);
+                        gv[e] = additive ? inv_l : inv_l * a;
+                        ga[e] = additive ? a : 0.f;
+                    }
                 } else {
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) gv[e] = gh;
+                    for (int e = 0; e < 8; ++e) {
+                        gv[e] = gh;
+                        ga[e] = gha;
+                    }
                 }
-                const float* o = reinterpret_cast<const float*>(r + 8 * q4);
-                sts_v4(addr, pack_bf16x2(o[0] * gv[0], o[1] * gv[1]), pack_bf16x2(o[2] * gv[2], o[3] * gv[3]),
-                       pack_bf16x2(o[4] * gv[4], o[5] * gv[5]), pack_bf16x2(o[6] * gv[6], o[7] * gv[7]));
+                sts_v4(addr, pack_bf16x2(fmaf(o[0], gv[0], ga[0]), fmaf(o[1], gv[1], ga[1])),
+                       pack_bf16x2(fmaf(o[2], gv[2], ga[2]), fmaf(o[3], gv[3], ga[3])),
+                       pack_bf16x2(fmaf(o[4], gv[4], ga[4]), fmaf(o[5], gv[5], ga[5])),
+                       pack_bf16x2(fmaf(o[6], gv[6], ga[6]), fmaf(o[7], gv[7], ga[7])));
+                }
             }
         }
         // O has been read: the next item's first PV may overwrite it
@@ -672,7 +708,7 @@ __device__ void pair_softmax(const PrefillParams& p, const PairBars& bars, uint3
 
 // ----------------------------------------------------------------- kernel
 
-template <int D>
+template <int D, bool GV>
 __global__ void __launch_bounds__(PairCfg<D>::THREADS, 1)
     prefill_pair_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                         const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmG,
@@ -730,7 +766,7 @@ __global__ void __launch_bounds__(PairCfg<D>::THREADS, 1)
 
     if (warp == 0) {
         if (lane == 0)
-            pair_producer<D>(&tmK, &tmV, &tmQ, &tmG, &tmO, p, bars, sbase, cl, ncl, cr, abort_flag, p.status);
+            pair_producer<D, GV>(&tmK, &tmV, &tmQ, &tmG, &tmO, p, bars, sbase, cl, ncl, cr, abort_flag, p.status);
         __syncwarp();
     } else if (warp == 1) {
         if (lane == 0) {
@@ -739,7 +775,7 @@ __global__ void __launch_bounds__(PairCfg<D>::THREADS, 1)
         }
         __syncwarp();
     } else {
-        pair_softmax<D>(p, bars, sbase, smem + C::OFF_X, tm, cr, warp & 3, (warp - 2) >> 2, lane, cl, ncl, abort_flag);
+        pair_softmax<D, GV>(p, bars, sbase, smem + C::OFF_X, tm, cr, warp & 3, (warp - 2) >> 2, lane, cl, ncl, abort_flag);
     }
     // both CTAs are done with the pair's TMEM (the issuer drained every MMA) before it is released
     tc_fence_before();
@@ -755,7 +791,9 @@ template <int D>
 cudaError_t launch_pair_d(const PrefillParams& p, const PrefillMaps& maps, cudaStream_t stream, cudaEvent_t ev_start,
                           cudaEvent_t ev_stop) {
     using C = PairCfg<D>;
-    cudaError_t e = set_smem_once(reinterpret_cast<const void*>(prefill_pair_kernel<D>), C::SMEM_ALLOC);
+    const bool gv = !gate_plain(p.gate_mode) || gate_layout(p.gate_mode) == GATTN_GATE_HEAD_SHARED;
+    auto kernel = gv ? prefill_pair_kernel<D, true> : prefill_pair_kernel<D, false>;
+    cudaError_t e = set_smem_once(reinterpret_cast<const void*>(kernel), C::SMEM_ALLOC);
     if (e != cudaSuccess) return e;
     const long long n_items = (long long)p.n_qtiles * p.B * (p.H / 2);
     const long long max_clusters = p.n_sms >= 2 ? p.n_sms / 2 : 1;
@@ -776,7 +814,7 @@ cudaError_t launch_pair_d(const PrefillParams& p, const PrefillMaps& maps, cudaS
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    cudaError_t err = cudaLaunchKernelEx(&cfg, prefill_pair_kernel<D>, maps.k, maps.v, maps.q, maps.gate, maps.out, p);
+    cudaError_t err = cudaLaunchKernelEx(&cfg, kernel, maps.k, maps.v, maps.q, maps.gate, maps.out, p);
     if (ev_stop) cudaEventRecord(ev_stop, stream);
     return err;
 }

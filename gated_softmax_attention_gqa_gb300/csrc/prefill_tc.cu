@@ -111,7 +111,7 @@ template <int D>
 __device__ void run_producer(const CUtensorMap* tmK, const CUtensorMap* tmV, const CUtensorMap* tmQ,
                              const CUtensorMap* tmG, const void* qnorm_w, const Bars& bars, uint32_t sbase, int n_kv,
                              int b, int g, int h,
-                             int qt, int G, bool gate_tile, volatile int* abort_flag, unsigned int* status) {
+                             int qt, int G, bool gate_tile, int gate_h, volatile int* abort_flag, unsigned int* status) {
     using C = PfCfg<D>;
     // raw Q tile into the (still unused) V ring, the q norm weights next to it
     mbar_arrive_expect_tx(bars.q_full(), C::QTILE_BYTES + D * 2);
@@ -177,7 +177,7 @@ __device__ void run_producer(const CUtensorMap* tmK, const CUtensorMap* tmV, con
             mbar_arrive_expect_tx(bars.g_full(), C::QTILE_BYTES);
 #pragma unroll
             for (int c = 0; c < C::KCH; ++c)
-                tma_load_4d(sbase + C::OFF_K + c * C::ROWBOX_BYTES, tmG, bars.g_full(), c * 64, h, qt * C::BM, b);
+                tma_load_4d(sbase + C::OFF_K + c * C::ROWBOX_BYTES, tmG, bars.g_full(), c * 64, gate_h, qt * C::BM, b);
             g_issued = true;
         }
     }
@@ -285,7 +285,10 @@ __device__ void run_mma(int parity, const Bars& bars, uint32_t sbase, uint32_t t
 
 // ----------------------------------------------------------------- softmax / prologue / epilogue
 
-template <int D>
+// GV: the gate variants (head-shared logits, NS-sigmoid, SiLU, additive) -- a
+// second instance of the kernel, so that the default elementwise / headwise
+// multiplicative sigmoid gate compiles exactly as it would alone.
+template <int D, bool GV>
 __device__ void run_softmax(const PrefillParams& p, const Bars& bars, uint32_t sbase, uint32_t tm, int quarter,
                             int lane, int qt, int b, int h, int n_kv, volatile int* abort_flag) {
     using C = PfCfg<D>;
@@ -296,8 +299,11 @@ __device__ void run_softmax(const PrefillParams& p, const Bars& bars, uint32_t s
     const bool valid = t < p.S;
     const int64_t tok = (int64_t)b * p.S + (valid ? t : 0);
     const bf16* grow = static_cast<const bf16*>(p.gate) + tok * p.gate_tok_stride + (int64_t)h * p.gate_head_stride;
-    float gate_head = 1.f;
-    if (p.gate_mode == GATTN_GATE_HEADWISE && valid) gate_head = sigmoidf_dev(__bfloat162float(grow[0]));
+    float gate_head = 1.f;  // the activation of a headwise logit
+    if ((GV ? gate_layout(p.gate_mode) : p.gate_mode) == GATTN_GATE_HEADWISE && valid) {
+        const float z = __bfloat162float(grow[0]);
+        gate_head = GV ? gate_act(z, sigmoidf_dev(z), p.gate_mode) : sigmoidf_dev(z);
+    }
 
     // ---- fused Q prologue: rmsnorm then partial rotate-half RoPE, bf16 into TMEM.
     // The raw row is read from the Q tile the producer placed in the V ring
@@ -483,50 +489,90 @@ __device__ void run_softmax(const PrefillParams& p, const Bars& bars, uint32_t s
         }
     }
 
-    // ---- epilogue: O / l * sigmoid(gate) -> bf16 [B,S,H*d]
+    // ---- epilogue: O / l * act(gate) (additive gate: O / l + act(gate)) -> bf16 [B,S,H*d]
     if (!__all_sync(0xffffffffu, mbar_wait(bars.o_final(), 0, abort_flag, p.status))) return;
-    const bool elementwise = p.gate_mode == GATTN_GATE_ELEMENTWISE;
+    const bool elementwise = GV ? gate_per_dim(p.gate_mode) : p.gate_mode == GATTN_GATE_ELEMENTWISE;
+    constexpr bool plain = !GV;
+    const bool additive = GV && gate_additive(p.gate_mode);
     if (elementwise && !__all_sync(0xffffffffu, mbar_wait(bars.g_full(), 0, abort_flag, p.status))) return;
     tc_fence_after();
     const float inv_l = 1.f / l;
-    const float gh = inv_l * gate_head;
+    // out = o * gv + ga
+    const float gh = additive ? inv_l : inv_l * gate_head, gha = additive ? gate_head : 0.f;
     bf16* orow = static_cast<bf16*>(p.out) + (tok * p.H + h) * D;
     const uint32_t gbase = sbase + C::OFF_K;
+    // the default multiplicative sigmoid gate keeps a loop of its own (its cost is
+    // the epilogue's); the variants share a second one
 #pragma unroll 1
     for (int c = 0; c < D; c += 32) {
         uint32_t r[32];
         __syncwarp();
         tmem_ld32(tl + C::TM_O + c, r);
         if (!valid) continue;
-        float gv[32];
+        uint4* dst = reinterpret_cast<uint4*>(orow + c);
+        if constexpr (plain) {
+            float gv[32];
+            if (elementwise) {
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4) {
+                    float f[8];
+                    unpack8(lds_v4(rowtile_addr(gbase, row, c + 8 * q4)), f);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) gv[8 * q4 + e] = inv_l * sigmoidf_dev(f[e]);
+                }
+            } else {
+#pragma unroll
+                for (int e = 0; e < 32; ++e) gv[e] = gh;
+            }
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+                uint32_t w[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int e = 8 * q4 + 2 * i;
+                    w[i] = pack_bf16x2(__uint_as_float(r[e]) * gv[e], __uint_as_float(r[e + 1]) * gv[e + 1]);
+                }
+                dst[q4] = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+        } else {
+        float gv[32], ga[32];
         if (elementwise) {
 #pragma unroll
             for (int q4 = 0; q4 < 4; ++q4) {
                 float f[8];
                 unpack8(lds_v4(rowtile_addr(gbase, row, c + 8 * q4)), f);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) gv[8 * q4 + e] = inv_l * sigmoidf_dev(f[e]);
+                for (int e = 0; e < 8; ++e) {
+                    const float a = gate_act(f[e], sigmoidf_dev(f[e]), p.gate_mode);
+                    gv[8 * q4 + e] = additive ? inv_l : inv_l * a;
+                    ga[8 * q4 + e] = additive ? a : 0.f;
+                }
             }
         } else {
 #pragma unroll
-            for (int e = 0; e < 32; ++e) gv[e] = gh;
+            for (int e = 0; e < 32; ++e) {
+                gv[e] = gh;
+                ga[e] = gha;
+            }
         }
-        uint4* dst = reinterpret_cast<uint4*>(orow + c);
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4) {
-            uint4 v;
-            v.x = pack_bf16x2(__uint_as_float(r[8 * q4 + 0]) * gv[8 * q4 + 0], __uint_as_float(r[8 * q4 + 1]) * gv[8 * q4 + 1]);
-            v.y = pack_bf16x2(__uint_as_float(r[8 * q4 + 2]) * gv[8 * q4 + 2], __uint_as_float(r[8 * q4 + 3]) * gv[8 * q4 + 3]);
-            v.z = pack_bf16x2(__uint_as_float(r[8 * q4 + 4]) * gv[8 * q4 + 4], __uint_as_float(r[8 * q4 + 5]) * gv[8 * q4 + 5]);
-            v.w = pack_bf16x2(__uint_as_float(r[8 * q4 + 6]) * gv[8 * q4 + 6], __uint_as_float(r[8 * q4 + 7]) * gv[8 * q4 + 7]);
-            dst[q4] = v;
+            uint32_t w[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int e = 8 * q4 + 2 * i;
+                w[i] = pack_bf16x2(fmaf(__uint_as_float(r[e]), gv[e], ga[e]),
+                                   fmaf(__uint_as_float(r[e + 1]), gv[e + 1], ga[e + 1]));
+            }
+            dst[q4] = make_uint4(w[0], w[1], w[2], w[3]);
+        }
         }
     }
 }
 
 // ----------------------------------------------------------------- kernel
 
-template <int D>
+template <int D, bool GV>
 __global__ void __launch_bounds__(PfCfg<D>::THREADS, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                       const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmG,
@@ -588,7 +634,8 @@ __global__ void __launch_bounds__(PfCfg<D>::THREADS, 1)
     if (warp == 0) {
         if (lane == 0)
             run_producer<D>(&tmK, &tmV, &tmQ, &tmG, p.qnorm_w, bars, sbase, n_kv, b, g, h, qt, p.G,
-                            p.gate_mode == GATTN_GATE_ELEMENTWISE, abort_flag, p.status);
+                            GV ? gate_per_dim(p.gate_mode) : p.gate_mode == GATTN_GATE_ELEMENTWISE,
+                            GV && gate_layout(p.gate_mode) == GATTN_GATE_HEAD_SHARED ? 0 : h, abort_flag, p.status);
         __syncwarp();
     } else if (warp == 1) {
         if (lane == 0) run_mma<D>(0, bars, sbase, tm, n_kv, abort_flag, p.status);
@@ -601,7 +648,7 @@ __global__ void __launch_bounds__(PfCfg<D>::THREADS, 1)
         }
         __syncwarp();
     } else {
-        run_softmax<D>(p, bars, sbase, tm, warp & 3, lane, qt, b, h, n_kv, abort_flag);
+        run_softmax<D, GV>(p, bars, sbase, tm, warp & 3, lane, qt, b, h, n_kv, abort_flag);
     }
     tc_fence_before();
     __syncthreads();
@@ -615,7 +662,9 @@ template <int D>
 cudaError_t launch_d(const PrefillParams& p, const PrefillMaps& maps, cudaStream_t stream, cudaEvent_t ev_start,
                      cudaEvent_t ev_stop) {
     using C = PfCfg<D>;
-    cudaError_t e = set_smem_once(reinterpret_cast<const void*>(prefill_tc_kernel<D>), C::SMEM_ALLOC);
+    const bool gv = !gate_plain(p.gate_mode) || gate_layout(p.gate_mode) == GATTN_GATE_HEAD_SHARED;
+    auto kernel = gv ? prefill_tc_kernel<D, true> : prefill_tc_kernel<D, false>;
+    cudaError_t e = set_smem_once(reinterpret_cast<const void*>(kernel), C::SMEM_ALLOC);
     if (e != cudaSuccess) return e;
     const long long blocks = (long long)p.n_qtiles * p.B * p.H;
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
@@ -630,7 +679,7 @@ cudaError_t launch_d(const PrefillParams& p, const PrefillMaps& maps, cudaStream
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t err = cudaLaunchKernelEx(&cfg, prefill_tc_kernel<D>, maps.k, maps.v, maps.q, maps.gate, p);
+    cudaError_t err = cudaLaunchKernelEx(&cfg, kernel, maps.k, maps.v, maps.q, maps.gate, p);
     if (ev_stop) cudaEventRecord(ev_stop, stream);
     return err;
 }

@@ -27,7 +27,7 @@ class Workload:
     d: int
     rotary_dim: int
     rope_base: float
-    gate_mode: str  # "elementwise" | "headwise" | "none"
+    gate_mode: str  # "elementwise" | "headwise" | "head_shared" | "none"
     dtype: str  # "bf16" | "fp32"
     seed: int
     S: int = 0  # prefill tokens per sequence
@@ -83,7 +83,8 @@ def _randn(gen, shape, dtype, std=1.0, chunk=1 << 26):
 def make_prefill_inputs(w: Workload, S: Optional[int] = None, B: Optional[int] = None, seed: Optional[int] = None):
     """Tensors (CPU) in the library layout, drawn in the fixed order
     q, k, v, gate, qnorm_w, knorm_w:
-      q [B,S,H,d]  k,v [B,S,G,d]  gate [B,S,H,d] or [B,S,H]  norm weights [d] = 1 + 0.1 N(0,1)."""
+      q [B,S,H,d]  k,v [B,S,G,d]  gate [B,S,H,d], [B,S,H] or [B,S,d] (head-shared)
+      norm weights [d] = 1 + 0.1 N(0,1)."""
     S = w.S if S is None else S
     B = w.B if B is None else B
     g = torch.Generator("cpu").manual_seed(w.seed if seed is None else seed)
@@ -91,7 +92,7 @@ def make_prefill_inputs(w: Workload, S: Optional[int] = None, B: Optional[int] =
     q = _randn(g, (B, S, w.H, w.d), dt)
     k = _randn(g, (B, S, w.G, w.d), dt)
     v = _randn(g, (B, S, w.G, w.d), dt)
-    gshape = (B, S, w.H, w.d) if w.gate_mode == "elementwise" else (B, S, w.H)
+    gshape = {"elementwise": (B, S, w.H, w.d), "head_shared": (B, S, w.d)}.get(w.gate_mode, (B, S, w.H))
     gate = _randn(g, gshape, dt, std=w.gate_std)
     qw = (1.0 + 0.1 * torch.randn(w.d, generator=g)).to(dt)
     kw = (1.0 + 0.1 * torch.randn(w.d, generator=g)).to(dt)
@@ -103,7 +104,7 @@ def make_decode_inputs(w: Workload, B: Optional[int] = None, Lmax: Optional[int]
     """Tensors (CPU) drawn in the order seqlens, kv_cache, q_new, gate, qnorm_w:
       seqlens [B] int32 uniform in the inclusive range; kv_cache [2,B,G,Lmax,d]
       (plane 0 = K, already normed and rotated; plane 1 = V); q_new [B,H,d];
-      gate [B,H,d] or [B,H]; qnorm_w [d]."""
+      gate [B,H,d], [B,H] or [B,d] (head-shared); qnorm_w [d]."""
     B = w.B if B is None else B
     Lmax = w.Lmax if Lmax is None else Lmax
     lo, hi = w.seqlen_range if seqlen_range is None else seqlen_range
@@ -112,7 +113,7 @@ def make_decode_inputs(w: Workload, B: Optional[int] = None, Lmax: Optional[int]
     seqlens = torch.randint(lo, hi + 1, (B,), generator=g, dtype=torch.int64).to(torch.int32)
     cache = _randn(g, (2, B, w.G, Lmax, w.d), dt)
     q = _randn(g, (B, w.H, w.d), dt)
-    gshape = (B, w.H, w.d) if w.gate_mode == "elementwise" else (B, w.H)
+    gshape = {"elementwise": (B, w.H, w.d), "head_shared": (B, w.d)}.get(w.gate_mode, (B, w.H))
     gate = _randn(g, gshape, dt, std=w.gate_std)
     qw = (1.0 + 0.1 * torch.randn(w.d, generator=g)).to(dt)
     return {"seqlens": seqlens, "kv_cache": cache, "q_new": q, "gate": gate, "qnorm_w": qw}

@@ -23,7 +23,11 @@
  *      sigmoid(gate logits) -- one logit per dimension (elementwise) or one per
  *      head (headwise) -- and the heads are concatenated to [tokens, H*d].
  *      ("Gated Attention" deep-dive, section "门放在哪里？"; paper reading notes,
- *      section "从标准注意力走到门控，计算流程有什么变化".)
+ *      section "从标准注意力走到门控，计算流程有什么变化".)  The variants the
+ *      deep-dive compares are epilogue switches of the same kernels (see
+ *      gattn_gate_mode): head-shared logits, NS-sigmoid (section "第二条机制
+ *      线索": 0.5 + 0.5 sigmoid), SiLU (z * sigmoid(z)) and the additive form
+ *      Y + act(z).
  *
  * Conventions for every entry point
  *   - All tensor pointers are DEVICE pointers owned by the caller.  The library
@@ -59,7 +63,30 @@ typedef enum {
     GATTN_ERR_DEVICE = 5        /* gattn_get_device_status found a device-side problem */
 } gattn_status;
 
-typedef enum { GATTN_GATE_NONE = 0, GATTN_GATE_ELEMENTWISE = 1, GATTN_GATE_HEADWISE = 2 } gattn_gate_mode;
+/*
+ * Gate mode = layout | activation | combine (bit fields; the plain layout values
+ * alone mean the default multiplicative sigmoid gate).
+ *   layout (bits 0-3): NONE (no gate; activation and combine must be 0),
+ *     ELEMENTWISE logits [B,S,H,d] (decode [B,H,d]), HEADWISE [B,S,H] ([B,H]),
+ *     HEAD_SHARED [B,S,d] ([B,d]): one vector of logits used by every head.
+ *   activation (bits 4-7): SIGMOID, NS_SIGMOID = 0.5 + 0.5 sigmoid(z),
+ *     SILU = z * sigmoid(z).
+ *   combine (bit 8): multiplicative out = o * act(z) (default) or
+ *     GATTN_GATE_ADDITIVE out = o + act(z).
+ * Any other value is GATTN_ERR_INVALID_ARG.
+ */
+typedef enum {
+    GATTN_GATE_NONE = 0,
+    GATTN_GATE_ELEMENTWISE = 1,
+    GATTN_GATE_HEADWISE = 2,
+    GATTN_GATE_HEAD_SHARED = 3,
+    GATTN_GATE_ACT_SIGMOID = 0x00,
+    GATTN_GATE_ACT_NS_SIGMOID = 0x10,
+    GATTN_GATE_ACT_SILU = 0x20,
+    GATTN_GATE_ADDITIVE = 0x100
+} gattn_gate_mode;
+#define GATTN_GATE_LAYOUT_MASK 0x0Fu
+#define GATTN_GATE_ACT_MASK 0xF0u
 
 typedef enum { GATTN_BF16 = 0, GATTN_FP32 = 1 } gattn_dtype;
 
@@ -89,8 +116,9 @@ size_t gattn_prefill_workspace_size(int B, int S, int H, int G, int d, int dtype
  * k, v     [B,S,G,d] contiguous raw key / value projections.
  * gate     gate logits; elementwise [B,S,H,d] at gate[(b*S+t)*gate_tok_stride +
  *          h*gate_head_stride + e] (defaults H*d, d), headwise [B,S,H] at
- *          gate[(b*S+t)*gate_tok_stride + h*gate_head_stride] (defaults H, 1).
- *          Ignored (may be NULL) for GATTN_GATE_NONE.
+ *          gate[(b*S+t)*gate_tok_stride + h*gate_head_stride] (defaults H, 1),
+ *          head-shared [B,S,d] at gate[(b*S+t)*gate_tok_stride + e] (default d;
+ *          gate_head_stride ignored).  Ignored (may be NULL) for GATTN_GATE_NONE.
  * qnorm_w, knorm_w  [d] RMSNorm weights, shared by all heads.
  * pos      [B,S] int32 RoPE positions, or NULL for positions 0..S-1.  The mask
  *          always uses the token index, not pos.

@@ -65,7 +65,14 @@ def prefill(lib, **kw):
     (dict(rd=130), INVALID),             # rotary_dim > d
     (dict(base=-1.0), INVALID),
     (dict(eps=float("nan")), INVALID),
-    (dict(gm=3), INVALID),
+    (dict(gm=4), INVALID),               # no such gate layout
+    (dict(gm=0x31), INVALID),            # no such gate activation
+    (dict(gm=0x201), INVALID),           # unknown gate bit
+    (dict(gm=0x10), INVALID),            # an activation without a gate
+    (dict(gm=0x100), INVALID),           # additive without a gate
+    (dict(gm=0x103, gate=None), INVALID),  # head-shared additive gate needs its logits
+    (dict(gm=3, gate=P(2)), INVALID),    # head-shared logits are loaded by TMA: 16-byte aligned
+    (dict(gm=0x23, gts=100), INVALID),   # head-shared token stride not a multiple of 8 elements
     (dict(dt=7), INVALID),
     (dict(d=96), UNSUPPORTED),           # no bf16 kernel for head_dim 96
     (dict(d=32, rd=16), UNSUPPORTED),    # bf16 needs d >= 64
@@ -104,6 +111,8 @@ def decode(lib, **kw):
     (dict(B=100000), UNSUPPORTED),
     (dict(rd=40), UNSUPPORTED),
     (dict(kv=P(8)), INVALID),            # cache must be 16-byte aligned for TMA
+    (dict(gm=0x12, gate=None), INVALID),  # headwise NS-sigmoid gate without logits
+    (dict(gm=0x40), INVALID),            # an activation without a gate
 ])
 def test_decode_rejects_bad_arguments(lib, kw, expect):
     assert decode(lib, **kw) == expect

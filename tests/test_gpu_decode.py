@@ -6,7 +6,7 @@ import torch
 import oracle
 from gated_softmax_attention_gqa_gb300 import gattn_decode, gattn_get_device_status, gattn_prefill
 from gated_softmax_attention_gqa_gb300.workloads import WORKLOADS, Workload, make_decode_inputs, make_prefill_inputs
-from tests.parity import assert_close_to_oracle
+from tests.parity import assert_close_to_oracle, gate_scale
 
 pytestmark = pytest.mark.gpu
 
@@ -54,6 +54,31 @@ def test_decode_parity_small(shape):
     torch.cuda.synchronize()
     assert gattn_get_device_status() == 0
     assert_close_to_oracle(out, run_oracle(inp, w), torch.bfloat16, str(shape))
+
+
+@pytest.mark.parametrize("shape", [(3, 8, 2, 256, 64, 1e7, 300, 1, 300), (4, 16, 8, 128, 128, 1e6, 500, 100, 500)],
+                         ids=["d256", "d128"])
+def test_decode_gate_variants(shape):
+    """Head-shared logits, NS-sigmoid, SiLU and the additive gate ("Gated Attention"
+    deep-dive, sections "门放在哪里？" and "第二条机制线索") in the decode combine."""
+    B, H, G, d, rd, base, Lmax, lo, hi = shape
+    for layout in ("elementwise", "headwise", "head_shared"):
+        w = dec_workload(B, H, G, d, rd, base, layout, Lmax, lo, hi, seed=B * 10 + d)
+        inp = make_decode_inputs(w)
+        dev = {k: v.to(DEV) for k, v in inp.items()}
+        lmax = int(inp["seqlens"].max())
+        for act in ("sigmoid", "ns_sigmoid", "silu"):
+            for additive in (False, True):
+                out = gattn_decode(dev["q_new"], dev["kv_cache"], dev["seqlens"], dev["gate"], dev["qnorm_w"],
+                                   rotary_dim=rd, rope_base=base, eps=w.eps, gate_mode=layout, gate_act=act,
+                                   gate_additive=additive)
+                torch.cuda.synchronize()
+                ref = oracle.decode(inp["q_new"], inp["kv_cache"][0][:, :, :lmax], inp["kv_cache"][1][:, :, :lmax],
+                                    inp["seqlens"], inp["gate"], inp["qnorm_w"], rd, base, w.eps,
+                                    oracle.gate_code(layout, act, additive))
+                assert_close_to_oracle(out, ref, torch.bfloat16, f"{shape} {layout} {act} additive={additive}",
+                                      scale=gate_scale(inp["gate"].double().numpy(), layout, act, ref.shape))
+    assert gattn_get_device_status() == 0
 
 
 def test_decode_ignores_cache_entries_past_each_sequence():

@@ -6,7 +6,7 @@ import torch
 import oracle
 from gated_softmax_attention_gqa_gb300 import gattn_get_device_status, gattn_prefill, workloads
 from gated_softmax_attention_gqa_gb300.workloads import WORKLOADS, Workload, make_prefill_inputs
-from tests.parity import assert_close_to_oracle, sample_rows
+from tests.parity import assert_close_to_oracle, gate_scale, sample_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -78,6 +78,40 @@ def test_bf16_parity_small(shape):
     out = run_gpu(inp, w)
     torch.cuda.synchronize()
     assert_close_to_oracle(out, run_oracle(inp, w), torch.bfloat16, str(shape))
+    assert gattn_get_device_status() == 0
+
+
+# gate variants ("Gated Attention" deep-dive, section "门放在哪里？" and the NS-sigmoid
+# control of section "第二条机制线索") through every prefill kernel: the CTA-pair
+# kernel (d 256, H/G even), the one-head kernel at d 128 and at d 256 with H/G odd,
+# and the fp32 kernel
+GATE_VARIANT_SHAPES = [
+    # B, S, H, G, d, rd, base, dtype
+    (1, 200, 4, 2, 256, 64, 1e7, "bf16"),
+    (2, 150, 4, 2, 128, 64, 1e6, "bf16"),
+    (1, 130, 3, 1, 256, 64, 1e7, "bf16"),
+    (1, 70, 4, 2, 64, 16, 1e4, "fp32"),
+]
+
+
+@pytest.mark.parametrize("shape", GATE_VARIANT_SHAPES, ids=[str(s) for s in GATE_VARIANT_SHAPES])
+def test_gate_variants(shape):
+    B, S, H, G, d, rd, base, dt = shape
+    tdt = torch.bfloat16 if dt == "bf16" else torch.float32
+    for layout in ("elementwise", "headwise", "head_shared"):
+        w = small("gates", B, S, H, G, d, rd, base, layout, dtype=dt, seed=S + d, gate_std=2.0)
+        inp = make_prefill_inputs(w)
+        dev = {k: v.to(DEV) for k, v in inp.items()}
+        for act in ("sigmoid", "ns_sigmoid", "silu"):
+            for additive in (False, True):
+                out = gattn_prefill(dev["q"], dev["k"], dev["v"], dev["gate"], dev["qnorm_w"], dev["knorm_w"],
+                                    rotary_dim=rd, rope_base=base, eps=w.eps, gate_mode=layout, gate_act=act,
+                                    gate_additive=additive)
+                torch.cuda.synchronize()
+                ref = oracle.prefill(inp["q"], inp["k"], inp["v"], inp["gate"], inp["qnorm_w"], inp["knorm_w"],
+                                     None, rd, base, w.eps, oracle.gate_code(layout, act, additive))
+                assert_close_to_oracle(out, ref, tdt, f"{shape} {layout} {act} additive={additive}",
+                                      scale=gate_scale(inp["gate"].double().numpy(), layout, act, ref.shape))
     assert gattn_get_device_status() == 0
 
 
