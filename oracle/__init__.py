@@ -59,6 +59,8 @@ def _load():
                                             _dbl, _dbl, _int, _I32, _I32, _int, _D]
         lib.oracle_decode.argtypes = [_D, _D, _D, _I32, _D, _D, _int, _int, _int, _int, _int, _int, _dbl, _dbl,
                                       _int, _D]
+        lib.oracle_decode_append.argtypes = [_D, _D, _D, _D, _D, _I32, _D, _D, _D, _int, _int, _int, _int, _int,
+                                             _int, _dbl, _dbl, _int, _D]
         _lib = lib
     return _lib
 
@@ -177,6 +179,26 @@ def decode(q_new, kcache, vcache, seqlens, gate_logits, qnorm_w, rotary_dim, rop
     _load().oracle_decode(_p(q), _p(kc), _p(vc), sl.ctypes.data_as(_I32), _p(z), _p(qw), B, H, G, d, Lmax,
                           int(rotary_dim), float(rope_base), float(eps), mode, _p(out))
     return out
+
+
+def decode_append(q_new, k_new, v_new, kcache, vcache, seqlens, gate_logits, qnorm_w, knorm_w, rotary_dim,
+                  rope_base, eps, gate_mode):
+    """Decode after appending the new token: k_new, v_new [B,G,d] raw; kcache,
+    vcache [B,G,Lmax,d] (copied, not modified).  Returns (out [B,H*d], kcache,
+    vcache) with the caches as updated."""
+    q, kn, vn, qw, kw = _f64(q_new), _f64(k_new), _f64(v_new), _f64(qnorm_w), _f64(knorm_w)
+    kc, vc = _f64(kcache).copy(), _f64(vcache).copy()
+    B, H, d = q.shape
+    G, Lmax = kc.shape[1], kc.shape[2]
+    mode = _gate_mode(gate_mode)
+    z = _f64(gate_logits) if (mode & 15) != GATE_NONE else np.zeros(1)
+    sl = np.ascontiguousarray(np.asarray(seqlens if not hasattr(seqlens, "cpu") else seqlens.cpu().numpy()),
+                              dtype=np.int32)
+    out = np.empty((B, H * d))
+    _load().oracle_decode_append(_p(q), _p(kn), _p(vn), _p(kc), _p(vc), sl.ctypes.data_as(_I32), _p(z), _p(qw),
+                                 _p(kw), B, H, G, d, Lmax, int(rotary_dim), float(rope_base), float(eps), mode,
+                                 _p(out))
+    return out, kc, vc
 
 
 def threads_used() -> int:

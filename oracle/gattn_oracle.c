@@ -304,3 +304,31 @@ void oracle_decode(const double* q_new, const double* kcache, const double* vcac
         }
     }
 }
+
+/* Decode step that first appends the new token to the cache, then attends
+ * ("Multi-head attention and GQA" chapter, section "拼接各头 → 用 W_O 投影": K and V
+ * are cached per token).  For every sequence b with 1 <= seqlens[b] <= Lmax and
+ * group g, the new token's key k_new[b,g] is normed with knorm_w and rotated at
+ * position seqlens[b]-1 and written to kcache[b,g,seqlens[b]-1]; its raw value
+ * v_new[b,g] goes to vcache[b,g,seqlens[b]-1].  Then oracle_decode.
+ *   k_new, v_new [B,G,d]; kcache, vcache [B,G,Lmax,d] (updated in place). */
+void oracle_decode_append(const double* q_new, const double* k_new, const double* v_new, double* kcache,
+                          double* vcache, const int32_t* seqlens, const double* gate, const double* qnorm_w,
+                          const double* knorm_w, int B, int H, int G, int d, int Lmax, int rd, double base,
+                          double eps, int gate_mode, double* out) {
+    double* tmp = (double*)malloc(sizeof(double) * (size_t)d);
+    for (int b = 0; b < B; ++b) {
+        int L = seqlens[b];
+        if (L < 1 || L > Lmax) continue;
+        for (int g = 0; g < G; ++g) {
+            const double* kn = k_new + ((int64_t)b * G + g) * d;
+            double* kdst = kcache + (((int64_t)b * G + g) * Lmax + (L - 1)) * d;
+            double* vdst = vcache + (((int64_t)b * G + g) * Lmax + (L - 1)) * d;
+            oracle_rmsnorm(kn, knorm_w, 1, d, eps, tmp);
+            rope_row(tmp, (double)(L - 1), d, rd, base, kdst);
+            memcpy(vdst, v_new + ((int64_t)b * G + g) * d, sizeof(double) * (size_t)d);
+        }
+    }
+    free(tmp);
+    oracle_decode(q_new, kcache, vcache, seqlens, gate, qnorm_w, B, H, G, d, Lmax, rd, base, eps, gate_mode, out);
+}

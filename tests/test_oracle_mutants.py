@@ -46,6 +46,12 @@ MUTANTS = {
     "ns_sigmoid_without_offset": ("return 0.5 + 0.5 * s;", "return 0.5 * s;"),
     "silu_is_sigmoid": ("return z * s;", "return s;"),
     "additive_multiplies": ("o[e] = additive ? o[e] + g : o[e] * g;", "o[e] = o[e] * g;"),
+    "append_at_seqlen": ("double* kdst = kcache + (((int64_t)b * G + g) * Lmax + (L - 1)) * d;",
+                         "double* kdst = kcache + (((int64_t)b * G + g) * Lmax + (L > 1 ? L - 2 : 0)) * d;"),
+    "append_normed_with_q_weight": ("oracle_rmsnorm(kn, knorm_w, 1, d, eps, tmp);",
+                                    "oracle_rmsnorm(kn, qnorm_w, 1, d, eps, tmp);"),
+    "append_rotated_at_seqlen": ("rope_row(tmp, (double)(L - 1), d, rd, base, kdst);",
+                                 "rope_row(tmp, (double)L, d, rd, base, kdst);"),
     "head_shared_previous_token": ("case ORACLE_GATE_HEAD_SHARED: return gate + bt * d;",
                                    "case ORACLE_GATE_HEAD_SHARED: return gate + (bt > 0 ? bt - 1 : 0) * d;"),
 }
@@ -91,7 +97,7 @@ def test_pins_catch_mutant(mutant, tmp_path):
     real = oracle._load()
     mutant_lib = ctypes.CDLL(libpath)
     for fname in ("oracle_sigmoid", "oracle_gate_act", "oracle_rmsnorm", "oracle_rope", "oracle_gate", "oracle_sdpa_gate",
-                  "oracle_prefill", "oracle_prefill_rows", "oracle_decode"):
+                  "oracle_prefill", "oracle_prefill_rows", "oracle_decode", "oracle_decode_append"):
         getattr(mutant_lib, fname).argtypes = getattr(real, fname).argtypes
         getattr(mutant_lib, fname).restype = getattr(real, fname).restype
     caught = []

@@ -401,6 +401,36 @@ def test_decode_head_shared_additive_equals_last_prefill_row():
         np.testing.assert_allclose(dec[b], full[b, seqlens[b] - 1], rtol=1e-12, atol=1e-13)
 
 
+def test_decode_append_equals_last_prefill_row():
+    """Appending token L-1 to a cache of L-1 tokens and decoding gives row L-1 of
+    the prefill; the appended K row is that token's normed, rotated key and the
+    appended V row its raw value."""
+    rng = np.random.default_rng(24)
+    B, S, H, G, d, rd, base, eps = 2, 11, 4, 2, 16, 8, 1e6, 1e-6
+    q, k, v, z, qw, kw = _full_inputs(rng, B, S, H, G, d)
+    full = oracle.prefill(q, k, v, z, qw, kw, None, rd, base, eps, "elementwise")
+    Lmax = 14
+    seqlens = [S, S - 4]
+    kc, vc = np.zeros((B, G, Lmax, d)), np.zeros((B, G, Lmax, d))
+    for b in range(B):
+        L = seqlens[b] - 1  # the cache holds the tokens before the new one
+        kr = oracle.rope(oracle.rmsnorm(k[b, :L], kw, eps), np.arange(L)[:, None], rd, base)
+        kc[b, :, :L] = kr.transpose(1, 0, 2)
+        vc[b, :, :L] = v[b, :L].transpose(1, 0, 2)
+    last = [seqlens[b] - 1 for b in range(B)]
+    qn = np.stack([q[b, last[b]] for b in range(B)])
+    kn = np.stack([k[b, last[b]] for b in range(B)])
+    vn = np.stack([v[b, last[b]] for b in range(B)])
+    zn = np.stack([z[b, last[b]] for b in range(B)])
+    out, kc2, vc2 = oracle.decode_append(qn, kn, vn, kc, vc, seqlens, zn, qw, kw, rd, base, eps, "elementwise")
+    for b in range(B):
+        np.testing.assert_allclose(out[b], full[b, last[b]], rtol=1e-12, atol=1e-13)
+        want_k = oracle.rope(oracle.rmsnorm(k[b, last[b]], kw, eps), [last[b]], rd, base)
+        np.testing.assert_allclose(kc2[b, :, last[b]], want_k, rtol=1e-13, atol=1e-14)
+        np.testing.assert_array_equal(vc2[b, :, last[b]], v[b, last[b]])
+        np.testing.assert_array_equal(kc2[b, :, :last[b]], kc[b, :, :last[b]])  # earlier rows untouched
+
+
 def test_kv_cache_byte_accounting(golden):
     from gated_softmax_attention_gqa_gb300 import workloads
 
