@@ -22,7 +22,7 @@ GATE_ACTS = {"sigmoid": 0x00, "ns_sigmoid": 0x10, "silu": 0x20}
 GATE_ADDITIVE = 0x100
 DTYPES = {torch.bfloat16: 0, torch.float32: 1}
 
-__all__ = ["gattn_prefill", "gattn_decode", "gattn_decode_noalloc", "gattn_prefill_workspace_size", "gattn_decode_workspace_size",
+__all__ = ["gattn_prefill", "gattn_decode", "gattn_decode_append", "gattn_decode_noalloc", "gattn_prefill_workspace_size", "gattn_decode_workspace_size",
            "gattn_get_device_status", "gattn_set_profile_events", "gattn_strerror", "GattnError", "GATE_MODES",
            "GATE_ACTS", "GATE_ADDITIVE"]
 
@@ -164,6 +164,40 @@ def gattn_decode(q_new, kv_cache, seqlens, gate, qnorm_w, *, rotary_dim, rope_ba
         Lmax, int(rotary_dim), float(rope_base), float(eps), mode, _ptr(workspace),
         workspace.numel() * workspace.element_size(), _ptr(out), _stream_handle(stream, q_new.device))
     check(st, "gattn_decode")
+    return out
+
+
+def gattn_decode_append(q_new, k_new, v_new, kv_cache, seqlens, gate, qnorm_w, knorm_w, *, rotary_dim, rope_base,
+                        eps=1e-6, gate_mode="elementwise", gate_act="sigmoid", gate_additive=False, out=None,
+                        workspace=None, stream=None):
+    """One decode step that first writes the new token into the cache: k_new,
+    v_new [B,G,d] raw (K is normed with knorm_w and rotated at position
+    seqlens[b]-1); kv_cache [2,B,G,Lmax,d] is updated in place at row
+    seqlens[b]-1; the rest as gattn_decode.  Returns out [B,H*d]."""
+    mode = _mode(gate_mode, gate_act, gate_additive)
+    B, H, d = q_new.shape
+    G, Lmax = kv_cache.shape[2], kv_cache.shape[3]
+    for name, t in (("q_new", q_new), ("k_new", k_new), ("v_new", v_new), ("kv_cache", kv_cache),
+                    ("seqlens", seqlens), ("qnorm_w", qnorm_w), ("knorm_w", knorm_w)):
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    if tuple(k_new.shape) != (B, G, d) or tuple(v_new.shape) != (B, G, d):
+        raise ValueError("k_new and v_new must be [B,G,d]")
+    if mode & 0x0F and not gate.is_contiguous():
+        raise ValueError("gate must be contiguous")
+    if seqlens.dtype != torch.int32:
+        raise ValueError("seqlens must be int32")
+    if out is None:
+        out = torch.empty((B, H * d), dtype=q_new.dtype, device=q_new.device)
+    need = gattn_decode_workspace_size(B, H, G, d, Lmax)
+    if workspace is None or workspace.numel() * workspace.element_size() < need:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q_new.device)
+    st = _lib.load().gattn_decode_append(
+        _ptr(q_new), _ptr(k_new), _ptr(v_new), _ptr(kv_cache), _ptr(seqlens), _ptr(gate if mode & 0x0F else None),
+        _ptr(qnorm_w), _ptr(knorm_w), B, H, G, d, Lmax, int(rotary_dim), float(rope_base), float(eps), mode,
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(out),
+        _stream_handle(stream, q_new.device))
+    check(st, "gattn_decode_append")
     return out
 
 

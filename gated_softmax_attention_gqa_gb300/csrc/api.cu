@@ -334,10 +334,16 @@ size_t gattn_decode_workspace_size(int B, int H, int G, int d, int Lmax) {
     return round_up((size_t)decode_num_slots(n, B, G) * decode_slot_floats(H / G, d) * sizeof(float), 256);
 }
 
-gattn_status gattn_decode(const void* q_new, const void* kv_cache, const int32_t* seqlens, const void* gate,
-                          const void* qnorm_w, int B, int H, int G, int d, int Lmax, int rotary_dim,
-                          double rope_base, float eps, int gate_mode, void* workspace, size_t workspace_bytes,
-                          void* out, void* stream_) {
+}  // extern "C"
+
+namespace {
+
+// The decode step; with append != NULL the new token's K and V are first written
+// into the cache (k_new, v_new, knorm_w of *append).
+gattn_status decode_impl(const void* q_new, const void* kv_cache, const int32_t* seqlens, const void* gate,
+                         const void* qnorm_w, int B, int H, int G, int d, int Lmax, int rotary_dim, double rope_base,
+                         float eps, int gate_mode, void* workspace, size_t workspace_bytes, void* out, void* stream_,
+                         const AppendParams* append) {
     if (!q_new || !kv_cache || !seqlens || !qnorm_w || !out) return GATTN_ERR_INVALID_ARG;
     if (!valid_gate_mode(gate_mode) || (gate_layout(gate_mode) != GATTN_GATE_NONE && !gate))
         return GATTN_ERR_INVALID_ARG;
@@ -384,9 +390,51 @@ gattn_status gattn_decode(const void* q_new, const void* kv_cache, const int32_t
     dp.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)d));
     dp.status = status;
     fill_inv_freq(dp.inv_freq, rotary_dim, rope_base);
+    if (append) {
+        AppendParams ap = *append;
+        ap.cache = const_cast<void*>(kv_cache);
+        ap.seqlens = seqlens;
+        ap.B = B;
+        ap.G = G;
+        ap.d = d;
+        ap.Lmax = Lmax;
+        ap.rd = rotary_dim;
+        ap.eps = eps;
+        std::memcpy(ap.inv_freq, dp.inv_freq, sizeof(ap.inv_freq));
+        if (launch_decode_append(ap, stream) != cudaSuccess) return GATTN_ERR_CUDA;
+    }
     if (launch_decode(dp, tm, stream, g_prof_start, g_prof_stop) != cudaSuccess) return GATTN_ERR_CUDA;
     return GATTN_OK;
 }
+
+}  // namespace
+
+extern "C" {
+
+gattn_status gattn_decode(const void* q_new, const void* kv_cache, const int32_t* seqlens, const void* gate,
+                          const void* qnorm_w, int B, int H, int G, int d, int Lmax, int rotary_dim,
+                          double rope_base, float eps, int gate_mode, void* workspace, size_t workspace_bytes,
+                          void* out, void* stream_) {
+    return decode_impl(q_new, kv_cache, seqlens, gate, qnorm_w, B, H, G, d, Lmax, rotary_dim, rope_base, eps,
+                       gate_mode, workspace, workspace_bytes, out, stream_, nullptr);
+}
+
+gattn_status gattn_decode_append(const void* q_new, const void* k_new, const void* v_new, void* kv_cache,
+                                 const int32_t* seqlens, const void* gate, const void* qnorm_w, const void* knorm_w,
+                                 int B, int H, int G, int d, int Lmax, int rotary_dim, double rope_base, float eps,
+                                 int gate_mode, void* workspace, size_t workspace_bytes, void* out, void* stream) {
+    if (!k_new || !v_new || !knorm_w) return GATTN_ERR_INVALID_ARG;
+    if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(knorm_w, 16)) return GATTN_ERR_INVALID_ARG;
+    AppendParams ap;
+    std::memset(&ap, 0, sizeof(ap));
+    ap.k_new = k_new;
+    ap.v_new = v_new;
+    ap.knorm_w = knorm_w;
+    return decode_impl(q_new, kv_cache, seqlens, gate, qnorm_w, B, H, G, d, Lmax, rotary_dim, rope_base, eps,
+                       gate_mode, workspace, workspace_bytes, out, stream, &ap);
+}
+
+
 
 gattn_status gattn_get_device_status(unsigned int* bits, void* stream_) {
     cudaStream_t stream = static_cast<cudaStream_t>(stream_);

@@ -492,7 +492,86 @@ cudaError_t launch_dec(const DecodeParams& p, const CUtensorMap& tm, cudaStream_
     return cudaLaunchKernelEx(&cfg, decode_combine_kernel<D>, p);
 }
 
+// The new token's K and V into the cache before the step reads it: one row of D
+// elements per (sequence, group), spread over D/8 lanes (16-byte loads and
+// stores); the RMS is a shuffle reduction over the row's lanes, and the rotation
+// partner of a lane's 8 features (e +- rd/2) sits rd/16 lanes away.  Sequences
+// whose length is outside [1, Lmax] are left alone (the step reports them).
+template <int D>
+__global__ void __launch_bounds__(256) decode_append_kernel(const __grid_constant__ AppendParams p) {
+    constexpr int LPR = D / 8, RPW = 32 / LPR;
+    const int lane = threadIdx.x & 31;
+    const int64_t row = ((int64_t)blockIdx.x * 8 + (threadIdx.x >> 5)) * RPW + lane / LPR;  // b * G + g
+    const bool in_range = row < (int64_t)p.B * p.G;
+    const int b = in_range ? (int)(row / p.G) : 0;
+    const int L = in_range ? p.seqlens[b] : 0;
+    const bool live = in_range && L >= 1 && L <= p.Lmax;
+    const int e0 = 8 * (lane % LPR);
+    const int half = p.rd >> 1, dl = half >> 3;
+    const bool first = e0 < half, rot = e0 < p.rd;
+    const int src = lane + (first ? dl : -dl);
+    const int64_t r = in_range ? row : 0;
+    const uint4 kv = *reinterpret_cast<const uint4*>(static_cast<const bf16*>(p.k_new) + r * D + e0);
+    const uint4 vv = *reinterpret_cast<const uint4*>(static_cast<const bf16*>(p.v_new) + r * D + e0);
+    const uint4 wv = *reinterpret_cast<const uint4*>(static_cast<const bf16*>(p.knorm_w) + e0);
+    const uint32_t xs[4] = {kv.x, kv.y, kv.z, kv.w}, ws[4] = {wv.x, wv.y, wv.z, wv.w};
+    float y[8], ss = 0.f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float a = bf16_lo(xs[i]), c = bf16_hi(xs[i]);
+        ss = fmaf(a, a, fmaf(c, c, ss));
+        y[2 * i] = a * bf16_lo(ws[i]);
+        y[2 * i + 1] = c * bf16_hi(ws[i]);
+    }
+#pragma unroll
+    for (int o = LPR / 2; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    const float rinv = rsqrtf(ss / (float)D + p.eps);
+    float q[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) q[i] = __shfl_sync(0xffffffffu, y[i], rot ? src : lane);
+    const float posf = live ? (float)(L - 1) : 0.f;
+    uint32_t o[4];
+#pragma unroll
+    for (int i = 0; i < 8; i += 2) {
+        float s0 = 0.f, c0 = 1.f, s1 = 0.f, c1 = 1.f;
+        if (rot) {
+            const int f = first ? e0 : e0 - half;
+            rope_sincos(posf * p.inv_freq[f + i], &s0, &c0);
+            rope_sincos(posf * p.inv_freq[f + i + 1], &s1, &c1);
+        }
+        // first half: x*cos - partner*sin; second half: x*cos + partner*sin
+        const float v0 = fmaf(y[i], c0, q[i] * (first ? -s0 : s0));
+        const float v1 = fmaf(y[i + 1], c1, q[i + 1] * (first ? -s1 : s1));
+        o[i >> 1] = pack_bf16x2(v0 * rinv, v1 * rinv);
+    }
+    if (live) {
+        const int64_t plane = (int64_t)p.B * p.G * p.Lmax * D;  // K half, then V half of the cache
+        const int64_t off = (r * p.Lmax + (L - 1)) * D + e0;
+        bf16* cache = static_cast<bf16*>(p.cache);
+        *reinterpret_cast<uint4*>(cache + off) = make_uint4(o[0], o[1], o[2], o[3]);
+        *reinterpret_cast<uint4*>(cache + plane + off) = vv;
+    }
+}
+
+template <int D>
+cudaError_t launch_append_d(const AppendParams& p, cudaStream_t stream) {
+    constexpr int RPW = 32 / (D / 8);
+    const int64_t rows = (int64_t)p.B * p.G;
+    const int64_t blocks = (rows + 8 * RPW - 1) / (8 * RPW);
+    decode_append_kernel<D><<<(unsigned)blocks, 256, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
 }  // namespace
+
+cudaError_t launch_decode_append(const AppendParams& p, cudaStream_t stream) {
+    switch (p.d) {
+        case 64: return launch_append_d<64>(p, stream);
+        case 128: return launch_append_d<128>(p, stream);
+        case 256: return launch_append_d<256>(p, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
 
 int decode_slot_floats(int r, int d) { return 2 * r + r * d; }
 int64_t decode_num_slots(int n_ctas, int B, int G) { return ((int64_t)n_ctas + (int64_t)B * G) * NCW; }

@@ -65,6 +65,19 @@ struct DecodeParams {
     float inv_freq[kMaxRotaryHalf];
 };
 
+// Append of the new token to the decode KV cache: k' = rope(rmsnorm(k_new) * w) at
+// position seqlens[b]-1 and the raw v_new, into cache[0/1, b, g, seqlens[b]-1, :].
+struct AppendParams {
+    const void* k_new;  // [B,G,d]
+    const void* v_new;  // [B,G,d]
+    const void* knorm_w;
+    void* cache;        // [2,B,G,Lmax,d]
+    const int32_t* seqlens;
+    int B, G, d, Lmax, rd;
+    float eps;
+    float inv_freq[kMaxRotaryHalf];
+};
+
 // TMA descriptors of the tcgen05 prefill: normed keys (workspace), raw V, raw Q,
 // (elementwise gate only) the gate logits and the output; all bf16, 64-element inner boxes.
 struct PrefillMaps {
@@ -84,6 +97,7 @@ cudaError_t launch_prefill_f32(const PrefillF32Params& p, cudaStream_t stream, c
                                cudaEvent_t ev_stop);
 cudaError_t launch_decode(const DecodeParams& p, const CUtensorMap& tm_kv, cudaStream_t stream,
                           cudaEvent_t ev_start, cudaEvent_t ev_stop);
+cudaError_t launch_decode_append(const AppendParams& p, cudaStream_t stream);
 
 // Prefill tile geometry for the tcgen05 kernel, per head_dim.
 int prefill_block_n(int d);

@@ -159,7 +159,8 @@ size_t gattn_decode_workspace_size(int B, int H, int G, int d, int Lmax);
  * seqlens  [B] int32 device array, cached tokens per sequence INCLUDING the new
  *          one, each in [1, Lmax].  A value outside that range sets
  *          GATTN_DEVICE_BAD_SEQLEN and leaves that sequence's output unwritten.
- * gate     [B,H,d] (elementwise) or [B,H] (headwise) logits; NULL for none.
+ * gate     [B,H,d] (elementwise), [B,H] (headwise) or [B,d] (head-shared)
+ *          logits; NULL for none.
  * qnorm_w  [d].  d in {64,128,256}; H/G <= 8; only GATTN_BF16 (implied).
  * workspace  >= gattn_decode_workspace_size() bytes, 256-byte aligned.
  * out      [B,H*d] bf16.
@@ -168,6 +169,30 @@ gattn_status gattn_decode(const void* q_new, const void* kv_cache, const int32_t
                           const void* qnorm_w, int B, int H, int G, int d, int Lmax, int rotary_dim,
                           double rope_base, float eps, int gate_mode, void* workspace, size_t workspace_bytes,
                           void* out, void* stream);
+
+/*
+ * One decode step that first appends the new token to the cache: for every
+ * sequence b with 1 <= seqlens[b] <= Lmax and KV head g,
+ *   kv_cache[0,b,g,seqlens[b]-1,:] = rope(rmsnorm(k_new[b,g,:]) * knorm_w)
+ *                                    at position seqlens[b]-1,
+ *   kv_cache[1,b,g,seqlens[b]-1,:] = v_new[b,g,:],
+ * then exactly gattn_decode (which reads the appended row).  This is the caller
+ * pass before gattn_decode folded into the call: the new token's QK-RMSNorm and
+ * partial RoPE for K ("Gated attention" handbook chapter, section "Four things
+ * Qwen3.5 adds to the textbook") and the per-token K/V cache ("Multi-head
+ * attention and GQA" chapter, section "拼接各头 → 用 W_O 投影").
+ *
+ * k_new, v_new  [B,G,d] bf16 contiguous raw key / value projections of the new
+ *          token, 16-byte aligned.
+ * kv_cache [2,B,G,Lmax,d] as for gattn_decode, written at row seqlens[b]-1.
+ * knorm_w  [d] bf16, 16-byte aligned.
+ * Everything else, and the errors, as gattn_decode; sequences whose length is
+ * outside [1, Lmax] are neither appended nor decoded (GATTN_DEVICE_BAD_SEQLEN).
+ */
+gattn_status gattn_decode_append(const void* q_new, const void* k_new, const void* v_new, void* kv_cache,
+                                 const int32_t* seqlens, const void* gate, const void* qnorm_w, const void* knorm_w,
+                                 int B, int H, int G, int d, int Lmax, int rotary_dim, double rope_base, float eps,
+                                 int gate_mode, void* workspace, size_t workspace_bytes, void* out, void* stream);
 
 /*
  * One decode step exactly like gattn_decode, for callers that cannot allocate

@@ -118,6 +118,29 @@ def test_decode_rejects_bad_arguments(lib, kw, expect):
     assert decode(lib, **kw) == expect
 
 
+def decode_append(lib, **kw):
+    a = dict(q=P(), kn=P(), vn=P(), kv=P(), sl=P(), gate=P(), qw=P(), kw=P(), B=4, H=8, G=2, d=256, L=1024, rd=64,
+             base=1e7, eps=1e-6, gm=1, ws=P(), wsb=1 << 40, out=P(1 << 20))
+    a.update(kw)
+    return lib.gattn_decode_append(a["q"], a["kn"], a["vn"], a["kv"], a["sl"], a["gate"], a["qw"], a["kw"], a["B"],
+                                   a["H"], a["G"], a["d"], a["L"], a["rd"], a["base"], a["eps"], a["gm"], a["ws"],
+                                   a["wsb"], a["out"], None)
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(kn=None), INVALID),
+    (dict(vn=None), INVALID),
+    (dict(kw=None), INVALID),
+    (dict(kn=P(8)), INVALID),            # k_new rows are read 16 bytes at a time
+    (dict(kw=P(4)), INVALID),
+    (dict(kv=None), INVALID),
+    (dict(d=96), UNSUPPORTED),
+    (dict(gm=0x40), INVALID),
+])
+def test_decode_append_rejects_bad_arguments(lib, kw, expect):
+    assert decode_append(lib, **kw) == expect
+
+
 def test_prefill_workspace_sizes(lib):
     assert lib.gattn_prefill_workspace_size(1, 4096, 8, 2, 256, 0) == 4096 * 2 * 256 * 2
     assert lib.gattn_prefill_workspace_size(1, 64, 2, 1, 32, 1) == (64 * 2 * 32 + 64 * 32) * 4

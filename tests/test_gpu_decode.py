@@ -4,7 +4,7 @@ import pytest
 import torch
 
 import oracle
-from gated_softmax_attention_gqa_gb300 import gattn_decode, gattn_get_device_status, gattn_prefill
+from gated_softmax_attention_gqa_gb300 import gattn_decode, gattn_decode_append, gattn_get_device_status, gattn_prefill
 from gated_softmax_attention_gqa_gb300.workloads import WORKLOADS, Workload, make_decode_inputs, make_prefill_inputs
 from tests.parity import assert_close_to_oracle, gate_scale
 
@@ -79,6 +79,35 @@ def test_decode_gate_variants(shape):
                 assert_close_to_oracle(out, ref, torch.bfloat16, f"{shape} {layout} {act} additive={additive}",
                                       scale=gate_scale(inp["gate"].double().numpy(), layout, act, ref.shape))
     assert gattn_get_device_status() == 0
+
+
+@pytest.mark.parametrize("shape", [(3, 8, 2, 256, 64, 1e7, 300, 1, 300), (5, 16, 8, 128, 128, 1e6, 700, 1, 700),
+                                   (4, 4, 4, 64, 32, 1e4, 129, 63, 129)], ids=["d256", "d128", "d64"])
+def test_decode_append_parity(shape):
+    """The new token's K (normed, rotated at seqlens-1) and V written into the cache
+    inside the call, then the step: output and cache against the oracle."""
+    B, H, G, d, rd, base, Lmax, lo, hi = shape
+    w = dec_workload(B, H, G, d, rd, base, "elementwise", Lmax, lo, hi, seed=B * 7 + d)
+    inp = make_decode_inputs(w)
+    g = torch.Generator().manual_seed(B + d)
+    k_new = torch.randn((B, G, d), generator=g).to(torch.bfloat16)
+    v_new = torch.randn((B, G, d), generator=g).to(torch.bfloat16)
+    knorm_w = (1 + 0.1 * torch.randn((d,), generator=g)).to(torch.bfloat16)
+    dev = {k: v.to(DEV) for k, v in inp.items()}
+    out = gattn_decode_append(dev["q_new"], k_new.to(DEV), v_new.to(DEV), dev["kv_cache"], dev["seqlens"],
+                              dev["gate"], dev["qnorm_w"], knorm_w.to(DEV), rotary_dim=rd, rope_base=base, eps=w.eps)
+    torch.cuda.synchronize()
+    assert gattn_get_device_status() == 0
+    ref, kc, vc = oracle.decode_append(inp["q_new"], k_new, v_new, inp["kv_cache"][0], inp["kv_cache"][1],
+                                       inp["seqlens"], inp["gate"], inp["qnorm_w"], knorm_w, rd, base, w.eps,
+                                       "elementwise")
+    assert_close_to_oracle(out, ref, torch.bfloat16, f"{shape} out")
+    cache = dev["kv_cache"].cpu()
+    for b in range(B):
+        L = int(inp["seqlens"][b])
+        assert_close_to_oracle(cache[0, b, :, L - 1], kc[b, :, L - 1], torch.bfloat16, f"{shape} K row of {b}")
+        assert torch.equal(cache[1, b, :, L - 1], v_new[b]), f"V row of sequence {b}"
+        assert torch.equal(cache[:, b, :, :L - 1], inp["kv_cache"][:, b, :, :L - 1]), f"earlier rows of {b}"
 
 
 def test_decode_ignores_cache_entries_past_each_sequence():
