@@ -22,7 +22,7 @@ GATE_ACTS = {"sigmoid": 0x00, "ns_sigmoid": 0x10, "silu": 0x20}
 GATE_ADDITIVE = 0x100
 DTYPES = {torch.bfloat16: 0, torch.float32: 1}
 
-__all__ = ["gattn_prefill", "gattn_decode", "gattn_decode_append", "gattn_decode_noalloc", "gattn_prefill_workspace_size", "gattn_decode_workspace_size",
+__all__ = ["gattn_prefill", "gattn_decode", "gattn_decode_append", "gattn_decode_paged", "gattn_decode_noalloc", "gattn_prefill_workspace_size", "gattn_decode_workspace_size",
            "gattn_get_device_status", "gattn_set_profile_events", "gattn_strerror", "GattnError", "GATE_MODES",
            "GATE_ACTS", "GATE_ADDITIVE"]
 
@@ -198,6 +198,40 @@ def gattn_decode_append(q_new, k_new, v_new, kv_cache, seqlens, gate, qnorm_w, k
         _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(out),
         _stream_handle(stream, q_new.device))
     check(st, "gattn_decode_append")
+    return out
+
+
+def gattn_decode_paged(q_new, kv_pages, block_table, seqlens, gate, qnorm_w, *, rotary_dim, rope_base, eps=1e-6,
+                       k_new=None, v_new=None, knorm_w=None, gate_mode="elementwise", gate_act="sigmoid",
+                       gate_additive=False, out=None, workspace=None, stream=None):
+    """One decode step against a paged cache: kv_pages [2,num_pages,G,page_size,d]
+    bf16, block_table [B,max_pages] int32 (page of each page_size-token block of
+    each sequence).  With k_new, v_new [B,G,d] and knorm_w the new token is first
+    written into its page.  The rest as gattn_decode.  Returns out [B,H*d]."""
+    mode = _mode(gate_mode, gate_act, gate_additive)
+    B, H, d = q_new.shape
+    num_pages, G, page_size = kv_pages.shape[1], kv_pages.shape[2], kv_pages.shape[3]
+    max_pages = block_table.shape[1]
+    for name, t in (("q_new", q_new), ("kv_pages", kv_pages), ("block_table", block_table), ("seqlens", seqlens),
+                    ("qnorm_w", qnorm_w)) + ((("k_new", k_new), ("v_new", v_new), ("knorm_w", knorm_w))
+                                             if k_new is not None else ()):
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    if block_table.dtype != torch.int32 or seqlens.dtype != torch.int32:
+        raise ValueError("block_table and seqlens must be int32")
+    if mode & 0x0F and not gate.is_contiguous():
+        raise ValueError("gate must be contiguous")
+    if out is None:
+        out = torch.empty((B, H * d), dtype=q_new.dtype, device=q_new.device)
+    need = gattn_decode_workspace_size(B, H, G, d, max_pages * page_size)
+    if workspace is None or workspace.numel() * workspace.element_size() < need:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q_new.device)
+    st = _lib.load().gattn_decode_paged(
+        _ptr(q_new), _ptr(k_new), _ptr(v_new), _ptr(kv_pages), _ptr(block_table), num_pages, page_size, max_pages,
+        _ptr(seqlens), _ptr(gate if mode & 0x0F else None), _ptr(qnorm_w), _ptr(knorm_w), B, H, G, d,
+        int(rotary_dim), float(rope_base), float(eps), mode, _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _ptr(out), _stream_handle(stream, q_new.device))
+    check(st, "gattn_decode_paged")
     return out
 
 

@@ -13,6 +13,7 @@ EXPORTS = (
     "gattn_decode_workspace_size",
     "gattn_decode",
     "gattn_decode_append",
+    "gattn_decode_paged",
     "gattn_decode_noalloc",
     "gattn_get_device_status",
     "gattn_set_profile_events",
@@ -53,6 +54,9 @@ def load():
     lib.gattn_decode_append.restype = _i
     lib.gattn_decode_append.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _d, _f, _i,
                                         _vp, _sz, _vp, _vp]
+    lib.gattn_decode_paged.restype = _i
+    lib.gattn_decode_paged.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _d,
+                                       _f, _i, _vp, _sz, _vp, _vp]
     lib.gattn_decode_noalloc.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _d, _f, _i, _vp, _vp]
     lib.gattn_get_device_status.restype = _i
     lib.gattn_get_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint), _vp]

@@ -338,12 +338,19 @@ size_t gattn_decode_workspace_size(int B, int H, int G, int d, int Lmax) {
 
 namespace {
 
+// A paged cache: [2, num_pages, G, page_size, d] and the [B, max_pages] block table.
+struct PagedCache {
+    const int32_t* block_table;
+    int num_pages, page_size, max_pages;
+};
+
 // The decode step; with append != NULL the new token's K and V are first written
-// into the cache (k_new, v_new, knorm_w of *append).
+// into the cache (k_new, v_new, knorm_w of *append); with paged != NULL the cache
+// is paged (Lmax = max_pages * page_size).
 gattn_status decode_impl(const void* q_new, const void* kv_cache, const int32_t* seqlens, const void* gate,
                          const void* qnorm_w, int B, int H, int G, int d, int Lmax, int rotary_dim, double rope_base,
                          float eps, int gate_mode, void* workspace, size_t workspace_bytes, void* out, void* stream_,
-                         const AppendParams* append) {
+                         const AppendParams* append, const PagedCache* paged) {
     if (!q_new || !kv_cache || !seqlens || !qnorm_w || !out) return GATTN_ERR_INVALID_ARG;
     if (!valid_gate_mode(gate_mode) || (gate_layout(gate_mode) != GATTN_GATE_NONE && !gate))
         return GATTN_ERR_INVALID_ARG;
@@ -353,7 +360,8 @@ gattn_status decode_impl(const void* q_new, const void* kv_cache, const int32_t*
     if (!(eps >= 0.f) || !std::isfinite(eps)) return GATTN_ERR_INVALID_ARG;
     if (!(d == 64 || d == 128 || d == 256) || H / G > 8 || rotary_dim % 16 != 0 || B > decode_max_batch())
         return GATTN_ERR_UNSUPPORTED;
-    if (2 * (int64_t)B * G * Lmax + kDecodeTileKeys > INT32_MAX) return GATTN_ERR_UNSUPPORTED;
+    const int64_t cache_rows = paged ? 2 * (int64_t)paged->num_pages * G * paged->page_size : 2 * (int64_t)B * G * Lmax;
+    if (cache_rows + kDecodeTileKeys > INT32_MAX) return GATTN_ERR_UNSUPPORTED;
     if (!aligned(kv_cache, 16) || !aligned(q_new, 4) || !aligned(qnorm_w, 4) || !aligned(out, 2))
         return GATTN_ERR_INVALID_ARG;
     const int n_ctas = sm_count();
@@ -365,7 +373,7 @@ gattn_status decode_impl(const void* q_new, const void* kv_cache, const int32_t*
     if (!status) return GATTN_ERR_CUDA;
 
     CUtensorMap tm;
-    const uint64_t dims[2] = {(uint64_t)d, 2ull * B * G * Lmax};
+    const uint64_t dims[2] = {(uint64_t)d, (uint64_t)cache_rows};
     const uint64_t str[1] = {(uint64_t)d * 2};
     const uint32_t box[2] = {64, (uint32_t)kDecodeTileKeys};
     if (!encode_bf16_map(&tm, kv_cache, 2, dims, str, box)) return GATTN_ERR_CUDA;
@@ -390,6 +398,12 @@ gattn_status decode_impl(const void* q_new, const void* kv_cache, const int32_t*
     dp.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)d));
     dp.status = status;
     fill_inv_freq(dp.inv_freq, rotary_dim, rope_base);
+    if (paged) {
+        dp.block_table = paged->block_table;
+        dp.num_pages = paged->num_pages;
+        dp.page_size = paged->page_size;
+        dp.max_pages = paged->max_pages;
+    }
     if (append) {
         AppendParams ap = *append;
         ap.cache = const_cast<void*>(kv_cache);
@@ -400,6 +414,11 @@ gattn_status decode_impl(const void* q_new, const void* kv_cache, const int32_t*
         ap.Lmax = Lmax;
         ap.rd = rotary_dim;
         ap.eps = eps;
+        ap.status = status;
+        ap.block_table = dp.block_table;
+        ap.num_pages = dp.num_pages;
+        ap.page_size = dp.page_size;
+        ap.max_pages = dp.max_pages;
         std::memcpy(ap.inv_freq, dp.inv_freq, sizeof(ap.inv_freq));
         if (launch_decode_append(ap, stream) != cudaSuccess) return GATTN_ERR_CUDA;
     }
@@ -416,7 +435,7 @@ gattn_status gattn_decode(const void* q_new, const void* kv_cache, const int32_t
                           double rope_base, float eps, int gate_mode, void* workspace, size_t workspace_bytes,
                           void* out, void* stream_) {
     return decode_impl(q_new, kv_cache, seqlens, gate, qnorm_w, B, H, G, d, Lmax, rotary_dim, rope_base, eps,
-                       gate_mode, workspace, workspace_bytes, out, stream_, nullptr);
+                       gate_mode, workspace, workspace_bytes, out, stream_, nullptr, nullptr);
 }
 
 gattn_status gattn_decode_append(const void* q_new, const void* k_new, const void* v_new, void* kv_cache,
@@ -431,7 +450,29 @@ gattn_status gattn_decode_append(const void* q_new, const void* k_new, const voi
     ap.v_new = v_new;
     ap.knorm_w = knorm_w;
     return decode_impl(q_new, kv_cache, seqlens, gate, qnorm_w, B, H, G, d, Lmax, rotary_dim, rope_base, eps,
-                       gate_mode, workspace, workspace_bytes, out, stream, &ap);
+                       gate_mode, workspace, workspace_bytes, out, stream, &ap, nullptr);
+}
+
+gattn_status gattn_decode_paged(const void* q_new, const void* k_new, const void* v_new, void* kv_pages,
+                                const int32_t* block_table, int num_pages, int page_size, int max_pages,
+                                const int32_t* seqlens, const void* gate, const void* qnorm_w, const void* knorm_w,
+                                int B, int H, int G, int d, int rotary_dim, double rope_base, float eps, int gate_mode,
+                                void* workspace, size_t workspace_bytes, void* out, void* stream) {
+    if (!block_table || num_pages < 1 || max_pages < 1 || page_size < 1) return GATTN_ERR_INVALID_ARG;
+    if (page_size % kDecodeTileKeys != 0) return GATTN_ERR_UNSUPPORTED;  // a key tile never straddles two pages
+    if ((int64_t)max_pages * page_size > INT32_MAX) return GATTN_ERR_INVALID_ARG;
+    PagedCache pc{block_table, num_pages, page_size, max_pages};
+    AppendParams ap;
+    std::memset(&ap, 0, sizeof(ap));
+    if (k_new || v_new) {
+        if (!k_new || !v_new || !knorm_w) return GATTN_ERR_INVALID_ARG;
+        if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(knorm_w, 16)) return GATTN_ERR_INVALID_ARG;
+        ap.k_new = k_new;
+        ap.v_new = v_new;
+        ap.knorm_w = knorm_w;
+    }
+    return decode_impl(q_new, kv_pages, seqlens, gate, qnorm_w, B, H, G, d, max_pages * page_size, rotary_dim,
+                       rope_base, eps, gate_mode, workspace, workspace_bytes, out, stream, k_new ? &ap : nullptr, &pc);
 }
 
 

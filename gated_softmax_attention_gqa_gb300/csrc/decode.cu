@@ -135,7 +135,9 @@ __global__ void __launch_bounds__(DecCfg<D>::THREADS, 1)
         if (lane == 0 && u_begin < u_end) {
             TileWalker wk;
             wk.seek(u_begin, pb, p.B, p.G);
-            const int64_t plane = (int64_t)p.B * p.G * p.Lmax;
+            const bool paged = p.block_table != nullptr;
+            const int64_t plane = paged ? (int64_t)p.num_pages * p.G * p.page_size : (int64_t)p.B * p.G * p.Lmax;
+            int cached_b = -1, cached_slot = -1, page = 0;  // the last block table entry read
             int n = 0;
             for (int64_t u = u_begin; u < u_end; ++u, ++n, wk.next(pb, p.B, p.G)) {
                 const int st = n % C::NS;
@@ -143,7 +145,22 @@ __global__ void __launch_bounds__(DecCfg<D>::THREADS, 1)
                     !mbar_wait(bar_empty + 8 * st, ((uint32_t)(n / C::NS) & 1u) ^ 1u, abort_flag, p.status))
                     break;
                 mbar_arrive_expect_tx(bar_full + 8 * st, C::STAGE_BYTES);
-                const int rowk = (int)(((int64_t)wk.b * p.G + wk.g) * p.Lmax + (int64_t)wk.i * BT);
+                int rowk;
+                if (paged) {
+                    const int key0 = wk.i * BT, slot = key0 / p.page_size;
+                    if (wk.b != cached_b || slot != cached_slot) {
+                        page = p.block_table[(int64_t)wk.b * p.max_pages + slot];
+                        if (page < 0 || page >= p.num_pages) {
+                            atomicOr(p.status, GATTN_DEVICE_BAD_PAGE);
+                            page = 0;
+                        }
+                        cached_b = wk.b;
+                        cached_slot = slot;
+                    }
+                    rowk = (int)(((int64_t)page * p.G + wk.g) * p.page_size + key0 % p.page_size);
+                } else {
+                    rowk = (int)(((int64_t)wk.b * p.G + wk.g) * p.Lmax + (int64_t)wk.i * BT);
+                }
                 const int rowv = (int)(rowk + plane);
                 const uint32_t dst = sbase + st * C::STAGE_BYTES;
 #pragma unroll
@@ -545,8 +562,21 @@ __global__ void __launch_bounds__(256) decode_append_kernel(const __grid_constan
         o[i >> 1] = pack_bf16x2(v0 * rinv, v1 * rinv);
     }
     if (live) {
-        const int64_t plane = (int64_t)p.B * p.G * p.Lmax * D;  // K half, then V half of the cache
-        const int64_t off = (r * p.Lmax + (L - 1)) * D + e0;
+        // the row of token L-1: contiguous [2,B,G,Lmax,d], or paged [2,pages,G,page_size,d]
+        int64_t plane, off;
+        if (p.block_table) {
+            const int g = (int)(r % p.G);
+            const int page = p.block_table[(int64_t)b * p.max_pages + (L - 1) / p.page_size];
+            if (page < 0 || page >= p.num_pages) {
+                if (lane % LPR == 0) atomicOr(p.status, GATTN_DEVICE_BAD_PAGE);
+                return;
+            }
+            plane = (int64_t)p.num_pages * p.G * p.page_size * D;
+            off = (((int64_t)page * p.G + g) * p.page_size + (L - 1) % p.page_size) * D + e0;
+        } else {
+            plane = (int64_t)p.B * p.G * p.Lmax * D;  // K half, then V half of the cache
+            off = (r * p.Lmax + (L - 1)) * D + e0;
+        }
         bf16* cache = static_cast<bf16*>(p.cache);
         *reinterpret_cast<uint4*>(cache + off) = make_uint4(o[0], o[1], o[2], o[3]);
         *reinterpret_cast<uint4*>(cache + plane + off) = vv;

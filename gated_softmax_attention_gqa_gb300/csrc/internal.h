@@ -62,6 +62,10 @@ struct DecodeParams {
     int B, H, G, d, Lmax, rd, gate_mode, n_ctas;
     float eps, scale_log2;
     unsigned int* status;
+    // paged cache (block_table != NULL): [2, num_pages, G, page_size, d]; the keys
+    // [p*page_size, (p+1)*page_size) of sequence b live in page block_table[b*max_pages + p]
+    const int32_t* block_table;
+    int max_pages, page_size, num_pages;
     float inv_freq[kMaxRotaryHalf];
 };
 
@@ -75,6 +79,9 @@ struct AppendParams {
     const int32_t* seqlens;
     int B, G, d, Lmax, rd;
     float eps;
+    unsigned int* status;
+    const int32_t* block_table;  // paged cache, as in DecodeParams (NULL: contiguous)
+    int max_pages, page_size, num_pages;
     float inv_freq[kMaxRotaryHalf];
 };
 

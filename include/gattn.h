@@ -93,6 +93,8 @@ typedef enum { GATTN_BF16 = 0, GATTN_FP32 = 1 } gattn_dtype;
 /* Device status bits (gattn_get_device_status). */
 #define GATTN_DEVICE_BAD_SEQLEN 0x1u  /* a decode seqlens[b] was outside [1, Lmax]; that sequence was skipped */
 #define GATTN_DEVICE_TIMEOUT 0x2u     /* a bounded wait inside a kernel ran out; its output is not valid */
+#define GATTN_DEVICE_BAD_PAGE 0x4u    /* a paged-cache block table entry was outside [0, num_pages); page 0 was read
+                                         instead and nothing was appended there */
 
 /* Human-readable name of a status code.  Never NULL. */
 const char* gattn_strerror(gattn_status status);
@@ -193,6 +195,33 @@ gattn_status gattn_decode_append(const void* q_new, const void* k_new, const voi
                                  const int32_t* seqlens, const void* gate, const void* qnorm_w, const void* knorm_w,
                                  int B, int H, int G, int d, int Lmax, int rotary_dim, double rope_base, float eps,
                                  int gate_mode, void* workspace, size_t workspace_bytes, void* out, void* stream);
+
+/*
+ * One decode step against a PAGED KV cache, optionally appending the new token
+ * first.  The cache is a pool of pages, each holding page_size consecutive tokens
+ * of one sequence for every KV head:
+ *   kv_pages    [2, num_pages, G, page_size, d] bf16 contiguous, 16-byte aligned
+ *               (plane 0 K normed and rotated, plane 1 raw V, as in gattn_decode);
+ *   block_table [B, max_pages] int32 device array: the tokens
+ *               [p*page_size, (p+1)*page_size) of sequence b are in page
+ *               block_table[b*max_pages + p].  Only the entries that cover tokens
+ *               0..seqlens[b]-1 are read.
+ * page_size must be a multiple of 64 (a key tile of the kernel never straddles
+ * two pages; others: GATTN_ERR_UNSUPPORTED); sequences hold at most
+ * max_pages*page_size tokens (seqlens[b] in [1, max_pages*page_size]).  An entry
+ * outside [0, num_pages) sets GATTN_DEVICE_BAD_PAGE (that step's output is not
+ * valid; nothing is read or written outside the pool).
+ * k_new, v_new, knorm_w: NULL for no append, else as gattn_decode_append (the new
+ * token goes to row (seqlens[b]-1) % page_size of page
+ * block_table[b*max_pages + (seqlens[b]-1)/page_size]).
+ * Everything else as gattn_decode, with Lmax = max_pages * page_size for
+ * gattn_decode_workspace_size.
+ */
+gattn_status gattn_decode_paged(const void* q_new, const void* k_new, const void* v_new, void* kv_pages,
+                                const int32_t* block_table, int num_pages, int page_size, int max_pages,
+                                const int32_t* seqlens, const void* gate, const void* qnorm_w, const void* knorm_w,
+                                int B, int H, int G, int d, int rotary_dim, double rope_base, float eps, int gate_mode,
+                                void* workspace, size_t workspace_bytes, void* out, void* stream);
 
 /*
  * One decode step exactly like gattn_decode, for callers that cannot allocate

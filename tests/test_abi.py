@@ -141,6 +141,30 @@ def test_decode_append_rejects_bad_arguments(lib, kw, expect):
     assert decode_append(lib, **kw) == expect
 
 
+def decode_paged(lib, **kw):
+    a = dict(q=P(), kn=None, vn=None, kv=P(), bt=P(), np_=64, ps=256, mp=16, sl=P(), gate=P(), qw=P(), kw=None,
+             B=4, H=8, G=2, d=256, rd=64, base=1e7, eps=1e-6, gm=1, ws=P(), wsb=1 << 40, out=P(1 << 20))
+    a.update(kw)
+    return lib.gattn_decode_paged(a["q"], a["kn"], a["vn"], a["kv"], a["bt"], a["np_"], a["ps"], a["mp"], a["sl"],
+                                  a["gate"], a["qw"], a["kw"], a["B"], a["H"], a["G"], a["d"], a["rd"], a["base"],
+                                  a["eps"], a["gm"], a["ws"], a["wsb"], a["out"], None)
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(bt=None), INVALID),
+    (dict(np_=0), INVALID),
+    (dict(mp=0), INVALID),
+    (dict(ps=96), UNSUPPORTED),          # a key tile would straddle two pages
+    (dict(kn=P()), INVALID),             # an append needs v_new and knorm_w too
+    (dict(kn=P(), vn=P(), kw=P(8)), INVALID),
+    (dict(kv=P(8)), INVALID),
+    (dict(d=96), UNSUPPORTED),
+    (dict(gm=0x40), INVALID),
+])
+def test_decode_paged_rejects_bad_arguments(lib, kw, expect):
+    assert decode_paged(lib, **kw) == expect
+
+
 def test_prefill_workspace_sizes(lib):
     assert lib.gattn_prefill_workspace_size(1, 4096, 8, 2, 256, 0) == 4096 * 2 * 256 * 2
     assert lib.gattn_prefill_workspace_size(1, 64, 2, 1, 32, 1) == (64 * 2 * 32 + 64 * 32) * 4

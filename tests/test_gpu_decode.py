@@ -4,7 +4,8 @@ import pytest
 import torch
 
 import oracle
-from gated_softmax_attention_gqa_gb300 import gattn_decode, gattn_decode_append, gattn_get_device_status, gattn_prefill
+from gated_softmax_attention_gqa_gb300 import (gattn_decode, gattn_decode_append, gattn_decode_paged,
+                                              gattn_get_device_status, gattn_prefill)
 from gated_softmax_attention_gqa_gb300.workloads import WORKLOADS, Workload, make_decode_inputs, make_prefill_inputs
 from tests.parity import assert_close_to_oracle, gate_scale
 
@@ -108,6 +109,51 @@ def test_decode_append_parity(shape):
         assert_close_to_oracle(cache[0, b, :, L - 1], kc[b, :, L - 1], torch.bfloat16, f"{shape} K row of {b}")
         assert torch.equal(cache[1, b, :, L - 1], v_new[b]), f"V row of sequence {b}"
         assert torch.equal(cache[:, b, :, :L - 1], inp["kv_cache"][:, b, :, :L - 1]), f"earlier rows of {b}"
+
+
+@pytest.mark.parametrize("shape", [(3, 8, 2, 256, 64, 1e7, 128, 4), (5, 16, 8, 128, 128, 1e6, 64, 12),
+                                   (2, 4, 1, 64, 32, 1e4, 192, 3)], ids=["d256p128", "d128p64", "d64p192"])
+def test_decode_paged_parity(shape):
+    """The cache scattered over a shuffled page pool (with spare pages holding
+    NaN): the paged step must match the oracle on the contiguous cache, with and
+    without appending the new token."""
+    B, H, G, d, rd, base, ps, mp = shape
+    Lmax = ps * mp
+    w = dec_workload(B, H, G, d, rd, base, "elementwise", Lmax, 1, Lmax, seed=B * 13 + d)
+    inp = make_decode_inputs(w)
+    g = torch.Generator().manual_seed(d + ps)
+    num_pages = B * mp + 3
+    table = torch.randperm(num_pages, generator=g)[:B * mp].view(B, mp).to(torch.int32)
+    pool = torch.full((2, num_pages, G, ps, d), float("nan"), dtype=torch.bfloat16)
+    for b in range(B):
+        for j in range(mp):
+            pool[:, table[b, j]] = inp["kv_cache"][:, b, :, j * ps:(j + 1) * ps]
+    dev = {k: v.to(DEV) for k, v in inp.items()}
+    pool_d, table_d = pool.to(DEV), table.to(DEV)
+    out = gattn_decode_paged(dev["q_new"], pool_d, table_d, dev["seqlens"], dev["gate"], dev["qnorm_w"],
+                             rotary_dim=rd, rope_base=base, eps=w.eps)
+    torch.cuda.synchronize()
+    assert gattn_get_device_status() == 0
+    assert_close_to_oracle(out, run_oracle(inp, w), torch.bfloat16, f"{shape} paged")
+    # with the new token appended into its page
+    k_new = torch.randn((B, G, d), generator=g).to(torch.bfloat16)
+    v_new = torch.randn((B, G, d), generator=g).to(torch.bfloat16)
+    knorm_w = (1 + 0.1 * torch.randn((d,), generator=g)).to(torch.bfloat16)
+    out = gattn_decode_paged(dev["q_new"], pool_d, table_d, dev["seqlens"], dev["gate"], dev["qnorm_w"],
+                             rotary_dim=rd, rope_base=base, eps=w.eps, k_new=k_new.to(DEV), v_new=v_new.to(DEV),
+                             knorm_w=knorm_w.to(DEV))
+    torch.cuda.synchronize()
+    assert gattn_get_device_status() == 0
+    ref, kc, _ = oracle.decode_append(inp["q_new"], k_new, v_new, inp["kv_cache"][0], inp["kv_cache"][1],
+                                      inp["seqlens"], inp["gate"], inp["qnorm_w"], knorm_w, rd, base, w.eps,
+                                      "elementwise")
+    assert_close_to_oracle(out, ref, torch.bfloat16, f"{shape} paged + append")
+    pool_after = pool_d.cpu()
+    for b in range(B):
+        L = int(inp["seqlens"][b])
+        page, row = int(table[b, (L - 1) // ps]), (L - 1) % ps
+        assert_close_to_oracle(pool_after[0, page, :, row], kc[b, :, L - 1], torch.bfloat16, f"K row of {b}")
+        assert torch.equal(pool_after[1, page, :, row], v_new[b])
 
 
 def test_decode_ignores_cache_entries_past_each_sequence():
