@@ -148,6 +148,28 @@ def prefill(q, k, v, gate_logits, qnorm_w, knorm_w, pos, rotary_dim, rope_base, 
     return out
 
 
+def prefill_varlen(q, k, v, gate_logits, qnorm_w, knorm_w, pos, cu_seqlens, rotary_dim, rope_base, eps,
+                   gate_mode):
+    """Packed variable-length prefill: sequences i = [cu_seqlens[i], cu_seqlens[i+1])
+    of q [T,H,d], k,v [T,G,d], gate [T,H,d] / [T,H] / [T,d]; pos [T] or None
+    (positions then restart at 0 in every sequence).  Each sequence is a batch
+    of one, attending only to its own keys.  Returns out [T, H*d]."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    T, H, d = q.shape
+    cu = [int(x) for x in np.asarray(cu_seqlens if not hasattr(cu_seqlens, "cpu") else cu_seqlens.cpu())]
+    mode = _gate_mode(gate_mode)
+    z = _f64(gate_logits) if (mode & 15) != GATE_NONE else None
+    p = _f64(pos)
+    out = np.zeros((T, H * d))
+    for i in range(len(cu) - 1):
+        s, e = cu[i], cu[i + 1]
+        if e <= s:
+            continue
+        out[s:e] = prefill(q[None, s:e], k[None, s:e], v[None, s:e], None if z is None else z[None, s:e], qnorm_w,
+                           knorm_w, None if p is None else p[None, s:e], rotary_dim, rope_base, eps, mode)[0]
+    return out
+
+
 def prefill_rows(q, k, v, gate_logits, qnorm_w, knorm_w, pos, rotary_dim, rope_base, eps, gate_mode, row_b,
                  row_t):
     """Prefill output for the selected tokens (row_b[i], row_t[i]) only: [n, H*d]."""

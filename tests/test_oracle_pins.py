@@ -431,6 +431,41 @@ def test_decode_append_equals_last_prefill_row():
         np.testing.assert_array_equal(kc2[b, :, :last[b]], kc[b, :, :last[b]])  # earlier rows untouched
 
 
+def test_varlen_sequences_are_independent_batches():
+    """Packed sequences: each one equals a batch of one on its own (positions
+    restarting at 0, keys of its own only); equal lengths equal the batched
+    prefill; changing a neighbour changes nothing."""
+    rng = np.random.default_rng(25)
+    H, G, d, rd, base, eps = 4, 2, 16, 8, 1e6, 1e-6
+    lens = [5, 1, 0, 9, 3]
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    T = int(cu[-1])
+    q, k, v, z, qw, kw = _full_inputs(rng, 1, T, H, G, d)
+    q, k, v, z = q[0], k[0], v[0], z[0]
+    out = oracle.prefill_varlen(q, k, v, z, qw, kw, None, cu, rd, base, eps, "elementwise")
+    for i, n in enumerate(lens):
+        s = int(cu[i])
+        if n == 0:
+            continue
+        alone = oracle.prefill(q[None, s:s + n], k[None, s:s + n], v[None, s:s + n], z[None, s:s + n], qw, kw, None,
+                               rd, base, eps, "elementwise")[0]
+        np.testing.assert_array_equal(out[s:s + n], alone)
+    # a perturbed neighbour leaves sequence 3 as it was
+    k2 = k.copy()
+    k2[:int(cu[3])] += 1.0
+    k2[int(cu[4]):] -= 1.0
+    out2 = oracle.prefill_varlen(q, k2, v, z, qw, kw, None, cu, rd, base, eps, "elementwise")
+    np.testing.assert_array_equal(out2[int(cu[3]):int(cu[4])], out[int(cu[3]):int(cu[4])])
+    # equal lengths: the batched prefill
+    B, S = 3, 6
+    qb, kb, vb, zb, _, _ = _full_inputs(rng, B, S, H, G, d)
+    batched = oracle.prefill(qb, kb, vb, zb, qw, kw, None, rd, base, eps, "elementwise").reshape(B * S, H * d)
+    packed = oracle.prefill_varlen(qb.reshape(B * S, H, d), kb.reshape(B * S, G, d), vb.reshape(B * S, G, d),
+                                   zb.reshape(B * S, H, d), qw, kw, None, np.arange(0, B * S + 1, S), rd, base, eps,
+                                   "elementwise")
+    np.testing.assert_array_equal(packed, batched)
+
+
 def test_kv_cache_byte_accounting(golden):
     from gated_softmax_attention_gqa_gb300 import workloads
 
