@@ -22,7 +22,7 @@ GATE_ACTS = {"sigmoid": 0x00, "ns_sigmoid": 0x10, "silu": 0x20}
 GATE_ADDITIVE = 0x100
 DTYPES = {torch.bfloat16: 0, torch.float32: 1}
 
-__all__ = ["gattn_prefill", "gattn_decode", "gattn_decode_append", "gattn_decode_paged", "gattn_decode_noalloc", "gattn_prefill_workspace_size", "gattn_decode_workspace_size",
+__all__ = ["gattn_prefill", "gattn_prefill_varlen", "gattn_decode", "gattn_decode_append", "gattn_decode_paged", "gattn_decode_noalloc", "gattn_prefill_workspace_size", "gattn_decode_workspace_size",
            "gattn_get_device_status", "gattn_set_profile_events", "gattn_strerror", "GattnError", "GATE_MODES",
            "GATE_ACTS", "GATE_ADDITIVE"]
 
@@ -134,6 +134,49 @@ def gattn_prefill(q, k, v, gate, qnorm_w, knorm_w, pos=None, *, rotary_dim, rope
         int(rotary_dim), float(rope_base), float(eps), mode, qts, qhs, gts, ghs, dt, _ptr(workspace),
         workspace.numel() * workspace.element_size(), _ptr(out), _stream_handle(stream, q.device))
     check(st, "gattn_prefill")
+    return out
+
+
+def gattn_prefill_varlen(q, k, v, gate, qnorm_w, knorm_w, cu_seqlens, pos=None, *, rotary_dim, rope_base,
+                         eps=1e-6, gate_mode="elementwise", gate_act="sigmoid", gate_additive=False, out=None,
+                         workspace=None, stream=None):
+    """Causal gated GQA attention over packed variable-length sequences: sequence i
+    is tokens [cu_seqlens[i], cu_seqlens[i+1]) of q [T,H,d] (last dimension
+    contiguous), k, v [T,G,d] contiguous and gate [T,H,d] / [T,H] / [T,d]; it sees
+    only its own keys and its positions restart at 0 unless pos [T] int32 is given.
+    cu_seqlens: host int32 sequence (list, numpy array or CPU tensor).  Returns
+    out [T,H*d]."""
+    mode = _mode(gate_mode, gate_act, gate_additive)
+    T, H, d = q.shape
+    G = k.shape[1]
+    cu = torch.as_tensor(cu_seqlens, dtype=torch.int32, device="cpu").contiguous()
+    nseq = cu.numel() - 1
+    if nseq < 1 or int(cu[-1]) != T:
+        raise ValueError("cu_seqlens must have nseq+1 entries ending at T")
+    if q.stride(-1) != 1:
+        raise ValueError("q: the last dimension must be contiguous")
+    if not (k.is_contiguous() and v.is_contiguous()):
+        raise ValueError("k and v must be contiguous [T,G,d]")
+    layout = mode & 0x0F
+    if layout == 0:
+        gate, gts, ghs = None, 0, 0
+    elif layout == GATE_MODES["head_shared"]:
+        gts, ghs = gate.stride(0), 0
+    else:
+        gts, ghs = gate.stride(0), gate.stride(1)
+    if pos is not None and (pos.dtype != torch.int32 or not pos.is_contiguous()):
+        raise ValueError("pos must be a contiguous int32 [T] tensor")
+    if out is None:
+        out = torch.empty((T, H * d), dtype=q.dtype, device=q.device)
+    dt = DTYPES[q.dtype]
+    need = _lib.load().gattn_prefill_varlen_workspace_size(T, nseq, H, G, d, dt)
+    if workspace is None or workspace.numel() * workspace.element_size() < need:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    st = _lib.load().gattn_prefill_varlen(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(gate), _ptr(qnorm_w), _ptr(knorm_w), _ptr(pos), ctypes.c_void_p(cu.data_ptr()),
+        nseq, H, G, d, int(rotary_dim), float(rope_base), float(eps), mode, q.stride(0), q.stride(1), gts, ghs, dt,
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(out), _stream_handle(stream, q.device))
+    check(st, "gattn_prefill_varlen")
     return out
 
 

@@ -10,6 +10,8 @@ EXPORTS = (
     "gattn_strerror",
     "gattn_prefill_workspace_size",
     "gattn_prefill",
+    "gattn_prefill_varlen_workspace_size",
+    "gattn_prefill_varlen",
     "gattn_decode_workspace_size",
     "gattn_decode",
     "gattn_decode_append",
@@ -47,6 +49,11 @@ def load():
     lib.gattn_prefill.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _d, _f, _i, _i64, _i64,
                                   _i64, _i64, _i, _vp, _sz, _vp, _vp]
     lib.gattn_decode_workspace_size.restype = _sz
+    lib.gattn_prefill_varlen_workspace_size.restype = _sz
+    lib.gattn_prefill_varlen_workspace_size.argtypes = [_i, _i, _i, _i, _i, _i]
+    lib.gattn_prefill_varlen.restype = _i
+    lib.gattn_prefill_varlen.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _d, _f, _i, _i64,
+                                         _i64, _i64, _i64, _i, _vp, _sz, _vp, _vp]
     lib.gattn_decode_workspace_size.argtypes = [_i, _i, _i, _i, _i]
     lib.gattn_decode.restype = _i
     lib.gattn_decode.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _d, _f, _i, _vp, _sz, _vp, _vp]

@@ -2,7 +2,9 @@
 // tensor maps and kernel launches.  See include/gattn.h for the contract.
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <cmath>
+#include <vector>
 #include <cstdint>
 #include <cstring>
 #include <mutex>
@@ -147,34 +149,26 @@ size_t prefill_ws(int B, int S, int H, int G, int d, int dtype) {
 
 }  // namespace
 
-extern "C" {
+// Packed sequences: host copy of the cumulative sequence lengths.
+struct Varlen {
+    const int32_t* cu;  // [nseq + 1]
+    int nseq;
+};
 
-const char* gattn_strerror(gattn_status s) {
-    switch (s) {
-        case GATTN_OK: return "GATTN_OK";
-        case GATTN_ERR_INVALID_ARG: return "GATTN_ERR_INVALID_ARG: invalid argument";
-        case GATTN_ERR_UNSUPPORTED: return "GATTN_ERR_UNSUPPORTED: no kernel for this configuration";
-        case GATTN_ERR_CUDA: return "GATTN_ERR_CUDA: a CUDA call or kernel launch failed";
-        case GATTN_ERR_WORKSPACE: return "GATTN_ERR_WORKSPACE: workspace missing, misaligned or too small";
-        case GATTN_ERR_DEVICE: return "GATTN_ERR_DEVICE: a kernel reported a device-side problem";
-    }
-    return "unknown gattn_status";
+// At most ceil(T/128) + nseq query tiles (each sequence adds at most one partial tile).
+size_t varlen_max_tiles(int T, int nseq) { return (size_t)(T + 127) / 128 + (size_t)nseq; }
+
+// Workspace after the K' (and q') part: the tile table, positions, sequence starts.
+size_t varlen_ws(int T, int nseq) {
+    return round_up(varlen_max_tiles(T, nseq) * 16, 256) + 2 * round_up((size_t)T * 4, 256);
 }
 
-void gattn_set_profile_events(void* start, void* stop) {
-    g_prof_start = static_cast<cudaEvent_t>(start);
-    g_prof_stop = static_cast<cudaEvent_t>(stop);
-}
-
-size_t gattn_prefill_workspace_size(int B, int S, int H, int G, int d, int dtype) {
-    return prefill_ws(B, S, H, G, d, dtype);
-}
-
-gattn_status gattn_prefill(const void* q, const void* k, const void* v, const void* gate, const void* qnorm_w,
+gattn_status prefill_impl(const void* q, const void* k, const void* v, const void* gate, const void* qnorm_w,
                            const void* knorm_w, const int32_t* pos, int B, int S, int H, int G, int d,
                            int rotary_dim, double rope_base, float eps, int gate_mode, int64_t q_tok_stride,
                            int64_t q_head_stride, int64_t gate_tok_stride, int64_t gate_head_stride, int dtype,
-                           void* workspace, size_t workspace_bytes, void* out, void* stream_) {
+                           void* workspace, size_t workspace_bytes, void* out, void* stream_,
+                          const Varlen* vl) {
     // ---- arguments
     if (!q || !k || !v || !qnorm_w || !knorm_w || !out) return GATTN_ERR_INVALID_ARG;
     if (!valid_gate_mode(gate_mode) || (gate_layout(gate_mode) != GATTN_GATE_NONE && !gate))
@@ -206,12 +200,40 @@ gattn_status gattn_prefill(const void* q, const void* k, const void* v, const vo
     if (gate_per_dim(gate_mode) && (!aligned(gate, 16) || gate_tok_stride % vec || gate_head_stride % vec))
         return GATTN_ERR_INVALID_ARG;
     if (bf && (!aligned(qnorm_w, 16) || !aligned(knorm_w, 16))) return GATTN_ERR_INVALID_ARG;
-    const size_t need = prefill_ws(B, S, H, G, d, dtype);
+    const size_t base_ws = prefill_ws(B, S, H, G, d, dtype);
+    const size_t need = base_ws + (vl ? varlen_ws(S, vl->nseq) : 0);
     if (!workspace || !aligned(workspace, 256) || workspace_bytes < need) return GATTN_ERR_WORKSPACE;
 
     cudaStream_t stream = static_cast<cudaStream_t>(stream_);
     unsigned int* status = status_ptr();
     if (!status) return GATTN_ERR_CUDA;
+
+    // ---- packed sequences: the query-tile table (heaviest first) into the workspace,
+    // then every token's position within its sequence (unless pos is given) and its
+    // sequence's first token
+    const int4* vtiles = nullptr;
+    int n_vtiles = 0;
+    int32_t* vstart = nullptr;
+    if (vl) {
+        std::vector<int4> tiles;
+        for (int i = 0; i < vl->nseq; ++i) {
+            const int len = vl->cu[i + 1] - vl->cu[i];
+            for (int qt = 0; qt * 128 < len; ++qt) tiles.push_back(make_int4(vl->cu[i], len, qt, i));
+        }
+        std::stable_sort(tiles.begin(), tiles.end(), [](const int4& x, const int4& y) { return x.z > y.z; });
+        char* extra = static_cast<char*>(workspace) + base_ws;
+        int4* dtiles = reinterpret_cast<int4*>(extra);
+        int32_t* vpos = reinterpret_cast<int32_t*>(extra + round_up(varlen_max_tiles(S, vl->nseq) * 16, 256));
+        vstart = vpos + round_up((size_t)S * 4, 256) / 4;
+        n_vtiles = (int)tiles.size();
+        if (n_vtiles > 0 &&
+            cudaMemcpyAsync(dtiles, tiles.data(), tiles.size() * sizeof(int4), cudaMemcpyHostToDevice, stream) !=
+                cudaSuccess)
+            return GATTN_ERR_CUDA;
+        if (launch_varlen_positions(dtiles, n_vtiles, vpos, vstart, stream) != cudaSuccess) return GATTN_ERR_CUDA;
+        vtiles = dtiles;
+        if (!pos) pos = vpos;
+    }
 
     // ---- K' = rope(rmsnorm(k)) into the workspace, [B,G,S,d]
     ProloguePlan kp;
@@ -287,6 +309,8 @@ gattn_status gattn_prefill(const void* q, const void* k, const void* v, const vo
         pp.eps = eps;
         pp.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)d));
         pp.status = status;
+        pp.vtiles = vtiles;
+        pp.n_vtiles = n_vtiles;
         std::memcpy(pp.inv_freq, kp.inv_freq, sizeof(pp.inv_freq));
         const cudaError_t le = pair ? launch_prefill_pair(pp, maps, stream, g_prof_start, g_prof_stop)
                                     : launch_prefill_tc(pp, maps, stream, g_prof_start, g_prof_stop);
@@ -323,8 +347,66 @@ gattn_status gattn_prefill(const void* q, const void* k, const void* v, const vo
     fp.d = d;
     fp.gate_mode = gate_mode;
     fp.scale = (float)(1.0 / std::sqrt((double)d));
+    fp.tok_start = vstart;
     if (launch_prefill_f32(fp, stream, g_prof_start, g_prof_stop) != cudaSuccess) return GATTN_ERR_CUDA;
     return GATTN_OK;
+}
+
+
+extern "C" {
+
+const char* gattn_strerror(gattn_status s) {
+    switch (s) {
+        case GATTN_OK: return "GATTN_OK";
+        case GATTN_ERR_INVALID_ARG: return "GATTN_ERR_INVALID_ARG: invalid argument";
+        case GATTN_ERR_UNSUPPORTED: return "GATTN_ERR_UNSUPPORTED: no kernel for this configuration";
+        case GATTN_ERR_CUDA: return "GATTN_ERR_CUDA: a CUDA call or kernel launch failed";
+        case GATTN_ERR_WORKSPACE: return "GATTN_ERR_WORKSPACE: workspace missing, misaligned or too small";
+        case GATTN_ERR_DEVICE: return "GATTN_ERR_DEVICE: a kernel reported a device-side problem";
+    }
+    return "unknown gattn_status";
+}
+
+void gattn_set_profile_events(void* start, void* stop) {
+    g_prof_start = static_cast<cudaEvent_t>(start);
+    g_prof_stop = static_cast<cudaEvent_t>(stop);
+}
+
+size_t gattn_prefill_workspace_size(int B, int S, int H, int G, int d, int dtype) {
+    return prefill_ws(B, S, H, G, d, dtype);
+}
+
+gattn_status gattn_prefill(const void* q, const void* k, const void* v, const void* gate, const void* qnorm_w,
+                           const void* knorm_w, const int32_t* pos, int B, int S, int H, int G, int d,
+                           int rotary_dim, double rope_base, float eps, int gate_mode, int64_t q_tok_stride,
+                           int64_t q_head_stride, int64_t gate_tok_stride, int64_t gate_head_stride, int dtype,
+                           void* workspace, size_t workspace_bytes, void* out, void* stream) {
+    return prefill_impl(q, k, v, gate, qnorm_w, knorm_w, pos, B, S, H, G, d, rotary_dim, rope_base, eps, gate_mode,
+                        q_tok_stride, q_head_stride, gate_tok_stride, gate_head_stride, dtype, workspace,
+                        workspace_bytes, out, stream, nullptr);
+}
+
+size_t gattn_prefill_varlen_workspace_size(int T, int nseq, int H, int G, int d, int dtype) {
+    if (T < 1 || nseq < 1) return 0;
+    const size_t base = prefill_ws(1, T, H, G, d, dtype);
+    return base ? base + varlen_ws(T, nseq) : 0;
+}
+
+gattn_status gattn_prefill_varlen(const void* q, const void* k, const void* v, const void* gate, const void* qnorm_w,
+                                  const void* knorm_w, const int32_t* pos, const int32_t* cu_seqlens, int nseq, int H,
+                                  int G, int d, int rotary_dim, double rope_base, float eps, int gate_mode,
+                                  int64_t q_tok_stride, int64_t q_head_stride, int64_t gate_tok_stride,
+                                  int64_t gate_head_stride, int dtype, void* workspace, size_t workspace_bytes,
+                                  void* out, void* stream) {
+    if (!cu_seqlens || nseq < 1 || cu_seqlens[0] != 0) return GATTN_ERR_INVALID_ARG;
+    for (int i = 0; i < nseq; ++i)
+        if (cu_seqlens[i + 1] < cu_seqlens[i]) return GATTN_ERR_INVALID_ARG;
+    const int T = cu_seqlens[nseq];
+    if (T < 1) return GATTN_OK;  // nothing to compute
+    const Varlen vl{cu_seqlens, nseq};
+    return prefill_impl(q, k, v, gate, qnorm_w, knorm_w, pos, 1, T, H, G, d, rotary_dim, rope_base, eps, gate_mode,
+                        q_tok_stride, q_head_stride, gate_tok_stride, gate_head_stride, dtype, workspace,
+                        workspace_bytes, out, stream, &vl);
 }
 
 size_t gattn_decode_workspace_size(int B, int H, int G, int d, int Lmax) {

@@ -36,6 +36,11 @@ struct PrefillParams {
     int n_sms;  // multiprocessors of the device (persistent grids)
     float eps, scale_log2;
     unsigned int* status;
+    // packed variable-length sequences (vtiles != NULL; then B = 1 and S is the
+    // packed token count): the query tiles, heaviest first, each
+    // {start token, sequence length, tile index within the sequence, sequence}
+    const int4* vtiles;
+    int n_vtiles;
     float inv_freq[kMaxRotaryHalf];
 };
 
@@ -49,6 +54,7 @@ struct PrefillF32Params {
     int64_t gate_tok_stride, gate_head_stride;
     int B, S, H, G, d, gate_mode;
     float scale;
+    const int32_t* tok_start;  // packed sequences: first token of each token's sequence (else NULL)
 };
 
 // bf16 split-KV decode.
@@ -92,6 +98,10 @@ struct PrefillMaps {
 };
 
 cudaError_t launch_prologue(const ProloguePlan& p, bool bf16_in, bool bf16_out, cudaStream_t stream);
+// Packed sequences: from the query-tile table, every token's position within its
+// sequence and the first token of its sequence.
+cudaError_t launch_varlen_positions(const int4* tiles, int n_tiles, int32_t* pos, int32_t* tok_start,
+                                    cudaStream_t stream);
 cudaError_t launch_prefill_tc(const PrefillParams& p, const PrefillMaps& maps, cudaStream_t stream,
                               cudaEvent_t ev_start, cudaEvent_t ev_stop);
 // CTA-pair (cta_group::2) tcgen05 prefill: two heads of one KV group per cluster.

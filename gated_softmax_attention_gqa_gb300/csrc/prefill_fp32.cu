@@ -37,7 +37,8 @@ __global__ void __launch_bounds__(kRowsPerBlock * 32) prefill_f32_kernel(const _
         o[i] = 0.f;
     }
     float m = -INFINITY, l = 0.f;
-    for (int j = 0; j <= t; ++j) {
+    // packed sequences: keys from the first token of this token's sequence
+    for (int j = p.tok_start ? p.tok_start[t] : 0; j <= t; ++j) {
         const float* kj = kb + (int64_t)j * d;
         float s = 0.f;
 #pragma unroll

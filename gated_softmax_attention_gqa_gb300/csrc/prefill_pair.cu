@@ -149,17 +149,36 @@ __device__ __forceinline__ void arrive_even(uint32_t bar, uint32_t cr) {
 // a tile counter that continues across items.
 struct PairItem {
     int qt, b, hp, n_kv;
+    int t0, len;  // the sequence's first token on the S axis of batch b, and its length
+    bool direct;  // a partial tile of packed sequences: rows are stored one by one
 };
 
+template <bool GV>
 __device__ __forceinline__ bool pair_item(const PrefillParams& p, int cl, int ncl, int r, PairItem& it) {
-    const int n_hp = p.H / 2, pairs = p.B * n_hp;
+    const int n_hp = p.H / 2;
     const long long u = (long long)r * ncl + ((r & 1) ? ncl - 1 - cl : cl);
-    if (u >= (long long)p.n_qtiles * pairs) return false;
-    it.qt = p.n_qtiles - 1 - (int)(u / pairs);
-    const int bp = (int)(u % pairs);
-    it.b = bp / n_hp;
-    it.hp = bp % n_hp;
-    it.n_kv = (min(p.S, (it.qt + 1) * 128) + 127) / 128;
+    if (GV && p.vtiles) {
+        // packed sequences: query tile u / n_hp of the table (heaviest first), head pair u % n_hp
+        if (u >= (long long)p.n_vtiles * n_hp) return false;
+        const int4 e = p.vtiles[u / n_hp];
+        it.qt = e.z;
+        it.t0 = e.x;
+        it.len = e.y;
+        it.b = 0;
+        it.hp = (int)(u % n_hp);
+        it.direct = (it.qt + 1) * 128 > it.len;  // a TMA store of 128 rows would reach the next sequence
+    } else {
+        const int pairs = p.B * n_hp;
+        if (u >= (long long)p.n_qtiles * pairs) return false;
+        it.qt = p.n_qtiles - 1 - (int)(u / pairs);
+        const int bp = (int)(u % pairs);
+        it.b = bp / n_hp;
+        it.hp = bp % n_hp;
+        it.t0 = 0;
+        it.len = p.S;
+        it.direct = false;
+    }
+    it.n_kv = (min(it.len, (it.qt + 1) * 128) + 127) / 128;
     return true;
 }
 
@@ -181,7 +200,8 @@ __device__ void pair_producer(const CUtensorMap* tmK, const CUtensorMap* tmV, co
     bool ok = true;
     PairItem it;
     // the previous item, whose output still occupies the V ring
-    int prev_h = 0, prev_qt = 0, prev_b = 0;
+    int prev_h = 0, prev_row = 0, prev_b = 0;  // prev_row: first query row on the S axis
+    bool prev_direct = false;
     // the V ring is free once every PV of the previous item has completed
     auto v_ring_idle = [&]() -> bool {
         for (int j = jb - C::NSV > 0 ? jb - C::NSV : 0; j < jb; ++j)
@@ -194,21 +214,22 @@ __device__ void pair_producer(const CUtensorMap* tmK, const CUtensorMap* tmV, co
 #pragma unroll
         for (int c = 0; c < C::KCH; ++c)
             tma_load_4d(sbase + C::OFF_V + c * C::ROWBOX_BYTES, tmG, bars.g_full(), c * 64, shared ? 0 : prev_h,
-                        prev_qt * C::BM,
-                        prev_b);
+                        prev_row, prev_b);
         ++n_g;
     };
     // the softmax warps staged the previous item's output rows in the V ring (over
     // the gate tile): write them out (TMA stores, rows past the end clipped) and wait
     // until the copies have read shared memory, after which the ring may be refilled
+    // (a partial tile of packed sequences was written row by row by the softmax warps)
     auto store_output = [&]() {
+        if (prev_direct) return;
 #pragma unroll
         for (int c = 0; c < C::KCH; ++c)
-            tma_store_4d(tmO, sbase + C::OFF_V + c * C::ROWBOX_BYTES, c * 64, prev_h, prev_qt * C::BM, prev_b);
+            tma_store_4d(tmO, sbase + C::OFF_V + c * C::ROWBOX_BYTES, c * 64, prev_h, prev_row, prev_b);
         bulk_commit_group();
         bulk_wait_group_read0();
     };
-    for (int r = 0; ok && pair_item(p, cl, ncl, r, it); ++r) {
+    for (int r = 0; ok && pair_item<GV>(p, cl, ncl, r, it); ++r) {
         const int h = 2 * it.hp + (int)cr, g = h / (p.H / p.G);
         // raw Q tile of this CTA's head (normalised in place later): the Q buffer is
         // free once every QK of the previous item has completed
@@ -218,12 +239,14 @@ __device__ void pair_producer(const CUtensorMap* tmK, const CUtensorMap* tmV, co
         if (n_it == 0) bulk_load(sbase + C::OFF_W, p.qnorm_w, D * 2, bars.q_full());
 #pragma unroll
         for (int c = 0; c < C::KCH; ++c)
-            tma_load_4d(sbase + C::OFF_Q + c * C::ROWBOX_BYTES, tmQ, bars.q_full(), c * 64, h, it.qt * C::BM, it.b);
+            tma_load_4d(sbase + C::OFF_Q + c * C::ROWBOX_BYTES, tmQ, bars.q_full(), c * 64, h,
+                        it.t0 + it.qt * C::BM, it.b);
         ++n_it;
         // the gate tile is read at the very end of the item: start it on its way to L2 now
         if (gate_tile) {
 #pragma unroll
-            for (int c = 0; c < C::KCH; ++c) tma_prefetch_l2_4d(tmG, c * 64, shared ? 0 : h, it.qt * C::BM, it.b);
+            for (int c = 0; c < C::KCH; ++c)
+                tma_prefetch_l2_4d(tmG, c * 64, shared ? 0 : h, it.t0 + it.qt * C::BM, it.b);
         }
         // K' comes from the pre-pass kernel launched just before this one
         if (n_it == 1) pdl_wait_prerequisites();
@@ -252,7 +275,7 @@ __device__ void pair_producer(const CUtensorMap* tmK, const CUtensorMap* tmV, co
 #pragma unroll
                 for (int c = 0; c < C::KCH; ++c)
                     tma_load_3d(kdst + c * C::K_CHUNK, tmK, bars.k_full(st), c * 64,
-                                (nk - jb) * C::BN + (int)cr * C::KH, it.b * p.G + g);
+                                it.t0 + (nk - jb) * C::BN + (int)cr * C::KH, it.b * p.G + g);
                 ++nk;
                 progressed = true;
             }
@@ -264,7 +287,7 @@ __device__ void pair_producer(const CUtensorMap* tmK, const CUtensorMap* tmV, co
 #pragma unroll
                 for (int c = 0; c < C::VCH; ++c)
                     tma_load_4d(vdst + c * C::V_CHUNK, tmV, bars.v_full(st), (int)cr * C::DH + c * 64, g,
-                                (nv - jb) * C::BN, it.b);
+                                it.t0 + (nv - jb) * C::BN, it.b);
                 ++nv;
                 progressed = true;
             }
@@ -284,8 +307,9 @@ __device__ void pair_producer(const CUtensorMap* tmK, const CUtensorMap* tmV, co
         if (nk != ke || nv != ve) { ok = false; break; }
         jb += it.n_kv;
         prev_h = h;
-        prev_qt = it.qt;
+        prev_row = it.t0 + it.qt * C::BM;
         prev_b = it.b;
+        prev_direct = it.direct;
     }
     // the last item's gate and output
     if (ok && n_it > 0) {
@@ -307,13 +331,13 @@ __device__ void pair_producer(const CUtensorMap* tmK, const CUtensorMap* tmV, co
 }
 
 // Odd CTA: tell the even CTA's issuer, in order, that each K'/V half has landed here.
-template <int D>
+template <int D, bool GV>
 __device__ void pair_forwarder(const PrefillParams& p, const PairBars& bars, int cl, int ncl, volatile int* abort_flag,
                                unsigned int* status) {
     using C = PairCfg<D>;
     int n_kv = 0;  // tiles over all of this cluster's items
     PairItem it;
-    for (int r = 0; pair_item(p, cl, ncl, r, it); ++r) n_kv += it.n_kv;
+    for (int r = 0; pair_item<GV>(p, cl, ncl, r, it); ++r) n_kv += it.n_kv;
     int fk = 0, fv = 0;
     const unsigned long long t0 = global_timer_ns();
     uint32_t spins = 0;
@@ -351,7 +375,7 @@ __device__ void pair_forwarder(const PrefillParams& p, const PairBars& bars, int
 // so the issuer runs almost in step with the pipe: the inputs of the next MMA
 // group are polled while the tail of the current one is still queued, so that
 // the commits and waits between groups do not leave the pipe idle.
-template <int D>
+template <int D, bool GV>
 __device__ void pair_mma(const PrefillParams& p, const PairBars& bars, uint32_t sbase, uint32_t tm, int cl, int ncl,
                          volatile int* abort_flag, unsigned int* status) {
     using C = PairCfg<D>;
@@ -394,7 +418,7 @@ __device__ void pair_mma(const PrefillParams& p, const PairBars& bars, uint32_t 
     bool ok = true;
     int jb = 0, n_it = 0;
     PairItem it;
-    for (int r = 0; ok && pair_item(p, cl, ncl, r, it); ++r, ++n_it) {
+    for (int r = 0; ok && pair_item<GV>(p, cl, ncl, r, it); ++r, ++n_it) {
         const int n = it.n_kv;
         ok = mbar_wait(bars.q_ready(), (uint32_t)n_it & 1u, abort_flag, status);  // Q' of both heads ready
         for (int j = 0; ok && j < 2 && j < n; ++j) {
@@ -440,9 +464,10 @@ __device__ void pair_mma(const PrefillParams& p, const PairBars& bars, uint32_t 
 
 // ----------------------------------------------------------------- softmax / prologue / epilogue
 
-// GV: the gate variants (head-shared logits, NS-sigmoid, SiLU, additive) -- a
-// second instance of the kernel, so that the default elementwise / headwise
-// multiplicative sigmoid gate compiles exactly as it would alone.
+// GV: the gate variants (head-shared logits, NS-sigmoid, SiLU, additive) and
+// packed variable-length sequences -- a second instance of the kernel, so that
+// the default (batched, elementwise / headwise multiplicative sigmoid gate)
+// compiles exactly as it would alone.
 template <int D, bool GV>
 __device__ void pair_softmax(const PrefillParams& p, const PairBars& bars, uint32_t sbase, uint8_t* smem_x, uint32_t tm,
                              uint32_t cr, int quarter, int hf, int lane, int cl, int ncl, volatile int* abort_flag) {
@@ -469,8 +494,8 @@ __device__ void pair_softmax(const PrefillParams& p, const PairBars& bars, uint3
     // are then shared out alternately, a rotated pair (i, i + rd/2) going with the
     // chunk of i.  Rows past the sequence end were zero-filled by TMA.
     auto q_prologue = [&](const PairItem& it, int k) -> bool {
-        const int t = it.qt * C::BM + row;
-        const bool valid = t < p.S;
+        const int t = it.qt * C::BM + row;  // from the start of the sequence
+        const bool valid = t < it.len;
         if (!__all_sync(0xffffffffu, mbar_wait(bars.q_full(), (uint32_t)k & 1u, abort_flag, p.status))) return false;
         const uint32_t qbase = sbase + C::OFF_Q;
         const uint32_t wbase = sbase + C::OFF_W;
@@ -486,7 +511,7 @@ __device__ void pair_softmax(const PrefillParams& p, const PairBars& bars, uint3
         // past the meet both halves have read the raw row: the writes below may begin
         if (!meet()) return false;
         const float rinv = rsqrtf((xss[row] + xss[C::BM + row]) / (float)D + p.eps);
-        const float posf = valid ? (p.pos ? (float)p.pos[(int64_t)it.b * p.S + t] : (float)t) : 0.f;
+        const float posf = valid ? (p.pos ? (float)p.pos[(int64_t)it.b * p.S + it.t0 + t] : (float)t) : 0.f;
         const int half = p.rd >> 1;
         for (int i0 = 8 * hf; i0 < half; i0 += 16) {
             float xa[8], xb[8], wa[8], wb[8];
@@ -524,15 +549,15 @@ __device__ void pair_softmax(const PrefillParams& p, const PairBars& bars, uint3
 
     int jb = 0, n_it = 0;
     PairItem item, next;
-    bool have = pair_item(p, cl, ncl, 0, item);
+    bool have = pair_item<GV>(p, cl, ncl, 0, item);
     if (have && !q_prologue(item, 0)) return;
     for (int r = 0; have; ++r, ++n_it) {
         const int qt = item.qt, b = item.b, h = 2 * item.hp + (int)cr, n_kv = item.n_kv;
-        const int t = qt * C::BM + row;
-        const bool valid = t < p.S;
+        const int t = qt * C::BM + row;  // from the start of the sequence
+        const bool valid = t < item.len;
         float gate_head = 1.f;  // the activation of a headwise logit
         if ((GV ? gate_layout(p.gate_mode) : p.gate_mode) == GATTN_GATE_HEADWISE && valid) {
-            const int64_t tok = (int64_t)b * p.S + t;
+            const int64_t tok = (int64_t)b * p.S + item.t0 + t;
             const bf16* grow = static_cast<const bf16*>(p.gate) + tok * p.gate_tok_stride + (int64_t)h * p.gate_head_stride;
             const float z = __bfloat162float(grow[0]);
             gate_head = GV ? gate_act(z, sigmoidf_dev(z), p.gate_mode) : sigmoidf_dev(z);
@@ -623,7 +648,7 @@ __device__ void pair_softmax(const PrefillParams& p, const PairBars& bars, uint3
         }
 
         // ---- the next item's Q prologue: its QK MMAs then run during this epilogue
-        const bool more = pair_item(p, cl, ncl, r + 1, next);
+        const bool more = pair_item<GV>(p, cl, ncl, r + 1, next);
         if (more && !q_prologue(next, n_it + 1)) return;
 
         // ---- epilogue: O / l * act(gate) (or O / l + act(gate) for an additive gate),
@@ -645,6 +670,14 @@ __device__ void pair_softmax(const PrefillParams& p, const PairBars& bars, uint3
         // out = o * gm + ga
         const float gh = additive ? inv_l : inv_l * gate_head, gha = additive ? gate_head : 0.f;
         const uint32_t gbase = sbase + C::OFF_V;
+        // staged for the producer's TMA store, or (a partial tile of packed
+        // sequences) stored straight to this row of out, valid rows only
+        const bool direct = item.direct;
+        bf16* orow = static_cast<bf16*>(p.out) + (((int64_t)b * p.S + item.t0 + t) * p.H + h) * D;
+        auto put = [&](uint32_t addr, int col, uint32_t w0, uint32_t w1, uint32_t w2, uint32_t w3) {
+            if (!direct) sts_v4(addr, w0, w1, w2, w3);
+            else if (valid) *reinterpret_cast<uint4*>(orow + col) = make_uint4(w0, w1, w2, w3);
+        };
 #pragma unroll 1
         for (int c = hf * (D / 2); c < (hf + 1) * (D / 2); c += 32) {
             uint32_t r[32];
@@ -665,8 +698,8 @@ __device__ void pair_softmax(const PrefillParams& p, const PairBars& bars, uint3
 #pragma unroll
                         for (int e = 0; e < 8; ++e) gv[e] = gh;
                     }
-                    sts_v4(addr, pack_bf16x2(o[0] * gv[0], o[1] * gv[1]), pack_bf16x2(o[2] * gv[2], o[3] * gv[3]),
-                           pack_bf16x2(o[4] * gv[4], o[5] * gv[5]), pack_bf16x2(o[6] * gv[6], o[7] * gv[7]));
+                    put(addr, c + 8 * q4, pack_bf16x2(o[0] * gv[0], o[1] * gv[1]), pack_bf16x2(o[2] * gv[2], o[3] * gv[3]),
+                        pack_bf16x2(o[4] * gv[4], o[5] * gv[5]), pack_bf16x2(o[6] * gv[6], o[7] * gv[7]));
                 } else {
                 float gv[8], ga[8];  // out = o * gv + ga
                 if (elementwise) {
@@ -685,7 +718,7 @@ __device__ void pair_softmax(const PrefillParams& p, const PairBars& bars, uint3
                         ga[e] = gha;
                     }
                 }
-                sts_v4(addr, pack_bf16x2(fmaf(o[0], gv[0], ga[0]), fmaf(o[1], gv[1], ga[1])),
+                put(addr, c + 8 * q4, pack_bf16x2(fmaf(o[0], gv[0], ga[0]), fmaf(o[1], gv[1], ga[1])),
                        pack_bf16x2(fmaf(o[2], gv[2], ga[2]), fmaf(o[3], gv[3], ga[3])),
                        pack_bf16x2(fmaf(o[4], gv[4], ga[4]), fmaf(o[5], gv[5], ga[5])),
                        pack_bf16x2(fmaf(o[6], gv[6], ga[6]), fmaf(o[7], gv[7], ga[7])));
@@ -770,8 +803,8 @@ __global__ void __launch_bounds__(PairCfg<D>::THREADS, 1)
         __syncwarp();
     } else if (warp == 1) {
         if (lane == 0) {
-            if (cr == 0) pair_mma<D>(p, bars, sbase, tm, cl, ncl, abort_flag, p.status);
-            else pair_forwarder<D>(p, bars, cl, ncl, abort_flag, p.status);
+            if (cr == 0) pair_mma<D, GV>(p, bars, sbase, tm, cl, ncl, abort_flag, p.status);
+            else pair_forwarder<D, GV>(p, bars, cl, ncl, abort_flag, p.status);
         }
         __syncwarp();
     } else {
@@ -791,11 +824,11 @@ template <int D>
 cudaError_t launch_pair_d(const PrefillParams& p, const PrefillMaps& maps, cudaStream_t stream, cudaEvent_t ev_start,
                           cudaEvent_t ev_stop) {
     using C = PairCfg<D>;
-    const bool gv = !gate_plain(p.gate_mode) || gate_layout(p.gate_mode) == GATTN_GATE_HEAD_SHARED;
+    const bool gv = !gate_plain(p.gate_mode) || gate_layout(p.gate_mode) == GATTN_GATE_HEAD_SHARED || p.vtiles;
     auto kernel = gv ? prefill_pair_kernel<D, true> : prefill_pair_kernel<D, false>;
     cudaError_t e = set_smem_once(reinterpret_cast<const void*>(kernel), C::SMEM_ALLOC);
     if (e != cudaSuccess) return e;
-    const long long n_items = (long long)p.n_qtiles * p.B * (p.H / 2);
+    const long long n_items = p.vtiles ? (long long)p.n_vtiles * (p.H / 2) : (long long)p.n_qtiles * p.B * (p.H / 2);
     const long long max_clusters = p.n_sms >= 2 ? p.n_sms / 2 : 1;
     const long long blocks = 2 * (n_items < max_clusters ? n_items : max_clusters);
     if (n_items * 2 > 0x7fffffffLL || blocks < 2) return cudaErrorInvalidValue;

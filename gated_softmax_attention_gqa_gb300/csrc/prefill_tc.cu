@@ -111,14 +111,15 @@ template <int D>
 __device__ void run_producer(const CUtensorMap* tmK, const CUtensorMap* tmV, const CUtensorMap* tmQ,
                              const CUtensorMap* tmG, const void* qnorm_w, const Bars& bars, uint32_t sbase, int n_kv,
                              int b, int g, int h,
-                             int qt, int G, bool gate_tile, int gate_h, volatile int* abort_flag, unsigned int* status) {
+                             int qt, int row0, int G, bool gate_tile, int gate_h, volatile int* abort_flag,
+                             unsigned int* status) {
     using C = PfCfg<D>;
     // raw Q tile into the (still unused) V ring, the q norm weights next to it
     mbar_arrive_expect_tx(bars.q_full(), C::QTILE_BYTES + D * 2);
     bulk_load(sbase + C::OFF_W, qnorm_w, D * 2, bars.q_full());
 #pragma unroll
     for (int c = 0; c < C::KCH; ++c)
-        tma_load_4d(sbase + C::OFF_V + c * C::ROWBOX_BYTES, tmQ, bars.q_full(), c * 64, h, qt * C::BM, b);
+        tma_load_4d(sbase + C::OFF_V + c * C::ROWBOX_BYTES, tmQ, bars.q_full(), c * 64, h, row0 + qt * C::BM, b);
 
     // K' is written by the pre-pass kernel just before this one (programmatic
     // dependent launch): wait for it to finish before the first K' load.
@@ -138,7 +139,7 @@ __device__ void run_producer(const CUtensorMap* tmK, const CUtensorMap* tmV, con
             const uint32_t kdst = sbase + C::OFF_K + st * C::TILE_BYTES;
 #pragma unroll
             for (int c = 0; c < C::KCH; ++c)
-                tma_load_3d(kdst + c * C::CHUNK_BYTES, tmK, bars.k_full(st), c * 64, nk * C::BN, b * G + g);
+                tma_load_3d(kdst + c * C::CHUNK_BYTES, tmK, bars.k_full(st), c * 64, row0 + nk * C::BN, b * G + g);
             ++nk;
             progressed = true;
         }
@@ -150,7 +151,7 @@ __device__ void run_producer(const CUtensorMap* tmK, const CUtensorMap* tmV, con
             const uint32_t vdst = sbase + C::OFF_V + st * C::TILE_BYTES;
 #pragma unroll
             for (int c = 0; c < C::KCH; ++c)
-                tma_load_4d(vdst + c * C::CHUNK_BYTES, tmV, bars.v_full(st), c * 64, g, nv * C::BN, b);
+                tma_load_4d(vdst + c * C::CHUNK_BYTES, tmV, bars.v_full(st), c * 64, g, row0 + nv * C::BN, b);
             ++nv;
             progressed = true;
         }
@@ -177,7 +178,8 @@ __device__ void run_producer(const CUtensorMap* tmK, const CUtensorMap* tmV, con
             mbar_arrive_expect_tx(bars.g_full(), C::QTILE_BYTES);
 #pragma unroll
             for (int c = 0; c < C::KCH; ++c)
-                tma_load_4d(sbase + C::OFF_K + c * C::ROWBOX_BYTES, tmG, bars.g_full(), c * 64, gate_h, qt * C::BM, b);
+                tma_load_4d(sbase + C::OFF_K + c * C::ROWBOX_BYTES, tmG, bars.g_full(), c * 64, gate_h,
+                            row0 + qt * C::BM, b);
             g_issued = true;
         }
     }
@@ -285,19 +287,20 @@ __device__ void run_mma(int parity, const Bars& bars, uint32_t sbase, uint32_t t
 
 // ----------------------------------------------------------------- softmax / prologue / epilogue
 
-// GV: the gate variants (head-shared logits, NS-sigmoid, SiLU, additive) -- a
-// second instance of the kernel, so that the default elementwise / headwise
-// multiplicative sigmoid gate compiles exactly as it would alone.
+// GV: the gate variants (head-shared logits, NS-sigmoid, SiLU, additive) and
+// packed variable-length sequences -- a second instance of the kernel, so that
+// the default (batched, elementwise / headwise multiplicative sigmoid gate)
+// compiles exactly as it would alone.
 template <int D, bool GV>
 __device__ void run_softmax(const PrefillParams& p, const Bars& bars, uint32_t sbase, uint32_t tm, int quarter,
-                            int lane, int qt, int b, int h, int n_kv, volatile int* abort_flag) {
+                            int lane, int qt, int t0, int slen, int b, int h, int n_kv, volatile int* abort_flag) {
     using C = PfCfg<D>;
     const int row = quarter * 32 + lane;
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     const uint32_t tl = tm + lane_off;
     const int t = qt * C::BM + row;
-    const bool valid = t < p.S;
-    const int64_t tok = (int64_t)b * p.S + (valid ? t : 0);
+    const bool valid = t < slen;  // t counts from the start of the sequence
+    const int64_t tok = (int64_t)b * p.S + t0 + (valid ? t : 0);
     const bf16* grow = static_cast<const bf16*>(p.gate) + tok * p.gate_tok_stride + (int64_t)h * p.gate_head_stride;
     float gate_head = 1.f;  // the activation of a headwise logit
     if ((GV ? gate_layout(p.gate_mode) : p.gate_mode) == GATTN_GATE_HEADWISE && valid) {
@@ -587,11 +590,21 @@ __global__ void __launch_bounds__(PfCfg<D>::THREADS, 1)
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
 
     // heaviest query tiles first; the heads of one KV group are adjacent
+    // (packed sequences: the tile table, also heaviest first, times the heads)
     const int bh_count = p.B * p.H;
-    const int qt = p.n_qtiles - 1 - (int)(blockIdx.x / bh_count);
-    const int bh = (int)(blockIdx.x % bh_count);
+    int qt, bh, t0 = 0, slen = p.S;
+    if (GV && p.vtiles) {
+        const int4 e = p.vtiles[blockIdx.x / p.H];
+        qt = e.z;
+        t0 = e.x;
+        slen = e.y;
+        bh = (int)(blockIdx.x % p.H);
+    } else {
+        qt = p.n_qtiles - 1 - (int)(blockIdx.x / bh_count);
+        bh = (int)(blockIdx.x % bh_count);
+    }
     const int b = bh / p.H, h = bh % p.H, g = h / (p.H / p.G);
-    const int q_end = min(p.S, (qt + 1) * C::BM);
+    const int q_end = min(slen, (qt + 1) * C::BM);
     const int n_kv = (q_end + C::BN - 1) / C::BN;
 
     if (threadIdx.x == 0) {
@@ -633,7 +646,7 @@ __global__ void __launch_bounds__(PfCfg<D>::THREADS, 1)
 
     if (warp == 0) {
         if (lane == 0)
-            run_producer<D>(&tmK, &tmV, &tmQ, &tmG, p.qnorm_w, bars, sbase, n_kv, b, g, h, qt, p.G,
+            run_producer<D>(&tmK, &tmV, &tmQ, &tmG, p.qnorm_w, bars, sbase, n_kv, b, g, h, qt, t0, p.G,
                             GV ? gate_per_dim(p.gate_mode) : p.gate_mode == GATTN_GATE_ELEMENTWISE,
                             GV && gate_layout(p.gate_mode) == GATTN_GATE_HEAD_SHARED ? 0 : h, abort_flag, p.status);
         __syncwarp();
@@ -648,7 +661,7 @@ __global__ void __launch_bounds__(PfCfg<D>::THREADS, 1)
         }
         __syncwarp();
     } else {
-        run_softmax<D, GV>(p, bars, sbase, tm, warp & 3, lane, qt, b, h, n_kv, abort_flag);
+        run_softmax<D, GV>(p, bars, sbase, tm, warp & 3, lane, qt, t0, slen, b, h, n_kv, abort_flag);
     }
     tc_fence_before();
     __syncthreads();
@@ -662,11 +675,11 @@ template <int D>
 cudaError_t launch_d(const PrefillParams& p, const PrefillMaps& maps, cudaStream_t stream, cudaEvent_t ev_start,
                      cudaEvent_t ev_stop) {
     using C = PfCfg<D>;
-    const bool gv = !gate_plain(p.gate_mode) || gate_layout(p.gate_mode) == GATTN_GATE_HEAD_SHARED;
+    const bool gv = !gate_plain(p.gate_mode) || gate_layout(p.gate_mode) == GATTN_GATE_HEAD_SHARED || p.vtiles;
     auto kernel = gv ? prefill_tc_kernel<D, true> : prefill_tc_kernel<D, false>;
     cudaError_t e = set_smem_once(reinterpret_cast<const void*>(kernel), C::SMEM_ALLOC);
     if (e != cudaSuccess) return e;
-    const long long blocks = (long long)p.n_qtiles * p.B * p.H;
+    const long long blocks = p.vtiles ? (long long)p.n_vtiles * p.H : (long long)p.n_qtiles * p.B * p.H;
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
     if (ev_start) cudaEventRecord(ev_start, stream);
     cudaLaunchConfig_t cfg = {};

@@ -189,7 +189,25 @@ cudaError_t launch_bf16(const ProloguePlan& p, cudaStream_t stream) {
     return cudaGetLastError();
 }
 
+// One CTA per query tile of the table: the tile's 128 tokens get their position
+// within the sequence and the sequence's first token.
+__global__ void __launch_bounds__(128) varlen_positions_kernel(const int4* tiles, int32_t* pos, int32_t* tok_start) {
+    const int4 e = tiles[blockIdx.x];  // start, length, tile, sequence
+    const int t = e.z * 128 + (int)threadIdx.x;
+    if (t < e.y) {
+        pos[e.x + t] = t;
+        tok_start[e.x + t] = e.x;
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_varlen_positions(const int4* tiles, int n_tiles, int32_t* pos, int32_t* tok_start,
+                                    cudaStream_t stream) {
+    if (n_tiles <= 0) return cudaSuccess;
+    varlen_positions_kernel<<<(unsigned)n_tiles, 128, 0, stream>>>(tiles, pos, tok_start);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_prologue(const ProloguePlan& p, bool bf16_in, bool bf16_out, cudaStream_t stream) {
     const int64_t n_rows = (int64_t)p.B * p.S * p.n_heads;

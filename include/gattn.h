@@ -142,6 +142,34 @@ gattn_status gattn_prefill(const void* q, const void* k, const void* v, const vo
                            void* workspace, size_t workspace_bytes, void* out, void* stream);
 
 /*
+ * Causal gated GQA attention over PACKED variable-length sequences (varlen):
+ * sequence i occupies tokens [cu_seqlens[i], cu_seqlens[i+1]) of the packed
+ * tensors and attends only to its own keys, its RoPE positions restarting at 0
+ * (a padding-free form of the causal / padding mask M of the "Gated Attention"
+ * deep-dive's statement of the layer).
+ *
+ * q        [T,H,d] at q[t*q_tok_stride + h*q_head_stride + e] (defaults H*d, d).
+ * k, v     [T,G,d] contiguous.
+ * gate     [T,H,d], [T,H] or [T,d] per gate_mode, strides as for gattn_prefill.
+ * pos      [T] int32 device positions, or NULL for 0..len-1 within each sequence.
+ * cu_seqlens  [nseq+1] int32 HOST array: 0 = cu_seqlens[0] <= ... <=
+ *          cu_seqlens[nseq] = T; empty sequences are allowed.  The library builds
+ *          its schedule from it on the host and copies that into the workspace on
+ *          `stream` before returning.
+ * out      [T,H*d].  Everything else as gattn_prefill, with B = 1 and S = T.
+ * workspace  >= gattn_prefill_varlen_workspace_size(T, nseq, H, G, d, dtype).
+ * T = 0 returns GATTN_OK without launching anything.
+ */
+size_t gattn_prefill_varlen_workspace_size(int T, int nseq, int H, int G, int d, int dtype);
+gattn_status gattn_prefill_varlen(const void* q, const void* k, const void* v, const void* gate, const void* qnorm_w,
+                                  const void* knorm_w, const int32_t* pos, const int32_t* cu_seqlens, int nseq, int H,
+                                  int G, int d, int rotary_dim, double rope_base, float eps, int gate_mode,
+                                  int64_t q_tok_stride, int64_t q_head_stride, int64_t gate_tok_stride,
+                                  int64_t gate_head_stride, int dtype, void* workspace, size_t workspace_bytes,
+                                  void* out, void* stream);
+
+/*
+ * Bytes of workspace gattn_decode needs/*
  * Bytes of workspace gattn_decode needs (per-split partial softmax states).
  * Depends on the current device's SM count.  Returns 0 for invalid sizes.
  */

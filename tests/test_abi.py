@@ -165,6 +165,42 @@ def test_decode_paged_rejects_bad_arguments(lib, kw, expect):
     assert decode_paged(lib, **kw) == expect
 
 
+def prefill_varlen(lib, cu, **kw):
+    arr = (ctypes.c_int32 * len(cu))(*cu) if cu is not None else None
+    a = dict(q=P(), k=P(), v=P(), gate=P(), qw=P(), kw=P(), pos=None, H=8, G=2, d=128, rd=64, base=1e6, eps=1e-6,
+             gm=1, qts=0, qhs=0, gts=0, ghs=0, dt=0, ws=P(), wsb=1 << 40, out=P(1 << 20))
+    a.update(kw)
+    return lib.gattn_prefill_varlen(a["q"], a["k"], a["v"], a["gate"], a["qw"], a["kw"], a["pos"],
+                                    ctypes.cast(arr, ctypes.c_void_p) if arr is not None else None,
+                                    max(len(cu) - 1, 0) if cu is not None else 1, a["H"], a["G"], a["d"], a["rd"],
+                                    a["base"], a["eps"], a["gm"], a["qts"], a["qhs"], a["gts"], a["ghs"], a["dt"],
+                                    a["ws"], a["wsb"], a["out"], None)
+
+
+@pytest.mark.parametrize("cu,kw,expect", [
+    (None, {}, INVALID),                  # no cumulative lengths
+    ([1, 5], {}, INVALID),                # must start at 0
+    ([0, 5, 3], {}, INVALID),             # decreasing
+    ([0], {}, INVALID),                   # no sequence
+    ([0, 0, 0], {}, OK),                  # only empty sequences: nothing to launch
+    ([0, 5, 9], dict(H=6, G=4), INVALID),
+    ([0, 5, 9], dict(d=96), UNSUPPORTED),
+    ([0, 5, 9], dict(gm=0x40), INVALID),
+    ([0, 5, 9], dict(wsb=1024), WORKSPACE),
+])
+def test_prefill_varlen_rejects_bad_arguments(lib, cu, kw, expect):
+    assert prefill_varlen(lib, cu, **kw) == expect
+
+
+def test_prefill_varlen_workspace_size(lib):
+    base = lib.gattn_prefill_workspace_size(1, 1000, 8, 2, 128, 0)
+    got = lib.gattn_prefill_varlen_workspace_size(1000, 3, 8, 2, 128, 0)
+    tiles = (1000 + 127) // 128 + 3
+    rnd = lambda x: (x + 255) // 256 * 256
+    assert got == base + rnd(tiles * 16) + 2 * rnd(1000 * 4)
+    assert lib.gattn_prefill_varlen_workspace_size(0, 3, 8, 2, 128, 0) == 0
+
+
 def test_prefill_workspace_sizes(lib):
     assert lib.gattn_prefill_workspace_size(1, 4096, 8, 2, 256, 0) == 4096 * 2 * 256 * 2
     assert lib.gattn_prefill_workspace_size(1, 64, 2, 1, 32, 1) == (64 * 2 * 32 + 64 * 32) * 4

@@ -4,7 +4,7 @@ import pytest
 import torch
 
 import oracle
-from gated_softmax_attention_gqa_gb300 import gattn_get_device_status, gattn_prefill, workloads
+from gated_softmax_attention_gqa_gb300 import gattn_get_device_status, gattn_prefill, gattn_prefill_varlen, workloads
 from gated_softmax_attention_gqa_gb300.workloads import WORKLOADS, Workload, make_prefill_inputs
 from tests.parity import assert_close_to_oracle, gate_scale, sample_rows
 
@@ -113,6 +113,62 @@ def test_gate_variants(shape):
                 assert_close_to_oracle(out, ref, tdt, f"{shape} {layout} {act} additive={additive}",
                                       scale=gate_scale(inp["gate"].double().numpy(), layout, act, ref.shape))
     assert gattn_get_device_status() == 0
+
+
+# packed variable-length sequences through every prefill kernel: ragged lengths
+# (1 token, one short of a tile, exactly a tile, one over, several tiles, empty)
+VARLEN_CASES = [
+    # H, G, d, rd, base, dtype, gate layout, lengths
+    (4, 2, 256, 64, 1e7, "bf16", "elementwise", [1, 127, 128, 129, 300, 0, 77]),   # CTA-pair kernel
+    (4, 2, 128, 64, 1e6, "bf16", "headwise", [200, 5, 0, 128, 257]),              # one-head kernel, d 128
+    (3, 1, 256, 64, 1e7, "bf16", "head_shared", [130, 64, 1]),                    # one-head kernel, d 256
+    (4, 2, 64, 16, 1e4, "fp32", "elementwise", [33, 1, 70, 0, 64]),               # fp32 kernel
+]
+
+
+@pytest.mark.parametrize("case", VARLEN_CASES, ids=[f"{c[5]}-d{c[2]}-{c[6]}" for c in VARLEN_CASES])
+def test_varlen_parity(case):
+    H, G, d, rd, base, dt, layout, lens = case
+    T = sum(lens)
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    w = small("varlen", 1, T, H, G, d, rd, base, layout, dtype=dt, seed=T + d)
+    inp = make_prefill_inputs(w)
+    flat = {k: (v[0] if k in ("q", "k", "v", "gate") else v) for k, v in inp.items()}
+    dev = {k: v.to(DEV) for k, v in flat.items()}
+    tdt = torch.bfloat16 if dt == "bf16" else torch.float32
+    out = gattn_prefill_varlen(dev["q"], dev["k"], dev["v"], dev["gate"], dev["qnorm_w"], dev["knorm_w"], cu,
+                               rotary_dim=rd, rope_base=base, eps=w.eps, gate_mode=layout)
+    torch.cuda.synchronize()
+    assert gattn_get_device_status() == 0
+    ref = oracle.prefill_varlen(flat["q"], flat["k"], flat["v"], flat["gate"], flat["qnorm_w"], flat["knorm_w"],
+                                None, cu, rd, base, w.eps, layout)
+    assert_close_to_oracle(out, ref, tdt, str(case))
+    # explicit positions: an offset per sequence
+    pos = torch.cat([torch.arange(n, dtype=torch.int32) + 1000 * i for i, n in enumerate(lens)])
+    out = gattn_prefill_varlen(dev["q"], dev["k"], dev["v"], dev["gate"], dev["qnorm_w"], dev["knorm_w"], cu,
+                               pos.to(DEV), rotary_dim=rd, rope_base=base, eps=w.eps, gate_mode=layout)
+    torch.cuda.synchronize()
+    ref = oracle.prefill_varlen(flat["q"], flat["k"], flat["v"], flat["gate"], flat["qnorm_w"], flat["knorm_w"],
+                                pos.double(), cu, rd, base, w.eps, layout)
+    assert_close_to_oracle(out, ref, tdt, str(case) + " with positions")
+
+
+@pytest.mark.parametrize("d,H,G", [(256, 8, 2), (128, 4, 2)])
+def test_varlen_equal_lengths_match_the_batched_call(d, H, G):
+    """Equal-length packed sequences give exactly the batched result: every query
+    tile is computed the same way, only the schedule differs."""
+    B, S = 3, 300
+    w = small("eq", B, S, H, G, d, 64, 1e6, "elementwise", seed=d)
+    inp = make_prefill_inputs(w)
+    dev = {k: v.to(DEV) for k, v in inp.items()}
+    batched = gattn_prefill(dev["q"], dev["k"], dev["v"], dev["gate"], dev["qnorm_w"], dev["knorm_w"], rotary_dim=64,
+                            rope_base=1e6, eps=w.eps, gate_mode="elementwise")
+    packed = gattn_prefill_varlen(dev["q"].reshape(B * S, H, d), dev["k"].reshape(B * S, G, d),
+                                  dev["v"].reshape(B * S, G, d), dev["gate"].reshape(B * S, H, d), dev["qnorm_w"],
+                                  dev["knorm_w"], [0, S, 2 * S, 3 * S], rotary_dim=64, rope_base=1e6, eps=w.eps,
+                                  gate_mode="elementwise")
+    torch.cuda.synchronize()
+    assert torch.equal(packed.view(B, S, H * d), batched)
 
 
 def test_bf16_packed_qproj_layout_and_positions():
