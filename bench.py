@@ -378,7 +378,7 @@ def main():
             "prefill_ms": t["p"], "prefill_kernel_ms": t["pk"],
             "roofline": {"bound": "tensor", "achieved": kern_tflops, "peak": bf16_peak, "unit": "TFLOP/s",
                          "frac": kern_tflops / bf16_peak, "peak_kind": f"{peak_kind} bf16 dense (burst)",
-                         "kernel": "prefill_pair_kernel<256>",
+                         "kernel": "prefill_pair_kernel<256, false>",
                          "traffic": profiled_traffic("prefill_pair_qwen35_08b.md", tc_src)},
             "decode": {"value": dec_gbs, "unit": "GB/s", "ms": t["d"], "kernel_ms": t["dk"],
                        "bytes_per_step": dbytes,
