@@ -94,7 +94,7 @@ struct AppendParams {
 // TMA descriptors of the tcgen05 prefill: normed keys (workspace), raw V, raw Q,
 // (elementwise gate only) the gate logits and the output; all bf16, 64-element inner boxes.
 struct PrefillMaps {
-    CUtensorMap k, v, q, gate, out;  // out: [B,S,H*d] as (d, H, S, B), written by TMA stores (pair kernel)
+    CUtensorMap k, v, q, gate, out;  // out: [B,S,H*d] as (d, H, S, B), written by TMA stores
 };
 
 cudaError_t launch_prologue(const ProloguePlan& p, bool bf16_in, bool bf16_out, cudaStream_t stream);

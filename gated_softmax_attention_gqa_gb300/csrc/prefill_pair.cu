@@ -560,7 +560,7 @@ __device__ void pair_softmax(const PrefillParams& p, const PairBars& bars, uint3
             const int64_t tok = (int64_t)b * p.S + item.t0 + t;
             const bf16* grow = static_cast<const bf16*>(p.gate) + tok * p.gate_tok_stride + (int64_t)h * p.gate_head_stride;
             const float z = __bfloat162float(grow[0]);
-            gate_head = GV ? gate_act(z, sigmoidf_dev(z), p.gate_mode) : sigmoidf_dev(z);
+            gate_head = GV ? gate_act(z, sigmoid_tanh(z), p.gate_mode) : sigmoid_tanh(z);
         }
 
         // ---- main loop: online softmax over the KV tiles this query tile can see.

@@ -9,29 +9,38 @@
 // scaling and stable softmax matter"; "Gated Attention" deep-dive, section
 // "门放在哪里？".)
 //
-// Roles (7 warps):
+// Roles (11 warps at d <= 128, 7 at d = 256):
 //   warp 0      TMA producer: the raw Q tile once, then K' tiles (keys normed and
 //               rotated by the pre-pass) and raw V tiles into 3-stage rings (128 B
 //               swizzle), K and V issued independently; at the end the gate tile.
 //   warps 1, 2  MMA issuers (warp 1 also owns TMEM): warp 1 + i issues S = Q'K'^T
 //               (tcgen05.mma, A read from TMEM) and O += P V of the KV tiles j
 //               with j % 2 == i.
-//   warps 3..6  one thread per query row: the fused Q prologue (RMSNorm + RoPE of
-//               the raw query row, read from shared memory, written as bf16
-//               straight into TMEM), the online softmax, and the gate epilogue.
+//   warps 3..   the fused Q prologue (RMSNorm + RoPE of the raw query row, read
+//               from shared memory, written as bf16 straight into TMEM), the online
+//               softmax, and the gate epilogue.  d <= 128: 8 warps, two threads per
+//               query row (warps w and w + 4 share the row's TMEM lanes), each owning
+//               half of the keys of every tile and half of O's columns; the halves
+//               swap their tile maxima through shared memory.  d = 256: 4 warps, one
+//               thread per row.
 //
 // Shared memory: K ring | V ring.  Before any V tile is loaded the V ring holds
-// the raw Q tile; once every K tile has been consumed the K ring receives the
-// gate tile.  Both reuses are ordered by mbarriers.
+// the raw Q tile, and once every PV is done it holds the output tile staged for the
+// TMA stores; once every K tile has been consumed the K ring receives the gate
+// tile.  Every reuse is ordered by mbarriers.
 //
 // TMEM (512 columns x 128 lanes, lane = query row):
 //   [0, d)             O accumulator, fp32
-//   [d, d+BN)          S buffer 0 (fp32 scores; overwritten in place by bf16 P)
+//   [d, d+BN)          S buffer 0 (fp32 scores)
 //   [d+BN, d+2BN)      S buffer 1
 //   [d+2BN, d+2BN+d/2) Q' as packed bf16 pairs (A operand of S = Q'K'^T)
+//   then (d <= 128)    P as packed bf16 pairs, BN/2 columns (A operand of O += PV)
 //
-// Pipeline: while the softmax threads turn S_j into P_j, the tensor core already
-// computes S_{j+1} into the other buffer; P_j V_j follows as soon as P_j lands.
+// Pipeline: a score buffer is handed back as soon as the softmax has loaded S_j,
+// so QK_{j+2} runs while the softmax still works on tile j (and S_{j+1} is already
+// waiting); P_j goes to its own buffer (TMEM, or shared memory at d = 256) once
+// PV_{j-1} (PV_{j-2} at d = 256) has read the previous P, and P_j V_j follows as
+// soon as P_j lands.
 // The running max is only refreshed (and O rescaled in TMEM) when it grows by
 // more than 2^8, so the rescale is rare and exact: O and l always share one
 // reference max.  The causal mask is applied by skipping every KV tile past the
@@ -46,10 +55,13 @@ template <int D>
 struct PfCfg {
     static constexpr int BM = 128;
     // d = 256: 64-key tiles (TMEM: O 256 + two S 64 + Q' 128 columns) and P goes to
-    // shared memory, so a score buffer is free again as soon as the softmax has read
-    // it.  d <= 128: 128-key tiles, P overwrites S in TMEM.
+    // shared memory.  d <= 128: 128-key tiles, P in a TMEM buffer of its own.
     static constexpr int BN = (D == 256) ? 64 : 128;
     static constexpr bool PSMEM = (D == 256);
+    // d <= 128: two threads per query row (8 softmax warps), each owning half of the
+    // row's keys in every tile and half of O's columns
+    static constexpr bool SPLIT = !PSMEM;
+    static constexpr int SOFTMAX_WARPS = SPLIT ? 8 : 4;
     static constexpr int NSB = 2;  // score buffers in TMEM: tile j uses buffer j % 2
     static constexpr int NPB = PSMEM ? 2 : 0;  // P buffers in shared memory
     static constexpr int NSK = 3;  // K ring stages
@@ -65,21 +77,25 @@ struct PfCfg {
     static constexpr int TM_O = 0;
     static constexpr int TM_S = D;                   // score buffer b at TM_S + b * BN
     static constexpr int TM_Q = D + NSB * BN;
+    // d <= 128: P (bf16 pairs) has a TMEM buffer of its own, so a score buffer is
+    // free as soon as the softmax has loaded it and QK_{j+2} need not wait for PV_j
+    static constexpr int TM_P = TM_Q + D / 2;
     static constexpr int TM_COLS = 512;
-    static_assert(TM_Q + D / 2 <= TM_COLS, "TMEM budget");
+    static_assert(TM_Q + D / 2 <= TM_COLS && (PSMEM || TM_P + BN / 2 <= TM_COLS), "TMEM budget");
     static constexpr int OFF_K = 0;
     static constexpr int OFF_V = NSK * TILE_BYTES;
     static constexpr int OFF_P = OFF_V + NSV * TILE_BYTES;
     static constexpr int OFF_BAR = OFF_P + NPB * P_BUF_BYTES;
-    static constexpr int NBAR = 2 * NSK + 2 * NSV + 13;
+    static constexpr int NBAR = 2 * NSK + 2 * NSV + 18;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr int OFF_W = (OFF_MISC + 16 + 127) & ~127;  // qnorm weights, D bf16
-    static constexpr int SMEM_BYTES = OFF_W + D * 2;
+    static constexpr int OFF_X = OFF_W + D * 2;                  // row-half exchange (SPLIT)
+    static constexpr int SMEM_BYTES = OFF_X + (SPLIT ? 8 * BM * 4 : 0);
     // + slack for 1024-byte alignment; never less than 120 KB, so that a second CTA
     // can never share the SM (each CTA allocates all 512 TMEM columns).
     static constexpr int SMEM_ALLOC = (SMEM_BYTES + 1024) > 122880 ? (SMEM_BYTES + 1024) : 122880;
     static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
-    static constexpr int THREADS = 224;
+    static constexpr int THREADS = 96 + 32 * SOFTMAX_WARPS;
     static constexpr uint32_t IDESC_QK = make_idesc_bf16(128, BN, false);
     static constexpr uint32_t IDESC_PV = make_idesc_bf16(128, D, true);
     static constexpr float RESCALE_THRESHOLD = 8.0f;  // log2 domain: rescale when the max grows by > 2^8
@@ -103,16 +119,17 @@ struct Bars {
     __device__ uint32_t drain() const { return at(r() + 10); }
     __device__ uint32_t q_full() const { return at(r() + 11); }   // raw Q tile landed
     __device__ uint32_t g_full() const { return at(r() + 12); }   // gate tile landed
+    __device__ uint32_t xchg(int q) const { return at(r() + 13 + q); }  // both halves of row quarter q posted
+    __device__ uint32_t o_staged() const { return at(r() + 17); }         // every softmax warp staged its output
 };
 
 // ----------------------------------------------------------------- producer
 
 template <int D>
 __device__ void run_producer(const CUtensorMap* tmK, const CUtensorMap* tmV, const CUtensorMap* tmQ,
-                             const CUtensorMap* tmG, const void* qnorm_w, const Bars& bars, uint32_t sbase, int n_kv,
-                             int b, int g, int h,
-                             int qt, int row0, int G, bool gate_tile, int gate_h, volatile int* abort_flag,
-                             unsigned int* status) {
+                             const CUtensorMap* tmG, const CUtensorMap* tmO, const void* qnorm_w, const Bars& bars,
+                             uint32_t sbase, int n_kv, int b, int g, int h, int qt, int row0, int G, bool gate_tile,
+                             int gate_h, bool store_tile, volatile int* abort_flag, unsigned int* status) {
     using C = PfCfg<D>;
     // raw Q tile into the (still unused) V ring, the q norm weights next to it
     mbar_arrive_expect_tx(bars.q_full(), C::QTILE_BYTES + D * 2);
@@ -190,6 +207,17 @@ __device__ void run_producer(const CUtensorMap* tmK, const CUtensorMap* tmV, con
     for (int j = nv > C::NSV ? nv - C::NSV : 0; j < nv; ++j)
         mbar_wait_drain(bars.v_full(j % C::NSV), (uint32_t)(j / C::NSV) & 1u, status);
     if (g_issued) mbar_wait_drain(bars.g_full(), 0, status);
+    // the softmax warps staged the output tile in the V ring: write it out and wait
+    // for the copies to complete before the CTA's shared memory goes away
+    if (store_tile) {
+        if (mbar_wait(bars.o_staged(), 0, abort_flag, status)) {
+#pragma unroll
+            for (int c = 0; c < C::KCH; ++c)
+                tma_store_4d(tmO, sbase + C::OFF_V + c * C::ROWBOX_BYTES, c * 64, h, row0 + qt * C::BM, b);
+            bulk_commit_group();
+        }
+        bulk_wait_group0();
+    }
 }
 
 // ----------------------------------------------------------------- MMA issuer
@@ -206,10 +234,8 @@ __device__ __forceinline__ bool issue_qk(int j, const Bars& bars, uint32_t tm, u
                                          volatile int* abort_flag, unsigned int* status) {
     using C = PfCfg<D>;
     const int sb = j & 1;
-    // score buffer sb was last used by tile j-2: with P in shared memory it is free
-    // once the softmax has read S_{j-2}; with P in TMEM this issuer already issued
-    // PV_{j-2} (which reads P_{j-2} there) before this QK, and the pipe runs in order.
-    if (C::PSMEM && j >= 2 && !mbar_wait(bars.s_free(sb), (uint32_t)((j >> 1) - 1) & 1u, abort_flag, status))
+    // score buffer sb was last used by tile j-2: it is free once the softmax has read S_{j-2}
+    if (j >= 2 && !mbar_wait(bars.s_free(sb), (uint32_t)((j >> 1) - 1) & 1u, abort_flag, status))
         return false;
     const int st = j % C::NSK;
     if (!mbar_wait(bars.k_full(st), (uint32_t)(j / C::NSK) & 1u, abort_flag, status)) return false;
@@ -246,10 +272,9 @@ __device__ __forceinline__ bool issue_pv(int j, const Bars& bars, uint32_t tm, u
             mma_ss(tm + C::TM_O, pd + (uint64_t)(((kk >> 2) * (C::BM * 128) + (kk & 3) * 32) >> 4),
                    vd + (uint64_t)((kk * 16 * 128) >> 4), C::IDESC_PV, 1u);
     } else {
-        const uint32_t p_tmem = tm + C::TM_S + (j & 1) * C::BN;
 #pragma unroll
         for (int kk = 0; kk < C::BN / 16; ++kk)
-            mma_ts(tm + C::TM_O, p_tmem + kk * 8, vd + (uint64_t)((kk * 16 * 128) >> 4), C::IDESC_PV, 1u);
+            mma_ts(tm + C::TM_O, tm + C::TM_P + kk * 8, vd + (uint64_t)((kk * 16 * 128) >> 4), C::IDESC_PV, 1u);
     }
     tc_commit(bars.v_empty(st));
     tc_commit(bars.pv_done(j & 1));
@@ -265,21 +290,12 @@ __device__ void run_mma(int parity, const Bars& bars, uint32_t sbase, uint32_t t
     const uint64_t kdesc0 = make_sdesc_sw128(sbase + C::OFF_K, 16, 1024);
     const uint64_t vdesc0 = make_sdesc_sw128(sbase + C::OFF_V, C::CHUNK_BYTES, 1024);
     const uint64_t pdesc0 = make_sdesc_sw128(sbase + C::OFF_P, 16, 1024);
-    if (C::PSMEM) {
-        // QK of the next own tile goes out as soon as its score buffer is free,
-        // ahead of the PV that is still waiting for its P.
-        if (ok && parity < n_kv) ok = issue_qk<D>(parity, bars, tm, kdesc0, abort_flag, status);
-        for (int j = parity; ok && j < n_kv; j += 2) {
-            if (j + 2 < n_kv && !issue_qk<D>(j + 2, bars, tm, kdesc0, abort_flag, status)) { ok = false; break; }
-            if (!issue_pv<D>(j, bars, tm, vdesc0, pdesc0, abort_flag, status)) { ok = false; break; }
-        }
-    } else {
-        // P_j lives in score buffer j%2: PV_j must be issued before QK_{j+2} overwrites it.
-        if (ok && parity < n_kv) ok = issue_qk<D>(parity, bars, tm, kdesc0, abort_flag, status);
-        for (int j = parity; ok && j < n_kv; j += 2) {
-            if (!issue_pv<D>(j, bars, tm, vdesc0, pdesc0, abort_flag, status)) { ok = false; break; }
-            if (j + 2 < n_kv && !issue_qk<D>(j + 2, bars, tm, kdesc0, abort_flag, status)) { ok = false; break; }
-        }
+    // QK of the next own tile goes out as soon as its score buffer is free, ahead of
+    // the PV that is still waiting for its P.
+    if (ok && parity < n_kv) ok = issue_qk<D>(parity, bars, tm, kdesc0, abort_flag, status);
+    for (int j = parity; ok && j < n_kv; j += 2) {
+        if (j + 2 < n_kv && !issue_qk<D>(j + 2, bars, tm, kdesc0, abort_flag, status)) { ok = false; break; }
+        if (!issue_pv<D>(j, bars, tm, vdesc0, pdesc0, abort_flag, status)) { ok = false; break; }
     }
     if (ok) tc_commit(bars.o_final());  // count 2: both issuers' PVs complete
     tc_commit(bars.drain());
@@ -292,9 +308,13 @@ __device__ void run_mma(int parity, const Bars& bars, uint32_t sbase, uint32_t t
 // the default (batched, elementwise / headwise multiplicative sigmoid gate)
 // compiles exactly as it would alone.
 template <int D, bool GV>
-__device__ void run_softmax(const PrefillParams& p, const Bars& bars, uint32_t sbase, uint32_t tm, int quarter,
-                            int lane, int qt, int t0, int slen, int b, int h, int n_kv, volatile int* abort_flag) {
+__device__ void run_softmax(const PrefillParams& p, const Bars& bars, uint32_t sbase, uint8_t* smem_x, uint32_t tm,
+                            int quarter, int hf, int lane, int qt, int t0, int slen, int b, int h, int n_kv,
+                            volatile int* abort_flag) {
     using C = PfCfg<D>;
+    constexpr int NH = C::SPLIT ? 2 : 1;  // threads per query row
+    constexpr int KB = C::BN / NH;        // keys of every tile owned by this thread: [hf KB, hf KB + KB)
+    constexpr int OC = D / NH;            // O columns owned by this thread: [hf OC, hf OC + OC)
     const int row = quarter * 32 + lane;
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     const uint32_t tl = tm + lane_off;
@@ -305,28 +325,49 @@ __device__ void run_softmax(const PrefillParams& p, const Bars& bars, uint32_t s
     float gate_head = 1.f;  // the activation of a headwise logit
     if ((GV ? gate_layout(p.gate_mode) : p.gate_mode) == GATTN_GATE_HEADWISE && valid) {
         const float z = __bfloat162float(grow[0]);
-        gate_head = GV ? gate_act(z, sigmoidf_dev(z), p.gate_mode) : sigmoidf_dev(z);
+        gate_head = GV ? gate_act(z, sigmoid_tanh(z), p.gate_mode) : sigmoid_tanh(z);
     }
+    // With two threads per row (warps w and w + 4 share the row's TMEM lanes) the
+    // halves swap values through shared memory and then meet on an mbarrier (one
+    // phase per use: the prologue, every tile and the epilogue).
+    float* xmax = reinterpret_cast<float*>(smem_x);  // [2][2][BM] tile maxima
+    float* xsum = xmax + 2 * 2 * C::BM;              // [2][BM] row sums
+    float* xss = xsum + 2 * C::BM;                   // [2][BM] sums of squares of q
+    const uint32_t xbar = bars.xchg(quarter);
+    int xphase = 0;
+    auto meet = [&]() -> bool {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(xbar);
+        return __all_sync(0xffffffffu, mbar_wait(xbar, (uint32_t)(xphase++) & 1u, abort_flag, p.status));
+    };
 
     // ---- fused Q prologue: rmsnorm then partial rotate-half RoPE, bf16 into TMEM.
     // The raw row is read from the Q tile the producer placed in the V ring
-    // (rows past the sequence end were zero-filled by TMA).
+    // (rows past the sequence end were zero-filled by TMA).  Split rows: each half
+    // sums the squares of its columns, and the 8-column chunks (a rotated pair
+    // (i, i + rd/2) going with the chunk of i) are shared out alternately.
     if (!__all_sync(0xffffffffu, mbar_wait(bars.q_full(), 0, abort_flag, p.status))) return;
     {
         const uint32_t qbase = sbase + C::OFF_V;
         const uint32_t wbase = sbase + C::OFF_W;
         float ss[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int c = 0; c < D / 8; ++c) {
+        for (int c = 0; c < OC / 8; ++c) {
             float f[8];
-            unpack8(lds_v4(rowtile_addr(qbase, row, 8 * c)), f);
+            unpack8(lds_v4(rowtile_addr(qbase, row, hf * OC + 8 * c)), f);
 #pragma unroll
             for (int e = 0; e < 8; ++e) ss[e & 3] = fmaf(f[e], f[e], ss[e & 3]);
         }
-        const float rinv = rsqrtf(((ss[0] + ss[1]) + (ss[2] + ss[3])) / (float)D + p.eps);
+        float sq = (ss[0] + ss[1]) + (ss[2] + ss[3]);
+        if constexpr (C::SPLIT) {
+            xss[hf * C::BM + row] = sq;
+            if (!meet()) return;
+            sq = xss[row] + xss[C::BM + row];
+        }
+        const float rinv = rsqrtf(sq / (float)D + p.eps);
         const float posf = valid ? (p.pos ? (float)p.pos[tok] : (float)t) : 0.f;
         const int half = p.rd >> 1;
-        for (int i0 = 0; i0 < half; i0 += 8) {
+        for (int i0 = 8 * hf; i0 < half; i0 += 8 * NH) {
             float xa[8], xb[8], wa[8], wb[8];
             unpack8(lds_v4(rowtile_addr(qbase, row, i0)), xa);
             unpack8(lds_v4(rowtile_addr(qbase, row, i0 + half)), xb);
@@ -347,7 +388,7 @@ __device__ void run_softmax(const PrefillParams& p, const Bars& bars, uint32_t s
             tmem_st4(tl + C::TM_Q + (i0 >> 1), lo[0], lo[1], lo[2], lo[3]);
             tmem_st4(tl + C::TM_Q + ((i0 + half) >> 1), hi[0], hi[1], hi[2], hi[3]);
         }
-        for (int e0 = p.rd; e0 < D; e0 += 8) {
+        for (int e0 = p.rd + 8 * hf; e0 < D; e0 += 8 * NH) {
             float x[8], w[8];
             unpack8(lds_v4(rowtile_addr(qbase, row, e0)), x);
             unpack8(lds_v4(wbase + 2 * e0), w);
@@ -363,7 +404,7 @@ __device__ void run_softmax(const PrefillParams& p, const Bars& bars, uint32_t s
 #pragma unroll
             for (int e = 0; e < 32; ++e) z[e] = 0u;
 #pragma unroll
-            for (int c = 0; c < D; c += 32) tmem_st32(tl + C::TM_O + c, z);
+            for (int c = 0; c < OC; c += 32) tmem_st32(tl + C::TM_O + hf * OC + c, z);
         }
         fence_proxy_async_smem();  // our reads of the V ring happen before the V tiles overwrite it
         tmem_wait_st();
@@ -375,42 +416,47 @@ __device__ void run_softmax(const PrefillParams& p, const Bars& bars, uint32_t s
     // ---- main loop: online softmax over the KV tiles this query tile can see
     const float sl2 = p.scale_log2;
     const int row_min = qt * C::BM;
-    float m_ref = -INFINITY;  // reference max (log2 domain) shared by O and l
-    float l = 0.f;
+    float m_ref = -INFINITY;  // reference max (log2 domain) shared by O and l (and by both halves of a row)
+    float l = 0.f;            // this thread's share of the row sum
     for (int j = 0; j < n_kv; ++j) {
         const int sb = j % C::NSB;
         const uint32_t s_col = C::TM_S + sb * C::BN;
         if (!__all_sync(0xffffffffu, mbar_wait(bars.s_full(sb), (uint32_t)(j / C::NSB) & 1u, abort_flag, p.status)))
             return;
         tc_fence_after();
-        float s[C::BN];
+        float s[KB];
         {
             uint32_t r[64];
 #pragma unroll
-            for (int c = 0; c < C::BN; c += 64) {
-                tmem_ld64(tl + s_col + c, r);
+            for (int c = 0; c < KB; c += 64) {
+                tmem_ld64(tl + s_col + hf * KB + c, r);
 #pragma unroll
                 for (int e = 0; e < 64; ++e) s[c + e] = __uint_as_float(r[e]);
             }
         }
-        if constexpr (C::PSMEM) {  // S_j is in registers: its buffer may take the next tile's scores
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bars.s_free(sb));
-        }
-        const int key0 = j * C::BN;
-        if (key0 + C::BN - 1 > row_min) {
+        // S_j is in registers: its buffer may take the scores of tile j + 2
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bars.s_free(sb));
+        const int key0 = j * C::BN + hf * KB;
+        if (key0 + KB - 1 > row_min) {
 #pragma unroll
-            for (int c = 0; c < C::BN; ++c)
+            for (int c = 0; c < KB; ++c)
                 if (key0 + c > t) s[c] = -INFINITY;
         }
         float mx[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) mx[i] = s[i];
 #pragma unroll
-        for (int c = 8; c < C::BN; ++c) mx[c & 7] = fmaxf(mx[c & 7], s[c]);
-        const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+        for (int c = 8; c < KB; c += 2) mx[(c >> 1) & 7] = max3(mx[(c >> 1) & 7], s[c], s[c + 1]);
+        float mt = max3(max3(mx[0], mx[1], mx[2]), max3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
+        if constexpr (C::SPLIT) {
+            // the row's maximum over the whole tile (buffer j%2, so a slow partner still
+            // reading tile j-1 is never overwritten)
+            xmax[((j & 1) * 2 + hf) * C::BM + row] = mt;
+            if (!meet()) return;
+            mt = fmaxf(mt, xmax[((j & 1) * 2 + (hf ^ 1)) * C::BM + row]);
+        }
         const float m_new = fmaxf(m_ref, mt * sl2);
         const bool need = (m_new - m_ref) > C::RESCALE_THRESHOLD;
         if (j == 0) {
@@ -432,7 +478,7 @@ __device__ void run_softmax(const PrefillParams& p, const Bars& bars, uint32_t s
                 return;
             tc_fence_after();
 #pragma unroll 1
-            for (int c = 0; c < D; c += 32) {
+            for (int c = hf * OC; c < (hf + 1) * OC; c += 32) {
                 uint32_t r[32];
                 tmem_ld32(tl + C::TM_O + c, r);
 #pragma unroll
@@ -440,8 +486,9 @@ __device__ void run_softmax(const PrefillParams& p, const Bars& bars, uint32_t s
                 tmem_st32(tl + C::TM_O + c, r);
             }
         }
-        // P = exp2(s * scale * log2e - m_ref), packed bf16: written over S in TMEM, or
-        // (PSMEM) as this thread's 128-byte-swizzled row of P buffer j%2.
+        // P = exp2(s * scale * log2e - m_ref), packed bf16: into the P buffer in TMEM
+        // (this half's keys to columns [hf KB/2, hf KB/2 + KB/2)), or (PSMEM) as this
+        // thread's 128-byte-swizzled row of P buffer j%2 in shared memory.
         float rs[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
         const float mref = m_ref;
         if constexpr (C::PSMEM) {
@@ -472,18 +519,26 @@ __device__ void run_softmax(const PrefillParams& p, const Bars& bars, uint32_t s
             __syncwarp();
             if (lane == 0) mbar_arrive(bars.p_full(j & 1));
         } else {
+            uint32_t pk[KB / 2];
+            float2 rs2[4] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
+            const float2 sl2x2 = make_float2(sl2, sl2), negm = make_float2(-mref, -mref);
 #pragma unroll
-            for (int c = 0; c < C::BN; c += 64) {
-                uint32_t pk[32];
-#pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    const float p0 = ex2_approx(fmaf(s[c + 2 * e], sl2, -mref));
-                    const float p1 = ex2_approx(fmaf(s[c + 2 * e + 1], sl2, -mref));
-                    rs[e & 7] += p0 + p1;
-                    pk[e] = pack_bf16x2(p0, p1);
-                }
-                tmem_st32(tl + s_col + (c >> 1), pk);
+            for (int e = 0; e < KB / 2; ++e) {
+                const float2 x = fma2(make_float2(s[2 * e], s[2 * e + 1]), sl2x2, negm);
+                const float2 pe = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+                rs2[e & 3] = add2(rs2[e & 3], pe);
+                pk[e] = pack_bf16x2(pe.x, pe.y);
             }
+            rs[0] = rs2[0].x; rs[1] = rs2[0].y; rs[2] = rs2[1].x; rs[3] = rs2[1].y;
+            rs[4] = rs2[2].x; rs[5] = rs2[2].y; rs[6] = rs2[3].x; rs[7] = rs2[3].y;
+            // the P buffer held P_{j-1}: PV_{j-1} must have finished reading it
+            if (j >= 1 && !__all_sync(0xffffffffu, mbar_wait(bars.pv_done((j - 1) & 1), (uint32_t)((j - 1) >> 1) & 1u,
+                                                              abort_flag, p.status)))
+                return;
+            tc_fence_after();
+#pragma unroll
+            for (int c = 0; c < KB / 2; c += 32)
+                tmem_st32(tl + C::TM_P + hf * (KB / 2) + c, *reinterpret_cast<const uint32_t(*)[32]>(pk + c));
             l += ((rs[0] + rs[1]) + (rs[2] + rs[3])) + ((rs[4] + rs[5]) + (rs[6] + rs[7]));
             tmem_wait_st();
             tc_fence_before();
@@ -492,27 +547,41 @@ __device__ void run_softmax(const PrefillParams& p, const Bars& bars, uint32_t s
         }
     }
 
-    // ---- epilogue: O / l * act(gate) (additive gate: O / l + act(gate)) -> bf16 [B,S,H*d]
+    // ---- epilogue: O / l * act(gate) (additive gate: O / l + act(gate)) -> bf16, this
+    // thread's O columns, into a staging tile in the V ring (idle once every PV is
+    // done); the producer writes the tile to [B,S,H*d] with TMA stores (rows past S
+    // clipped).  A partial tile of packed sequences is stored row by row instead (a
+    // 128-row TMA store would reach into the next sequence).
+    float l_row = l;
+    if constexpr (C::SPLIT) {
+        xsum[hf * C::BM + row] = l;
+        if (!meet()) return;
+        l_row = xsum[row] + xsum[C::BM + row];
+    }
     if (!__all_sync(0xffffffffu, mbar_wait(bars.o_final(), 0, abort_flag, p.status))) return;
     const bool elementwise = GV ? gate_per_dim(p.gate_mode) : p.gate_mode == GATTN_GATE_ELEMENTWISE;
     constexpr bool plain = !GV;
     const bool additive = GV && gate_additive(p.gate_mode);
     if (elementwise && !__all_sync(0xffffffffu, mbar_wait(bars.g_full(), 0, abort_flag, p.status))) return;
     tc_fence_after();
-    const float inv_l = 1.f / l;
+    const float inv_l = 1.f / l_row;
     // out = o * gv + ga
     const float gh = additive ? inv_l : inv_l * gate_head, gha = additive ? gate_head : 0.f;
     bf16* orow = static_cast<bf16*>(p.out) + (tok * p.H + h) * D;
     const uint32_t gbase = sbase + C::OFF_K;
+    const uint32_t obase = sbase + C::OFF_V;
+    const bool direct = GV && p.vtiles && (qt + 1) * C::BM > slen;
+    auto put = [&](int col, uint32_t w0, uint32_t w1, uint32_t w2, uint32_t w3) {
+        if (!direct) sts_v4(rowtile_addr(obase, row, col), w0, w1, w2, w3);
+        else if (valid) *reinterpret_cast<uint4*>(orow + col) = make_uint4(w0, w1, w2, w3);
+    };
     // the default multiplicative sigmoid gate keeps a loop of its own (its cost is
     // the epilogue's); the variants share a second one
 #pragma unroll 1
-    for (int c = 0; c < D; c += 32) {
+    for (int c = hf * OC; c < (hf + 1) * OC; c += 32) {
         uint32_t r[32];
         __syncwarp();
         tmem_ld32(tl + C::TM_O + c, r);
-        if (!valid) continue;
-        uint4* dst = reinterpret_cast<uint4*>(orow + c);
         if constexpr (plain) {
             float gv[32];
             if (elementwise) {
@@ -521,7 +590,7 @@ __device__ void run_softmax(const PrefillParams& p, const Bars& bars, uint32_t s
                     float f[8];
                     unpack8(lds_v4(rowtile_addr(gbase, row, c + 8 * q4)), f);
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) gv[8 * q4 + e] = inv_l * sigmoidf_dev(f[e]);
+                    for (int e = 0; e < 8; ++e) gv[8 * q4 + e] = inv_l * sigmoid_tanh(f[e]);
                 }
             } else {
 #pragma unroll
@@ -535,7 +604,7 @@ __device__ void run_softmax(const PrefillParams& p, const Bars& bars, uint32_t s
                     const int e = 8 * q4 + 2 * i;
                     w[i] = pack_bf16x2(__uint_as_float(r[e]) * gv[e], __uint_as_float(r[e + 1]) * gv[e + 1]);
                 }
-                dst[q4] = make_uint4(w[0], w[1], w[2], w[3]);
+                put(c + 8 * q4, w[0], w[1], w[2], w[3]);
             }
         } else {
         float gv[32], ga[32];
@@ -546,7 +615,7 @@ __device__ void run_softmax(const PrefillParams& p, const Bars& bars, uint32_t s
                 unpack8(lds_v4(rowtile_addr(gbase, row, c + 8 * q4)), f);
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
-                    const float a = gate_act(f[e], sigmoidf_dev(f[e]), p.gate_mode);
+                    const float a = gate_act(f[e], sigmoid_tanh(f[e]), p.gate_mode);
                     gv[8 * q4 + e] = additive ? inv_l : inv_l * a;
                     ga[8 * q4 + e] = additive ? a : 0.f;
                 }
@@ -567,9 +636,14 @@ __device__ void run_softmax(const PrefillParams& p, const Bars& bars, uint32_t s
                 w[i] = pack_bf16x2(fmaf(__uint_as_float(r[e]), gv[e], ga[e]),
                                    fmaf(__uint_as_float(r[e + 1]), gv[e + 1], ga[e + 1]));
             }
-            dst[q4] = make_uint4(w[0], w[1], w[2], w[3]);
+            put(c + 8 * q4, w[0], w[1], w[2], w[3]);
         }
         }
+    }
+    if (!direct) {
+        fence_proxy_async_smem();  // the TMA stores read the staging tile through the async proxy
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bars.o_staged());
     }
 }
 
@@ -579,7 +653,7 @@ template <int D, bool GV>
 __global__ void __launch_bounds__(PfCfg<D>::THREADS, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                       const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmG,
-                      const __grid_constant__ PrefillParams p) {
+                      const __grid_constant__ CUtensorMap tmO, const __grid_constant__ PrefillParams p) {
     using C = PfCfg<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -618,12 +692,14 @@ __global__ void __launch_bounds__(PfCfg<D>::THREADS, 1)
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(bars.s_full(i), 1);
-            mbar_init(bars.s_free(i), 4);
-            mbar_init(bars.p_full(i), 4);
+            mbar_init(bars.s_free(i), C::SOFTMAX_WARPS);
+            mbar_init(bars.p_full(i), C::SOFTMAX_WARPS);
             mbar_init(bars.pv_done(i), 1);
         }
+        for (int q = 0; q < 4; ++q) mbar_init(bars.xchg(q), 2);
         mbar_init(bars.o_final(), 2);
-        mbar_init(bars.q_ready(), 4);
+        mbar_init(bars.q_ready(), C::SOFTMAX_WARPS);
+        mbar_init(bars.o_staged(), C::SOFTMAX_WARPS);
         mbar_init(bars.drain(), 2);
         mbar_init(bars.q_full(), 1);
         mbar_init(bars.g_full(), 1);
@@ -634,6 +710,7 @@ __global__ void __launch_bounds__(PfCfg<D>::THREADS, 1)
         tma_prefetch_desc(&tmQ);
         tma_prefetch_desc(&tmK);
         tma_prefetch_desc(&tmV);
+        tma_prefetch_desc(&tmO);
     }
     if (warp == 1) {
         tmem_alloc(smem_u32(tmem_slot), C::TM_COLS);
@@ -646,9 +723,10 @@ __global__ void __launch_bounds__(PfCfg<D>::THREADS, 1)
 
     if (warp == 0) {
         if (lane == 0)
-            run_producer<D>(&tmK, &tmV, &tmQ, &tmG, p.qnorm_w, bars, sbase, n_kv, b, g, h, qt, t0, p.G,
+            run_producer<D>(&tmK, &tmV, &tmQ, &tmG, &tmO, p.qnorm_w, bars, sbase, n_kv, b, g, h, qt, t0, p.G,
                             GV ? gate_per_dim(p.gate_mode) : p.gate_mode == GATTN_GATE_ELEMENTWISE,
-                            GV && gate_layout(p.gate_mode) == GATTN_GATE_HEAD_SHARED ? 0 : h, abort_flag, p.status);
+                            GV && gate_layout(p.gate_mode) == GATTN_GATE_HEAD_SHARED ? 0 : h,
+                            !(GV && p.vtiles && (qt + 1) * C::BM > slen), abort_flag, p.status);
         __syncwarp();
     } else if (warp == 1) {
         if (lane == 0) run_mma<D>(0, bars, sbase, tm, n_kv, abort_flag, p.status);
@@ -661,7 +739,8 @@ __global__ void __launch_bounds__(PfCfg<D>::THREADS, 1)
         }
         __syncwarp();
     } else {
-        run_softmax<D, GV>(p, bars, sbase, tm, warp & 3, lane, qt, t0, slen, b, h, n_kv, abort_flag);
+        run_softmax<D, GV>(p, bars, sbase, smem + C::OFF_X, tm, warp & 3, (warp - 3) >> 2, lane, qt, t0, slen, b, h,
+                           n_kv, abort_flag);
     }
     tc_fence_before();
     __syncthreads();
@@ -692,7 +771,7 @@ cudaError_t launch_d(const PrefillParams& p, const PrefillMaps& maps, cudaStream
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t err = cudaLaunchKernelEx(&cfg, kernel, maps.k, maps.v, maps.q, maps.gate, p);
+    cudaError_t err = cudaLaunchKernelEx(&cfg, kernel, maps.k, maps.v, maps.q, maps.gate, maps.out, p);
     if (ev_stop) cudaEventRecord(ev_stop, stream);
     return err;
 }
