@@ -1,6 +1,6 @@
 // prefill_tc.cu -- bf16 causal gated GQA attention on 5th-generation tensor cores.
 //
-// One CTA computes one 128-row query tile of one head:
+// A CTA computes 128-row query tiles of one head at a time:
 //   out[b, t, h*d:(h+1)*d] = sigmoid(z) * sum_{j<=t} softmax_j(q'_t . k'_j / sqrt(d)) v_j
 // where q' = rope(rmsnorm(q)), k' = rope(rmsnorm(k)) and head h reads KV group
 // g = floor(h / (H/G)).  ("Gated attention" handbook chapter, sections "The
@@ -9,13 +9,21 @@
 // scaling and stable softmax matter"; "Gated Attention" deep-dive, section
 // "门放在哪里？".)
 //
+// d <= 128: the grid is persistent (one CTA per SM at most) and walks a list of
+// work items (query tile, head, batch), heaviest tile first, in a snake over
+// rounds; ring stages, score buffers and barrier phases run on tile and item
+// counters that continue across items.  While one item finishes (last softmax,
+// PV, epilogue, output store) the next one's Q tile has landed, its prologue has
+// run and its first QK MMAs are in the tensor pipe.  d = 256 (odd H/G only): one
+// item per CTA.
+//
 // Roles (11 warps at d <= 128, 7 at d = 256):
-//   warp 0      TMA producer: the raw Q tile once, then K' tiles (keys normed and
-//               rotated by the pre-pass) and raw V tiles into 3-stage rings (128 B
-//               swizzle), K and V issued independently; at the end the gate tile.
+//   warp 0      TMA producer: per item the raw Q tile, K' tiles (keys normed and
+//               rotated by the pre-pass) and raw V tiles into 2-stage rings (128 B
+//               swizzle), the gate tile, and the TMA stores of the staged output.
 //   warps 1, 2  MMA issuers (warp 1 also owns TMEM): warp 1 + i issues S = Q'K'^T
 //               (tcgen05.mma, A read from TMEM) and O += P V of the KV tiles j
-//               with j % 2 == i.
+//               with j % 2 == i (j counting tiles over all items).
 //   warps 3..   the fused Q prologue (RMSNorm + RoPE of the raw query row, read
 //               from shared memory, written as bf16 straight into TMEM), the online
 //               softmax, and the gate epilogue.  d <= 128: 8 warps, two threads per
@@ -24,13 +32,15 @@
 //               swap their tile maxima through shared memory.  d = 256: 4 warps, one
 //               thread per row.
 //
-// Shared memory: K ring | V ring.  Before any V tile is loaded the V ring holds
-// the raw Q tile, and once every PV is done it holds the output tile staged for the
-// TMA stores; once every K tile has been consumed the K ring receives the gate
-// tile.  Every reuse is ordered by mbarriers.
+// Shared memory, d <= 128: raw Q tile | K ring | V ring | gate tile, which the
+// epilogue overwrites with the output tile staged for the TMA stores.  d = 256:
+// K ring | V ring | two P buffers; the raw Q tile sits in the V ring before any V
+// tile is loaded, the gate tile in the K ring once every K' tile is consumed, the
+// staged output in the V ring once every PV is done.  Every reuse is ordered by
+// mbarriers.
 //
 // TMEM (512 columns x 128 lanes, lane = query row):
-//   [0, d)             O accumulator, fp32
+//   [0, d)             O accumulator, fp32 (the first PV of an item overwrites it)
 //   [d, d+BN)          S buffer 0 (fp32 scores)
 //   [d+BN, d+2BN)      S buffer 1
 //   [d+2BN, d+2BN+d/2) Q' as packed bf16 pairs (A operand of S = Q'K'^T)
@@ -58,21 +68,21 @@ struct PfCfg {
     // shared memory.  d <= 128: 128-key tiles, P in a TMEM buffer of its own.
     static constexpr int BN = (D == 256) ? 64 : 128;
     static constexpr bool PSMEM = (D == 256);
-    // d <= 128: two threads per query row (8 softmax warps), each owning half of the
-    // row's keys in every tile and half of O's columns
+    // d <= 128: persistent CTAs with their own raw-Q and gate/output buffers, and two
+    // threads per query row (8 softmax warps), each owning half of the row's keys
+    // in every tile and half of O's columns
+    static constexpr bool PERSIST = !PSMEM;
     static constexpr bool SPLIT = !PSMEM;
     static constexpr int SOFTMAX_WARPS = SPLIT ? 8 : 4;
     static constexpr int NSB = 2;  // score buffers in TMEM: tile j uses buffer j % 2
     static constexpr int NPB = PSMEM ? 2 : 0;  // P buffers in shared memory
-    static constexpr int NSK = 3;  // K ring stages
-    static constexpr int NSV = 3;  // V ring stages
+    static constexpr int NSK = PERSIST ? 2 : 3;  // K ring stages
+    static constexpr int NSV = PERSIST ? 2 : 3;  // V ring stages
     static constexpr int KCH = D / 64;               // 128-byte chunks along head_dim
     static constexpr int CHUNK_BYTES = BN * 128;     // one K/V TMA box: BN rows x 64 bf16
     static constexpr int TILE_BYTES = BN * D * 2;
-    static constexpr int ROWBOX_BYTES = BM * 128;    // one Q/gate TMA box: 128 rows x 64 bf16
+    static constexpr int ROWBOX_BYTES = BM * 128;    // one Q/gate/output TMA box: 128 rows x 64 bf16
     static constexpr int QTILE_BYTES = BM * D * 2;
-    static_assert(QTILE_BYTES <= NSV * TILE_BYTES && QTILE_BYTES <= NSK * TILE_BYTES,
-                  "raw Q and gate tiles must fit the V and K rings");
     static constexpr int P_BUF_BYTES = PSMEM ? BM * BN * 2 : 0;  // [BN/64 chunks][128 rows][128 B]
     static constexpr int TM_O = 0;
     static constexpr int TM_S = D;                   // score buffer b at TM_S + b * BN
@@ -82,11 +92,19 @@ struct PfCfg {
     static constexpr int TM_P = TM_Q + D / 2;
     static constexpr int TM_COLS = 512;
     static_assert(TM_Q + D / 2 <= TM_COLS && (PSMEM || TM_P + BN / 2 <= TM_COLS), "TMEM budget");
-    static constexpr int OFF_K = 0;
-    static constexpr int OFF_V = NSK * TILE_BYTES;
-    static constexpr int OFF_P = OFF_V + NSV * TILE_BYTES;
+    static constexpr int OFF_QB = 0;                                  // raw Q tile (PERSIST)
+    static constexpr int OFF_K = PERSIST ? QTILE_BYTES : 0;
+    static constexpr int OFF_V = OFF_K + NSK * TILE_BYTES;
+    static constexpr int OFF_GB = OFF_V + NSV * TILE_BYTES;           // gate / output tile (PERSIST)
+    static constexpr int OFF_P = OFF_GB + (PERSIST ? QTILE_BYTES : 0);
     static constexpr int OFF_BAR = OFF_P + NPB * P_BUF_BYTES;
-    static constexpr int NBAR = 2 * NSK + 2 * NSV + 18;
+    // where the raw Q tile, the gate tile and the staged output live
+    static constexpr int OFF_Q = PERSIST ? OFF_QB : OFF_V;
+    static constexpr int OFF_G = PERSIST ? OFF_GB : OFF_K;
+    static constexpr int OFF_OUT = PERSIST ? OFF_GB : OFF_V;
+    static_assert(PERSIST || (QTILE_BYTES <= NSV * TILE_BYTES && QTILE_BYTES <= NSK * TILE_BYTES),
+                  "raw Q, gate and output tiles must fit the rings they borrow");
+    static constexpr int NBAR = 2 * NSK + 2 * NSV + 19;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr int OFF_W = (OFF_MISC + 16 + 127) & ~127;  // qnorm weights, D bf16
     static constexpr int OFF_X = OFF_W + D * 2;                  // row-half exchange (SPLIT)
@@ -114,110 +132,209 @@ struct Bars {
     __device__ uint32_t s_free(int i) const { return at(r() + 2 + i); }    // S of a tile read out of buffer i
     __device__ uint32_t p_full(int i) const { return at(r() + 4 + i); }    // P_j ready, j % 2 == i
     __device__ uint32_t pv_done(int i) const { return at(r() + 6 + i); }   // PV_j complete, j % 2 == i
-    __device__ uint32_t o_final() const { return at(r() + 8); }
-    __device__ uint32_t q_ready() const { return at(r() + 9); }   // Q' in TMEM, raw Q no longer read
+    __device__ uint32_t o_final() const { return at(r() + 8); }   // every PV of an item complete
+    __device__ uint32_t q_ready() const { return at(r() + 9); }   // an item's Q' in TMEM, its raw Q no longer read
     __device__ uint32_t drain() const { return at(r() + 10); }
-    __device__ uint32_t q_full() const { return at(r() + 11); }   // raw Q tile landed
-    __device__ uint32_t g_full() const { return at(r() + 12); }   // gate tile landed
+    __device__ uint32_t q_full() const { return at(r() + 11); }   // an item's raw Q tile landed
+    __device__ uint32_t g_full() const { return at(r() + 12); }   // an item's gate tile landed / output buffer free
     __device__ uint32_t xchg(int q) const { return at(r() + 13 + q); }  // both halves of row quarter q posted
-    __device__ uint32_t o_staged() const { return at(r() + 17); }         // every softmax warp staged its output
+    __device__ uint32_t o_staged() const { return at(r() + 17); }  // every softmax warp staged an item's output
+    __device__ uint32_t o_free() const { return at(r() + 18); }    // an item's epilogue has read O
 };
+
+// ----------------------------------------------------------------- work items
+
+// Work item u: query tile n_qtiles - 1 - u / (B*H) (heaviest first) of batch and
+// head u % (B*H), heads of one KV group adjacent (their CTAs share K/V tiles in
+// L2); packed sequences: tile u / H of the table (also heaviest first), head u % H.
+// CTA c of n takes items c, 2n - 1 - c, 2n + c, ... (a snake over rounds, so that
+// heavy and light tiles share a CTA).
+struct TcItem {
+    int qt, b, h, n_kv;
+    int t0, len;  // the sequence's first token on the S axis of batch b, and its length
+    bool direct;  // a partial tile of packed sequences: rows are stored one by one
+};
+
+template <int D, bool GV>
+__device__ __forceinline__ bool tc_item(const PrefillParams& p, int c, int n, int r, TcItem& it) {
+    using C = PfCfg<D>;
+    const long long u = (long long)r * n + ((r & 1) ? n - 1 - c : c);
+    if (GV && p.vtiles) {
+        if (u >= (long long)p.n_vtiles * p.H) return false;
+        const int4 e = p.vtiles[u / p.H];
+        it.qt = e.z;
+        it.t0 = e.x;
+        it.len = e.y;
+        it.b = 0;
+        it.h = (int)(u % p.H);
+        it.direct = (it.qt + 1) * C::BM > it.len;  // a TMA store of 128 rows would reach the next sequence
+    } else {
+        const long long bh_count = (long long)p.B * p.H;
+        if (u >= (long long)p.n_qtiles * bh_count) return false;
+        it.qt = p.n_qtiles - 1 - (int)(u / bh_count);
+        const int bh = (int)(u % bh_count);
+        it.b = bh / p.H;
+        it.h = bh % p.H;
+        it.t0 = 0;
+        it.len = p.S;
+        it.direct = false;
+    }
+    it.n_kv = (min(it.len, (it.qt + 1) * C::BM) + C::BN - 1) / C::BN;
+    return true;
+}
 
 // ----------------------------------------------------------------- producer
 
-template <int D>
+template <int D, bool GV>
 __device__ void run_producer(const CUtensorMap* tmK, const CUtensorMap* tmV, const CUtensorMap* tmQ,
-                             const CUtensorMap* tmG, const CUtensorMap* tmO, const void* qnorm_w, const Bars& bars,
-                             uint32_t sbase, int n_kv, int b, int g, int h, int qt, int row0, int G, bool gate_tile,
-                             int gate_h, bool store_tile, volatile int* abort_flag, unsigned int* status) {
+                             const CUtensorMap* tmG, const CUtensorMap* tmO, const PrefillParams& p, const Bars& bars,
+                             uint32_t sbase, int cta, int ncta, volatile int* abort_flag, unsigned int* status) {
     using C = PfCfg<D>;
-    // raw Q tile into the (still unused) V ring, the q norm weights next to it
-    mbar_arrive_expect_tx(bars.q_full(), C::QTILE_BYTES + D * 2);
-    bulk_load(sbase + C::OFF_W, qnorm_w, D * 2, bars.q_full());
-#pragma unroll
-    for (int c = 0; c < C::KCH; ++c)
-        tma_load_4d(sbase + C::OFF_V + c * C::ROWBOX_BYTES, tmQ, bars.q_full(), c * 64, h, row0 + qt * C::BM, b);
-
-    // K' is written by the pre-pass kernel just before this one (programmatic
-    // dependent launch): wait for it to finish before the first K' load.
-    pdl_wait_prerequisites();
-
-    // K and V tiles, each stream as soon as its own stage frees up
-    int nk = 0, nv = 0;
-    bool v_open = false;  // the V ring is free once the raw Q tile has been read
-    const unsigned long long t0 = global_timer_ns();
-    uint32_t spins = 0;
-    while (nk < n_kv || nv < n_kv) {
-        bool progressed = false;
-        if (nk < n_kv &&
-            (nk < C::NSK || mbar_test_wait(bars.k_empty(nk % C::NSK), ((uint32_t)(nk / C::NSK) & 1u) ^ 1u))) {
-            const int st = nk % C::NSK;
-            mbar_arrive_expect_tx(bars.k_full(st), C::TILE_BYTES);
-            const uint32_t kdst = sbase + C::OFF_K + st * C::TILE_BYTES;
-#pragma unroll
-            for (int c = 0; c < C::KCH; ++c)
-                tma_load_3d(kdst + c * C::CHUNK_BYTES, tmK, bars.k_full(st), c * 64, row0 + nk * C::BN, b * G + g);
-            ++nk;
-            progressed = true;
-        }
-        if (!v_open) v_open = mbar_test_wait(bars.q_ready(), 0);
-        if (v_open && nv < n_kv &&
-            (nv < C::NSV || mbar_test_wait(bars.v_empty(nv % C::NSV), ((uint32_t)(nv / C::NSV) & 1u) ^ 1u))) {
-            const int st = nv % C::NSV;
-            mbar_arrive_expect_tx(bars.v_full(st), C::TILE_BYTES);
-            const uint32_t vdst = sbase + C::OFF_V + st * C::TILE_BYTES;
-#pragma unroll
-            for (int c = 0; c < C::KCH; ++c)
-                tma_load_4d(vdst + c * C::CHUNK_BYTES, tmV, bars.v_full(st), c * 64, g, row0 + nv * C::BN, b);
-            ++nv;
-            progressed = true;
-        }
-        if (progressed) {
-            spins = 0;
-            continue;
-        }
-        if ((++spins & 63u) == 0) {
-            if (*abort_flag) break;
-            if (global_timer_ns() - t0 > 4 * kWaitLimitNs) {
-                *abort_flag = 1;
-                atomicOr(status, GATTN_DEVICE_TIMEOUT);
-                break;
-            }
-        }
-    }
-    // gate tile into the K ring once every K stage has been consumed for the last time
-    bool g_issued = false;
-    if (gate_tile && nk == n_kv) {
-        bool ok = true;
-        for (int j = n_kv > C::NSK ? n_kv - C::NSK : 0; ok && j < n_kv; ++j)
-            ok = mbar_wait(bars.k_empty(j % C::NSK), (uint32_t)(j / C::NSK) & 1u, abort_flag, status);
-        if (ok) {
+    // a gate tile per item when the logits vary over head_dim (elementwise, or one
+    // head-shared vector per token: the gate map then has a single head)
+    const bool gate_tile = GV ? gate_per_dim(p.gate_mode) : p.gate_mode == GATTN_GATE_ELEMENTWISE;
+    const bool shared = GV && gate_layout(p.gate_mode) == GATTN_GATE_HEAD_SHARED;
+    int nk = 0, nv = 0;  // K' / V tiles issued, over all items
+    int jb = 0;          // tiles of the items before the current one
+    int n_it = 0;
+    int q_last = -1, g_last = -1;  // the items whose raw Q / gate tile copies were issued last
+    bool ok = true;
+    TcItem it, prev;
+    auto row0_of = [&](const TcItem& x) { return x.t0 + x.qt * C::BM; };
+    // an item's gate tile into the gate/output buffer, or (no gate tile) just the
+    // news that the buffer is free for the item's staged output
+    auto gate_in = [&](const TcItem& x) {
+        if (gate_tile) {
             mbar_arrive_expect_tx(bars.g_full(), C::QTILE_BYTES);
 #pragma unroll
             for (int c = 0; c < C::KCH; ++c)
-                tma_load_4d(sbase + C::OFF_K + c * C::ROWBOX_BYTES, tmG, bars.g_full(), c * 64, gate_h,
-                            row0 + qt * C::BM, b);
-            g_issued = true;
+                tma_load_4d(sbase + C::OFF_G + c * C::ROWBOX_BYTES, tmG, bars.g_full(), c * 64, shared ? 0 : x.h,
+                            row0_of(x), x.b);
+            g_last = n_it;
+        } else {
+            mbar_arrive(bars.g_full());
         }
+    };
+    // an item's output, staged by the softmax warps: TMA stores (rows past S clipped),
+    // then wait until the copies have read shared memory (a partial tile of packed
+    // sequences was stored row by row instead)
+    auto store_out = [&](const TcItem& x) {
+        if (x.direct) return;
+#pragma unroll
+        for (int c = 0; c < C::KCH; ++c)
+            tma_store_4d(tmO, sbase + C::OFF_OUT + c * C::ROWBOX_BYTES, c * 64, x.h, row0_of(x), x.b);
+        bulk_commit_group();
+        bulk_wait_group_read0();
+    };
+
+    for (int r = 0; ok && tc_item<D, GV>(p, cta, ncta, r, it); ++r, ++n_it) {
+        const int g = it.h / (p.H / p.G);
+        // raw Q tile: its buffer is free once the previous item's prologue has read it
+        if (C::PERSIST && n_it > 0 && !(ok = mbar_wait(bars.q_ready(), (uint32_t)(n_it - 1) & 1u, abort_flag, status)))
+            break;
+        mbar_arrive_expect_tx(bars.q_full(), C::QTILE_BYTES + (n_it == 0 ? D * 2 : 0));
+        if (n_it == 0) bulk_load(sbase + C::OFF_W, p.qnorm_w, D * 2, bars.q_full());
+#pragma unroll
+        for (int c = 0; c < C::KCH; ++c)
+            tma_load_4d(sbase + C::OFF_Q + c * C::ROWBOX_BYTES, tmQ, bars.q_full(), c * 64, it.h, row0_of(it), it.b);
+        q_last = n_it;
+        // the gate tile is read at the very end of the item: start it on its way to L2 now
+        if (gate_tile) {
+#pragma unroll
+            for (int c = 0; c < C::KCH; ++c)
+                tma_prefetch_l2_4d(tmG, c * 64, shared ? 0 : it.h, row0_of(it), it.b);
+        }
+        // K' is written by the pre-pass kernel just before this one (programmatic
+        // dependent launch): wait for it to finish before the first K' load.
+        if (n_it == 0) pdl_wait_prerequisites();
+        // Persistent: the first item's gate goes straight in; later ones once the
+        // previous item's output has been stored.  One item per CTA: the gate tile
+        // borrows the K ring after the last K' tile (below), and the V tiles wait
+        // until the prologue has read the raw Q tile out of the V ring.
+        bool g_done = !C::PERSIST;
+        if (C::PERSIST && n_it == 0) {
+            gate_in(it);
+            g_done = true;
+        }
+        bool v_open = C::PERSIST;
+        const int ke = nk + it.n_kv, ve = nv + it.n_kv;
+        const unsigned long long t0 = global_timer_ns();
+        uint32_t spins = 0;
+        while (nk < ke || nv < ve) {
+            bool progressed = false;
+            if (!g_done && mbar_test_wait(bars.o_staged(), (uint32_t)(n_it - 1) & 1u)) {
+                store_out(prev);
+                gate_in(it);
+                g_done = progressed = true;
+            }
+            if (nk < ke &&
+                (nk < C::NSK || mbar_test_wait(bars.k_empty(nk % C::NSK), ((uint32_t)(nk / C::NSK) & 1u) ^ 1u))) {
+                const int st = nk % C::NSK;
+                mbar_arrive_expect_tx(bars.k_full(st), C::TILE_BYTES);
+                const uint32_t kdst = sbase + C::OFF_K + st * C::TILE_BYTES;
+#pragma unroll
+                for (int c = 0; c < C::KCH; ++c)
+                    tma_load_3d(kdst + c * C::CHUNK_BYTES, tmK, bars.k_full(st), c * 64, it.t0 + (nk - jb) * C::BN,
+                                it.b * p.G + g);
+                ++nk;
+                progressed = true;
+            }
+            if (!v_open) v_open = mbar_test_wait(bars.q_ready(), 0);
+            if (v_open && nv < ve &&
+                (nv < C::NSV || mbar_test_wait(bars.v_empty(nv % C::NSV), ((uint32_t)(nv / C::NSV) & 1u) ^ 1u))) {
+                const int st = nv % C::NSV;
+                mbar_arrive_expect_tx(bars.v_full(st), C::TILE_BYTES);
+                const uint32_t vdst = sbase + C::OFF_V + st * C::TILE_BYTES;
+#pragma unroll
+                for (int c = 0; c < C::KCH; ++c)
+                    tma_load_4d(vdst + c * C::CHUNK_BYTES, tmV, bars.v_full(st), c * 64, g, it.t0 + (nv - jb) * C::BN,
+                                it.b);
+                ++nv;
+                progressed = true;
+            }
+            if (progressed) {
+                spins = 0;
+                continue;
+            }
+            if ((++spins & 63u) == 0) {
+                if (*abort_flag) break;
+                if (global_timer_ns() - t0 > 4 * kWaitLimitNs) {
+                    *abort_flag = 1;
+                    atomicOr(status, GATTN_DEVICE_TIMEOUT);
+                    break;
+                }
+            }
+        }
+        if (nk != ke || nv != ve) {
+            ok = false;
+            break;
+        }
+        if (!g_done) {  // persistent: the previous output has not been staged yet
+            if (!(ok = mbar_wait(bars.o_staged(), (uint32_t)(n_it - 1) & 1u, abort_flag, status))) break;
+            store_out(prev);
+            gate_in(it);
+        }
+        if (!C::PERSIST && gate_tile) {
+            // one item per CTA: the gate tile goes into the K ring once every K' stage
+            // has been consumed for the last time
+            for (int j = ke > C::NSK ? ke - C::NSK : 0; ok && j < ke; ++j)
+                ok = mbar_wait(bars.k_empty(j % C::NSK), (uint32_t)(j / C::NSK) & 1u, abort_flag, status);
+            if (!ok) break;
+            gate_in(it);
+        }
+        jb = ke;
+        prev = it;
     }
+    // the last item's output
+    if (ok && n_it > 0 && mbar_wait(bars.o_staged(), (uint32_t)(n_it - 1) & 1u, abort_flag, status)) store_out(prev);
+    bulk_wait_group0();
     // Drain: every copy this thread started must land before the CTA can exit.
-    mbar_wait_drain(bars.q_full(), 0, status);
+    if (q_last >= 0) mbar_wait_drain(bars.q_full(), (uint32_t)q_last & 1u, status);
     for (int j = nk > C::NSK ? nk - C::NSK : 0; j < nk; ++j)
         mbar_wait_drain(bars.k_full(j % C::NSK), (uint32_t)(j / C::NSK) & 1u, status);
     for (int j = nv > C::NSV ? nv - C::NSV : 0; j < nv; ++j)
         mbar_wait_drain(bars.v_full(j % C::NSV), (uint32_t)(j / C::NSV) & 1u, status);
-    if (g_issued) mbar_wait_drain(bars.g_full(), 0, status);
-    // the softmax warps staged the output tile in the V ring: write it out and wait
-    // for the copies to complete before the CTA's shared memory goes away
-    if (store_tile) {
-        if (mbar_wait(bars.o_staged(), 0, abort_flag, status)) {
-#pragma unroll
-            for (int c = 0; c < C::KCH; ++c)
-                tma_store_4d(tmO, sbase + C::OFF_V + c * C::ROWBOX_BYTES, c * 64, h, row0 + qt * C::BM, b);
-            bulk_commit_group();
-        }
-        bulk_wait_group0();
-    }
+    if (g_last >= 0) mbar_wait_drain(bars.g_full(), (uint32_t)g_last & 1u, status);
 }
 
 // ----------------------------------------------------------------- MMA issuer
@@ -226,9 +343,9 @@ __device__ void run_producer(const CUtensorMap* tmK, const CUtensorMap* tmV, con
 // ~54 cycles whatever its size (measured on GB300), which at d = 256 (D/16 narrow
 // QK^T MMAs per 64-key tile) is slower than the tensor pipe executes them.  So
 // there is one issuer per tile parity: issuer i issues QK^T and PV of the tiles j
-// with j % 2 == i, each issuing half the MMAs; their MMAs interleave freely in the
-// pipe.  PV_j waits for PV_{j-1} to complete, so O sums the tiles in the same
-// order on every run (the result is deterministic).
+// with j % 2 == i (j counting tiles over all items), each issuing half the MMAs;
+// their MMAs interleave freely in the pipe.  PV_j waits for PV_{j-1} to complete,
+// so O sums the tiles in the same order on every run (the result is deterministic).
 template <int D>
 __device__ __forceinline__ bool issue_qk(int j, const Bars& bars, uint32_t tm, uint64_t kdesc0,
                                          volatile int* abort_flag, unsigned int* status) {
@@ -251,15 +368,18 @@ __device__ __forceinline__ bool issue_qk(int j, const Bars& bars, uint32_t tm, u
     return true;
 }
 
+// PV_j; the first tile of an item (first) overwrites O, once the previous item's
+// epilogue (item n_it - 1) has read it
 template <int D>
-__device__ __forceinline__ bool issue_pv(int j, const Bars& bars, uint32_t tm, uint64_t vdesc0, uint64_t pdesc0,
-                                         volatile int* abort_flag, unsigned int* status) {
+__device__ __forceinline__ bool issue_pv(int j, bool first, int n_it, const Bars& bars, uint32_t tm, uint64_t vdesc0,
+                                         uint64_t pdesc0, volatile int* abort_flag, unsigned int* status) {
     using C = PfCfg<D>;
     if (!mbar_wait(bars.p_full(j & 1), (uint32_t)(j >> 1) & 1u, abort_flag, status)) return false;
     // O accumulates the PVs in tile order, run after run: PV_j starts once the
     // other issuer's PV_{j-1} has completed (its QKs keep the pipe busy meanwhile).
     if (j >= 1 && !mbar_wait(bars.pv_done((j - 1) & 1), (uint32_t)((j - 1) >> 1) & 1u, abort_flag, status))
         return false;
+    if (first && n_it > 0 && !mbar_wait(bars.o_free(), (uint32_t)(n_it - 1) & 1u, abort_flag, status)) return false;
     tc_fence_after();
     const int st = j % C::NSV;
     if (!mbar_wait(bars.v_full(st), (uint32_t)(j / C::NSV) & 1u, abort_flag, status)) return false;
@@ -270,34 +390,44 @@ __device__ __forceinline__ bool issue_pv(int j, const Bars& bars, uint32_t tm, u
 #pragma unroll
         for (int kk = 0; kk < C::BN / 16; ++kk)
             mma_ss(tm + C::TM_O, pd + (uint64_t)(((kk >> 2) * (C::BM * 128) + (kk & 3) * 32) >> 4),
-                   vd + (uint64_t)((kk * 16 * 128) >> 4), C::IDESC_PV, 1u);
+                   vd + (uint64_t)((kk * 16 * 128) >> 4), C::IDESC_PV, (first && kk == 0) ? 0u : 1u);
     } else {
 #pragma unroll
         for (int kk = 0; kk < C::BN / 16; ++kk)
-            mma_ts(tm + C::TM_O, tm + C::TM_P + kk * 8, vd + (uint64_t)((kk * 16 * 128) >> 4), C::IDESC_PV, 1u);
+            mma_ts(tm + C::TM_O, tm + C::TM_P + kk * 8, vd + (uint64_t)((kk * 16 * 128) >> 4), C::IDESC_PV,
+                   (first && kk == 0) ? 0u : 1u);
     }
     tc_commit(bars.v_empty(st));
     tc_commit(bars.pv_done(j & 1));
     return true;
 }
 
-template <int D>
-__device__ void run_mma(int parity, const Bars& bars, uint32_t sbase, uint32_t tm, int n_kv,
-                        volatile int* abort_flag, unsigned int* status) {
+template <int D, bool GV>
+__device__ void run_mma(int parity, const PrefillParams& p, const Bars& bars, uint32_t sbase, uint32_t tm, int cta,
+                        int ncta, volatile int* abort_flag, unsigned int* status) {
     using C = PfCfg<D>;
-    bool ok = mbar_wait(bars.q_ready(), 0, abort_flag, status);  // Q' in TMEM, O zeroed
-    tc_fence_after();
     const uint64_t kdesc0 = make_sdesc_sw128(sbase + C::OFF_K, 16, 1024);
     const uint64_t vdesc0 = make_sdesc_sw128(sbase + C::OFF_V, C::CHUNK_BYTES, 1024);
     const uint64_t pdesc0 = make_sdesc_sw128(sbase + C::OFF_P, 16, 1024);
-    // QK of the next own tile goes out as soon as its score buffer is free, ahead of
-    // the PV that is still waiting for its P.
-    if (ok && parity < n_kv) ok = issue_qk<D>(parity, bars, tm, kdesc0, abort_flag, status);
-    for (int j = parity; ok && j < n_kv; j += 2) {
-        if (j + 2 < n_kv && !issue_qk<D>(j + 2, bars, tm, kdesc0, abort_flag, status)) { ok = false; break; }
-        if (!issue_pv<D>(j, bars, tm, vdesc0, pdesc0, abort_flag, status)) { ok = false; break; }
+    bool ok = true;
+    int jb = 0, n_it = 0;
+    TcItem it;
+    for (int r = 0; ok && tc_item<D, GV>(p, cta, ncta, r, it); ++r, ++n_it) {
+        const int je = jb + it.n_kv;
+        // the item's Q' is in TMEM
+        if (!(ok = mbar_wait(bars.q_ready(), (uint32_t)n_it & 1u, abort_flag, status))) break;
+        tc_fence_after();
+        // QK of this issuer's next tile goes out as soon as its score buffer is free,
+        // ahead of the PV that is still waiting for its P
+        const int j0 = jb + ((jb & 1) != parity ? 1 : 0);
+        if (j0 < je) ok = issue_qk<D>(j0, bars, tm, kdesc0, abort_flag, status);
+        for (int j = j0; ok && j < je; j += 2) {
+            if (j + 2 < je && !issue_qk<D>(j + 2, bars, tm, kdesc0, abort_flag, status)) { ok = false; break; }
+            if (!issue_pv<D>(j, j == jb, n_it, bars, tm, vdesc0, pdesc0, abort_flag, status)) { ok = false; break; }
+        }
+        if (ok) tc_commit(bars.o_final());  // count 2: both issuers' PVs of the item complete
+        jb = je;
     }
-    if (ok) tc_commit(bars.o_final());  // count 2: both issuers' PVs complete
     tc_commit(bars.drain());
 }
 
@@ -309,8 +439,7 @@ __device__ void run_mma(int parity, const Bars& bars, uint32_t sbase, uint32_t t
 // compiles exactly as it would alone.
 template <int D, bool GV>
 __device__ void run_softmax(const PrefillParams& p, const Bars& bars, uint32_t sbase, uint8_t* smem_x, uint32_t tm,
-                            int quarter, int hf, int lane, int qt, int t0, int slen, int b, int h, int n_kv,
-                            volatile int* abort_flag) {
+                            int quarter, int hf, int lane, int cta, int ncta, volatile int* abort_flag) {
     using C = PfCfg<D>;
     constexpr int NH = C::SPLIT ? 2 : 1;  // threads per query row
     constexpr int KB = C::BN / NH;        // keys of every tile owned by this thread: [hf KB, hf KB + KB)
@@ -318,18 +447,9 @@ __device__ void run_softmax(const PrefillParams& p, const Bars& bars, uint32_t s
     const int row = quarter * 32 + lane;
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     const uint32_t tl = tm + lane_off;
-    const int t = qt * C::BM + row;
-    const bool valid = t < slen;  // t counts from the start of the sequence
-    const int64_t tok = (int64_t)b * p.S + t0 + (valid ? t : 0);
-    const bf16* grow = static_cast<const bf16*>(p.gate) + tok * p.gate_tok_stride + (int64_t)h * p.gate_head_stride;
-    float gate_head = 1.f;  // the activation of a headwise logit
-    if ((GV ? gate_layout(p.gate_mode) : p.gate_mode) == GATTN_GATE_HEADWISE && valid) {
-        const float z = __bfloat162float(grow[0]);
-        gate_head = GV ? gate_act(z, sigmoid_tanh(z), p.gate_mode) : sigmoid_tanh(z);
-    }
     // With two threads per row (warps w and w + 4 share the row's TMEM lanes) the
     // halves swap values through shared memory and then meet on an mbarrier (one
-    // phase per use: the prologue, every tile and the epilogue).
+    // phase per use: every prologue, tile and epilogue).
     float* xmax = reinterpret_cast<float*>(smem_x);  // [2][2][BM] tile maxima
     float* xsum = xmax + 2 * 2 * C::BM;              // [2][BM] row sums
     float* xss = xsum + 2 * C::BM;                   // [2][BM] sums of squares of q
@@ -341,14 +461,18 @@ __device__ void run_softmax(const PrefillParams& p, const Bars& bars, uint32_t s
         return __all_sync(0xffffffffu, mbar_wait(xbar, (uint32_t)(xphase++) & 1u, abort_flag, p.status));
     };
 
-    // ---- fused Q prologue: rmsnorm then partial rotate-half RoPE, bf16 into TMEM.
-    // The raw row is read from the Q tile the producer placed in the V ring
-    // (rows past the sequence end were zero-filled by TMA).  Split rows: each half
-    // sums the squares of its columns, and the 8-column chunks (a rotated pair
-    // (i, i + rd/2) going with the chunk of i) are shared out alternately.
-    if (!__all_sync(0xffffffffu, mbar_wait(bars.q_full(), 0, abort_flag, p.status))) return;
-    {
-        const uint32_t qbase = sbase + C::OFF_V;
+    // ---- fused Q prologue of item k: rmsnorm then partial rotate-half RoPE, bf16
+    // into TMEM.  The raw row is read from the item's Q tile (rows past the sequence
+    // end were zero-filled by TMA).  Split rows: each half sums the squares of its
+    // columns, and the 8-column chunks (a rotated pair (i, i + rd/2) going with the
+    // chunk of i) are shared out alternately.  Q' of the previous item is no longer
+    // read: the softmax has seen the scores of its last tile.
+    auto prologue = [&](const TcItem& it, int k) -> bool {
+        const int t = it.qt * C::BM + row;  // from the start of the sequence
+        const bool valid = t < it.len;
+        const int64_t tok = (int64_t)it.b * p.S + it.t0 + (valid ? t : 0);
+        if (!__all_sync(0xffffffffu, mbar_wait(bars.q_full(), (uint32_t)k & 1u, abort_flag, p.status))) return false;
+        const uint32_t qbase = sbase + C::OFF_Q;
         const uint32_t wbase = sbase + C::OFF_W;
         float ss[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -361,7 +485,7 @@ __device__ void run_softmax(const PrefillParams& p, const Bars& bars, uint32_t s
         float sq = (ss[0] + ss[1]) + (ss[2] + ss[3]);
         if constexpr (C::SPLIT) {
             xss[hf * C::BM + row] = sq;
-            if (!meet()) return;
+            if (!meet()) return false;
             sq = xss[row] + xss[C::BM + row];
         }
         const float rinv = rsqrtf(sq / (float)D + p.eps);
@@ -398,252 +522,285 @@ __device__ void run_softmax(const PrefillParams& p, const Bars& bars, uint32_t s
                      pack_bf16x2(x[4] * w[4] * rinv, x[5] * w[5] * rinv),
                      pack_bf16x2(x[6] * w[6] * rinv, x[7] * w[7] * rinv));
         }
-        // O starts at zero and every PV accumulates into it
-        {
-            uint32_t z[32];
-#pragma unroll
-            for (int e = 0; e < 32; ++e) z[e] = 0u;
-#pragma unroll
-            for (int c = 0; c < OC; c += 32) tmem_st32(tl + C::TM_O + hf * OC + c, z);
-        }
-        fence_proxy_async_smem();  // our reads of the V ring happen before the V tiles overwrite it
+        fence_proxy_async_smem();  // our reads of the raw Q tile happen before the next copy overwrites it
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bars.q_ready());
-    }
+        return true;
+    };
 
-    // ---- main loop: online softmax over the KV tiles this query tile can see
     const float sl2 = p.scale_log2;
-    const int row_min = qt * C::BM;
-    float m_ref = -INFINITY;  // reference max (log2 domain) shared by O and l (and by both halves of a row)
-    float l = 0.f;            // this thread's share of the row sum
-    for (int j = 0; j < n_kv; ++j) {
-        const int sb = j % C::NSB;
-        const uint32_t s_col = C::TM_S + sb * C::BN;
-        if (!__all_sync(0xffffffffu, mbar_wait(bars.s_full(sb), (uint32_t)(j / C::NSB) & 1u, abort_flag, p.status)))
+    int jb = 0, n_it = 0;
+    TcItem item, next;
+    bool have = tc_item<D, GV>(p, cta, ncta, 0, item);
+    if (have && !prologue(item, 0)) return;
+    for (int r = 0; have; ++r, ++n_it) {
+        const int qt = item.qt, b = item.b, h = item.h, n_kv = item.n_kv;
+        const int t = qt * C::BM + row;  // from the start of the sequence
+        const bool valid = t < item.len;
+        const int64_t tok = (int64_t)b * p.S + item.t0 + (valid ? t : 0);
+        float gate_head = 1.f;  // the activation of a headwise logit
+        if ((GV ? gate_layout(p.gate_mode) : p.gate_mode) == GATTN_GATE_HEADWISE && valid) {
+            const bf16* grow =
+                static_cast<const bf16*>(p.gate) + tok * p.gate_tok_stride + (int64_t)h * p.gate_head_stride;
+            const float z = __bfloat162float(grow[0]);
+            gate_head = GV ? gate_act(z, sigmoid_tanh(z), p.gate_mode) : sigmoid_tanh(z);
+        }
+
+        // ---- main loop: online softmax over the KV tiles this query tile can see
+        const int row_min = qt * C::BM;
+        float m_ref = -INFINITY;  // reference max (log2 domain) shared by O and l (and by both halves of a row)
+        float l = 0.f;            // this thread's share of the row sum
+        for (int j = 0; j < n_kv; ++j) {
+            const int jg = jb + j;  // tile counter over all items: buffers and phases
+            const int sb = jg & 1;
+            const uint32_t s_col = C::TM_S + sb * C::BN;
+            if (!__all_sync(0xffffffffu, mbar_wait(bars.s_full(sb), (uint32_t)(jg >> 1) & 1u, abort_flag, p.status)))
+                return;
+            tc_fence_after();
+            float s[KB];
+            {
+                uint32_t rr[64];
+#pragma unroll
+                for (int c = 0; c < KB; c += 64) {
+                    tmem_ld64(tl + s_col + hf * KB + c, rr);
+#pragma unroll
+                    for (int e = 0; e < 64; ++e) s[c + e] = __uint_as_float(rr[e]);
+                }
+            }
+            // S_j is in registers: its buffer may take the scores of tile j + 2
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bars.s_free(sb));
+            const int key0 = j * C::BN + hf * KB;
+            if (key0 + KB - 1 > row_min) {
+#pragma unroll
+                for (int c = 0; c < KB; ++c)
+                    if (key0 + c > t) s[c] = -INFINITY;
+            }
+            float mx[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) mx[i] = s[i];
+#pragma unroll
+            for (int c = 8; c < KB; c += 2) mx[(c >> 1) & 7] = max3(mx[(c >> 1) & 7], s[c], s[c + 1]);
+            float mt = max3(max3(mx[0], mx[1], mx[2]), max3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
+            if constexpr (C::SPLIT) {
+                // the row's maximum over the whole tile (buffer jg%2, so a slow partner
+                // still reading tile jg-1 is never overwritten)
+                xmax[((jg & 1) * 2 + hf) * C::BM + row] = mt;
+                if (!meet()) return;
+                mt = fmaxf(mt, xmax[((jg & 1) * 2 + (hf ^ 1)) * C::BM + row]);
+            }
+            const float m_new = fmaxf(m_ref, mt * sl2);
+            const bool need = (m_new - m_ref) > C::RESCALE_THRESHOLD;
+            if (j == 0) {
+                m_ref = m_new;
+            } else if (__any_sync(0xffffffffu, need)) {
+                const float alpha = need ? ex2_approx(m_ref - m_new) : 1.f;
+                if (need) {
+                    l *= alpha;
+                    m_ref = m_new;
+                }
+                __syncwarp();
+                // O is only touched once every earlier P V of the item has landed (the
+                // two issuers' PVs may complete in either order).
+                if (!__all_sync(0xffffffffu, mbar_wait(bars.pv_done((jg - 1) & 1), (uint32_t)((jg - 1) >> 1) & 1u,
+                                                       abort_flag, p.status)))
+                    return;
+                if (j >= 2 && !__all_sync(0xffffffffu, mbar_wait(bars.pv_done(jg & 1), (uint32_t)((jg - 2) >> 1) & 1u,
+                                                                  abort_flag, p.status)))
+                    return;
+                tc_fence_after();
+#pragma unroll 1
+                for (int c = hf * OC; c < (hf + 1) * OC; c += 32) {
+                    uint32_t rr[32];
+                    tmem_ld32(tl + C::TM_O + c, rr);
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) rr[e] = __float_as_uint(__uint_as_float(rr[e]) * alpha);
+                    tmem_st32(tl + C::TM_O + c, rr);
+                }
+            }
+            // P = exp2(s * scale * log2e - m_ref), packed bf16: into the P buffer in TMEM
+            // (this half's keys to columns [hf KB/2, hf KB/2 + KB/2)), or (PSMEM) as this
+            // thread's 128-byte-swizzled row of P buffer jg%2 in shared memory.
+            float rs[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            const float mref = m_ref;
+            if constexpr (C::PSMEM) {
+                // P buffer jg%2 held P_{jg-2}: PV_{jg-2} must have finished reading it
+                if (jg >= 2 && !__all_sync(0xffffffffu, mbar_wait(bars.pv_done(jg & 1), (uint32_t)((jg - 2) >> 1) & 1u,
+                                                                   abort_flag, p.status)))
+                    return;
+                const uint32_t pbase = sbase + C::OFF_P + (jg & 1) * C::P_BUF_BYTES;
+#pragma unroll
+                for (int c8 = 0; c8 < C::BN / 8; ++c8) {
+                    uint32_t pk[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float p0 = ex2_approx(fmaf(s[8 * c8 + 2 * e], sl2, -mref));
+                        const float p1 = ex2_approx(fmaf(s[8 * c8 + 2 * e + 1], sl2, -mref));
+                        rs[(2 * c8 + (e >> 1)) & 7] += p0 + p1;
+                        pk[e] = pack_bf16x2(p0, p1);
+                    }
+                    const uint32_t addr = pbase + (uint32_t)(c8 >> 3) * (C::BM * 128) + sw128_offset(row, c8 & 7);
+                    asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(pk[0]), "r"(pk[1]),
+                                 "r"(pk[2]), "r"(pk[3])
+                                 : "memory");
+                }
+                l += ((rs[0] + rs[1]) + (rs[2] + rs[3])) + ((rs[4] + rs[5]) + (rs[6] + rs[7]));
+                fence_proxy_async_smem();  // the tensor core reads P through the async proxy
+                tmem_wait_st();            // an O rescale above, if any, has landed
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bars.p_full(jg & 1));
+            } else {
+                uint32_t pk[KB / 2];
+                float2 rs2[4] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
+                const float2 sl2x2 = make_float2(sl2, sl2), negm = make_float2(-mref, -mref);
+#pragma unroll
+                for (int e = 0; e < KB / 2; ++e) {
+                    const float2 x = fma2(make_float2(s[2 * e], s[2 * e + 1]), sl2x2, negm);
+                    const float2 pe = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+                    rs2[e & 3] = add2(rs2[e & 3], pe);
+                    pk[e] = pack_bf16x2(pe.x, pe.y);
+                }
+                // the P buffer held P_{jg-1}: PV_{jg-1} must have finished reading it
+                if (jg >= 1 && !__all_sync(0xffffffffu, mbar_wait(bars.pv_done((jg - 1) & 1), (uint32_t)((jg - 1) >> 1) & 1u,
+                                                                   abort_flag, p.status)))
+                    return;
+                tc_fence_after();
+#pragma unroll
+                for (int c = 0; c < KB / 2; c += 32)
+                    tmem_st32(tl + C::TM_P + hf * (KB / 2) + c, *reinterpret_cast<const uint32_t(*)[32]>(pk + c));
+                l += ((rs2[0].x + rs2[0].y) + (rs2[1].x + rs2[1].y)) + ((rs2[2].x + rs2[2].y) + (rs2[3].x + rs2[3].y));
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bars.p_full(jg & 1));
+            }
+        }
+
+        // ---- the next item's Q prologue: its first QK MMAs then run during this epilogue
+        const bool more = tc_item<D, GV>(p, cta, ncta, r + 1, next);
+        if (more && !prologue(next, n_it + 1)) return;
+
+        // ---- epilogue: O / l * act(gate) (additive gate: O / l + act(gate)) -> bf16, this
+        // thread's O columns, into the output tile (over the gate tile, each thread
+        // overwriting only gate values it has read; d = 256: in the idle V ring); the
+        // producer writes it to [B,S,H*d] with TMA stores (rows past S clipped).  A
+        // partial tile of packed sequences is stored row by row instead (a 128-row TMA
+        // store would reach into the next sequence).
+        float l_row = l;
+        if constexpr (C::SPLIT) {
+            xsum[hf * C::BM + row] = l;
+            if (!meet()) return;
+            l_row = xsum[row] + xsum[C::BM + row];
+        }
+        if (!__all_sync(0xffffffffu, mbar_wait(bars.o_final(), (uint32_t)n_it & 1u, abort_flag, p.status))) return;
+        const bool elementwise = GV ? gate_per_dim(p.gate_mode) : p.gate_mode == GATTN_GATE_ELEMENTWISE;
+        constexpr bool plain = !GV;
+        const bool additive = GV && gate_additive(p.gate_mode);
+        // persistent: the gate/output buffer holds this item's gate tile (or is free)
+        if ((C::PERSIST || elementwise) &&
+            !__all_sync(0xffffffffu, mbar_wait(bars.g_full(), (uint32_t)n_it & 1u, abort_flag, p.status)))
             return;
         tc_fence_after();
-        float s[KB];
-        {
-            uint32_t r[64];
-#pragma unroll
-            for (int c = 0; c < KB; c += 64) {
-                tmem_ld64(tl + s_col + hf * KB + c, r);
-#pragma unroll
-                for (int e = 0; e < 64; ++e) s[c + e] = __uint_as_float(r[e]);
-            }
-        }
-        // S_j is in registers: its buffer may take the scores of tile j + 2
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bars.s_free(sb));
-        const int key0 = j * C::BN + hf * KB;
-        if (key0 + KB - 1 > row_min) {
-#pragma unroll
-            for (int c = 0; c < KB; ++c)
-                if (key0 + c > t) s[c] = -INFINITY;
-        }
-        float mx[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) mx[i] = s[i];
-#pragma unroll
-        for (int c = 8; c < KB; c += 2) mx[(c >> 1) & 7] = max3(mx[(c >> 1) & 7], s[c], s[c + 1]);
-        float mt = max3(max3(mx[0], mx[1], mx[2]), max3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
-        if constexpr (C::SPLIT) {
-            // the row's maximum over the whole tile (buffer j%2, so a slow partner still
-            // reading tile j-1 is never overwritten)
-            xmax[((j & 1) * 2 + hf) * C::BM + row] = mt;
-            if (!meet()) return;
-            mt = fmaxf(mt, xmax[((j & 1) * 2 + (hf ^ 1)) * C::BM + row]);
-        }
-        const float m_new = fmaxf(m_ref, mt * sl2);
-        const bool need = (m_new - m_ref) > C::RESCALE_THRESHOLD;
-        if (j == 0) {
-            m_ref = m_new;
-        } else if (__any_sync(0xffffffffu, need)) {
-            const float alpha = need ? ex2_approx(m_ref - m_new) : 1.f;
-            if (need) {
-                l *= alpha;
-                m_ref = m_new;
-            }
-            __syncwarp();
-            // O is only touched once every earlier P V has landed (the two issuers'
-            // PVs may complete in either order).
-            if (!__all_sync(0xffffffffu, mbar_wait(bars.pv_done((j - 1) & 1), (uint32_t)((j - 1) >> 1) & 1u,
-                                                   abort_flag, p.status)))
-                return;
-            if (j >= 2 && !__all_sync(0xffffffffu, mbar_wait(bars.pv_done(j & 1), (uint32_t)((j - 2) >> 1) & 1u,
-                                                              abort_flag, p.status)))
-                return;
-            tc_fence_after();
+        const float inv_l = 1.f / l_row;
+        // out = o * gv + ga
+        const float gh = additive ? inv_l : inv_l * gate_head, gha = additive ? gate_head : 0.f;
+        bf16* orow = static_cast<bf16*>(p.out) + (tok * p.H + h) * D;
+        const uint32_t gbase = sbase + C::OFF_G;
+        const uint32_t obase = sbase + C::OFF_OUT;
+        const bool direct = item.direct;
+        auto put = [&](int col, uint32_t w0, uint32_t w1, uint32_t w2, uint32_t w3) {
+            if (!direct) sts_v4(rowtile_addr(obase, row, col), w0, w1, w2, w3);
+            else if (valid) *reinterpret_cast<uint4*>(orow + col) = make_uint4(w0, w1, w2, w3);
+        };
+        // persistent: all of this thread's O columns are read first, so that the next
+        // item's first PV may overwrite O while the outputs are formed
+        constexpr int OCH = C::PERSIST ? OC : 32;
 #pragma unroll 1
-            for (int c = hf * OC; c < (hf + 1) * OC; c += 32) {
-                uint32_t r[32];
-                tmem_ld32(tl + C::TM_O + c, r);
-#pragma unroll
-                for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
-                tmem_st32(tl + C::TM_O + c, r);
-            }
-        }
-        // P = exp2(s * scale * log2e - m_ref), packed bf16: into the P buffer in TMEM
-        // (this half's keys to columns [hf KB/2, hf KB/2 + KB/2)), or (PSMEM) as this
-        // thread's 128-byte-swizzled row of P buffer j%2 in shared memory.
-        float rs[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        const float mref = m_ref;
-        if constexpr (C::PSMEM) {
-            // P buffer j%2 held P_{j-2}: PV_{j-2} must have finished reading it
-            if (j >= 2 && !__all_sync(0xffffffffu, mbar_wait(bars.pv_done(j & 1), (uint32_t)((j - 2) >> 1) & 1u,
-                                                              abort_flag, p.status)))
-                return;
-            const uint32_t pbase = sbase + C::OFF_P + (j & 1) * C::P_BUF_BYTES;
-#pragma unroll
-            for (int c8 = 0; c8 < C::BN / 8; ++c8) {
-                uint32_t pk[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float p0 = ex2_approx(fmaf(s[8 * c8 + 2 * e], sl2, -mref));
-                    const float p1 = ex2_approx(fmaf(s[8 * c8 + 2 * e + 1], sl2, -mref));
-                    rs[(2 * c8 + (e >> 1)) & 7] += p0 + p1;
-                    pk[e] = pack_bf16x2(p0, p1);
-                }
-                const uint32_t addr = pbase + (uint32_t)(c8 >> 3) * (C::BM * 128) + sw128_offset(row, c8 & 7);
-                asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(pk[0]), "r"(pk[1]), "r"(pk[2]),
-                             "r"(pk[3])
-                             : "memory");
-            }
-            l += ((rs[0] + rs[1]) + (rs[2] + rs[3])) + ((rs[4] + rs[5]) + (rs[6] + rs[7]));
-            fence_proxy_async_smem();  // the tensor core reads P through the async proxy
-            tmem_wait_st();            // an O rescale above, if any, has landed
-            tc_fence_before();
+        for (int c0 = hf * OC; c0 < (hf + 1) * OC; c0 += OCH) {
+            uint32_t ro[OCH];
             __syncwarp();
-            if (lane == 0) mbar_arrive(bars.p_full(j & 1));
-        } else {
-            uint32_t pk[KB / 2];
-            float2 rs2[4] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
-            const float2 sl2x2 = make_float2(sl2, sl2), negm = make_float2(-mref, -mref);
 #pragma unroll
-            for (int e = 0; e < KB / 2; ++e) {
-                const float2 x = fma2(make_float2(s[2 * e], s[2 * e + 1]), sl2x2, negm);
-                const float2 pe = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-                rs2[e & 3] = add2(rs2[e & 3], pe);
-                pk[e] = pack_bf16x2(pe.x, pe.y);
-            }
-            rs[0] = rs2[0].x; rs[1] = rs2[0].y; rs[2] = rs2[1].x; rs[3] = rs2[1].y;
-            rs[4] = rs2[2].x; rs[5] = rs2[2].y; rs[6] = rs2[3].x; rs[7] = rs2[3].y;
-            // the P buffer held P_{j-1}: PV_{j-1} must have finished reading it
-            if (j >= 1 && !__all_sync(0xffffffffu, mbar_wait(bars.pv_done((j - 1) & 1), (uint32_t)((j - 1) >> 1) & 1u,
-                                                              abort_flag, p.status)))
-                return;
-            tc_fence_after();
-#pragma unroll
-            for (int c = 0; c < KB / 2; c += 32)
-                tmem_st32(tl + C::TM_P + hf * (KB / 2) + c, *reinterpret_cast<const uint32_t(*)[32]>(pk + c));
-            l += ((rs[0] + rs[1]) + (rs[2] + rs[3])) + ((rs[4] + rs[5]) + (rs[6] + rs[7]));
-            tmem_wait_st();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bars.p_full(j & 1));
-        }
-    }
-
-    // ---- epilogue: O / l * act(gate) (additive gate: O / l + act(gate)) -> bf16, this
-    // thread's O columns, into a staging tile in the V ring (idle once every PV is
-    // done); the producer writes the tile to [B,S,H*d] with TMA stores (rows past S
-    // clipped).  A partial tile of packed sequences is stored row by row instead (a
-    // 128-row TMA store would reach into the next sequence).
-    float l_row = l;
-    if constexpr (C::SPLIT) {
-        xsum[hf * C::BM + row] = l;
-        if (!meet()) return;
-        l_row = xsum[row] + xsum[C::BM + row];
-    }
-    if (!__all_sync(0xffffffffu, mbar_wait(bars.o_final(), 0, abort_flag, p.status))) return;
-    const bool elementwise = GV ? gate_per_dim(p.gate_mode) : p.gate_mode == GATTN_GATE_ELEMENTWISE;
-    constexpr bool plain = !GV;
-    const bool additive = GV && gate_additive(p.gate_mode);
-    if (elementwise && !__all_sync(0xffffffffu, mbar_wait(bars.g_full(), 0, abort_flag, p.status))) return;
-    tc_fence_after();
-    const float inv_l = 1.f / l_row;
-    // out = o * gv + ga
-    const float gh = additive ? inv_l : inv_l * gate_head, gha = additive ? gate_head : 0.f;
-    bf16* orow = static_cast<bf16*>(p.out) + (tok * p.H + h) * D;
-    const uint32_t gbase = sbase + C::OFF_K;
-    const uint32_t obase = sbase + C::OFF_V;
-    const bool direct = GV && p.vtiles && (qt + 1) * C::BM > slen;
-    auto put = [&](int col, uint32_t w0, uint32_t w1, uint32_t w2, uint32_t w3) {
-        if (!direct) sts_v4(rowtile_addr(obase, row, col), w0, w1, w2, w3);
-        else if (valid) *reinterpret_cast<uint4*>(orow + col) = make_uint4(w0, w1, w2, w3);
-    };
-    // the default multiplicative sigmoid gate keeps a loop of its own (its cost is
-    // the epilogue's); the variants share a second one
-#pragma unroll 1
-    for (int c = hf * OC; c < (hf + 1) * OC; c += 32) {
-        uint32_t r[32];
-        __syncwarp();
-        tmem_ld32(tl + C::TM_O + c, r);
-        if constexpr (plain) {
-            float gv[32];
-            if (elementwise) {
-#pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4) {
-                    float f[8];
-                    unpack8(lds_v4(rowtile_addr(gbase, row, c + 8 * q4)), f);
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) gv[8 * q4 + e] = inv_l * sigmoid_tanh(f[e]);
-                }
-            } else {
-#pragma unroll
-                for (int e = 0; e < 32; ++e) gv[e] = gh;
+            for (int c = 0; c < OCH; c += 32)
+                tmem_ld32(tl + C::TM_O + c0 + c, *reinterpret_cast<uint32_t(*)[32]>(ro + c));
+            if (C::PERSIST) {
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bars.o_free());
             }
 #pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
-                uint32_t w[4];
+            for (int c1 = 0; c1 < OCH; c1 += 32) {
+                const int c = c0 + c1;
+                const uint32_t* ov = ro + c1;
+                if constexpr (plain) {
+                    float gv[32];
+                    if (elementwise) {
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int e = 8 * q4 + 2 * i;
-                    w[i] = pack_bf16x2(__uint_as_float(r[e]) * gv[e], __uint_as_float(r[e + 1]) * gv[e + 1]);
-                }
-                put(c + 8 * q4, w[0], w[1], w[2], w[3]);
-            }
-        } else {
-        float gv[32], ga[32];
-        if (elementwise) {
+                        for (int q4 = 0; q4 < 4; ++q4) {
+                            float f[8];
+                            unpack8(lds_v4(rowtile_addr(gbase, row, c + 8 * q4)), f);
 #pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
-                float f[8];
-                unpack8(lds_v4(rowtile_addr(gbase, row, c + 8 * q4)), f);
+                            for (int e = 0; e < 8; ++e) gv[8 * q4 + e] = inv_l * sigmoid_tanh(f[e]);
+                        }
+                    } else {
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const float a = gate_act(f[e], sigmoid_tanh(f[e]), p.gate_mode);
-                    gv[8 * q4 + e] = additive ? inv_l : inv_l * a;
-                    ga[8 * q4 + e] = additive ? a : 0.f;
+                        for (int e = 0; e < 32; ++e) gv[e] = gh;
+                    }
+#pragma unroll
+                    for (int q4 = 0; q4 < 4; ++q4) {
+                        uint32_t w[4];
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const int e = 8 * q4 + 2 * i;
+                            w[i] = pack_bf16x2(__uint_as_float(ov[e]) * gv[e], __uint_as_float(ov[e + 1]) * gv[e + 1]);
+                        }
+                        put(c + 8 * q4, w[0], w[1], w[2], w[3]);
+                    }
+                } else {
+                    float gv[32], ga[32];
+                    if (elementwise) {
+#pragma unroll
+                        for (int q4 = 0; q4 < 4; ++q4) {
+                            float f[8];
+                            unpack8(lds_v4(rowtile_addr(gbase, row, c + 8 * q4)), f);
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) {
+                                const float a = gate_act(f[e], sigmoid_tanh(f[e]), p.gate_mode);
+                                gv[8 * q4 + e] = additive ? inv_l : inv_l * a;
+                                ga[8 * q4 + e] = additive ? a : 0.f;
+                            }
+                        }
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) {
+                            gv[e] = gh;
+                            ga[e] = gha;
+                        }
+                    }
+#pragma unroll
+                    for (int q4 = 0; q4 < 4; ++q4) {
+                        uint32_t w[4];
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const int e = 8 * q4 + 2 * i;
+                            w[i] = pack_bf16x2(fmaf(__uint_as_float(ov[e]), gv[e], ga[e]),
+                                               fmaf(__uint_as_float(ov[e + 1]), gv[e + 1], ga[e + 1]));
+                        }
+                        put(c + 8 * q4, w[0], w[1], w[2], w[3]);
+                    }
                 }
             }
-        } else {
-#pragma unroll
-            for (int e = 0; e < 32; ++e) {
-                gv[e] = gh;
-                ga[e] = gha;
-            }
         }
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-            uint32_t w[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int e = 8 * q4 + 2 * i;
-                w[i] = pack_bf16x2(fmaf(__uint_as_float(r[e]), gv[e], ga[e]),
-                                   fmaf(__uint_as_float(r[e + 1]), gv[e + 1], ga[e + 1]));
-            }
-            put(c + 8 * q4, w[0], w[1], w[2], w[3]);
-        }
-        }
-    }
-    if (!direct) {
-        fence_proxy_async_smem();  // the TMA stores read the staging tile through the async proxy
+        // the output buffer may be written out (a directly stored tile only frees it)
+        fence_proxy_async_smem();  // the TMA stores read the staged tile through the async proxy
         __syncwarp();
         if (lane == 0) mbar_arrive(bars.o_staged());
+        jb += n_kv;
+        item = next;
+        have = more;
     }
 }
 
@@ -662,24 +819,7 @@ __global__ void __launch_bounds__(PfCfg<D>::THREADS, 1)
     const Bars bars{sbase + C::OFF_BAR, C::NSK, C::NSV};
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
-
-    // heaviest query tiles first; the heads of one KV group are adjacent
-    // (packed sequences: the tile table, also heaviest first, times the heads)
-    const int bh_count = p.B * p.H;
-    int qt, bh, t0 = 0, slen = p.S;
-    if (GV && p.vtiles) {
-        const int4 e = p.vtiles[blockIdx.x / p.H];
-        qt = e.z;
-        t0 = e.x;
-        slen = e.y;
-        bh = (int)(blockIdx.x % p.H);
-    } else {
-        qt = p.n_qtiles - 1 - (int)(blockIdx.x / bh_count);
-        bh = (int)(blockIdx.x % bh_count);
-    }
-    const int b = bh / p.H, h = bh % p.H, g = h / (p.H / p.G);
-    const int q_end = min(slen, (qt + 1) * C::BM);
-    const int n_kv = (q_end + C::BN - 1) / C::BN;
+    const int cta = (int)blockIdx.x, ncta = (int)gridDim.x;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::NSK; ++s) {
@@ -700,6 +840,7 @@ __global__ void __launch_bounds__(PfCfg<D>::THREADS, 1)
         mbar_init(bars.o_final(), 2);
         mbar_init(bars.q_ready(), C::SOFTMAX_WARPS);
         mbar_init(bars.o_staged(), C::SOFTMAX_WARPS);
+        mbar_init(bars.o_free(), C::SOFTMAX_WARPS);
         mbar_init(bars.drain(), 2);
         mbar_init(bars.q_full(), 1);
         mbar_init(bars.g_full(), 1);
@@ -722,25 +863,21 @@ __global__ void __launch_bounds__(PfCfg<D>::THREADS, 1)
     const uint32_t tm = *tmem_slot;
 
     if (warp == 0) {
-        if (lane == 0)
-            run_producer<D>(&tmK, &tmV, &tmQ, &tmG, &tmO, p.qnorm_w, bars, sbase, n_kv, b, g, h, qt, t0, p.G,
-                            GV ? gate_per_dim(p.gate_mode) : p.gate_mode == GATTN_GATE_ELEMENTWISE,
-                            GV && gate_layout(p.gate_mode) == GATTN_GATE_HEAD_SHARED ? 0 : h,
-                            !(GV && p.vtiles && (qt + 1) * C::BM > slen), abort_flag, p.status);
+        if (lane == 0) run_producer<D, GV>(&tmK, &tmV, &tmQ, &tmG, &tmO, p, bars, sbase, cta, ncta, abort_flag, p.status);
         __syncwarp();
     } else if (warp == 1) {
-        if (lane == 0) run_mma<D>(0, bars, sbase, tm, n_kv, abort_flag, p.status);
+        if (lane == 0) run_mma<D, GV>(0, p, bars, sbase, tm, cta, ncta, abort_flag, p.status);
         __syncwarp();
     } else if (warp == 2) {
         if (lane == 0) {
-            run_mma<D>(1, bars, sbase, tm, n_kv, abort_flag, p.status);
+            run_mma<D, GV>(1, p, bars, sbase, tm, cta, ncta, abort_flag, p.status);
             // Whatever happened, no MMA of either issuer may still be in flight when TMEM is released.
             mbar_wait_drain(bars.drain(), 0, p.status);
         }
         __syncwarp();
     } else {
-        run_softmax<D, GV>(p, bars, sbase, smem + C::OFF_X, tm, warp & 3, (warp - 3) >> 2, lane, qt, t0, slen, b, h,
-                           n_kv, abort_flag);
+        run_softmax<D, GV>(p, bars, sbase, smem + C::OFF_X, tm, warp & 3, (warp - 3) >> 2, lane, cta, ncta,
+                           abort_flag);
     }
     tc_fence_before();
     __syncthreads();
@@ -758,8 +895,10 @@ cudaError_t launch_d(const PrefillParams& p, const PrefillMaps& maps, cudaStream
     auto kernel = gv ? prefill_tc_kernel<D, true> : prefill_tc_kernel<D, false>;
     cudaError_t e = set_smem_once(reinterpret_cast<const void*>(kernel), C::SMEM_ALLOC);
     if (e != cudaSuccess) return e;
-    const long long blocks = p.vtiles ? (long long)p.n_vtiles * p.H : (long long)p.n_qtiles * p.B * p.H;
-    if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
+    const long long n_items = p.vtiles ? (long long)p.n_vtiles * p.H : (long long)p.n_qtiles * p.B * p.H;
+    if (n_items > 0x7fffffffLL || n_items < 1) return cudaErrorInvalidValue;
+    // persistent: one CTA per SM at most; one item per CTA otherwise
+    const long long blocks = C::PERSIST && p.n_sms > 0 && n_items > p.n_sms ? p.n_sms : n_items;
     if (ev_start) cudaEventRecord(ev_start, stream);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)blocks);
