@@ -593,8 +593,8 @@ __device__ void pair_softmax(const PrefillParams& p, const PairBars& bars, uint3
 #pragma unroll
             for (int i = 0; i < 8; ++i) mx[i] = s[i];
 #pragma unroll
-            for (int c = 8; c < HB; ++c) mx[c & 7] = fmaxf(mx[c & 7], s[c]);
-            float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+            for (int c = 8; c < HB; c += 2) mx[(c >> 1) & 7] = max3(mx[(c >> 1) & 7], s[c], s[c + 1]);
+            float mt = max3(max3(mx[0], mx[1], mx[2]), max3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
             // the row's maximum over the whole tile: swap halves (buffer j%2, so a slow
             // partner still reading tile j-1 is never overwritten).  Passing the meet also
             // means the partner has read its S columns, which P overwrites below.
@@ -629,18 +629,19 @@ __device__ void pair_softmax(const PrefillParams& p, const PairBars& bars, uint3
             }
             // P = exp2(s * scale * log2e - m_ref) as bf16 pairs over this thread's keys:
             // columns [32 hf, 32 hf + 32) of the score buffer
-            float rs[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
             const float mref = m_ref;
             uint32_t pk[32];
+            float2 rs2[4] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
+            const float2 sl2x2 = make_float2(sl2, sl2), negm = make_float2(-mref, -mref);
 #pragma unroll
             for (int e = 0; e < 32; ++e) {
-                const float p0 = ex2_approx(fmaf(s[2 * e], sl2, -mref));
-                const float p1 = ex2_approx(fmaf(s[2 * e + 1], sl2, -mref));
-                rs[e & 7] += p0 + p1;
-                pk[e] = pack_bf16x2(p0, p1);
+                const float2 x = fma2(make_float2(s[2 * e], s[2 * e + 1]), sl2x2, negm);
+                const float2 pe = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+                rs2[e & 3] = add2(rs2[e & 3], pe);
+                pk[e] = pack_bf16x2(pe.x, pe.y);
             }
             tmem_st32(tl + s_col + hf * (HB / 2), pk);
-            l += ((rs[0] + rs[1]) + (rs[2] + rs[3])) + ((rs[4] + rs[5]) + (rs[6] + rs[7]));
+            l += ((rs2[0].x + rs2[0].y) + (rs2[1].x + rs2[1].y)) + ((rs2[2].x + rs2[2].y) + (rs2[3].x + rs2[3].y));
             tmem_wait_st();  // P (and an O rescale above, if any) has landed
             tc_fence_before();
             __syncwarp();

@@ -68,12 +68,13 @@ struct PfCfg {
     // shared memory.  d <= 128: 128-key tiles, P in a TMEM buffer of its own.
     static constexpr int BN = (D == 256) ? 64 : 128;
     static constexpr bool PSMEM = (D == 256);
-    // d <= 128: persistent CTAs with their own raw-Q and gate/output buffers, and two
-    // threads per query row (8 softmax warps), each owning half of the row's keys
-    // in every tile and half of O's columns
+    // d <= 128: persistent CTAs with their own raw-Q and gate/output buffers, and NH
+    // threads per query row (4 NH softmax warps), each owning 1/NH of the row's keys
+    // in every tile and of O's columns
     static constexpr bool PERSIST = !PSMEM;
-    static constexpr bool SPLIT = !PSMEM;
-    static constexpr int SOFTMAX_WARPS = SPLIT ? 8 : 4;
+    static constexpr int NH = PSMEM ? 1 : 2;
+    static constexpr bool SPLIT = NH > 1;
+    static constexpr int SOFTMAX_WARPS = 4 * NH;
     static constexpr int NSB = 2;  // score buffers in TMEM: tile j uses buffer j % 2
     static constexpr int NPB = PSMEM ? 2 : 0;  // P buffers in shared memory
     static constexpr int NSK = PERSIST ? 2 : 3;  // K ring stages
@@ -107,8 +108,8 @@ struct PfCfg {
     static constexpr int NBAR = 2 * NSK + 2 * NSV + 19;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr int OFF_W = (OFF_MISC + 16 + 127) & ~127;  // qnorm weights, D bf16
-    static constexpr int OFF_X = OFF_W + D * 2;                  // row-half exchange (SPLIT)
-    static constexpr int SMEM_BYTES = OFF_X + (SPLIT ? 8 * BM * 4 : 0);
+    static constexpr int OFF_X = OFF_W + D * 2;                  // exchange between a row's threads (SPLIT)
+    static constexpr int SMEM_BYTES = OFF_X + (SPLIT ? 4 * NH * BM * 4 : 0);
     // + slack for 1024-byte alignment; never less than 120 KB, so that a second CTA
     // can never share the SM (each CTA allocates all 512 TMEM columns).
     static constexpr int SMEM_ALLOC = (SMEM_BYTES + 1024) > 122880 ? (SMEM_BYTES + 1024) : 122880;
@@ -441,18 +442,18 @@ template <int D, bool GV>
 __device__ void run_softmax(const PrefillParams& p, const Bars& bars, uint32_t sbase, uint8_t* smem_x, uint32_t tm,
                             int quarter, int hf, int lane, int cta, int ncta, volatile int* abort_flag) {
     using C = PfCfg<D>;
-    constexpr int NH = C::SPLIT ? 2 : 1;  // threads per query row
+    constexpr int NH = C::NH;             // threads per query row
     constexpr int KB = C::BN / NH;        // keys of every tile owned by this thread: [hf KB, hf KB + KB)
     constexpr int OC = D / NH;            // O columns owned by this thread: [hf OC, hf OC + OC)
     const int row = quarter * 32 + lane;
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     const uint32_t tl = tm + lane_off;
-    // With two threads per row (warps w and w + 4 share the row's TMEM lanes) the
-    // halves swap values through shared memory and then meet on an mbarrier (one
+    // With several threads per row (warps w, w + 4, ... share the row's TMEM lanes)
+    // the parts swap values through shared memory and then meet on an mbarrier (one
     // phase per use: every prologue, tile and epilogue).
-    float* xmax = reinterpret_cast<float*>(smem_x);  // [2][2][BM] tile maxima
-    float* xsum = xmax + 2 * 2 * C::BM;              // [2][BM] row sums
-    float* xss = xsum + 2 * C::BM;                   // [2][BM] sums of squares of q
+    float* xmax = reinterpret_cast<float*>(smem_x);  // [2][NH][BM] tile maxima
+    float* xsum = xmax + 2 * NH * C::BM;             // [NH][BM] row sums
+    float* xss = xsum + NH * C::BM;                  // [NH][BM] sums of squares of q
     const uint32_t xbar = bars.xchg(quarter);
     int xphase = 0;
     auto meet = [&]() -> bool {
@@ -486,7 +487,9 @@ __device__ void run_softmax(const PrefillParams& p, const Bars& bars, uint32_t s
         if constexpr (C::SPLIT) {
             xss[hf * C::BM + row] = sq;
             if (!meet()) return false;
-            sq = xss[row] + xss[C::BM + row];
+            sq = xss[row];
+#pragma unroll
+            for (int i = 1; i < NH; ++i) sq += xss[i * C::BM + row];
         }
         const float rinv = rsqrtf(sq / (float)D + p.eps);
         const float posf = valid ? (p.pos ? (float)p.pos[tok] : (float)t) : 0.f;
@@ -561,12 +564,20 @@ __device__ void run_softmax(const PrefillParams& p, const Bars& bars, uint32_t s
             tc_fence_after();
             float s[KB];
             {
-                uint32_t rr[64];
+                if constexpr (KB >= 64) {
+                    uint32_t rr[64];
 #pragma unroll
-                for (int c = 0; c < KB; c += 64) {
-                    tmem_ld64(tl + s_col + hf * KB + c, rr);
+                    for (int c = 0; c < KB; c += 64) {
+                        tmem_ld64(tl + s_col + hf * KB + c, rr);
 #pragma unroll
-                    for (int e = 0; e < 64; ++e) s[c + e] = __uint_as_float(rr[e]);
+                        for (int e = 0; e < 64; ++e) s[c + e] = __uint_as_float(rr[e]);
+                    }
+                } else {
+                    static_assert(KB == 32, "32 or a multiple of 64 keys per thread");
+                    uint32_t rr[32];
+                    tmem_ld32(tl + s_col + hf * KB, rr);
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) s[e] = __uint_as_float(rr[e]);
                 }
             }
             // S_j is in registers: its buffer may take the scores of tile j + 2
@@ -588,9 +599,11 @@ __device__ void run_softmax(const PrefillParams& p, const Bars& bars, uint32_t s
             if constexpr (C::SPLIT) {
                 // the row's maximum over the whole tile (buffer jg%2, so a slow partner
                 // still reading tile jg-1 is never overwritten)
-                xmax[((jg & 1) * 2 + hf) * C::BM + row] = mt;
+                xmax[((jg & 1) * NH + hf) * C::BM + row] = mt;
                 if (!meet()) return;
-                mt = fmaxf(mt, xmax[((jg & 1) * 2 + (hf ^ 1)) * C::BM + row]);
+#pragma unroll
+                for (int i = 0; i < NH; ++i)
+                    if (i != hf) mt = fmaxf(mt, xmax[((jg & 1) * NH + i) * C::BM + row]);
             }
             const float m_new = fmaxf(m_ref, mt * sl2);
             const bool need = (m_new - m_ref) > C::RESCALE_THRESHOLD;
@@ -669,9 +682,13 @@ __device__ void run_softmax(const PrefillParams& p, const Bars& bars, uint32_t s
                                                                    abort_flag, p.status)))
                     return;
                 tc_fence_after();
+                if constexpr (KB / 2 >= 32) {
 #pragma unroll
-                for (int c = 0; c < KB / 2; c += 32)
-                    tmem_st32(tl + C::TM_P + hf * (KB / 2) + c, *reinterpret_cast<const uint32_t(*)[32]>(pk + c));
+                    for (int c = 0; c < KB / 2; c += 32)
+                        tmem_st32(tl + C::TM_P + hf * (KB / 2) + c, *reinterpret_cast<const uint32_t(*)[32]>(pk + c));
+                } else {
+                    tmem_st16(tl + C::TM_P + hf * (KB / 2), pk);
+                }
                 l += ((rs2[0].x + rs2[0].y) + (rs2[1].x + rs2[1].y)) + ((rs2[2].x + rs2[2].y) + (rs2[3].x + rs2[3].y));
                 tmem_wait_st();
                 tc_fence_before();
@@ -694,7 +711,9 @@ __device__ void run_softmax(const PrefillParams& p, const Bars& bars, uint32_t s
         if constexpr (C::SPLIT) {
             xsum[hf * C::BM + row] = l;
             if (!meet()) return;
-            l_row = xsum[row] + xsum[C::BM + row];
+            l_row = xsum[row];
+#pragma unroll
+            for (int i = 1; i < NH; ++i) l_row += xsum[i * C::BM + row];
         }
         if (!__all_sync(0xffffffffu, mbar_wait(bars.o_final(), (uint32_t)n_it & 1u, abort_flag, p.status))) return;
         const bool elementwise = GV ? gate_per_dim(p.gate_mode) : p.gate_mode == GATTN_GATE_ELEMENTWISE;
@@ -836,7 +855,7 @@ __global__ void __launch_bounds__(PfCfg<D>::THREADS, 1)
             mbar_init(bars.p_full(i), C::SOFTMAX_WARPS);
             mbar_init(bars.pv_done(i), 1);
         }
-        for (int q = 0; q < 4; ++q) mbar_init(bars.xchg(q), 2);
+        for (int q = 0; q < 4; ++q) mbar_init(bars.xchg(q), C::NH);
         mbar_init(bars.o_final(), 2);
         mbar_init(bars.q_ready(), C::SOFTMAX_WARPS);
         mbar_init(bars.o_staged(), C::SOFTMAX_WARPS);
