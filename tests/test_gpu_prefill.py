@@ -284,3 +284,27 @@ def test_rope_rotation_error_bound_at_long_positions():
     ref = np.concatenate([a * c - b_ * s, b_ * c + a * s, kn[..., rd:]], axis=-1).transpose(0, 2, 1, 3)
     err = np.abs(kr - ref)
     assert err.max() < 2e-5, err.max()
+
+
+@pytest.mark.parametrize("d, H, G", [(256, 8, 2), (128, 4, 2)])
+def test_output_feeds_the_o_projection(d, H, G):
+    """The gated attention output is handed to the output projection as written: a
+    [B*S, H*d] row-major bf16 matrix with the gate already applied, which is where
+    the gate sits (between SDPA and W_O: "Gated attention" handbook chapter, "The
+    code: qwen/attention.py"; "Gated Attention" deep-dive, "门放在哪里？").  A bf16
+    GEMM reads it in place (same storage, no re-layout) and gives the oracle's output
+    times W_O^T.  W_O rows have unit norm, so an output error e moves each projected
+    value by at most |e|_2 and typically by its RMS: the bf16 bounds still apply."""
+    B, S, hidden = 2, 200, 512
+    w = small("oproj", B, S, H, G, d, 64, 1e6, "elementwise", seed=21)
+    inp = make_prefill_inputs(w)
+    out = run_gpu(inp, w)
+    a = out.view(B * S, H * d)
+    assert a.data_ptr() == out.data_ptr() and a.is_contiguous() and a.dtype == torch.bfloat16
+    g = torch.Generator().manual_seed(22)
+    w_o = torch.randn(hidden, H * d, generator=g, dtype=torch.float64)
+    w_o = (w_o / w_o.norm(dim=1, keepdim=True)).to(torch.bfloat16)
+    y = a @ w_o.to(DEV).t()
+    torch.cuda.synchronize()
+    ref = np.asarray(run_oracle(inp, w), dtype=np.float64).reshape(B * S, H * d) @ w_o.double().numpy().T
+    assert_close_to_oracle(y, ref, torch.bfloat16, f"o_proj d{d}")
