@@ -67,6 +67,15 @@ __device__ __forceinline__ float2 add2(float2 a, float2 b) {
         : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
     return d;
 }
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
 // max of three fp32 values in one instruction (sm_100 and later)
 __device__ __forceinline__ float max3(float a, float b, float c) {
     float d;
@@ -127,6 +136,51 @@ __device__ __forceinline__ void rope_sincos(float x, float* s, float* c) {
     r = fmaf(-k, k2PiLo, r);
     *s = __sinf(r);
     *c = __cosf(r);
+}
+
+// rope_sincos of two angles, the reduction in paired fp32 arithmetic: the same
+// values as two rope_sincos calls (each lane is rounded as the scalar instruction).
+__device__ __forceinline__ void rope_sincos2(float2 x, float2* s, float2* c) {
+    constexpr float kInv2Pi = 0.15915494309189535f;
+    constexpr float k2PiHi = 6.28318548202514648f;
+    constexpr float k2PiLo = -1.7484556000744487e-07f;
+    const float2 kx = mul2(x, make_float2(kInv2Pi, kInv2Pi));
+    const float2 nk = make_float2(-rintf(kx.x), -rintf(kx.y));
+    float2 r = fma2(nk, make_float2(k2PiHi, k2PiHi), x);
+    r = fma2(nk, make_float2(k2PiLo, k2PiLo), r);
+    *s = make_float2(__sinf(r.x), __sinf(r.y));
+    *c = make_float2(__cosf(r.x), __cosf(r.y));
+}
+
+// One rotated pair of chunks of a RoPE row (x_i and x_{i+rd/2}, 8 values each,
+// with their norm weights) scaled by rinv: lo = (a cos - b sin), hi = (b cos +
+// a sin) with a = x_i w_i rinv, b = x_{i+rd/2} w_{i+rd/2} rinv, as bf16 pairs.
+__device__ __forceinline__ void rope_rotate8(const float (&xa)[8], const float (&xb)[8], const float (&wa)[8],
+                                             const float (&wb)[8], const float* inv_freq, float posf, float rinv,
+                                             uint32_t (&lo)[4], uint32_t (&hi)[4]) {
+    const float2 r2 = make_float2(rinv, rinv), p2 = make_float2(posf, posf);
+#pragma unroll
+    for (int e = 0; e < 8; e += 2) {
+        float2 sn, cs;
+        rope_sincos2(mul2(p2, make_float2(inv_freq[e], inv_freq[e + 1])), &sn, &cs);
+        const float2 a = mul2(make_float2(xa[e], xa[e + 1]), mul2(make_float2(wa[e], wa[e + 1]), r2));
+        const float2 b = mul2(make_float2(xb[e], xb[e + 1]), mul2(make_float2(wb[e], wb[e + 1]), r2));
+        const float2 bs = mul2(b, sn), as = mul2(a, sn);
+        const float2 l = fma2(a, cs, make_float2(-bs.x, -bs.y));
+        const float2 h = fma2(b, cs, as);
+        lo[e >> 1] = pack_bf16x2(l.x, l.y);
+        hi[e >> 1] = pack_bf16x2(h.x, h.y);
+    }
+}
+
+// Eight values x w rinv (x times its norm weight, then rinv) as four bf16 pairs.
+__device__ __forceinline__ void scale8_bf16(const float (&x)[8], const float (&w)[8], float rinv, uint32_t (&o)[4]) {
+    const float2 r2 = make_float2(rinv, rinv);
+#pragma unroll
+    for (int e = 0; e < 8; e += 2) {
+        const float2 v = mul2(mul2(make_float2(x[e], x[e + 1]), make_float2(w[e], w[e + 1])), r2);
+        o[e >> 1] = pack_bf16x2(v.x, v.y);
+    }
 }
 
 // Raise a kernel's dynamic shared-memory limit once per device (host side).

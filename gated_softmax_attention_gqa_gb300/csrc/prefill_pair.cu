@@ -520,16 +520,7 @@ __device__ void pair_softmax(const PrefillParams& p, const PairBars& bars, uint3
             unpack8(lds_v4(wbase + 2 * i0), wa);
             unpack8(lds_v4(wbase + 2 * (i0 + half)), wb);
             uint32_t lo[4], hi[4];
-#pragma unroll
-            for (int e = 0; e < 8; e += 2) {
-                float s0, c0, s1, c1;
-                rope_sincos(posf * p.inv_freq[i0 + e], &s0, &c0);
-                rope_sincos(posf * p.inv_freq[i0 + e + 1], &s1, &c1);
-                const float a0 = xa[e] * wa[e], b0 = xb[e] * wb[e];
-                const float a1 = xa[e + 1] * wa[e + 1], b1 = xb[e + 1] * wb[e + 1];
-                lo[e >> 1] = pack_bf16x2((a0 * c0 - b0 * s0) * rinv, (a1 * c1 - b1 * s1) * rinv);
-                hi[e >> 1] = pack_bf16x2((b0 * c0 + a0 * s0) * rinv, (b1 * c1 + a1 * s1) * rinv);
-            }
+            rope_rotate8(xa, xb, wa, wb, p.inv_freq + i0, posf, rinv, lo, hi);
             sts_v4(rowtile_addr(qbase, row, i0), lo[0], lo[1], lo[2], lo[3]);
             sts_v4(rowtile_addr(qbase, row, i0 + half), hi[0], hi[1], hi[2], hi[3]);
         }
@@ -537,9 +528,9 @@ __device__ void pair_softmax(const PrefillParams& p, const PairBars& bars, uint3
             float x[8], w[8];
             unpack8(lds_v4(rowtile_addr(qbase, row, e0)), x);
             unpack8(lds_v4(wbase + 2 * e0), w);
-            sts_v4(rowtile_addr(qbase, row, e0), pack_bf16x2(x[0] * w[0] * rinv, x[1] * w[1] * rinv),
-                   pack_bf16x2(x[2] * w[2] * rinv, x[3] * w[3] * rinv), pack_bf16x2(x[4] * w[4] * rinv, x[5] * w[5] * rinv),
-                   pack_bf16x2(x[6] * w[6] * rinv, x[7] * w[7] * rinv));
+            uint32_t o[4];
+            scale8_bf16(x, w, rinv, o);
+            sts_v4(rowtile_addr(qbase, row, e0), o[0], o[1], o[2], o[3]);
         }
         fence_proxy_async_smem();  // the tensor core reads Q' through the async proxy
         __syncwarp();

@@ -501,16 +501,7 @@ __device__ void run_softmax(const PrefillParams& p, const Bars& bars, uint32_t s
             unpack8(lds_v4(wbase + 2 * i0), wa);
             unpack8(lds_v4(wbase + 2 * (i0 + half)), wb);
             uint32_t lo[4], hi[4];
-#pragma unroll
-            for (int e = 0; e < 8; e += 2) {
-                float s0, c0, s1, c1;
-                rope_sincos(posf * p.inv_freq[i0 + e], &s0, &c0);
-                rope_sincos(posf * p.inv_freq[i0 + e + 1], &s1, &c1);
-                const float a0 = xa[e] * wa[e], b0 = xb[e] * wb[e];
-                const float a1 = xa[e + 1] * wa[e + 1], b1 = xb[e + 1] * wb[e + 1];
-                lo[e >> 1] = pack_bf16x2((a0 * c0 - b0 * s0) * rinv, (a1 * c1 - b1 * s1) * rinv);
-                hi[e >> 1] = pack_bf16x2((b0 * c0 + a0 * s0) * rinv, (b1 * c1 + a1 * s1) * rinv);
-            }
+            rope_rotate8(xa, xb, wa, wb, p.inv_freq + i0, posf, rinv, lo, hi);
             __syncwarp();
             tmem_st4(tl + C::TM_Q + (i0 >> 1), lo[0], lo[1], lo[2], lo[3]);
             tmem_st4(tl + C::TM_Q + ((i0 + half) >> 1), hi[0], hi[1], hi[2], hi[3]);
@@ -519,11 +510,10 @@ __device__ void run_softmax(const PrefillParams& p, const Bars& bars, uint32_t s
             float x[8], w[8];
             unpack8(lds_v4(rowtile_addr(qbase, row, e0)), x);
             unpack8(lds_v4(wbase + 2 * e0), w);
+            uint32_t o[4];
+            scale8_bf16(x, w, rinv, o);
             __syncwarp();
-            tmem_st4(tl + C::TM_Q + (e0 >> 1), pack_bf16x2(x[0] * w[0] * rinv, x[1] * w[1] * rinv),
-                     pack_bf16x2(x[2] * w[2] * rinv, x[3] * w[3] * rinv),
-                     pack_bf16x2(x[4] * w[4] * rinv, x[5] * w[5] * rinv),
-                     pack_bf16x2(x[6] * w[6] * rinv, x[7] * w[7] * rinv));
+            tmem_st4(tl + C::TM_Q + (e0 >> 1), o[0], o[1], o[2], o[3]);
         }
         fence_proxy_async_smem();  // our reads of the raw Q tile happen before the next copy overwrites it
         tmem_wait_st();
