@@ -228,17 +228,30 @@ __device__ void run_producer(const CUtensorMap* tmK, const CUtensorMap* tmV, con
         bulk_wait_group_read0();
     };
 
-    for (int r = 0; ok && tc_item<D, GV>(p, cta, ncta, r, it); ++r, ++n_it) {
-        const int g = it.h / (p.H / p.G);
-        // raw Q tile: its buffer is free once the previous item's prologue has read it
-        if (C::PERSIST && n_it > 0 && !(ok = mbar_wait(bars.q_ready(), (uint32_t)(n_it - 1) & 1u, abort_flag, status)))
-            break;
-        mbar_arrive_expect_tx(bars.q_full(), C::QTILE_BYTES + (n_it == 0 ? D * 2 : 0));
-        if (n_it == 0) bulk_load(sbase + C::OFF_W, p.qnorm_w, D * 2, bars.q_full());
+    // item k's raw Q tile (and with the first item the q norm weights)
+    auto load_q = [&](const TcItem& x, int k) {
+        mbar_arrive_expect_tx(bars.q_full(), C::QTILE_BYTES + (k == 0 ? D * 2 : 0));
+        if (k == 0) bulk_load(sbase + C::OFF_W, p.qnorm_w, D * 2, bars.q_full());
 #pragma unroll
         for (int c = 0; c < C::KCH; ++c)
-            tma_load_4d(sbase + C::OFF_Q + c * C::ROWBOX_BYTES, tmQ, bars.q_full(), c * 64, it.h, row0_of(it), it.b);
-        q_last = n_it;
+            tma_load_4d(sbase + C::OFF_Q + c * C::ROWBOX_BYTES, tmQ, bars.q_full(), c * 64, x.h, row0_of(x), x.b);
+        q_last = k;
+    };
+    TcItem nxt;
+    bool have = tc_item<D, GV>(p, cta, ncta, 0, it);
+    bool q_sent = false;  // the current item's raw Q tile is already on its way
+    for (int r = 0; ok && have; ++r, ++n_it) {
+        const int g = it.h / (p.H / p.G);
+        const bool more = tc_item<D, GV>(p, cta, ncta, r + 1, nxt);
+        // raw Q tile: its buffer is free once the previous item's prologue has read it
+        // (persistent: normally sent during the previous item already, see below)
+        if (!q_sent) {
+            if (C::PERSIST && n_it > 0 &&
+                !(ok = mbar_wait(bars.q_ready(), (uint32_t)(n_it - 1) & 1u, abort_flag, status)))
+                break;
+            load_q(it, n_it);
+        }
+        bool nq_sent = false;  // the next item's raw Q tile is on its way
         // the gate tile is read at the very end of the item: start it on its way to L2 now
         if (gate_tile) {
 #pragma unroll
@@ -263,6 +276,12 @@ __device__ void run_producer(const CUtensorMap* tmK, const CUtensorMap* tmV, con
         uint32_t spins = 0;
         while (nk < ke || nv < ve) {
             bool progressed = false;
+            // persistent: the next item's raw Q tile as soon as this item's prologue has
+            // read the buffer, so that it has landed by the time this item ends
+            if (C::PERSIST && more && !nq_sent && mbar_test_wait(bars.q_ready(), (uint32_t)n_it & 1u)) {
+                load_q(nxt, n_it + 1);
+                nq_sent = progressed = true;
+            }
             if (!g_done && mbar_test_wait(bars.o_staged(), (uint32_t)(n_it - 1) & 1u)) {
                 store_out(prev);
                 gate_in(it);
@@ -325,6 +344,9 @@ __device__ void run_producer(const CUtensorMap* tmK, const CUtensorMap* tmV, con
         }
         jb = ke;
         prev = it;
+        it = nxt;
+        have = more;
+        q_sent = nq_sent;
     }
     // the last item's output
     if (ok && n_it > 0 && mbar_wait(bars.o_staged(), (uint32_t)(n_it - 1) & 1u, abort_flag, status)) store_out(prev);
