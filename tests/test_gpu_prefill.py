@@ -308,3 +308,57 @@ def test_output_feeds_the_o_projection(d, H, G):
     torch.cuda.synchronize()
     ref = np.asarray(run_oracle(inp, w), dtype=np.float64).reshape(B * S, H * d) @ w_o.double().numpy().T
     assert_close_to_oracle(y, ref, torch.bfloat16, f"o_proj d{d}")
+
+
+# More work items than the persistent grids have CTAs (152) or CTA pairs (76), so
+# that every CTA walks several items: the next item's Q tile, gate tile and output
+# buffer, the tile counters and barrier phases all cross item boundaries, in the
+# kernels' second instance (packed sequences and gate variants), with partial tiles
+# of packed sequences (stored row by row) between TMA-stored ones.
+MULTI_ITEM_VARLEN = [
+    # H, G, d, gate layout, act, additive
+    (16, 8, 128, "elementwise", "sigmoid", False),  # one-CTA kernel: 28 tiles x 16 heads = 448 items
+    (8, 2, 256, "headwise", "ns_sigmoid", False),    # CTA pairs: 28 tiles x 4 head pairs = 112 items
+]
+
+
+@pytest.mark.parametrize("case", MULTI_ITEM_VARLEN, ids=[f"d{c[2]}-{c[3]}" for c in MULTI_ITEM_VARLEN])
+def test_varlen_many_items_per_cta(case):
+    H, G, d, layout, act, additive = case
+    lens = [700, 129, 1, 300, 513, 256, 90, 1024]
+    T = sum(lens)
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    w = small("varlen_multi", 1, T, H, G, d, 64, 1e6, layout, seed=31 + d)
+    inp = make_prefill_inputs(w)
+    flat = {k: (v[0] if k in ("q", "k", "v", "gate") else v) for k, v in inp.items()}
+    dev = {k: v.to(DEV) for k, v in flat.items()}
+    out = gattn_prefill_varlen(dev["q"], dev["k"], dev["v"], dev["gate"], dev["qnorm_w"], dev["knorm_w"], cu,
+                               rotary_dim=64, rope_base=1e6, eps=w.eps, gate_mode=layout, gate_act=act,
+                               gate_additive=additive)
+    torch.cuda.synchronize()
+    assert gattn_get_device_status() == 0
+    ref = oracle.prefill_varlen(flat["q"], flat["k"], flat["v"], flat["gate"], flat["qnorm_w"], flat["knorm_w"],
+                                None, cu, 64, 1e6, w.eps, oracle.gate_code(layout, act, additive))
+    assert_close_to_oracle(out, ref, torch.bfloat16, str(case))
+
+
+@pytest.mark.parametrize("d,H,G,S,layout", [(128, 16, 8, 1280, "head_shared"), (256, 8, 2, 2560, "elementwise")])
+def test_gate_variant_many_items_per_cta(d, H, G, S, layout):
+    """SiLU, additive: the gate-variant instance with several items per CTA (320 items
+    over 152 CTAs at d = 128, 80 over 76 CTA pairs at d = 256); sampled rows."""
+    B = 2 if d == 128 else 1
+    w = small("gv_multi", B, S, H, G, d, 64, 1e6, layout, seed=41 + d, gate_std=2.0)
+    inp = make_prefill_inputs(w)
+    dev = {k: v.to(DEV) for k, v in inp.items()}
+    out = gattn_prefill(dev["q"], dev["k"], dev["v"], dev["gate"], dev["qnorm_w"], dev["knorm_w"], rotary_dim=64,
+                        rope_base=1e6, eps=w.eps, gate_mode=layout, gate_act="silu", gate_additive=True)
+    torch.cuda.synchronize()
+    assert gattn_get_device_status() == 0
+    rb, rt = sample_rows(S, B, seed=d, n_random=64, edge=16)
+    code = oracle.gate_code(layout, "silu", True)
+    ref = oracle.prefill_rows(inp["q"], inp["k"], inp["v"], inp["gate"], inp["qnorm_w"], inp["knorm_w"], None, 64,
+                              1e6, w.eps, code, rb, rt)
+    got = out.view(B, S, -1)[torch.from_numpy(rb).long(), torch.from_numpy(rt).long()]
+    z = inp["gate"].double().numpy()
+    zr = z[rb, rt]  # the sampled tokens' logits: [n, H, d] / [n, H] / [n, d]
+    assert_close_to_oracle(got, ref, torch.bfloat16, f"d{d} {layout}", scale=gate_scale(zr, layout, "silu", ref.shape))
