@@ -68,9 +68,9 @@ struct PfCfg {
     // shared memory.  d <= 128: 128-key tiles, P in a TMEM buffer of its own.
     static constexpr int BN = (D == 256) ? 64 : 128;
     static constexpr bool PSMEM = (D == 256);
-    // d <= 128: persistent CTAs with their own raw-Q and gate/output buffers, and NH
-    // threads per query row (4 NH softmax warps), each owning 1/NH of the row's keys
-    // in every tile and of O's columns
+    // d <= 128: persistent CTAs with their own raw-Q and gate/output buffers, and two
+    // threads per query row (8 softmax warps), each owning half of the row's keys in
+    // every tile and half of O's columns (four per row, 16 warps, measured slower)
     static constexpr bool PERSIST = !PSMEM;
     static constexpr int NH = PSMEM ? 1 : 2;
     static constexpr bool SPLIT = NH > 1;
@@ -466,6 +466,7 @@ __device__ void run_softmax(const PrefillParams& p, const Bars& bars, uint32_t s
     using C = PfCfg<D>;
     constexpr int NH = C::NH;             // threads per query row
     constexpr int KB = C::BN / NH;        // keys of every tile owned by this thread: [hf KB, hf KB + KB)
+    static_assert(KB == 64, "one 64-column TMEM load of S and one 32-column store of P per thread and tile");
     constexpr int OC = D / NH;            // O columns owned by this thread: [hf OC, hf OC + OC)
     const int row = quarter * 32 + lane;
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
@@ -576,21 +577,10 @@ __device__ void run_softmax(const PrefillParams& p, const Bars& bars, uint32_t s
             tc_fence_after();
             float s[KB];
             {
-                if constexpr (KB >= 64) {
-                    uint32_t rr[64];
+                uint32_t rr[64];
+                tmem_ld64(tl + s_col + hf * KB, rr);
 #pragma unroll
-                    for (int c = 0; c < KB; c += 64) {
-                        tmem_ld64(tl + s_col + hf * KB + c, rr);
-#pragma unroll
-                        for (int e = 0; e < 64; ++e) s[c + e] = __uint_as_float(rr[e]);
-                    }
-                } else {
-                    static_assert(KB == 32, "32 or a multiple of 64 keys per thread");
-                    uint32_t rr[32];
-                    tmem_ld32(tl + s_col + hf * KB, rr);
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) s[e] = __uint_as_float(rr[e]);
-                }
+                for (int e = 0; e < 64; ++e) s[e] = __uint_as_float(rr[e]);
             }
             // S_j is in registers: its buffer may take the scores of tile j + 2
             tc_fence_before();
@@ -694,13 +684,7 @@ __device__ void run_softmax(const PrefillParams& p, const Bars& bars, uint32_t s
                                                                    abort_flag, p.status)))
                     return;
                 tc_fence_after();
-                if constexpr (KB / 2 >= 32) {
-#pragma unroll
-                    for (int c = 0; c < KB / 2; c += 32)
-                        tmem_st32(tl + C::TM_P + hf * (KB / 2) + c, *reinterpret_cast<const uint32_t(*)[32]>(pk + c));
-                } else {
-                    tmem_st16(tl + C::TM_P + hf * (KB / 2), pk);
-                }
+                tmem_st32(tl + C::TM_P + hf * (KB / 2), pk);
                 l += ((rs2[0].x + rs2[0].y) + (rs2[1].x + rs2[1].y)) + ((rs2[2].x + rs2[2].y) + (rs2[3].x + rs2[3].y));
                 tmem_wait_st();
                 tc_fence_before();
