@@ -12,7 +12,8 @@ it runs on.
   roofline     the dominant kernel (tcgen05 prefill) against measured bf16 peak,
                plus the decode split kernel against measured HBM copy bandwidth
   e2e          prefill through the public API with pinned host buffers, H2D and
-               D2H copies inside the timed region
+               D2H copies inside the timed region (steps pipelined: two device
+               slots, copy streams beside the compute stream)
   cpu_baseline the fp64 oracle on a bounded sample of the prefill workload
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
@@ -333,28 +334,53 @@ def main():
     dec_gbs = world * dbytes / (t["d"] * 1e-3) / 1e9 if do_d else float("nan")
     dec_kern_gbs = dbytes / (t["dk"] * 1e-3) / 1e9 if do_d else float("nan")
 
-    # ---- end to end through the public API: pinned host -> device, prefill, device -> host
+    # ---- end to end through the public API: pinned host -> device, prefill, device -> host.
+    # Steps are pipelined the way a serving loop runs them: two device slots; step i's
+    # inputs go in on a copy stream while step i-1 computes, and its result comes back
+    # on another copy stream while step i+1 computes.  Every step's copies are inside
+    # the timed region (it ends when the last result has reached the host).
     host_in = {k: v.pin_memory() for k, v in pin.items()}
     host_out = torch.empty(p_out.shape, dtype=p_out.dtype).pin_memory()
     h2d = sum(v.numel() * v.element_size() for v in host_in.values())
     d2h = host_out.numel() * host_out.element_size()
-    e2e_bufs = {k: torch.empty_like(v, device=dev) for k, v in pin.items()}
+    NSLOT = 2
+    e2e_in = [{k: torch.empty_like(v, device=dev) for k, v in pin.items()} for _ in range(NSLOT)]
+    e2e_out = [torch.empty_like(p_out) for _ in range(NSLOT)]
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ev_in = [torch.cuda.Event() for _ in range(NSLOT)]    # the slot's inputs have landed
+    ev_done = [torch.cuda.Event() for _ in range(NSLOT)]  # the slot's prefill is done (inputs free, result ready)
+    ev_out = [torch.cuda.Event() for _ in range(NSLOT)]   # the slot's result has been copied out
 
-    def e2e_step():
-        for k, v in host_in.items():
-            e2e_bufs[k].copy_(v, non_blocking=True)
-        ga.gattn_prefill(e2e_bufs["q"], e2e_bufs["k"], e2e_bufs["v"], e2e_bufs["gate"], e2e_bufs["qnorm_w"],
-                         e2e_bufs["knorm_w"], rotary_dim=wp.rotary_dim, rope_base=wp.rope_base, eps=wp.eps,
-                         gate_mode=wp.gate_mode, out=p_out, workspace=p_ws)
-        host_out.copy_(p_out, non_blocking=True)
+    def e2e_step(i):
+        sl = i % NSLOT
+        s_in.wait_event(ev_done[sl])  # step i-2 no longer reads the slot's inputs
+        with torch.cuda.stream(s_in):
+            for k, v in host_in.items():
+                e2e_in[sl][k].copy_(v, non_blocking=True)
+        ev_in[sl].record(s_in)
+        stream.wait_event(ev_in[sl])
+        stream.wait_event(ev_out[sl])  # step i-2's result has left the slot
+        b = e2e_in[sl]
+        ga.gattn_prefill(b["q"], b["k"], b["v"], b["gate"], b["qnorm_w"], b["knorm_w"], rotary_dim=wp.rotary_dim,
+                         rope_base=wp.rope_base, eps=wp.eps, gate_mode=wp.gate_mode, out=e2e_out[sl],
+                         workspace=p_ws, stream=stream)
+        ev_done[sl].record(stream)
+        s_out.wait_event(ev_done[sl])
+        with torch.cuda.stream(s_out):
+            host_out.copy_(e2e_out[sl], non_blocking=True)
+        ev_out[sl].record(s_out)
 
-    for _ in range(3 if do_p else 0):
-        e2e_step()
+    for i in range(3 if do_p else 0):
+        e2e_step(i)
     torch.cuda.synchronize()
     e0, e1 = ev(), ev()
     e0.record(stream)
-    for _ in range(K if do_p else 0):
-        e2e_step()
+    s_in.wait_event(e0)
+    s_out.wait_event(e0)
+    for i in range(K if do_p else 0):
+        e2e_step(i)
+    for sl in range(NSLOT):
+        stream.wait_event(ev_out[sl])  # the last results are on the host
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / K
