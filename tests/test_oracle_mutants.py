@@ -12,6 +12,7 @@ import os
 import subprocess
 import ctypes
 
+import numpy as np
 import pytest
 
 import oracle
@@ -114,3 +115,50 @@ def test_pins_catch_mutant(mutant, tmp_path):
     finally:
         oracle._lib = real
     assert caught, "no pin caught mutant " + mutant
+
+
+# The packed-sequence oracle is a Python wrapper over the batched one: plausible
+# mistakes in it, planted in a copy of the wrapper, must fail a pin too.
+def _varlen_mutant(kind):
+    def mutant(q, k, v, gate_logits, qnorm_w, knorm_w, pos, cu_seqlens, rotary_dim, rope_base, eps, gate_mode):
+        q, k, v = np.asarray(q, np.float64), np.asarray(k, np.float64), np.asarray(v, np.float64)
+        T, H, d = q.shape
+        cu = [int(x) for x in np.asarray(cu_seqlens)]
+        z = None if gate_logits is None else np.asarray(gate_logits, np.float64)
+        p = None if pos is None else np.asarray(pos, np.float64)
+        out = np.zeros((T, H * d))
+        for i in range(len(cu) - 1):
+            s, e = cu[i], cu[i + 1]
+            if e <= s:
+                continue
+            ps = p[s:e] if p is not None else None
+            if kind == "positions_continue" and p is None:
+                ps = np.arange(s, e, dtype=np.float64)  # positions run on across sequences
+            lo = s
+            if kind == "keys_leak_from_previous" and i > 0:
+                lo = cu[i - 1]  # the previous sequence's tokens are visible too
+                if ps is not None:
+                    ps = np.concatenate([np.arange(s - lo, dtype=np.float64), ps])
+            zs = None if z is None else z[lo:e]
+            if kind == "gate_of_previous_sequence" and z is not None and i > 0 and cu[i] - cu[i - 1] >= e - s:
+                zs = z[cu[i - 1]:cu[i - 1] + (e - s)]
+            res = oracle.prefill(q[None, lo:e], k[None, lo:e], v[None, lo:e], None if zs is None else zs[None],
+                                 qnorm_w, knorm_w, None if ps is None else ps[None], rotary_dim, rope_base, eps,
+                                 gate_mode)[0]
+            out[s:e] = res[s - lo:]
+        return out
+    return mutant
+
+
+@pytest.mark.parametrize("kind", ["positions_continue", "keys_leak_from_previous", "gate_of_previous_sequence"])
+def test_pins_catch_varlen_mutant(kind, monkeypatch):
+    monkeypatch.setattr(oracle, "prefill_varlen", _varlen_mutant(kind))
+    with pytest.raises(AssertionError):
+        pins.test_varlen_sequences_are_independent_batches()
+
+
+def test_varlen_mutant_harness_is_faithful(monkeypatch):
+    """With no mistake planted the copied wrapper passes the pin (so the mutants
+    above fail for their mistake, not for the copy)."""
+    monkeypatch.setattr(oracle, "prefill_varlen", _varlen_mutant("none"))
+    pins.test_varlen_sequences_are_independent_batches()
