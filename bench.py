@@ -65,6 +65,9 @@ def parse():
     ap.add_argument("--decode-batch", type=int, default=None,
                     help="override the decode batch (smaller profiling case; not a bench line)")
     ap.add_argument("--cpu-budget-s", type=float, default=12.0)
+    ap.add_argument("--next-rows", action="store_true",
+                    help="time the scope table's next rows (append / paged decode, packed sequences, gate "
+                         "variants) and print their own JSON line")
     return ap.parse_args()
 
 
@@ -216,10 +219,139 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def run_next_rows(args):
+    """The scope table's next rows, each timed like the headline calls (CUDA events
+    around the call on its stream, L2 flushed before each, median of --steps after
+    --warmup) on the headline shapes: decode with the new token appended and decode
+    through a paged cache (GB/s of the algorithmic K/V + q/gate/out bytes, against
+    the measured HBM copy), packed-sequence prefill and two gate variants (TFLOP/s
+    against the measured bf16 peak).  One JSON line; one GPU."""
+    import torch
+
+    import gated_softmax_attention_gqa_gb300 as ga
+    from gated_softmax_attention_gqa_gb300.workloads import (WORKLOADS, decode_io_bytes, make_decode_inputs,
+                                                             make_prefill_inputs, prefill_flops)
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    hbm_peak, bf16_peak, peak_kind = peaks()
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def timed(fn):
+        for _ in range(max(3, args.warmup)):
+            flush.zero_()
+            fn()
+        torch.cuda.synchronize()
+        evs = []
+        for _ in range(args.steps):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            evs.append((a, b))
+        torch.cuda.synchronize()
+        if ga.gattn_get_device_status() != 0:
+            raise RuntimeError("device status set")
+        return statistics.median(a.elapsed_time(b) for a, b in evs)
+
+    rows = {}
+    gen = torch.Generator().manual_seed(7)
+
+    # ---- decode (the 64-sequence bf16-cache step): contiguous, with append, paged
+    wd = WORKLOADS[DECODE]
+    din = make_decode_inputs(wd)
+    d = {k: v.to(dev) for k, v in din.items()}
+    seqlens = din["seqlens"].tolist()
+    dbytes = decode_io_bytes(seqlens, wd.H, wd.G, wd.d, wd.gate_mode)
+    d_out = torch.empty((wd.B, wd.H * wd.d), dtype=torch.bfloat16, device=dev)
+    d_ws = torch.empty(ga.gattn_decode_workspace_size(wd.B, wd.H, wd.G, wd.d, wd.Lmax), dtype=torch.uint8,
+                       device=dev)
+    dkw = dict(rotary_dim=wd.rotary_dim, rope_base=wd.rope_base, eps=wd.eps, gate_mode=wd.gate_mode, out=d_out,
+               workspace=d_ws)
+
+    def hbm_row(ms):
+        gbs = dbytes / (ms * 1e-3) / 1e9
+        return {"ms": ms, "value": gbs, "unit": "GB/s", "frac": gbs / hbm_peak}
+
+    rows["decode_contiguous"] = hbm_row(timed(lambda: ga.gattn_decode(d["q_new"], d["kv_cache"], d["seqlens"],
+                                                                       d["gate"], d["qnorm_w"], **dkw)))
+    k_new = torch.randn(wd.B, wd.G, wd.d, generator=gen).to(torch.bfloat16).to(dev)
+    v_new = torch.randn(wd.B, wd.G, wd.d, generator=gen).to(torch.bfloat16).to(dev)
+    knorm_w = (1.0 + 0.1 * torch.randn(wd.d, generator=gen)).to(torch.bfloat16).to(dev)
+    rows["decode_append"] = hbm_row(timed(lambda: ga.gattn_decode_append(
+        d["q_new"], k_new, v_new, d["kv_cache"], d["seqlens"], d["gate"], d["qnorm_w"], knorm_w, **dkw)))
+    # the same cache in a page pool: 256-token pages, each sequence's pages scattered
+    # over the pool by a seeded permutation
+    ps = 256
+    n_pages = [(L + ps - 1) // ps for L in seqlens]
+    perm = torch.randperm(sum(n_pages), generator=gen)
+    pool = torch.empty((2, sum(n_pages), wd.G, ps, wd.d), dtype=torch.bfloat16, device=dev)
+    table = torch.zeros((wd.B, max(n_pages)), dtype=torch.int32)
+    at = 0
+    for b, n in enumerate(n_pages):
+        ids = perm[at:at + n]
+        at += n
+        table[b, :n] = ids.to(torch.int32)
+        src = d["kv_cache"][:, b, :, :n * ps].reshape(2, wd.G, n, ps, wd.d).permute(0, 2, 1, 3, 4)
+        pool[:, ids.to(dev)] = src
+    table = table.to(dev)
+    rows["decode_paged_256"] = hbm_row(timed(lambda: ga.gattn_decode_paged(
+        d["q_new"], pool, table, d["seqlens"], d["gate"], d["qnorm_w"], **dkw)))
+    del pool, d
+
+    # ---- prefill on the Qwen3.5-0.8B-shaped layer's 4096 tokens
+    wp = WORKLOADS[PREFILL]
+    pin = make_prefill_inputs(wp)
+    p = {k: v.to(dev) for k, v in pin.items()}
+    p_out = torch.empty((wp.B, wp.S, wp.H * wp.d), dtype=torch.bfloat16, device=dev)
+    p_ws = torch.empty(ga.gattn_prefill_workspace_size(wp.B, wp.S, wp.H, wp.G, wp.d), dtype=torch.uint8, device=dev)
+    pkw = dict(rotary_dim=wp.rotary_dim, rope_base=wp.rope_base, eps=wp.eps)
+
+    def tensor_row(ms, flops):
+        tf = flops / (ms * 1e-3) / 1e12
+        return {"ms": ms, "value": tf, "unit": "TFLOP/s", "frac": tf / bf16_peak}
+
+    full = prefill_flops(wp.B, wp.S, wp.H, wp.d)
+    rows["prefill_default_gate"] = tensor_row(timed(lambda: ga.gattn_prefill(
+        p["q"], p["k"], p["v"], p["gate"], p["qnorm_w"], p["knorm_w"], gate_mode=wp.gate_mode, out=p_out,
+        workspace=p_ws, **pkw)), full)
+    rows["prefill_silu_additive_gate"] = tensor_row(timed(lambda: ga.gattn_prefill(
+        p["q"], p["k"], p["v"], p["gate"], p["qnorm_w"], p["knorm_w"], gate_mode="elementwise", gate_act="silu",
+        gate_additive=True, out=p_out, workspace=p_ws, **pkw)), full)
+    z_shared = torch.randn(wp.B, wp.S, wp.d, generator=gen).to(torch.bfloat16).to(dev)
+    rows["prefill_head_shared_gate"] = tensor_row(timed(lambda: ga.gattn_prefill(
+        p["q"], p["k"], p["v"], z_shared, p["qnorm_w"], p["knorm_w"], gate_mode="head_shared", out=p_out,
+        workspace=p_ws, **pkw)), full)
+    # the same tokens as packed sequences of mixed lengths
+    lens = [2048, 1024, 512, 256, 128, 128]
+    assert sum(lens) == wp.S
+    cu = [0]
+    for n in lens:
+        cu.append(cu[-1] + n)
+    vflops = sum(prefill_flops(1, n, wp.H, wp.d) for n in lens)
+    v_ws = torch.empty(ga.gattn_prefill_varlen_workspace_size(wp.S, len(lens), wp.H, wp.G, wp.d),
+                       dtype=torch.uint8, device=dev)
+    rows["prefill_packed_6_sequences"] = tensor_row(timed(lambda: ga.gattn_prefill_varlen(
+        p["q"][0], p["k"][0], p["v"][0], p["gate"][0], p["qnorm_w"], p["knorm_w"], cu, gate_mode=wp.gate_mode,
+        out=p_out[0], workspace=v_ws, **pkw)), vflops)
+
+    line = {"next_rows": rows, "peaks": {"hbm_gbs": hbm_peak, "bf16_tflops": bf16_peak, "kind": peak_kind},
+            "steps": args.steps, "warmup": args.warmup, "l2": "flushed (256 MiB write) before every timed call",
+            "config": {"decode": f"{DECODE} (B{wd.B} H{wd.H} G{wd.G} d{wd.d}, lengths U[16384,32768]); paged: "
+                                 f"{ps}-token pages in a shuffled pool",
+                       "prefill": f"{PREFILL} (B1 S4096 H8 G2 d256); packed: lengths {lens}"}}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse()
     if args.impl == "reference":
         run_reference(args)
+        return
+    if args.next_rows:
+        run_next_rows(args)
         return
 
     import torch

@@ -22,7 +22,7 @@ GATE_ACTS = {"sigmoid": 0x00, "ns_sigmoid": 0x10, "silu": 0x20}
 GATE_ADDITIVE = 0x100
 DTYPES = {torch.bfloat16: 0, torch.float32: 1}
 
-__all__ = ["gattn_prefill", "gattn_prefill_varlen", "gattn_decode", "gattn_decode_append", "gattn_decode_paged", "gattn_decode_noalloc", "gattn_prefill_workspace_size", "gattn_decode_workspace_size",
+__all__ = ["gattn_prefill", "gattn_prefill_varlen", "gattn_decode", "gattn_decode_append", "gattn_decode_paged", "gattn_decode_noalloc", "gattn_prefill_workspace_size", "gattn_prefill_varlen_workspace_size", "gattn_decode_workspace_size",
            "gattn_get_device_status", "gattn_set_profile_events", "gattn_strerror", "GattnError", "GATE_MODES",
            "GATE_ACTS", "GATE_ADDITIVE"]
 
@@ -55,6 +55,10 @@ def gattn_strerror(status: int) -> str:
 
 def gattn_prefill_workspace_size(B, S, H, G, d, dtype=torch.bfloat16) -> int:
     return _lib.load().gattn_prefill_workspace_size(B, S, H, G, d, DTYPES[dtype])
+
+
+def gattn_prefill_varlen_workspace_size(T, nseq, H, G, d, dtype=torch.bfloat16) -> int:
+    return _lib.load().gattn_prefill_varlen_workspace_size(T, nseq, H, G, d, DTYPES[dtype])
 
 
 def gattn_decode_workspace_size(B, H, G, d, Lmax) -> int:
