@@ -64,7 +64,7 @@ def parse():
                     help="run one half of the path only (profiling runs; not a bench line)")
     ap.add_argument("--decode-batch", type=int, default=None,
                     help="override the decode batch (smaller profiling case; not a bench line)")
-    ap.add_argument("--cpu-budget-s", type=float, default=12.0)
+    ap.add_argument("--cpu-budget-s", type=float, default=8.0)
     ap.add_argument("--next-rows", action="store_true",
                     help="time the scope table's next rows (append / paged decode, packed sequences, gate "
                          "variants) and print their own JSON line")
@@ -173,8 +173,8 @@ def cpu_baseline(w, inputs, budget_s):
             rb = np.repeat(np.arange(w.B, dtype=np.int32), w.S)
             rt = np.tile(np.arange(w.S, dtype=np.int32), w.B)
         else:
-            rt = np.sort(rng.choice(w.S, size=n, replace=False)).astype(np.int32)
-            rb = rng.integers(0, w.B, size=n).astype(np.int32)
+            flat = np.sort(rng.choice(w.B * w.S, size=n, replace=False))
+            rb, rt = (flat // w.S).astype(np.int32), (flat % w.S).astype(np.int32)
         t0 = time.perf_counter()
         oracle.prefill_rows(inputs["q"], inputs["k"], inputs["v"], inputs["gate"], inputs["qnorm_w"],
                             inputs["knorm_w"], None, w.rotary_dim, w.rope_base, w.eps, w.gate_mode, rb, rt)
@@ -190,33 +190,54 @@ def cpu_baseline(w, inputs, budget_s):
 
 
 def run_reference(args):
-    """Reference arm: the fp64 oracle timed on the host cores (rank 0 only)."""
+    """Reference arm: the fp64 oracle timed on the host cores (rank 0 only), on the
+    same step as the GPU arm -- the headline prefill then the decode step -- each a
+    bounded sample of its workload.  value = prefill TFLOP/s of the sample;
+    ms_per_step = the oracle's time for one whole step at the sampled rates."""
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
-    from gated_softmax_attention_gqa_gb300.workloads import WORKLOADS, make_prefill_inputs
+    from gated_softmax_attention_gqa_gb300.workloads import (WORKLOADS, decode_io_bytes, make_decode_inputs,
+                                                             make_prefill_inputs, prefill_flops)
 
     w = WORKLOADS[args.prefill]
+    wd = WORKLOADS[DECODE]
     inputs = make_prefill_inputs(w)
     per_step = max(2.0, 60.0 / max(1, args.steps + args.warmup))
     for _ in range(args.warmup):
         cpu_baseline(w, inputs, min(per_step, 2.0))
-    vals, secs = [], 0.0
-    last = None
+    vals, dvals = [], []
+    last = dlast = None
     for _ in range(args.steps):
-        last = cpu_baseline(w, inputs, per_step)
+        last = cpu_baseline(w, inputs, per_step * 0.75)
+        dlast = cpu_decode_baseline(wd, per_step * 0.25)
         vals.append(last["value"])
-        secs += last["seconds"]
-    v = statistics.median(vals)
+        dvals.append(dlast["value"])
+    v, dv = statistics.median(vals), statistics.median(dvals)
+    # the full step at these rates: the whole prefill's FLOPs and the whole decode step's bytes
+    seqlens = torch_free_seqlens(wd)
+    step_ms = 1e3 * (prefill_flops(w.B, w.S, w.H, w.d) / (v * 1e12) +
+                     decode_io_bytes(seqlens, wd.H, wd.G, wd.d, wd.gate_mode) / (dv * 1e9))
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "TFLOP/s", "n_gpus": args.gpus,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * secs / args.steps,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": w.name, "B": w.B, "S": w.S, "H": w.H, "G": w.G, "d": w.d,
-                       "rotary_dim": w.rotary_dim, "gate": w.gate_mode},
+            "config": step_config(w, wd, args.gpus, seqlens),
+            "decode": {"value": dv, "unit": "GB/s", "sample": dlast["sample"]},
             "cpu_baseline": {"value": v, "unit": "TFLOP/s", "cores": last["cores"], "kind": "oracle",
-                             "sample": last["sample"]},
+                             "sample": last["sample"] + "; decode: " + dlast["sample"] +
+                             "; ms_per_step extrapolates both samples' rates to the whole step"},
             "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
+
+
+def torch_free_seqlens(wd):
+    """The decode workload's sequence lengths (the same seeded draw as its inputs,
+    without generating the cache)."""
+    import torch
+
+    g = torch.Generator("cpu").manual_seed(wd.seed)
+    lo, hi = wd.seqlen_range
+    return torch.randint(lo, hi + 1, (wd.B,), generator=g, dtype=torch.int64).tolist()
 
 
 def run_next_rows(args):
@@ -345,6 +366,86 @@ def run_next_rows(args):
     print(json.dumps(line), flush=True)
 
 
+# prefill workloads of the default run: the headline (Qwen3.5-0.8B-shaped layer) first, then the
+# Qwen3-0.6B-shaped and the paper-MoE-shaped layers, each timed and reported on its own
+PREFILLS = [PREFILL, "qwen3_06b_prefill", "paper_moe_prefill"]
+
+
+def prefill_kernel(w):
+    """(name, source files, committed ncu summary) of the attention kernel a bf16
+    prefill workload runs on."""
+    common = ["common.cuh", "internal.h"]
+    if w.d == 256 and (w.H // w.G) % 2 == 0:
+        return "prefill_pair_kernel<256, false>", ["prefill_pair.cu"] + common, "prefill_pair_qwen35_08b.md"
+    summary = {"qwen3_06b_prefill": "prefill_tc_qwen3_06b.md", "paper_moe_prefill": "prefill_tc_paper_moe.md"}
+    return f"prefill_tc_kernel<{w.d}, false>", ["prefill_tc.cu"] + common, summary.get(w.name, "")
+
+
+def step_config(wp, wd, world, seqlens):
+    """The workload description shared by both arms' JSON lines."""
+    return {"workload": f"{wp.name} + {wd.name}",
+            "prefill": {"B": wp.B, "S": wp.S, "H": wp.H, "G": wp.G, "d": wp.d, "rotary_dim": wp.rotary_dim,
+                        "rope_base": wp.rope_base, "gate": wp.gate_mode},
+            "decode": {"B": wd.B, "H": wd.H, "G": wd.G, "d": wd.d, "Lmax": wd.Lmax,
+                       "seqlens": f"U[{wd.seqlen_range[0]},{wd.seqlen_range[1]}] seed {wd.seed}",
+                       "sum_seqlens": sum(seqlens)},
+            "l2": "flushed (256 MiB write) before every timed call", "parallelism": f"replicas x{world}"}
+
+
+def cpu_decode_baseline(w, budget_s):
+    """The fp64 oracle on a bounded sample of the decode workload: whole sequences of
+    its shape and length distribution (a two-sequence cache is generated for it);
+    GB/s of the algorithmic K/V + q/gate/out bytes of the sequences computed."""
+    import oracle
+    from gated_softmax_attention_gqa_gb300.workloads import decode_io_bytes, make_decode_inputs
+
+    inp = make_decode_inputs(w, B=2)
+    sl = inp["seqlens"].tolist()
+    n, dt = 0, 0.0
+    t0 = time.perf_counter()
+    while dt < budget_s * 0.5 or n == 0:
+        oracle.decode(inp["q_new"], inp["kv_cache"][0], inp["kv_cache"][1], inp["seqlens"], inp["gate"],
+                      inp["qnorm_w"], w.rotary_dim, w.rope_base, w.eps, w.gate_mode)
+        n += 1
+        dt = time.perf_counter() - t0
+    nbytes = n * decode_io_bytes(sl, w.H, w.G, w.d, w.gate_mode)
+    return {"value": nbytes / dt / 1e9, "unit": "GB/s", "cores": oracle.threads_used(), "kind": "oracle",
+            "sample": f"{n} x 2 sequences of {w.name} (lengths {sl}, H{w.H} G{w.G} d{w.d}); fp64 C loops, OpenMP; "
+                      f"{dt:.1f} s", "seconds": dt}
+
+
+def host_link_rates(dev, nbytes):
+    """Plain pinned-memory copy rates between this process's host buffers and the GPU
+    (one cudaMemcpyAsync of nbytes each way, median of 5), with the NUMA node the
+    GPU reports and the CPUs this process may run on."""
+    import torch
+
+    h = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    dbuf = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    out = {"bytes": nbytes}
+    for name, fn in (("h2d_gbs", lambda: dbuf.copy_(h, non_blocking=True)),
+                     ("d2h_gbs", lambda: h.copy_(dbuf, non_blocking=True))):
+        ts = []
+        for _ in range(6):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b))
+        out[name] = nbytes / (statistics.median(ts[1:]) * 1e-3) / 1e9
+    try:
+        bus = torch.cuda.get_device_properties(dev).pci_bus_id if hasattr(
+            torch.cuda.get_device_properties(dev), "pci_bus_id") else None
+        out["cpus_allowed"] = len(os.sched_getaffinity(0))
+        if bus:
+            with open(f"/sys/bus/pci/devices/{bus.lower()}/numa_node") as f:
+                out["gpu_numa_node"] = int(f.read().strip())
+    except (OSError, ValueError, AttributeError):
+        pass
+    return out
+
+
 def main():
     args = parse()
     if args.impl == "reference":
@@ -371,28 +472,37 @@ def main():
     stream = torch.cuda.current_stream(dev)
     hbm_peak, bf16_peak, peak_kind = peaks()
 
+    profiling = bool(args.only or args.decode_batch)
     do_p, do_d = args.only in (None, "prefill"), args.only in (None, "decode")
-    wp, wd = WORKLOADS[args.prefill], WORKLOADS[DECODE]
+    # the headline prefill (a profiling run may pick another); the other two are
+    # timed after the headline step in the default run
+    head = args.prefill
+    others = [n for n in PREFILLS if n != head] if not profiling else []
+    wd = WORKLOADS[DECODE]
     if args.decode_batch:
         wd = dataclasses.replace(wd, B=args.decode_batch)
-    pin = make_prefill_inputs(wp)
-    p_dev = {k: v.to(dev) for k, v in pin.items()} if do_p else {}
+
+    P = {}  # per prefill workload: workload, host inputs, device inputs, out, workspace
+    for name in ([head] if do_p else []) + others:
+        w = WORKLOADS[name]
+        pin = make_prefill_inputs(w)
+        P[name] = {"w": w, "pin": pin, "dev": {k: v.to(dev) for k, v in pin.items()},
+                   "out": torch.empty((w.B, w.S, w.H * w.d), dtype=torch.bfloat16, device=dev),
+                   "ws": torch.empty(ga.gattn_prefill_workspace_size(w.B, w.S, w.H, w.G, w.d), dtype=torch.uint8,
+                                     device=dev)}
     din = make_decode_inputs(wd) if do_d else None
     d_dev = {k: v.to(dev) for k, v in din.items()} if do_d else {}
     seqlens = din["seqlens"].tolist() if do_d else [1]
-    p_out = torch.empty((wp.B, wp.S, wp.H * wp.d), dtype=torch.bfloat16, device=dev)
-    p_ws = torch.empty(ga.gattn_prefill_workspace_size(wp.B, wp.S, wp.H, wp.G, wp.d), dtype=torch.uint8, device=dev)
     d_out = torch.empty((wd.B, wd.H * wd.d), dtype=torch.bfloat16, device=dev)
     d_ws = torch.empty(ga.gattn_decode_workspace_size(wd.B, wd.H, wd.G, wd.d, wd.Lmax), dtype=torch.uint8,
                        device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
 
-    def prefill():
-        if not do_p:
-            return
-        ga.gattn_prefill(p_dev["q"], p_dev["k"], p_dev["v"], p_dev["gate"], p_dev["qnorm_w"], p_dev["knorm_w"],
-                         rotary_dim=wp.rotary_dim, rope_base=wp.rope_base, eps=wp.eps, gate_mode=wp.gate_mode,
-                         out=p_out, workspace=p_ws)
+    def prefill(name):
+        e = P[name]
+        w, x = e["w"], e["dev"]
+        ga.gattn_prefill(x["q"], x["k"], x["v"], x["gate"], x["qnorm_w"], x["knorm_w"], rotary_dim=w.rotary_dim,
+                         rope_base=w.rope_base, eps=w.eps, gate_mode=w.gate_mode, out=e["out"], workspace=e["ws"])
 
     def decode():
         if not do_d:
@@ -405,8 +515,9 @@ def main():
         return torch.cuda.Event(enable_timing=True)
 
     for _ in range(max(3, args.warmup)):
-        flush.zero_()
-        prefill()
+        for name in P:
+            flush.zero_()
+            prefill(name)
         flush.zero_()
         decode()
     torch.cuda.synchronize()
@@ -414,7 +525,8 @@ def main():
         raise RuntimeError("device status set during warm-up")
 
     K = args.steps
-    evs = {k: [(ev(), ev()) for _ in range(K)] for k in ("p", "pk", "d", "dk")}
+    keys = ["d", "dk"] + [f"{n}:call" for n in P] + [f"{n}:kernel" for n in P]
+    evs = {k: [(ev(), ev()) for _ in range(K)] for k in keys}
     for pairs in evs.values():  # create every event before the timed region
         for a, b in pairs:
             a.record(stream)
@@ -425,139 +537,172 @@ def main():
         dist.barrier()
     torch.cuda.synchronize()
     sampler.mark_start()
-    # Timed region 1: the calls exactly as a user makes them (the headline numbers).
+    # Timed region 1: the headline step exactly as a user makes its calls: the prefill,
+    # then the decode step.
     for i in range(K):
-        flush.zero_()
-        evs["p"][i][0].record(stream)
-        prefill()
-        evs["p"][i][1].record(stream)
+        if do_p:
+            flush.zero_()
+            evs[f"{head}:call"][i][0].record(stream)
+            prefill(head)
+            evs[f"{head}:call"][i][1].record(stream)
         flush.zero_()
         evs["d"][i][0].record(stream)
         decode()
         evs["d"][i][1].record(stream)
-    # Timed region 2: the same calls with the library recording events around its
-    # main attention kernel (the roofline numbers).  Kept separate because an event
-    # between the K pre-pass and the attention kernel stops them from overlapping.
+    # Timed region 2: the same calls with the library recording events around its main
+    # attention kernel (the roofline numbers).  Kept separate because an event between
+    # the K pre-pass and the attention kernel stops them from overlapping.
     for i in range(K):
-        flush.zero_()
-        ga.gattn_set_profile_events(*evs["pk"][i])
-        prefill()
+        if do_p:
+            flush.zero_()
+            ga.gattn_set_profile_events(*evs[f"{head}:kernel"][i])
+            prefill(head)
         flush.zero_()
         ga.gattn_set_profile_events(*evs["dk"][i])
         decode()
+    ga.gattn_set_profile_events(None, None)
+    # Timed region 3: the other prefill workloads, whole calls then kernel alone.
+    for name in others:
+        for i in range(K):
+            flush.zero_()
+            evs[f"{name}:call"][i][0].record(stream)
+            prefill(name)
+            evs[f"{name}:call"][i][1].record(stream)
+        for i in range(K):
+            flush.zero_()
+            ga.gattn_set_profile_events(*evs[f"{name}:kernel"][i])
+            prefill(name)
+        ga.gattn_set_profile_events(None, None)
     torch.cuda.synchronize()
     sampler.mark_end()
     if world > 1:
         dist.barrier()
-    ga.gattn_set_profile_events(None, None)
     clocks = sampler.stop()
 
     def ms(key):
-        return [a.elapsed_time(b) for a, b in evs[key]]
+        return statistics.mean(a.elapsed_time(b) for a, b in evs[key])
 
-    t = {k: statistics.mean(ms(k)) if (do_p if k[0] == "p" else do_d) else float("nan") for k in evs}
-    t = dict(zip(("p", "pk", "d", "dk"), reduce_max([t["p"], t["pk"], t["d"], t["dk"]], dev)))
+    t = {k: ms(k) if (k[0] != "d" or do_d) else float("nan") for k in keys}
+    t = dict(zip(keys, reduce_max([t[k] for k in keys], dev)))
     status = ga.gattn_get_device_status()
 
-    flops = prefill_flops(wp.B, wp.S, wp.H, wp.d)
     dbytes = decode_io_bytes(seqlens, wd.H, wd.G, wd.d, wd.gate_mode)
-    value = world * flops / (t["p"] * 1e-3) / 1e12 if do_p else float("nan")
-    kern_tflops = flops / (t["pk"] * 1e-3) / 1e12 if do_p else float("nan")
     dec_gbs = world * dbytes / (t["d"] * 1e-3) / 1e9 if do_d else float("nan")
     dec_kern_gbs = dbytes / (t["dk"] * 1e-3) / 1e9 if do_d else float("nan")
+
+    def prefill_entry(name):
+        w = P[name]["w"]
+        flops = prefill_flops(w.B, w.S, w.H, w.d)
+        call, kern = t[f"{name}:call"], t[f"{name}:kernel"]
+        kname, src, summary = prefill_kernel(w)
+        kt = flops / (kern * 1e-3) / 1e12
+        return {"workload": name, "shape": {"B": w.B, "S": w.S, "H": w.H, "G": w.G, "d": w.d,
+                                            "rotary_dim": w.rotary_dim, "gate": w.gate_mode},
+                "flops": flops, "ms": call, "kernel_ms": kern, "value": world * flops / (call * 1e-3) / 1e12,
+                "unit": "TFLOP/s",
+                "roofline": {"bound": "tensor", "achieved": kt, "peak": bf16_peak, "unit": "TFLOP/s",
+                             "frac": kt / bf16_peak, "peak_kind": f"{peak_kind} bf16 dense (burst)", "kernel": kname,
+                             "traffic": profiled_traffic(summary, src) if summary else None}}
+
+    configs = {name: prefill_entry(name) for name in P}
+    value = configs[head]["value"] if do_p else float("nan")
 
     # ---- end to end through the public API: pinned host -> device, prefill, device -> host.
     # Steps are pipelined the way a serving loop runs them: two device slots; step i's
     # inputs go in on a copy stream while step i-1 computes, and its result comes back
     # on another copy stream while step i+1 computes.  Every step's copies are inside
     # the timed region (it ends when the last result has reached the host).
-    host_in = {k: v.pin_memory() for k, v in pin.items()}
-    host_out = torch.empty(p_out.shape, dtype=p_out.dtype).pin_memory()
-    h2d = sum(v.numel() * v.element_size() for v in host_in.values())
-    d2h = host_out.numel() * host_out.element_size()
-    NSLOT = 2
-    e2e_in = [{k: torch.empty_like(v, device=dev) for k, v in pin.items()} for _ in range(NSLOT)]
-    e2e_out = [torch.empty_like(p_out) for _ in range(NSLOT)]
-    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-    ev_in = [torch.cuda.Event() for _ in range(NSLOT)]    # the slot's inputs have landed
-    ev_done = [torch.cuda.Event() for _ in range(NSLOT)]  # the slot's prefill is done (inputs free, result ready)
-    ev_out = [torch.cuda.Event() for _ in range(NSLOT)]   # the slot's result has been copied out
+    e2e_val, e2e_ms, h2d, d2h, link = float("nan"), float("nan"), 0, 0, {}
+    if do_p:
+        wp, pin, p_out, p_ws = P[head]["w"], P[head]["pin"], P[head]["out"], P[head]["ws"]
+        host_in = {k: v.pin_memory() for k, v in pin.items()}
+        host_out = torch.empty(p_out.shape, dtype=p_out.dtype).pin_memory()
+        h2d = sum(v.numel() * v.element_size() for v in host_in.values())
+        d2h = host_out.numel() * host_out.element_size()
+        NSLOT = 2
+        e2e_in = [{k: torch.empty_like(v, device=dev) for k, v in pin.items()} for _ in range(NSLOT)]
+        e2e_out = [torch.empty_like(p_out) for _ in range(NSLOT)]
+        s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+        ev_in = [torch.cuda.Event() for _ in range(NSLOT)]    # the slot's inputs have landed
+        ev_done = [torch.cuda.Event() for _ in range(NSLOT)]  # the slot's prefill is done (inputs free, result ready)
+        ev_out = [torch.cuda.Event() for _ in range(NSLOT)]   # the slot's result has been copied out
 
-    def e2e_step(i):
-        sl = i % NSLOT
-        s_in.wait_event(ev_done[sl])  # step i-2 no longer reads the slot's inputs
-        with torch.cuda.stream(s_in):
-            for k, v in host_in.items():
-                e2e_in[sl][k].copy_(v, non_blocking=True)
-        ev_in[sl].record(s_in)
-        stream.wait_event(ev_in[sl])
-        stream.wait_event(ev_out[sl])  # step i-2's result has left the slot
-        b = e2e_in[sl]
-        ga.gattn_prefill(b["q"], b["k"], b["v"], b["gate"], b["qnorm_w"], b["knorm_w"], rotary_dim=wp.rotary_dim,
-                         rope_base=wp.rope_base, eps=wp.eps, gate_mode=wp.gate_mode, out=e2e_out[sl],
-                         workspace=p_ws, stream=stream)
-        ev_done[sl].record(stream)
-        s_out.wait_event(ev_done[sl])
-        with torch.cuda.stream(s_out):
-            host_out.copy_(e2e_out[sl], non_blocking=True)
-        ev_out[sl].record(s_out)
+        def e2e_step(i):
+            sl = i % NSLOT
+            s_in.wait_event(ev_done[sl])  # step i-2 no longer reads the slot's inputs
+            with torch.cuda.stream(s_in):
+                for k, v in host_in.items():
+                    e2e_in[sl][k].copy_(v, non_blocking=True)
+            ev_in[sl].record(s_in)
+            stream.wait_event(ev_in[sl])
+            stream.wait_event(ev_out[sl])  # step i-2's result has left the slot
+            b = e2e_in[sl]
+            ga.gattn_prefill(b["q"], b["k"], b["v"], b["gate"], b["qnorm_w"], b["knorm_w"],
+                             rotary_dim=wp.rotary_dim, rope_base=wp.rope_base, eps=wp.eps, gate_mode=wp.gate_mode,
+                             out=e2e_out[sl], workspace=p_ws, stream=stream)
+            ev_done[sl].record(stream)
+            s_out.wait_event(ev_done[sl])
+            with torch.cuda.stream(s_out):
+                host_out.copy_(e2e_out[sl], non_blocking=True)
+            ev_out[sl].record(s_out)
 
-    for i in range(3 if do_p else 0):
-        e2e_step(i)
-    torch.cuda.synchronize()
-    e0, e1 = ev(), ev()
-    e0.record(stream)
-    s_in.wait_event(e0)
-    s_out.wait_event(e0)
-    for i in range(K if do_p else 0):
-        e2e_step(i)
-    for sl in range(NSLOT):
-        stream.wait_event(ev_out[sl])  # the last results are on the host
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / K
-    e2e_ms = reduce_max([e2e_ms], dev)[0]
-    e2e_val = world * flops / (e2e_ms * 1e-3) / 1e12 if do_p and e2e_ms > 0 else float("nan")
+        for i in range(3):
+            e2e_step(i)
+        torch.cuda.synchronize()
+        e0, e1 = ev(), ev()
+        e0.record(stream)
+        s_in.wait_event(e0)
+        s_out.wait_event(e0)
+        for i in range(K):
+            e2e_step(i)
+        for sl in range(NSLOT):
+            stream.wait_event(ev_out[sl])  # the last results are on the host
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = reduce_max([e0.elapsed_time(e1) / K], dev)[0]
+        e2e_val = world * configs[head]["flops"] / (e2e_ms * 1e-3) / 1e12
+        link = host_link_rates(dev, h2d)
 
     if rank == 0:
-        tc_src = ["prefill_pair.cu", "common.cuh", "internal.h"]
         dec_src = ["decode.cu", "common.cuh", "internal.h"]
+        hc = configs.get(head, {})
+        # launches of this library's kernels inside the timed regions: a prefill call is
+        # the K pre-pass + the attention kernel, a decode call the split + combine kernels
+        launches = {"headline_step": 2 * K * (2 * do_p + 2 * do_d), "other_prefills": 4 * K * len(others),
+                    "e2e": 2 * K * do_p}
+        wp = P[head]["w"] if do_p else WORKLOADS[head]
         line = {
             "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": K,
-            "warmup": args.warmup, "ms_per_step": t["p"] + t["d"], "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": f"{wp.name} + {wd.name}",
-                       "prefill": {"B": wp.B, "S": wp.S, "H": wp.H, "G": wp.G, "d": wp.d,
-                                   "rotary_dim": wp.rotary_dim, "rope_base": wp.rope_base, "gate": wp.gate_mode},
-                       "decode": {"B": wd.B, "H": wd.H, "G": wd.G, "d": wd.d, "Lmax": wd.Lmax,
-                                  "seqlens": f"U[{wd.seqlen_range[0]},{wd.seqlen_range[1]}] seed {wd.seed}",
-                                  "sum_seqlens": sum(seqlens)},
-                       "l2": "flushed (256 MiB write) before every timed call", "parallelism": f"replicas x{world}"},
-            "prefill_ms": t["p"], "prefill_kernel_ms": t["pk"],
-            "roofline": {"bound": "tensor", "achieved": kern_tflops, "peak": bf16_peak, "unit": "TFLOP/s",
-                         "frac": kern_tflops / bf16_peak, "peak_kind": f"{peak_kind} bf16 dense (burst)",
-                         "kernel": "prefill_pair_kernel<256, false>",
-                         "traffic": profiled_traffic("prefill_pair_qwen35_08b.md", tc_src)},
+            "warmup": args.warmup, "ms_per_step": (hc.get("ms", 0.0) if do_p else 0.0) + (t["d"] if do_d else 0.0),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": step_config(wp, wd, world, seqlens),
+            "prefill_ms": hc.get("ms"), "prefill_kernel_ms": hc.get("kernel_ms"),
+            "roofline": hc.get("roofline"),
             "decode": {"value": dec_gbs, "unit": "GB/s", "ms": t["d"], "kernel_ms": t["dk"],
                        "bytes_per_step": dbytes,
                        "roofline": {"bound": "hbm", "achieved": dec_kern_gbs, "peak": hbm_peak, "unit": "GB/s",
                                     "frac": dec_kern_gbs / hbm_peak, "frac_of_8TBs": dec_kern_gbs / 8000.0,
                                     "peak_kind": f"{peak_kind} HBM copy", "kernel": "decode_split_kernel<256>",
                                     "traffic": profiled_traffic("decode_split_qwen35_08b.md", dec_src)}},
+            "prefill_configs": configs,
             "e2e": {"value": e2e_val, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                    "ms_per_step": e2e_ms},
-            "gpu_launches": 8 * K,
+                    "ms_per_step": e2e_ms, "host_link": link},
+            "gpu_launches": sum(launches.values()), "gpu_launches_by_region": launches,
             "clocks": clocks,
             "device_status": status,
         }
-        if args.only or args.decode_batch:
-            line = {"profiling_run": True, "only": args.only, "decode_batch": wd.B, "prefill_ms": t["p"],
-                    "prefill_kernel_ms": t["pk"], "decode_ms": t["d"], "decode_kernel_ms": t["dk"],
-                    "prefill_kernel_tflops": kern_tflops, "decode_kernel_gbs": dec_kern_gbs, "clocks": clocks}
+        if profiling:
+            line = {"profiling_run": True, "only": args.only, "decode_batch": wd.B, "prefill": head,
+                    "prefill_ms": hc.get("ms"), "prefill_kernel_ms": hc.get("kernel_ms"),
+                    "decode_ms": t["d"], "decode_kernel_ms": t["dk"],
+                    "prefill_kernel_tflops": hc.get("roofline", {}).get("achieved"),
+                    "decode_kernel_gbs": dec_kern_gbs, "clocks": clocks}
         elif not args.no_cpu_baseline:
-            cb = cpu_baseline(wp, pin, args.cpu_budget_s)
-            cb.pop("seconds", None)
-            line["cpu_baseline"] = cb
+            for name in P:
+                cb = cpu_baseline(P[name]["w"], P[name]["pin"], args.cpu_budget_s)
+                cb.pop("seconds", None)
+                configs[name]["cpu_baseline"] = cb
+            line["cpu_baseline"] = configs[head]["cpu_baseline"]
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.barrier()

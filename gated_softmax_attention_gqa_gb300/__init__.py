@@ -23,7 +23,7 @@ GATE_ADDITIVE = 0x100
 DTYPES = {torch.bfloat16: 0, torch.float32: 1}
 
 __all__ = ["gattn_prefill", "gattn_prefill_varlen", "gattn_decode", "gattn_decode_append", "gattn_decode_paged", "gattn_decode_noalloc", "gattn_prefill_workspace_size", "gattn_prefill_varlen_workspace_size", "gattn_decode_workspace_size",
-           "gattn_get_device_status", "gattn_set_profile_events", "gattn_strerror", "GattnError", "GATE_MODES",
+           "gattn_get_device_status", "gattn_set_profile_events", "gattn_selftest_wait_timeout", "gattn_strerror", "GattnError", "GATE_MODES",
            "GATE_ACTS", "GATE_ADDITIVE"]
 
 
@@ -79,9 +79,18 @@ def gattn_get_device_status(stream=None) -> int:
     """Read and clear the device status bits (GATTN_DEVICE_* in gattn.h)."""
     bits = ctypes.c_uint(0)
     st = _lib.load().gattn_get_device_status(ctypes.byref(bits), _stream_handle(stream, None))
-    if st not in (0, 5):
+    if st not in (0, 5, 6):
         check(st, "gattn_get_device_status")
     return bits.value
+
+
+def gattn_selftest_wait_timeout(limit_ns, waited_ns=None, stream=None):
+    """Launch the bounded-wait self-test: a wait on an mbarrier nothing arrives on,
+    given up after limit_ns (1e6 .. 1e8).  waited_ns: optional int64 CUDA tensor of
+    one element that receives the wait's duration.  The timeout is read back with
+    gattn_get_device_status()."""
+    st = _lib.load().gattn_selftest_wait_timeout(int(limit_ns), _ptr(waited_ns), _stream_handle(stream, None))
+    check(st, "gattn_selftest_wait_timeout")
 
 
 def _head_strides(t, name):
@@ -184,6 +193,22 @@ def gattn_prefill_varlen(q, k, v, gate, qnorm_w, knorm_w, cu_seqlens, pos=None, 
     return out
 
 
+def _check_decode_inputs(q_new, kv_cache, seqlens, gate, qnorm_w, mode, out):
+    """The layout checks every contiguous-cache decode entry point makes before it
+    hands pointers to the library: the kernels index these tensors as dense arrays."""
+    for name, t in (("q_new", q_new), ("kv_cache", kv_cache), ("seqlens", seqlens), ("qnorm_w", qnorm_w)):
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    if mode & 0x0F and not gate.is_contiguous():
+        raise ValueError("gate must be contiguous")
+    if seqlens.dtype != torch.int32:
+        raise ValueError("seqlens must be int32")
+    if q_new.dim() != 3 or kv_cache.dim() != 5 or kv_cache.shape[0] != 2 or kv_cache.shape[1] != q_new.shape[0]:
+        raise ValueError("q_new must be [B,H,d] and kv_cache [2,B,G,Lmax,d]")
+    if out is not None and (not out.is_contiguous() or out.numel() != q_new.numel()):
+        raise ValueError("out must be a contiguous [B,H*d] tensor")
+
+
 def gattn_decode(q_new, kv_cache, seqlens, gate, qnorm_w, *, rotary_dim, rope_base, eps=1e-6,
                  gate_mode="elementwise", gate_act="sigmoid", gate_additive=False, out=None, workspace=None,
                  stream=None):
@@ -194,13 +219,7 @@ def gattn_decode(q_new, kv_cache, seqlens, gate, qnorm_w, *, rotary_dim, rope_ba
     mode = _mode(gate_mode, gate_act, gate_additive)
     B, H, d = q_new.shape
     G, Lmax = kv_cache.shape[2], kv_cache.shape[3]
-    for name, t in (("q_new", q_new), ("kv_cache", kv_cache), ("seqlens", seqlens), ("qnorm_w", qnorm_w)):
-        if not t.is_contiguous():
-            raise ValueError(f"{name} must be contiguous")
-    if mode & 0x0F and not gate.is_contiguous():
-        raise ValueError("gate must be contiguous")
-    if seqlens.dtype != torch.int32:
-        raise ValueError("seqlens must be int32")
+    _check_decode_inputs(q_new, kv_cache, seqlens, gate, qnorm_w, mode, out)
     if out is None:
         out = torch.empty((B, H * d), dtype=q_new.dtype, device=q_new.device)
     need = gattn_decode_workspace_size(B, H, G, d, Lmax)
@@ -291,6 +310,7 @@ def gattn_decode_noalloc(q_new, kv_cache, seqlens, gate, qnorm_w, *, rotary_dim,
     mode = _mode(gate_mode, gate_act, gate_additive)
     B, H, d = q_new.shape
     G, Lmax = kv_cache.shape[2], kv_cache.shape[3]
+    _check_decode_inputs(q_new, kv_cache, seqlens, gate, qnorm_w, mode, out)
     if out is None:
         out = torch.empty((B, H * d), dtype=q_new.dtype, device=q_new.device)
     st = _lib.load().gattn_decode_noalloc(

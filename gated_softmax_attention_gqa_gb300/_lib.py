@@ -19,6 +19,7 @@ EXPORTS = (
     "gattn_decode_noalloc",
     "gattn_get_device_status",
     "gattn_set_profile_events",
+    "gattn_selftest_wait_timeout",
 )
 
 _lib = None
@@ -67,6 +68,8 @@ def load():
     lib.gattn_decode_noalloc.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _d, _f, _i, _vp, _vp]
     lib.gattn_get_device_status.restype = _i
     lib.gattn_get_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint), _vp]
+    lib.gattn_selftest_wait_timeout.restype = _i
+    lib.gattn_selftest_wait_timeout.argtypes = [ctypes.c_ulonglong, _vp, _vp]
     lib.gattn_set_profile_events.restype = None
     lib.gattn_set_profile_events.argtypes = [_vp, _vp]
     _lib = lib

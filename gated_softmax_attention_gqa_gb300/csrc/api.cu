@@ -139,6 +139,33 @@ bool valid_gate_mode(int m) {
     return layout != GATTN_GATE_NONE || m == GATTN_GATE_NONE;
 }
 
+// The bounded-wait self-test: an mbarrier that nothing arrives on.  Warp 0 waits on
+// it through mbar_wait with the caller's short limit, runs out, raises the abort
+// flag and the GATTN_DEVICE_TIMEOUT bit; warp 1 waits with the kernels' own 2 s
+// limit and must leave on the abort flag alone, as a kernel's other roles do when
+// one of them gives up.  Every wait ends; the block exits normally.
+__global__ void __launch_bounds__(64) selftest_wait_kernel(unsigned long long limit_ns, unsigned int* status,
+                                                           unsigned long long* waited_ns) {
+    __shared__ __align__(8) unsigned long long bar;
+    __shared__ int abort_word;
+    const uint32_t b = smem_u32(&bar);
+    if (threadIdx.x == 0) {
+        mbar_init(b, 1);
+        abort_word = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    volatile int* abort_flag = &abort_word;
+    const unsigned long long t0 = global_timer_ns();
+    if (threadIdx.x < 32) {
+        mbar_wait(b, 0, abort_flag, status, limit_ns);
+        if (threadIdx.x == 0 && waited_ns) *waited_ns = global_timer_ns() - t0;
+    } else {
+        mbar_wait(b, 0, abort_flag, status);
+    }
+    __syncthreads();
+}
+
 size_t prefill_ws(int B, int S, int H, int G, int d, int dtype) {
     if (B < 1 || S < 1 || H < 1 || G < 1 || d < 1) return 0;
     const size_t kr = (size_t)B * G * S * d, qr = (size_t)B * H * S * d;
@@ -363,6 +390,7 @@ const char* gattn_strerror(gattn_status s) {
         case GATTN_ERR_CUDA: return "GATTN_ERR_CUDA: a CUDA call or kernel launch failed";
         case GATTN_ERR_WORKSPACE: return "GATTN_ERR_WORKSPACE: workspace missing, misaligned or too small";
         case GATTN_ERR_DEVICE: return "GATTN_ERR_DEVICE: a kernel reported a device-side problem";
+        case GATTN_ERR_DEVICE_TIMEOUT: return "GATTN_ERR_DEVICE_TIMEOUT: a bounded wait inside a kernel ran out";
     }
     return "unknown gattn_status";
 }
@@ -429,10 +457,14 @@ struct PagedCache {
 // The decode step; with append != NULL the new token's K and V are first written
 // into the cache (k_new, v_new, knorm_w of *append); with paged != NULL the cache
 // is paged (Lmax = max_pages * page_size).
-gattn_status decode_impl(const void* q_new, const void* kv_cache, const int32_t* seqlens, const void* gate,
-                         const void* qnorm_w, int B, int H, int G, int d, int Lmax, int rotary_dim, double rope_base,
-                         float eps, int gate_mode, void* workspace, size_t workspace_bytes, void* out, void* stream_,
-                         const AppendParams* append, const PagedCache* paged) {
+}  // namespace
+
+// Every host-side check of a decode step's arguments except the workspace (shared
+// by gattn_decode and its variants, so that they report the same status).
+gattn_status gattn::decode_check_args(const void* q_new, const void* kv_cache, const int32_t* seqlens,
+                                      const void* gate, const void* qnorm_w, int B, int H, int G, int d, int Lmax,
+                                      int rotary_dim, double rope_base, float eps, int gate_mode, const void* out,
+                                      int64_t cache_rows) {
     if (!q_new || !kv_cache || !seqlens || !qnorm_w || !out) return GATTN_ERR_INVALID_ARG;
     if (!valid_gate_mode(gate_mode) || (gate_layout(gate_mode) != GATTN_GATE_NONE && !gate))
         return GATTN_ERR_INVALID_ARG;
@@ -442,10 +474,23 @@ gattn_status decode_impl(const void* q_new, const void* kv_cache, const int32_t*
     if (!(eps >= 0.f) || !std::isfinite(eps)) return GATTN_ERR_INVALID_ARG;
     if (!(d == 64 || d == 128 || d == 256) || H / G > 8 || rotary_dim % 16 != 0 || B > decode_max_batch())
         return GATTN_ERR_UNSUPPORTED;
-    const int64_t cache_rows = paged ? 2 * (int64_t)paged->num_pages * G * paged->page_size : 2 * (int64_t)B * G * Lmax;
+    if (cache_rows < 0) cache_rows = 2 * (int64_t)B * G * Lmax;
     if (cache_rows + kDecodeTileKeys > INT32_MAX) return GATTN_ERR_UNSUPPORTED;
     if (!aligned(kv_cache, 16) || !aligned(q_new, 4) || !aligned(qnorm_w, 4) || !aligned(out, 2))
         return GATTN_ERR_INVALID_ARG;
+    return GATTN_OK;
+}
+
+namespace {
+
+gattn_status decode_impl(const void* q_new, const void* kv_cache, const int32_t* seqlens, const void* gate,
+                         const void* qnorm_w, int B, int H, int G, int d, int Lmax, int rotary_dim, double rope_base,
+                         float eps, int gate_mode, void* workspace, size_t workspace_bytes, void* out, void* stream_,
+                         const AppendParams* append, const PagedCache* paged) {
+    const int64_t cache_rows = paged ? 2 * (int64_t)paged->num_pages * G * paged->page_size : 2 * (int64_t)B * G * Lmax;
+    const gattn_status arg = decode_check_args(q_new, kv_cache, seqlens, gate, qnorm_w, B, H, G, d, Lmax, rotary_dim,
+                                               rope_base, eps, gate_mode, out, cache_rows);
+    if (arg != GATTN_OK) return arg;
     const int n_ctas = sm_count();
     if (n_ctas <= 0) return GATTN_ERR_CUDA;
     const size_t need = gattn_decode_workspace_size(B, H, G, d, Lmax);
@@ -568,7 +613,15 @@ gattn_status gattn_get_device_status(unsigned int* bits, void* stream_) {
     if (cudaMemsetAsync(status, 0, sizeof(h), stream) != cudaSuccess) return GATTN_ERR_CUDA;
     if (cudaStreamSynchronize(stream) != cudaSuccess) return GATTN_ERR_CUDA;
     if (bits) *bits = h;
-    return h ? GATTN_ERR_DEVICE : GATTN_OK;
+    return (h & GATTN_DEVICE_TIMEOUT) ? GATTN_ERR_DEVICE_TIMEOUT : h ? GATTN_ERR_DEVICE : GATTN_OK;
+}
+
+gattn_status gattn_selftest_wait_timeout(unsigned long long limit_ns, unsigned long long* waited_ns, void* stream_) {
+    if (limit_ns < 1000000ull || limit_ns > 100000000ull) return GATTN_ERR_INVALID_ARG;
+    unsigned int* status = status_ptr();
+    if (!status) return GATTN_ERR_CUDA;
+    selftest_wait_kernel<<<1, 64, 0, static_cast<cudaStream_t>(stream_)>>>(limit_ns, status, waited_ns);
+    return cudaGetLastError() == cudaSuccess ? GATTN_OK : GATTN_ERR_CUDA;
 }
 
 }  // extern "C"

@@ -250,17 +250,18 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Wait for the phase with the given parity to complete.  Gives up when another
-// thread of the CTA raised *abort, or after kWaitLimitNs; on a timeout it
-// raises *abort and the device status bit.  Returns true iff the phase completed.
+// thread of the CTA raised *abort, or after limit_ns of wall-clock time (2 s in
+// every attention kernel; the wait self-test passes a short limit); on a timeout
+// it raises *abort and the device status bit.  Returns true iff the phase completed.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort,
-                                          unsigned int* status) {
+                                          unsigned int* status, unsigned long long limit_ns = kWaitLimitNs) {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = global_timer_ns();
     for (uint32_t i = 1;; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((i & 63u) == 0) {
             if (*abort) return false;
-            if (global_timer_ns() - t0 > kWaitLimitNs) {
+            if (global_timer_ns() - t0 > limit_ns) {
                 *abort = 1;
                 atomicOr(status, GATTN_DEVICE_TIMEOUT);
                 return false;
@@ -271,11 +272,12 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
 
 // Teardown wait: ignores the abort flag (used to drain copies already in
 // flight before a CTA exits), still bounded by the wall-clock limit.
-__device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, unsigned int* status) {
+__device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, unsigned int* status,
+                                                unsigned long long limit_ns = kWaitLimitNs) {
     const unsigned long long t0 = global_timer_ns();
     for (uint32_t i = 0;; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((i & 63u) == 63u && global_timer_ns() - t0 > kWaitLimitNs) {
+        if ((i & 63u) == 63u && global_timer_ns() - t0 > limit_ns) {
             atomicOr(status, GATTN_DEVICE_TIMEOUT);
             return false;
         }

@@ -50,7 +50,11 @@ extern "C" gattn_status gattn_decode_noalloc(const void* q_new, const void* kv_c
                                              int Lmax, int rotary_dim, double rope_base, float eps, int gate_mode,
                                              void* out, void* stream) {
     static_assert(GATTN_DECODE_NOALLOC_SCRATCH_BYTES == kScratchBytes, "header and library disagree on the limit");
-    // Argument errors are reported exactly as gattn_decode reports them.
+    // Argument errors first, with the status gattn_decode gives them; only then the
+    // scratch limit and the one-time address lookup.
+    const gattn_status arg = gattn::decode_check_args(q_new, kv_cache, seqlens, gate, qnorm_w, B, H, G, d, Lmax,
+                                                      rotary_dim, rope_base, eps, gate_mode, out, -1);
+    if (arg != GATTN_OK) return arg;
     const size_t need = gattn_decode_workspace_size(B, H, G, d, Lmax);
     if (need > kScratchBytes) return GATTN_ERR_WORKSPACE;
     void* scratch = scratch_address();

@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "gattn.h"
+
 namespace gattn {
 
 constexpr int kMaxRotaryHalf = 128;  // rotary_dim <= 256
@@ -120,6 +122,13 @@ cudaError_t launch_decode_append(const AppendParams& p, cudaStream_t stream);
 int prefill_block_n(int d);
 
 int decode_max_batch();
+
+// Host-side argument checks of a decode step, every one but the workspace's, with
+// the status gattn_decode returns for them (cache_rows < 0: the contiguous cache
+// [2,B,G,Lmax,d]).
+gattn_status decode_check_args(const void* q_new, const void* kv_cache, const int32_t* seqlens, const void* gate,
+                               const void* qnorm_w, int B, int H, int G, int d, int Lmax, int rotary_dim,
+                               double rope_base, float eps, int gate_mode, const void* out, int64_t cache_rows);
 
 // Decode work split: the size of one partial-state slot in floats and the
 // number of slots the workspace must hold.

@@ -60,7 +60,8 @@ typedef enum {
     GATTN_ERR_UNSUPPORTED = 2,  /* valid arguments this build has no kernel for (e.g. head_dim 96) */
     GATTN_ERR_CUDA = 3,         /* a CUDA runtime/driver call or launch failed */
     GATTN_ERR_WORKSPACE = 4,    /* workspace pointer missing, misaligned or too small */
-    GATTN_ERR_DEVICE = 5        /* gattn_get_device_status found a device-side problem */
+    GATTN_ERR_DEVICE = 5,       /* gattn_get_device_status found a device-side problem (not a timeout) */
+    GATTN_ERR_DEVICE_TIMEOUT = 6 /* gattn_get_device_status found that a bounded wait inside a kernel ran out */
 } gattn_status;
 
 /*
@@ -127,6 +128,9 @@ size_t gattn_prefill_workspace_size(int B, int S, int H, int G, int d, int dtype
  * B,S,H,G,d  batch, tokens per sequence, query heads, KV heads, head_dim.
  *          Requires H % G == 0, S >= 1.  d in {64,128,256} for GATTN_BF16 and
  *          d in {32,64,128,256} for GATTN_FP32 (others: GATTN_ERR_UNSUPPORTED).
+ *          bf16 d = 32 has no kernel: the tensor-core kernels move Q, K, V, the
+ *          gate and the output as 128-byte (64-element) swizzled TMA boxes along
+ *          head_dim, and a 32-element bf16 row is only 64 bytes wide.
  * rotary_dim  even, 0 <= rotary_dim <= d.  rope_base > 0.  eps >= 0.
  * workspace  device buffer of at least gattn_prefill_workspace_size() bytes,
  *          256-byte aligned.
@@ -169,7 +173,6 @@ gattn_status gattn_prefill_varlen(const void* q, const void* k, const void* v, c
                                   void* out, void* stream);
 
 /*
- * Bytes of workspace gattn_decode needs/*
  * Bytes of workspace gattn_decode needs (per-split partial softmax states).
  * Depends on the current device's SM count.  Returns 0 for invalid sizes.
  */
@@ -282,9 +285,26 @@ gattn_status gattn_decode_noalloc(const void* q_new, const void* kv_cache, const
 /*
  * Read (synchronously on `stream`) and clear the device status word.  Writes the
  * GATTN_DEVICE_* bits seen since the last call to *bits (may be NULL) and returns
- * GATTN_ERR_DEVICE if any bit was set, GATTN_OK otherwise.
+ * GATTN_ERR_DEVICE_TIMEOUT if GATTN_DEVICE_TIMEOUT is among them,
+ * GATTN_ERR_DEVICE if any other bit was set, GATTN_OK otherwise.
  */
 gattn_status gattn_get_device_status(unsigned int* bits, void* stream);
+
+/*
+ * Self-test of the bounded-wait machinery every kernel of this library relies on
+ * (no counterpart on the source pages).  Launches one small kernel on `stream`
+ * whose threads wait on an mbarrier that nothing ever arrives on, through the same
+ * wait routine the attention kernels use, with a wall-clock limit of
+ * `limit_ns` nanoseconds (1 .. 100 ms) instead of the kernels' 2 s.  One thread
+ * runs out of time, raises the block's abort flag and sets GATTN_DEVICE_TIMEOUT in
+ * the device status word; the other threads see the flag and stop waiting; the
+ * block returns normally, so the CUDA context stays usable.  *waited_ns (device
+ * memory, may be NULL) receives how long the timed-out wait lasted.
+ * Returns GATTN_ERR_INVALID_ARG for a limit outside that range, GATTN_ERR_CUDA if
+ * the launch fails, GATTN_OK otherwise; the timeout itself is read back with
+ * gattn_get_device_status().
+ */
+gattn_status gattn_selftest_wait_timeout(unsigned long long limit_ns, unsigned long long* waited_ns, void* stream);
 
 /*
  * Profiling hook.  When both events are non-NULL (cudaEvent_t passed as void*),

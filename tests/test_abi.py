@@ -12,7 +12,7 @@ from gated_softmax_attention_gqa_gb300 import _lib
 from gated_softmax_attention_gqa_gb300.workloads import prefill_flops
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-OK, INVALID, UNSUPPORTED, CUDA, WORKSPACE, DEVICE = range(6)
+OK, INVALID, UNSUPPORTED, CUDA, WORKSPACE, DEVICE, DEVICE_TIMEOUT = range(7)
 FAKE = 0x7F0000000000  # 256-byte aligned, never dereferenced by argument checks
 
 
@@ -36,7 +36,7 @@ def test_exports_every_declared_symbol(lib):
 
 
 def test_strerror_covers_every_status(lib):
-    for s in range(6):
+    for s in range(7):
         assert lib.gattn_strerror(s).decode().startswith("GATTN_")
     assert b"unknown" in lib.gattn_strerror(99)
 
@@ -116,6 +116,33 @@ def decode(lib, **kw):
 ])
 def test_decode_rejects_bad_arguments(lib, kw, expect):
     assert decode(lib, **kw) == expect
+
+
+def decode_noalloc(lib, **kw):
+    a = dict(q=P(), kv=P(), sl=P(), gate=P(), qw=P(), B=4, H=8, G=2, d=256, L=1024, rd=64, base=1e7, eps=1e-6, gm=1,
+             out=P(1 << 20))
+    a.update(kw)
+    return lib.gattn_decode_noalloc(a["q"], a["kv"], a["sl"], a["gate"], a["qw"], a["B"], a["H"], a["G"], a["d"],
+                                    a["L"], a["rd"], a["base"], a["eps"], a["gm"], a["out"], None)
+
+
+# The no-allocation decode reports every argument error exactly as gattn_decode
+# does, before looking at its scratch limit -- also on shapes far beyond it.
+@pytest.mark.parametrize("kw", [
+    dict(kv=None), dict(sl=None), dict(q=None), dict(H=8, G=3), dict(L=0), dict(rd=7), dict(d=96),
+    dict(H=32, G=2), dict(B=100000), dict(rd=40), dict(kv=P(8)), dict(gm=0x12, gate=None), dict(gm=0x40),
+    dict(B=2048, G=8, q=None), dict(B=2048, G=8, rd=7), dict(B=2049, G=8),
+])
+def test_decode_noalloc_rejects_bad_arguments_like_decode(lib, kw):
+    expect = decode(lib, **kw)
+    assert expect in (INVALID, UNSUPPORTED)
+    assert decode_noalloc(lib, **kw) == expect
+
+
+def test_selftest_wait_timeout_rejects_bad_limits(lib):
+    assert lib.gattn_selftest_wait_timeout(0, None, None) == INVALID
+    assert lib.gattn_selftest_wait_timeout(999_999, None, None) == INVALID
+    assert lib.gattn_selftest_wait_timeout(100_000_001, None, None) == INVALID
 
 
 def decode_append(lib, **kw):

@@ -168,18 +168,19 @@ def test_decode_ignores_cache_entries_past_each_sequence():
     assert_close_to_oracle(out, run_oracle(inp, w), torch.bfloat16, "poisoned tail")
 
 
-def test_decode_full_size_sampled_sequences():
+def test_decode_full_size_every_sequence():
     """The benchmark's decode workload at full size (64 sequences, 16k-32k cached
-    tokens); the oracle checks six seeded sequences in full, all heads."""
+    tokens), every sequence and head against the oracle: the split kernel cuts the
+    global tile list at arbitrary points, so each sequence is split differently."""
     w = WORKLOADS["qwen35_08b_decode"]
     inp = make_decode_inputs(w)
     out = run_gpu(inp, w)
     torch.cuda.synchronize()
     assert gattn_get_device_status() == 0
-    rows = np.sort(np.random.default_rng(w.seed).choice(w.B, size=6, replace=False))
-    ref = run_oracle(inp, w, rows=torch.from_numpy(rows).long())
-    assert_close_to_oracle(out[torch.from_numpy(rows).long()], ref, torch.bfloat16, "decode full size")
-    assert torch.isfinite(out).all()
+    for b0 in range(0, w.B, 8):  # eight sequences at a time keeps the fp64 copies near 1 GB
+        rows = torch.arange(b0, min(b0 + 8, w.B))
+        ref = run_oracle(inp, w, rows=rows)
+        assert_close_to_oracle(out[rows], ref, torch.bfloat16, f"decode full size, sequences {b0}..{b0 + 7}")
 
 
 def test_decode_equals_last_prefill_row():

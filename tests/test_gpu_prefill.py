@@ -203,6 +203,17 @@ def test_bf16_full_size_sampled_rows(name):
     got = out.view(w.B, w.S, -1)[torch.from_numpy(rb).long(), torch.from_numpy(rt).long()]
     assert_close_to_oracle(got, ref, torch.bfloat16, name)
     assert torch.isfinite(out).all()
+    # every query row of one whole (batch, head): the last batch, the last head (the
+    # last head of the last KV group), computed by the oracle on that head alone
+    b, h = w.B - 1, w.H - 1
+    g = h // (w.H // w.G)
+    one = {"q": inp["q"][b:b + 1, :, h:h + 1], "k": inp["k"][b:b + 1, :, g:g + 1], "v": inp["v"][b:b + 1, :, g:g + 1],
+           "gate": inp["gate"][b:b + 1, :, h:h + 1], "qnorm_w": inp["qnorm_w"], "knorm_w": inp["knorm_w"]}
+    all_t = np.arange(w.S, dtype=np.int32)
+    ref_bh = oracle.prefill_rows(one["q"], one["k"], one["v"], one["gate"], one["qnorm_w"], one["knorm_w"], None,
+                                 w.rotary_dim, w.rope_base, w.eps, w.gate_mode, np.zeros_like(all_t), all_t)
+    got_bh = out.view(w.B, w.S, w.H, w.d)[b, :, h]
+    assert_close_to_oracle(got_bh, ref_bh, torch.bfloat16, f"{name}: every row of batch {b}, head {h}")
 
 
 def test_every_output_written_and_guard_band_untouched():
