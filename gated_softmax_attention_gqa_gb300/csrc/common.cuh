@@ -426,8 +426,31 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// Order this thread's generic-proxy global-memory writes before later async-proxy
+// (TMA) reads of the same memory.
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 __device__ __forceinline__ void named_barrier(int id, int nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// Named barrier of nthreads threads that also ANDs a predicate over them: every
+// participant gets true only if all of them passed true.  Threads that must give up
+// (a bounded wait ran out) still arrive, with false, so that all of them leave
+// together and none is left waiting at the barrier.
+__device__ __forceinline__ bool named_barrier_and(int id, int nthreads, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "barrier.cta.red.and.pred q, %2, %3, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)pred), "r"(id), "r"(nthreads)
+        : "memory");
+    return r != 0;
 }
 
 // ------------------------------------------------------------------ tcgen05
@@ -524,6 +547,60 @@ __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_
         "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate));
 }
 
+// The same two MMAs with every shared-memory descriptor given as its low word plus a
+// compile-time offset (16-byte units) and a common high word, the additions done
+// inside the asm.  An unrolled stream of these leaves the compiler nothing to hoist
+// (hoisted descriptors spill in a thread with few registers), and the issuing thread
+// runs only a handful of instructions per MMA: with warps of the same sub-partition
+// busy on softmax work, a thread that runs more issues an M128 N128 MMA only every
+// 100-140 cycles against the 64 the tensor pipe needs (measured on GB300).
+template <int A_OFF, int B_OFF>
+__device__ __forceinline__ void mma_ss_lo(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo, uint32_t d_hi, uint32_t idesc,
+                                          uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t.reg .b32 la, lb;\n\t.reg .b64 da, db;\n\t"
+        "add.u32 la, %1, %6;\n\tadd.u32 lb, %2, %7;\n\tmov.b64 da, {la, %3};\n\tmov.b64 db, {lb, %3};\n\t"
+        "setp.ne.b32 p, %5, 0;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %4, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_lo), "r"(b_lo), "r"(d_hi), "r"(idesc), "r"(accumulate), "n"(A_OFF), "n"(B_OFF));
+}
+template <int A_COL, int B_OFF>
+__device__ __forceinline__ void mma_ts_lo(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo, uint32_t d_hi, uint32_t idesc,
+                                          uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t.reg .b32 ta, lb;\n\t.reg .b64 db;\n\t"
+        "add.u32 ta, %1, %6;\n\tadd.u32 lb, %2, %7;\n\tmov.b64 db, {lb, %3};\n\t"
+        "setp.ne.b32 p, %5, 0;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %4, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "r"(b_lo), "r"(d_hi), "r"(idesc), "r"(accumulate), "n"(A_COL), "n"(B_OFF));
+}
+
+// The same for a CTA pair (cta_group::2), issued by one thread of the even CTA.
+template <int A_OFF, int B_OFF>
+__device__ __forceinline__ void mma2_ss_lo(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo, uint32_t d_hi,
+                                           uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t.reg .b32 la, lb;\n\t.reg .b64 da, db;\n\t"
+        "add.u32 la, %1, %6;\n\tadd.u32 lb, %2, %7;\n\tmov.b64 da, {la, %3};\n\tmov.b64 db, {lb, %3};\n\t"
+        "setp.ne.b32 p, %5, 0;\n\ttcgen05.mma.cta_group::2.kind::f16 [%0], da, db, %4, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_lo), "r"(b_lo), "r"(d_hi), "r"(idesc), "r"(accumulate), "n"(A_OFF), "n"(B_OFF));
+}
+template <int A_COL, int B_OFF>
+__device__ __forceinline__ void mma2_ts_lo(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo, uint32_t d_hi,
+                                           uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t.reg .b32 ta, lb;\n\t.reg .b64 db;\n\t"
+        "add.u32 ta, %1, %6;\n\tadd.u32 lb, %2, %7;\n\tmov.b64 db, {lb, %3};\n\t"
+        "setp.ne.b32 p, %5, 0;\n\ttcgen05.mma.cta_group::2.kind::f16 [%0], [ta], db, %4, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "r"(b_lo), "r"(d_hi), "r"(idesc), "r"(accumulate), "n"(A_COL), "n"(B_OFF));
+}
+
+// High word of every 128-byte-swizzled shared-memory descriptor used here (stride
+// 1024 bytes, descriptor version, swizzle mode); descriptors differ only in their
+// low word, start address >> 4 (14 bits) and leading-byte offset.
+__host__ __device__ constexpr uint32_t sdesc_sw128_hi() { return (uint32_t)((1024u >> 4) | (1u << 14) | (2u << 29)); }
+__device__ __forceinline__ uint32_t sdesc_sw128_lo(uint32_t saddr, uint32_t lbo_bytes) {
+    return ((saddr >> 4) & 0x3FFFu) | (((lbo_bytes >> 4) & 0x3FFFu) << 16);
+}
+
 // Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, dense.
 // b_mn_major: B stored with N contiguous (otherwise K contiguous).
 __host__ __device__ constexpr uint32_t make_idesc_bf16(int M, int N, bool b_mn_major) {
@@ -580,6 +657,52 @@ __device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&r)[64]) {
         : "memory");
 }
 
+// Two runs of 64 consecutive columns at independent addresses (four loads, one wait).
+__device__ __forceinline__ void tmem_ld64x2(uint32_t taddr_a, uint32_t (&a)[64], uint32_t taddr_b, uint32_t (&b)[64]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%128];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,"
+        "%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%129];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%64,%65,%66,%67,%68,%69,%70,%71,%72,%73,%74,%75,%76,%77,%78,%79,"
+        "%80,%81,%82,%83,%84,%85,%86,%87,%88,%89,%90,%91,%92,%93,%94,%95}, [%130];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%96,%97,%98,%99,%100,%101,%102,%103,%104,%105,%106,%107,%108,%109,%110,%111,"
+        "%112,%113,%114,%115,%116,%117,%118,%119,%120,%121,%122,%123,%124,%125,%126,%127}, [%131];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : GATTN_R8(a, 0), GATTN_R8(a, 8), GATTN_R8(a, 16), GATTN_R8(a, 24), GATTN_R8(a, 32), GATTN_R8(a, 40),
+          GATTN_R8(a, 48), GATTN_R8(a, 56), GATTN_R8(b, 0), GATTN_R8(b, 8), GATTN_R8(b, 16), GATTN_R8(b, 24),
+          GATTN_R8(b, 32), GATTN_R8(b, 40), GATTN_R8(b, 48), GATTN_R8(b, 56)
+        : "r"(taddr_a), "r"(taddr_a + 32), "r"(taddr_b), "r"(taddr_b + 32)
+        : "memory");
+}
+
+// 128 consecutive columns (four loads, one wait).
+__device__ __forceinline__ void tmem_ld128(uint32_t taddr, uint32_t (&r)[128]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%128];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,"
+        "%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%129];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%64,%65,%66,%67,%68,%69,%70,%71,%72,%73,%74,%75,%76,%77,%78,%79,"
+        "%80,%81,%82,%83,%84,%85,%86,%87,%88,%89,%90,%91,%92,%93,%94,%95}, [%130];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%96,%97,%98,%99,%100,%101,%102,%103,%104,%105,%106,%107,%108,%109,%110,%111,"
+        "%112,%113,%114,%115,%116,%117,%118,%119,%120,%121,%122,%123,%124,%125,%126,%127}, [%131];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : GATTN_R8(r, 0), GATTN_R8(r, 8), GATTN_R8(r, 16), GATTN_R8(r, 24), GATTN_R8(r, 32), GATTN_R8(r, 40),
+          GATTN_R8(r, 48), GATTN_R8(r, 56), GATTN_R8(r, 64), GATTN_R8(r, 72), GATTN_R8(r, 80), GATTN_R8(r, 88),
+          GATTN_R8(r, 96), GATTN_R8(r, 104), GATTN_R8(r, 112), GATTN_R8(r, 120)
+        : "r"(taddr), "r"(taddr + 32), "r"(taddr + 64), "r"(taddr + 96)
+        : "memory");
+}
+
 // Store 32 / 16 / 4 consecutive 32-bit columns of this thread's lane (no wait).
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
     asm volatile(
@@ -605,6 +728,17 @@ __device__ __forceinline__ void tmem_st4(uint32_t taddr, uint32_t a, uint32_t b,
 }
 
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// ------------------------------------------------------------------ register split
+
+// Hand registers between the warpgroups of a block (every warp of a warpgroup runs
+// the same one).  The block's total never changes: what the .dec warpgroups give
+// back is what the .inc ones take, so the sum over warpgroups of the new counts
+// must equal the count the block was launched with -- an .inc beyond that waits.
+template <int N>
+__device__ __forceinline__ void regs_raise() { asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N)); }
+template <int N>
+__device__ __forceinline__ void regs_lower() { asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N)); }
 
 // ------------------------------------------------------------------ warp-level mma (decode)
 

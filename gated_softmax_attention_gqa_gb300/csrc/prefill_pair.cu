@@ -370,6 +370,33 @@ __device__ void pair_forwarder(const PrefillParams& p, const PairBars& bars, int
 
 // ----------------------------------------------------------------- MMA issuer (even CTA)
 
+// The K-steps [k0, k1) of S = Q'K'^T (A = Q' and B = K' K-major in shared memory)
+// and of O += P V (A = P in TMEM, B = V MN-major in shared memory), unrolled at
+// compile time with immediate descriptor offsets (mma2_ss_lo): a few instructions
+// per MMA, so that the tensor pipe is fed at its own rate even while softmax warps
+// of the same sub-partition are busy.
+template <int D, int KK>
+__device__ __forceinline__ void pair_qk_steps(uint32_t d_tmem, uint32_t q_lo, uint32_t k_lo, int k0, int k1) {
+    using C = PairCfg<D>;
+    if constexpr (KK < D / 16) {
+        if (KK >= k0 && KK < k1)
+            mma2_ss_lo<((KK >> 2) * C::ROWBOX_BYTES + (KK & 3) * 32) / 16, ((KK >> 2) * C::K_CHUNK + (KK & 3) * 32) / 16>(
+                d_tmem, q_lo, k_lo, sdesc_sw128_hi(), C::IDESC_QK, KK > 0 ? 1u : 0u);
+        pair_qk_steps<D, KK + 1>(d_tmem, q_lo, k_lo, k0, k1);
+    }
+}
+template <int D, int KK>
+__device__ __forceinline__ void pair_pv_steps(uint32_t d_tmem, uint32_t p_tmem, uint32_t v_lo, uint32_t acc0, int k0,
+                                              int k1) {
+    using C = PairCfg<D>;
+    if constexpr (KK < C::BN / 16) {
+        if (KK >= k0 && KK < k1)
+            mma2_ts_lo<KK * 8, KK * 16 * 128 / 16>(d_tmem, p_tmem, v_lo, sdesc_sw128_hi(), C::IDESC_PV,
+                                                   KK > 0 ? 1u : acc0);
+        pair_pv_steps<D, KK + 1>(d_tmem, p_tmem, v_lo, acc0, k0, k1);
+    }
+}
+
 // Issue order QK(0), QK(1), then per tile PV(j), QK(j+2).  One thread can put an
 // MMA into the tensor queue only every ~47 cycles, and the queue is mostly full,
 // so the issuer runs almost in step with the pipe: the inputs of the next MMA
@@ -381,28 +408,18 @@ __device__ void pair_mma(const PrefillParams& p, const PairBars& bars, uint32_t 
     using C = PairCfg<D>;
     constexpr int QK_MMAS = D / 16, PV_MMAS = C::BN / 16;
     constexpr int QK_HEAD = QK_MMAS - 4, PV_HEAD = PV_MMAS - 2;  // issued before polling the next group's inputs
-    const uint64_t qdesc0 = make_sdesc_sw128(sbase + C::OFF_Q, 16, 1024);
-    const uint64_t kdesc0 = make_sdesc_sw128(sbase + C::OFF_K, 16, 1024);
-    const uint64_t vdesc0 = make_sdesc_sw128(sbase + C::OFF_V, C::V_CHUNK, 1024);
+    const uint32_t q_lo = sdesc_sw128_lo(sbase + C::OFF_Q, 16);
+    const uint32_t k_lo = sdesc_sw128_lo(sbase + C::OFF_K, 16);
+    const uint32_t v_lo = sdesc_sw128_lo(sbase + C::OFF_V, C::V_CHUNK);
     // S_j = Q' K'_j^T into score buffer j % 2, MMAs [k0, k1) of the group (j counts tiles over all items)
     auto qk = [&](int j, int k0, int k1) {
-        const uint64_t kd = kdesc0 + (uint64_t)(((j % C::NSK) * C::K_TILE) >> 4);
-        const uint32_t d_tmem = tm + C::TM_S + (uint32_t)(j & 1) * C::BN;
-#pragma unroll
-        for (int kk = 0; kk < QK_MMAS; ++kk)
-            if (kk >= k0 && kk < k1)
-                mma2_ss(d_tmem, qdesc0 + (uint64_t)(((kk >> 2) * C::ROWBOX_BYTES + (kk & 3) * 32) >> 4),
-                        kd + (uint64_t)(((kk >> 2) * C::K_CHUNK + (kk & 3) * 32) >> 4), C::IDESC_QK, kk > 0 ? 1u : 0u);
+        pair_qk_steps<D, 0>(tm + C::TM_S + (uint32_t)(j & 1) * C::BN, q_lo,
+                            k_lo + (uint32_t)(((j % C::NSK) * C::K_TILE) >> 4), k0, k1);
     };
     // O += P_j V_j, P_j read from TMEM where it overwrote S_j; the first tile of an item overwrites O
     auto pv = [&](int j, bool first, int k0, int k1) {
-        const uint64_t vd = vdesc0 + (uint64_t)(((j % C::NSV) * C::V_TILE) >> 4);
-        const uint32_t p_tmem = tm + C::TM_S + (uint32_t)(j & 1) * C::BN;
-#pragma unroll
-        for (int kk = 0; kk < PV_MMAS; ++kk)
-            if (kk >= k0 && kk < k1)
-                mma2_ts(tm + C::TM_O, p_tmem + kk * 8, vd + (uint64_t)((kk * 16 * 128) >> 4), C::IDESC_PV,
-                        (!first || kk > 0) ? 1u : 0u);
+        pair_pv_steps<D, 0>(tm + C::TM_O, tm + C::TM_S + (uint32_t)(j & 1) * C::BN,
+                            v_lo + (uint32_t)(((j % C::NSV) * C::V_TILE) >> 4), first ? 0u : 1u, k0, k1);
     };
     auto k_ready = [&](int j) { return mbar_test_wait(bars.k_full(j % C::NSK), (uint32_t)(j / C::NSK) & 1u); };
     auto k_wait = [&](int j) { return mbar_wait(bars.k_full(j % C::NSK), (uint32_t)(j / C::NSK) & 1u, abort_flag, status); };

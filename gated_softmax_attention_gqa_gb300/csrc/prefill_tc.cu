@@ -369,8 +369,37 @@ __device__ void run_producer(const CUtensorMap* tmK, const CUtensorMap* tmV, con
 // with j % 2 == i (j counting tiles over all items), each issuing half the MMAs;
 // their MMAs interleave freely in the pipe.  PV_j waits for PV_{j-1} to complete,
 // so O sums the tiles in the same order on every run (the result is deterministic).
+// The K-steps of S = Q'K'^T (A = Q' in TMEM, B = K' K-major in shared memory) and of
+// O += P V (A = P in TMEM, or at d = 256 in shared memory; B = V MN-major in shared
+// memory), unrolled at compile time with immediate descriptor offsets (mma_ts_lo):
+// a few instructions per MMA, so that the tensor pipe is fed at its own rate even
+// while softmax warps of the same sub-partition are busy.
+template <int D, int KK>
+__device__ __forceinline__ void tc_qk_steps(uint32_t d_tmem, uint32_t q_tmem, uint32_t k_lo) {
+    using C = PfCfg<D>;
+    if constexpr (KK < D / 16) {
+        mma_ts_lo<KK * 8, ((KK >> 2) * C::CHUNK_BYTES + (KK & 3) * 32) / 16>(d_tmem, q_tmem, k_lo, sdesc_sw128_hi(),
+                                                                           C::IDESC_QK, KK > 0 ? 1u : 0u);
+        tc_qk_steps<D, KK + 1>(d_tmem, q_tmem, k_lo);
+    }
+}
+template <int D, int KK>
+__device__ __forceinline__ void tc_pv_steps(uint32_t d_tmem, uint32_t p_tmem, uint32_t p_lo, uint32_t v_lo,
+                                            uint32_t acc0) {
+    using C = PfCfg<D>;
+    if constexpr (KK < C::BN / 16) {
+        if constexpr (C::PSMEM)
+            mma_ss_lo<((KK >> 2) * (C::BM * 128) + (KK & 3) * 32) / 16, KK * 16 * 128 / 16>(
+                d_tmem, p_lo, v_lo, sdesc_sw128_hi(), C::IDESC_PV, KK > 0 ? 1u : acc0);
+        else
+            mma_ts_lo<KK * 8, KK * 16 * 128 / 16>(d_tmem, p_tmem, v_lo, sdesc_sw128_hi(), C::IDESC_PV,
+                                                  KK > 0 ? 1u : acc0);
+        tc_pv_steps<D, KK + 1>(d_tmem, p_tmem, p_lo, v_lo, acc0);
+    }
+}
+
 template <int D>
-__device__ __forceinline__ bool issue_qk(int j, const Bars& bars, uint32_t tm, uint64_t kdesc0,
+__device__ __forceinline__ bool issue_qk(int j, const Bars& bars, uint32_t tm, uint32_t k_lo0,
                                          volatile int* abort_flag, unsigned int* status) {
     using C = PfCfg<D>;
     const int sb = j & 1;
@@ -380,12 +409,7 @@ __device__ __forceinline__ bool issue_qk(int j, const Bars& bars, uint32_t tm, u
     const int st = j % C::NSK;
     if (!mbar_wait(bars.k_full(st), (uint32_t)(j / C::NSK) & 1u, abort_flag, status)) return false;
     tc_fence_after();
-    const uint32_t d_tmem = tm + C::TM_S + sb * C::BN;
-    const uint64_t kd = kdesc0 + (uint64_t)((st * C::TILE_BYTES) >> 4);
-#pragma unroll
-    for (int kk = 0; kk < D / 16; ++kk)
-        mma_ts(d_tmem, tm + C::TM_Q + kk * 8, kd + (uint64_t)(((kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32) >> 4),
-               C::IDESC_QK, kk > 0 ? 1u : 0u);
+    tc_qk_steps<D, 0>(tm + C::TM_S + sb * C::BN, tm + C::TM_Q, k_lo0 + (uint32_t)((st * C::TILE_BYTES) >> 4));
     tc_commit(bars.k_empty(st));
     tc_commit(bars.s_full(sb));
     return true;
@@ -394,8 +418,8 @@ __device__ __forceinline__ bool issue_qk(int j, const Bars& bars, uint32_t tm, u
 // PV_j; the first tile of an item (first) overwrites O, once the previous item's
 // epilogue (item n_it - 1) has read it
 template <int D>
-__device__ __forceinline__ bool issue_pv(int j, bool first, int n_it, const Bars& bars, uint32_t tm, uint64_t vdesc0,
-                                         uint64_t pdesc0, volatile int* abort_flag, unsigned int* status) {
+__device__ __forceinline__ bool issue_pv(int j, bool first, int n_it, const Bars& bars, uint32_t tm, uint32_t v_lo0,
+                                         uint32_t p_lo0, volatile int* abort_flag, unsigned int* status) {
     using C = PfCfg<D>;
     if (!mbar_wait(bars.p_full(j & 1), (uint32_t)(j >> 1) & 1u, abort_flag, status)) return false;
     // O accumulates the PVs in tile order, run after run: PV_j starts once the
@@ -407,19 +431,8 @@ __device__ __forceinline__ bool issue_pv(int j, bool first, int n_it, const Bars
     const int st = j % C::NSV;
     if (!mbar_wait(bars.v_full(st), (uint32_t)(j / C::NSV) & 1u, abort_flag, status)) return false;
     tc_fence_after();
-    const uint64_t vd = vdesc0 + (uint64_t)((st * C::TILE_BYTES) >> 4);
-    if constexpr (C::PSMEM) {
-        const uint64_t pd = pdesc0 + (uint64_t)(((j & 1) * C::P_BUF_BYTES) >> 4);
-#pragma unroll
-        for (int kk = 0; kk < C::BN / 16; ++kk)
-            mma_ss(tm + C::TM_O, pd + (uint64_t)(((kk >> 2) * (C::BM * 128) + (kk & 3) * 32) >> 4),
-                   vd + (uint64_t)((kk * 16 * 128) >> 4), C::IDESC_PV, (first && kk == 0) ? 0u : 1u);
-    } else {
-#pragma unroll
-        for (int kk = 0; kk < C::BN / 16; ++kk)
-            mma_ts(tm + C::TM_O, tm + C::TM_P + kk * 8, vd + (uint64_t)((kk * 16 * 128) >> 4), C::IDESC_PV,
-                   (first && kk == 0) ? 0u : 1u);
-    }
+    tc_pv_steps<D, 0>(tm + C::TM_O, tm + C::TM_P, p_lo0 + (uint32_t)(((j & 1) * C::P_BUF_BYTES) >> 4),
+                      v_lo0 + (uint32_t)((st * C::TILE_BYTES) >> 4), first ? 0u : 1u);
     tc_commit(bars.v_empty(st));
     tc_commit(bars.pv_done(j & 1));
     return true;
@@ -429,9 +442,9 @@ template <int D, bool GV>
 __device__ void run_mma(int parity, const PrefillParams& p, const Bars& bars, uint32_t sbase, uint32_t tm, int cta,
                         int ncta, volatile int* abort_flag, unsigned int* status) {
     using C = PfCfg<D>;
-    const uint64_t kdesc0 = make_sdesc_sw128(sbase + C::OFF_K, 16, 1024);
-    const uint64_t vdesc0 = make_sdesc_sw128(sbase + C::OFF_V, C::CHUNK_BYTES, 1024);
-    const uint64_t pdesc0 = make_sdesc_sw128(sbase + C::OFF_P, 16, 1024);
+    const uint32_t kdesc0 = sdesc_sw128_lo(sbase + C::OFF_K, 16);
+    const uint32_t vdesc0 = sdesc_sw128_lo(sbase + C::OFF_V, C::CHUNK_BYTES);
+    const uint32_t pdesc0 = sdesc_sw128_lo(sbase + C::OFF_P, 16);
     bool ok = true;
     int jb = 0, n_it = 0;
     TcItem it;

@@ -253,19 +253,29 @@ def test_zero_gate_logits_halve_the_ungated_output():
     assert torch.equal(half, plain * 0.5)
 
 
-def test_gqa_equals_mha_with_replicated_kv():
+@pytest.mark.parametrize("d", [128, 256])
+def test_gqa_equals_mha_with_replicated_kv(d):
     """Head h reads group floor(h/(H/G)): replicating each group's K and V to its
-    H/G heads and running with G = H gives the same output."""
-    B, S, H, G, d = 1, 150, 8, 2, 128
+    H/G heads gives the same output.  G = 2 against G = 4 (both even group sizes,
+    so the same kernel computes both) must agree bit for bit; G = H (plain MHA, the
+    one-head kernel) is checked against the oracle of the G = 2 problem."""
+    B, S, H, G = 1, 150, 8, 2
     w = small("gqa", B, S, H, G, d, 64, 1e6, "elementwise", seed=8)
     inp = make_prefill_inputs(w)
     a = run_gpu(inp, w)
-    rep = H // G
-    inp_m = dict(inp, k=inp["k"].repeat_interleave(rep, dim=2).contiguous(),
-                 v=inp["v"].repeat_interleave(rep, dim=2).contiguous())
-    b = run_gpu(inp_m, small("mha", B, S, H, H, d, 64, 1e6, "elementwise"))
+
+    def replicated(g2):
+        rep = g2 // G
+        return dict(inp, k=inp["k"].repeat_interleave(rep, dim=2).contiguous(),
+                    v=inp["v"].repeat_interleave(rep, dim=2).contiguous())
+
+    b = run_gpu(replicated(4), small("gqa4", B, S, H, 4, d, 64, 1e6, "elementwise"))
+    c = run_gpu(replicated(H), small("mha", B, S, H, H, d, 64, 1e6, "elementwise"))
     torch.cuda.synchronize()
     assert torch.equal(a, b)
+    ref = run_oracle(inp, w)
+    assert_close_to_oracle(a, ref, torch.bfloat16, "G = 2")
+    assert_close_to_oracle(c, ref, torch.bfloat16, "G = H with replicated K/V")
 
 
 def test_rope_rotation_error_bound_at_long_positions():
