@@ -318,6 +318,7 @@ gattn_status prefill_impl(const void* q, const void* k, const void* v, const voi
         pp.q = q;
         pp.gate = gate;
         pp.qnorm_w = qnorm_w;
+        pp.knorm_w = knorm_w;
         pp.pos = pos;
         pp.out = out;
         pp.q_tok_stride = q_tok_stride;

@@ -38,6 +38,34 @@ __device__ __forceinline__ float ex2_approx(float x) {
     return y;
 }
 
+// A fixed reference for the softmax exponent, in place of the running row maximum.
+// q' and k' are RMS-normalised (|x / rms(x)|_2 <= sqrt(d)), scaled by the norm
+// weights and rotated (which keeps the norm), so |q'|_2 <= sqrt(d) max|w_q|, the
+// same for k', and every logit obeys |q'.k'| scale_log2 <= d max|w_q| max|w_k|
+// scale_log2 = bound (with a 2^-6 margin for the bf16 rounding of q' and k' and for
+// the fp32 sums).  Softmax is unchanged by the constant subtracted from the
+// logits; with the bound every exponent is <= 0, so no running maximum, no
+// exchange of it and no rescale of O are needed.  Used only while bound <=
+// kFixedRefLimit: the largest P of a row is then >= 2^(-2 bound), so P, l and O
+// stay far from fp32 underflow.  Returns +INF (use the running maximum) otherwise.
+// All 32 lanes of the warp call it.
+constexpr float kFixedRefLimit = 40.f;
+__device__ __forceinline__ float fixed_logit_ref(const __nv_bfloat16* wq, const __nv_bfloat16* wk, int d,
+                                                 float scale_log2) {
+    float mq = 0.f, mk = 0.f;
+    for (int i = (int)(threadIdx.x & 31u); i < d; i += 32) {
+        mq = fmaxf(mq, fabsf(__bfloat162float(wq[i])));
+        mk = fmaxf(mk, fabsf(__bfloat162float(wk[i])));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        mq = fmaxf(mq, __shfl_xor_sync(0xffffffffu, mq, o));
+        mk = fmaxf(mk, __shfl_xor_sync(0xffffffffu, mk, o));
+    }
+    const float b = (float)d * mq * mk * fabsf(scale_log2) * (1.f + 1.f / 64.f);
+    return b <= kFixedRefLimit ? b : INFINITY;
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&v);

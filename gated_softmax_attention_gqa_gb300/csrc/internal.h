@@ -31,6 +31,7 @@ struct PrefillParams {
     const void* q;
     const void* gate;
     const void* qnorm_w;
+    const void* knorm_w;  // read by the attention kernels only to bound the logits
     const int32_t* pos;
     void* out;
     int64_t q_tok_stride, q_head_stride, gate_tok_stride, gate_head_stride;

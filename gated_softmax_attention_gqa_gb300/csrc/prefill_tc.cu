@@ -88,11 +88,13 @@ struct PfCfg {
     static constexpr int TM_O = 0;
     static constexpr int TM_S = D;                   // score buffer b at TM_S + b * BN
     static constexpr int TM_Q = D + NSB * BN;
-    // d <= 128: P (bf16 pairs) has a TMEM buffer of its own, so a score buffer is
-    // free as soon as the softmax has loaded it and QK_{j+2} need not wait for PV_j
-    static constexpr int TM_P = TM_Q + D / 2;
     static constexpr int TM_COLS = 512;
-    static_assert(TM_Q + D / 2 <= TM_COLS && (PSMEM || TM_P + BN / 2 <= TM_COLS), "TMEM budget");
+    static_assert(TM_Q + D / 2 <= TM_COLS, "TMEM budget");
+    // d <= 128: P_j (bf16 pairs) is written over S_j in TMEM, and the issuer of tile j
+    // issues S_{j+2} = Q'K'_{j+2}^T right behind PV_j (the tensor pipe runs one
+    // thread's MMAs in issue order).  d = 256: P_j in shared memory, S_{j+2} as soon
+    // as the softmax has read S_j.
+    static constexpr bool P_OVER_S = !PSMEM;
     static constexpr int OFF_QB = 0;                                  // raw Q tile (PERSIST)
     static constexpr int OFF_K = PERSIST ? QTILE_BYTES : 0;
     static constexpr int OFF_V = OFF_K + NSK * TILE_BYTES;
@@ -391,9 +393,9 @@ __device__ __forceinline__ void tc_pv_steps(uint32_t d_tmem, uint32_t p_tmem, ui
         if constexpr (C::PSMEM)
             mma_ss_lo<((KK >> 2) * (C::BM * 128) + (KK & 3) * 32) / 16, KK * 16 * 128 / 16>(
                 d_tmem, p_lo, v_lo, sdesc_sw128_hi(), C::IDESC_PV, KK > 0 ? 1u : acc0);
-        else
-            mma_ts_lo<KK * 8, KK * 16 * 128 / 16>(d_tmem, p_tmem, v_lo, sdesc_sw128_hi(), C::IDESC_PV,
-                                                  KK > 0 ? 1u : acc0);
+        else  // keys [16 KK, 16 KK + 16) of half h = KK / 4: P columns 32 h + 8 KK of the score buffer
+            mma_ts_lo<KK * 8 + 32 * (KK / 4), KK * 16 * 128 / 16>(d_tmem, p_tmem, v_lo, sdesc_sw128_hi(), C::IDESC_PV,
+                                                                 KK > 0 ? 1u : acc0);
         tc_pv_steps<D, KK + 1>(d_tmem, p_tmem, p_lo, v_lo, acc0);
     }
 }
@@ -403,8 +405,10 @@ __device__ __forceinline__ bool issue_qk(int j, const Bars& bars, uint32_t tm, u
                                          volatile int* abort_flag, unsigned int* status) {
     using C = PfCfg<D>;
     const int sb = j & 1;
-    // score buffer sb was last used by tile j-2: it is free once the softmax has read S_{j-2}
-    if (j >= 2 && !mbar_wait(bars.s_free(sb), (uint32_t)((j >> 1) - 1) & 1u, abort_flag, status))
+    // score buffer sb was last used by tile j-2.  P over S: P_{j-2} there is read by
+    // PV_{j-2}, which this thread issued before.  Else the buffer is free once the
+    // softmax has read S_{j-2}.
+    if (!C::P_OVER_S && j >= 2 && !mbar_wait(bars.s_free(sb), (uint32_t)((j >> 1) - 1) & 1u, abort_flag, status))
         return false;
     const int st = j % C::NSK;
     if (!mbar_wait(bars.k_full(st), (uint32_t)(j / C::NSK) & 1u, abort_flag, status)) return false;
@@ -421,17 +425,18 @@ template <int D>
 __device__ __forceinline__ bool issue_pv(int j, bool first, int n_it, const Bars& bars, uint32_t tm, uint32_t v_lo0,
                                          uint32_t p_lo0, volatile int* abort_flag, unsigned int* status) {
     using C = PfCfg<D>;
-    if (!mbar_wait(bars.p_full(j & 1), (uint32_t)(j >> 1) & 1u, abort_flag, status)) return false;
-    // O accumulates the PVs in tile order, run after run: PV_j starts once the
-    // other issuer's PV_{j-1} has completed (its QKs keep the pipe busy meanwhile).
+    // The waits that are normally over already come first, so that the MMAs follow
+    // the wait for P_j directly.  O accumulates the PVs in tile order, run after run:
+    // PV_j starts once the other issuer's PV_{j-1} has completed (its QKs keep the
+    // pipe busy meanwhile).
     if (j >= 1 && !mbar_wait(bars.pv_done((j - 1) & 1), (uint32_t)((j - 1) >> 1) & 1u, abort_flag, status))
         return false;
     if (first && n_it > 0 && !mbar_wait(bars.o_free(), (uint32_t)(n_it - 1) & 1u, abort_flag, status)) return false;
-    tc_fence_after();
     const int st = j % C::NSV;
     if (!mbar_wait(bars.v_full(st), (uint32_t)(j / C::NSV) & 1u, abort_flag, status)) return false;
+    if (!mbar_wait(bars.p_full(j & 1), (uint32_t)(j >> 1) & 1u, abort_flag, status)) return false;
     tc_fence_after();
-    tc_pv_steps<D, 0>(tm + C::TM_O, tm + C::TM_P, p_lo0 + (uint32_t)(((j & 1) * C::P_BUF_BYTES) >> 4),
+    tc_pv_steps<D, 0>(tm + C::TM_O, tm + C::TM_S + (j & 1) * C::BN, p_lo0 + (uint32_t)(((j & 1) * C::P_BUF_BYTES) >> 4),
                       v_lo0 + (uint32_t)((st * C::TILE_BYTES) >> 4), first ? 0u : 1u);
     tc_commit(bars.v_empty(st));
     tc_commit(bars.pv_done(j & 1));
@@ -453,13 +458,19 @@ __device__ void run_mma(int parity, const PrefillParams& p, const Bars& bars, ui
         // the item's Q' is in TMEM
         if (!(ok = mbar_wait(bars.q_ready(), (uint32_t)n_it & 1u, abort_flag, status))) break;
         tc_fence_after();
-        // QK of this issuer's next tile goes out as soon as its score buffer is free,
-        // ahead of the PV that is still waiting for its P
         const int j0 = jb + ((jb & 1) != parity ? 1 : 0);
         if (j0 < je) ok = issue_qk<D>(j0, bars, tm, kdesc0, abort_flag, status);
         for (int j = j0; ok && j < je; j += 2) {
-            if (j + 2 < je && !issue_qk<D>(j + 2, bars, tm, kdesc0, abort_flag, status)) { ok = false; break; }
-            if (!issue_pv<D>(j, j == jb, n_it, bars, tm, vdesc0, pdesc0, abort_flag, status)) { ok = false; break; }
+            if constexpr (C::P_OVER_S) {
+                // S_{j+2} is written over P_j, right behind the PV_j that reads it
+                if (!issue_pv<D>(j, j == jb, n_it, bars, tm, vdesc0, pdesc0, abort_flag, status)) { ok = false; break; }
+                if (j + 2 < je && !issue_qk<D>(j + 2, bars, tm, kdesc0, abort_flag, status)) { ok = false; break; }
+            } else {
+                // QK of this issuer's next tile goes out as soon as its score buffer is
+                // free, ahead of the PV that is still waiting for its P
+                if (j + 2 < je && !issue_qk<D>(j + 2, bars, tm, kdesc0, abort_flag, status)) { ok = false; break; }
+                if (!issue_pv<D>(j, j == jb, n_it, bars, tm, vdesc0, pdesc0, abort_flag, status)) { ok = false; break; }
+            }
         }
         if (ok) tc_commit(bars.o_final());  // count 2: both issuers' PVs of the item complete
         jb = je;
@@ -560,6 +571,12 @@ __device__ void run_softmax(const PrefillParams& p, const Bars& bars, uint32_t s
     };
 
     const float sl2 = p.scale_log2;
+    // the exponent's reference: the logits' bound when it is small enough (the same
+    // in every thread), else the running maximum
+    const float m_fix = fixed_logit_ref(static_cast<const bf16*>(p.qnorm_w), static_cast<const bf16*>(p.knorm_w), D,
+                                        sl2);
+    const bool fixed = m_fix != INFINITY;
+    bool s_seen = false;  // the next tile's scores were seen in TMEM already
     int jb = 0, n_it = 0;
     TcItem item, next;
     bool have = tc_item<D, GV>(p, cta, ncta, 0, item);
@@ -585,7 +602,8 @@ __device__ void run_softmax(const PrefillParams& p, const Bars& bars, uint32_t s
             const int jg = jb + j;  // tile counter over all items: buffers and phases
             const int sb = jg & 1;
             const uint32_t s_col = C::TM_S + sb * C::BN;
-            if (!__all_sync(0xffffffffu, mbar_wait(bars.s_full(sb), (uint32_t)(jg >> 1) & 1u, abort_flag, p.status)))
+            if (!__all_sync(0xffffffffu, s_seen) &&
+                !__all_sync(0xffffffffu, mbar_wait(bars.s_full(sb), (uint32_t)(jg >> 1) & 1u, abort_flag, p.status)))
                 return;
             tc_fence_after();
             float s[KB];
@@ -595,63 +613,74 @@ __device__ void run_softmax(const PrefillParams& p, const Bars& bars, uint32_t s
 #pragma unroll
                 for (int e = 0; e < 64; ++e) s[e] = __uint_as_float(rr[e]);
             }
-            // S_j is in registers: its buffer may take the scores of tile j + 2
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bars.s_free(sb));
+            // S_j is in registers: its buffer may now take the scores of tile j + 2 (P
+            // over S: once PV_j has read P_j from it, which the issuers see to)
+            if constexpr (!C::P_OVER_S) {
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bars.s_free(sb));
+            }
             const int key0 = j * C::BN + hf * KB;
             if (key0 + KB - 1 > row_min) {
 #pragma unroll
                 for (int c = 0; c < KB; ++c)
                     if (key0 + c > t) s[c] = -INFINITY;
             }
-            float mx[8];
+            if (fixed) {
+                m_ref = m_fix;
+            } else {
+                float mx[8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) mx[i] = s[i];
+                for (int i = 0; i < 8; ++i) mx[i] = s[i];
 #pragma unroll
-            for (int c = 8; c < KB; c += 2) mx[(c >> 1) & 7] = max3(mx[(c >> 1) & 7], s[c], s[c + 1]);
-            float mt = max3(max3(mx[0], mx[1], mx[2]), max3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
-            if constexpr (C::SPLIT) {
-                // the row's maximum over the whole tile (buffer jg%2, so a slow partner
-                // still reading tile jg-1 is never overwritten)
-                xmax[((jg & 1) * NH + hf) * C::BM + row] = mt;
-                if (!meet()) return;
+                for (int c = 8; c < KB; c += 2) mx[(c >> 1) & 7] = max3(mx[(c >> 1) & 7], s[c], s[c + 1]);
+                float mt = max3(max3(mx[0], mx[1], mx[2]), max3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
+                if constexpr (C::SPLIT) {
+                    // the row's maximum over the whole tile (buffer jg%2, so a slow partner
+                    // still reading tile jg-1 is never overwritten)
+                    xmax[((jg & 1) * NH + hf) * C::BM + row] = mt;
+                    if (!meet()) return;
 #pragma unroll
-                for (int i = 0; i < NH; ++i)
-                    if (i != hf) mt = fmaxf(mt, xmax[((jg & 1) * NH + i) * C::BM + row]);
-            }
-            const float m_new = fmaxf(m_ref, mt * sl2);
-            const bool need = (m_new - m_ref) > C::RESCALE_THRESHOLD;
-            if (j == 0) {
-                m_ref = m_new;
-            } else if (__any_sync(0xffffffffu, need)) {
-                const float alpha = need ? ex2_approx(m_ref - m_new) : 1.f;
-                if (need) {
-                    l *= alpha;
+                    for (int i = 0; i < NH; ++i)
+                        if (i != hf) mt = fmaxf(mt, xmax[((jg & 1) * NH + i) * C::BM + row]);
+                }
+                const float m_new = fmaxf(m_ref, mt * sl2);
+                const bool need = (m_new - m_ref) > C::RESCALE_THRESHOLD;
+                if (j == 0) {
                     m_ref = m_new;
-                }
-                __syncwarp();
-                // O is only touched once every earlier P V of the item has landed (the
-                // two issuers' PVs may complete in either order).
-                if (!__all_sync(0xffffffffu, mbar_wait(bars.pv_done((jg - 1) & 1), (uint32_t)((jg - 1) >> 1) & 1u,
-                                                       abort_flag, p.status)))
-                    return;
-                if (j >= 2 && !__all_sync(0xffffffffu, mbar_wait(bars.pv_done(jg & 1), (uint32_t)((jg - 2) >> 1) & 1u,
-                                                                  abort_flag, p.status)))
-                    return;
-                tc_fence_after();
+                } else if (__any_sync(0xffffffffu, need)) {
+                    const float alpha = need ? ex2_approx(m_ref - m_new) : 1.f;
+                    if (need) {
+                        l *= alpha;
+                        m_ref = m_new;
+                    }
+                    __syncwarp();
+                    // O is only touched once every earlier P V of the item has landed (the
+                    // two issuers' PVs may complete in either order).
+                    if (!__all_sync(0xffffffffu, mbar_wait(bars.pv_done((jg - 1) & 1), (uint32_t)((jg - 1) >> 1) & 1u,
+                                                           abort_flag, p.status)))
+                        return;
+                    if (j >= 2 && !__all_sync(0xffffffffu, mbar_wait(bars.pv_done(jg & 1), (uint32_t)((jg - 2) >> 1) & 1u,
+                                                                      abort_flag, p.status)))
+                        return;
+                    tc_fence_after();
 #pragma unroll 1
-                for (int c = hf * OC; c < (hf + 1) * OC; c += 32) {
-                    uint32_t rr[32];
-                    tmem_ld32(tl + C::TM_O + c, rr);
+                    for (int c = hf * OC; c < (hf + 1) * OC; c += 32) {
+                        uint32_t rr[32];
+                        tmem_ld32(tl + C::TM_O + c, rr);
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) rr[e] = __float_as_uint(__uint_as_float(rr[e]) * alpha);
-                    tmem_st32(tl + C::TM_O + c, rr);
+                        for (int e = 0; e < 32; ++e) rr[e] = __float_as_uint(__uint_as_float(rr[e]) * alpha);
+                        tmem_st32(tl + C::TM_O + c, rr);
+                    }
                 }
             }
-            // P = exp2(s * scale * log2e - m_ref), packed bf16: into the P buffer in TMEM
-            // (this half's keys to columns [hf KB/2, hf KB/2 + KB/2)), or (PSMEM) as this
-            // thread's 128-byte-swizzled row of P buffer jg%2 in shared memory.
+            // whether the next tile's scores are in, asked now and used after the
+            // exponentials, so that the answer is not waited for
+            s_seen = j + 1 < n_kv && mbar_test_wait(bars.s_full(sb ^ 1), (uint32_t)((jg + 1) >> 1) & 1u);
+            // P = exp2(s * scale * log2e - m_ref), packed bf16: over this thread's own
+            // scores in TMEM (this half's keys to columns [hf KB, hf KB + KB/2) of the
+            // score buffer), or (PSMEM) as this thread's 128-byte-swizzled row of P
+            // buffer jg%2 in shared memory.
             float rs[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
             const float mref = m_ref;
             if constexpr (C::PSMEM) {
@@ -692,12 +721,7 @@ __device__ void run_softmax(const PrefillParams& p, const Bars& bars, uint32_t s
                     rs2[e & 3] = add2(rs2[e & 3], pe);
                     pk[e] = pack_bf16x2(pe.x, pe.y);
                 }
-                // the P buffer held P_{jg-1}: PV_{jg-1} must have finished reading it
-                if (jg >= 1 && !__all_sync(0xffffffffu, mbar_wait(bars.pv_done((jg - 1) & 1), (uint32_t)((jg - 1) >> 1) & 1u,
-                                                                   abort_flag, p.status)))
-                    return;
-                tc_fence_after();
-                tmem_st32(tl + C::TM_P + hf * (KB / 2), pk);
+                tmem_st32(tl + s_col + hf * KB, pk);
                 l += ((rs2[0].x + rs2[0].y) + (rs2[1].x + rs2[1].y)) + ((rs2[2].x + rs2[2].y) + (rs2[3].x + rs2[3].y));
                 tmem_wait_st();
                 tc_fence_before();
