@@ -82,17 +82,19 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) qk_prologue_kernel(const 
 
 // bf16 -> bf16 with rotary_dim % 16 == 0 (the tensor-core path).
 //
-// A row of D elements is spread over D/8 lanes, one 16-byte load and one 16-byte
-// store each, so a warp holds RPW = 32*8/D whole rows at a time.  The RMS is a
-// shuffle reduction inside the row's lanes, and the rotation partner of a lane's
-// 8 elements (e +- rd/2) sits in the lane rd/16 away within the same row.
+// A row of D elements is spread over D/16 lanes: the first rd/16 lanes of a row
+// each own 8 rotation pairs (x_i and x_{i+rd/2}, i in [8k, 8k+8)), the others 16
+// consecutive unrotated features, as two 16-byte loads and stores each -- so a lane
+// has both members of every pair it rotates, and a warp step covers RPW = 512/D
+// rows.  The RMS is a shuffle reduction inside the row's lanes.
 //
-// A work item is one RoPE position and up to U*RPW of the rows rotated by it: with
-// default positions (pos == NULL) that is token t of every batch and head,
-// otherwise token t of one batch, every head.  The lane's 8 (cos, sin) pairs are
-// computed once and reused for all of those rows, so the sine/cosine work is per
-// position rather than per row; the U row loads are issued together before any
-// arithmetic.
+// A work item is RPW consecutive tokens of one batch and every head (plane) of the
+// tensor: the RPW rows of a warp step are those tokens of one head, and the warp
+// walks the heads, PF of them loaded ahead.  A lane's token is fixed for the item,
+// so its 8 (cos, sin) pairs -- folded with its norm weights into the four factors
+// of the rotation -- are computed once and serve every head, and the item reads
+// whole token rows (all heads) and writes RPW consecutive rows of each head's
+// plane.
 //
 // The grid is one resident wave (the launch sizes it to the blocks the SMs hold at
 // once) and each warp walks the items with a stride.  The attention kernel launched
@@ -101,85 +103,96 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) qk_prologue_kernel(const 
 // this pass still waiting to run.
 template <int D>
 __global__ void __launch_bounds__(256) qk_prologue_bf16_kernel(const __grid_constant__ ProloguePlan p,
-                                                               uint32_t n_items, uint32_t n_tau, int nb) {
-    constexpr int LPR = D / 8;        // lanes per row
-    constexpr int RPW = 32 / LPR;     // rows per warp step
-    constexpr int U = 4;              // warp steps per item
+                                                                  uint32_t n_items, uint32_t n_tblocks) {
+    constexpr int LPR = D / 16;       // lanes per row
+    constexpr int RPW = 32 / LPR;     // rows (tokens) per warp step
+    constexpr int PF = 4;             // heads loaded ahead
     pdl_launch_dependents();  // the attention kernel may start its own prologue now
-    // lanes read different frequencies: from shared memory, not the (serialising) parameter bank
-    __shared__ float inv_freq[kMaxRotaryHalf];
-    if (threadIdx.x < kMaxRotaryHalf) inv_freq[threadIdx.x] = p.inv_freq[threadIdx.x];
-    __syncthreads();
     const int lane = threadIdx.x & 31;
-    const int sub = lane % LPR;       // this lane's 8-element block within the row
-    const int e0 = 8 * sub;
-    const uint4 wv = *reinterpret_cast<const uint4*>(static_cast<const bf16*>(p.w) + e0);
-    const uint32_t ws[4] = {wv.x, wv.y, wv.z, wv.w};
-    const uint32_t n_rows = (uint32_t)nb * (uint32_t)p.n_heads;  // rows sharing a position
+    const int sub = lane % LPR;                    // this lane's place within the row
+    const int rsub = lane / LPR;                   // this lane's token within the item
+    const int npl = p.rd >> 4;                     // pair lanes per row
+    const bool rot = sub < npl;
+    // this lane's two 8-element blocks: x_i and x_{i+rd/2}, or 16 unrotated features
+    const int o1 = rot ? 8 * sub : p.rd + 16 * (sub - npl);
+    const int o2 = rot ? o1 + (p.rd >> 1) : o1 + 8;
+    const int nh = p.n_heads;
     const uint32_t stride = gridDim.x * (blockDim.x >> 5);
     for (uint32_t item = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); item < n_items; item += stride) {
-        // the position this warp rotates by: tau = t (default positions) or b*S + t.
-        // Consecutive warps take consecutive positions of the same chunk of rows, so a
-        // CTA reads and writes contiguous runs of every (batch, head) plane.
-        const uint32_t chunk = item / n_tau;
-        const uint32_t tau = item - chunk * n_tau;
-        const int t = p.pos ? (int)(tau % (uint32_t)p.S) : (int)tau;
-        const int b_fixed = p.pos ? (int)(tau / (uint32_t)p.S) : 0;
-        const float posf = p.pos ? (float)p.pos[tau] : (float)tau;
-        const int half = p.rd >> 1, dl = half >> 3;  // rotation partner distance in lanes
-        const bool first = e0 < half, rot = e0 < p.rd;
-        const int src = lane + (first ? dl : -dl);
-        float cs[8], sn[8];
-    #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            cs[i] = 1.f;
-            sn[i] = 0.f;
-            if (rot) rope_sincos(posf * inv_freq[(first ? e0 : e0 - half) + i], &sn[i], &cs[i]);
-        }
-        uint4 xv[U];
-        int rb[U], rh[U];
-        bool live[U];
-    #pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const uint32_t r = (chunk * U + u) * RPW + (uint32_t)(lane / LPR);
-            live[u] = r < n_rows;
-            const uint32_t rr = live[u] ? r : 0u;
-            rh[u] = (int)(rr % (uint32_t)p.n_heads);
-            rb[u] = p.pos ? b_fixed : (int)(rr / (uint32_t)p.n_heads);
-            const bf16* x = static_cast<const bf16*>(p.x) + ((int64_t)rb[u] * p.S + t) * p.tok_stride +
-                            (int64_t)rh[u] * p.head_stride + e0;
-            xv[u] = live[u] ? __ldcs(reinterpret_cast<const uint4*>(x)) : make_uint4(0, 0, 0, 0);
-        }
-    #pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const uint32_t xs[4] = {xv[u].x, xv[u].y, xv[u].z, xv[u].w};
-            float y[8];
-            float ss = 0.f;
-    #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const float a = bf16_lo(xs[i]), c = bf16_hi(xs[i]);
-                ss = fmaf(a, a, fmaf(c, c, ss));
-                y[2 * i] = a * bf16_lo(ws[i]);
-                y[2 * i + 1] = c * bf16_hi(ws[i]);
-            }
-    #pragma unroll
-            for (int o = LPR / 2; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-            const float rinv = rsqrtf(ss / (float)D + p.eps);
-            float q[8];
-    #pragma unroll
-            for (int i = 0; i < 8; ++i) q[i] = __shfl_sync(0xffffffffu, y[i], rot ? src : lane);
-            uint32_t o[4];
-    #pragma unroll
+        const int b = (int)(item / n_tblocks);
+        const int t = (int)(item - (uint32_t)b * n_tblocks) * RPW + rsub;
+        const bool live = t < p.S;
+        const int tc = live ? t : 0;
+        const bf16* x0 = static_cast<const bf16*>(p.x) + ((int64_t)b * p.S + tc) * p.tok_stride;
+        bf16* d0 = static_cast<bf16*>(p.dst) + ((int64_t)b * nh * p.S + tc) * D;
+        const int64_t dplane = (int64_t)p.S * D;  // from one head's plane to the next
+        uint4 xa[PF], xb[PF];
+        auto load = [&](int j, int hh) {
+            const bf16* x = x0 + (int64_t)hh * p.head_stride;
+            const bool ok = live && hh < nh;
+            xa[j] = ok ? __ldcs(reinterpret_cast<const uint4*>(x + o1)) : make_uint4(0, 0, 0, 0);
+            xb[j] = ok ? __ldcs(reinterpret_cast<const uint4*>(x + o2)) : make_uint4(0, 0, 0, 0);
+        };
+#pragma unroll
+        for (int j = 0; j < PF; ++j) load(j, j);
+        // this lane's rotation at its token's position, with the norm weights w (of x_i)
+        // and w' (of x_{i+rd/2}): lo = (x_i ka + x_{i+rd/2} kb) rinv, hi = (x_{i+rd/2} kc +
+        // x_i kd) rinv with ka = w cos, kb = -w' sin, kc = w' cos, kd = w sin (cos = 1,
+        // sin = 0 for unrotated features)
+        float2 ka[4], kb[4], kc[4], kd[4];
+        {
+            float wa[8], wb[8];
+            unpack8(*reinterpret_cast<const uint4*>(static_cast<const bf16*>(p.w) + o1), wa);
+            unpack8(*reinterpret_cast<const uint4*>(static_cast<const bf16*>(p.w) + o2), wb);
+            const float posf = p.pos ? (float)p.pos[(int64_t)b * p.S + tc] : (float)tc;
+#pragma unroll
             for (int i = 0; i < 8; i += 2) {
-                // first half: x*cos - partner*sin; second half: x*cos + partner*sin (cs=1, sn=0 past rd)
-                const float s0 = first ? -sn[i] : sn[i], s1 = first ? -sn[i + 1] : sn[i + 1];
-                const float v0 = fmaf(y[i], cs[i], q[i] * s0);
-                const float v1 = fmaf(y[i + 1], cs[i + 1], q[i + 1] * s1);
-                o[i >> 1] = pack_bf16x2(v0 * rinv, v1 * rinv);
+                float2 s2 = make_float2(0.f, 0.f), c2 = make_float2(1.f, 1.f);
+                if (rot)
+                    rope_sincos2(mul2(make_float2(posf, posf),
+                                      make_float2(p.inv_freq[8 * sub + i], p.inv_freq[8 * sub + i + 1])),
+                                 &s2, &c2);
+                const float2 w1 = make_float2(wa[i], wa[i + 1]), w2 = make_float2(wb[i], wb[i + 1]);
+                ka[i >> 1] = mul2(w1, c2);
+                kb[i >> 1] = mul2(w2, make_float2(-s2.x, -s2.y));
+                kc[i >> 1] = mul2(w2, c2);
+                kd[i >> 1] = mul2(w1, s2);
             }
-            if (live[u]) {
-                bf16* dst = static_cast<bf16*>(p.dst) + (((int64_t)rb[u] * p.n_heads + rh[u]) * p.S + t) * D + e0;
-                *reinterpret_cast<uint4*>(dst) = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+        for (int h0 = 0; h0 < nh; h0 += PF) {
+#pragma unroll
+            for (int j = 0; j < PF; ++j) {
+                const int h = h0 + j;  // warp-uniform
+                if (h >= nh) break;
+                float a[8], bv[8];
+                unpack8(xa[j], a);
+                unpack8(xb[j], bv);
+                load(j, h + PF);  // the head PF further on, into the registers just read
+                float2 ss2 = make_float2(0.f, 0.f);
+#pragma unroll
+                for (int i = 0; i < 8; i += 2) {
+                    ss2 = fma2(make_float2(a[i], a[i + 1]), make_float2(a[i], a[i + 1]), ss2);
+                    ss2 = fma2(make_float2(bv[i], bv[i + 1]), make_float2(bv[i], bv[i + 1]), ss2);
+                }
+                float ss = ss2.x + ss2.y;
+#pragma unroll
+                for (int o = LPR / 2; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+                const float rinv = rsqrtf(ss / (float)D + p.eps);
+                const float2 r2 = make_float2(rinv, rinv);
+                uint32_t lo[4], hi[4];
+#pragma unroll
+                for (int i = 0; i < 8; i += 2) {
+                    const float2 av = make_float2(a[i], a[i + 1]), bw = make_float2(bv[i], bv[i + 1]);
+                    const float2 l = mul2(fma2(av, ka[i >> 1], mul2(bw, kb[i >> 1])), r2);
+                    const float2 r = mul2(fma2(bw, kc[i >> 1], mul2(av, kd[i >> 1])), r2);
+                    lo[i >> 1] = pack_bf16x2(l.x, l.y);
+                    hi[i >> 1] = pack_bf16x2(r.x, r.y);
+                }
+                if (live) {
+                    bf16* d = d0 + (int64_t)h * dplane;
+                    *reinterpret_cast<uint4*>(d + o1) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                    *reinterpret_cast<uint4*>(d + o2) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                }
             }
         }
     }
@@ -187,13 +200,10 @@ __global__ void __launch_bounds__(256) qk_prologue_bf16_kernel(const __grid_cons
 
 template <int D>
 cudaError_t launch_bf16(const ProloguePlan& p, cudaStream_t stream) {
-    constexpr int RPW = 32 / (D / 8);
-    constexpr int U = 4;
-    const int64_t n_tau = p.pos ? (int64_t)p.B * p.S : (int64_t)p.S;
-    const int64_t rows_per_tau = p.pos ? (int64_t)p.n_heads : (int64_t)p.B * p.n_heads;
-    const int64_t n_chunks = (rows_per_tau + U * RPW - 1) / (U * RPW);
-    const int64_t n_items = n_tau * n_chunks;
-    if (rows_per_tau >= 0x7fffffffLL || n_items + 8 >= 0x7fffffffLL) return cudaErrorInvalidValue;
+    constexpr int RPW = 32 / (D / 16);
+    const int64_t n_tblocks = (p.S + RPW - 1) / RPW;
+    const int64_t n_items = (int64_t)p.B * n_tblocks;
+    if (n_items + 2048 >= 0x7fffffffLL) return cudaErrorInvalidValue;
     // one resident wave at most (see the kernel)
     static int per_sm[3] = {0, 0, 0};
     int& occ = per_sm[D == 64 ? 0 : D == 128 ? 1 : 2];
@@ -206,8 +216,7 @@ cudaError_t launch_bf16(const ProloguePlan& p, cudaStream_t stream) {
         occ = (b > 0 ? b : 1) * n_sm;
     }
     const int64_t blocks = std::min<int64_t>((n_items + 7) / 8, occ);
-    qk_prologue_bf16_kernel<D><<<(unsigned)blocks, 256, 0, stream>>>(p, (uint32_t)n_items, (uint32_t)n_tau,
-                                                                        p.pos ? 1 : p.B);
+    qk_prologue_bf16_kernel<D><<<(unsigned)blocks, 256, 0, stream>>>(p, (uint32_t)n_items, (uint32_t)n_tblocks);
     return cudaGetLastError();
 }
 

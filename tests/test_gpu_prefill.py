@@ -383,3 +383,72 @@ def test_gate_variant_many_items_per_cta(d, H, G, S, layout):
     z = inp["gate"].double().numpy()
     zr = z[rb, rt]  # the sampled tokens' logits: [n, H, d] / [n, H] / [n, d]
     assert_close_to_oracle(got, ref, torch.bfloat16, f"d{d} {layout}", scale=gate_scale(zr, layout, "silu", ref.shape))
+
+
+# The softmax's reference for the exponent: while the logits' bound from the norm
+# weights (d max|w_q| max|w_k| log2(e)/sqrt(d), with a 2^-6 margin) is at most 40,
+# the one-head kernel subtracts that bound; above it, the running row maximum with
+# lazy rescale.  Weights 2.5x the benchmark's put every shape on the running
+# maximum, and the larger logits make its rescale run often.
+RUNNING_MAX_SHAPES = [
+    # B, S, H, G, d, rd, base, gate
+    (1, 700, 4, 2, 128, 64, 1e6, "headwise"),      # several items per CTA, ragged
+    (2, 300, 2, 1, 64, 32, 1e4, "elementwise"),
+    (1, 520, 8, 2, 256, 64, 1e7, "elementwise"),   # CTA-pair kernel
+    (1, 260, 3, 1, 256, 64, 1e7, "headwise"),      # one-head kernel at d = 256 (odd H/G)
+]
+
+
+def bf16_operand_reference(inp, w):
+    """The oracle's attention on q' = rope(rmsnorm(q)) and k' likewise, each rounded to
+    bf16 as the tensor-core contraction takes them: the reference for the kernel's
+    own arithmetic once the logits are large enough for the operands' rounding to
+    show (an error of a few 2^-9 of |q'||k'| in every logit)."""
+    B, S = inp["q"].shape[:2]
+    pos = np.broadcast_to(np.arange(S, dtype=np.float64)[None, :, None], (B, S, 1))
+    def op(x, wt):
+        y = oracle.rope(oracle.rmsnorm(x, wt, w.eps), pos, w.rotary_dim, w.rope_base)
+        return torch.from_numpy(y).to(torch.bfloat16).double().numpy()
+    return oracle.sdpa_gate(op(inp["q"], inp["qnorm_w"]), op(inp["k"], inp["knorm_w"]), inp["v"], inp["gate"],
+                            w.gate_mode)
+
+
+@pytest.mark.parametrize("shape", RUNNING_MAX_SHAPES, ids=[str(s) for s in RUNNING_MAX_SHAPES])
+def test_running_max_path_with_large_norm_weights(shape):
+    B, S, H, G, d, rd, base, gm = shape
+    w = small("rm", B, S, H, G, d, rd, base, gm, seed=S + 5)
+    inp = make_prefill_inputs(w)
+    inp["qnorm_w"] = (inp["qnorm_w"].float() * 2.5).to(inp["qnorm_w"].dtype)
+    inp["knorm_w"] = (inp["knorm_w"].float() * 2.5).to(inp["knorm_w"].dtype)
+    out = run_gpu(inp, w)
+    torch.cuda.synchronize()
+    assert gattn_get_device_status() == 0
+    ref_op = bf16_operand_reference(inp, w)
+    assert_close_to_oracle(out, ref_op, torch.bfloat16, f"{shape} against bf16 q', k'")
+    # against the exact oracle: no further than the operands' rounding moves it
+    exact = run_oracle(inp, w)
+    got = out.double().cpu().numpy().reshape(exact.shape)
+    assert (np.abs(got - exact) <= np.abs(ref_op - exact) + 2e-2).all(), str(shape)
+
+
+@pytest.mark.parametrize("d,wn,sign", [(128, 1.55, -1.0), (128, 1.55, 1.0), (64, 1.8, -1.0), (256, 1.3, -1.0)])
+def test_logits_at_the_fixed_bound(d, wn, sign):
+    """Constant q and k = sign * q with constant norm weights wn, no rotary part: every
+    logit equals sign * d wn^2 / sqrt(d), within 2% of the bound (just under 40 in
+    log2 units for d <= 128), so with sign = -1 every P of a row is about 2^-79.  The
+    softmax is uniform either way: out_t = the mean of v_0..v_t (no gate)."""
+    B, S, H, G = 1, 300, 2, 1
+    w = small("bound", B, S, H, G, d, 0, 1e4, "none", seed=d)
+    inp = make_prefill_inputs(w)
+    inp["q"] = torch.full_like(inp["q"], 0.75)
+    inp["k"] = torch.full_like(inp["k"], 0.75 * sign)
+    inp["qnorm_w"] = torch.full_like(inp["qnorm_w"], wn)
+    inp["knorm_w"] = torch.full_like(inp["knorm_w"], wn)
+    out = run_gpu(inp, w)
+    torch.cuda.synchronize()
+    assert gattn_get_device_status() == 0
+    v = inp["v"][0, :, 0].double()                                   # [S, d]
+    mean = torch.cumsum(v, 0) / torch.arange(1, S + 1, dtype=torch.float64)[:, None]
+    want = mean[:, None, :].expand(S, H, d).reshape(1, S, H * d)
+    assert_close_to_oracle(out, want.numpy(), torch.bfloat16, f"d={d} sign={sign}")
+    assert_close_to_oracle(out, run_oracle(inp, w), torch.bfloat16, f"d={d} sign={sign} oracle")
