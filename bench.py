@@ -36,6 +36,10 @@ sys.path.insert(0, ROOT)
 METRIC = "gated-attn causal prefill TFLOP/s (% bf16 peak); decode KV GB/s (% HBM)"
 PREFILL = "qwen35_08b_prefill"
 DECODE = "qwen35_08b_decode"
+# The projection after the path: Qwen3.5-0.8B's W_O maps the concatenated heads (8 x 256
+# = 2048) back to its residual width 1024 ("Multi-head attention and GQA" chapter,
+# glossary entry d_model).
+OPROJ_PREFILL, OPROJ_HIDDEN = PREFILL, 1024
 L2_FLUSH_BYTES = 256 << 20
 
 
@@ -60,7 +64,7 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--prefill", default=PREFILL, help="prefill workload name (parity/tuning runs)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", choices=["prefill", "decode"], default=None,
+    ap.add_argument("--only", choices=["prefill", "decode", "oproj"], default=None,
                     help="run one half of the path only (profiling runs; not a bench line)")
     ap.add_argument("--decode-batch", type=int, default=None,
                     help="override the decode batch (smaller profiling case; not a bench line)")
@@ -474,6 +478,7 @@ def main():
 
     profiling = bool(args.only or args.decode_batch)
     do_p, do_d = args.only in (None, "prefill"), args.only in (None, "decode")
+    do_o = args.only in (None, "oproj") and not args.decode_batch
     # the headline prefill (a profiling run may pick another); the other two are
     # timed after the headline step in the default run
     head = args.prefill
@@ -607,6 +612,41 @@ def main():
     configs = {name: prefill_entry(name) for name in P}
     value = configs[head]["value"] if do_p else float("nan")
 
+    # ---- Timed region 4: the output projection that follows the path (y = x W_O^T, the
+    # library's tcgen05 GEMM), on the Qwen3.5-0.8B shape: x = the headline prefill's
+    # output [B*S, H*d] = [4096, 2048], W_O [hidden 1024, 2048] (synthetic N(0, 1/K)).
+    oproj = None
+    if do_o:
+        ow = WORKLOADS[OPROJ_PREFILL]
+        T_o, K_o, N_o = ow.B * ow.S, ow.H * ow.d, OPROJ_HIDDEN
+        x_o = (P[OPROJ_PREFILL]["out"] if OPROJ_PREFILL in P else
+               torch.randn(T_o, K_o, generator=torch.Generator().manual_seed(7)).to(torch.bfloat16).to(dev))
+        x_o = x_o.view(T_o, K_o)
+        w_o = (torch.randn(N_o, K_o, generator=torch.Generator().manual_seed(8)) / K_o ** 0.5).to(torch.bfloat16)
+        w_o = w_o.to(dev)
+        y_o = torch.empty(T_o, N_o, dtype=torch.bfloat16, device=dev)
+        for _ in range(max(3, args.warmup)):
+            flush.zero_()
+            ga.gattn_o_proj(x_o, w_o, out=y_o)
+        pairs = [(ev(), ev()) for _ in range(K)]
+        torch.cuda.synchronize()
+        for i in range(K):
+            flush.zero_()
+            pairs[i][0].record(stream)
+            ga.gattn_o_proj(x_o, w_o, out=y_o)
+            pairs[i][1].record(stream)
+        torch.cuda.synchronize()
+        o_ms = reduce_max([statistics.median(a.elapsed_time(b) for a, b in pairs)], dev)[0]
+        o_flops = 2 * T_o * K_o * N_o
+        o_tf = o_flops / (o_ms * 1e-3) / 1e12
+        oproj = {"workload": f"{OPROJ_PREFILL} o_proj", "shape": {"T": T_o, "K": K_o, "N": N_o}, "flops": o_flops,
+                 "ms": o_ms, "value": world * o_tf, "unit": "TFLOP/s",
+                 "roofline": {"bound": "tensor", "achieved": o_tf, "peak": bf16_peak, "unit": "TFLOP/s",
+                              "frac": o_tf / bf16_peak, "peak_kind": f"{peak_kind} bf16 dense (burst)",
+                              "kernel": "oproj_kernel<256>",
+                              "traffic": profiled_traffic("oproj_qwen35_08b.md", ["oproj.cu", "common.cuh",
+                                                                                 "internal.h"])}}
+
     # ---- end to end through the public API: pinned host -> device, prefill, device -> host.
     # Steps are pipelined the way a serving loop runs them: two device slots; step i's
     # inputs go in on a copy stream while step i-1 computes, and its result comes back
@@ -669,7 +709,7 @@ def main():
         # launches of this library's kernels inside the timed regions: a prefill call is
         # the K pre-pass + the attention kernel, a decode call the split + combine kernels
         launches = {"headline_step": 2 * K * (2 * do_p + 2 * do_d), "other_prefills": 4 * K * len(others),
-                    "e2e": 2 * K * do_p}
+                    "o_proj": K * do_o, "e2e": 2 * K * do_p}
         wp = P[head]["w"] if do_p else WORKLOADS[head]
         line = {
             "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": K,
@@ -685,6 +725,7 @@ def main():
                                     "peak_kind": f"{peak_kind} HBM copy", "kernel": "decode_split_kernel<256>",
                                     "traffic": profiled_traffic("decode_split_qwen35_08b.md", dec_src)}},
             "prefill_configs": configs,
+            "o_proj": oproj,
             "e2e": {"value": e2e_val, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "ms_per_step": e2e_ms, "host_link": link},
             "gpu_launches": sum(launches.values()), "gpu_launches_by_region": launches,
@@ -696,7 +737,7 @@ def main():
                     "prefill_ms": hc.get("ms"), "prefill_kernel_ms": hc.get("kernel_ms"),
                     "decode_ms": t["d"], "decode_kernel_ms": t["dk"],
                     "prefill_kernel_tflops": hc.get("roofline", {}).get("achieved"),
-                    "decode_kernel_gbs": dec_kern_gbs, "clocks": clocks}
+                    "decode_kernel_gbs": dec_kern_gbs, "o_proj": oproj, "clocks": clocks}
         elif not args.no_cpu_baseline:
             for name in P:
                 cb = cpu_baseline(P[name]["w"], P[name]["pin"], args.cpu_budget_s)

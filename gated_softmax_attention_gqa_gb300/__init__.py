@@ -23,7 +23,7 @@ GATE_ADDITIVE = 0x100
 DTYPES = {torch.bfloat16: 0, torch.float32: 1}
 
 __all__ = ["gattn_prefill", "gattn_prefill_varlen", "gattn_decode", "gattn_decode_append", "gattn_decode_paged", "gattn_decode_noalloc", "gattn_prefill_workspace_size", "gattn_prefill_varlen_workspace_size", "gattn_decode_workspace_size",
-           "gattn_get_device_status", "gattn_set_profile_events", "gattn_selftest_wait_timeout", "gattn_strerror", "GattnError", "GATE_MODES",
+           "gattn_get_device_status", "gattn_set_profile_events", "gattn_selftest_wait_timeout", "gattn_o_proj", "gattn_strerror", "GattnError", "GATE_MODES",
            "GATE_ACTS", "GATE_ADDITIVE"]
 
 
@@ -91,6 +91,30 @@ def gattn_selftest_wait_timeout(limit_ns, waited_ns=None, stream=None):
     gattn_get_device_status()."""
     st = _lib.load().gattn_selftest_wait_timeout(int(limit_ns), _ptr(waited_ns), _stream_handle(stream, None))
     check(st, "gattn_selftest_wait_timeout")
+
+
+def gattn_o_proj(x, w_o, out=None, stream=None):
+    """Output projection of the attention output: out = x w_o^T.
+
+    x [..., K] bf16 CUDA (the [B,S,H*d] or [T,H*d] output of gattn_prefill /
+    gattn_prefill_varlen), contiguous; w_o [N, K] bf16 CUDA, contiguous (a linear
+    layer's weight); out [..., N] bf16 (allocated if None).  K and N multiples of 64."""
+    if x.dtype != torch.bfloat16 or w_o.dtype != torch.bfloat16:
+        raise ValueError("x and w_o must be bfloat16")
+    if not x.is_contiguous() or not w_o.is_contiguous() or w_o.dim() != 2:
+        raise ValueError("x and w_o must be contiguous; w_o is [N, K]")
+    K = x.shape[-1]
+    N = w_o.shape[0]
+    if w_o.shape[1] != K:
+        raise ValueError(f"w_o is [{N}, {w_o.shape[1]}], x has K = {K}")
+    T = x.numel() // K if K else 0
+    if out is None:
+        out = torch.empty(*x.shape[:-1], N, dtype=torch.bfloat16, device=x.device)
+    elif out.dtype != torch.bfloat16 or not out.is_contiguous() or out.numel() != T * N:
+        raise ValueError("out must be a contiguous bf16 tensor of T x N elements")
+    st = _lib.load().gattn_o_proj(_ptr(x), _ptr(w_o), T, K, N, _ptr(out), _stream_handle(stream, x.device))
+    check(st, "gattn_o_proj")
+    return out
 
 
 def _head_strides(t, name):

@@ -20,6 +20,7 @@ EXPORTS = (
     "gattn_get_device_status",
     "gattn_set_profile_events",
     "gattn_selftest_wait_timeout",
+    "gattn_o_proj",
 )
 
 _lib = None
@@ -70,6 +71,8 @@ def load():
     lib.gattn_get_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint), _vp]
     lib.gattn_selftest_wait_timeout.restype = _i
     lib.gattn_selftest_wait_timeout.argtypes = [ctypes.c_ulonglong, _vp, _vp]
+    lib.gattn_o_proj.restype = _i
+    lib.gattn_o_proj.argtypes = [_vp, _vp, _i, _i, _i, _vp, _vp]
     lib.gattn_set_profile_events.restype = None
     lib.gattn_set_profile_events.argtypes = [_vp, _vp]
     _lib = lib

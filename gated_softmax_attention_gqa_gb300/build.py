@@ -16,7 +16,8 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(HERE, "libgattn.so")
-SOURCES = ["api.cu", "prologue.cu", "prefill_tc.cu", "prefill_pair.cu", "prefill_fp32.cu", "decode.cu", "decode_noalloc.cu"]
+SOURCES = ["api.cu", "prologue.cu", "prefill_tc.cu", "prefill_pair.cu", "prefill_fp32.cu", "decode.cu", "decode_noalloc.cu",
+           "oproj.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -415,6 +415,34 @@ gattn_status gattn_prefill(const void* q, const void* k, const void* v, const vo
                         workspace_bytes, out, stream, nullptr);
 }
 
+gattn_status gattn_o_proj(const void* x, const void* w_o, int T, int K, int N, void* y, void* stream_) {
+    if (!x || !w_o || !y) return GATTN_ERR_INVALID_ARG;
+    if (T < 1 || K < 64 || N < 64 || K % 64 != 0 || N % 64 != 0) return GATTN_ERR_INVALID_ARG;
+    if ((int64_t)T * K >= ((int64_t)1 << 40) || (int64_t)T * N >= ((int64_t)1 << 40)) return GATTN_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(w_o, 16) || !aligned(y, 16)) return GATTN_ERR_INVALID_ARG;
+    unsigned int* status = status_ptr();
+    if (!status) return GATTN_ERR_CUDA;
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+    // x [T, K] and W_O [N, K] as (K, rows): 64-element (128-byte) slices, 128 rows of x
+    // and oproj_block_n(N) rows of W_O per box
+    CUtensorMap ta, tb;
+    const uint64_t adims[2] = {(uint64_t)K, (uint64_t)T}, bdims[2] = {(uint64_t)K, (uint64_t)N};
+    const uint64_t str[1] = {(uint64_t)K * 2};
+    const uint32_t abox[2] = {64, 128}, bbox[2] = {64, (uint32_t)oproj_block_n(N)};
+    if (!encode_bf16_map(&ta, x, 2, adims, str, abox)) return GATTN_ERR_CUDA;
+    if (!encode_bf16_map(&tb, w_o, 2, bdims, str, bbox)) return GATTN_ERR_CUDA;
+    OprojParams op;
+    std::memset(&op, 0, sizeof(op));
+    op.y = y;
+    op.T = T;
+    op.K = K;
+    op.N = N;
+    op.n_sms = sm_count();
+    op.status = status;
+    if (launch_oproj(op, ta, tb, stream, g_prof_start, g_prof_stop) != cudaSuccess) return GATTN_ERR_CUDA;
+    return GATTN_OK;
+}
+
 size_t gattn_prefill_varlen_workspace_size(int T, int nseq, int H, int G, int d, int dtype) {
     if (T < 1 || nseq < 1) return 0;
     const size_t base = prefill_ws(1, T, H, G, d, dtype);

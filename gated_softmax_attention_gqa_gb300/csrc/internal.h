@@ -119,6 +119,17 @@ cudaError_t launch_decode(const DecodeParams& p, const CUtensorMap& tm_kv, cudaS
                           cudaEvent_t ev_start, cudaEvent_t ev_stop);
 cudaError_t launch_decode_append(const AppendParams& p, cudaStream_t stream);
 
+// Output projection y = x W_O^T (bf16, tcgen05): x [T, K], W_O [N, K], y [T, N].
+struct OprojParams {
+    void* y;
+    int T, K, N;
+    int n_sms;
+    unsigned int* status;
+};
+int oproj_block_n(int N);  // output columns per tile (W_O rows per TMA box)
+cudaError_t launch_oproj(const OprojParams& p, const CUtensorMap& tmA, const CUtensorMap& tmB, cudaStream_t stream,
+                         cudaEvent_t ev_start, cudaEvent_t ev_stop);
+
 // Prefill tile geometry for the tcgen05 kernel, per head_dim.
 int prefill_block_n(int d);
 

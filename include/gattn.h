@@ -173,6 +173,24 @@ gattn_status gattn_prefill_varlen(const void* q, const void* k, const void* v, c
                                   void* out, void* stream);
 
 /*
+ * Output projection that follows the attention: y = x W_O^T, x the gated attention
+ * output in the layout gattn_prefill / gattn_prefill_varlen write ("Transformer by
+ * Hand, ch. 6", section "The code: qwen/attention.py": the concatenated heads, times
+ * the gate's sigmoid, go through o_proj; "Gated Attention for LLMs 论文阅读": the
+ * gate acts on the SDPA output ahead of the output projection).
+ *
+ * x    [T, K] bf16 device, row-major (K = H*d; row stride K elements).
+ * w_o  [N, K] bf16 device, row-major: the weight of a linear layer, y = x w_o^T.
+ * y    [T, N] bf16 device, row-major: sum_k x[t,k] w_o[n,k] in fp32, rounded once.
+ * T >= 1; K and N multiples of 64 (>= 64); x, w_o and y 16-byte aligned.  y must
+ * not overlap x or w_o.  Asynchronous on `stream`; the caller owns every buffer.
+ * Returns GATTN_ERR_INVALID_ARG for bad sizes, pointers or alignment, GATTN_ERR_CUDA
+ * if a launch fails; a bounded wait that runs out inside the kernel sets
+ * GATTN_DEVICE_TIMEOUT (gattn_get_device_status) and leaves y incomplete.
+ */
+gattn_status gattn_o_proj(const void* x, const void* w_o, int T, int K, int N, void* y, void* stream);
+
+/*
  * Bytes of workspace gattn_decode needs (per-split partial softmax states).
  * Depends on the current device's SM count.  Returns 0 for invalid sizes.
  */
@@ -308,8 +326,8 @@ gattn_status gattn_selftest_wait_timeout(unsigned long long limit_ns, unsigned l
 
 /*
  * Profiling hook.  When both events are non-NULL (cudaEvent_t passed as void*),
- * every later gattn_prefill / gattn_decode records `start` on its stream just
- * before its main attention kernel and `stop` just after it, so a caller can
+ * every later gattn_prefill / gattn_decode / gattn_o_proj records `start` on its
+ * stream just before its main kernel and `stop` just after it, so a caller can
  * time that kernel alone.  Pass NULL, NULL to switch it off.  Not thread-safe.
  */
 void gattn_set_profile_events(void* start, void* stop);

@@ -134,6 +134,16 @@ def sdpa_gate(q, k, v, gate_logits, gate_mode, want_attn=False):
     return (out, attn) if want_attn else out
 
 
+def o_proj(x, w_o):
+    """The output projection that follows the gated attention: the concatenated,
+    gated heads x [..., K] (K = H*d) times the o_proj weight w_o [N, K] transposed,
+    y[..., n] = sum_k x[..., k] w_o[n, k], in fp64 ("Transformer by Hand, ch. 6",
+    section "The code: qwen/attention.py": o_proj after the gate; the weight is a
+    linear layer's, applied as x W^T)."""
+    x, w = _f64(x), _f64(w_o)
+    return x @ w.T
+
+
 def prefill(q, k, v, gate_logits, qnorm_w, knorm_w, pos, rotary_dim, rope_base, eps, gate_mode):
     """Full prefill on raw q [B,S,H,d], k,v [B,S,G,d]; pos [B,S] or None."""
     q, k, v, qw, kw = _f64(q), _f64(k), _f64(v), _f64(qnorm_w), _f64(knorm_w)

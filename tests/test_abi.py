@@ -243,3 +243,14 @@ def test_flop_accounting_matches_the_causal_triangle():
     B, S, H, d = 2, 5, 3, 4
     madds = sum(2 * d for b in range(B) for h in range(H) for t in range(S) for j in range(t + 1))
     assert prefill_flops(B, S, H, d) == 2 * madds
+
+
+@pytest.mark.parametrize("kw", [
+    dict(x=None), dict(w=None), dict(y=None), dict(T=0), dict(K=32), dict(K=96), dict(N=0), dict(N=200),
+    dict(x=FAKE + 2), dict(w=FAKE + 8), dict(y=FAKE + 4),
+], ids=lambda kw: ",".join(f"{k}={v}" for k, v in kw.items()))
+def test_o_proj_rejects_bad_arguments(lib, kw):
+    a = dict(x=FAKE, w=FAKE + (1 << 30), T=4096, K=2048, N=1024, y=FAKE + (1 << 31))
+    a.update(kw)
+    vp = lambda v: None if v is None else ctypes.c_void_p(v)
+    assert lib.gattn_o_proj(vp(a["x"]), vp(a["w"]), a["T"], a["K"], a["N"], vp(a["y"]), None) == INVALID

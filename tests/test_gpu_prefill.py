@@ -4,7 +4,8 @@ import pytest
 import torch
 
 import oracle
-from gated_softmax_attention_gqa_gb300 import gattn_get_device_status, gattn_prefill, gattn_prefill_varlen, workloads
+from gated_softmax_attention_gqa_gb300 import (gattn_get_device_status, gattn_o_proj, gattn_prefill, gattn_prefill_varlen,
+                                               workloads)
 from gated_softmax_attention_gqa_gb300.workloads import WORKLOADS, Workload, make_prefill_inputs
 from tests.parity import assert_close_to_oracle, gate_scale, sample_rows
 
@@ -314,8 +315,10 @@ def test_output_feeds_the_o_projection(d, H, G):
     the gate sits (between SDPA and W_O: "Gated attention" handbook chapter, "The
     code: qwen/attention.py"; "Gated Attention" deep-dive, "门放在哪里？").  A bf16
     GEMM reads it in place (same storage, no re-layout) and gives the oracle's output
-    times W_O^T.  W_O rows have unit norm, so an output error e moves each projected
-    value by at most |e|_2 and typically by its RMS: the bf16 bounds still apply."""
+    times W_O^T -- through the library's own tcgen05 projection (gattn_o_proj) and,
+    as a cross-check of the handoff alone, through torch's GEMM.  W_O rows have unit
+    norm, so an output error e moves each projected value by at most |e|_2 and
+    typically by its RMS: the bf16 bounds still apply."""
     B, S, hidden = 2, 200, 512
     w = small("oproj", B, S, H, G, d, 64, 1e6, "elementwise", seed=21)
     inp = make_prefill_inputs(w)
@@ -325,10 +328,13 @@ def test_output_feeds_the_o_projection(d, H, G):
     g = torch.Generator().manual_seed(22)
     w_o = torch.randn(hidden, H * d, generator=g, dtype=torch.float64)
     w_o = (w_o / w_o.norm(dim=1, keepdim=True)).to(torch.bfloat16)
-    y = a @ w_o.to(DEV).t()
+    y = gattn_o_proj(a, w_o.to(DEV))
+    y_torch = a @ w_o.to(DEV).t()
     torch.cuda.synchronize()
-    ref = np.asarray(run_oracle(inp, w), dtype=np.float64).reshape(B * S, H * d) @ w_o.double().numpy().T
+    assert gattn_get_device_status() == 0
+    ref = oracle.o_proj(np.asarray(run_oracle(inp, w), dtype=np.float64).reshape(B * S, H * d), w_o)
     assert_close_to_oracle(y, ref, torch.bfloat16, f"o_proj d{d}")
+    assert_close_to_oracle(y_torch, ref, torch.bfloat16, f"o_proj d{d} (torch GEMM)")
 
 
 # More work items than the persistent grids have CTAs (152) or CTA pairs (76), so

@@ -475,3 +475,26 @@ def test_kv_cache_byte_accounting(golden):
     for kv_heads, key in ((g["G"], "expected_total_MB_gqa"), (g["H"], "expected_total_MB_mha")):
         total = g["layers"] * workloads.decode_kv_bytes([g["seq_len"]], kv_heads, g["d"], g["bytes_per_number"])
         assert round(total / 2**20, 1) == g[key]
+
+
+# ---- o_proj: y = x W_O^T (the step after the path)
+
+def test_o_proj_identity_and_permutation():
+    rng = np.random.default_rng(3)
+    x = rng.standard_normal((5, 8))
+    np.testing.assert_array_equal(oracle.o_proj(x, np.eye(8)), x)
+    perm = np.array([3, 0, 7, 1])
+    w = np.eye(8)[perm]  # row n of W_O selects feature perm[n]
+    np.testing.assert_array_equal(oracle.o_proj(x, w), x[:, perm])
+
+
+def test_o_proj_brute_force_and_linearity():
+    rng = np.random.default_rng(4)
+    x1, x2 = rng.standard_normal((3, 6)), rng.standard_normal((3, 6))
+    w = rng.standard_normal((2, 6))
+    want = np.array([[sum(x1[t, k] * w[n, k] for k in range(6)) for n in range(2)] for t in range(3)])
+    assert np.abs(oracle.o_proj(x1, w) - want).max() < 1e-12
+    lhs = oracle.o_proj(2.0 * x1 - 3.0 * x2, w)
+    rhs = 2.0 * oracle.o_proj(x1, w) - 3.0 * oracle.o_proj(x2, w)
+    assert np.abs(lhs - rhs).max() < 1e-12
+    assert oracle.o_proj(x1[None], w).shape == (1, 3, 2)  # leading dimensions pass through
