@@ -424,11 +424,11 @@ gattn_status gattn_o_proj(const void* x, const void* w_o, int T, int K, int N, v
     if (!status) return GATTN_ERR_CUDA;
     cudaStream_t stream = static_cast<cudaStream_t>(stream_);
     // x [T, K] and W_O [N, K] as (K, rows): 64-element (128-byte) slices, 128 rows of x
-    // and oproj_block_n(N) rows of W_O per box
+    // and oproj_box_rows(N) rows of W_O per box
     CUtensorMap ta, tb;
     const uint64_t adims[2] = {(uint64_t)K, (uint64_t)T}, bdims[2] = {(uint64_t)K, (uint64_t)N};
     const uint64_t str[1] = {(uint64_t)K * 2};
-    const uint32_t abox[2] = {64, 128}, bbox[2] = {64, (uint32_t)oproj_block_n(N)};
+    const uint32_t abox[2] = {64, 128}, bbox[2] = {64, (uint32_t)oproj_box_rows(N)};
     if (!encode_bf16_map(&ta, x, 2, adims, str, abox)) return GATTN_ERR_CUDA;
     if (!encode_bf16_map(&tb, w_o, 2, bdims, str, bbox)) return GATTN_ERR_CUDA;
     OprojParams op;

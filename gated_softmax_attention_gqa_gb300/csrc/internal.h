@@ -126,7 +126,8 @@ struct OprojParams {
     int n_sms;
     unsigned int* status;
 };
-int oproj_block_n(int N);  // output columns per tile (W_O rows per TMA box)
+int oproj_block_n(int N);   // output columns per tile
+int oproj_box_rows(int N);  // W_O rows per TMA box (half a tile's: each CTA of a pair holds half)
 cudaError_t launch_oproj(const OprojParams& p, const CUtensorMap& tmA, const CUtensorMap& tmB, cudaStream_t stream,
                          cudaEvent_t ev_start, cudaEvent_t ev_stop);
 
