@@ -75,6 +75,14 @@ struct PfCfg {
     static constexpr int NH = PSMEM ? 1 : 2;
     static constexpr bool SPLIT = NH > 1;
     static constexpr int SOFTMAX_WARPS = 4 * NH;
+    // d <= 128: a warpgroup of its own runs the Q prologue of the next item while the
+    // current one is computed, into the other of two Q' buffers in TMEM, so that an
+    // item boundary costs the softmax warps only the epilogue.  d = 256: the softmax
+    // warps run the prologue (no TMEM left for a second Q').
+    static constexpr bool QPW = PERSIST;
+    static constexpr int NQB = QPW ? 2 : 1;            // Q' buffers in TMEM: item n uses n % NQB
+    static constexpr int SM_WARP0 = QPW ? 4 : 3;       // first softmax warp
+    static constexpr int PRO_WARPS = QPW ? 4 : 0;      // prologue warps (the last warpgroup)
     static constexpr int NSB = 2;  // score buffers in TMEM: tile j uses buffer j % 2
     static constexpr int NPB = PSMEM ? 2 : 0;  // P buffers in shared memory
     static constexpr int NSK = PERSIST ? 2 : 3;  // K ring stages
@@ -89,7 +97,7 @@ struct PfCfg {
     static constexpr int TM_S = D;                   // score buffer b at TM_S + b * BN
     static constexpr int TM_Q = D + NSB * BN;
     static constexpr int TM_COLS = 512;
-    static_assert(TM_Q + D / 2 <= TM_COLS, "TMEM budget");
+    static_assert(TM_Q + NQB * (D / 2) <= TM_COLS, "TMEM budget");
     // d <= 128: P_j (bf16 pairs) is written over S_j in TMEM, and the issuer of tile j
     // issues S_{j+2} = Q'K'_{j+2}^T right behind PV_j (the tensor pipe runs one
     // thread's MMAs in issue order).  d = 256: P_j in shared memory, S_{j+2} as soon
@@ -107,7 +115,7 @@ struct PfCfg {
     static constexpr int OFF_OUT = PERSIST ? OFF_GB : OFF_V;
     static_assert(PERSIST || (QTILE_BYTES <= NSV * TILE_BYTES && QTILE_BYTES <= NSK * TILE_BYTES),
                   "raw Q, gate and output tiles must fit the rings they borrow");
-    static constexpr int NBAR = 2 * NSK + 2 * NSV + 19;
+    static constexpr int NBAR = 2 * NSK + 2 * NSV + 21;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr int OFF_W = (OFF_MISC + 16 + 127) & ~127;  // qnorm weights, D bf16
     static constexpr int OFF_X = OFF_W + D * 2;                  // exchange between a row's threads (SPLIT)
@@ -116,7 +124,16 @@ struct PfCfg {
     // can never share the SM (each CTA allocates all 512 TMEM columns).
     static constexpr int SMEM_ALLOC = (SMEM_BYTES + 1024) > 122880 ? (SMEM_BYTES + 1024) : 122880;
     static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
-    static constexpr int THREADS = 96 + 32 * SOFTMAX_WARPS;
+    // QPW: warpgroup 0 = producer, two issuers and an idle warp; warpgroups 1-2 the
+    // softmax; warpgroup 3 the prologue.  The registers of the launch (128 a thread)
+    // are split by setmaxnreg: 72 | 176 | 88, summing exactly to the 64 K the block
+    // was launched with.
+    static constexpr int THREADS = QPW ? 128 * 4 : 96 + 32 * SOFTMAX_WARPS;
+    static constexpr int REG_LAUNCH = 128, REG_CTRL = 72, REG_SOFTMAX = 176, REG_PRO = 88;
+    static_assert(!QPW || (SM_WARP0 == 4 && SOFTMAX_WARPS == 8 && PRO_WARPS == 4), "one role per warpgroup");
+    static_assert(!QPW || 128 * REG_CTRL + 32 * SOFTMAX_WARPS * REG_SOFTMAX + 32 * PRO_WARPS * REG_PRO <=
+                              THREADS * REG_LAUNCH,
+                  "register split within the launch allocation");
     static constexpr uint32_t IDESC_QK = make_idesc_bf16(128, BN, false);
     static constexpr uint32_t IDESC_PV = make_idesc_bf16(128, D, true);
     static constexpr float RESCALE_THRESHOLD = 8.0f;  // log2 domain: rescale when the max grows by > 2^8
@@ -143,6 +160,7 @@ struct Bars {
     __device__ uint32_t xchg(int q) const { return at(r() + 13 + q); }  // both halves of row quarter q posted
     __device__ uint32_t o_staged() const { return at(r() + 17); }  // every softmax warp staged an item's output
     __device__ uint32_t o_free() const { return at(r() + 18); }    // an item's epilogue has read O
+    __device__ uint32_t q_free(int i) const { return at(r() + 19 + i); }  // QPW: Q' buffer i no longer read
 };
 
 // ----------------------------------------------------------------- work items
@@ -401,7 +419,7 @@ __device__ __forceinline__ void tc_pv_steps(uint32_t d_tmem, uint32_t p_tmem, ui
 }
 
 template <int D>
-__device__ __forceinline__ bool issue_qk(int j, const Bars& bars, uint32_t tm, uint32_t k_lo0,
+__device__ __forceinline__ bool issue_qk(int j, const Bars& bars, uint32_t tm, uint32_t q_col, uint32_t k_lo0,
                                          volatile int* abort_flag, unsigned int* status) {
     using C = PfCfg<D>;
     const int sb = j & 1;
@@ -413,7 +431,7 @@ __device__ __forceinline__ bool issue_qk(int j, const Bars& bars, uint32_t tm, u
     const int st = j % C::NSK;
     if (!mbar_wait(bars.k_full(st), (uint32_t)(j / C::NSK) & 1u, abort_flag, status)) return false;
     tc_fence_after();
-    tc_qk_steps<D, 0>(tm + C::TM_S + sb * C::BN, tm + C::TM_Q, k_lo0 + (uint32_t)((st * C::TILE_BYTES) >> 4));
+    tc_qk_steps<D, 0>(tm + C::TM_S + sb * C::BN, tm + q_col, k_lo0 + (uint32_t)((st * C::TILE_BYTES) >> 4));
     tc_commit(bars.k_empty(st));
     tc_commit(bars.s_full(sb));
     return true;
@@ -458,24 +476,104 @@ __device__ void run_mma(int parity, const PrefillParams& p, const Bars& bars, ui
         // the item's Q' is in TMEM
         if (!(ok = mbar_wait(bars.q_ready(), (uint32_t)n_it & 1u, abort_flag, status))) break;
         tc_fence_after();
+        const uint32_t q_col = (uint32_t)(C::TM_Q + (n_it % C::NQB) * (D / 2));  // the item's Q' buffer
         const int j0 = jb + ((jb & 1) != parity ? 1 : 0);
-        if (j0 < je) ok = issue_qk<D>(j0, bars, tm, kdesc0, abort_flag, status);
+        if (j0 < je) ok = issue_qk<D>(j0, bars, tm, q_col, kdesc0, abort_flag, status);
         for (int j = j0; ok && j < je; j += 2) {
             if constexpr (C::P_OVER_S) {
                 // S_{j+2} is written over P_j, right behind the PV_j that reads it
                 if (!issue_pv<D>(j, j == jb, n_it, bars, tm, vdesc0, pdesc0, abort_flag, status)) { ok = false; break; }
-                if (j + 2 < je && !issue_qk<D>(j + 2, bars, tm, kdesc0, abort_flag, status)) { ok = false; break; }
+                if (j + 2 < je && !issue_qk<D>(j + 2, bars, tm, q_col, kdesc0, abort_flag, status)) { ok = false; break; }
             } else {
                 // QK of this issuer's next tile goes out as soon as its score buffer is
                 // free, ahead of the PV that is still waiting for its P
-                if (j + 2 < je && !issue_qk<D>(j + 2, bars, tm, kdesc0, abort_flag, status)) { ok = false; break; }
+                if (j + 2 < je && !issue_qk<D>(j + 2, bars, tm, q_col, kdesc0, abort_flag, status)) { ok = false; break; }
                 if (!issue_pv<D>(j, j == jb, n_it, bars, tm, vdesc0, pdesc0, abort_flag, status)) { ok = false; break; }
             }
         }
         if (ok) tc_commit(bars.o_final());  // count 2: both issuers' PVs of the item complete
+        // QPW: and with them every QK of the item (each issuer's last MMAs of an item are
+        // a PV): its Q' buffer may take item n_it + 2's
+        if (C::QPW && ok) tc_commit(bars.q_free(n_it & 1));
         jb = je;
     }
     tc_commit(bars.drain());
+}
+
+// ----------------------------------------------------------------- Q prologue warpgroup (QPW)
+
+// Item n's Q' = rope(rmsnorm(q)) as bf16 pairs into TMEM buffer n % 2, one thread per
+// query row (warp w reaches TMEM lanes 32 (w % 4) + [0, 32)).  Buffer n % 2 was
+// last read by item n - 2's QK MMAs (q_free); the raw Q tile has landed (q_full).
+// The arithmetic is the softmax warps' split-row prologue in the same order (the
+// two halves' sums of squares, each over four interleaved partial sums, then added;
+// every rotated pair on its own), so Q' is bit for bit the same either way.
+template <int D, bool GV>
+__device__ void run_qprologue(const PrefillParams& p, const Bars& bars, uint32_t sbase, uint32_t tm, int quarter,
+                              int lane, int cta, int ncta, volatile int* abort_flag) {
+    using C = PfCfg<D>;
+    constexpr int OC = D / C::NH;
+    const int row = quarter * 32 + lane;
+    const uint32_t tl = tm + ((uint32_t)(quarter * 32) << 16);
+    const uint32_t qbase = sbase + C::OFF_Q;
+    const uint32_t wbase = sbase + C::OFF_W;
+    TcItem it;
+    for (int r = 0; tc_item<D, GV>(p, cta, ncta, r, it); ++r) {
+        if (r >= 2 &&
+            !__all_sync(0xffffffffu, mbar_wait(bars.q_free(r & 1), (uint32_t)((r >> 1) - 1) & 1u, abort_flag, p.status)))
+            return;
+        if (!__all_sync(0xffffffffu, mbar_wait(bars.q_full(), (uint32_t)r & 1u, abort_flag, p.status))) return;
+        tc_fence_after();
+        const int t = it.qt * C::BM + row;  // from the start of the sequence
+        const bool valid = t < it.len;
+        const int64_t tok = (int64_t)it.b * p.S + it.t0 + (valid ? t : 0);
+        float sq = 0.f;
+#pragma unroll
+        for (int hf = 0; hf < C::NH; ++hf) {
+            float ss[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int c = 0; c < OC / 8; ++c) {
+                float f[8];
+                unpack8(lds_v4(rowtile_addr(qbase, row, hf * OC + 8 * c)), f);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) ss[e & 3] = fmaf(f[e], f[e], ss[e & 3]);
+            }
+            const float part = (ss[0] + ss[1]) + (ss[2] + ss[3]);
+            sq = hf == 0 ? part : sq + part;
+        }
+        const float rinv = rsqrtf(sq / (float)D + p.eps);
+        const float posf = valid ? (p.pos ? (float)p.pos[tok] : (float)t) : 0.f;
+        const int half = p.rd >> 1;
+        const uint32_t qcol = tl + (uint32_t)(C::TM_Q + (r & 1) * (D / 2));
+#pragma unroll 1
+        for (int i0 = 0; i0 < half; i0 += 8) {
+            float xa[8], xb[8], wa[8], wb[8];
+            unpack8(lds_v4(rowtile_addr(qbase, row, i0)), xa);
+            unpack8(lds_v4(rowtile_addr(qbase, row, i0 + half)), xb);
+            unpack8(lds_v4(wbase + 2 * i0), wa);
+            unpack8(lds_v4(wbase + 2 * (i0 + half)), wb);
+            uint32_t lo[4], hi[4];
+            rope_rotate8(xa, xb, wa, wb, p.inv_freq + i0, posf, rinv, lo, hi);
+            __syncwarp();
+            tmem_st4(qcol + (i0 >> 1), lo[0], lo[1], lo[2], lo[3]);
+            tmem_st4(qcol + ((i0 + half) >> 1), hi[0], hi[1], hi[2], hi[3]);
+        }
+#pragma unroll 1
+        for (int e0 = p.rd; e0 < D; e0 += 8) {
+            float x[8], w[8];
+            unpack8(lds_v4(rowtile_addr(qbase, row, e0)), x);
+            unpack8(lds_v4(wbase + 2 * e0), w);
+            uint32_t o[4];
+            scale8_bf16(x, w, rinv, o);
+            __syncwarp();
+            tmem_st4(qcol + (e0 >> 1), o[0], o[1], o[2], o[3]);
+        }
+        fence_proxy_async_smem();  // our reads of the raw Q tile happen before the next copy overwrites it
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bars.q_ready());
+    }
 }
 
 // ----------------------------------------------------------------- softmax / prologue / epilogue
@@ -580,7 +678,7 @@ __device__ void run_softmax(const PrefillParams& p, const Bars& bars, uint32_t s
     int jb = 0, n_it = 0;
     TcItem item, next;
     bool have = tc_item<D, GV>(p, cta, ncta, 0, item);
-    if (have && !prologue(item, 0)) return;
+    if (!C::QPW && have && !prologue(item, 0)) return;
     for (int r = 0; have; ++r, ++n_it) {
         const int qt = item.qt, b = item.b, h = item.h, n_kv = item.n_kv;
         const int t = qt * C::BM + row;  // from the start of the sequence
@@ -730,9 +828,10 @@ __device__ void run_softmax(const PrefillParams& p, const Bars& bars, uint32_t s
             }
         }
 
-        // ---- the next item's Q prologue: its first QK MMAs then run during this epilogue
+        // ---- the next item's Q prologue (unless a warpgroup of its own has run it
+        // already): its first QK MMAs then run during this epilogue
         const bool more = tc_item<D, GV>(p, cta, ncta, r + 1, next);
-        if (more && !prologue(next, n_it + 1)) return;
+        if (!C::QPW && more && !prologue(next, n_it + 1)) return;
 
         // ---- epilogue: O / l * act(gate) (additive gate: O / l + act(gate)) -> bf16, this
         // thread's O columns, into the output tile (over the gate tile, each thread
@@ -890,7 +989,8 @@ __global__ void __launch_bounds__(PfCfg<D>::THREADS, 1)
         }
         for (int q = 0; q < 4; ++q) mbar_init(bars.xchg(q), C::NH);
         mbar_init(bars.o_final(), 2);
-        mbar_init(bars.q_ready(), C::SOFTMAX_WARPS);
+        mbar_init(bars.q_ready(), C::QPW ? C::PRO_WARPS : C::SOFTMAX_WARPS);
+        for (int i = 0; i < 2; ++i) mbar_init(bars.q_free(i), 2);
         mbar_init(bars.o_staged(), C::SOFTMAX_WARPS);
         mbar_init(bars.o_free(), C::SOFTMAX_WARPS);
         mbar_init(bars.drain(), 2);
@@ -914,7 +1014,29 @@ __global__ void __launch_bounds__(PfCfg<D>::THREADS, 1)
     tc_fence_after();
     const uint32_t tm = *tmem_slot;
 
-    if (warp == 0) {
+    if constexpr (C::QPW) {
+        if (warp >= C::SM_WARP0 + C::SOFTMAX_WARPS) {
+            regs_lower<C::REG_PRO>();
+            run_qprologue<D, GV>(p, bars, sbase, tm, warp & 3, lane, cta, ncta, abort_flag);
+        } else if (warp >= C::SM_WARP0) {
+            regs_raise<C::REG_SOFTMAX>();
+            run_softmax<D, GV>(p, bars, sbase, smem + C::OFF_X, tm, warp & 3, (warp - C::SM_WARP0) >> 2, lane, cta,
+                               ncta, abort_flag);
+        } else {
+            regs_lower<C::REG_CTRL>();
+            if (warp == 0) {
+                if (lane == 0)
+                    run_producer<D, GV>(&tmK, &tmV, &tmQ, &tmG, &tmO, p, bars, sbase, cta, ncta, abort_flag, p.status);
+            } else if (warp == 1 || warp == 2) {
+                if (lane == 0) {
+                    run_mma<D, GV>(warp - 1, p, bars, sbase, tm, cta, ncta, abort_flag, p.status);
+                    // no MMA of either issuer may still be in flight when TMEM is released
+                    if (warp == 2) mbar_wait_drain(bars.drain(), 0, p.status);
+                }
+            }
+            __syncwarp();
+        }
+    } else if (warp == 0) {
         if (lane == 0) run_producer<D, GV>(&tmK, &tmV, &tmQ, &tmG, &tmO, p, bars, sbase, cta, ncta, abort_flag, p.status);
         __syncwarp();
     } else if (warp == 1) {
@@ -928,8 +1050,8 @@ __global__ void __launch_bounds__(PfCfg<D>::THREADS, 1)
         }
         __syncwarp();
     } else {
-        run_softmax<D, GV>(p, bars, sbase, smem + C::OFF_X, tm, warp & 3, (warp - 3) >> 2, lane, cta, ncta,
-                           abort_flag);
+        run_softmax<D, GV>(p, bars, sbase, smem + C::OFF_X, tm, warp & 3, (warp - C::SM_WARP0) >> 2, lane, cta,
+                           ncta, abort_flag);
     }
     tc_fence_before();
     __syncthreads();
@@ -947,6 +1069,12 @@ cudaError_t launch_d(const PrefillParams& p, const PrefillMaps& maps, cudaStream
     auto kernel = gv ? prefill_tc_kernel<D, true> : prefill_tc_kernel<D, false>;
     cudaError_t e = set_smem_once(reinterpret_cast<const void*>(kernel), C::SMEM_ALLOC);
     if (e != cudaSuccess) return e;
+    if (C::QPW) {
+        // the setmaxnreg split draws on the launch's registers: never launch with fewer
+        cudaFuncAttributes fa;
+        if ((e = cudaFuncGetAttributes(&fa, reinterpret_cast<const void*>(kernel))) != cudaSuccess) return e;
+        if (fa.numRegs != C::REG_LAUNCH) return cudaErrorInvalidConfiguration;
+    }
     const long long n_items = p.vtiles ? (long long)p.n_vtiles * p.H : (long long)p.n_qtiles * p.B * p.H;
     if (n_items > 0x7fffffffLL || n_items < 1) return cudaErrorInvalidValue;
     // persistent: one CTA per SM at most; one item per CTA otherwise
