@@ -13,24 +13,27 @@
 // work items (query tile, head, batch), heaviest tile first, in a snake over
 // rounds; ring stages, score buffers and barrier phases run on tile and item
 // counters that continue across items.  While one item finishes (last softmax,
-// PV, epilogue, output store) the next one's Q tile has landed, its prologue has
-// run and its first QK MMAs are in the tensor pipe.  d = 256 (odd H/G only): one
-// item per CTA.
+// PV, epilogue, output store) the next one's Q' is in TMEM already (computed by a
+// warpgroup of its own during the previous item), its first K' tiles have landed
+// and its first QK MMAs are in the tensor pipe.  d = 256 (odd H/G only): one item
+// per CTA.
 //
-// Roles (11 warps at d <= 128, 7 at d = 256):
+// Roles (16 warps at d <= 128, 7 at d = 256):
 //   warp 0      TMA producer: per item the raw Q tile, K' tiles (keys normed and
 //               rotated by the pre-pass) and raw V tiles into 2-stage rings (128 B
 //               swizzle), the gate tile, and the TMA stores of the staged output.
 //   warps 1, 2  MMA issuers (warp 1 also owns TMEM): warp 1 + i issues S = Q'K'^T
 //               (tcgen05.mma, A read from TMEM) and O += P V of the KV tiles j
 //               with j % 2 == i (j counting tiles over all items).
-//   warps 3..   the fused Q prologue (RMSNorm + RoPE of the raw query row, read
-//               from shared memory, written as bf16 straight into TMEM), the online
-//               softmax, and the gate epilogue.  d <= 128: 8 warps, two threads per
-//               query row (warps w and w + 4 share the row's TMEM lanes), each owning
-//               half of the keys of every tile and half of O's columns; the halves
-//               swap their tile maxima through shared memory.  d = 256: 4 warps, one
-//               thread per row.
+//   softmax     the online softmax and the gate epilogue.  d <= 128: warps 4..11,
+//               two threads per query row (warps w and w + 4 share the row's TMEM
+//               lanes), each owning half of the keys of every tile and half of O's
+//               columns (the halves swap tile maxima through shared memory); d = 256:
+//               warps 3..6, one thread per row, which also run the Q prologue.
+//   prologue    d <= 128: warps 12..15, the fused Q prologue (RMSNorm + RoPE of the
+//               raw query row, read from shared memory, written as bf16 straight
+//               into TMEM), one thread per row, an item ahead of the softmax.
+//   (warp 3 is idle at d <= 128: setmaxnreg acts on whole warpgroups.)
 //
 // Shared memory, d <= 128: raw Q tile | K ring | V ring | gate tile, which the
 // epilogue overwrites with the output tile staged for the TMA stores.  d = 256:
@@ -43,18 +46,23 @@
 //   [0, d)             O accumulator, fp32 (the first PV of an item overwrites it)
 //   [d, d+BN)          S buffer 0 (fp32 scores)
 //   [d+BN, d+2BN)      S buffer 1
-//   [d+2BN, d+2BN+d/2) Q' as packed bf16 pairs (A operand of S = Q'K'^T)
-//   then (d <= 128)    P as packed bf16 pairs, BN/2 columns (A operand of O += PV)
+//   [d+2BN, d+2BN+d/2) Q' as packed bf16 pairs (A operand of S = Q'K'^T); d <= 128:
+//                      two such buffers, item n in buffer n % 2
+//   P (bf16 pairs, the A operand of O += PV) is written over its own scores (d <=
+//   128), or goes to shared memory (d = 256)
 //
-// Pipeline: a score buffer is handed back as soon as the softmax has loaded S_j,
-// so QK_{j+2} runs while the softmax still works on tile j (and S_{j+1} is already
-// waiting); P_j goes to its own buffer (TMEM, or shared memory at d = 256) once
-// PV_{j-1} (PV_{j-2} at d = 256) has read the previous P, and P_j V_j follows as
-// soon as P_j lands.
-// The running max is only refreshed (and O rescaled in TMEM) when it grows by
-// more than 2^8, so the rescale is rare and exact: O and l always share one
-// reference max.  The causal mask is applied by skipping every KV tile past the
-// query tile and masking only the tiles that straddle the diagonal.
+// Pipeline, d <= 128: the issuer of tile j issues S_{j+2} = Q'K'_{j+2}^T into
+// tile j's score buffer right behind PV_j, which reads P_j from there (one
+// thread's MMAs run in issue order), so S_{j+1} is waiting while the softmax works
+// on tile j.  d = 256: a score buffer is handed back as soon as the softmax has
+// loaded S_j, and P_j goes to shared-memory buffer j % 2 once PV_{j-2} has read it.
+// P_j V_j follows as soon as P_j lands.
+// The exponent's reference is the logits' bound from the QK-norm weights when that
+// is small enough (no row maximum at all); otherwise a running max, refreshed (and
+// O rescaled in TMEM) only when it grows by more than 2^8, so the rescale is rare
+// and exact: O and l always share one reference.  The causal mask is applied by
+// skipping every KV tile past the query tile and masking only the tiles that
+// straddle the diagonal.
 #include "common.cuh"
 #include "internal.h"
 
@@ -291,7 +299,11 @@ __device__ void run_producer(const CUtensorMap* tmK, const CUtensorMap* tmV, con
             g_done = true;
         }
         bool v_open = C::PERSIST;
-        const int ke = nk + it.n_kv, ve = nv + it.n_kv;
+        // tiles [jb, ke) of K' and V belong to this item.  Persistent: once its K' tiles
+        // are all on their way, the next item's first ones (up to the ring's depth) go
+        // out from this loop too, while it still waits for ring stages of V.
+        const int ke = jb + it.n_kv, ve = jb + it.n_kv;
+        const int kx = ke + (C::PERSIST && more ? min(nxt.n_kv, C::NSK) : 0);
         const unsigned long long t0 = global_timer_ns();
         uint32_t spins = 0;
         while (nk < ke || nv < ve) {
@@ -307,15 +319,17 @@ __device__ void run_producer(const CUtensorMap* tmK, const CUtensorMap* tmV, con
                 gate_in(it);
                 g_done = progressed = true;
             }
-            if (nk < ke &&
+            if (nk < kx &&
                 (nk < C::NSK || mbar_test_wait(bars.k_empty(nk % C::NSK), ((uint32_t)(nk / C::NSK) & 1u) ^ 1u))) {
                 const int st = nk % C::NSK;
                 mbar_arrive_expect_tx(bars.k_full(st), C::TILE_BYTES);
                 const uint32_t kdst = sbase + C::OFF_K + st * C::TILE_BYTES;
+                const bool cur = nk < ke;
+                const int krow = cur ? it.t0 + (nk - jb) * C::BN : nxt.t0 + (nk - ke) * C::BN;
+                const int kgrp = cur ? it.b * p.G + g : nxt.b * p.G + nxt.h / (p.H / p.G);
 #pragma unroll
                 for (int c = 0; c < C::KCH; ++c)
-                    tma_load_3d(kdst + c * C::CHUNK_BYTES, tmK, bars.k_full(st), c * 64, it.t0 + (nk - jb) * C::BN,
-                                it.b * p.G + g);
+                    tma_load_3d(kdst + c * C::CHUNK_BYTES, tmK, bars.k_full(st), c * 64, krow, kgrp);
                 ++nk;
                 progressed = true;
             }
@@ -345,7 +359,7 @@ __device__ void run_producer(const CUtensorMap* tmK, const CUtensorMap* tmV, con
                 }
             }
         }
-        if (nk != ke || nv != ve) {
+        if (nk < ke || nv != ve) {
             ok = false;
             break;
         }
@@ -492,9 +506,6 @@ __device__ void run_mma(int parity, const PrefillParams& p, const Bars& bars, ui
             }
         }
         if (ok) tc_commit(bars.o_final());  // count 2: both issuers' PVs of the item complete
-        // QPW: and with them every QK of the item (each issuer's last MMAs of an item are
-        // a PV): its Q' buffer may take item n_it + 2's
-        if (C::QPW && ok) tc_commit(bars.q_free(n_it & 1));
         jb = je;
     }
     tc_commit(bars.drain());
@@ -949,6 +960,9 @@ __device__ void run_softmax(const PrefillParams& p, const Bars& bars, uint32_t s
         fence_proxy_async_smem();  // the TMA stores read the staged tile through the async proxy
         __syncwarp();
         if (lane == 0) mbar_arrive(bars.o_staged());
+        // QPW: every QK of the item completed before its last PV (o_final): its Q' buffer
+        // may take item n_it + 2's, whose prologue then runs after this epilogue
+        if (C::QPW && lane == 0) mbar_arrive(bars.q_free(n_it & 1));
         jb += n_kv;
         item = next;
         have = more;
@@ -990,7 +1004,7 @@ __global__ void __launch_bounds__(PfCfg<D>::THREADS, 1)
         for (int q = 0; q < 4; ++q) mbar_init(bars.xchg(q), C::NH);
         mbar_init(bars.o_final(), 2);
         mbar_init(bars.q_ready(), C::QPW ? C::PRO_WARPS : C::SOFTMAX_WARPS);
-        for (int i = 0; i < 2; ++i) mbar_init(bars.q_free(i), 2);
+        for (int i = 0; i < 2; ++i) mbar_init(bars.q_free(i), C::SOFTMAX_WARPS);
         mbar_init(bars.o_staged(), C::SOFTMAX_WARPS);
         mbar_init(bars.o_free(), C::SOFTMAX_WARPS);
         mbar_init(bars.drain(), 2);
