@@ -184,26 +184,33 @@ struct TcItem {
     bool direct;  // a partial tile of packed sequences: rows are stored one by one
 };
 
+// The launch keeps the item count below 2^31, so u (at most the count plus the
+// grid size) and every product here fit 32-bit unsigned arithmetic, whose
+// division is a few instructions (the 64-bit one is a long software sequence, run
+// by every role at every item boundary).
 template <int D, bool GV>
 __device__ __forceinline__ bool tc_item(const PrefillParams& p, int c, int n, int r, TcItem& it) {
     using C = PfCfg<D>;
-    const long long u = (long long)r * n + ((r & 1) ? n - 1 - c : c);
+    const unsigned u = (unsigned)r * (unsigned)n + (unsigned)((r & 1) ? n - 1 - c : c);
+    const unsigned nh = (unsigned)p.H;
     if (GV && p.vtiles) {
-        if (u >= (long long)p.n_vtiles * p.H) return false;
-        const int4 e = p.vtiles[u / p.H];
+        if (u >= (unsigned)p.n_vtiles * nh) return false;
+        const unsigned tile = u / nh;
+        const int4 e = p.vtiles[tile];
         it.qt = e.z;
         it.t0 = e.x;
         it.len = e.y;
         it.b = 0;
-        it.h = (int)(u % p.H);
+        it.h = (int)(u - tile * nh);
         it.direct = (it.qt + 1) * C::BM > it.len;  // a TMA store of 128 rows would reach the next sequence
     } else {
-        const long long bh_count = (long long)p.B * p.H;
-        if (u >= (long long)p.n_qtiles * bh_count) return false;
-        it.qt = p.n_qtiles - 1 - (int)(u / bh_count);
-        const int bh = (int)(u % bh_count);
-        it.b = bh / p.H;
-        it.h = bh % p.H;
+        const unsigned bh_count = (unsigned)p.B * nh;
+        if (u >= (unsigned)p.n_qtiles * bh_count) return false;
+        const unsigned q = u / bh_count;
+        it.qt = p.n_qtiles - 1 - (int)q;
+        const unsigned bh = u - q * bh_count, b = bh / nh;
+        it.b = (int)b;
+        it.h = (int)(bh - b * nh);
         it.t0 = 0;
         it.len = p.S;
         it.direct = false;
@@ -695,13 +702,12 @@ __device__ void run_softmax(const PrefillParams& p, const Bars& bars, uint32_t s
         const int t = qt * C::BM + row;  // from the start of the sequence
         const bool valid = t < item.len;
         const int64_t tok = (int64_t)b * p.S + item.t0 + (valid ? t : 0);
-        float gate_head = 1.f;  // the activation of a headwise logit
-        if ((GV ? gate_layout(p.gate_mode) : p.gate_mode) == GATTN_GATE_HEADWISE && valid) {
-            const bf16* grow =
-                static_cast<const bf16*>(p.gate) + tok * p.gate_tok_stride + (int64_t)h * p.gate_head_stride;
-            const float z = __bfloat162float(grow[0]);
-            gate_head = GV ? gate_act(z, sigmoid_tanh(z), p.gate_mode) : sigmoid_tanh(z);
-        }
+        // a headwise logit: loaded now, activated in the epilogue (so that nothing
+        // waits for the load before the first scores)
+        const bool headwise = (GV ? gate_layout(p.gate_mode) : p.gate_mode) == GATTN_GATE_HEADWISE && valid;
+        bf16 z_head = __float2bfloat16(0.f);
+        if (headwise)
+            z_head = static_cast<const bf16*>(p.gate)[tok * p.gate_tok_stride + (int64_t)h * p.gate_head_stride];
 
         // ---- main loop: online softmax over the KV tiles this query tile can see
         const int row_min = qt * C::BM;
@@ -869,6 +875,11 @@ __device__ void run_softmax(const PrefillParams& p, const Bars& bars, uint32_t s
         tc_fence_after();
         const float inv_l = 1.f / l_row;
         // out = o * gv + ga
+        float gate_head = 1.f;  // the activation of the headwise logit
+        if (headwise) {
+            const float z = __bfloat162float(z_head);
+            gate_head = GV ? gate_act(z, sigmoid_tanh(z), p.gate_mode) : sigmoid_tanh(z);
+        }
         const float gh = additive ? inv_l : inv_l * gate_head, gha = additive ? gate_head : 0.f;
         bf16* orow = static_cast<bf16*>(p.out) + (tok * p.H + h) * D;
         const uint32_t gbase = sbase + C::OFF_G;
