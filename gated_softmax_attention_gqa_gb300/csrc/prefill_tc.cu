@@ -25,14 +25,15 @@
 //   warps 1, 2  MMA issuers (warp 1 also owns TMEM): warp 1 + i issues S = Q'K'^T
 //               (tcgen05.mma, A read from TMEM) and O += P V of the KV tiles j
 //               with j % 2 == i (j counting tiles over all items).
-//   softmax     the online softmax and the gate epilogue.  d <= 128: warps 4..11,
-//               two threads per query row (warps w and w + 4 share the row's TMEM
-//               lanes), each owning half of the keys of every tile and half of O's
-//               columns (the halves swap tile maxima through shared memory); d = 256:
-//               warps 3..6, one thread per row, which also run the Q prologue.
-//   prologue    d <= 128: warps 12..15, the fused Q prologue (RMSNorm + RoPE of the
-//               raw query row, read from shared memory, written as bf16 straight
-//               into TMEM), one thread per row, an item ahead of the softmax.
+//   softmax     the online softmax.  d <= 128: warps 4..11, two threads per query
+//               row (warps w and w + 4 share the row's TMEM lanes), each owning half
+//               of the keys of every tile and half of O's columns (the halves swap
+//               tile maxima through shared memory); d = 256: warps 3..6, one thread
+//               per row, which also run the Q prologue and the gate epilogue.
+//   prologue /  d <= 128: warps 12..15, one thread per query row: the fused Q
+//   epilogue    prologue (RMSNorm + RoPE of the raw query row, read from shared
+//               memory, written as bf16 straight into TMEM) of the item after next,
+//               and the gate epilogue of the item the softmax has just finished.
 //   (warp 3 is idle at d <= 128: setmaxnreg acts on whole warpgroups.)
 //
 // Shared memory, d <= 128: raw Q tile | K ring | V ring | gate tile, which the
@@ -83,10 +84,10 @@ struct PfCfg {
     static constexpr int NH = PSMEM ? 1 : 2;
     static constexpr bool SPLIT = NH > 1;
     static constexpr int SOFTMAX_WARPS = 4 * NH;
-    // d <= 128: a warpgroup of its own runs the Q prologue of the next item while the
-    // current one is computed, into the other of two Q' buffers in TMEM, so that an
-    // item boundary costs the softmax warps only the epilogue.  d = 256: the softmax
-    // warps run the prologue (no TMEM left for a second Q').
+    // d <= 128: a warpgroup of its own runs each item's epilogue and the Q prologue
+    // two items ahead, into the other of two Q' buffers in TMEM, so that the softmax
+    // warps go from an item's last tile straight to the next item's first.  d = 256:
+    // the softmax warps run both (no TMEM left for a second Q').
     static constexpr bool QPW = PERSIST;
     static constexpr int NQB = QPW ? 2 : 1;            // Q' buffers in TMEM: item n uses n % NQB
     static constexpr int SM_WARP0 = QPW ? 4 : 3;       // first softmax warp
@@ -133,11 +134,11 @@ struct PfCfg {
     static constexpr int SMEM_ALLOC = (SMEM_BYTES + 1024) > 122880 ? (SMEM_BYTES + 1024) : 122880;
     static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
     // QPW: warpgroup 0 = producer, two issuers and an idle warp; warpgroups 1-2 the
-    // softmax; warpgroup 3 the prologue.  The registers of the launch (128 a thread)
-    // are split by setmaxnreg: 72 | 176 | 88, summing exactly to the 64 K the block
-    // was launched with.
+    // softmax; warpgroup 3 the Q prologues and the epilogues.  The registers of the
+    // launch (128 a thread) are split by setmaxnreg: 72 | 168 | 104, summing exactly
+    // to the 64 K the block was launched with.
     static constexpr int THREADS = QPW ? 128 * 4 : 96 + 32 * SOFTMAX_WARPS;
-    static constexpr int REG_LAUNCH = 128, REG_CTRL = 72, REG_SOFTMAX = 176, REG_PRO = 88;
+    static constexpr int REG_LAUNCH = 128, REG_CTRL = 72, REG_SOFTMAX = 168, REG_PRO = 104;
     static_assert(!QPW || (SM_WARP0 == 4 && SOFTMAX_WARPS == 8 && PRO_WARPS == 4), "one role per warpgroup");
     static_assert(!QPW || 128 * REG_CTRL + 32 * SOFTMAX_WARPS * REG_SOFTMAX + 32 * PRO_WARPS * REG_PRO <=
                               THREADS * REG_LAUNCH,
@@ -166,9 +167,10 @@ struct Bars {
     __device__ uint32_t q_full() const { return at(r() + 11); }   // an item's raw Q tile landed
     __device__ uint32_t g_full() const { return at(r() + 12); }   // an item's gate tile landed / output buffer free
     __device__ uint32_t xchg(int q) const { return at(r() + 13 + q); }  // both halves of row quarter q posted
-    __device__ uint32_t o_staged() const { return at(r() + 17); }  // every softmax warp staged an item's output
+    __device__ uint32_t o_staged() const { return at(r() + 17); }  // every epilogue warp staged an item's output
     __device__ uint32_t o_free() const { return at(r() + 18); }    // an item's epilogue has read O
-    __device__ uint32_t q_free(int i) const { return at(r() + 19 + i); }  // QPW: Q' buffer i no longer read
+    // QPW: the softmax posted the row sums of item n, n % 2 == i
+    __device__ uint32_t l_full(int i) const { return at(r() + 19 + i); }
 };
 
 // ----------------------------------------------------------------- work items
@@ -518,29 +520,88 @@ __device__ void run_mma(int parity, const PrefillParams& p, const Bars& bars, ui
     tc_commit(bars.drain());
 }
 
-// ----------------------------------------------------------------- Q prologue warpgroup (QPW)
+// ----------------------------------------------------------------- gated output
 
-// Item n's Q' = rope(rmsnorm(q)) as bf16 pairs into TMEM buffer n % 2, one thread per
-// query row (warp w reaches TMEM lanes 32 (w % 4) + [0, 32)).  Buffer n % 2 was
-// last read by item n - 2's QK MMAs (q_free); the raw Q tile has landed (q_full).
-// The arithmetic is the softmax warps' split-row prologue in the same order (the
-// two halves' sums of squares, each over four interleaved partial sums, then added;
+// Columns [c, c + 32) of one query row of the output: o (the unnormalised O row from
+// TMEM, fp32 bits) / l times act(gate), or plus act(gate) for an additive gate, as
+// bf16 pairs handed to put(col, w0, w1, w2, w3), 8 columns at a time.  Logits that
+// vary over head_dim are read from the row-major gate tile at gbase; otherwise the
+// factors are the headwise (or unit) ones: out = o gh + gha.
+template <bool GV, typename Put>
+__device__ __forceinline__ void gate_out32(const PrefillParams& p, const uint32_t* ov, int c, int row, uint32_t gbase,
+                                           bool elementwise, bool additive, float inv_l, float gh, float gha,
+                                           Put&& put) {
+#pragma unroll
+    for (int q4 = 0; q4 < 4; ++q4) {
+        float gv[8], ga[8];  // out = o * gv + ga
+        if (elementwise) {
+            float f[8];
+            unpack8(lds_v4(rowtile_addr(gbase, row, c + 8 * q4)), f);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                if constexpr (GV) {
+                    const float a = gate_act(f[e], sigmoid_tanh(f[e]), p.gate_mode);
+                    gv[e] = additive ? inv_l : inv_l * a;
+                    ga[e] = additive ? a : 0.f;
+                } else {
+                    gv[e] = inv_l * sigmoid_tanh(f[e]);
+                    ga[e] = 0.f;
+                }
+            }
+        } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                gv[e] = gh;
+                ga[e] = gha;
+            }
+        }
+        uint32_t w[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int e = 2 * i;
+            const float o0 = __uint_as_float(ov[8 * q4 + e]), o1 = __uint_as_float(ov[8 * q4 + e + 1]);
+            if constexpr (GV)
+                w[i] = pack_bf16x2(fmaf(o0, gv[e], ga[e]), fmaf(o1, gv[e + 1], ga[e + 1]));
+            else
+                w[i] = pack_bf16x2(o0 * gv[e], o1 * gv[e + 1]);
+        }
+        put(c + 8 * q4, w[0], w[1], w[2], w[3]);
+    }
+}
+
+// ----------------------------------------------------------------- Q prologue / epilogue warpgroup (QPW)
+
+// The warpgroup runs, one thread per query row (warp w reaches TMEM lanes
+// 32 (w % 4) + [0, 32)), the Q prologues of items 0 and 1 and then, per item n, the
+// epilogue of item n followed by the prologue of item n + 2, so that the softmax
+// warps go from an item's last tile straight to the next one.
+//
+// Prologue of item n: Q' = rope(rmsnorm(q)) as bf16 pairs into TMEM buffer n % 2,
+// which item n - 2's QK MMAs last read (this warpgroup saw them complete in that
+// item's epilogue); the raw Q tile has landed (q_full).  The arithmetic is the
+// split-row prologue of the softmax warps (d = 256) in the same order (the two
+// halves' sums of squares, each over four interleaved partial sums, then added;
 // every rotated pair on its own), so Q' is bit for bit the same either way.
+//
+// Epilogue of item n: the row sum (the softmax's two halves, posted in shared memory
+// buffer n % 2), every PV of the item complete (o_final), the gate tile landed, then
+// O / l * act(gate) (additive gate: O / l + act(gate)) as bf16 into the staged output
+// tile (over the gate tile, each thread overwriting only gate values it has read),
+// which the producer writes to [B,S,H*d] with TMA stores (rows past S clipped); a
+// partial tile of packed sequences is stored row by row instead.  O is released
+// (o_free) once read, so that the next item's first PV may overwrite it.
 template <int D, bool GV>
-__device__ void run_qprologue(const PrefillParams& p, const Bars& bars, uint32_t sbase, uint32_t tm, int quarter,
-                              int lane, int cta, int ncta, volatile int* abort_flag) {
+__device__ void run_qwg(const PrefillParams& p, const Bars& bars, uint32_t sbase, const float* xsum, uint32_t tm,
+                        int quarter, int lane, int cta, int ncta, volatile int* abort_flag) {
     using C = PfCfg<D>;
     constexpr int OC = D / C::NH;
     const int row = quarter * 32 + lane;
     const uint32_t tl = tm + ((uint32_t)(quarter * 32) << 16);
     const uint32_t qbase = sbase + C::OFF_Q;
     const uint32_t wbase = sbase + C::OFF_W;
-    TcItem it;
-    for (int r = 0; tc_item<D, GV>(p, cta, ncta, r, it); ++r) {
-        if (r >= 2 &&
-            !__all_sync(0xffffffffu, mbar_wait(bars.q_free(r & 1), (uint32_t)((r >> 1) - 1) & 1u, abort_flag, p.status)))
-            return;
-        if (!__all_sync(0xffffffffu, mbar_wait(bars.q_full(), (uint32_t)r & 1u, abort_flag, p.status))) return;
+
+    auto prologue = [&](const TcItem& it, int n) -> bool {
+        if (!__all_sync(0xffffffffu, mbar_wait(bars.q_full(), (uint32_t)n & 1u, abort_flag, p.status))) return false;
         tc_fence_after();
         const int t = it.qt * C::BM + row;  // from the start of the sequence
         const bool valid = t < it.len;
@@ -562,7 +623,7 @@ __device__ void run_qprologue(const PrefillParams& p, const Bars& bars, uint32_t
         const float rinv = rsqrtf(sq / (float)D + p.eps);
         const float posf = valid ? (p.pos ? (float)p.pos[tok] : (float)t) : 0.f;
         const int half = p.rd >> 1;
-        const uint32_t qcol = tl + (uint32_t)(C::TM_Q + (r & 1) * (D / 2));
+        const uint32_t qcol = tl + (uint32_t)(C::TM_Q + (n & 1) * (D / 2));
 #pragma unroll 1
         for (int i0 = 0; i0 < half; i0 += 8) {
             float xa[8], xb[8], wa[8], wb[8];
@@ -591,6 +652,77 @@ __device__ void run_qprologue(const PrefillParams& p, const Bars& bars, uint32_t
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bars.q_ready());
+        return true;
+    };
+
+    auto epilogue = [&](const TcItem& it, int n) -> bool {
+        const int t = it.qt * C::BM + row;
+        const bool valid = t < it.len;
+        const int64_t tok = (int64_t)it.b * p.S + it.t0 + (valid ? t : 0);
+        const bool headwise = (GV ? gate_layout(p.gate_mode) : p.gate_mode) == GATTN_GATE_HEADWISE && valid;
+        bf16 z_head = __float2bfloat16(0.f);
+        if (headwise)
+            z_head = static_cast<const bf16*>(p.gate)[tok * p.gate_tok_stride + (int64_t)it.h * p.gate_head_stride];
+        if (!__all_sync(0xffffffffu, mbar_wait(bars.l_full(n & 1), (uint32_t)(n >> 1) & 1u, abort_flag, p.status)))
+            return false;
+        const float* xs = xsum + (n & 1) * C::NH * C::BM;
+        float l_row = xs[row];
+#pragma unroll
+        for (int i = 1; i < C::NH; ++i) l_row += xs[i * C::BM + row];
+        if (!__all_sync(0xffffffffu, mbar_wait(bars.o_final(), (uint32_t)n & 1u, abort_flag, p.status))) return false;
+        // the gate/output buffer holds this item's gate tile (or is free)
+        if (!__all_sync(0xffffffffu, mbar_wait(bars.g_full(), (uint32_t)n & 1u, abort_flag, p.status))) return false;
+        tc_fence_after();
+        const bool elementwise = GV ? gate_per_dim(p.gate_mode) : p.gate_mode == GATTN_GATE_ELEMENTWISE;
+        const bool additive = GV && gate_additive(p.gate_mode);
+        const float inv_l = 1.f / l_row;
+        float gate_head = 1.f;  // the activation of the headwise logit
+        if (headwise) {
+            const float z = __bfloat162float(z_head);
+            gate_head = GV ? gate_act(z, sigmoid_tanh(z), p.gate_mode) : sigmoid_tanh(z);
+        }
+        const float gh = additive ? inv_l : inv_l * gate_head, gha = additive ? gate_head : 0.f;
+        bf16* orow = static_cast<bf16*>(p.out) + (tok * p.H + it.h) * D;
+        const uint32_t gbase = sbase + C::OFF_G;
+        const uint32_t obase = sbase + C::OFF_OUT;
+        const bool direct = it.direct;
+        auto put = [&](int col, uint32_t w0, uint32_t w1, uint32_t w2, uint32_t w3) {
+            if (!direct) sts_v4(rowtile_addr(obase, row, col), w0, w1, w2, w3);
+            else if (valid) *reinterpret_cast<uint4*>(orow + col) = make_uint4(w0, w1, w2, w3);
+        };
+#pragma unroll 1
+        for (int c0 = 0; c0 < D; c0 += 32) {
+            uint32_t ro[32];
+            __syncwarp();
+            tmem_ld32(tl + C::TM_O + c0, ro);
+            if (c0 + 32 == D) {  // all of O read: the next item's first PV may overwrite it
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bars.o_free());
+            }
+            gate_out32<GV>(p, ro, c0, row, gbase, elementwise, additive, inv_l, gh, gha, put);
+        }
+        // the output buffer may be written out (a directly stored tile only frees it)
+        fence_proxy_async_smem();  // the TMA stores read the staged tile through the async proxy
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bars.o_staged());
+        return true;
+    };
+
+    TcItem it[3];  // items n, n + 1, n + 2
+    bool have[3];
+    have[0] = tc_item<D, GV>(p, cta, ncta, 0, it[0]);
+    have[1] = tc_item<D, GV>(p, cta, ncta, 1, it[1]);
+    if (have[0] && !prologue(it[0], 0)) return;
+    if (have[1] && !prologue(it[1], 1)) return;
+    for (int n = 0; have[0]; ++n) {
+        if (!epilogue(it[0], n)) return;
+        have[2] = tc_item<D, GV>(p, cta, ncta, n + 2, it[2]);
+        if (have[2] && !prologue(it[2], n + 2)) return;
+        it[0] = it[1];
+        have[0] = have[1];
+        it[1] = it[2];
+        have[1] = have[2];
     }
 }
 
@@ -615,8 +747,8 @@ __device__ void run_softmax(const PrefillParams& p, const Bars& bars, uint32_t s
     // the parts swap values through shared memory and then meet on an mbarrier (one
     // phase per use: every prologue, tile and epilogue).
     float* xmax = reinterpret_cast<float*>(smem_x);  // [2][NH][BM] tile maxima
-    float* xsum = xmax + 2 * NH * C::BM;             // [NH][BM] row sums
-    float* xss = xsum + NH * C::BM;                  // [NH][BM] sums of squares of q
+    float* xsum = xmax + 2 * NH * C::BM;             // [NH][BM] row sums (QPW: [2][NH][BM], by item parity)
+    float* xss = xsum + NH * C::BM;                  // [NH][BM] sums of squares of q (not QPW)
     const uint32_t xbar = bars.xchg(quarter);
     int xphase = 0;
     auto meet = [&]() -> bool {
@@ -845,10 +977,20 @@ __device__ void run_softmax(const PrefillParams& p, const Bars& bars, uint32_t s
             }
         }
 
-        // ---- the next item's Q prologue (unless a warpgroup of its own has run it
-        // already): its first QK MMAs then run during this epilogue
         const bool more = tc_item<D, GV>(p, cta, ncta, r + 1, next);
-        if (!C::QPW && more && !prologue(next, n_it + 1)) return;
+        if constexpr (C::QPW) {
+            // this half's row sum to the epilogue warpgroup (buffer n_it % 2), which
+            // finishes the item; on to the next item's first tile
+            xsum[((n_it & 1) * NH + hf) * C::BM + row] = l;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bars.l_full(n_it & 1));
+            jb += n_kv;
+            item = next;
+            have = more;
+            continue;
+        }
+        // ---- the next item's Q prologue: its first QK MMAs then run during this epilogue
+        if (more && !prologue(next, n_it + 1)) return;
 
         // ---- epilogue: O / l * act(gate) (additive gate: O / l + act(gate)) -> bf16, this
         // thread's O columns, into the output tile (over the gate tile, each thread
@@ -866,7 +1008,6 @@ __device__ void run_softmax(const PrefillParams& p, const Bars& bars, uint32_t s
         }
         if (!__all_sync(0xffffffffu, mbar_wait(bars.o_final(), (uint32_t)n_it & 1u, abort_flag, p.status))) return;
         const bool elementwise = GV ? gate_per_dim(p.gate_mode) : p.gate_mode == GATTN_GATE_ELEMENTWISE;
-        constexpr bool plain = !GV;
         const bool additive = GV && gate_additive(p.gate_mode);
         // persistent: the gate/output buffer holds this item's gate tile (or is free)
         if ((C::PERSIST || elementwise) &&
@@ -905,75 +1046,13 @@ __device__ void run_softmax(const PrefillParams& p, const Bars& bars, uint32_t s
                 if (lane == 0) mbar_arrive(bars.o_free());
             }
 #pragma unroll
-            for (int c1 = 0; c1 < OCH; c1 += 32) {
-                const int c = c0 + c1;
-                const uint32_t* ov = ro + c1;
-                if constexpr (plain) {
-                    float gv[32];
-                    if (elementwise) {
-#pragma unroll
-                        for (int q4 = 0; q4 < 4; ++q4) {
-                            float f[8];
-                            unpack8(lds_v4(rowtile_addr(gbase, row, c + 8 * q4)), f);
-#pragma unroll
-                            for (int e = 0; e < 8; ++e) gv[8 * q4 + e] = inv_l * sigmoid_tanh(f[e]);
-                        }
-                    } else {
-#pragma unroll
-                        for (int e = 0; e < 32; ++e) gv[e] = gh;
-                    }
-#pragma unroll
-                    for (int q4 = 0; q4 < 4; ++q4) {
-                        uint32_t w[4];
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            const int e = 8 * q4 + 2 * i;
-                            w[i] = pack_bf16x2(__uint_as_float(ov[e]) * gv[e], __uint_as_float(ov[e + 1]) * gv[e + 1]);
-                        }
-                        put(c + 8 * q4, w[0], w[1], w[2], w[3]);
-                    }
-                } else {
-                    float gv[32], ga[32];
-                    if (elementwise) {
-#pragma unroll
-                        for (int q4 = 0; q4 < 4; ++q4) {
-                            float f[8];
-                            unpack8(lds_v4(rowtile_addr(gbase, row, c + 8 * q4)), f);
-#pragma unroll
-                            for (int e = 0; e < 8; ++e) {
-                                const float a = gate_act(f[e], sigmoid_tanh(f[e]), p.gate_mode);
-                                gv[8 * q4 + e] = additive ? inv_l : inv_l * a;
-                                ga[8 * q4 + e] = additive ? a : 0.f;
-                            }
-                        }
-                    } else {
-#pragma unroll
-                        for (int e = 0; e < 32; ++e) {
-                            gv[e] = gh;
-                            ga[e] = gha;
-                        }
-                    }
-#pragma unroll
-                    for (int q4 = 0; q4 < 4; ++q4) {
-                        uint32_t w[4];
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            const int e = 8 * q4 + 2 * i;
-                            w[i] = pack_bf16x2(fmaf(__uint_as_float(ov[e]), gv[e], ga[e]),
-                                               fmaf(__uint_as_float(ov[e + 1]), gv[e + 1], ga[e + 1]));
-                        }
-                        put(c + 8 * q4, w[0], w[1], w[2], w[3]);
-                    }
-                }
-            }
+            for (int c1 = 0; c1 < OCH; c1 += 32)
+                gate_out32<GV>(p, ro + c1, c0 + c1, row, gbase, elementwise, additive, inv_l, gh, gha, put);
         }
         // the output buffer may be written out (a directly stored tile only frees it)
         fence_proxy_async_smem();  // the TMA stores read the staged tile through the async proxy
         __syncwarp();
         if (lane == 0) mbar_arrive(bars.o_staged());
-        // QPW: every QK of the item completed before its last PV (o_final): its Q' buffer
-        // may take item n_it + 2's, whose prologue then runs after this epilogue
-        if (C::QPW && lane == 0) mbar_arrive(bars.q_free(n_it & 1));
         jb += n_kv;
         item = next;
         have = more;
@@ -1015,9 +1094,9 @@ __global__ void __launch_bounds__(PfCfg<D>::THREADS, 1)
         for (int q = 0; q < 4; ++q) mbar_init(bars.xchg(q), C::NH);
         mbar_init(bars.o_final(), 2);
         mbar_init(bars.q_ready(), C::QPW ? C::PRO_WARPS : C::SOFTMAX_WARPS);
-        for (int i = 0; i < 2; ++i) mbar_init(bars.q_free(i), C::SOFTMAX_WARPS);
-        mbar_init(bars.o_staged(), C::SOFTMAX_WARPS);
-        mbar_init(bars.o_free(), C::SOFTMAX_WARPS);
+        for (int i = 0; i < 2; ++i) mbar_init(bars.l_full(i), C::SOFTMAX_WARPS);
+        mbar_init(bars.o_staged(), C::QPW ? C::PRO_WARPS : C::SOFTMAX_WARPS);
+        mbar_init(bars.o_free(), C::QPW ? C::PRO_WARPS : C::SOFTMAX_WARPS);
         mbar_init(bars.drain(), 2);
         mbar_init(bars.q_full(), 1);
         mbar_init(bars.g_full(), 1);
@@ -1042,7 +1121,8 @@ __global__ void __launch_bounds__(PfCfg<D>::THREADS, 1)
     if constexpr (C::QPW) {
         if (warp >= C::SM_WARP0 + C::SOFTMAX_WARPS) {
             regs_lower<C::REG_PRO>();
-            run_qprologue<D, GV>(p, bars, sbase, tm, warp & 3, lane, cta, ncta, abort_flag);
+            run_qwg<D, GV>(p, bars, sbase, reinterpret_cast<const float*>(smem + C::OFF_X) + 2 * C::NH * C::BM, tm,
+                           warp & 3, lane, cta, ncta, abort_flag);
         } else if (warp >= C::SM_WARP0) {
             regs_raise<C::REG_SOFTMAX>();
             run_softmax<D, GV>(p, bars, sbase, smem + C::OFF_X, tm, warp & 3, (warp - C::SM_WARP0) >> 2, lane, cta,
