@@ -18,9 +18,10 @@
 //       operand.  Warp-level mma keeps the arithmetic far off the critical path
 //       of this memory-bound loop.  At the end of each (sequence, group) piece a
 //       warp writes its partial softmax state (max, sum, unnormalised O).
-//   decode_combine_kernel  one CTA per (sequence, group): merges the partial
-//       states of the CTAs that covered it, divides by the sum and applies
-//       sigmoid(gate), writing bf16 [B, H*d].
+//   decode_combine_kernel  one CTA per (sequence, group), one warp per query
+//       head: merges the partial states of the CTAs that covered it (all the
+//       loads of eight slots in flight together, no barrier), divides by the sum
+//       and applies sigmoid(gate), writing bf16 [B, H*d].
 #include "common.cuh"
 #include "internal.h"
 
@@ -30,7 +31,6 @@ namespace {
 constexpr int BT = kDecodeTileKeys;  // keys per tile
 constexpr int NCW = kDecodeConsumerWarps;
 constexpr int MAXB = 2048;           // sequences per call
-constexpr int kCombineThreads = 512;
 
 template <int D>
 struct DecCfg {
@@ -363,16 +363,18 @@ __global__ void __launch_bounds__(DecCfg<D>::THREADS, 1)
 // weights w_s = 2^(m_s - max_s m_s) in shared memory, then every output element is
 // sum_s w_s O_s / sum_s w_s l_s -- independent, coalesced loads across the slots.
 template <int D>
-__global__ void __launch_bounds__(kCombineThreads) decode_combine_kernel(const __grid_constant__ DecodeParams p) {
-    extern __shared__ float cw[];  // [n_slots][r] merge weights
-    __shared__ int red[2][kCombineThreads / 32];
-    __shared__ float den[8];
+__global__ void __launch_bounds__(256, 1) decode_combine_kernel(const __grid_constant__ DecodeParams p) {
+    // one CTA per (sequence, group), one warp per query head of the group; lane l
+    // owns columns [l DPL, l DPL + DPL) of the head's output
+    constexpr int DPL = D / 32;
+    constexpr int CH = 8;  // slots whose loads are in flight together
     const int b = blockIdx.x / p.G, g = blockIdx.x % p.G;
     const int r = p.H / p.G;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int lane = threadIdx.x & 31, hl = threadIdx.x >> 5;
+    const int h = g * r + hl;
     // tiles before this sequence, and in total
     int before = 0, total = 0;
-    for (int i = tid; i < p.B; i += blockDim.x) {
+    for (int i = lane; i < p.B; i += 32) {
         const int nt = seq_tiles(p.seqlens[i], p.Lmax);
         total += nt;
         if (i < b) before += nt;
@@ -382,20 +384,10 @@ __global__ void __launch_bounds__(kCombineThreads) decode_combine_kernel(const _
         before += __shfl_xor_sync(0xffffffffu, before, o);
         total += __shfl_xor_sync(0xffffffffu, total, o);
     }
-    if (lane == 0) {
-        red[0][warp] = before;
-        red[1][warp] = total;
-    }
-    __syncthreads();
-    before = total = 0;
-    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) {
-        before += red[0][w];
-        total += red[1][w];
-    }
     const int L = p.seqlens[b];
     const int nt = seq_tiles(L, p.Lmax);
     if (nt == 0) {
-        if (tid == 0 && g == 0) atomicOr(p.status, GATTN_DEVICE_BAD_SEQLEN);
+        if (lane == 0 && hl == 0 && g == 0) atomicOr(p.status, GATTN_DEVICE_BAD_SEQLEN);
         return;
     }
     const int64_t T = (int64_t)p.G * total, N = p.n_ctas;
@@ -405,76 +397,90 @@ __global__ void __launch_bounds__(kCombineThreads) decode_combine_kernel(const _
         return c < N - 1 ? c : N - 1;
     };
     const int64_t c_first = cmax(u0);
-    const int n_c = (int)(cmax(u1) - c_first + 1);
-    const int n_slots = n_c * NCW;
+    const int n_slots = (int)(cmax(u1) - c_first + 1) * NCW;
     const int64_t seg = (int64_t)b * p.G + g;
     const int slot_floats = 2 * r + r * D;
     const float* part0 = p.part + (c_first + seg) * NCW * (int64_t)slot_floats;  // slot s at part0 + s*slot_floats
+    // whether slot s holds a state of this (sequence, group): its CTA's tile range
+    // meets the piece (a slot of a CTA that covered none of it may hold stale data)
+    auto covers = [&](int sl) -> bool {
+        const int64_t c = c_first + sl / NCW;
+        const int64_t s0 = c * T / N, s1 = (c + 1) * T / N;
+        return s0 < s1 && s0 <= u1 && s1 > u0;
+    };
+    // gate logits of this lane's columns: [B,H,d] elementwise, [B,H] headwise, [B,d] head-shared
+    const int layout = gate_layout(p.gate_mode);
+    float gl[DPL];
+#pragma unroll
+    for (int k = 0; k < DPL; ++k) {
+        const int e = lane * DPL + k;
+        gl[k] = 0.f;
+        if (layout == GATTN_GATE_ELEMENTWISE)
+            gl[k] = __bfloat162float(static_cast<const bf16*>(p.gate)[((int64_t)b * p.H + h) * D + e]);
+        else if (layout == GATTN_GATE_HEADWISE)
+            gl[k] = __bfloat162float(static_cast<const bf16*>(p.gate)[(int64_t)b * p.H + h]);
+        else if (layout == GATTN_GATE_HEAD_SHARED)
+            gl[k] = __bfloat162float(static_cast<const bf16*>(p.gate)[(int64_t)b * D + e]);
+    }
 
     // everything above reads only the inputs; the partial states come from the split kernel
     pdl_wait_prerequisites();
-    // 1. each slot's max, or -inf when its CTA covered no tile of this (sequence, group)
-    for (int i = tid; i < n_slots * r; i += blockDim.x) {
-        const int sl = i / r, hl = i % r;
-        const int64_t c = c_first + sl / NCW;
-        const int64_t s0 = c * T / N, s1 = (c + 1) * T / N;
-        const bool covers = s0 < s1 && s0 <= u1 && s1 > u0;
-        cw[i] = covers ? part0[(int64_t)sl * slot_floats + hl] : -INFINITY;
-    }
-    __syncthreads();
-    // 2. one warp per head: the common max, the weights and the merged sum
-    if (warp < r) {
-        float mx = -INFINITY;
-        for (int sl = lane; sl < n_slots; sl += 32) mx = fmaxf(mx, cw[sl * r + warp]);
+    // o = sum_s w_s O_s / sum_s w_s l_s with w_s = 2^(m_s - max_s m_s), the slots taken
+    // CH at a time with every load of a group in flight together; a later group with a
+    // larger maximum rescales what is summed so far (never the case for pieces
+    // covered by at most CH / NCW CTAs, where this is one pass with the common max)
+    float m_run = -INFINITY, den = 0.f, num[DPL];
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-        float dsum = 0.f;
-        for (int sl = lane; sl < n_slots; sl += 32) {
-            const float m = cw[sl * r + warp];
-            const float wgt = m == -INFINITY ? 0.f : ex2_approx(m - mx);
-            cw[sl * r + warp] = wgt;
-            const float l = part0[(int64_t)sl * slot_floats + r + warp];
-            dsum += wgt != 0.f ? wgt * l : 0.f;
-        }
+    for (int k = 0; k < DPL; ++k) num[k] = 0.f;
+    for (int sl0 = 0; sl0 < n_slots; sl0 += CH) {
+        float ms[CH], ls[CH], os[CH][DPL];
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) dsum += __shfl_xor_sync(0xffffffffu, dsum, o);
-        if (lane == 0) den[warp] = dsum;
-    }
-    __syncthreads();
-    // 3. outputs: o = sum_s w_s O_s / sum_s w_s l_s, times the gate.  The slots are
-    // read eight at a time with no branch between the loads, so they are in flight
-    // together; a slot with weight 0 (its CTA covered none of this sequence) may
-    // hold stale data and is dropped by a select, never multiplied.
-    constexpr int CH = 8;
-    for (int idx = tid; idx < r * D; idx += blockDim.x) {
-        const int hl = idx / D, e = idx % D;
-        const int h = g * r + hl;
-        // gate logit: [B,H,d] elementwise, [B,H] headwise, [B,d] head-shared
-        const int layout = gate_layout(p.gate_mode);
-        float gl = 0.f;
-        if (layout == GATTN_GATE_ELEMENTWISE)
-            gl = __bfloat162float(static_cast<const bf16*>(p.gate)[((int64_t)b * p.H + h) * D + e]);
-        else if (layout == GATTN_GATE_HEADWISE)
-            gl = __bfloat162float(static_cast<const bf16*>(p.gate)[(int64_t)b * p.H + h]);
-        else if (layout == GATTN_GATE_HEAD_SHARED)
-            gl = __bfloat162float(static_cast<const bf16*>(p.gate)[(int64_t)b * D + e]);
-        const float* src = part0 + 2 * r + hl * D + e;
-        float num = 0.f;
-        for (int sl0 = 0; sl0 < n_slots; sl0 += CH) {
-            float v[CH];
+        for (int j = 0; j < CH; ++j) {
+            const int sl = sl0 + j;
+            const bool live = sl < n_slots && covers(sl);
+            const float* ps = part0 + (int64_t)(live ? sl : 0) * slot_floats;
+            ms[j] = live ? ps[hl] : -INFINITY;
+            ls[j] = live ? ps[r + hl] : 0.f;
+            const float* po = ps + 2 * r + hl * D + lane * DPL;
+            if constexpr (DPL % 2 == 0) {
 #pragma unroll
-            for (int j = 0; j < CH; ++j) v[j] = sl0 + j < n_slots ? src[(int64_t)(sl0 + j) * slot_floats] : 0.f;
+                for (int k = 0; k < DPL; k += 2) {
+                    const float2 v = live ? *reinterpret_cast<const float2*>(po + k) : make_float2(0.f, 0.f);
+                    os[j][k] = v.x;
+                    os[j][k + 1] = v.y;
+                }
+            } else {
 #pragma unroll
-            for (int j = 0; j < CH; ++j) {
-                const float wgt = sl0 + j < n_slots ? cw[(sl0 + j) * r + hl] : 0.f;
-                num += wgt != 0.f ? wgt * v[j] : 0.f;
+                for (int k = 0; k < DPL; ++k) os[j][k] = live ? po[k] : 0.f;
             }
         }
-        const float gv = layout == GATTN_GATE_NONE ? 1.f : gate_act(gl, sigmoidf_dev(gl), p.gate_mode);
-        const float o = num / den[hl];
-        static_cast<bf16*>(p.out)[((int64_t)b * p.H + h) * D + e] =
-            __float2bfloat16_rn(gate_additive(p.gate_mode) ? o + gv : o * gv);
+        float mx = m_run;
+#pragma unroll
+        for (int j = 0; j < CH; ++j) mx = fmaxf(mx, ms[j]);
+        if (mx == -INFINITY) continue;  // no state in this group yet
+        const float keep = m_run == -INFINITY ? 0.f : ex2_approx(m_run - mx);
+        den *= keep;
+#pragma unroll
+        for (int k = 0; k < DPL; ++k) num[k] *= keep;
+#pragma unroll
+        for (int j = 0; j < CH; ++j) {
+            const float wgt = ms[j] == -INFINITY ? 0.f : ex2_approx(ms[j] - mx);
+            den += wgt != 0.f ? wgt * ls[j] : 0.f;
+#pragma unroll
+            for (int k = 0; k < DPL; ++k) num[k] += wgt != 0.f ? wgt * os[j][k] : 0.f;
+        }
+        m_run = mx;
     }
+    bf16 ob[DPL];
+#pragma unroll
+    for (int k = 0; k < DPL; ++k) {
+        const float gv = layout == GATTN_GATE_NONE ? 1.f : gate_act(gl[k], sigmoidf_dev(gl[k]), p.gate_mode);
+        const float o = num[k] / den;
+        ob[k] = __float2bfloat16_rn(gate_additive(p.gate_mode) ? o + gv : o * gv);
+    }
+    bf16* orow = static_cast<bf16*>(p.out) + ((int64_t)b * p.H + h) * D + lane * DPL;
+#pragma unroll
+    for (int k = 0; k < DPL; ++k) orow[k] = ob[k];
 }
 
 template <int D>
@@ -488,18 +494,12 @@ cudaError_t launch_dec(const DecodeParams& p, const CUtensorMap& tm, cudaStream_
     e = cudaGetLastError();
     if (ev_stop) cudaEventRecord(ev_stop, stream);
     if (e != cudaSuccess) return e;
-    // merge weights: at most (n_ctas + 1) CTAs cover one (sequence, group)
-    const size_t cw_bytes = (size_t)(p.n_ctas + 1) * NCW * (p.H / p.G) * sizeof(float);
-    if (cw_bytes > 48 * 1024) {
-        e = cudaFuncSetAttribute(decode_combine_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)cw_bytes);
-        if (e != cudaSuccess) return e;
-    }
     // programmatic serialisation: the combine CTAs become resident while the split
     // kernel drains and wait on its completion inside the kernel
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(p.B * p.G));
-    cfg.blockDim = dim3(kCombineThreads);
-    cfg.dynamicSmemBytes = cw_bytes;
+    cfg.blockDim = dim3(32 * (p.H / p.G));
+    cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
