@@ -43,6 +43,9 @@ SHAPES = [
     (4, 32, 4, 128, 64, 1e6, "elementwise", 1000, 500, 1000),
     (2, 4, 4, 64, 32, 1e4, "none", 129, 63, 129),
     (7, 8, 1, 128, 16, 1e4, "elementwise", 2048, 1, 2048),
+    # one long sequence spread over most of the grid: its merge takes some 300 partial
+    # states, eight at a time, each group with its own maximum
+    (1, 8, 2, 256, 64, 1e7, "elementwise", 8192, 8192, 8192),
 ]
 
 
