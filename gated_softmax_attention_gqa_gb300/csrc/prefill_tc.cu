@@ -173,6 +173,47 @@ struct Bars {
     __device__ uint32_t l_full(int i) const { return at(r() + 19 + i); }
 };
 
+// ----------------------------------------------------------------- TMA with L2 priorities
+
+// L2 eviction priorities for TMA copies (an access-policy operand; it changes only
+// which lines L2 gives up first, never what is read or written): evict_first for
+// data touched once, evict_last for tiles that other CTAs or later items read again.
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+__device__ __forceinline__ void tma_load_3d_hint(uint32_t dst, const CUtensorMap* map, uint32_t bar, int c0, int c1,
+                                                 int c2, uint64_t pol) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, "
+        "{%3, %4, %5}], [%2], %6;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "l"(pol)
+        : "memory");
+}
+__device__ __forceinline__ void tma_load_4d_hint(uint32_t dst, const CUtensorMap* map, uint32_t bar, int c0, int c1,
+                                                 int c2, int c3, uint64_t pol) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, "
+        "{%3, %4, %5, %6}], [%2], %7;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "l"(pol)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_store_4d_hint(const CUtensorMap* map, uint32_t src, int c0, int c1, int c2,
+                                                  int c3, uint64_t pol) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.global.shared::cta.tile.bulk_group.L2::cache_hint [%0, {%2, %3, %4, %5}], [%1], "
+        "%6;" ::"l"(reinterpret_cast<uint64_t>(map)),
+        "r"(src), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "l"(pol)
+        : "memory");
+}
+
 // ----------------------------------------------------------------- work items
 
 // Work item u: query tile n_qtiles - 1 - u / (B*H) (heaviest first) of batch and
@@ -232,6 +273,9 @@ __device__ void run_producer(const CUtensorMap* tmK, const CUtensorMap* tmV, con
     // head-shared vector per token: the gate map then has a single head)
     const bool gate_tile = GV ? gate_per_dim(p.gate_mode) : p.gate_mode == GATTN_GATE_ELEMENTWISE;
     const bool shared = GV && gate_layout(p.gate_mode) == GATTN_GATE_HEAD_SHARED;
+    // raw Q, gate and output tiles pass through L2 once; K'/V tiles are read again by
+    // the group's other heads and by later query tiles, so they are the ones L2 keeps
+    const uint64_t pol_once = l2_policy_evict_first(), pol_kv = l2_policy_evict_last();
     int nk = 0, nv = 0;  // K' / V tiles issued, over all items
     int jb = 0;          // tiles of the items before the current one
     int n_it = 0;
@@ -246,8 +290,8 @@ __device__ void run_producer(const CUtensorMap* tmK, const CUtensorMap* tmV, con
             mbar_arrive_expect_tx(bars.g_full(), C::QTILE_BYTES);
 #pragma unroll
             for (int c = 0; c < C::KCH; ++c)
-                tma_load_4d(sbase + C::OFF_G + c * C::ROWBOX_BYTES, tmG, bars.g_full(), c * 64, shared ? 0 : x.h,
-                            row0_of(x), x.b);
+                tma_load_4d_hint(sbase + C::OFF_G + c * C::ROWBOX_BYTES, tmG, bars.g_full(), c * 64, shared ? 0 : x.h,
+                                 row0_of(x), x.b, pol_once);
             g_last = n_it;
         } else {
             mbar_arrive(bars.g_full());
@@ -260,7 +304,7 @@ __device__ void run_producer(const CUtensorMap* tmK, const CUtensorMap* tmV, con
         if (x.direct) return;
 #pragma unroll
         for (int c = 0; c < C::KCH; ++c)
-            tma_store_4d(tmO, sbase + C::OFF_OUT + c * C::ROWBOX_BYTES, c * 64, x.h, row0_of(x), x.b);
+            tma_store_4d_hint(tmO, sbase + C::OFF_OUT + c * C::ROWBOX_BYTES, c * 64, x.h, row0_of(x), x.b, pol_once);
         bulk_commit_group();
         bulk_wait_group_read0();
     };
@@ -271,7 +315,8 @@ __device__ void run_producer(const CUtensorMap* tmK, const CUtensorMap* tmV, con
         if (k == 0) bulk_load(sbase + C::OFF_W, p.qnorm_w, D * 2, bars.q_full());
 #pragma unroll
         for (int c = 0; c < C::KCH; ++c)
-            tma_load_4d(sbase + C::OFF_Q + c * C::ROWBOX_BYTES, tmQ, bars.q_full(), c * 64, x.h, row0_of(x), x.b);
+            tma_load_4d_hint(sbase + C::OFF_Q + c * C::ROWBOX_BYTES, tmQ, bars.q_full(), c * 64, x.h, row0_of(x), x.b,
+                             pol_once);
         q_last = k;
     };
     TcItem nxt;
@@ -338,7 +383,7 @@ __device__ void run_producer(const CUtensorMap* tmK, const CUtensorMap* tmV, con
                 const int kgrp = cur ? it.b * p.G + g : nxt.b * p.G + nxt.h / (p.H / p.G);
 #pragma unroll
                 for (int c = 0; c < C::KCH; ++c)
-                    tma_load_3d(kdst + c * C::CHUNK_BYTES, tmK, bars.k_full(st), c * 64, krow, kgrp);
+                    tma_load_3d_hint(kdst + c * C::CHUNK_BYTES, tmK, bars.k_full(st), c * 64, krow, kgrp, pol_kv);
                 ++nk;
                 progressed = true;
             }
@@ -350,8 +395,8 @@ __device__ void run_producer(const CUtensorMap* tmK, const CUtensorMap* tmV, con
                 const uint32_t vdst = sbase + C::OFF_V + st * C::TILE_BYTES;
 #pragma unroll
                 for (int c = 0; c < C::KCH; ++c)
-                    tma_load_4d(vdst + c * C::CHUNK_BYTES, tmV, bars.v_full(st), c * 64, g, it.t0 + (nv - jb) * C::BN,
-                                it.b);
+                    tma_load_4d_hint(vdst + c * C::CHUNK_BYTES, tmV, bars.v_full(st), c * 64, g,
+                                     it.t0 + (nv - jb) * C::BN, it.b, pol_kv);
                 ++nv;
                 progressed = true;
             }
